@@ -1,0 +1,179 @@
+"""fp64 CPU oracle for the linear-recurrence hot path -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never calls it and
+shares no code with it.  The arithmetic lives in ``lr_oracle.c`` (plain C,
+fp64, sequential in time); this module only compiles it with gcc, loads it with
+ctypes and converts numpy arrays to contiguous fp64.
+
+Every function here follows the pages cited in ``lr_oracle.c``:
+  scan_fwd / scan_bwd  -- the diagonal linear recurrence and its BPTT gradient
+  sru_fwd / sru_bwd    -- the linear-form SRU layer and its gradient
+  deer / deer_step     -- DEER Newton iteration on a diagonal tanh RNN
+  rollout_tanh         -- the direct sequential tanh RNN
+Each is pinned by tests in ``tests/test_oracle_pins.py`` against closed forms,
+library linear solves, finite differences and brute-force evaluation orders.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lr_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "liblroracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# -ffp-contract=off: no fused multiply-add, so x86 and Arm hosts give the same
+# bits; -O2 keeps IEEE semantics (no -ffast-math).
+CFLAGS = ["-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared"]
+
+
+def build(force: bool = False) -> str:
+    """Compile lr_oracle.c into a shared library (idempotent)."""
+    with _lock:
+        if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+            return _LIB
+        os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+        tmp = _LIB + f".{os.getpid()}.tmp"
+        subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+        return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        lib.lro_scan_fwd.argtypes = [I64, I64, P, P, P, P]
+        lib.lro_scan_bwd.argtypes = [I64, I64, P, P, P, P, P, P, P]
+        lib.lro_sru_fwd.argtypes = [I64, I64, I64] + [P] * 9
+        lib.lro_sru_bwd.argtypes = [I64, I64, I64] + [P] * 15
+        lib.lro_rollout_tanh.argtypes = [I64, I64, I64, P, P, P, P]
+        lib.lro_deer_step.argtypes = [I64, I64, I64, P, P, P, P, P, P]
+        lib.lro_deer.argtypes = [I64, I64, I64, P, P, P, ctypes.c_double, ctypes.c_int, P, P, P]
+        lib.lro_deer.restype = ctypes.c_int
+        lib.lro_num_threads.restype = ctypes.c_int
+        lib.lro_set_num_threads.argtypes = [ctypes.c_int]
+        _lib = lib
+    return _lib
+
+
+def set_num_threads(n: int) -> None:
+    """0 = OpenMP default (all cores)."""
+    _load().lro_set_num_threads(int(n))
+
+
+def num_threads() -> int:
+    return int(_load().lro_num_threads())
+
+
+def _f64(x):
+    if x is None:
+        return None
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _p(x):
+    return None if x is None else x.ctypes.data_as(ctypes.c_void_p)
+
+
+def _tc(x):
+    """[T, B, D] or [T, C] -> (T, C)."""
+    T = x.shape[0]
+    return T, int(np.prod(x.shape[1:])) if x.ndim > 1 else 1
+
+
+def scan_fwd(a, b, h0=None):
+    """h_t = a_t h_{t-1} + b_t along axis 0; returns fp64 h shaped like a."""
+    a, b, h0 = _f64(a), _f64(b), _f64(h0)
+    T, C = _tc(a)
+    h = np.empty_like(a)
+    _load().lro_scan_fwd(T, C, _p(a), _p(b), _p(h0), _p(h))
+    return h
+
+
+def scan_bwd(a, h, g, h0=None):
+    """Returns (da, db, dh0) for loss sum(g * h), given the forward h."""
+    a, h, g, h0 = _f64(a), _f64(h), _f64(g), _f64(h0)
+    T, C = _tc(a)
+    da, db = np.empty_like(a), np.empty_like(a)
+    dh0 = np.empty(a.shape[1:], dtype=np.float64)
+    _load().lro_scan_bwd(T, C, _p(a), _p(h), _p(h0), _p(g), _p(da), _p(db), _p(dh0))
+    return da, db, dh0
+
+
+def sru_fwd(xt, uf, ur, x, bf, br, c0=None):
+    """Returns (h, c). Sequence tensors [T, B, D]; bf, br [D]."""
+    xt, uf, ur, x, bf, br, c0 = map(_f64, (xt, uf, ur, x, bf, br, c0))
+    T, C = _tc(xt)
+    D = bf.shape[0]
+    h, c = np.empty_like(xt), np.empty_like(xt)
+    _load().lro_sru_fwd(T, C, D, *map(_p, (xt, uf, ur, x, bf, br, c0, h, c)))
+    return h, c
+
+
+def sru_bwd(xt, uf, ur, x, bf, br, c, dh, c0=None):
+    """Returns (dxt, duf, dur, dx, dbf, dbr, dc0) given the forward c."""
+    xt, uf, ur, x, bf, br, c, dh, c0 = map(_f64, (xt, uf, ur, x, bf, br, c, dh, c0))
+    T, C = _tc(xt)
+    D = bf.shape[0]
+    dxt, duf, dur, dx = (np.empty_like(xt) for _ in range(4))
+    dbf, dbr = np.empty(D), np.empty(D)
+    dc0 = np.empty(xt.shape[1:], dtype=np.float64)
+    _load().lro_sru_bwd(T, C, D, *map(_p, (xt, uf, ur, x, bf, br, c0, c, dh,
+                                            dxt, duf, dur, dx, dbf, dbr, dc0)))
+    return dxt, duf, dur, dx, dbf, dbr, dc0
+
+
+def rollout_tanh(w, u, h0=None):
+    """Direct sequential h_t = tanh(w h_{t-1} + u_t)."""
+    w, u, h0 = _f64(w), _f64(u), _f64(h0)
+    T, C = _tc(u)
+    y = np.empty_like(u)
+    _load().lro_rollout_tanh(T, C, w.shape[0], _p(w), _p(u), _p(h0), _p(y))
+    return y
+
+
+def deer_step(w, u, yprev=None, h0=None):
+    """One Newton step from yprev (None = all-zero guess); returns (ynew, rho)."""
+    w, u, yprev, h0 = _f64(w), _f64(u), _f64(yprev), _f64(h0)
+    T, C = _tc(u)
+    y = np.empty_like(u)
+    rho = ctypes.c_double(0.0)
+    _load().lro_deer_step(T, C, w.shape[0], _p(w), _p(u), _p(h0), _p(yprev), _p(y),
+                          ctypes.byref(rho))
+    return y, rho.value
+
+
+DEER_CONVERGED, DEER_NOT_CONVERGED, DEER_NONFINITE = 0, 1, 2
+
+
+def deer(w, u, h0=None, eps=1e-5, kmax=20):
+    """Returns (y, iters, rho_history, status) -- status 0 converged, 1 hit kmax."""
+    w, u, h0 = _f64(w), _f64(u), _f64(h0)
+    T, C = _tc(u)
+    y = np.empty_like(u)
+    hist = np.zeros(kmax, dtype=np.float64)
+    iters = ctypes.c_int(0)
+    st = _load().lro_deer(T, C, w.shape[0], _p(w), _p(u), _p(h0), float(eps), int(kmax),
+                          _p(y), _p(hist), ctypes.byref(iters))
+    if st < 0:
+        raise MemoryError("oracle deer: allocation failed")
+    return y, int(iters.value), hist[: iters.value].copy(), int(st)
+
+
+def rel_err(got, ref) -> float:
+    """max|got - ref| / max(1, max|ref|) -- the parity measure, per tensor."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if ref.size == 0:
+        return 0.0
+    return float(np.max(np.abs(got - ref)) / max(1.0, float(np.max(np.abs(ref)))))

@@ -1,0 +1,295 @@
+/*
+ * lr_oracle.c -- plain, sequential, fp64 CPU oracle for the linear-recurrence
+ * hot path.  TEST INFRASTRUCTURE ONLY: it is called by the tests, by the smoke
+ * check and by the benchmark's CPU-baseline leg, never by the product path.
+ * It shares no code, header or constant with the CUDA library.
+ *
+ * Sources (four blog pages from blog.hotdry.top, all dated 2025-09-21):
+ *   [P1] "CUDA并行化RNN训练：从O(T)到O(log T)的工程实践与参数调优"
+ *        (CUDA-parallel RNN training, O(T) -> O(log T)): the SRU paragraph
+ *        (forget gate, highway reset gate) and the parallel-scan paragraph
+ *        (an associative operation evaluated for forward and backward).
+ *   [P2] "RNN CUDA内核优化：实现序列长度无关的恒定推理延迟"
+ *        (RNN CUDA kernel optimisation): the paragraph that isolates the
+ *        linear part C_t = f_t*C_{t-1} + i_t*C~_t and solves it by tree
+ *        reduction in log2(T) stages.
+ *   [P4] the DEER page (.../cuda-parallel-rnn-training-logt-optimization),
+ *        section "核心原理：DEER 框架与牛顿法的工程映射" (Newton form, the
+ *        three steps: f and Jacobian J, G_p times a vector, the linear inverse
+ *        solved as a prefix scan) and section "工程实现" (the stopping rule
+ *        ||y^(i+1) - y^(i)|| < eps or K_max).
+ *
+ * Everything is the plain definition: strictly sequential in t, fp64, libm
+ * exp/tanh only.  No blocking, no re-association.  Channels are independent,
+ * so threads (OpenMP) split the channel range and nothing else.
+ *
+ * Layout: every sequence tensor is [T, C] row-major with C = B*D channels
+ * contiguous; channel c uses the per-feature parameter index d = c % D.
+ * A NULL initial state means zeros.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---------------------------------------------------------------- threads */
+
+static int g_threads = 0; /* 0: OpenMP default */
+
+void lro_set_num_threads(int n) { g_threads = n; }
+
+int lro_num_threads(void) {
+#ifdef _OPENMP
+    return g_threads > 0 ? g_threads : omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Channel range [*c0, *c1) owned by thread `tid` of `nt`. */
+static void chan_range(int64_t C, int tid, int nt, int64_t* c0, int64_t* c1) {
+    int64_t per = C / nt, rem = C % nt;
+    *c0 = tid * per + (tid < rem ? tid : rem);
+    *c1 = *c0 + per + (tid < rem ? 1 : 0);
+}
+
+#ifdef _OPENMP
+#define PAR_BEGIN                                                     \
+    _Pragma("omp parallel num_threads(lro_num_threads())") {          \
+        int tid_ = omp_get_thread_num(), nt_ = omp_get_num_threads(); \
+        int64_t c0_, c1_;                                             \
+        chan_range(C, tid_, nt_, &c0_, &c1_);
+#define PAR_END }
+#else
+#define PAR_BEGIN                 \
+    {                             \
+        int64_t c0_ = 0, c1_ = C;
+#define PAR_END }
+#endif
+
+/* ------------------------------------------------------- forward (row a1) */
+/*
+ * h_t = a_t * h_{t-1} + b_t,  h_{-1} = h0  (elementwise per channel).
+ * [P2] LSTM paragraph: the state update is a linear recurrence with
+ * time-varying coefficient; [P1] parallel-scan paragraph.
+ */
+void lro_scan_fwd(int64_t T, int64_t C, const double* a, const double* b,
+                  const double* h0, double* h) {
+    PAR_BEGIN
+    for (int64_t c = c0_; c < c1_; ++c) h[c] = a[c] * (h0 ? h0[c] : 0.0) + b[c];
+    for (int64_t t = 1; t < T; ++t)
+        for (int64_t c = c0_; c < c1_; ++c)
+            h[t * C + c] = a[t * C + c] * h[(t - 1) * C + c] + b[t * C + c];
+    PAR_END
+}
+
+/* ------------------------------------------------------ backward (row a2) */
+/*
+ * Given the forward states h and the upstream gradient g = dL/dh_t for every
+ * t, back-propagation through time of h_t = a_t h_{t-1} + b_t:
+ *   delta_{T-1} = g_{T-1},   delta_t = g_t + a_{t+1} * delta_{t+1}
+ *   dL/db_t = delta_t,   dL/da_t = delta_t * h_{t-1},   dL/dh0 = a_0 * delta_0
+ * [P1] parallel-scan paragraph: the same associative evaluation serves the
+ * backward pass, which is this recurrence run in reverse time.
+ * dh0 may be NULL (skipped).
+ */
+void lro_scan_bwd(int64_t T, int64_t C, const double* a, const double* h,
+                  const double* h0, const double* g, double* da, double* db,
+                  double* dh0) {
+    PAR_BEGIN
+    for (int64_t c = c0_; c < c1_; ++c) db[(T - 1) * C + c] = g[(T - 1) * C + c];
+    for (int64_t t = T - 2; t >= 0; --t)
+        for (int64_t c = c0_; c < c1_; ++c)
+            db[t * C + c] = g[t * C + c] + a[(t + 1) * C + c] * db[(t + 1) * C + c];
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t c = c0_; c < c1_; ++c) {
+            double hprev = t > 0 ? h[(t - 1) * C + c] : (h0 ? h0[c] : 0.0);
+            da[t * C + c] = db[t * C + c] * hprev;
+        }
+    if (dh0)
+        for (int64_t c = c0_; c < c1_; ++c) dh0[c] = a[c] * db[c];
+    PAR_END
+}
+
+/* --------------------------------------------------- SRU forward (row a3) */
+
+static double sigm(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+/*
+ * SRU in its linear form (v_f = 0), per [P1] SRU paragraph (forget gate from
+ * the current input only; highway reset gate mixing input and memory):
+ *   f_t = sigma(U_f,t + b_f),  r_t = sigma(U_r,t + b_r)
+ *   c_t = f_t c_{t-1} + (1 - f_t) xt_t,        c_{-1} = c0
+ *   h_t = r_t tanh(c_t) + (1 - r_t) x_t
+ * U_f, U_r, xt are the precomputed projections; bf, br are [D].
+ */
+void lro_sru_fwd(int64_t T, int64_t C, int64_t D, const double* xt,
+                 const double* uf, const double* ur, const double* x,
+                 const double* bf, const double* br, const double* c0,
+                 double* h, double* c) {
+    PAR_BEGIN
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t k = c0_; k < c1_; ++k) {
+            int64_t i = t * C + k, d = k % D;
+            double cprev = t > 0 ? c[i - C] : (c0 ? c0[k] : 0.0);
+            double f = sigm(uf[i] + bf[d]);
+            double r = sigm(ur[i] + br[d]);
+            c[i] = f * cprev + (1.0 - f) * xt[i];
+            h[i] = r * tanh(c[i]) + (1.0 - r) * x[i];
+        }
+    PAR_END
+}
+
+/* -------------------------------------------------- SRU backward (row a4) */
+/*
+ * Gradients of the SRU forward above given the memory states c and the
+ * upstream dh = dL/dh_t (the only upstream gradient):
+ *   dr_t   = dh_t (tanh c_t - x_t),     dU_r = dr_t r_t (1 - r_t)
+ *   dx_t   = dh_t (1 - r_t)
+ *   dc_t   = dh_t r_t (1 - tanh^2 c_t) + f_{t+1} dc_{t+1}    (reverse in t)
+ *   dxt_t  = dc_t (1 - f_t)
+ *   dU_f,t = dc_t (c_{t-1} - xt_t) f_t (1 - f_t)
+ *   dc0    = f_0 dc_0
+ *   db_f[d] = sum over t and batch of dU_f,  db_r[d] likewise of dU_r.
+ * dc0 may be NULL.
+ */
+void lro_sru_bwd(int64_t T, int64_t C, int64_t D, const double* xt,
+                 const double* uf, const double* ur, const double* x,
+                 const double* bf, const double* br, const double* c0,
+                 const double* c, const double* dh, double* dxt, double* duf,
+                 double* dur, double* dx, double* dbf, double* dbr,
+                 double* dc0) {
+    double* dc = (double*)malloc(sizeof(double) * (size_t)(T * C));
+    double* sf = (double*)calloc((size_t)C, sizeof(double));
+    double* sr = (double*)calloc((size_t)C, sizeof(double));
+    PAR_BEGIN
+    /* memory-state gradient, reverse in time */
+    for (int64_t t = T - 1; t >= 0; --t)
+        for (int64_t k = c0_; k < c1_; ++k) {
+            int64_t i = t * C + k, d = k % D;
+            double r = sigm(ur[i] + br[d]);
+            double th = tanh(c[i]);
+            double e = dh[i] * r * (1.0 - th * th);
+            double carry = 0.0;
+            if (t + 1 < T) carry = sigm(uf[i + C] + bf[d]) * dc[i + C];
+            dc[i] = e + carry;
+        }
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t k = c0_; k < c1_; ++k) {
+            int64_t i = t * C + k, d = k % D;
+            double f = sigm(uf[i] + bf[d]);
+            double r = sigm(ur[i] + br[d]);
+            double th = tanh(c[i]);
+            double cprev = t > 0 ? c[i - C] : (c0 ? c0[k] : 0.0);
+            double dr = dh[i] * (th - x[i]);
+            dur[i] = dr * r * (1.0 - r);
+            dx[i] = dh[i] * (1.0 - r);
+            dxt[i] = dc[i] * (1.0 - f);
+            duf[i] = dc[i] * (cprev - xt[i]) * f * (1.0 - f);
+            sf[k] += duf[i];
+            sr[k] += dur[i];
+        }
+    if (dc0)
+        for (int64_t k = c0_; k < c1_; ++k) dc0[k] = sigm(uf[k] + bf[k % D]) * dc[k];
+    PAR_END
+    /* bias gradients: sum the per-channel sums over the batch, serially */
+    for (int64_t d = 0; d < D; ++d) { dbf[d] = 0.0; dbr[d] = 0.0; }
+    for (int64_t k = 0; k < C; ++k) { dbf[k % D] += sf[k]; dbr[k % D] += sr[k]; }
+    free(dc);
+    free(sf);
+    free(sr);
+}
+
+/* -------------------------------------------------- DEER (row a5), tanh RNN */
+/*
+ * Target recurrence: h_t = tanh(w (.) h_{t-1} + u_t), h_{-1} = h0, w in [D].
+ *
+ * The direct sequential evaluation ([P1]/[P4]: the O(T) serial RNN).
+ */
+void lro_rollout_tanh(int64_t T, int64_t C, int64_t D, const double* w,
+                      const double* u, const double* h0, double* y) {
+    PAR_BEGIN
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t k = c0_; k < c1_; ++k) {
+            int64_t i = t * C + k;
+            double prev = t > 0 ? y[i - C] : (h0 ? h0[k] : 0.0);
+            y[i] = tanh(w[k % D] * prev + u[i]);
+        }
+    PAR_END
+}
+
+/*
+ * One DEER / Newton step ([P4] "核心原理": (1) evaluate f and its Jacobian J at
+ * the current guess, (2) form G_p times the guess, G_p = -J, (3) apply the
+ * linear inverse operator, which for an RNN is a linear recurrence with an
+ * initial condition).  For the diagonal tanh cell, with ytil_{t-1} the
+ * previous iterate shifted by one step (ytil_{-1} = h0):
+ *   s_t   = w ytil_{t-1} + u_t
+ *   J_t   = w (1 - tanh^2 s_t)
+ *   rhs_t = tanh(s_t) - J_t ytil_{t-1}
+ *   ynew_t = J_t ynew_{t-1} + rhs_t,   ynew_{-1} = h0     (sequential here)
+ * yprev == NULL means the all-zero initial guess.  Returns, through *rho,
+ * max |ynew - yprev| over all B*T*D entries.
+ */
+void lro_deer_step(int64_t T, int64_t C, int64_t D, const double* w,
+                   const double* u, const double* h0, const double* yprev,
+                   double* ynew, double* rho) {
+    double best = 0.0;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(lro_num_threads()) reduction(max : best)
+#endif
+    {
+        int64_t c0_ = 0, c1_ = C;
+#ifdef _OPENMP
+        chan_range(C, omp_get_thread_num(), omp_get_num_threads(), &c0_, &c1_);
+#endif
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t k = c0_; k < c1_; ++k) {
+                int64_t i = t * C + k;
+                double wk = w[k % D];
+                double init = h0 ? h0[k] : 0.0;
+                double ytil = t > 0 ? (yprev ? yprev[i - C] : 0.0) : init;
+                double s = wk * ytil + u[i];
+                double th = tanh(s);
+                double J = wk * (1.0 - th * th);
+                double rhs = th - J * ytil;
+                double ylast = t > 0 ? ynew[i - C] : init;
+                ynew[i] = J * ylast + rhs;
+                double diff = fabs(ynew[i] - (yprev ? yprev[i] : 0.0));
+                if (diff > best) best = diff;
+            }
+    }
+    *rho = best;
+}
+
+/*
+ * DEER fixed-point iteration from the all-zero guess ([P4] "工程实现": stop
+ * when ||y^(i+1) - y^(i)|| < eps, here the max-abs norm over all entries, or
+ * after kmax iterations).  K counts the scans performed, including the one
+ * whose residual fell below eps.  rho_hist[k-1] = residual of iteration k.
+ * Returns 0 when converged, 1 when kmax was reached without convergence,
+ * 2 when a residual was not finite, -1 on allocation failure.
+ */
+int lro_deer(int64_t T, int64_t C, int64_t D, const double* w, const double* u,
+             const double* h0, double eps, int kmax, double* y,
+             double* rho_hist, int* iters) {
+    size_t n = (size_t)(T * C);
+    double* prev = (double*)malloc(sizeof(double) * n);
+    if (!prev) return -1;
+    int status = 1, k;
+    for (k = 1; k <= kmax; ++k) {
+        double rho = 0.0;
+        lro_deer_step(T, C, D, w, u, h0, k == 1 ? NULL : prev, y, &rho);
+        rho_hist[k - 1] = rho;
+        if (!isfinite(rho)) { status = 2; break; }
+        if (rho < eps) { status = 0; break; }
+        memcpy(prev, y, sizeof(double) * n);
+    }
+    *iters = k > kmax ? kmax : k;
+    free(prev);
+    return status;
+}

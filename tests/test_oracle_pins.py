@@ -1,0 +1,349 @@
+"""Pins of the fp64 oracle against facts fixed outside the oracle itself.
+
+Each test checks the oracle against something other than its own loop: a
+closed form, a library linear solve (scipy), a library filter, central finite
+differences, a brute-force evaluation of the associative operator in random
+tree orders, Newton's method written from the residual function, or a
+hand-worked example under tests/golden/.  A plausible slip in the oracle (a
+dropped term, a wrong sign or time index, a transposed operand) fails at least
+one of them.  CPU only.
+"""
+import os
+import random
+
+import numpy as np
+import pytest
+import scipy.linalg
+import scipy.signal
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(1234)
+
+
+def _bidiag_solve(a, rhs):
+    """Solve (I - S_a) h = rhs for one channel, S_a having a_t at (t, t-1)."""
+    T = a.shape[0]
+    ab = np.zeros((2, T))
+    ab[0] = 1.0
+    ab[1, :-1] = -a[1:]
+    return scipy.linalg.solve_banded((1, 0), ab, rhs)
+
+
+def _bidiag_solve_T(a, rhs):
+    """Solve (I - S_a)^T x = rhs (upper bidiagonal) for one channel."""
+    T = a.shape[0]
+    ab = np.zeros((2, T))
+    ab[1] = 1.0
+    ab[0, 1:] = -a[1:]
+    return scipy.linalg.solve_banded((0, 1), ab, rhs)
+
+
+# ------------------------------------------------------------ forward scan
+
+def test_golden_dyadic_example():
+    vals = {}
+    with open(os.path.join(GOLDEN, "scan_dyadic_T4.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                k, *v = line.split()
+                vals[k] = np.array([float(x) for x in v])
+    a, b, g = (vals[k].reshape(4, 1) for k in ("a", "b", "g"))
+    h0 = vals["h0"].reshape(1)
+    h = oracle.scan_fwd(a, b, h0)
+    assert np.array_equal(h[:, 0], vals["h"])
+    da, db, dh0 = oracle.scan_bwd(a, h, g, h0)
+    assert np.array_equal(db[:, 0], vals["db"])
+    assert np.array_equal(da[:, 0], vals["da"])
+    assert np.array_equal(dh0, vals["dh0"])
+
+
+def test_scan_a_zero_gives_b_exactly():
+    b = rng.standard_normal((37, 3, 5))
+    h = oracle.scan_fwd(np.zeros_like(b), b, rng.standard_normal((3, 5)))
+    assert np.array_equal(h, b)
+
+
+def test_scan_a_one_is_running_sum():
+    b = rng.standard_normal((200, 7))
+    h0 = rng.standard_normal(7)
+    h = oracle.scan_fwd(np.ones_like(b), b, h0)
+    np.testing.assert_allclose(h, h0 + np.cumsum(b, axis=0), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("alpha", [0.3, -0.7, 0.99, 1.5])
+def test_scan_constant_coefficients_geometric_series(alpha):
+    T, beta, h0 = 60, 0.25, -1.5
+    h = oracle.scan_fwd(np.full((T, 1), alpha), np.full((T, 1), beta), np.array([h0]))
+    t = np.arange(T) + 1.0
+    closed = alpha ** t * h0 + beta * (1 - alpha ** t) / (1 - alpha)
+    np.testing.assert_allclose(h[:, 0], closed, rtol=1e-11, atol=1e-12)
+
+
+def test_scan_constant_a_matches_iir_filter():
+    alpha = 0.87
+    b = rng.standard_normal((300, 4))
+    h0 = rng.standard_normal(4)
+    h = oracle.scan_fwd(np.full_like(b, alpha), b, h0)
+    for c in range(4):
+        ref, _ = scipy.signal.lfilter([1.0], [1.0, -alpha], b[:, c], zi=[alpha * h0[c]])
+        np.testing.assert_allclose(h[:, c], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_scan_time_varying_matches_banded_solve():
+    T, C = 150, 6
+    a = rng.uniform(-1.2, 1.2, (T, C))
+    b = rng.standard_normal((T, C))
+    h0 = rng.standard_normal(C)
+    h = oracle.scan_fwd(a, b, h0)
+    for c in range(C):
+        rhs = b[:, c].copy()
+        rhs[0] += a[0, c] * h0[c]
+        np.testing.assert_allclose(h[:, c], _bidiag_solve(a[:, c], rhs), rtol=1e-10, atol=1e-10)
+
+
+def _combine(x, y):
+    """(a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2), earlier element on the left."""
+    return (x[0] * y[0], y[0] * x[1] + y[1])
+
+
+def _random_tree(elems, r):
+    if len(elems) == 1:
+        return elems[0]
+    k = r.randint(1, len(elems) - 1)
+    return _combine(_random_tree(elems[:k], r), _random_tree(elems[k:], r))
+
+
+def _blelloch_inclusive(elems):
+    """Up-sweep / down-sweep (work-efficient) exclusive scan, made inclusive."""
+    n = len(elems)
+    x = list(elems)
+    d = 1
+    while d < n:
+        for i in range(2 * d - 1, n, 2 * d):
+            x[i] = _combine(x[i - d], x[i])
+        d *= 2
+    x[n - 1] = (1.0, 0.0)  # identity
+    d = n // 2
+    while d >= 1:
+        for i in range(2 * d - 1, n, 2 * d):
+            left = x[i - d]
+            x[i - d] = x[i]
+            x[i] = _combine(x[i], left)
+        d //= 2
+    return [_combine(x[i], elems[i]) for i in range(n)]
+
+
+def test_scan_brute_force_tree_orders_dyadic():
+    """Every parenthesisation of the operator reproduces the sequential oracle
+    bit for bit on dyadic inputs (all intermediate values exact)."""
+    r = random.Random(7)
+    for trial in range(40):
+        T = r.randint(1, 16)
+        a = np.array([r.choice([0.0, 0.5, -0.5, 1.0, -1.0, 2.0]) for _ in range(T)])
+        b = np.array([float(r.randint(-4, 4)) for _ in range(T)])
+        h0 = float(r.randint(-3, 3))
+        h = oracle.scan_fwd(a.reshape(T, 1), b.reshape(T, 1), np.array([h0]))[:, 0]
+        elems = [(0.0, h0)] + [(a[t], b[t]) for t in range(T)]
+        for t in range(T):
+            for _ in range(3):
+                assert _random_tree(elems[: t + 2], r)[1] == h[t]
+        if T in (1, 2, 4, 8, 16):
+            # element 0 carries h0; pad to a power of two with identities
+            seq = [(a[0], a[0] * h0 + b[0])] + [(a[t], b[t]) for t in range(1, T)]
+            inc = _blelloch_inclusive(seq)
+            assert [v[1] for v in inc] == list(h)
+
+
+# ----------------------------------------------------------- backward scan
+
+def _fd(fun, x, eps=1e-6):
+    g = np.zeros_like(x)
+    flat = x.reshape(-1)
+    for i in range(flat.size):
+        old = flat[i]
+        flat[i] = old + eps
+        fp = fun()
+        flat[i] = old - eps
+        fm = fun()
+        flat[i] = old
+        g.reshape(-1)[i] = (fp - fm) / (2 * eps)
+    return g
+
+
+def test_scan_bwd_finite_differences():
+    T, C = 9, 3
+    a = rng.uniform(-0.9, 0.9, (T, C))
+    b = rng.standard_normal((T, C))
+    h0 = rng.standard_normal(C)
+    g = rng.standard_normal((T, C))
+    loss = lambda: float(np.sum(g * oracle.scan_fwd(a, b, h0)))
+    h = oracle.scan_fwd(a, b, h0)
+    da, db, dh0 = oracle.scan_bwd(a, h, g, h0)
+    np.testing.assert_allclose(da, _fd(loss, a), rtol=1e-7, atol=1e-8)
+    np.testing.assert_allclose(db, _fd(loss, b), rtol=1e-7, atol=1e-8)
+    np.testing.assert_allclose(dh0, _fd(loss, h0), rtol=1e-7, atol=1e-8)
+
+
+def test_scan_bwd_is_transposed_solve():
+    T, C = 120, 4
+    a = rng.uniform(-1.1, 1.1, (T, C))
+    b = rng.standard_normal((T, C))
+    g = rng.standard_normal((T, C))
+    h = oracle.scan_fwd(a, b)
+    da, db, dh0 = oracle.scan_bwd(a, h, g)
+    for c in range(C):
+        np.testing.assert_allclose(db[:, c], _bidiag_solve_T(a[:, c], g[:, c]), rtol=1e-10, atol=1e-10)
+    # h0 absent means zeros: da_0 = 0
+    assert np.all(da[0] == 0.0)
+
+
+# --------------------------------------------------------------------- SRU
+
+def _sru_inputs(T, B, D, seed=5):
+    r = np.random.default_rng(seed)
+    return dict(xt=r.standard_normal((T, B, D)), uf=r.standard_normal((T, B, D)),
+                ur=r.standard_normal((T, B, D)), x=r.standard_normal((T, B, D)),
+                bf=r.standard_normal(D), br=r.standard_normal(D),
+                c0=r.standard_normal((B, D)))
+
+
+def test_sru_forget_closed_gives_c_equal_xt():
+    p = _sru_inputs(20, 2, 3)
+    p["uf"][:] = -40.0
+    p["bf"][:] = 0.0
+    h, c = oracle.sru_fwd(**p)
+    np.testing.assert_allclose(c, p["xt"], rtol=0, atol=1e-15)
+
+
+def test_sru_reset_gate_limits():
+    p = _sru_inputs(20, 2, 3)
+    p["br"][:] = 0.0
+    p["ur"][:] = 40.0
+    h, c = oracle.sru_fwd(**p)
+    np.testing.assert_allclose(h, np.tanh(c), rtol=0, atol=1e-15)
+    p["ur"][:] = -40.0
+    h, c = oracle.sru_fwd(**p)
+    np.testing.assert_allclose(h, p["x"], rtol=0, atol=1e-15)
+
+
+def test_sru_memory_is_linear_recurrence_solve():
+    p = _sru_inputs(80, 2, 3)
+    h, c = oracle.sru_fwd(**p)
+    f = 1.0 / (1.0 + np.exp(-(p["uf"] + p["bf"])))
+    for bb in range(2):
+        for d in range(3):
+            a = f[:, bb, d]
+            rhs = (1 - a) * p["xt"][:, bb, d]
+            rhs[0] += a[0] * p["c0"][bb, d]
+            np.testing.assert_allclose(c[:, bb, d], _bidiag_solve(a, rhs), rtol=1e-11, atol=1e-12)
+
+
+def test_sru_bwd_finite_differences():
+    T, B, D = 7, 2, 3
+    p = _sru_inputs(T, B, D)
+    dh = np.random.default_rng(9).standard_normal((T, B, D))
+    loss = lambda: float(np.sum(dh * oracle.sru_fwd(**p)[0]))
+    h, c = oracle.sru_fwd(**p)
+    dxt, duf, dur, dx, dbf, dbr, dc0 = oracle.sru_bwd(c=c, dh=dh, **p)
+    for got, key in ((dxt, "xt"), (duf, "uf"), (dur, "ur"), (dx, "x"),
+                     (dbf, "bf"), (dbr, "br"), (dc0, "c0")):
+        np.testing.assert_allclose(got, _fd(loss, p[key]), rtol=1e-6, atol=1e-8, err_msg=key)
+
+
+# -------------------------------------------------------------------- DEER
+
+def test_rollout_w_zero_is_tanh():
+    u = rng.standard_normal((50, 2, 4))
+    y = oracle.rollout_tanh(np.zeros(4), u, rng.standard_normal((2, 4)))
+    np.testing.assert_allclose(y, np.tanh(u), rtol=0, atol=1e-15)
+
+
+def test_rollout_small_signal_is_linear_recurrence():
+    """tanh(z) = z + O(z^3): at amplitude 1e-6 the rollout equals the linear
+    recurrence y_t = w y_{t-1} + u_t to ~1e-18 absolute."""
+    T, D = 200, 5
+    w = rng.uniform(-0.9, 0.9, D)
+    u = 1e-6 * rng.standard_normal((T, 1, D))
+    y = oracle.rollout_tanh(w, u)
+    for d in range(D):
+        lin = _bidiag_solve(np.full(T, w[d]), u[:, 0, d])
+        np.testing.assert_allclose(y[:, 0, d], lin, rtol=0, atol=1e-16)
+
+
+def test_deer_step_is_newton_on_residual():
+    """One iteration equals y - J_F(y)^{-1} F(y) for F(y)_t = y_t - tanh(w y_{t-1} + u_t),
+    with J_F formed by differentiating F and solved by a banded library solve."""
+    T, B, D = 40, 2, 3
+    w = rng.uniform(-0.9, 0.9, D)
+    u = rng.standard_normal((T, B, D))
+    h0 = rng.standard_normal((B, D))
+    y = rng.standard_normal((T, B, D)) * 0.5
+    ynew, rho = oracle.deer_step(w, u, y, h0)
+    ref = np.empty_like(y)
+    for bb in range(B):
+        for d in range(D):
+            yc = y[:, bb, d]
+            prev = np.concatenate([[h0[bb, d]], yc[:-1]])
+            s = w[d] * prev + u[:, bb, d]
+            F = yc - np.tanh(s)
+            sub = -w[d] * (1 - np.tanh(s) ** 2)  # dF_t / dy_{t-1}
+            ab = np.zeros((2, T))
+            ab[0] = 1.0
+            ab[1, :-1] = sub[1:]
+            ref[:, bb, d] = yc - scipy.linalg.solve_banded((1, 0), ab, F)
+    np.testing.assert_allclose(ynew, ref, rtol=1e-10, atol=1e-12)
+    assert rho == pytest.approx(np.max(np.abs(ref - y)), rel=1e-12)
+
+
+def test_deer_prefix_exact_after_k_iterations():
+    """After k iterations from zero, y^(k)_t is exact for t < k."""
+    T, D = 12, 4
+    w = rng.uniform(-0.9, 0.9, D)
+    u = rng.standard_normal((T, 1, D))
+    h0 = rng.standard_normal((1, D))
+    roll = oracle.rollout_tanh(w, u, h0)
+    y = None
+    for k in range(1, T + 1):
+        y, _ = oracle.deer_step(w, u, y, h0)
+        np.testing.assert_allclose(y[:k], roll[:k], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(y, roll, rtol=0, atol=1e-14)
+
+
+def test_deer_converges_to_rollout():
+    T, B, D = 3000, 2, 8
+    w = rng.uniform(-0.9, 0.9, D)
+    u = rng.standard_normal((T, B, D))
+    y, k, hist, st = oracle.deer(w, u, eps=1e-12, kmax=60)
+    assert st == oracle.DEER_CONVERGED
+    np.testing.assert_allclose(y, oracle.rollout_tanh(w, u), rtol=0, atol=1e-11)
+    assert hist[-1] < 1e-12 <= hist[-2]
+
+
+def test_deer_w_zero_takes_two_iterations():
+    u = rng.standard_normal((100, 2, 3))
+    y, k, hist, st = oracle.deer(np.zeros(3), u, eps=1e-5, kmax=20)
+    assert (k, st) == (2, oracle.DEER_CONVERGED)
+    assert hist[1] == 0.0
+    np.testing.assert_allclose(y, np.tanh(u), rtol=0, atol=1e-15)
+
+
+def test_deer_stopping_rule_edges():
+    w = rng.uniform(-0.9, 0.9, 3)
+    u = rng.standard_normal((64, 1, 3))
+    _, k, hist, st = oracle.deer(w, u, eps=1e9, kmax=20)
+    assert (k, st, len(hist)) == (1, oracle.DEER_CONVERGED, 1)
+    _, k, hist, st = oracle.deer(w, u, eps=0.0, kmax=5)
+    assert (k, st, len(hist)) == (5, oracle.DEER_NOT_CONVERGED, 5)
+
+
+def test_oracle_threads_do_not_change_results():
+    a = rng.uniform(-1, 1, (300, 33))
+    b = rng.standard_normal((300, 33))
+    oracle.set_num_threads(1)
+    h1 = oracle.scan_fwd(a, b)
+    oracle.set_num_threads(4)
+    h4 = oracle.scan_fwd(a, b)
+    oracle.set_num_threads(0)
+    assert np.array_equal(h1, h4)
