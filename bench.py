@@ -1,0 +1,559 @@
+#!/usr/bin/env python3
+"""Benchmark of the chunked linear-recurrence hot path on one GB300 (or N
+independent replicas under torchrun).
+
+One step = one pass of every hot-path operation over its full-size synthetic
+workload, in this order ([T, B, D] layout, seed 0):
+  scan_tiny   fp32 4x1024x256      forward + backward scan
+  sru         fp32 32x2048x1024    fused SRU forward + backward
+  scan_long   fp32 1x1048576x128   forward scan (million-step carry)
+  scan_large  bf16 16x8192x4096    forward + backward scan
+  deer        fp32 4x65536x256     DEER Newton solve to max|dy| < 1e-5 (K iterations)
+
+Metric: scan elements per second (each element of each pass counts once; a
+DEER solve counts N*K) and the algorithmic HBM bytes per second.  Inputs are
+resident in HBM before the timed region; every input except scan_tiny's
+(12.6 MB) is larger than the 129 MB L2, and each step streams ~18 GB, so no
+step starts with its inputs cached.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "scan elements/s and achieved HBM GB/s (fraction of GB300 peak), fwd+bwd"
+UNIT = "elements/s"
+FALLBACK_HBM_GBS = 6800.0
+EPS, KMAX = 1e-5, 20
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture, keyed by operation; valid only while the kernel sources hash to
+# `src`.  Filled from the committed ncu summaries under profiles/.
+NCU_TRAFFIC = {}
+
+
+def src_hash() -> str:
+    h = hashlib.sha256()
+    cdir = os.path.join(ROOT, "linear_recurrence_scan_chunked_gb300", "csrc")
+    for n in sorted(os.listdir(cdir)):
+        if n.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(cdir, n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for k in ("hbm_gbs", "hbm_GBs", "hbm"):
+                if k in d:
+                    v = d[k]
+                    v = v.get("value", v.get("burst")) if isinstance(v, dict) else v
+                    return float(v), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# --------------------------------------------------------------- workloads
+
+def esize(wl):
+    return 2 if wl.dtype == "bf16" else 4
+
+
+# (name, workload, passes); bytes per element per pass (algorithmic)
+ROWS = [("scan_tiny", W.SCAN_TINY, ("fwd", "bwd")),
+        ("sru", W.SRU, ("fwd", "bwd")),
+        ("scan_long", W.SCAN_LONG, ("fwd",)),
+        ("scan_large", W.SCAN_BF16, ("fwd", "bwd")),
+        ("deer", W.DEER, ("solve",))]
+
+
+def select_rows(only, T):
+    """Restrict the step to the named operations (name or name.pass)."""
+    global ROWS
+    if not only:
+        return
+    keep = []
+    for name, wl, passes in ROWS:
+        ps = tuple(p for p in passes if name in only or f"{name}.{p}" in only)
+        if ps:
+            keep.append((name, W.like(wl, T=T, name=wl.name) if T else wl, ps))
+    if not keep:
+        raise SystemExit(f"--only {only}: no such operation")
+    ROWS = keep
+
+
+def pass_bytes(wl, p, k=1):
+    """Algorithmic HBM bytes of one pass (state/parameter vectors included)."""
+    es, N, C, D = esize(wl), wl.N, wl.C, wl.D
+    if wl.kind == "scan":
+        return (3 * es * N + es * C) if p == "fwd" else (5 * es * N + 2 * es * C)
+    if wl.kind == "sru":
+        return (6 * es * N + es * C + 8 * D) if p == "fwd" else (10 * es * N + 2 * es * C + 16 * D)
+    # DEER: iteration 1 reads u and writes y; later iterations also read y_old
+    return es * N * (2 + 3 * (k - 1)) + 4 * D * k
+
+
+def pass_elems(wl, p, k=1):
+    return wl.N * (k if p == "solve" else 1)
+
+
+class Bench:
+    def __init__(self, dev):
+        import torch
+        import linear_recurrence_scan_chunked_gb300 as lrs
+        self.torch, self.lrs, self.dev = torch, lrs, dev
+        lrs.load()
+        self.host = {}
+        self.d = {}
+        for name, wl, _ in ROWS:
+            inp = W.make_inputs(wl, 0)
+            self.host[name] = inp
+            self.d[name] = {k: self._to_dev(v, wl, k) for k, v in inp.items()}
+            o = self.d[name]
+            e = lambda: torch.empty((wl.T, wl.B, wl.D), dtype=self._tdt(wl), device=dev)
+            if wl.kind == "scan":
+                o["h"] = e()
+                if wl.backward:
+                    o["da"], o["db"] = e(), e()
+                    o["dh0"] = torch.empty((wl.B, wl.D), dtype=self._tdt(wl), device=dev)
+            elif wl.kind == "sru":
+                o["h"], o["c"] = e(), e()
+                o["grad"] = {k: e() for k in ("dxt", "duf", "dur", "dx")}
+                o["grad"]["dbf"] = torch.empty(wl.D, device=dev)
+                o["grad"]["dbr"] = torch.empty(wl.D, device=dev)
+                o["grad"]["dc0"] = torch.empty((wl.B, wl.D), dtype=self._tdt(wl), device=dev)
+            else:
+                o["y"] = e()
+        self.k_last = 0
+        torch.cuda.synchronize()
+
+    def _tdt(self, wl):
+        return self.torch.bfloat16 if wl.dtype == "bf16" else self.torch.float32
+
+    def _to_dev(self, v, wl, key):
+        t = self.torch
+        if key in ("w", "bf", "br") or wl.dtype == "f32":
+            return t.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to(self.dev)
+        return t.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(t.bfloat16).to(self.dev)
+
+    # one row; returns (elements, bytes, launches)
+    def run_row(self, name, wl, passes, ev=None):
+        L, o = self.lrs, self.d[name]
+        elems = byts = launches = 0
+        for p in passes:
+            if ev is not None:
+                ev[(name, p)][0].record()
+            if wl.kind == "scan" and p == "fwd":
+                L.lr_scan_fwd(o["a"], o["b"], o["h0"], o["h"])
+                launches += 1
+            elif wl.kind == "scan":
+                L.lr_scan_bwd(o["a"], o["h"], o["g"], o["h0"], o["da"], o["db"], o["dh0"])
+                launches += 1
+            elif wl.kind == "sru" and p == "fwd":
+                L.sru_fwd(o["xt"], o["uf"], o["ur"], o["x"], o["bf"], o["br"], o["c0"], o["h"], o["c"])
+                launches += 1
+            elif wl.kind == "sru":
+                L.sru_bwd(o["xt"], o["uf"], o["ur"], o["x"], o["bf"], o["br"], o["c"], o["dh"],
+                          o["c0"], out=o["grad"])
+                launches += 2
+            else:
+                _, k, _, _, st = L.deer_diag_solve(o["w"], o["u"], o["h0"], o["y"], eps=EPS, kmax=KMAX)
+                if st != L.LR_OK:
+                    raise RuntimeError(f"DEER did not converge (status {st})")
+                self.k_last = k
+                launches += k
+            if ev is not None:
+                ev[(name, p)][1].record()
+            k = self.k_last if p == "solve" else 1
+            elems += pass_elems(wl, p, k)
+            byts += pass_bytes(wl, p, k)
+        return elems, byts, launches
+
+    def step(self, ev=None):
+        tot = [0, 0, 0]
+        for name, wl, passes in ROWS:
+            r = self.run_row(name, wl, passes, ev)
+            tot = [a + b for a, b in zip(tot, r)]
+        return tot
+
+    # ---- end to end: host buffers, copies inside the timed region
+    def setup_e2e(self):
+        t = self.torch
+        self.pin_in, self.pin_out = {}, {}
+        self.h2d = self.d2h = 0
+        for name, wl, passes in ROWS:
+            o = self.d[name]
+            ins = [k for k in self.host[name] if k not in ("w", "bf", "br")]
+            self.pin_in[name] = {k: o[k].cpu().pin_memory() for k in ins}
+            outs = {}
+            if wl.kind == "scan":
+                outs = {k: o[k] for k in (("h", "da", "db", "dh0") if wl.backward else ("h",))}
+            elif wl.kind == "sru":
+                outs = {"h": o["h"], "c": o["c"], **o["grad"]}
+            else:
+                outs = {"y": o["y"]}
+            self.pin_out[name] = {k: (v, t.empty(v.shape, dtype=v.dtype, pin_memory=True))
+                                  for k, v in outs.items()}
+            self.h2d += sum(v.numel() * v.element_size() for v in self.pin_in[name].values())
+            self.d2h += sum(v.numel() * v.element_size() for v, _ in self.pin_out[name].values())
+
+    def e2e_step(self):
+        elems = 0
+        for name, wl, passes in ROWS:
+            o = self.d[name]
+            for k, hv in self.pin_in[name].items():
+                o[k].copy_(hv, non_blocking=True)
+            e, _, _ = self.run_row(name, wl, passes)
+            elems += e
+            for k, (dv, hv) in self.pin_out[name].items():
+                hv.copy_(dv, non_blocking=True)
+        self.torch.cuda.current_stream().synchronize()
+        return elems
+
+
+# ------------------------------------------------------------ clocks
+
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.p, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                out, _ = self.p.communicate(timeout=5)
+            except Exception:
+                self.p.kill()
+                out, _ = self.p.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------- CPU (oracle) side
+
+class OracleSampler:
+    """Times the fp64 oracle, as it stands, on a bounded sample of every row's
+    workload: the first T' time steps of C' channels (a time prefix of a
+    channel subset is an exact sub-problem).  A short calibration run sizes the
+    sample so each row takes about budget_s / rows seconds; the sampled inputs
+    are generated once and reused by every timed run."""
+
+    def __init__(self, budget_s: float):
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        self.nth = oracle.num_threads()
+        per = budget_s / len(ROWS)
+        self.subs = {}
+        for name, wl, passes in ROWS:
+            Cs = min(wl.C, max(128, 8 * self.nth))
+            Tc = min(wl.T, 256)
+            inp = self._inputs(wl, Tc, Cs)
+            el, dt, _ = self._run(wl, passes, inp)
+            target = el / max(dt, 1e-4) * per  # elements that take about `per` seconds
+            Ts = int(min(wl.T, max(Tc, target / (el / Tc))))
+            if Ts == wl.T:  # the whole time axis fits: widen the channel sample instead
+                Cs = int(min(wl.C, max(Cs, (target / (el / (Tc * Cs)) / wl.T) // 128 * 128)))
+            self.subs[name] = self._inputs(wl, Ts, Cs)
+
+    @staticmethod
+    def _inputs(wl, T, Cs):
+        if wl.kind == "sru":
+            sub = W.like(wl, T=T, B=max(1, Cs // min(wl.D, 128)), D=min(wl.D, 128))
+        else:
+            sub = W.like(wl, T=T, B=1, D=Cs)
+        inp = {k: (np.asarray(v, np.float64) if k in ("w", "bf", "br") else W.to_f64(v, wl.dtype))
+               for k, v in W.make_inputs(sub, 0).items()}
+        return sub, inp
+
+    def _run(self, wl, passes, sub_inp):
+        o, (sub, inp) = self.oracle, sub_inp
+        t0 = time.perf_counter()
+        el, k = 0, 1
+        if wl.kind == "scan":
+            h = o.scan_fwd(inp["a"], inp["b"], inp["h0"])
+            el += sub.N
+            if "bwd" in passes:
+                o.scan_bwd(inp["a"], h, inp["g"], inp["h0"])
+                el += sub.N
+        elif wl.kind == "sru":
+            h, c = o.sru_fwd(inp["xt"], inp["uf"], inp["ur"], inp["x"], inp["bf"], inp["br"], inp["c0"])
+            o.sru_bwd(inp["xt"], inp["uf"], inp["ur"], inp["x"], inp["bf"], inp["br"], c, inp["dh"], inp["c0"])
+            el += 2 * sub.N
+        else:
+            _, k, _, _ = o.deer(inp["w"], inp["u"], inp["h0"], eps=EPS, kmax=KMAX)
+            el += sub.N * k
+        return el, time.perf_counter() - t0, k
+
+    def run(self):
+        """One pass over the samples: (elements/s per row, description, DEER K)."""
+        rates, desc, kd = {}, [], 1
+        for name, wl, passes in ROWS:
+            el, dt, k = self._run(wl, passes, self.subs[name])
+            if wl.kind == "deer":
+                kd = k
+            rates[name] = el / dt
+            sub = self.subs[name][0]
+            desc.append(f"{name}: first {sub.T} of T={wl.T} steps x {sub.C} of C={wl.C} channels, "
+                        f"{dt:.2f} s ({el / dt / 1e6:.1f} M el/s)")
+        return rates, "; ".join(desc), kd
+
+
+def step_rate_from_rows(rates: dict, k_deer: int) -> float:
+    """Elements/s of one full step when each row runs at its measured rate."""
+    tot_el = tot_t = 0.0
+    for name, wl, passes in ROWS:
+        for p in passes:
+            e = pass_elems(wl, p, k_deer)
+            tot_el += e
+            tot_t += e / rates[name]
+    return tot_el / tot_t
+
+
+# ------------------------------------------------------------------- main
+
+def dist_init(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def config_dict():
+    return {"workload": "; ".join(f"{n} {wl.dtype} T={wl.T} B={wl.B} D={wl.D} "
+                                  f"{'+'.join(p)}" for n, wl, p in ROWS),
+            "layout": "[T,B,D], D contiguous", "seed": 0,
+            "l2": "inputs larger than the 129 MB L2 except scan_tiny (12.6 MB); each step streams ~18 GB",
+            "deer": {"eps": EPS, "kmax": KMAX},
+            "distributions": "see workloads/__init__.py (N(0,0.01) read as std 0.01)"}
+
+
+def run_reference(args, ws, rank):
+    """The oracle on the host cores, same metric and step structure; each step
+    is a bounded sample of the workload (the whole run stays within minutes)."""
+    if rank != 0:
+        return
+    budget = max(4.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    smp = OracleSampler(budget)
+    for _ in range(args.warmup):
+        smp.run()
+    vals, ks = [], []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r, desc, kd = smp.run()
+        ks.append(kd)
+        vals.append(step_rate_from_rows(r, kd))
+    wall = time.perf_counter() - t0
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": smp.nth, "kind": "oracle",
+                             "sample": desc + f"; rates combined in the step's element mix, "
+                                              f"DEER counted as N*K with the sample's K={ks[-1]}"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--only", action="append", default=[],
+                    help="run only these operations (e.g. scan_large.bwd); for profiling cases")
+    ap.add_argument("--T", type=int, default=0, help="override T of the selected rows (profiling cases)")
+    args = ap.parse_args()
+    select_rows(args.only, args.T)
+    ws, rank, local = dist_init(args)
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        barrier(ws)
+        return
+
+    import torch
+    import linear_recurrence_scan_chunked_gb300 as lrs
+    if args.warmup < 3:
+        print("note: fewer than 3 warm-up steps requested; using 3", file=sys.stderr)
+        args.warmup = 3
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    b = Bench(dev)
+    for _ in range(args.warmup):
+        b.step()
+    torch.cuda.synchronize()
+    if lrs.last_error() != lrs.LR_OK:
+        raise RuntimeError("device error during warm-up")
+
+    ev = {(n, p): (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for n, _, ps in ROWS for p in ps}
+    per = {key: [] for key in ev}
+    ks = []
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    elems = byts = launches = 0
+    with Clocks(local) as clk:
+        start.record()
+        for _ in range(args.steps):
+            e, by, la = b.step(ev)
+            elems, byts, launches = elems + e, byts + by, launches + la
+            ks.append(b.k_last)
+            torch.cuda.synchronize()  # per-row events are read per step
+            for key, (e0, e1) in ev.items():
+                per[key].append(e0.elapsed_time(e1))
+        end.record()
+        torch.cuda.synchronize()
+    barrier(ws)
+    ms = start.elapsed_time(end)
+    ms = max_over_ranks(ms, ws)
+    if lrs.last_error() != lrs.LR_OK:
+        raise RuntimeError("device error during the timed region")
+    ms_step = ms / args.steps
+    value = elems * ws / (ms / 1e3)
+    gbs = byts * ws / (ms / 1e3) / 1e9
+
+    # per-operation breakdown and the dominant kernel's roofline
+    peak, peak_kind = peak_hbm()
+    k_med = int(statistics.median(ks))
+    ops = {}
+    for (n, p), ts in per.items():
+        wl = next(w for nn, w, _ in ROWS if nn == n)
+        k = k_med if p == "solve" else 1
+        t_ms = statistics.mean(ts)
+        launches_op = k if p == "solve" else 1
+        byt = pass_bytes(wl, p, k)
+        ops[f"{n}.{p}"] = {"ms": round(t_ms, 4), "launches": launches_op,
+                           "GBps": round(byt / (t_ms / 1e3) / 1e9, 1),
+                           "frac": round(byt / (t_ms / 1e3) / 1e9 / peak, 3)}
+    dom = max(ops, key=lambda k: ops[k]["ms"])
+    dn, dp = dom.split(".")
+    dwl = next(w for nn, w, _ in ROWS if nn == dn)
+    k = k_med if dp == "solve" else 1
+    launch_ms = ops[dom]["ms"] / ops[dom]["launches"]
+    bytes_per_launch = pass_bytes(dwl, dp, k) / ops[dom]["launches"]
+    achieved = bytes_per_launch / (launch_ms / 1e3) / 1e9
+    tr = NCU_TRAFFIC.get(dom)
+    traffic = tr["bytes"] if tr and tr.get("src") == src_hash() else None
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": dom,
+            "peak_source": f"{peak_kind} HBM copy bandwidth",
+            "bytes_per_launch": bytes_per_launch}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32 compute (f32 and bf16 storage)",
+            "data": "synthetic", "config": config_dict(),
+            "hbm_GBps": round(gbs, 1), "hbm_frac": round(gbs / peak, 4), "deer_iters": k_med,
+            "gpu_launches": launches, "clocks": clk.summary(), "roofline": roof, "ops": ops}
+
+    if not args.no_e2e:
+        b.setup_e2e()
+        b.e2e_step()  # warm
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0.record()
+        el = 0
+        for _ in range(args.e2e_steps):
+            el += b.e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        t = max_over_ranks(e0.elapsed_time(e1), ws)
+        line["e2e"] = {"value": el * ws / (t / 1e3), "unit": UNIT, "h2d_bytes_per_step": b.h2d,
+                       "d2h_bytes_per_step": b.d2h, "ms_per_step": t / args.e2e_steps}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        smp = OracleSampler(args.cpu_budget)
+        rates, desc, _ = smp.run()
+        line["cpu_baseline"] = {"value": step_rate_from_rows(rates, k_med), "unit": UNIT,
+                                "cores": smp.nth, "kind": "oracle",
+                                "sample": desc + f"; extrapolated to the step mix with K={k_med}"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    barrier(ws)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * lrscan.h -- C ABI of the GB300 (sm_103a) chunked linear-recurrence library.
+ *
+ * The library evaluates the elementwise (diagonal) first-order linear
+ * recurrence
+ *
+ *     h_t = a_t (.) h_{t-1} + b_t ,   h_{-1} = h0 ,
+ *
+ * along the sequence axis as a parallel prefix scan over the associative
+ * operator (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2) (earlier element on the
+ * left, identity (1, 0)), and four computations built on that scan.
+ *
+ * Sources (blog.hotdry.top, all dated 2025-09-21):
+ *   [P1] "CUDA并行化RNN训练：从O(T)到O(log T)的工程实践与参数调优":
+ *        SRU paragraph (forget gate without h_{t-1}, highway reset gate),
+ *        parallel-scan paragraph (associative operation, divide and conquer
+ *        in log T for forward and backward), checklist item 2 (fuse all
+ *        sigmoid/tanh/multiply-add into one kernel).
+ *   [P2] "RNN CUDA内核优化：实现序列长度无关的恒定推理延迟":
+ *        LSTM paragraph (C_t = f_t*C_{t-1} + i_t*C~_t is a linear recurrence,
+ *        tree reduction in log2 T stages), memory paragraph (shared-memory
+ *        tiling, coalesced access, warp-level non-divergent boundaries).
+ *   [P4] DEER page (.../cuda-parallel-rnn-training-logt-optimization),
+ *        section "核心原理：DEER 框架与牛顿法的工程映射" (Newton form, the three
+ *        steps, the linear inverse solved as a prefix scan) and section
+ *        "工程实现：CUDA 内核与内存布局的关键参数" (stop at ||y^(i+1)-y^(i)|| < eps
+ *        or K_max).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Sequence tensors are [T, B, D] row-major with D contiguous (channel
+ *    c = b*D + d, element (t, c) at offset t*B*D + c).  Per-step state tensors
+ *    (h0, dh0, c0, dc0) are [B, D].  Per-feature parameters (w, bf, br and
+ *    their gradients) are [D] and always fp32.
+ *  - `dtype` is the storage type of every sequence and state tensor:
+ *    LR_F32 (fp32) or LR_BF16 (bfloat16).  All arithmetic is fp32; bf16
+ *    results are rounded to nearest-even when stored.
+ *  - All pointers are DEVICE pointers owned by the caller; the library never
+ *    frees or retains them.  Inputs are read-only.  No output may alias an
+ *    input or another output.  Pointers must be aligned to the element size;
+ *    16-byte alignment plus D a multiple of 4 (fp32) or 8 (bf16) selects the
+ *    128-bit vector path, anything else the scalar path.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *    asynchronous on it except deer_diag_solve, which synchronises the stream
+ *    once per Newton iteration to read the residual.
+ *  - Sizes: B, T, D >= 0 with B*T*D < 2^62; an empty problem is a no-op
+ *    (gradients of the initial state are zeroed).
+ *  - The library keeps one internal workspace per device (look-back tile
+ *    descriptors, a tile ticket, an error word, DEER's second iterate buffer,
+ *    SRU bias partials), grown on demand with cudaMalloc.  Calls on different
+ *    streams are serialised through it with CUDA events.
+ *  - Return value: LR_OK, or an lr_status describing an argument or launch
+ *    error detected before or while enqueuing the work.  Errors detected on
+ *    the device while the kernels run (a look-back wait that ran out) are
+ *    recorded in a sticky device error word read by lr_last_error().
+ */
+#ifndef LRSCAN_H
+#define LRSCAN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { LR_F32 = 0, LR_BF16 = 1 } lr_dtype;
+
+typedef enum {
+    LR_OK = 0,
+    LR_ERR_INVALID_ARG = 1,   /* NULL required pointer, negative size, bad dtype */
+    LR_ERR_ALIGN = 2,         /* pointer not aligned to its element size */
+    LR_ERR_CUDA = 3,          /* a CUDA runtime call failed (message: lr_cuda_error_string) */
+    LR_ERR_TIMEOUT = 4,       /* device: a look-back wait ran out; outputs are NaN */
+    LR_ERR_NONFINITE = 5,     /* DEER: a residual was NaN or Inf */
+    LR_ERR_NOT_CONVERGED = 6, /* DEER: kmax iterations without residual < eps */
+    LR_ERR_TOO_LARGE = 7      /* sizes beyond the supported range */
+} lr_status;
+
+/*
+ * Forward scan (row a1): h_t = a_t * h_{t-1} + b_t for t = 0..T-1 with
+ * h_{-1} = h0.  [P1] parallel-scan paragraph; [P2] LSTM paragraph.
+ *   a, b : [T,B,D] in   coefficients and inputs
+ *   h0   : [B,D]   in   initial state; NULL means zeros
+ *   h    : [T,B,D] out  states (h0 is not repeated in h)
+ */
+int lr_scan_fwd(const void* a, const void* b, const void* h0, void* h,
+                int64_t B, int64_t T, int64_t D, int dtype, void* stream);
+
+/*
+ * Backward scan (row a2): BPTT of the forward scan for the loss whose
+ * gradient with respect to every h_t is dh_t.  With
+ *   delta_{T-1} = dh_{T-1},  delta_t = dh_t + a_{t+1} delta_{t+1}:
+ *   db_t = delta_t,  da_t = delta_t h_{t-1} (h_{-1} = h0),  dh0 = a_0 delta_0.
+ * [P1] parallel-scan paragraph (the same log-depth scan serves backward).
+ *   a, h, dh : [T,B,D] in   (h = output of lr_scan_fwd)
+ *   h0       : [B,D]   in   NULL means zeros
+ *   da, db   : [T,B,D] out
+ *   dh0      : [B,D]   out  may be NULL (not computed)
+ */
+int lr_scan_bwd(const void* a, const void* h, const void* h0, const void* dh,
+                void* da, void* db, void* dh0,
+                int64_t B, int64_t T, int64_t D, int dtype, void* stream);
+
+/*
+ * SRU layer forward, linear form (row a3), fused into one scan launch.
+ * [P1] SRU paragraph and checklist item 2:
+ *   f_t = sigmoid(uf_t + bf),  r_t = sigmoid(ur_t + br)
+ *   c_t = f_t c_{t-1} + (1 - f_t) xt_t   (c_{-1} = c0)
+ *   h_t = r_t tanh(c_t) + (1 - r_t) x_t
+ *   xt, uf, ur, x : [T,B,D] in   precomputed projections and highway input
+ *   bf, br        : [D] fp32 in  forget / reset biases
+ *   c0            : [B,D]   in   NULL means zeros
+ *   h, c          : [T,B,D] out  (c is kept for sru_bwd)
+ */
+int sru_fwd(const void* xt, const void* uf, const void* ur, const void* x,
+            const float* bf, const float* br, const void* c0, void* h, void* c,
+            int64_t B, int64_t T, int64_t D, int dtype, void* stream);
+
+/*
+ * SRU layer backward (row a4), given the forward c and the upstream dh:
+ *   dr = dh (tanh c - x), dur = dr r (1-r), dx = dh (1-r),
+ *   dc_t = dh_t r_t (1 - tanh^2 c_t) + f_{t+1} dc_{t+1}   (reverse scan)
+ *   dxt = dc (1-f), duf = dc (c_{t-1} - xt) f (1-f), dc0 = f_0 dc_0,
+ *   dbf[d] = sum_{t,b} duf,  dbr[d] = sum_{t,b} dur  (deterministic order).
+ *   dxt, duf, dur, dx : [T,B,D] out;  dbf, dbr : [D] fp32 out (overwritten);
+ *   dc0 : [B,D] out, may be NULL.
+ */
+int sru_bwd(const void* xt, const void* uf, const void* ur, const void* x,
+            const float* bf, const float* br, const void* c0, const void* c,
+            const void* dh, void* dxt, void* duf, void* dur, void* dx,
+            float* dbf, float* dbr, void* dc0,
+            int64_t B, int64_t T, int64_t D, int dtype, void* stream);
+
+/*
+ * DEER solve of the diagonal tanh RNN h_t = tanh(w (.) h_{t-1} + u_t) (row a5).
+ * [P4] "核心原理": Newton iteration from the all-zero guess; iteration k
+ * builds, from the previous iterate shifted by one step (ytil_{-1} = h0),
+ *   s_t = w ytil_{t-1} + u_t,  J_t = w (1 - tanh^2 s_t),
+ *   rhs_t = tanh(s_t) - J_t ytil_{t-1},
+ * and solves y_t = J_t y_{t-1} + rhs_t by the scan (one fused launch).
+ * [P4] "工程实现": stop at the first k with max|y^(k) - y^(k-1)| < eps (max
+ * over all B*T*D entries) or at k = kmax.
+ *   w          : [D] fp32 in
+ *   u          : [T,B,D] in;  h0 : [B,D] in (NULL = zeros)
+ *   y          : [T,B,D] out  the last iterate
+ *   iters_out  : host int out, iterations performed (>= 1 unless T*B*D = 0)
+ *   resid_out  : host float out, residual of the last iteration (may be NULL)
+ *   resid_hist : host float[kmax] out, residual of every iteration (may be NULL)
+ * Returns LR_ERR_NOT_CONVERGED or LR_ERR_NONFINITE (with y, iters and
+ * residuals still written) when the iteration did not reach eps.
+ */
+int deer_diag_solve(const float* w, const void* u, const void* h0, void* y,
+                    int64_t B, int64_t T, int64_t D, float eps, int kmax,
+                    int* iters_out, float* resid_out, float* resid_hist,
+                    int dtype, void* stream);
+
+/*
+ * Reads and clears the device error word of the current device (synchronises
+ * the device).  Returns LR_OK or the first recorded device error
+ * (LR_ERR_TIMEOUT).
+ */
+int lr_last_error(void);
+
+/* Static text for a status code. */
+const char* lr_status_str(int status);
+
+/* Text of the last CUDA runtime error seen by this thread's calls. */
+const char* lr_cuda_error_string(void);
+
+/* Bytes of device workspace currently held on the current device. */
+int64_t lr_workspace_bytes(void);
+
+/*
+ * Test hook for the bounded look-back wait: launches the forward scan kernel
+ * on a private 2-chunk problem whose first chunk is never published, with the
+ * wait limited to `spin_limit` polls, so the second chunk's wait runs out.
+ * It leaves LR_ERR_TIMEOUT in the device error word.  Nothing faults or hangs.
+ */
+int lr_test_lookback_timeout(uint32_t spin_limit, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LRSCAN_H */

@@ -1,0 +1,395 @@
+// lr_api.cu -- the C ABI declared in include/lrscan.h: argument checks, the
+// per-device workspace, launch geometry, and the DEER host loop.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "lr_launch.h"
+#include "lrscan.h"
+
+namespace {
+
+using namespace lrs;
+
+constexpr uint32_t kEpochMax = (1u << 30) - 1;
+constexpr uint32_t kSpinLimit = 1u << 21;  // polls (backing off to ~1 us each): ~2 s
+constexpr int kMaxIters = 4096;            // DEER kmax bound (residual slots)
+
+thread_local char g_cuda_msg[256] = "";
+
+int cuda_fail(cudaError_t e) {
+    snprintf(g_cuda_msg, sizeof g_cuda_msg, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return LR_ERR_CUDA;
+}
+#define CK(x)                                  \
+    do {                                       \
+        cudaError_t e_ = (x);                  \
+        if (e_ != cudaSuccess) return cuda_fail(e_); \
+    } while (0)
+
+// Per-device workspace.  Everything the kernels need besides the caller's
+// buffers: look-back descriptors (flags + payload), the tile ticket, the
+// error word, DEER residual slots and second iterate, SRU bias partials.
+struct DevWS {
+    uint32_t* flags = nullptr;   size_t flags_cap = 0;    // entries
+    float* payload = nullptr;    size_t payload_cap = 0;  // floats
+    uint32_t* words = nullptr;   // [0] ticket, [1] error bits, [2..] DEER residual slots
+    float* partials = nullptr;   size_t partials_cap = 0; // floats
+    void* ybuf = nullptr;        size_t ybuf_cap = 0;     // bytes
+    uint32_t* host_word = nullptr;                        // pinned, for residual reads
+    void* test_buf = nullptr;                             // timeout-test problem
+    uint32_t epoch = 0;
+    cudaEvent_t done = nullptr;
+    cudaStream_t last_stream = nullptr;
+    bool has_last = false;
+    int64_t bytes = 0;
+};
+
+std::mutex g_mu;
+std::vector<DevWS*> g_ws;
+
+int get_ws(DevWS** out) {
+    int dev = 0;
+    CK(cudaGetDevice(&dev));
+    if ((int)g_ws.size() <= dev) g_ws.resize(dev + 1, nullptr);
+    if (!g_ws[dev]) {
+        DevWS* w = new DevWS();
+        CK(cudaMalloc(&w->words, sizeof(uint32_t) * (2 + kMaxIters)));
+        CK(cudaMemset(w->words, 0, sizeof(uint32_t) * (2 + kMaxIters)));
+        CK(cudaHostAlloc(&w->host_word, sizeof(uint32_t), cudaHostAllocDefault));
+        CK(cudaEventCreateWithFlags(&w->done, cudaEventDisableTiming));
+        w->bytes = sizeof(uint32_t) * (2 + kMaxIters);
+        g_ws[dev] = w;
+    }
+    *out = g_ws[dev];
+    return LR_OK;
+}
+
+template <typename T>
+int grow(DevWS& ws, T** p, size_t* cap, size_t need, bool zero) {
+    if (need <= *cap) return LR_OK;
+    size_t n = need + need / 4;
+    CK(cudaDeviceSynchronize());  // nothing in flight may still use the old buffer
+    if (*p) {
+        CK(cudaFree(*p));
+        ws.bytes -= (int64_t)(*cap * sizeof(T));
+    }
+    *p = nullptr;
+    *cap = 0;
+    CK(cudaMalloc((void**)p, n * sizeof(T)));
+    if (zero) CK(cudaMemset(*p, 0, n * sizeof(T)));
+    *cap = n;
+    ws.bytes += (int64_t)(n * sizeof(T));
+    return LR_OK;
+}
+
+// Order this call after the previous call on any other stream.
+int enter(DevWS& ws, cudaStream_t s) {
+    if (ws.has_last && ws.last_stream != s) CK(cudaStreamWaitEvent(s, ws.done, 0));
+    return LR_OK;
+}
+int leave(DevWS& ws, cudaStream_t s) {
+    CK(cudaEventRecord(ws.done, s));
+    ws.last_stream = s;
+    ws.has_last = true;
+    return LR_OK;
+}
+
+// Geometry + descriptors for one launch of `op`.
+int plan(DevWS& ws, Op op, int dtype, bool vec, int64_t T, int64_t C, int64_t D, Geom* g,
+         Lookback* lb, cudaStream_t s) {
+    const TileShape ts = tile_shape(op, dtype, vec);
+    g->T = T;
+    g->C = C;
+    g->D = D;
+    g->n_chunks = (T + ts.L - 1) / ts.L;
+    g->n_ct = (int)((C + ts.CW - 1) / ts.CW);
+    const int64_t tiles = g->n_chunks * (int64_t)g->n_ct;
+    if ((C + ts.CW - 1) / ts.CW > INT32_MAX || tiles > INT32_MAX) return LR_ERR_TOO_LARGE;
+    g->n_launch = (uint32_t)tiles;
+    g->ticket_base = 0;
+    int st = grow(ws, &ws.flags, &ws.flags_cap, (size_t)tiles, true);
+    if (st) return st;
+    st = grow(ws, &ws.payload, &ws.payload_cap, (size_t)tiles * ts.CW * 3, false);
+    if (st) return st;
+    if (++ws.epoch > kEpochMax) {  // wrap: clear every flag once
+        ws.epoch = 1;
+        CK(cudaMemsetAsync(ws.flags, 0, ws.flags_cap * sizeof(uint32_t), s));
+    }
+    const size_t np = (size_t)tiles * ts.CW;
+    lb->flags = ws.flags;
+    lb->agg_a = ws.payload;
+    lb->agg_b = ws.payload + np;
+    lb->inc = ws.payload + 2 * np;
+    lb->ticket = ws.words;
+    lb->err = ws.words + 1;
+    lb->epoch = ws.epoch;
+    lb->spin_limit = kSpinLimit;
+    return LR_OK;
+}
+
+size_t esize(int dtype) { return dtype == LR_BF16 ? 2 : 4; }
+
+int check_sizes(int64_t B, int64_t T, int64_t D, int dtype) {
+    if (dtype != LR_F32 && dtype != LR_BF16) return LR_ERR_INVALID_ARG;
+    if (B < 0 || T < 0 || D < 0) return LR_ERR_INVALID_ARG;
+    const int64_t lim = (int64_t)1 << 62;
+    if (B && T && D) {
+        if (B > lim / T) return LR_ERR_TOO_LARGE;
+        if (B * T > lim / D) return LR_ERR_TOO_LARGE;
+        if (B * T * D >= lim) return LR_ERR_TOO_LARGE;
+    }
+    return LR_OK;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Required/optional pointer checks.  Returns status; sets *vec when every
+// pointer allows the 16-byte path and D is a multiple of the vector width.
+int check_ptrs(std::initializer_list<const void*> req, std::initializer_list<const void*> opt,
+               std::initializer_list<const void*> params, int dtype, int64_t D, bool* vec) {
+    const size_t es = esize(dtype);
+    bool v = (D % kvec(dtype, true)) == 0;
+    for (const void* p : req) {
+        if (!p) return LR_ERR_INVALID_ARG;
+        if (!aligned(p, es)) return LR_ERR_ALIGN;
+        v = v && aligned(p, 16);
+    }
+    for (const void* p : opt) {
+        if (!p) continue;
+        if (!aligned(p, es)) return LR_ERR_ALIGN;
+        v = v && aligned(p, 16);
+    }
+    for (const void* p : params) {
+        if (!p) return LR_ERR_INVALID_ARG;
+        if (!aligned(p, 4)) return LR_ERR_ALIGN;
+        v = v && aligned(p, 16);
+    }
+    *vec = v;
+    return LR_OK;
+}
+
+}  // namespace
+
+#define GUARD std::lock_guard<std::mutex> lock_(g_mu)
+#define TRY(x)                \
+    do {                      \
+        int st_ = (x);        \
+        if (st_) return st_;  \
+    } while (0)
+
+extern "C" {
+
+int lr_scan_fwd(const void* a, const void* b, const void* h0, void* h, int64_t B, int64_t T,
+                int64_t D, int dtype, void* stream) {
+    TRY(check_sizes(B, T, D, dtype));
+    if (B * T * D == 0) return LR_OK;
+    bool vec;
+    TRY(check_ptrs({a, b, h}, {h0}, {}, dtype, D, &vec));
+    GUARD;
+    cudaStream_t s = (cudaStream_t)stream;
+    DevWS* ws;
+    TRY(get_ws(&ws));
+    Geom g;
+    Lookback lb;
+    TRY(enter(*ws, s));
+    TRY(plan(*ws, OP_SCAN_FWD, dtype, vec, T, B * D, D, &g, &lb, s));
+    CK(launch_scan_fwd(dtype, vec, a, b, h0, h, g, lb, s));
+    return leave(*ws, s);
+}
+
+int lr_scan_bwd(const void* a, const void* h, const void* h0, const void* dh, void* da, void* db,
+                void* dh0, int64_t B, int64_t T, int64_t D, int dtype, void* stream) {
+    TRY(check_sizes(B, T, D, dtype));
+    cudaStream_t s = (cudaStream_t)stream;
+    if (B * T * D == 0) {
+        if (dh0 && B * D > 0) {
+            if (!aligned(dh0, esize(dtype))) return LR_ERR_ALIGN;
+            CK(cudaMemsetAsync(dh0, 0, (size_t)(B * D) * esize(dtype), s));
+        }
+        return LR_OK;
+    }
+    bool vec;
+    TRY(check_ptrs({a, h, dh, da, db}, {h0, dh0}, {}, dtype, D, &vec));
+    GUARD;
+    DevWS* ws;
+    TRY(get_ws(&ws));
+    Geom g;
+    Lookback lb;
+    TRY(enter(*ws, s));
+    TRY(plan(*ws, OP_SCAN_BWD, dtype, vec, T, B * D, D, &g, &lb, s));
+    CK(launch_scan_bwd(dtype, vec, a, h, h0, dh, da, db, dh0, g, lb, s));
+    return leave(*ws, s);
+}
+
+int sru_fwd(const void* xt, const void* uf, const void* ur, const void* x, const float* bf,
+            const float* br, const void* c0, void* h, void* c, int64_t B, int64_t T, int64_t D,
+            int dtype, void* stream) {
+    TRY(check_sizes(B, T, D, dtype));
+    if (B * T * D == 0) return LR_OK;
+    bool vec;
+    TRY(check_ptrs({xt, uf, ur, x, h, c}, {c0}, {bf, br}, dtype, D, &vec));
+    GUARD;
+    cudaStream_t s = (cudaStream_t)stream;
+    DevWS* ws;
+    TRY(get_ws(&ws));
+    Geom g;
+    Lookback lb;
+    TRY(enter(*ws, s));
+    TRY(plan(*ws, OP_SRU_FWD, dtype, vec, T, B * D, D, &g, &lb, s));
+    CK(launch_sru_fwd(dtype, vec, xt, uf, ur, x, bf, br, c0, h, c, g, lb, s));
+    return leave(*ws, s);
+}
+
+int sru_bwd(const void* xt, const void* uf, const void* ur, const void* x, const float* bf,
+            const float* br, const void* c0, const void* c, const void* dh, void* dxt, void* duf,
+            void* dur, void* dx, float* dbf, float* dbr, void* dc0, int64_t B, int64_t T,
+            int64_t D, int dtype, void* stream) {
+    TRY(check_sizes(B, T, D, dtype));
+    cudaStream_t s = (cudaStream_t)stream;
+    if (B * T * D == 0) {
+        if (D > 0) {
+            if (!dbf || !dbr) return LR_ERR_INVALID_ARG;
+            CK(cudaMemsetAsync(dbf, 0, (size_t)D * 4, s));
+            CK(cudaMemsetAsync(dbr, 0, (size_t)D * 4, s));
+        }
+        if (dc0 && B * D > 0) CK(cudaMemsetAsync(dc0, 0, (size_t)(B * D) * esize(dtype), s));
+        return LR_OK;
+    }
+    bool vec;
+    TRY(check_ptrs({xt, uf, ur, x, c, dh, dxt, duf, dur, dx}, {c0, dc0}, {bf, br, dbf, dbr}, dtype,
+                   D, &vec));
+    GUARD;
+    DevWS* ws;
+    TRY(get_ws(&ws));
+    Geom g;
+    Lookback lb;
+    TRY(enter(*ws, s));
+    TRY(plan(*ws, OP_SRU_BWD, dtype, vec, T, B * D, D, &g, &lb, s));
+    TRY(grow(*ws, &ws->partials, &ws->partials_cap, (size_t)(2 * g.n_chunks * g.C), false));
+    CK(launch_sru_bwd(dtype, vec, xt, uf, ur, x, bf, br, c0, c, dh, dxt, duf, dur, dx, dc0,
+                      ws->partials, g, lb, s));
+    CK(launch_bias_reduce(ws->partials, g.n_chunks, B, D, dbf, dbr, s));
+    return leave(*ws, s);
+}
+
+int deer_diag_solve(const float* w, const void* u, const void* h0, void* y, int64_t B, int64_t T,
+                    int64_t D, float eps, int kmax, int* iters_out, float* resid_out,
+                    float* resid_hist, int dtype, void* stream) {
+    TRY(check_sizes(B, T, D, dtype));
+    if (!iters_out || kmax < 1 || kmax > kMaxIters || !(eps >= 0.f)) return LR_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (B * T * D == 0) {
+        *iters_out = 0;
+        if (resid_out) *resid_out = 0.f;
+        return LR_OK;
+    }
+    bool vec;
+    TRY(check_ptrs({u, y}, {h0}, {w}, dtype, D, &vec));
+    GUARD;
+    DevWS* ws;
+    TRY(get_ws(&ws));
+    const size_t nbytes = (size_t)(B * T * D) * esize(dtype);
+    {
+        size_t cap = ws->ybuf_cap;
+        char* p = (char*)ws->ybuf;
+        TRY(grow(*ws, &p, &cap, nbytes, false));
+        ws->ybuf = p;
+        ws->ybuf_cap = cap;
+    }
+    TRY(enter(*ws, s));
+    uint32_t* slots = ws->words + 2;
+    CK(cudaMemsetAsync(slots, 0, sizeof(uint32_t) * kmax, s));
+    // iterate k writes buf[k % 2]; buf[1] is the caller's y
+    void* buf[2] = {ws->ybuf, y};
+    int k = 0, status = LR_ERR_NOT_CONVERGED;
+    float rho = 0.f;
+    for (k = 1; k <= kmax; ++k) {
+        Geom g;
+        Lookback lb;
+        TRY(plan(*ws, OP_DEER, dtype, vec, T, B * D, D, &g, &lb, s));
+        CK(launch_deer_iter(dtype, vec, w, u, h0, k == 1 ? nullptr : buf[(k - 1) & 1], buf[k & 1],
+                            slots + (k - 1), g, lb, s));
+        CK(cudaMemcpyAsync(ws->host_word, slots + (k - 1), sizeof(uint32_t),
+                           cudaMemcpyDeviceToHost, s));
+        CK(cudaStreamSynchronize(s));
+        uint32_t bits = *ws->host_word;
+        memcpy(&rho, &bits, sizeof rho);
+        if (resid_hist) resid_hist[k - 1] = rho;
+        if (!(rho <= 3.4e38f)) { status = LR_ERR_NONFINITE; break; }
+        if (rho < eps) { status = LR_OK; break; }
+    }
+    if (k > kmax) k = kmax;
+    if ((k & 1) == 0) CK(cudaMemcpyAsync(y, ws->ybuf, nbytes, cudaMemcpyDeviceToDevice, s));
+    *iters_out = k;
+    if (resid_out) *resid_out = rho;
+    TRY(leave(*ws, s));
+    return status;
+}
+
+int lr_last_error(void) {
+    GUARD;
+    DevWS* ws;
+    TRY(get_ws(&ws));
+    CK(cudaDeviceSynchronize());
+    uint32_t bits = 0;
+    CK(cudaMemcpy(&bits, ws->words + 1, sizeof bits, cudaMemcpyDeviceToHost));
+    CK(cudaMemset(ws->words + 1, 0, sizeof(uint32_t)));
+    if (bits & ERRBIT_TIMEOUT) return LR_ERR_TIMEOUT;
+    return LR_OK;
+}
+
+const char* lr_status_str(int st) {
+    switch (st) {
+        case LR_OK: return "ok";
+        case LR_ERR_INVALID_ARG: return "invalid argument";
+        case LR_ERR_ALIGN: return "pointer not aligned to its element size";
+        case LR_ERR_CUDA: return "CUDA runtime error";
+        case LR_ERR_TIMEOUT: return "look-back wait ran out on the device";
+        case LR_ERR_NONFINITE: return "non-finite residual";
+        case LR_ERR_NOT_CONVERGED: return "not converged within kmax iterations";
+        case LR_ERR_TOO_LARGE: return "problem size beyond the supported range";
+        default: return "unknown status";
+    }
+}
+
+const char* lr_cuda_error_string(void) { return g_cuda_msg; }
+
+int64_t lr_workspace_bytes(void) {
+    GUARD;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if ((int)g_ws.size() <= dev || !g_ws[dev]) return 0;
+    return g_ws[dev]->bytes;
+}
+
+int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
+    GUARD;
+    cudaStream_t s = (cudaStream_t)stream;
+    DevWS* ws;
+    TRY(get_ws(&ws));
+    const TileShape ts = tile_shape(OP_SCAN_FWD, LR_F32, true);
+    const int64_t T = 2 * ts.L, C = ts.CW;
+    if (!ws->test_buf) {
+        CK(cudaMalloc(&ws->test_buf, (size_t)(3 * T * C) * sizeof(float)));
+        CK(cudaMemset(ws->test_buf, 0, (size_t)(3 * T * C) * sizeof(float)));
+        ws->bytes += 3 * T * C * (int64_t)sizeof(float);
+    }
+    float* a = (float*)ws->test_buf;
+    Geom g;
+    Lookback lb;
+    TRY(enter(*ws, s));
+    TRY(plan(*ws, OP_SCAN_FWD, LR_F32, true, T, C, C, &g, &lb, s));
+    // One CTA, handed tile 1: it waits for tile 0, which nobody publishes.
+    g.n_launch = 1;
+    g.ticket_base = 1;
+    lb.spin_limit = spin_limit;
+    CK(launch_scan_fwd(LR_F32, true, a, a + T * C, nullptr, a + 2 * T * C, g, lb, s));
+    return leave(*ws, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,215 @@
+"""GPU vs fp64 oracle, element by element, on seeded inputs at sizes the oracle
+finishes in seconds: several tiles along time and channels, ragged time and
+channel tails, the scalar (unaligned / odd D) path, bf16 storage, and the
+degenerate cases (T = 1, one channel, empty problems).  All calls go through
+the C ABI (via the thin binding)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from lrtest import assert_close, dev_inputs, f64_inputs, to_f64, TOL
+
+pytestmark = pytest.mark.gpu
+
+# (T, B, D): tiles are 64 (fp32 fwd) / 32 rows and 128 / 256 channels wide
+SHAPES = [(1, 1, 4), (5, 2, 8), (64, 1, 128), (65, 1, 128), (200, 3, 96), (1000, 2, 64),
+          (333, 4, 40), (77, 3, 5), (513, 1, 129), (2048, 2, 256), (3, 1, 1)]
+LONG = [(100003, 1, 4), (20000, 1, 128)]
+
+
+def _scan_case(cuda, T, B, D, dtype, seed=0):
+    wl = W.like(W.SCAN_TINY, T, B, D, dtype)
+    inp = W.make_inputs(wl, seed)
+    inp["h0"] = W.store(W.normal(seed, 99, (B, D)), dtype)  # nonzero initial state
+    dv, f = dev_inputs(inp, dtype), f64_inputs(inp, dtype)
+    h = cuda.lr_scan_fwd(dv["a"], dv["b"], dv["h0"])
+    href = oracle.scan_fwd(f["a"], f["b"], f["h0"])
+    assert_close("h", to_f64(h), href, dtype)
+    da, db, dh0 = cuda.lr_scan_bwd(dv["a"], h, dv["g"], dv["h0"])
+    rda, rdb, rdh0 = oracle.scan_bwd(f["a"], href, f["g"], f["h0"])
+    assert_close("da", to_f64(da), rda, dtype)
+    assert_close("db", to_f64(db), rdb, dtype)
+    assert_close("dh0", to_f64(dh0), rdh0, dtype)
+
+
+@pytest.mark.parametrize("shape", SHAPES + LONG)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_scan_fwd_bwd(cuda, shape, dtype):
+    _scan_case(cuda, *shape, dtype)
+
+
+@pytest.mark.parametrize("shape", SHAPES[:9])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_sru_fwd_bwd(cuda, shape, dtype):
+    T, B, D = shape
+    wl = W.like(W.SRU, T, B, D, dtype)
+    inp = W.make_inputs(wl, 3)
+    inp["bf"] = W.normal(3, 40, (D,))
+    inp["br"] = W.normal(3, 41, (D,))
+    inp["c0"] = W.store(W.normal(3, 42, (B, D)), dtype)
+    dv, f = dev_inputs(inp, dtype), f64_inputs(inp, dtype)
+    h, c = cuda.sru_fwd(dv["xt"], dv["uf"], dv["ur"], dv["x"], dv["bf"], dv["br"], dv["c0"])
+    rh, rc = oracle.sru_fwd(f["xt"], f["uf"], f["ur"], f["x"], f["bf"], f["br"], f["c0"])
+    assert_close("h", to_f64(h), rh, dtype)
+    assert_close("c", to_f64(c), rc, dtype)
+    g = cuda.sru_bwd(dv["xt"], dv["uf"], dv["ur"], dv["x"], dv["bf"], dv["br"], c, dv["dh"], dv["c0"])
+    ref = oracle.sru_bwd(f["xt"], f["uf"], f["ur"], f["x"], f["bf"], f["br"], rc, f["dh"], f["c0"])
+    for k, r in zip(("dxt", "duf", "dur", "dx", "dbf", "dbr", "dc0"), ref):
+        # the bias gradients are sums over T*B terms: compare against the
+        # magnitude of the sum's terms, scaled like the other tensors
+        assert_close(k, to_f64(g[k]), r, dtype)
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 4), (64, 2, 8), (300, 3, 40), (77, 2, 5), (5000, 1, 128)])
+@pytest.mark.parametrize("dtype", ["f32"])
+def test_deer(cuda, shape, dtype):
+    T, B, D = shape
+    wl = W.like(W.DEER, T, B, D, dtype)
+    inp = W.make_inputs(wl, 5)
+    inp["h0"] = W.store(W.normal(5, 43, (B, D)), dtype)
+    dv, f = dev_inputs(inp, dtype), f64_inputs(inp, dtype)
+    y, k, resid, hist, st = cuda.deer_diag_solve(dv["w"], dv["u"], dv["h0"], eps=1e-5, kmax=20)
+    ry, rk, rhist, rst = oracle.deer(f["w"], f["u"], f["h0"], eps=1e-5, kmax=20)
+    assert (k, st) == (rk, rst), (k, rk, hist, list(rhist))
+    assert_close("y", to_f64(y), ry, dtype)
+    np.testing.assert_allclose(hist, rhist, rtol=1e-3, atol=1e-6)
+
+
+def test_scan_integer_valued_is_bit_exact(cuda):
+    """a in {0, +1, -1}, b small integers: every association order is exact,
+    so the chunked scan must equal the sequential oracle bit for bit."""
+    r = np.random.default_rng(11)
+    for (T, B, D) in [(4097, 2, 128), (50000, 1, 8), (999, 3, 7)]:
+        a = r.choice([0.0, 1.0, 1.0, 1.0, -1.0], size=(T, B, D)).astype(np.float32)
+        b = r.integers(-3, 4, size=(T, B, D)).astype(np.float32)
+        h0 = r.integers(-5, 6, size=(B, D)).astype(np.float32)
+        g = r.integers(-3, 4, size=(T, B, D)).astype(np.float32)
+        ta, tb, th0, tg = (torch.from_numpy(x).cuda() for x in (a, b, h0, g))
+        h = cuda.lr_scan_fwd(ta, tb, th0)
+        href = oracle.scan_fwd(a, b, h0)
+        assert np.array_equal(to_f64(h), href)
+        da, db, dh0 = cuda.lr_scan_bwd(ta, h, tg, th0)
+        rda, rdb, rdh0 = oracle.scan_bwd(a, href, g, h0)
+        assert np.array_equal(to_f64(db), rdb)
+        assert np.array_equal(to_f64(da), rda)
+        assert np.array_equal(to_f64(dh0), rdh0)
+
+
+def test_scan_a_zero_gives_b_bit_exact(cuda):
+    b = torch.randn(3000, 2, 64, device="cuda")
+    h = cuda.lr_scan_fwd(torch.zeros_like(b), b, torch.randn(2, 64, device="cuda"))
+    assert torch.equal(h, b)
+
+
+def test_unaligned_pointers_take_scalar_path(cuda):
+    T, B, D = 300, 2, 64
+    wl = W.like(W.SCAN_TINY, T, B, D, "f32")
+    inp = W.make_inputs(wl, 8)
+    n = T * B * D
+    buf_a = torch.empty(n + 1, device="cuda")
+    buf_b = torch.empty(n + 1, device="cuda")
+    buf_h = torch.empty(n + 1, device="cuda")
+    a = buf_a[1:].view(T, B, D)
+    b = buf_b[1:].view(T, B, D)
+    h = buf_h[1:].view(T, B, D)
+    a.copy_(torch.from_numpy(inp["a"]))
+    b.copy_(torch.from_numpy(inp["b"]))
+    cuda.lr_scan_fwd(a, b, None, h)
+    assert_close("h", to_f64(h), oracle.scan_fwd(inp["a"], inp["b"]), "f32")
+
+
+def test_null_optional_states(cuda):
+    T, B, D = 130, 2, 16
+    wl = W.like(W.SCAN_TINY, T, B, D, "f32")
+    inp = W.make_inputs(wl, 9)
+    dv, f = dev_inputs(inp, "f32"), f64_inputs(inp, "f32")
+    h = cuda.lr_scan_fwd(dv["a"], dv["b"], None)
+    href = oracle.scan_fwd(f["a"], f["b"])
+    assert_close("h", to_f64(h), href, "f32")
+    da, db, dh0 = cuda.lr_scan_bwd(dv["a"], h, dv["g"], None, want_dh0=False)
+    assert dh0 is None
+    rda, rdb, _ = oracle.scan_bwd(f["a"], href, f["g"])
+    assert_close("da", to_f64(da), rda, "f32")
+
+
+def test_empty_problems(cuda):
+    e = torch.empty(0, 3, 8, device="cuda")
+    h = cuda.lr_scan_fwd(e, e)
+    assert h.shape == (0, 3, 8)
+    dh0 = torch.full((3, 8), 7.0, device="cuda")
+    cuda.lr_scan_bwd(e, e, e, dh0=dh0)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dh0) == 0
+    y, k, resid, hist, st = cuda.deer_diag_solve(torch.zeros(8, device="cuda"), e)
+    assert (k, st) == (0, cuda.LR_OK)
+
+
+def test_repeat_is_bitwise_deterministic(cuda):
+    T, B, D = 2048, 4, 256
+    wl = W.like(W.SRU, T, B, D, "f32")
+    inp = W.make_inputs(wl, 4)
+    dv = dev_inputs(inp, "f32")
+    outs = []
+    for _ in range(3):
+        h, c = cuda.sru_fwd(dv["xt"], dv["uf"], dv["ur"], dv["x"], dv["bf"], dv["br"], dv["c0"])
+        g = cuda.sru_bwd(dv["xt"], dv["uf"], dv["ur"], dv["x"], dv["bf"], dv["br"], c, dv["dh"], dv["c0"])
+        outs.append([h.clone(), c.clone()] + [g[k].clone() for k in sorted(g)])
+    for o in outs[1:]:
+        for x, y in zip(outs[0], o):
+            assert torch.equal(x, y)
+
+
+def test_long_scan_is_bitwise_deterministic(cuda):
+    """Many chunks along time: the look-back sees different inclusive
+    predecessors from run to run, yet the carry is folded in a fixed order."""
+    T, B, D = 300000, 1, 128
+    wl = W.like(W.SCAN_LONG, T, B, D)
+    dv = dev_inputs(W.make_inputs(wl, 13), "f32")
+    hs = [cuda.lr_scan_fwd(dv["a"], dv["b"], dv["h0"]).clone() for _ in range(4)]
+    for h in hs[1:]:
+        assert torch.equal(h, hs[0])
+
+
+def test_calls_on_two_streams(cuda):
+    T, B, D = 4096, 2, 128
+    wl = W.like(W.SCAN_TINY, T, B, D, "f32")
+    inp = W.make_inputs(wl, 12)
+    dv, f = dev_inputs(inp, "f32"), f64_inputs(inp, "f32")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    outs = []
+    for i in range(6):
+        s = s1 if i % 2 else s2
+        with torch.cuda.stream(s):
+            outs.append(cuda.lr_scan_fwd(dv["a"], dv["b"], dv["h0"], stream=s))
+    torch.cuda.synchronize()
+    href = oracle.scan_fwd(f["a"], f["b"], f["h0"])
+    for h in outs:
+        assert_close("h", to_f64(h), href, "f32")
+
+
+def test_lookback_wait_runs_out_cleanly(cuda):
+    """A chunk whose predecessor never publishes gives up after the poll limit,
+    records LR_ERR_TIMEOUT, and the context stays usable."""
+    assert cuda.last_error() == cuda.LR_OK
+    assert cuda.test_lookback_timeout(2000) == cuda.LR_OK
+    assert cuda.last_error() == cuda.LR_ERR_TIMEOUT
+    assert cuda.last_error() == cuda.LR_OK  # cleared by the read
+    _scan_case(cuda, 500, 2, 64, "f32")
+
+
+def test_argument_errors(cuda):
+    a = torch.randn(10, 2, 8, device="cuda")
+    with pytest.raises(ValueError):
+        cuda.lr_scan_fwd(a, torch.randn(10, 2, 7, device="cuda"))
+    with pytest.raises(TypeError):
+        cuda.lr_scan_fwd(a.double(), a.double())
+    lib = cuda.load()
+    assert lib.lr_scan_fwd(None, None, None, None, 2, 10, 8, 0, None) == cuda.LR_ERR_INVALID_ARG
+    bad = a.view(-1)[1:].view(torch.uint8)[1:]  # byte-offset pointer
+    import ctypes
+    st = lib.lr_scan_fwd(ctypes.c_void_p(bad.data_ptr()), ctypes.c_void_p(a.data_ptr()), None,
+                         ctypes.c_void_p(a.data_ptr()), 1, 1, 1, 0, None)
+    assert st == cuda.LR_ERR_ALIGN
