@@ -1,0 +1,64 @@
+"""The C-ABI library: it builds, loads and exports every function that
+include/lrscan.h declares; argument errors are reported before any CUDA call.
+CPU only (no compute call)."""
+import ctypes
+
+import pytest
+
+import linear_recurrence_scan_chunked_gb300 as lrs
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lrs.build()
+    return lrs.load()
+
+
+def test_every_declared_function_is_exported(lib):
+    names = lrs.declared_functions()
+    for required in ("lr_scan_fwd", "lr_scan_bwd", "sru_fwd", "sru_bwd", "deer_diag_solve",
+                     "lr_last_error", "lr_status_str"):
+        assert required in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for st in range(8):
+        assert lrs.status_str(st)
+    assert lrs.status_str(999) == "unknown status"
+
+
+def test_argument_errors_before_cuda(lib):
+    P = None
+    # null required pointers, bad dtype, negative sizes
+    assert lib.lr_scan_fwd(P, P, P, P, 2, 3, 4, 0, P) == lrs.LR_ERR_INVALID_ARG
+    assert lib.lr_scan_fwd(P, P, P, P, 2, 3, 4, 7, P) == lrs.LR_ERR_INVALID_ARG
+    assert lib.lr_scan_fwd(P, P, P, P, -1, 3, 4, 0, P) == lrs.LR_ERR_INVALID_ARG
+    assert lib.lr_scan_bwd(P, P, P, P, P, P, P, 2, 3, 4, 0, P) == lrs.LR_ERR_INVALID_ARG
+    assert lib.sru_fwd(*([P] * 9), 2, 3, 4, 0, P) == lrs.LR_ERR_INVALID_ARG
+    assert lib.sru_bwd(*([P] * 16), 2, 3, 4, 0, P) == lrs.LR_ERR_INVALID_ARG
+    iters = ctypes.c_int(0)
+    assert lib.deer_diag_solve(P, P, P, P, 2, 3, 4, ctypes.c_float(1e-5), 20, ctypes.byref(iters),
+                               P, P, 0, P) == lrs.LR_ERR_INVALID_ARG
+    assert lib.deer_diag_solve(P, P, P, P, 2, 3, 4, ctypes.c_float(1e-5), 0, ctypes.byref(iters),
+                               P, P, 0, P) == lrs.LR_ERR_INVALID_ARG
+    # sizes beyond 2^62 elements
+    assert lib.lr_scan_fwd(P, P, P, P, 1 << 31, 1 << 31, 4, 0, P) == lrs.LR_ERR_TOO_LARGE
+    # misaligned (odd byte address) fp32 pointer
+    buf = ctypes.create_string_buffer(64)
+    odd = ctypes.c_void_p(ctypes.addressof(buf) + 1)
+    assert lib.lr_scan_fwd(odd, odd, P, odd, 1, 1, 1, 0, P) == lrs.LR_ERR_ALIGN
+
+
+def test_empty_problem_is_a_no_op(lib):
+    # B*T*D == 0 returns before touching the device
+    assert lib.lr_scan_fwd(None, None, None, None, 0, 5, 4, 0, None) == lrs.LR_OK
+    assert lib.sru_fwd(*([None] * 9), 3, 0, 4, 0, None) == lrs.LR_OK
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(lrs, "_lib", None)
+    monkeypatch.setattr(lrs, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        lrs.load()
