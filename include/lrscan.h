@@ -155,6 +155,30 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y,
                     int dtype, void* stream);
 
 /*
+ * Forward scan that allocates nothing (no counterpart in the pages: this is a
+ * deployment variant of lr_scan_fwd, same arguments and results).
+ * For callers that may not allocate device memory: code running under an
+ * engine or framework that owns every device byte (a hidden cudaMalloc can
+ * fail at run time or fragment its pool) and latency-critical loops (the
+ * cudaFree that grows lr_scan_fwd's cached workspace synchronises the device).
+ * Its look-back scratch is one fixed 4 MiB __device__ array that every GPU
+ * loading this library holds until the process exits.
+ *   - Problems needing more scratch than that return LR_ERR_TOO_LARGE (the
+ *     limit is ~2,700 tiles of 64 time steps x 128 fp32 channels, i.e.
+ *     ~22 M fp32 elements; about half as many tiles for bf16).
+ *   - All calls share the array: calls whose kernels overlap on the GPU race
+ *     and give wrong results; order them on one stream or with events.
+ *   - The first call on a device looks up the array's address; make it before
+ *     any stream capture.
+ *   - err_dev: optional device word (4-byte aligned) into which device-side
+ *     errors are OR-ed (bit 0: a look-back wait ran out; h is then NaN); NULL
+ *     keeps them inside the scratch array.  lr_last_error() does not see them.
+ */
+int lr_scan_fwd_noalloc(const void* a, const void* b, const void* h0, void* h,
+                        int64_t B, int64_t T, int64_t D, int dtype,
+                        uint32_t* err_dev, void* stream);
+
+/*
  * Reads and clears the device error word of the current device (synchronises
  * the device).  Returns LR_OK or the first recorded device error
  * (LR_ERR_TIMEOUT).

@@ -1,0 +1,128 @@
+// noalloc.cu -- lr_scan_fwd_noalloc: the forward scan for callers that must
+// not allocate device memory.
+//
+// Who needs it: code that runs under someone else's memory manager -- an
+// inference engine or framework plugin that owns every device byte and plans
+// its budget ahead, a latency-critical server loop.  lr_scan_fwd grows a
+// cached workspace with cudaMalloc on first use (and cudaFree + cudaMalloc
+// when a larger problem arrives); a hidden allocation can fail at run time,
+// fragments the owner's pool, and cudaFree synchronises the whole device.
+// This variant keeps its look-back scratch (tile flags, tile descriptors, the
+// tile ticket) in one fixed, file-scope __device__ array instead, so it calls
+// no cudaMalloc, cudaFree or allocating library routine.
+//
+// Costs and rules of the fixed array:
+//   * every GPU that loads the library holds kScratchBytes (4 MiB) of device
+//     memory until the process exits;
+//   * problems needing more look-back descriptors than fit are rejected with
+//     LR_ERR_TOO_LARGE (about 2,700 tiles of 64 time steps x 128 fp32
+//     channels, i.e. ~22 M fp32 elements; half that many tiles for bf16);
+//   * every call shares the one array: two calls whose kernels overlap on the
+//     GPU (different streams, no ordering between them) race on it and give
+//     wrong results.  Order such calls on one stream or with events.
+//   * the array keeps the last call's contents; flags are tagged with a
+//     per-call epoch so old ones are ignored, and the tile ticket is cleared
+//     (a 4-byte memset, not an allocation) before every launch.
+//   * the first call on a device looks up the array's device address with
+//     cudaGetSymbolAddress (host code cannot use the symbol itself); make that
+//     first call before any stream capture.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "lr_launch.h"
+#include "lrscan.h"
+
+namespace {
+
+using namespace lrs;
+
+constexpr size_t kScratchBytes = size_t(4) << 20;
+constexpr size_t kHeaderBytes = 256;  // [0] ticket, [1] error word
+constexpr uint32_t kEpochMax = (1u << 30) - 1;
+constexpr uint32_t kSpinLimit = 1u << 21;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+
+struct NoAllocDev {
+    unsigned char* base = nullptr;  // device address of g_scratch on this device
+    uint32_t epoch = 0;
+};
+std::mutex g_na_mu;
+NoAllocDev g_na[kMaxDevices];
+
+size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+
+}  // namespace
+
+extern "C" int lr_scan_fwd_noalloc(const void* a, const void* b, const void* h0, void* h,
+                                   int64_t B, int64_t T, int64_t D, int dtype,
+                                   uint32_t* err_dev, void* stream) {
+    if (dtype != LR_F32 && dtype != LR_BF16) return LR_ERR_INVALID_ARG;
+    if (B < 0 || T < 0 || D < 0) return LR_ERR_INVALID_ARG;
+    if (B == 0 || T == 0 || D == 0) return LR_OK;
+    const int64_t lim = (int64_t)1 << 62;
+    if (B > lim / T || B * T > lim / D) return LR_ERR_TOO_LARGE;
+    if (!a || !b || !h) return LR_ERR_INVALID_ARG;
+    const size_t es = dtype == LR_BF16 ? 2 : 4;
+    bool vec = (D % kvec(dtype, true)) == 0;
+    for (const void* p : {a, b, (const void*)h, h0}) {
+        if (!p) continue;
+        if ((uintptr_t)p % es) return LR_ERR_ALIGN;
+        vec = vec && ((uintptr_t)p % 16 == 0);
+    }
+    if (err_dev && ((uintptr_t)err_dev % 4)) return LR_ERR_ALIGN;
+
+    const TileShape ts = tile_shape(OP_SCAN_FWD, dtype, vec);
+    const int64_t C = B * D;
+    const int64_t n_chunks = (T + ts.L - 1) / ts.L;
+    const int64_t n_ct = (C + ts.CW - 1) / ts.CW;
+    if (n_ct > INT32_MAX || n_chunks > INT32_MAX / n_ct) return LR_ERR_TOO_LARGE;
+    const size_t tiles = (size_t)(n_chunks * n_ct);
+    const size_t flag_bytes = round256(tiles * sizeof(uint32_t));
+    const size_t payload_bytes = tiles * (size_t)ts.CW * 3 * sizeof(float);
+    if (kHeaderBytes + flag_bytes + payload_bytes > kScratchBytes) return LR_ERR_TOO_LARGE;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LR_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    std::lock_guard<std::mutex> lock(g_na_mu);
+    NoAllocDev& nd = g_na[dev];
+    if (!nd.base) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return LR_ERR_CUDA;
+        nd.base = (unsigned char*)p;
+    }
+    uint32_t* words = (uint32_t*)nd.base;
+    uint32_t* flags = (uint32_t*)(nd.base + kHeaderBytes);
+    float* payload = (float*)(nd.base + kHeaderBytes + flag_bytes);
+    if (++nd.epoch > kEpochMax) {  // wrap: forget every old flag once
+        nd.epoch = 1;
+        if (cudaMemsetAsync(flags, 0, kScratchBytes - kHeaderBytes, s) != cudaSuccess)
+            return LR_ERR_CUDA;
+    }
+    if (cudaMemsetAsync(words, 0, sizeof(uint32_t), s) != cudaSuccess) return LR_ERR_CUDA;
+
+    Geom g;
+    g.T = T;
+    g.C = C;
+    g.D = D;
+    g.n_chunks = n_chunks;
+    g.n_ct = (int)n_ct;
+    g.n_launch = (uint32_t)tiles;
+    g.ticket_base = 0;
+    Lookback lb;
+    const size_t np = tiles * (size_t)ts.CW;
+    lb.flags = flags;
+    lb.agg_a = payload;
+    lb.agg_b = payload + np;
+    lb.inc = payload + 2 * np;
+    lb.ticket = words;
+    lb.err = err_dev ? err_dev : words + 1;
+    lb.epoch = nd.epoch;
+    lb.spin_limit = kSpinLimit;
+    if (launch_scan_fwd(dtype, vec, a, b, h0, h, g, lb, s) != cudaSuccess) return LR_ERR_CUDA;
+    return LR_OK;
+}
