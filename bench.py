@@ -174,7 +174,7 @@ class Bench:
             elif wl.kind == "sru":
                 L.sru_bwd(o["xt"], o["uf"], o["ur"], o["x"], o["bf"], o["br"], o["c"], o["dh"],
                           o["c0"], out=o["grad"])
-                launches += 2
+                launches += 3  # fused backward + two bias-reduction stages
             else:
                 _, k, _, _, st = L.deer_diag_solve(o["w"], o["u"], o["h0"], o["y"], eps=EPS, kmax=KMAX)
                 if st != L.LR_OK:

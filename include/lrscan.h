@@ -161,11 +161,13 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y,
  * engine or framework that owns every device byte (a hidden cudaMalloc can
  * fail at run time or fragment its pool) and latency-critical loops (the
  * cudaFree that grows lr_scan_fwd's cached workspace synchronises the device).
- * Its look-back scratch is one fixed 4 MiB __device__ array that every GPU
- * loading this library holds until the process exits.
- *   - Problems needing more scratch than that return LR_ERR_TOO_LARGE (the
- *     limit is ~2,700 tiles of 64 time steps x 128 fp32 channels, i.e.
- *     ~22 M fp32 elements; about half as many tiles for bf16).
+ * Its scratch (chunk-state packets, tile ticket) is one fixed 4 MiB
+ * __device__ array that every GPU loading this library holds until the
+ * process exits.
+ *   - Problems needing more scratch than that return LR_ERR_TOO_LARGE: the
+ *     array holds ~524 K channel-chunks (one chunk = 64 fp32 or 32 bf16 time
+ *     steps; a third of that when the sequence is long enough for the walker
+ *     protocol), e.g. B*D = 1024 channels up to T = 32 K fp32 steps.
  *   - All calls share the array: calls whose kernels overlap on the GPU race
  *     and give wrong results; order them on one stream or with events.
  *   - The first call on a device looks up the array's address; make it before

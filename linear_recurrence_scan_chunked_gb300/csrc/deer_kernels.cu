@@ -15,134 +15,144 @@
 // section "工程实现": ||y^(i+1) - y^(i)|| < eps, here the max-abs norm).
 // yold == nullptr is the all-zero initial guess (not read).
 #include "lr_launch.h"
+#include "lr_persist.cuh"
 
 namespace lrs {
 
-template <typename S, int VEC, int NW, int R>
-__global__ void __launch_bounds__(NW * 32, 2)
-    k_deer_iter(const float* __restrict__ w, const S* __restrict__ u, const S* __restrict__ h0,
-                const S* __restrict__ yold, S* __restrict__ ynew, uint32_t* __restrict__ resid,
-                Geom g, Lookback lb) {
-    constexpr int L = NW * R, CW = 32 * VEC;
-    __shared__ CarrySmem<VEC, NW> sm;
-    __shared__ uint32_t s_max[NW];
-    const uint32_t tile = take_ticket(lb, g);
-    const int64_t q = tile / g.n_ct;
-    const int j = tile % g.n_ct;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t ch = (int64_t)j * CW + lane * VEC;
-    const bool cok = ch < g.C;
-    const int64_t d = cok ? ch % g.D : 0;
-    const int64_t t0 = q * L + warp * R;
+template <typename S_, int VEC_, int NW_, int R_>
+struct DeerOp {
+    using S = S_;
+    static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
+    static constexpr bool REV = false;
+    static constexpr int IN_ARRAYS = 2;  // u, previous iterate
+    struct Params {
+        const float* w;
+        const S* u;
+        const S* h0;
+        const S* yold;
+        S* ynew;
+        uint32_t* resid;
+    };
+    struct Regs {
+        Pack<S, VEC> u[R];
+        Pack<S, VEC> yo[R + 1];  // previous iterate at rows t0-1 .. t0+R-1 (row -1 is h0)
+    };
+    struct Work {
+        float J[R][VEC], Rh[R][VEC];
+    };
+    struct Smem {
+        uint32_t mx[NW];
+    };
+    struct Acc {
+        uint32_t mx;  // max |y - yold| as bits: fp32 order of non-negative values, NaN on top
+    };
+    __device__ static void acc_init(Acc& a) { a.mx = 0; }
+    __device__ static const S* init_ptr(const Params& p) { return p.h0; }
 
-    float wv[VEC];
+    __device__ static void load(const Params& p, const Geom& g, const TileCoord& tc, Regs& rg) {
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) wv[v] = 0.f;
-    if (cok) load_param<VEC>(w + d, wv);
-
-    // previous iterate at rows t0-1 .. t0+R-1 (row -1 is h0)
-    Pack<S, VEC> yo[R + 1];
+        for (int i = 0; i <= R; ++i) {
+            const int64_t t = tc.t0 - 1 + i;
+            if (!tc.cok || t >= g.T) rg.yo[i].ident(0.f);
+            else if (t < 0) {
+                if (p.h0 != nullptr) rg.yo[i].load(p.h0 + tc.c);
+                else rg.yo[i].ident(0.f);
+            } else if (p.yold != nullptr) rg.yo[i].load(p.yold + t * g.C + tc.c);
+            else rg.yo[i].ident(0.f);
+        }
 #pragma unroll
-    for (int i = 0; i <= R; ++i) {
-        const int64_t t = t0 - 1 + i;
-        if (!cok || t >= g.T) yo[i].ident(0.f);
-        else if (t < 0) {
-            if (h0 != nullptr) yo[i].load(h0 + ch);
-            else yo[i].ident(0.f);
-        } else if (yold != nullptr) yo[i].load(yold + t * g.C + ch);
-        else yo[i].ident(0.f);
+        for (int r = 0; r < R; ++r) {
+            const int64_t t = tc.t0 + r;
+            if (tc.cok && t < g.T) rg.u[r].load(p.u + t * g.C + tc.c);
+            else rg.u[r].ident(0.f);
+        }
     }
-    float J[R][VEC], Rh[R][VEC];
+    __device__ static void aggregate(const Params& p, const Geom& g, const TileCoord& tc,
+                                     const Regs& rg, Work& w, float (&A)[VEC], float (&B)[VEC],
+                                     bool) {
+        float wv[VEC];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int64_t t = t0 + r;
-        if (cok && t < g.T) {
-            Pack<S, VEC> pu;
-            pu.load(u + t * g.C + ch);
+        for (int v = 0; v < VEC; ++v) wv[v] = 0.f;
+        if (tc.cok) load_param<VEC>(p.w + tc.c % g.D, wv);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { A[v] = 1.f; B[v] = 0.f; }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const bool ok = tc.cok && tc.t0 + r < g.T;
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
-                const float yt = yo[r].get(v);
-                const float th = tanhf(wv[v] * yt + pu.get(v));
+                const float yt = rg.yo[r].get(v);
+                const float th = tanhf(wv[v] * yt + rg.u[r].get(v));
                 const float jac = wv[v] * (1.f - th * th);
-                J[r][v] = jac;
-                Rh[r][v] = th - jac * yt;
-            }
-        } else {
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) { J[r][v] = 1.f; Rh[r][v] = 0.f; }
-        }
-    }
-    float A[VEC], Bs[VEC];
-#pragma unroll
-    for (int v = 0; v < VEC; ++v) { A[v] = 1.f; Bs[v] = 0.f; }
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            Bs[v] = J[r][v] * Bs[v] + Rh[r][v];
-            A[v] *= J[r][v];
-        }
-    float init[VEC];
-#pragma unroll
-    for (int v = 0; v < VEC; ++v) init[v] = 0.f;
-    if (q == 0 && warp == 0 && h0 != nullptr && cok) load_vec<S, VEC>(h0 + ch, init);
-
-    float s[VEC];
-    tile_carry<VEC, NW>(sm, A, Bs, init, s, lb, q, j, g.n_ct);
-
-    uint32_t mx = 0;  // max |y - yold| as bits: fp32 order of non-negative values, NaN on top
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int64_t t = t0 + r;
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) s[v] = J[r][v] * s[v] + Rh[r][v];
-        if (cok && t < g.T) {
-            store_vec<S, VEC>(ynew + t * g.C + ch, s);
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) {
-                // the stored (rounded) value is the iterate the next step reads
-                float yv = s[v];
-                if constexpr (sizeof(S) == 2) yv = bf_lo(bf_bits(yv));
-                const uint32_t bits = __float_as_uint(fabsf(yv - yo[r + 1].get(v)));
-                mx = bits > mx ? bits : mx;
+                w.J[r][v] = ok ? jac : 1.f;
+                w.Rh[r][v] = ok ? th - jac * yt : 0.f;
+                B[v] = w.J[r][v] * B[v] + w.Rh[r][v];
+                A[v] *= w.J[r][v];
             }
         }
     }
+    __device__ static void finish(const Params& p, const Geom& g, const TileCoord& tc,
+                                  const Regs& rg, Work& w, float (&s)[VEC], Smem&, Acc& acc) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const uint32_t o = __shfl_xor_sync(0xffffffffu, mx, off);
-        mx = o > mx ? o : mx;
-    }
-    if (lane == 0) s_max[warp] = mx;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        uint32_t m = 0;
+        for (int r = 0; r < R; ++r) {
+            const int64_t t = tc.t0 + r;
 #pragma unroll
-        for (int i = 0; i < NW; ++i) m = s_max[i] > m ? s_max[i] : m;
-        if (m) atomicMax(resid, m);
+            for (int v = 0; v < VEC; ++v) s[v] = w.J[r][v] * s[v] + w.Rh[r][v];
+            if (tc.cok && t < g.T) {
+                store_vec<S, VEC>(p.ynew + t * g.C + tc.c, s);
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    // the stored (rounded) value is the iterate the next step reads
+                    float yv = s[v];
+                    if constexpr (sizeof(S) == 2) yv = bf_lo(bf_bits(yv));
+                    const uint32_t bits = __float_as_uint(fabsf(yv - rg.yo[r + 1].get(v)));
+                    acc.mx = bits > acc.mx ? bits : acc.mx;
+                }
+            }
+        }
     }
-}
+    __device__ static void at_exit(const Params& p, Smem& xs, Acc& acc) {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        uint32_t mx = acc.mx;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const uint32_t o = __shfl_xor_sync(0xffffffffu, mx, off);
+            mx = o > mx ? o : mx;
+        }
+        if (lane == 0) xs.mx[warp] = mx;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int i = 0; i < NW; ++i) m = xs.mx[i] > m ? xs.mx[i] : m;
+            if (m) atomicMax(p.resid, m);
+        }
+    }
+};
 
 template <typename S, bool VP>
-static cudaError_t deer_t(const float* w, const void* u, const void* h0, const void* yold,
-                          void* ynew, uint32_t* resid, const Geom& g, const Lookback& lb,
-                          cudaStream_t s) {
-    constexpr int DT = sizeof(S) == 2 ? 1 : 0;
-    constexpr KCfg k = kcfg(OP_DEER, DT);
-    constexpr int VEC = kvec(DT, VP);
-    k_deer_iter<S, VEC, k.NW, k.R><<<g.n_launch, 32 * k.NW, 0, s>>>(
-        w, (const S*)u, (const S*)h0, (const S*)yold, (S*)ynew, resid, g, lb);
-    return cudaGetLastError();
-}
+using DeerOpT = DeerOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_DEER, sizeof(S) == 2).NW,
+                       kcfg(OP_DEER, sizeof(S) == 2).R>;
 
 cudaError_t launch_deer_iter(int dtype, bool vec, const float* w, const void* u, const void* h0,
                              const void* yold, void* ynew, uint32_t* resid, const Geom& g,
-                             const Lookback& lb, cudaStream_t s) {
-    if (dtype == 0)
-        return vec ? deer_t<float, true>(w, u, h0, yold, ynew, resid, g, lb, s)
-                   : deer_t<float, false>(w, u, h0, yold, ynew, resid, g, lb, s);
-    return vec ? deer_t<__nv_bfloat16, true>(w, u, h0, yold, ynew, resid, g, lb, s)
-               : deer_t<__nv_bfloat16, false>(w, u, h0, yold, ynew, resid, g, lb, s);
+                             const Carry& cr, cudaStream_t s) {
+    if (dtype == 0) {
+        const typename DeerOpT<float, true>::Params p{w, (const float*)u, (const float*)h0,
+                                                       (const float*)yold, (float*)ynew, resid};
+        return vec ? launch_persist<DeerOpT<float, true>>(p, g, cr, s)
+                   : launch_persist<DeerOpT<float, false>>(
+                         {w, (const float*)u, (const float*)h0, (const float*)yold, (float*)ynew,
+                          resid},
+                         g, cr, s);
+    }
+    using B16 = __nv_bfloat16;
+    return vec ? launch_persist<DeerOpT<B16, true>>(
+                     {w, (const B16*)u, (const B16*)h0, (const B16*)yold, (B16*)ynew, resid}, g,
+                     cr, s)
+               : launch_persist<DeerOpT<B16, false>>(
+                     {w, (const B16*)u, (const B16*)h0, (const B16*)yold, (B16*)ynew, resid}, g,
+                     cr, s);
 }
 
 }  // namespace lrs

@@ -15,7 +15,6 @@ namespace {
 
 using namespace lrs;
 
-constexpr uint32_t kEpochMax = (1u << 30) - 1;
 constexpr uint32_t kSpinLimit = 1u << 21;  // polls (backing off to ~1 us each): ~2 s
 constexpr int kMaxIters = 4096;            // DEER kmax bound (residual slots)
 
@@ -32,11 +31,10 @@ int cuda_fail(cudaError_t e) {
     } while (0)
 
 // Per-device workspace.  Everything the kernels need besides the caller's
-// buffers: look-back descriptors (flags + payload), the tile ticket, the
+// buffers: carry packets (chunk states and aggregates), the tile ticket, the
 // error word, DEER residual slots and second iterate, SRU bias partials.
 struct DevWS {
-    uint32_t* flags = nullptr;   size_t flags_cap = 0;    // entries
-    float* payload = nullptr;    size_t payload_cap = 0;  // floats
+    u64* pk = nullptr;           size_t pk_cap = 0;        // carry packets (state, aggregate)
     uint32_t* words = nullptr;   // [0] ticket, [1] error bits, [2..] DEER residual slots
     float* partials = nullptr;   size_t partials_cap = 0; // floats
     void* ybuf = nullptr;        size_t ybuf_cap = 0;     // bytes
@@ -99,36 +97,38 @@ int leave(DevWS& ws, cudaStream_t s) {
     return LR_OK;
 }
 
-// Geometry + descriptors for one launch of `op`.
+// Geometry + carry state for one launch of `op`.
 int plan(DevWS& ws, Op op, int dtype, bool vec, int64_t T, int64_t C, int64_t D, Geom* g,
-         Lookback* lb, cudaStream_t s) {
+         Carry* cr, cudaStream_t s) {
     const TileShape ts = tile_shape(op, dtype, vec);
     g->T = T;
     g->C = C;
     g->D = D;
     g->n_chunks = (T + ts.L - 1) / ts.L;
     g->n_ct = (int)((C + ts.CW - 1) / ts.CW);
+    if ((C + ts.CW - 1) / ts.CW > INT32_MAX) return LR_ERR_TOO_LARGE;
     const int64_t tiles = g->n_chunks * (int64_t)g->n_ct;
-    if ((C + ts.CW - 1) / ts.CW > INT32_MAX || tiles > INT32_MAX) return LR_ERR_TOO_LARGE;
-    g->n_launch = (uint32_t)tiles;
+    const CarryPlan cp = carry_plan(op, dtype, g->n_chunks, C);
+    if (tiles + cp.n_walk > INT32_MAX / 2) return LR_ERR_TOO_LARGE;
+    g->n_tiles = (uint32_t)tiles;
+    g->n_draws = 0;  // set by the launcher from the grid it picks
     g->ticket_base = 0;
-    int st = grow(ws, &ws.flags, &ws.flags_cap, (size_t)tiles, true);
+    g->max_grid = 0;
+    int st = grow(ws, &ws.pk, &ws.pk_cap, cp.inc_elems + cp.agg_elems, true);
     if (st) return st;
-    st = grow(ws, &ws.payload, &ws.payload_cap, (size_t)tiles * ts.CW * 3, false);
-    if (st) return st;
-    if (++ws.epoch > kEpochMax) {  // wrap: clear every flag once
+    if (++ws.epoch == 0) {  // 32-bit wrap: forget every packet once
         ws.epoch = 1;
-        CK(cudaMemsetAsync(ws.flags, 0, ws.flags_cap * sizeof(uint32_t), s));
+        CK(cudaMemsetAsync(ws.pk, 0, ws.pk_cap * sizeof(u64), s));
     }
-    const size_t np = (size_t)tiles * ts.CW;
-    lb->flags = ws.flags;
-    lb->agg_a = ws.payload;
-    lb->agg_b = ws.payload + np;
-    lb->inc = ws.payload + 2 * np;
-    lb->ticket = ws.words;
-    lb->err = ws.words + 1;
-    lb->epoch = ws.epoch;
-    lb->spin_limit = kSpinLimit;
+    cr->inc = ws.pk;
+    cr->agg = ws.pk + cp.inc_elems;
+    cr->ticket = ws.words;
+    cr->err = ws.words + 1;
+    cr->epoch = ws.epoch;
+    cr->spin_limit = kSpinLimit;
+    cr->mode = cp.mode;
+    cr->n_walk = cp.n_walk;
+    cr->wv = cp.wv;
     return LR_OK;
 }
 
@@ -195,10 +195,10 @@ int lr_scan_fwd(const void* a, const void* b, const void* h0, void* h, int64_t B
     DevWS* ws;
     TRY(get_ws(&ws));
     Geom g;
-    Lookback lb;
+    Carry cr;
     TRY(enter(*ws, s));
-    TRY(plan(*ws, OP_SCAN_FWD, dtype, vec, T, B * D, D, &g, &lb, s));
-    CK(launch_scan_fwd(dtype, vec, a, b, h0, h, g, lb, s));
+    TRY(plan(*ws, OP_SCAN_FWD, dtype, vec, T, B * D, D, &g, &cr, s));
+    CK(launch_scan_fwd(dtype, vec, a, b, h0, h, g, cr, s));
     return leave(*ws, s);
 }
 
@@ -219,10 +219,10 @@ int lr_scan_bwd(const void* a, const void* h, const void* h0, const void* dh, vo
     DevWS* ws;
     TRY(get_ws(&ws));
     Geom g;
-    Lookback lb;
+    Carry cr;
     TRY(enter(*ws, s));
-    TRY(plan(*ws, OP_SCAN_BWD, dtype, vec, T, B * D, D, &g, &lb, s));
-    CK(launch_scan_bwd(dtype, vec, a, h, h0, dh, da, db, dh0, g, lb, s));
+    TRY(plan(*ws, OP_SCAN_BWD, dtype, vec, T, B * D, D, &g, &cr, s));
+    CK(launch_scan_bwd(dtype, vec, a, h, h0, dh, da, db, dh0, g, cr, s));
     return leave(*ws, s);
 }
 
@@ -238,10 +238,10 @@ int sru_fwd(const void* xt, const void* uf, const void* ur, const void* x, const
     DevWS* ws;
     TRY(get_ws(&ws));
     Geom g;
-    Lookback lb;
+    Carry cr;
     TRY(enter(*ws, s));
-    TRY(plan(*ws, OP_SRU_FWD, dtype, vec, T, B * D, D, &g, &lb, s));
-    CK(launch_sru_fwd(dtype, vec, xt, uf, ur, x, bf, br, c0, h, c, g, lb, s));
+    TRY(plan(*ws, OP_SRU_FWD, dtype, vec, T, B * D, D, &g, &cr, s));
+    CK(launch_sru_fwd(dtype, vec, xt, uf, ur, x, bf, br, c0, h, c, g, cr, s));
     return leave(*ws, s);
 }
 
@@ -267,12 +267,12 @@ int sru_bwd(const void* xt, const void* uf, const void* ur, const void* x, const
     DevWS* ws;
     TRY(get_ws(&ws));
     Geom g;
-    Lookback lb;
+    Carry cr;
     TRY(enter(*ws, s));
-    TRY(plan(*ws, OP_SRU_BWD, dtype, vec, T, B * D, D, &g, &lb, s));
-    TRY(grow(*ws, &ws->partials, &ws->partials_cap, (size_t)(2 * g.n_chunks * g.C), false));
+    TRY(plan(*ws, OP_SRU_BWD, dtype, vec, T, B * D, D, &g, &cr, s));
+    TRY(grow(*ws, &ws->partials, &ws->partials_cap, (size_t)(2 * g.n_chunks * g.C + 2 * g.C), false));
     CK(launch_sru_bwd(dtype, vec, xt, uf, ur, x, bf, br, c0, c, dh, dxt, duf, dur, dx, dc0,
-                      ws->partials, g, lb, s));
+                      ws->partials, g, cr, s));
     CK(launch_bias_reduce(ws->partials, g.n_chunks, B, D, dbf, dbr, s));
     return leave(*ws, s);
 }
@@ -310,10 +310,10 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y, int6
     float rho = 0.f;
     for (k = 1; k <= kmax; ++k) {
         Geom g;
-        Lookback lb;
-        TRY(plan(*ws, OP_DEER, dtype, vec, T, B * D, D, &g, &lb, s));
+        Carry cr;
+        TRY(plan(*ws, OP_DEER, dtype, vec, T, B * D, D, &g, &cr, s));
         CK(launch_deer_iter(dtype, vec, w, u, h0, k == 1 ? nullptr : buf[(k - 1) & 1], buf[k & 1],
-                            slots + (k - 1), g, lb, s));
+                            slots + (k - 1), g, cr, s));
         CK(cudaMemcpyAsync(ws->host_word, slots + (k - 1), sizeof(uint32_t),
                            cudaMemcpyDeviceToHost, s));
         CK(cudaStreamSynchronize(s));
@@ -381,14 +381,17 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
     }
     float* a = (float*)ws->test_buf;
     Geom g;
-    Lookback lb;
+    Carry cr;
     TRY(enter(*ws, s));
-    TRY(plan(*ws, OP_SCAN_FWD, LR_F32, true, T, C, C, &g, &lb, s));
-    // One CTA, handed tile 1: it waits for tile 0, which nobody publishes.
-    g.n_launch = 1;
+    TRY(plan(*ws, OP_SCAN_FWD, LR_F32, true, T, C, C, &g, &cr, s));
+    // One CTA, handed tile 1: it waits for the state after tile 0, which
+    // nobody publishes.
+    g.max_grid = 1;
     g.ticket_base = 1;
-    lb.spin_limit = spin_limit;
-    CK(launch_scan_fwd(LR_F32, true, a, a + T * C, nullptr, a + 2 * T * C, g, lb, s));
+    cr.mode = CARRY_CHAIN;
+    cr.n_walk = 0;
+    cr.spin_limit = spin_limit;
+    CK(launch_scan_fwd(LR_F32, true, a, a + T * C, nullptr, a + 2 * T * C, g, cr, s));
     return leave(*ws, s);
 }
 

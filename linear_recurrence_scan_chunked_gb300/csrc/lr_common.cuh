@@ -1,7 +1,6 @@
 // lr_common.cuh -- device machinery shared by every chunked-scan kernel:
 // storage packs (fp32 / bf16, 16-byte vectors), the tile ticket, and the
-// single-pass decoupled look-back that carries the recurrence state across
-// time chunks.
+// single-pass carry of the recurrence state across time chunks.
 //
 // The scan is the one of page [P1] "CUDA并行化RNN训练：从O(T)到O(log T)的工程实践与
 // 参数调优" (parallel-scan paragraph: an associative operation evaluated by
@@ -17,16 +16,30 @@
 //     owns channels [l*VEC, l*VEC+VEC) of the tile (one 16-byte vector per row,
 //     so one warp row is a 512-byte coalesced segment), warp w owns the R
 //     consecutive rows [w*R, w*R+R) in scan order;
-//   * each thread scans its R rows sequentially in registers (depth R), the
-//     NW warp aggregates are combined through shared memory (depth NW), and the
-//     tiles along time are chained by decoupled look-back over a window of 32
-//     predecessors at a time (depth ~ number of tiles / 32 in the worst case,
-//     one step in the common case), so a million-step sequence is one launch;
-//   * tiles are handed out by an atomic ticket in scan order, so every tile a
-//     CTA waits for belongs to a CTA that is already running: the wait always
-//     ends.  Every wait is still bounded (spin_limit polls); when it runs out
-//     the tile records LR_ERR_TIMEOUT in the error word, publishes NaN and
-//     finishes, so its successors do not wait in turn.
+//   * each thread scans its R rows sequentially in registers (depth R), the NW
+//     warp aggregates are combined through shared memory (depth NW), and the
+//     carry between time chunks comes from one of two single-pass protocols:
+//       CHAIN -- tile q waits for the state after chunk q-1 and publishes the
+//                state after chunk q.  One L2 round trip per chunk level: best
+//                when there are many channel tiles and few chunks, because the
+//                tiles of one chunk level stream while the chain advances;
+//       WALK  -- tile q publishes its aggregate (A, B) and waits for the state
+//                after chunk q-1, which dedicated walker CTAs compute: a warp
+//                owns a few channels, its lanes own 32 consecutive chunks, and a
+//                Kogge-Stone prefix over the 32 aggregates plus the carried
+//                block state gives 32 states at once.  Best for long sequences
+//                with few channels (the chain would cost one round trip per
+//                chunk; here it costs one per 32 chunks, overlapped).
+//     Both fix the association of every floating-point operation by position
+//     alone, so results are bitwise reproducible run to run.
+//   * every published value is a self-validating 64-bit packet (value << 32 |
+//     epoch): no memory fence sits on the critical path, and packets left by
+//     earlier launches (older epochs) are simply not accepted;
+//   * tiles (and walkers, which take the first tickets) are handed out by an
+//     atomic ticket, so every producer a CTA waits for is already running: the
+//     wait always ends.  Every wait is still bounded (spin_limit polls); when
+//     it runs out the CTA records LR_ERR_TIMEOUT and publishes NaN, so nothing
+//     downstream waits in turn.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -35,23 +48,28 @@
 
 namespace lrs {
 
-constexpr uint32_t ST_X = 0;    // nothing published (or an older launch's flag)
-constexpr uint32_t ST_AGG = 1;  // tile aggregate (A, B) published
-constexpr uint32_t ST_INC = 2;  // inclusive state at the tile's last row published
 constexpr uint32_t ERRBIT_TIMEOUT = 1u;
+constexpr int CARRY_CHAIN = 0;
+constexpr int CARRY_WALK = 1;
+constexpr int WALK_MAX_WV = 4;  // channels per walker warp (upper bound)
+constexpr int WALK_P = 4;       // consecutive chunks per walker lane
 
-// Look-back descriptors: one flag word and 3*CW floats per tile.  A flag is
-// (epoch << 2) | state; a flag whose epoch differs from this launch's is read
-// as ST_X, so the descriptors never need clearing between launches.
-struct Lookback {
-    uint32_t* flags;     // [n_tiles]
-    float* agg_a;        // [n_tiles * CW]  product of a over the tile
-    float* agg_b;        // [n_tiles * CW]  state after the tile from zero
-    float* inc;          // [n_tiles * CW]  state after the tile (true carry)
-    uint32_t* ticket;    // tile ticket counter (0 between launches)
-    uint32_t* err;       // sticky error bits
-    uint32_t epoch;      // 1 .. 2^30-1
-    uint32_t spin_limit; // polls before a wait gives up
+typedef unsigned long long u64;
+
+// Carry-protocol state of one launch.
+struct Carry {
+    u64* agg;             // WALK: [C][n_chunks][2] packets (A, B) of every tile
+    u64* inc;             // packets: state after chunk q (scan order); CHAIN stores
+                          // them chunk-major [n_chunks][C] (a tile reads one row),
+                          // WALK channel-major [C][n_chunks] (a walker warp reads
+                          // and writes 32 consecutive chunks of one channel)
+    uint32_t* ticket;     // ticket counter (0 between launches)
+    uint32_t* err;        // sticky error bits
+    uint32_t epoch;       // 1 .. 2^32-1, one per launch
+    uint32_t spin_limit;  // polls before a wait gives up
+    int mode;             // CARRY_CHAIN or CARRY_WALK
+    uint32_t n_walk;      // walker CTAs (first tickets); 0 in CHAIN mode
+    int wv;               // channels per walker warp (WALK)
 };
 
 struct Geom {
@@ -60,8 +78,10 @@ struct Geom {
     int64_t D;            // features (per-feature parameters use c % D)
     int64_t n_chunks;     // ceil(T / L)
     int n_ct;             // ceil(C / CW)
-    uint32_t n_launch;    // CTAs launched (= tiles; the timeout test launches fewer)
-    uint32_t ticket_base; // first ticket value mapped to tile 0 + ticket_base
+    uint32_t n_tiles;     // n_chunks * n_ct
+    uint32_t n_draws;     // tickets drawn by the whole launch (the last drawer resets)
+    uint32_t ticket_base; // added to every ticket (the timeout test starts past tile 0)
+    uint32_t max_grid;    // 0, or an upper bound on the CTAs launched (timeout test)
 };
 
 // ------------------------------------------------------------- memory ops
@@ -198,122 +218,262 @@ __device__ __forceinline__ void load_param(const float* p, float (&x)[VEC]) {
     }
 }
 
-// Descriptor payload: VEC floats per lane, L2 only (.cg) so no stale L1 line
-// from an earlier launch is ever read.
+// ------------------------------------------------------------------ packets
+
+__device__ __forceinline__ u64 pkt(float v, uint32_t e) {
+    return ((u64)__float_as_uint(v) << 32) | e;
+}
+__device__ __forceinline__ float pkt_val(u64 p) { return __uint_as_float((uint32_t)(p >> 32)); }
+__device__ __forceinline__ bool pkt_ok(u64 p, uint32_t e) { return (uint32_t)p == e; }
+
+__device__ __forceinline__ void ld_pkt2(const u64* p, u64& a, u64& b) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ u64 ld_pkt(const u64* p) {
+    u64 a;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(a) : "l"(p) : "memory");
+    return a;
+}
+__device__ __forceinline__ void st_pkt2(u64* p, u64 a, u64 b) {
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1,%2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ void st_pkt(u64* p, u64 a) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(a) : "memory");
+}
+
+// L2-only (.cg) packet accesses for the walker's hot loop: coalesced across
+// the warp, never served from a stale L1 line; an aligned 8-byte access is
+// never torn, and a packet is only accepted when its epoch matches.
+__device__ __forceinline__ void ld_pkt2_cg(const u64* p, u64& a, u64& b) {
+    asm volatile("ld.global.cg.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ void st_pkt_cg(u64* p, u64 a) {
+    asm volatile("st.global.cg.u64 [%0], %1;" ::"l"(p), "l"(a) : "memory");
+}
+
+// VEC state packets of one lane (16-byte aligned when VEC is even).
 template <int VEC>
-__device__ __forceinline__ void put_payload(float* p, const float (&x)[VEC]) {
-    if constexpr (VEC % 4 == 0) {
+__device__ __forceinline__ void put_states(u64* p, const float (&x)[VEC], uint32_t e) {
+    if constexpr (VEC % 2 == 0) {
 #pragma unroll
-        for (int i = 0; i < VEC; i += 4)
-            __stcg(reinterpret_cast<float4*>(p + i), make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]));
+        for (int i = 0; i < VEC; i += 2) st_pkt2(p + i, pkt(x[i], e), pkt(x[i + 1], e));
     } else {
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) __stcg(p + i, x[i]);
+        for (int i = 0; i < VEC; ++i) st_pkt(p + i, pkt(x[i], e));
     }
 }
 template <int VEC>
-__device__ __forceinline__ void get_payload(const float* p, float (&x)[VEC]) {
-    if constexpr (VEC % 4 == 0) {
+__device__ __forceinline__ bool get_states(const u64* p, float (&x)[VEC], uint32_t e) {
+    bool ok = true;
+    if constexpr (VEC % 2 == 0) {
 #pragma unroll
-        for (int i = 0; i < VEC; i += 4) {
-            float4 f = __ldcg(reinterpret_cast<const float4*>(p + i));
-            x[i] = f.x; x[i + 1] = f.y; x[i + 2] = f.z; x[i + 3] = f.w;
+        for (int i = 0; i < VEC; i += 2) {
+            u64 a, b;
+            ld_pkt2(p + i, a, b);
+            ok = ok && pkt_ok(a, e) && pkt_ok(b, e);
+            x[i] = pkt_val(a);
+            x[i + 1] = pkt_val(b);
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) x[i] = __ldcg(p + i);
+        for (int i = 0; i < VEC; ++i) {
+            const u64 a = ld_pkt(p + i);
+            ok = ok && pkt_ok(a, e);
+            x[i] = pkt_val(a);
+        }
     }
+    return ok;
 }
 
-// ------------------------------------------------------------ the ticket
-
-// Returns this CTA's tile number (in scan order).  The CTA that draws the last
-// ticket of the launch resets the counter for the next launch on the stream.
-__device__ __forceinline__ uint32_t take_ticket(const Lookback& lb, const Geom& g) {
-    __shared__ uint32_t s_ticket;
-    if (threadIdx.x == 0) {
-        uint32_t t = atomicAdd(lb.ticket, 1u);
-        if (t == g.n_launch - 1) atomicExch(lb.ticket, 0u);
-        s_ticket = t + g.ticket_base;
-    }
-    __syncthreads();
-    return s_ticket;
-}
-
-// ---------------------------------------------------------- publication
-
-// Whole warp: write this lane's payload, then lane 0 raises the flag.
+// VEC state packets of one lane stored `stride` packets apart (channel-major).
 template <int VEC>
-__device__ __forceinline__ void publish(float* payload, const float (&x)[VEC], uint32_t* flag,
-                                        uint32_t word) {
-    put_payload<VEC>(payload, x);
-    __threadfence();
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) st_release_u32(flag, word);
+__device__ __forceinline__ bool get_states_strided(const u64* p, int64_t stride, float (&x)[VEC],
+                                                   uint32_t e) {
+    bool ok = true;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+        const u64 a = ld_pkt(p + i * stride);
+        ok = ok && pkt_ok(a, e);
+        x[i] = pkt_val(a);
+    }
+    return ok;
 }
 
-// Whole warp: the carry entering scan-order chunk q (q >= 1) for channel tile
-// j, i.e. the state after chunk q-1.  Walks back over windows of 32
-// predecessors (lane i watches chunk base-i) until the nearest chunk p whose
-// inclusive state is visible, with every chunk between p and q-1 showing its
-// aggregate.  The carry is then rebuilt by folding forward, oldest first:
-//     h = INC(p);  h = A(i) h + B(i)  for i = p+1 .. q-1,
-// which is exactly the fused multiply-add each of those chunks performs when
-// it publishes its own inclusive state.  The result is therefore bitwise the
-// same whichever p the race happened to expose: the scan is deterministic.
-// Returns false (carry = NaN, error bit set) when the wait ran out.
-template <int VEC, int CW>
-__device__ bool lookback(const Lookback& lb, int64_t q, int j, int n_ct, float (&cin)[VEC]) {
-    const int lane = threadIdx.x & 31;
-    int64_t base = q - 1;
-    int64_t first = -1;  // nearest chunk with a visible inclusive state
-    uint32_t spins = 0;
-    uint32_t sleep_ns = 0;
-    while (first < 0) {
-        const int64_t pred = base - lane;
-        uint32_t st = ST_X;
-        if (pred >= 0) {
-            const uint32_t f = ld_acquire_u32(lb.flags + pred * n_ct + j);
-            if ((f >> 2) == lb.epoch) st = f & 3u;
-        }
-        const unsigned inc = __ballot_sync(0xffffffffu, pred >= 0 && st == ST_INC);
-        const unsigned ok = __ballot_sync(0xffffffffu, pred < 0 || st != ST_X);
-        if (inc) {
-            const int p = __ffs(inc) - 1;
-            const unsigned need = p == 31 ? 0xffffffffu : ((2u << p) - 1u);
-            if ((ok & need) == need) { first = base - p; break; }
-        } else if (ok == 0xffffffffu) {
-            base -= 32;  // 32 aggregates, no inclusive state yet: look further back
-            continue;
-        }
-        ++spins;
-        bool give_up = spins > lb.spin_limit;
-        if ((spins & 63u) == 0 && (ld_relaxed_u32(lb.err) & ERRBIT_TIMEOUT)) give_up = true;
-        if (__any_sync(0xffffffffu, give_up)) {
-            if (lane == 0) atomicOr(lb.err, ERRBIT_TIMEOUT);
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) cin[v] = __int_as_float(0x7fc00000);
-            return false;
-        }
-        if (sleep_ns) __nanosleep(sleep_ns);
-        sleep_ns = sleep_ns == 0 ? 32 : (sleep_ns < 1024 ? sleep_ns * 2 : 1024);
+// Bounded wait helper: returns true when the caller should give up.  Sleeps
+// grow to max_sleep_ns between polls (0: pure spin -- the walker, which is on
+// every tile's critical path, must notice new aggregates at once).
+__device__ __forceinline__ bool wait_step(const Carry& cr, uint32_t& spins, uint32_t& sleep_ns,
+                                          uint32_t max_sleep_ns) {
+    ++spins;
+    if (spins > cr.spin_limit) return true;
+    if ((spins & 63u) == 0) {
+        uint32_t e;
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(e) : "l"(cr.err) : "memory");
+        if (e & ERRBIT_TIMEOUT) return true;
     }
-    __syncwarp();
-    float h[VEC];
-    get_payload<VEC>(lb.inc + (first * n_ct + j) * CW + lane * VEC, h);
-#pragma unroll 4
-    for (int64_t i = first + 1; i < q; ++i) {
-        const int64_t tile = i * n_ct + j;
-        float pa[VEC], pb[VEC];
-        get_payload<VEC>(lb.agg_a + tile * CW + lane * VEC, pa);
-        get_payload<VEC>(lb.agg_b + tile * CW + lane * VEC, pb);
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) h[v] = __fmaf_rn(pa[v], h[v], pb[v]);
-    }
-#pragma unroll
-    for (int v = 0; v < VEC; ++v) cin[v] = h[v];
-    return true;
+    if (sleep_ns) __nanosleep(sleep_ns);
+    sleep_ns = sleep_ns == 0 ? (max_sleep_ns ? 16 : 0)
+                             : (sleep_ns * 2 < max_sleep_ns ? sleep_ns * 2 : max_sleep_ns);
+    return false;
 }
+constexpr uint32_t kTileMaxSleepNs = 64;
+
+// ------------------------------------------------------------- the walker
+
+// One walker CTA (NW warps).  Warp gw = wid*NW + warp owns channels
+// [gw*wv, gw*wv + wv).  It sweeps the chunks in windows of 32*WALK_P: lane l
+// owns the WALK_P consecutive chunks w0 + l*WALK_P + k.  With every
+// aggregate of a window loaded in one round trip, it forms each lane's left
+// fold over its chunks, an inclusive Kogge-Stone prefix of those folds across
+// the lanes, and then, lane by lane, the chunk states
+//     state(q) = a_q * state(q-1) + b_q   from the lane's entering state
+// s_l = E_l.A * s_in + E_l.B (E_l: exclusive prefix, s_in: state after the
+// previous window).  The association of every operation depends on the chunk
+// index only, so the states are bitwise reproducible.  States are published
+// as soon as the aggregates before them are visible -- a lane whose later
+// chunks are not visible yet still publishes its leading ones -- so no tile
+// ever waits for a tile with a larger ticket.
+template <typename S, int NW>
+__device__ void walker(const Carry& cr, const Geom& g, uint32_t wid, const S* __restrict__ init) {
+    constexpr int P = WALK_P, MV = WALK_MAX_WV;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t c0 = ((int64_t)wid * NW + warp) * cr.wv;
+    const int64_t last = g.n_chunks - 1;  // states are needed for chunks 0 .. last-1
+    if (c0 >= g.C || last <= 0) return;
+    const int wv = cr.wv;
+    bool chan[MV];
+#pragma unroll
+    for (int v = 0; v < MV; ++v) chan[v] = v < wv && c0 + v < g.C;
+    float s_in[MV];
+#pragma unroll
+    for (int v = 0; v < MV; ++v) {
+        s_in[v] = 0.f;
+        if (chan[v] && init != nullptr) {
+            Pack<S, 1> pk;
+            pk.load(init + c0 + v);
+            s_in[v] = pk.get(0);
+        }
+    }
+    const u64* agg = cr.agg;
+    uint32_t spins = 0, sleep_ns = 0;
+    bool dead = false;  // a wait ran out: every remaining state is published as NaN
+    for (int64_t w0 = 0; w0 < last; w0 += 32 * P) {
+        const int n_win = (int)((last - w0) < 32 * P ? (last - w0) : 32 * P);  // chunks here
+        const int64_t q0 = w0 + (int64_t)lane * P;  // this lane's first chunk
+        u64 pk[P][MV][2];
+        bool okk[P];
+#pragma unroll
+        for (int k = 0; k < P; ++k) {
+            okk[k] = false;
+#pragma unroll
+            for (int v = 0; v < MV; ++v) {
+                pk[k][v][0] = pk[k][v][1] = 0;
+                if (chan[v] && lane * P + k < n_win)
+                    ld_pkt2_cg(agg + 2 * ((c0 + v) * g.n_chunks + q0 + k), pk[k][v][0], pk[k][v][1]);
+            }
+        }
+        int pub = 0;  // chunks of this window already published (a prefix)
+        while (true) {
+            // vp: leading chunks of this lane whose aggregates are visible (chunks
+            // past the end of the problem count as visible)
+            int vp = 0;
+            bool run = true;
+#pragma unroll
+            for (int k = 0; k < P; ++k) {
+                bool ok = okk[k] || lane * P + k >= n_win;
+                if (!ok) {
+                    ok = true;
+#pragma unroll
+                    for (int v = 0; v < MV; ++v)
+                        if (chan[v]) ok = ok && pkt_ok(pk[k][v][0], cr.epoch) && pkt_ok(pk[k][v][1], cr.epoch);
+                    okk[k] = ok;
+                }
+                run = run && ok;
+                vp += run ? 1 : 0;
+            }
+            const unsigned notfull = ~__ballot_sync(0xffffffffu, vp == P);
+            const int npre = notfull ? __ffs(notfull) - 1 : 32;  // leading complete lanes
+            const int vp_part = __shfl_sync(0xffffffffu, vp, npre < 32 ? npre : 31);
+            int limit = npre * P + (npre < 32 ? vp_part : 0);
+            if (limit > n_win) limit = n_win;
+            if (dead) limit = n_win;
+            float s_end[MV];
+            if (limit > pub) {
+                float A[MV], B[MV];
+#pragma unroll
+                for (int v = 0; v < MV; ++v) { A[v] = 1.f; B[v] = 0.f; }
+                if (lane < npre) {  // left fold over this lane's chunks
+#pragma unroll
+                    for (int k = 0; k < P; ++k)
+#pragma unroll
+                        for (int v = 0; v < MV; ++v)
+                            if (chan[v] && lane * P + k < n_win) {
+                                const float a = pkt_val(pk[k][v][0]);
+                                B[v] = __fmaf_rn(a, B[v], pkt_val(pk[k][v][1]));
+                                A[v] *= a;
+                            }
+                }
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+#pragma unroll
+                    for (int v = 0; v < MV; ++v) {
+                        if (v >= wv) continue;
+                        const float pa = __shfl_up_sync(0xffffffffu, A[v], off);
+                        const float pb = __shfl_up_sync(0xffffffffu, B[v], off);
+                        if (lane >= off) {
+                            B[v] = __fmaf_rn(A[v], pb, B[v]);
+                            A[v] = pa * A[v];
+                        }
+                    }
+                }
+                float st[MV];
+#pragma unroll
+                for (int v = 0; v < MV; ++v) {  // exclusive prefix -> entering state
+                    const float ea = __shfl_up_sync(0xffffffffu, A[v], 1);
+                    const float eb = __shfl_up_sync(0xffffffffu, B[v], 1);
+                    st[v] = lane == 0 ? s_in[v] : __fmaf_rn(ea, s_in[v], eb);
+                }
+#pragma unroll
+                for (int k = 0; k < P; ++k) {
+                    const int rel = lane * P + k;
+#pragma unroll
+                    for (int v = 0; v < MV; ++v) {
+                        if (!chan[v]) continue;
+                        if (rel < limit)
+                            st[v] = dead ? __int_as_float(0x7fc00000)
+                                         : __fmaf_rn(pkt_val(pk[k][v][0]), st[v], pkt_val(pk[k][v][1]));
+                        if (rel >= pub && rel < limit)
+                            st_pkt_cg(cr.inc + (c0 + v) * g.n_chunks + q0 + k, pkt(st[v], cr.epoch));
+                    }
+                }
+#pragma unroll
+                for (int v = 0; v < MV; ++v) s_end[v] = st[v];
+                pub = limit;
+            }
+            if (pub == n_win) {  // state after the window's last chunk -> next window
+                const int owner = (n_win - 1) / P;
+#pragma unroll
+                for (int v = 0; v < MV; ++v) s_in[v] = __shfl_sync(0xffffffffu, s_end[v], owner);
+                break;
+            }
+            if (__any_sync(0xffffffffu, wait_step(cr, spins, sleep_ns, 0))) {
+                if (lane == 0) atomicOr(cr.err, ERRBIT_TIMEOUT);
+                dead = true;  // publish NaN for the rest so no tile keeps waiting
+                continue;
+            }
+#pragma unroll
+            for (int k = 0; k < P; ++k)  // re-poll what was not visible
+#pragma unroll
+                for (int v = 0; v < MV; ++v)
+                    if (chan[v] && !okk[k] && lane * P + k < n_win)
+                        ld_pkt2_cg(agg + 2 * ((c0 + v) * g.n_chunks + q0 + k), pk[k][v][0], pk[k][v][1]);
+        }
+        spins = 0;
+        sleep_ns = 0;
+    }
+}
+
+// -------------------------------------------------------------- the tile
 
 // Shared memory for combining the NW warp aggregates of a tile.
 template <int VEC, int NW>
@@ -324,14 +484,15 @@ struct CarrySmem {
 };
 
 // Whole CTA.  (A, B): this thread's aggregate over its R rows (scan order).
-// init: state before the whole scan (used by warp 0 when q == 0).
-// Returns in `start` the state entering this thread's first row.
+// init: state before the whole scan (used by warp 0 when q == 0).  c: first
+// channel of this lane, cok: it is inside the problem.  Returns in `start` the
+// state entering this thread's first row.
 template <int VEC, int NW>
 __device__ __forceinline__ void tile_carry(CarrySmem<VEC, NW>& sm, const float (&A)[VEC],
                                            const float (&B)[VEC], const float (&init)[VEC],
-                                           float (&start)[VEC], const Lookback& lb, int64_t q,
-                                           int j, int n_ct) {
-    constexpr int CW = 32 * VEC;
+                                           float (&start)[VEC], const Carry& cr, const Geom& g,
+                                           int64_t q, int64_t c, bool cok,
+                                           bool publish_agg = true) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
     for (int v = 0; v < VEC; ++v) {
@@ -348,24 +509,62 @@ __device__ __forceinline__ void tile_carry(CarrySmem<VEC, NW>& sm, const float (
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
                 const float a = sm.a[w][lane][v], b = sm.b[w][lane][v];
-                TB[v] = a * TB[v] + b;
+                TB[v] = __fmaf_rn(a, TB[v], b);
                 TA[v] *= a;
             }
-        const int64_t tile = q * n_ct + j;
+        constexpr int CW = 32 * VEC;
         float cin[VEC];
-        if (q == 0) {
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) cin[v] = init[v];
-        } else {
-            put_payload<VEC>(lb.agg_a + tile * CW + lane * VEC, TA);
-            publish<VEC>(lb.agg_b + tile * CW + lane * VEC, TB, lb.flags + tile,
-                         (lb.epoch << 2) | ST_AGG);
-            lookback<VEC, CW>(lb, q, j, n_ct, cin);
+        for (int v = 0; v < VEC; ++v) cin[v] = 0.f;
+        const bool more = q < g.n_chunks - 1;  // a later chunk needs this one's state
+        const int64_t base = q * g.C + c;
+        const bool walk = cr.mode == CARRY_WALK;
+        if (cok && walk && more && publish_agg) {
+#pragma unroll
+            for (int v = 0; v < VEC; ++v)
+                st_pkt2(cr.agg + 2 * ((c + v) * g.n_chunks + q), pkt(TA[v], cr.epoch),
+                        pkt(TB[v], cr.epoch));
         }
-        float hend[VEC];
+        if (q == 0) {
+            if (cok) {
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) hend[v] = __fmaf_rn(TA[v], cin[v], TB[v]);
-        publish<VEC>(lb.inc + tile * CW + lane * VEC, hend, lb.flags + tile, (lb.epoch << 2) | ST_INC);
+                for (int v = 0; v < VEC; ++v) cin[v] = init[v];
+            }
+        } else {
+            // Lane 0 polls one packet, the state of one channel of the tile; once it
+            // is there every lane reads its own.  One 8-byte poll per tile keeps the
+            // L2 free for the data, and the polled channel rotates with the chunk
+            // so that neighbouring tiles never poll the same cache line.
+            const int64_t c_first = c - lane * VEC;
+            int64_t n_tile_ch = g.C - c_first;
+            if (n_tile_ch > CW) n_tile_ch = CW;
+            const int64_t c_rep = c_first + (int64_t)((q * 37) % n_tile_ch);
+            const u64* rep = walk ? cr.inc + c_rep * g.n_chunks + q - 1 : cr.inc + (q - 1) * g.C + c_rep;
+            uint32_t spins = 0, sleep_ns = 0;
+            while (true) {
+                bool rep_ok = false;
+                if (lane == 0) rep_ok = pkt_ok(ld_pkt(rep), cr.epoch);
+                if (__shfl_sync(0xffffffffu, rep_ok, 0)) {
+                    const bool ok =
+                        !cok || (walk ? get_states_strided<VEC>(cr.inc + c * g.n_chunks + q - 1,
+                                                                 g.n_chunks, cin, cr.epoch)
+                                      : get_states<VEC>(cr.inc + base - g.C, cin, cr.epoch));
+                    if (__all_sync(0xffffffffu, ok)) break;
+                }
+                if (__any_sync(0xffffffffu, wait_step(cr, spins, sleep_ns, kTileMaxSleepNs))) {
+                    if (lane == 0) atomicOr(cr.err, ERRBIT_TIMEOUT);
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) cin[v] = __int_as_float(0x7fc00000);
+                    break;
+                }
+            }
+        }
+        if (cok && !walk && more) {
+            float hend[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) hend[v] = __fmaf_rn(TA[v], cin[v], TB[v]);
+            put_states<VEC>(cr.inc + base, hend, cr.epoch);
+        }
 #pragma unroll
         for (int v = 0; v < VEC; ++v) sm.carry[lane][v] = cin[v];
     }
@@ -379,13 +578,46 @@ __device__ __forceinline__ void tile_carry(CarrySmem<VEC, NW>& sm, const float (
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
                 const float a = sm.a[w][lane][v], b = sm.b[w][lane][v];
-                PB[v] = a * PB[v] + b;
+                PB[v] = __fmaf_rn(a, PB[v], b);
                 PA[v] *= a;
             }
         }
     }
 #pragma unroll
     for (int v = 0; v < VEC; ++v) start[v] = __fmaf_rn(PA[v], sm.carry[lane][v], PB[v]);
+}
+
+// Whole CTA, walker protocol, look-ahead phase: combine the warp aggregates
+// of a tile and publish the tile aggregate (no wait, no output).
+template <int VEC, int NW>
+__device__ __forceinline__ void tile_publish_agg(CarrySmem<VEC, NW>& sm, const float (&A)[VEC],
+                                                 const float (&B)[VEC], const Carry& cr,
+                                                 const Geom& g, int64_t q, int64_t c, bool cok) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+        sm.a[warp][lane][v] = A[v];
+        sm.b[warp][lane][v] = B[v];
+    }
+    __syncthreads();
+    if (warp == 0 && cok && q < g.n_chunks - 1) {
+        float TA[VEC], TB[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { TA[v] = 1.f; TB[v] = 0.f; }
+#pragma unroll
+        for (int w = 0; w < NW; ++w)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                const float a = sm.a[w][lane][v], b = sm.b[w][lane][v];
+                TB[v] = __fmaf_rn(a, TB[v], b);
+                TA[v] *= a;
+            }
+#pragma unroll
+        for (int v = 0; v < VEC; ++v)
+            st_pkt2(cr.agg + 2 * ((c + v) * g.n_chunks + q), pkt(TA[v], cr.epoch),
+                    pkt(TB[v], cr.epoch));
+    }
+    __syncthreads();  // the smem is reused by the next phase
 }
 
 }  // namespace lrs

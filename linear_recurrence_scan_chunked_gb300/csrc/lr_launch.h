@@ -21,18 +21,20 @@ enum Op { OP_SCAN_FWD = 0, OP_SCAN_BWD, OP_SRU_FWD, OP_SRU_BWD, OP_DEER, OP_COUN
 
 // Launch configuration of every kernel: NW warps per CTA, R rows per thread
 // (tile = NW*R rows), VEC channels per lane (16-byte vectors on the vector
-// path, one element on the scalar path).  One table, used both to instantiate
-// the kernels and to size the workspace.
+// path, one element on the scalar path).  R is sized so that two tiles (the
+// one being processed and the one being loaded) fit in the registers of a
+// thread at two CTAs per SM.  One table, used both to instantiate the
+// kernels and to size the workspace.
 struct KCfg {
     int NW;
     int R;
 };
 constexpr KCfg kcfg(Op op, int dtype) {
-    return op == OP_SCAN_FWD ? KCfg{8, dtype == 1 ? 4 : 8}
-         : op == OP_SCAN_BWD ? KCfg{8, dtype == 1 ? 2 : 4}
-         : op == OP_SRU_FWD  ? KCfg{8, dtype == 1 ? 2 : 4}
-         : op == OP_SRU_BWD  ? KCfg{8, dtype == 1 ? 2 : 4}
-         :                     KCfg{8, dtype == 1 ? 2 : 4};
+    return op == OP_SCAN_FWD ? KCfg{8, 4}
+         : op == OP_SCAN_BWD ? KCfg{8, 2}
+         : op == OP_SRU_FWD  ? KCfg{8, 2}
+         : op == OP_SRU_BWD  ? KCfg{8, 1}
+         :                     KCfg{8, 2};
 }
 constexpr int kvec(int dtype, bool vec) { return vec ? (dtype == 1 ? 8 : 4) : 1; }
 
@@ -41,23 +43,74 @@ inline TileShape tile_shape(Op op, int dtype, bool vec) {
     return TileShape{k.NW * k.R, 32 * kvec(dtype, vec), 32 * k.NW};
 }
 
+// Which carry protocol a launch uses, and the packet storage it needs.
+// WALK pays off once the chunk chain is long (a round trip per chunk would
+// dominate) and the channels are few enough for a handful of walker CTAs;
+// otherwise CHAIN.  The choice depends on the shape only, so a given problem
+// always gets the same association of its floating-point operations.
+struct CarryPlan {
+    int mode;          // CARRY_CHAIN / CARRY_WALK
+    uint32_t n_walk;   // walker CTAs
+    int wv;            // channels per walker warp
+    size_t inc_elems;  // state packets: n_chunks * C
+    size_t agg_elems;  // aggregate packets (WALK): 2 * n_chunks * C
+};
+constexpr int64_t kWalkMinChunks = 128;
+constexpr int64_t kWalkMaxCtas = 32;
+
+inline CarryPlan carry_plan(Op op, int dtype, int64_t n_chunks, int64_t C) {
+    CarryPlan p{CARRY_CHAIN, 0u, 0, (size_t)(n_chunks * C), 0};
+    if (n_chunks >= kWalkMinChunks) {
+        const int wv = C <= 256 ? 1 : WALK_MAX_WV;  // spread the walkers' reads over more SMs
+        const int64_t warps = (C + wv - 1) / wv;
+        const int64_t ctas = (warps + kcfg(op, dtype).NW - 1) / kcfg(op, dtype).NW;
+        if (ctas <= kWalkMaxCtas) {
+            p.mode = CARRY_WALK;
+            p.n_walk = (uint32_t)ctas;
+            p.wv = wv;
+            p.agg_elems = (size_t)(2 * n_chunks * C);
+        }
+    }
+    return p;
+}
+
+// Grid of a persistent launch: every walker plus as many tile CTAs as can be
+// resident at once (never more than there are tiles).
+inline uint32_t persist_grid(const Geom& g, const Carry& cr, int occ_per_sm) {
+    static int sms[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int& n_sm = sms[dev & 63];
+    if (n_sm <= 0) {
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+        if (n_sm <= 0) n_sm = 1;
+    }
+    const uint64_t want = (uint64_t)cr.n_walk + g.n_tiles;
+    uint64_t cap = (uint64_t)occ_per_sm * (uint64_t)n_sm;
+    if (cap < (uint64_t)cr.n_walk + 1) cap = (uint64_t)cr.n_walk + 1;
+    uint64_t grid = want < cap ? want : cap;
+    if (g.max_grid && grid > g.max_grid) grid = g.max_grid;
+    return (uint32_t)grid;
+}
+
 cudaError_t launch_scan_fwd(int dtype, bool vec, const void* a, const void* b, const void* h0,
-                            void* h, const Geom& g, const Lookback& lb, cudaStream_t s);
+                            void* h, const Geom& g, const Carry& cr, cudaStream_t s);
 
 cudaError_t launch_scan_bwd(int dtype, bool vec, const void* a, const void* h, const void* h0,
                             const void* dh, void* da, void* db, void* dh0, const Geom& g,
-                            const Lookback& lb, cudaStream_t s);
+                            const Carry& cr, cudaStream_t s);
 
 cudaError_t launch_sru_fwd(int dtype, bool vec, const void* xt, const void* uf, const void* ur,
                            const void* x, const float* bf, const float* br, const void* c0,
-                           void* h, void* c, const Geom& g, const Lookback& lb, cudaStream_t s);
+                           void* h, void* c, const Geom& g, const Carry& cr, cudaStream_t s);
 
-// partials: [n_chunks, C] x 2 (forget, reset) fp32 scratch
+// partials: [2][n_chunks][C] (forget, reset) fp32 scratch, followed by 2*C
+// floats that launch_bias_reduce uses for its per-channel sums
 cudaError_t launch_sru_bwd(int dtype, bool vec, const void* xt, const void* uf, const void* ur,
                            const void* x, const float* bf, const float* br, const void* c0,
                            const void* c, const void* dh, void* dxt, void* duf, void* dur,
                            void* dx, void* dc0, float* partials, const Geom& g,
-                           const Lookback& lb, cudaStream_t s);
+                           const Carry& cr, cudaStream_t s);
 
 cudaError_t launch_bias_reduce(const float* partials, int64_t n_chunks, int64_t B, int64_t D,
                                float* dbf, float* dbr, cudaStream_t s);
@@ -65,6 +118,6 @@ cudaError_t launch_bias_reduce(const float* partials, int64_t n_chunks, int64_t 
 // resid: one fp32 slot (as bits), zeroed before the launch, receives max|ynew-yold|
 cudaError_t launch_deer_iter(int dtype, bool vec, const float* w, const void* u, const void* h0,
                              const void* yold, void* ynew, uint32_t* resid, const Geom& g,
-                             const Lookback& lb, cudaStream_t s);
+                             const Carry& cr, cudaStream_t s);
 
 }  // namespace lrs

@@ -7,20 +7,21 @@
 // cached workspace with cudaMalloc on first use (and cudaFree + cudaMalloc
 // when a larger problem arrives); a hidden allocation can fail at run time,
 // fragments the owner's pool, and cudaFree synchronises the whole device.
-// This variant keeps its look-back scratch (tile flags, tile descriptors, the
-// tile ticket) in one fixed, file-scope __device__ array instead, so it calls
+// This variant keeps its scratch (the chunk-state packets and the tile
+// ticket) in one fixed, file-scope __device__ array instead, so it calls
 // no cudaMalloc, cudaFree or allocating library routine.
 //
 // Costs and rules of the fixed array:
 //   * every GPU that loads the library holds kScratchBytes (4 MiB) of device
 //     memory until the process exits;
-//   * problems needing more look-back descriptors than fit are rejected with
-//     LR_ERR_TOO_LARGE (about 2,700 tiles of 64 time steps x 128 fp32
-//     channels, i.e. ~22 M fp32 elements; half that many tiles for bf16);
+//   * problems needing more carry packets than fit are rejected with
+//     LR_ERR_TOO_LARGE: one 8-byte state packet per channel per chunk of 64
+//     time steps (three per channel-chunk when the walker protocol is used),
+//     i.e. ~524 K channel-chunks, ~33 M elements in the common case;
 //   * every call shares the one array: two calls whose kernels overlap on the
 //     GPU (different streams, no ordering between them) race on it and give
 //     wrong results.  Order such calls on one stream or with events.
-//   * the array keeps the last call's contents; flags are tagged with a
+//   * the array keeps the last call's contents; packets are tagged with a
 //     per-call epoch so old ones are ignored, and the tile ticket is cleared
 //     (a 4-byte memset, not an allocation) before every launch.
 //   * the first call on a device looks up the array's device address with
@@ -40,7 +41,6 @@ using namespace lrs;
 
 constexpr size_t kScratchBytes = size_t(4) << 20;
 constexpr size_t kHeaderBytes = 256;  // [0] ticket, [1] error word
-constexpr uint32_t kEpochMax = (1u << 30) - 1;
 constexpr uint32_t kSpinLimit = 1u << 21;
 constexpr int kMaxDevices = 64;
 
@@ -52,8 +52,6 @@ struct NoAllocDev {
 };
 std::mutex g_na_mu;
 NoAllocDev g_na[kMaxDevices];
-
-size_t round256(size_t n) { return (n + 255) / 256 * 256; }
 
 }  // namespace
 
@@ -80,10 +78,11 @@ extern "C" int lr_scan_fwd_noalloc(const void* a, const void* b, const void* h0,
     const int64_t n_chunks = (T + ts.L - 1) / ts.L;
     const int64_t n_ct = (C + ts.CW - 1) / ts.CW;
     if (n_ct > INT32_MAX || n_chunks > INT32_MAX / n_ct) return LR_ERR_TOO_LARGE;
+    const CarryPlan cp = carry_plan(OP_SCAN_FWD, dtype, n_chunks, C);
     const size_t tiles = (size_t)(n_chunks * n_ct);
-    const size_t flag_bytes = round256(tiles * sizeof(uint32_t));
-    const size_t payload_bytes = tiles * (size_t)ts.CW * 3 * sizeof(float);
-    if (kHeaderBytes + flag_bytes + payload_bytes > kScratchBytes) return LR_ERR_TOO_LARGE;
+    if (tiles + cp.n_walk > INT32_MAX / 2) return LR_ERR_TOO_LARGE;
+    const size_t pk_bytes = (cp.inc_elems + cp.agg_elems) * sizeof(u64);
+    if (kHeaderBytes + pk_bytes > kScratchBytes) return LR_ERR_TOO_LARGE;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LR_ERR_CUDA;
@@ -96,11 +95,10 @@ extern "C" int lr_scan_fwd_noalloc(const void* a, const void* b, const void* h0,
         nd.base = (unsigned char*)p;
     }
     uint32_t* words = (uint32_t*)nd.base;
-    uint32_t* flags = (uint32_t*)(nd.base + kHeaderBytes);
-    float* payload = (float*)(nd.base + kHeaderBytes + flag_bytes);
-    if (++nd.epoch > kEpochMax) {  // wrap: forget every old flag once
+    u64* pk = (u64*)(nd.base + kHeaderBytes);
+    if (++nd.epoch == 0) {  // 32-bit wrap: forget every old packet once
         nd.epoch = 1;
-        if (cudaMemsetAsync(flags, 0, kScratchBytes - kHeaderBytes, s) != cudaSuccess)
+        if (cudaMemsetAsync(pk, 0, kScratchBytes - kHeaderBytes, s) != cudaSuccess)
             return LR_ERR_CUDA;
     }
     if (cudaMemsetAsync(words, 0, sizeof(uint32_t), s) != cudaSuccess) return LR_ERR_CUDA;
@@ -111,18 +109,20 @@ extern "C" int lr_scan_fwd_noalloc(const void* a, const void* b, const void* h0,
     g.D = D;
     g.n_chunks = n_chunks;
     g.n_ct = (int)n_ct;
-    g.n_launch = (uint32_t)tiles;
+    g.n_tiles = (uint32_t)tiles;
+    g.n_draws = 0;
     g.ticket_base = 0;
-    Lookback lb;
-    const size_t np = tiles * (size_t)ts.CW;
-    lb.flags = flags;
-    lb.agg_a = payload;
-    lb.agg_b = payload + np;
-    lb.inc = payload + 2 * np;
-    lb.ticket = words;
-    lb.err = err_dev ? err_dev : words + 1;
-    lb.epoch = nd.epoch;
-    lb.spin_limit = kSpinLimit;
-    if (launch_scan_fwd(dtype, vec, a, b, h0, h, g, lb, s) != cudaSuccess) return LR_ERR_CUDA;
+    g.max_grid = 0;
+    Carry cr;
+    cr.inc = pk;
+    cr.agg = pk + cp.inc_elems;
+    cr.ticket = words;
+    cr.err = err_dev ? err_dev : words + 1;
+    cr.epoch = nd.epoch;
+    cr.spin_limit = kSpinLimit;
+    cr.mode = cp.mode;
+    cr.n_walk = cp.n_walk;
+    cr.wv = cp.wv;
+    if (launch_scan_fwd(dtype, vec, a, b, h0, h, g, cr, s) != cudaSuccess) return LR_ERR_CUDA;
     return LR_OK;
 }

@@ -14,176 +14,196 @@
 // needs only row-t data, so the carry between tiles is u at the tile edge.
 //
 // Each element of a, b (resp. a, h, dh) is read once from HBM and each output
-// written once: the tile is held in registers between the local scan and the
-// output pass while the look-back resolves the carry.
+// written once: a tile is held in registers between the local scan and the
+// output pass while its carry resolves, and the next tile's loads are already
+// in flight (lr_persist.cuh).
 #include "lr_launch.h"
+#include "lr_persist.cuh"
 
 namespace lrs {
 
-template <typename S, int VEC, int NW, int R>
-__global__ void __launch_bounds__(NW * 32, 2)
-    k_scan_fwd(const S* __restrict__ a, const S* __restrict__ b, const S* __restrict__ h0,
-               S* __restrict__ h, Geom g, Lookback lb) {
-    constexpr int L = NW * R, CW = 32 * VEC;
-    __shared__ CarrySmem<VEC, NW> sm;
-    const uint32_t tile = take_ticket(lb, g);
-    const int64_t q = tile / g.n_ct;
-    const int j = tile % g.n_ct;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t c = (int64_t)j * CW + lane * VEC;
-    const bool cok = c < g.C;
-    const int64_t t0 = q * L + warp * R;
+template <typename S_, int VEC_, int NW_, int R_>
+struct ScanFwdOp {
+    using S = S_;
+    static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
+    static constexpr bool REV = false;
+    static constexpr int IN_ARRAYS = 2;  // a, b
+    struct Params {
+        const S* a;
+        const S* b;
+        const S* h0;
+        S* h;
+    };
+    struct Regs {
+        Pack<S, VEC> a[R], b[R];
+    };
+    struct Work {};
+    struct Smem {
+        int unused;
+    };
+    struct Acc {};
+    __device__ static void acc_init(Acc&) {}
+    __device__ static const S* init_ptr(const Params& p) { return p.h0; }
 
-    Pack<S, VEC> pa[R], pb[R];
+    __device__ static void load(const Params& p, const Geom& g, const TileCoord& tc, Regs& rg) {
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int64_t t = t0 + r;
-        if (cok && t < g.T) {
-            pa[r].load(a + t * g.C + c);
-            pb[r].load(b + t * g.C + c);
-        } else {  // identity element (1, 0) outside the problem
-            pa[r].ident(1.f);
-            pb[r].ident(0.f);
+        for (int r = 0; r < R; ++r) {
+            const int64_t t = tc.t0 + r;
+            if (tc.cok && t < g.T) {
+                rg.a[r].load(p.a + t * g.C + tc.c);
+                rg.b[r].load(p.b + t * g.C + tc.c);
+            } else {  // identity element (1, 0) outside the problem
+                rg.a[r].ident(1.f);
+                rg.b[r].ident(0.f);
+            }
         }
     }
-    float A[VEC], Bs[VEC];
+    __device__ static void aggregate(const Params&, const Geom&, const TileCoord&, const Regs& rg,
+                                     Work&, float (&A)[VEC], float (&B)[VEC], bool) {
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) { A[v] = 1.f; Bs[v] = 0.f; }
+        for (int v = 0; v < VEC; ++v) { A[v] = 1.f; B[v] = 0.f; }
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+        for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            const float av = pa[r].get(v);
-            Bs[v] = av * Bs[v] + pb[r].get(v);
-            A[v] *= av;
-        }
-    float init[VEC];
-#pragma unroll
-    for (int v = 0; v < VEC; ++v) init[v] = 0.f;
-    if (q == 0 && warp == 0 && h0 != nullptr && cok) load_vec<S, VEC>(h0 + c, init);
-
-    float s[VEC];
-    tile_carry<VEC, NW>(sm, A, Bs, init, s, lb, q, j, g.n_ct);
-
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int64_t t = t0 + r;
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) s[v] = pa[r].get(v) * s[v] + pb[r].get(v);
-        if (cok && t < g.T) store_vec<S, VEC>(h + t * g.C + c, s);
+            for (int v = 0; v < VEC; ++v) {
+                const float av = rg.a[r].get(v);
+                B[v] = av * B[v] + rg.b[r].get(v);
+                A[v] *= av;
+            }
     }
-}
-
-template <typename S, int VEC, int NW, int R>
-__global__ void __launch_bounds__(NW * 32, 2)
-    k_scan_bwd(const S* __restrict__ a, const S* __restrict__ h, const S* __restrict__ h0,
-               const S* __restrict__ dh, S* __restrict__ da, S* __restrict__ db,
-               S* __restrict__ dh0, Geom g, Lookback lb) {
-    constexpr int L = NW * R, CW = 32 * VEC;
-    __shared__ CarrySmem<VEC, NW> sm;
-    const uint32_t tile = take_ticket(lb, g);
-    const int64_t q = tile / g.n_ct;  // scan order: q = 0 is the last time chunk
-    const int j = tile % g.n_ct;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t c = (int64_t)j * CW + lane * VEC;
-    const bool cok = c < g.C;
-    const int64_t tchunk = g.n_chunks - 1 - q;
-    const int64_t tb = tchunk * L + (L - 1) - warp * R;  // time of this thread's first row
-
-    Pack<S, VEC> pa[R], pg[R], ph[R];  // a_t, dh_t, h_{t-1}
+    __device__ static void finish(const Params& p, const Geom& g, const TileCoord& tc,
+                                  const Regs& rg, Work&, float (&s)[VEC], Smem&, Acc&) {
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int64_t t = tb - r;
-        if (cok && t < g.T) {
-            pa[r].load(a + t * g.C + c);
-            pg[r].load(dh + t * g.C + c);
-            if (t > 0) ph[r].load(h + (t - 1) * g.C + c);
-            else if (h0 != nullptr) ph[r].load(h0 + c);
-            else ph[r].ident(0.f);
-        } else {
-            pa[r].ident(1.f);
-            pg[r].ident(0.f);
-            ph[r].ident(0.f);
+        for (int r = 0; r < R; ++r) {
+            const int64_t t = tc.t0 + r;
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) s[v] = rg.a[r].get(v) * s[v] + rg.b[r].get(v);
+            if (tc.cok && t < g.T) store_vec<S, VEC>(p.h + t * g.C + tc.c, s);
         }
     }
-    float A[VEC], Bs[VEC];
-#pragma unroll
-    for (int v = 0; v < VEC; ++v) { A[v] = 1.f; Bs[v] = 0.f; }
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            const float av = pa[r].get(v);
-            Bs[v] = av * (pg[r].get(v) + Bs[v]);
-            A[v] *= av;
-        }
-    float init[VEC];
-#pragma unroll
-    for (int v = 0; v < VEC; ++v) init[v] = 0.f;  // u_T = 0
+    __device__ static void at_exit(const Params&, Smem&, Acc&) {}
+};
 
-    float s[VEC];
-    tile_carry<VEC, NW>(sm, A, Bs, init, s, lb, q, j, g.n_ct);
+template <typename S_, int VEC_, int NW_, int R_>
+struct ScanBwdOp {
+    using S = S_;
+    static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
+    static constexpr bool REV = true;
+    static constexpr int IN_ARRAYS = 3;  // a, dh, h
+    struct Params {
+        const S* a;
+        const S* h;
+        const S* h0;
+        const S* dh;
+        S* da;
+        S* db;
+        S* dh0;
+    };
+    struct Regs {
+        Pack<S, VEC> a[R], g[R], hp[R];  // a_t, dh_t, h_{t-1}
+    };
+    struct Work {};
+    struct Smem {
+        int unused;
+    };
+    struct Acc {};
+    __device__ static void acc_init(Acc&) {}
+    __device__ static const S* init_ptr(const Params&) { return nullptr; }  // u_T = 0
 
+    __device__ static void load(const Params& p, const Geom& g, const TileCoord& tc, Regs& rg) {
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int64_t t = tb - r;
-        float dv[VEC], av[VEC];
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            const float d = pg[r].get(v) + s[v];
-            dv[v] = d;
-            av[v] = d * ph[r].get(v);
-            s[v] = pa[r].get(v) * d;
-        }
-        if (cok && t < g.T) {
-            store_vec<S, VEC>(db + t * g.C + c, dv);
-            store_vec<S, VEC>(da + t * g.C + c, av);
+        for (int r = 0; r < R; ++r) {
+            const int64_t t = tc.t0 - r;
+            if (tc.cok && t < g.T) {
+                rg.a[r].load(p.a + t * g.C + tc.c);
+                rg.g[r].load(p.dh + t * g.C + tc.c);
+                if (t > 0) rg.hp[r].load(p.h + (t - 1) * g.C + tc.c);
+                else if (p.h0 != nullptr) rg.hp[r].load(p.h0 + tc.c);
+                else rg.hp[r].ident(0.f);
+            } else {
+                rg.a[r].ident(1.f);
+                rg.g[r].ident(0.f);
+                rg.hp[r].ident(0.f);
+            }
         }
     }
-    // row 0 is the last row of the last warp of time chunk 0: s = u_0 = dh0
-    if (tchunk == 0 && warp == NW - 1 && dh0 != nullptr && cok) store_vec<S, VEC>(dh0 + c, s);
-}
+    __device__ static void aggregate(const Params&, const Geom&, const TileCoord&, const Regs& rg,
+                                     Work&, float (&A)[VEC], float (&B)[VEC], bool) {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { A[v] = 1.f; B[v] = 0.f; }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                const float av = rg.a[r].get(v);
+                B[v] = av * (rg.g[r].get(v) + B[v]);
+                A[v] *= av;
+            }
+    }
+    __device__ static void finish(const Params& p, const Geom& g, const TileCoord& tc,
+                                  const Regs& rg, Work&, float (&s)[VEC], Smem&, Acc&) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int64_t t = tc.t0 - r;
+            float dv[VEC], av[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                const float d = rg.g[r].get(v) + s[v];
+                dv[v] = d;
+                av[v] = d * rg.hp[r].get(v);
+                s[v] = rg.a[r].get(v) * d;
+            }
+            if (tc.cok && t < g.T) {
+                store_vec<S, VEC>(p.db + t * g.C + tc.c, dv);
+                store_vec<S, VEC>(p.da + t * g.C + tc.c, av);
+            }
+        }
+        // row 0 is the last row of the last warp of time chunk 0: s = u_0 = dh0
+        if (tc.tchunk == 0 && (threadIdx.x >> 5) == NW - 1 && p.dh0 != nullptr && tc.cok)
+            store_vec<S, VEC>(p.dh0 + tc.c, s);
+    }
+    __device__ static void at_exit(const Params&, Smem&, Acc&) {}
+};
 
 template <typename S, bool VP>
-static cudaError_t scan_fwd_t(const void* a, const void* b, const void* h0, void* h,
-                              const Geom& g, const Lookback& lb, cudaStream_t s) {
-    constexpr int DT = sizeof(S) == 2 ? 1 : 0;
-    constexpr KCfg k = kcfg(OP_SCAN_FWD, DT);
-    constexpr int VEC = kvec(DT, VP);
-    k_scan_fwd<S, VEC, k.NW, k.R><<<g.n_launch, 32 * k.NW, 0, s>>>(
-        (const S*)a, (const S*)b, (const S*)h0, (S*)h, g, lb);
-    return cudaGetLastError();
+using FwdOpT = ScanFwdOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_SCAN_FWD, sizeof(S) == 2).NW,
+                         kcfg(OP_SCAN_FWD, sizeof(S) == 2).R>;
+template <typename S, bool VP>
+using BwdOpT = ScanBwdOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_SCAN_BWD, sizeof(S) == 2).NW,
+                         kcfg(OP_SCAN_BWD, sizeof(S) == 2).R>;
+
+template <typename S, bool VP>
+static cudaError_t scan_fwd_t(const void* a, const void* b, const void* h0, void* h, const Geom& g,
+                              const Carry& cr, cudaStream_t s) {
+    return launch_persist<FwdOpT<S, VP>>({(const S*)a, (const S*)b, (const S*)h0, (S*)h}, g, cr, s);
 }
 
 template <typename S, bool VP>
 static cudaError_t scan_bwd_t(const void* a, const void* h, const void* h0, const void* dh,
-                              void* da, void* db, void* dh0, const Geom& g, const Lookback& lb,
+                              void* da, void* db, void* dh0, const Geom& g, const Carry& cr,
                               cudaStream_t s) {
-    constexpr int DT = sizeof(S) == 2 ? 1 : 0;
-    constexpr KCfg k = kcfg(OP_SCAN_BWD, DT);
-    constexpr int VEC = kvec(DT, VP);
-    k_scan_bwd<S, VEC, k.NW, k.R><<<g.n_launch, 32 * k.NW, 0, s>>>(
-        (const S*)a, (const S*)h, (const S*)h0, (const S*)dh, (S*)da, (S*)db, (S*)dh0, g, lb);
-    return cudaGetLastError();
+    return launch_persist<BwdOpT<S, VP>>({(const S*)a, (const S*)h, (const S*)h0, (const S*)dh,
+                                          (S*)da, (S*)db, (S*)dh0},
+                                         g, cr, s);
 }
 
 cudaError_t launch_scan_fwd(int dtype, bool vec, const void* a, const void* b, const void* h0,
-                            void* h, const Geom& g, const Lookback& lb, cudaStream_t s) {
+                            void* h, const Geom& g, const Carry& cr, cudaStream_t s) {
     if (dtype == 0)
-        return vec ? scan_fwd_t<float, true>(a, b, h0, h, g, lb, s)
-                   : scan_fwd_t<float, false>(a, b, h0, h, g, lb, s);
-    return vec ? scan_fwd_t<__nv_bfloat16, true>(a, b, h0, h, g, lb, s)
-               : scan_fwd_t<__nv_bfloat16, false>(a, b, h0, h, g, lb, s);
+        return vec ? scan_fwd_t<float, true>(a, b, h0, h, g, cr, s)
+                   : scan_fwd_t<float, false>(a, b, h0, h, g, cr, s);
+    return vec ? scan_fwd_t<__nv_bfloat16, true>(a, b, h0, h, g, cr, s)
+               : scan_fwd_t<__nv_bfloat16, false>(a, b, h0, h, g, cr, s);
 }
 
 cudaError_t launch_scan_bwd(int dtype, bool vec, const void* a, const void* h, const void* h0,
                             const void* dh, void* da, void* db, void* dh0, const Geom& g,
-                            const Lookback& lb, cudaStream_t s) {
+                            const Carry& cr, cudaStream_t s) {
     if (dtype == 0)
-        return vec ? scan_bwd_t<float, true>(a, h, h0, dh, da, db, dh0, g, lb, s)
-                   : scan_bwd_t<float, false>(a, h, h0, dh, da, db, dh0, g, lb, s);
-    return vec ? scan_bwd_t<__nv_bfloat16, true>(a, h, h0, dh, da, db, dh0, g, lb, s)
-               : scan_bwd_t<__nv_bfloat16, false>(a, h, h0, dh, da, db, dh0, g, lb, s);
+        return vec ? scan_bwd_t<float, true>(a, h, h0, dh, da, db, dh0, g, cr, s)
+                   : scan_bwd_t<float, false>(a, h, h0, dh, da, db, dh0, g, cr, s);
+    return vec ? scan_bwd_t<__nv_bfloat16, true>(a, h, h0, dh, da, db, dh0, g, cr, s)
+               : scan_bwd_t<__nv_bfloat16, false>(a, h, h0, dh, da, db, dh0, g, cr, s);
 }
 
 }  // namespace lrs

@@ -13,313 +13,355 @@
 //   dxt = dc (1-f),  duf = dc (c_{t-1} - xt) f (1-f),  dc0 = u_0,
 //   dur = dh (tanh c - x) r (1-r),  dx = dh (1-r)  (no scan needed: written
 //   before the carry is known),
-//   dbf, dbr: per-tile channel sums -> [n_chunks, C] partials -> a fixed-order
-//   reduction over chunks and batch (deterministic).
+//   dbf, dbr: per-tile channel sums -> [2][n_chunks][C] partials -> a
+//   fixed-order reduction over chunks, then over the batch (deterministic).
 #include "lr_launch.h"
+#include "lr_persist.cuh"
 
 namespace lrs {
 
 __device__ __forceinline__ float sigmoidf_(float z) { return 1.f / (1.f + expf(-z)); }
 
-template <typename S, int VEC, int NW, int R>
-__global__ void __launch_bounds__(NW * 32, 2)
-    k_sru_fwd(const S* __restrict__ xt, const S* __restrict__ uf, const S* __restrict__ ur,
-              const S* __restrict__ x, const float* __restrict__ bf,
-              const float* __restrict__ br, const S* __restrict__ c0, S* __restrict__ h,
-              S* __restrict__ cst, Geom g, Lookback lb) {
-    constexpr int L = NW * R, CW = 32 * VEC;
-    __shared__ CarrySmem<VEC, NW> sm;
-    const uint32_t tile = take_ticket(lb, g);
-    const int64_t q = tile / g.n_ct;
-    const int j = tile % g.n_ct;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t ch = (int64_t)j * CW + lane * VEC;
-    const bool cok = ch < g.C;
-    const int64_t d = cok ? ch % g.D : 0;
-    const int64_t t0 = q * L + warp * R;
+template <typename S_, int VEC_, int NW_, int R_>
+struct SruFwdOp {
+    using S = S_;
+    static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
+    static constexpr bool REV = false;
+    static constexpr int IN_ARRAYS = 4;  // xt, uf, ur, x
+    struct Params {
+        const S* xt;
+        const S* uf;
+        const S* ur;
+        const S* x;
+        const float* bf;
+        const float* br;
+        const S* c0;
+        S* h;
+        S* c;
+    };
+    struct Regs {
+        Pack<S, VEC> xt[R], uf[R], ur[R], x[R];
+    };
+    struct Work {
+        float fa[R][VEC], fb[R][VEC];  // scan element (f, (1-f) xt)
+    };
+    struct Smem {
+        int unused;
+    };
+    struct Acc {};
+    __device__ static void acc_init(Acc&) {}
+    __device__ static const S* init_ptr(const Params& p) { return p.c0; }
 
-    float bfv[VEC], brv[VEC];
+    __device__ static void load(const Params& p, const Geom& g, const TileCoord& tc, Regs& rg) {
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) { bfv[v] = 0.f; brv[v] = 0.f; }
-    if (cok) {
-        load_param<VEC>(bf + d, bfv);
-        load_param<VEC>(br + d, brv);
+        for (int r = 0; r < R; ++r) {
+            const int64_t t = tc.t0 + r;
+            if (tc.cok && t < g.T) {
+                const int64_t o = t * g.C + tc.c;
+                rg.xt[r].load(p.xt + o);
+                rg.uf[r].load(p.uf + o);
+                rg.ur[r].load(p.ur + o);
+                rg.x[r].load(p.x + o);
+            } else {
+                rg.xt[r].ident(0.f);
+                rg.uf[r].ident(0.f);
+                rg.ur[r].ident(0.f);
+                rg.x[r].ident(0.f);
+            }
+        }
     }
-    float fa[R][VEC], fb[R][VEC];  // scan element (f, (1-f) xt)
-    Pack<S, VEC> pur[R], px[R];
+    __device__ static void aggregate(const Params& p, const Geom& g, const TileCoord& tc,
+                                     const Regs& rg, Work& w, float (&A)[VEC], float (&B)[VEC],
+                                     bool side) {
+        float bfv[VEC];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int64_t t = t0 + r;
-        if (cok && t < g.T) {
-            Pack<S, VEC> pxt, puf;
-            pxt.load(xt + t * g.C + ch);
-            puf.load(uf + t * g.C + ch);
-            pur[r].load(ur + t * g.C + ch);
-            px[r].load(x + t * g.C + ch);
+        for (int v = 0; v < VEC; ++v) bfv[v] = 0.f;
+        if (tc.cok) load_param<VEC>(p.bf + tc.c % g.D, bfv);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { A[v] = 1.f; B[v] = 0.f; }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const bool ok = tc.cok && tc.t0 + r < g.T;
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
-                const float f = sigmoidf_(puf.get(v) + bfv[v]);
-                fa[r][v] = f;
-                fb[r][v] = (1.f - f) * pxt.get(v);
+                const float f = sigmoidf_(rg.uf[r].get(v) + bfv[v]);
+                w.fa[r][v] = ok ? f : 1.f;
+                w.fb[r][v] = ok ? (1.f - f) * rg.xt[r].get(v) : 0.f;
+                B[v] = w.fa[r][v] * B[v] + w.fb[r][v];
+                A[v] *= w.fa[r][v];
             }
-        } else {
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) { fa[r][v] = 1.f; fb[r][v] = 0.f; }
-            pur[r].ident(0.f);
-            px[r].ident(0.f);
         }
     }
-    float A[VEC], Bs[VEC];
+    __device__ static void finish(const Params& p, const Geom& g, const TileCoord& tc,
+                                  const Regs& rg, Work& w, float (&s)[VEC], Smem&, Acc&) {
+        float brv[VEC];
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) { A[v] = 1.f; Bs[v] = 0.f; }
+        for (int v = 0; v < VEC; ++v) brv[v] = 0.f;
+        if (tc.cok) load_param<VEC>(p.br + tc.c % g.D, brv);
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+        for (int r = 0; r < R; ++r) {
+            const int64_t t = tc.t0 + r;
+            float hv[VEC];
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            Bs[v] = fa[r][v] * Bs[v] + fb[r][v];
-            A[v] *= fa[r][v];
-        }
-    float init[VEC];
-#pragma unroll
-    for (int v = 0; v < VEC; ++v) init[v] = 0.f;
-    if (q == 0 && warp == 0 && c0 != nullptr && cok) load_vec<S, VEC>(c0 + ch, init);
-
-    float s[VEC];
-    tile_carry<VEC, NW>(sm, A, Bs, init, s, lb, q, j, g.n_ct);
-
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int64_t t = t0 + r;
-        float hv[VEC];
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            s[v] = fa[r][v] * s[v] + fb[r][v];
-            const float rg = sigmoidf_(pur[r].get(v) + brv[v]);
-            hv[v] = rg * tanhf(s[v]) + (1.f - rg) * px[r].get(v);
-        }
-        if (cok && t < g.T) {
-            store_vec<S, VEC>(cst + t * g.C + ch, s);
-            store_vec<S, VEC>(h + t * g.C + ch, hv);
+            for (int v = 0; v < VEC; ++v) {
+                s[v] = w.fa[r][v] * s[v] + w.fb[r][v];
+                const float rg_ = sigmoidf_(rg.ur[r].get(v) + brv[v]);
+                hv[v] = rg_ * tanhf(s[v]) + (1.f - rg_) * rg.x[r].get(v);
+            }
+            if (tc.cok && t < g.T) {
+                store_vec<S, VEC>(p.c + t * g.C + tc.c, s);
+                store_vec<S, VEC>(p.h + t * g.C + tc.c, hv);
+            }
         }
     }
-}
+    __device__ static void at_exit(const Params&, Smem&, Acc&) {}
+};
 
-template <typename S, int VEC, int NW, int R>
-__global__ void __launch_bounds__(NW * 32, 2)
-    k_sru_bwd(const S* __restrict__ xt, const S* __restrict__ uf, const S* __restrict__ ur,
-              const S* __restrict__ x, const float* __restrict__ bf,
-              const float* __restrict__ br, const S* __restrict__ c0,
-              const S* __restrict__ cst, const S* __restrict__ dh, S* __restrict__ dxt,
-              S* __restrict__ duf, S* __restrict__ dur, S* __restrict__ dx,
-              S* __restrict__ dc0, float* __restrict__ partials, Geom g, Lookback lb) {
-    constexpr int L = NW * R, CW = 32 * VEC;
-    __shared__ CarrySmem<VEC, NW> sm;
-    const uint32_t tile = take_ticket(lb, g);
-    const int64_t q = tile / g.n_ct;
-    const int j = tile % g.n_ct;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t ch = (int64_t)j * CW + lane * VEC;
-    const bool cok = ch < g.C;
-    const int64_t d = cok ? ch % g.D : 0;
-    const int64_t tchunk = g.n_chunks - 1 - q;
-    const int64_t tb = tchunk * L + (L - 1) - warp * R;
+template <typename S_, int VEC_, int NW_, int R_>
+struct SruBwdOp {
+    using S = S_;
+    static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
+    static constexpr bool REV = true;
+    static constexpr int IN_ARRAYS = 7;  // xt, uf, ur, x, c, c_{t-1}, dh
+    struct Params {
+        const S* xt;
+        const S* uf;
+        const S* ur;
+        const S* x;
+        const float* bf;
+        const float* br;
+        const S* c0;
+        const S* c;
+        const S* dh;
+        S* dxt;
+        S* duf;
+        S* dur;
+        S* dx;
+        S* dc0;
+        float* partials;  // [2][n_chunks][C]
+    };
+    struct Regs {
+        Pack<S, VEC> xt[R], uf[R], ur[R], x[R], c[R], cp[R], dh[R];
+    };
+    struct Work {
+        float F[R][VEC], E[R][VEC], XT[R][VEC], CP[R][VEC];
+        float sum_r[VEC];
+    };
+    struct Smem {
+        float pf[NW][32][VEC];
+        float pr[NW][32][VEC];
+    };
+    struct Acc {};
+    __device__ static void acc_init(Acc&) {}
+    __device__ static const S* init_ptr(const Params&) { return nullptr; }  // u_T = 0
 
-    float bfv[VEC], brv[VEC];
+    __device__ static void load(const Params& p, const Geom& g, const TileCoord& tc, Regs& rg) {
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) { bfv[v] = 0.f; brv[v] = 0.f; }
-    if (cok) {
-        load_param<VEC>(bf + d, bfv);
-        load_param<VEC>(br + d, brv);
+        for (int r = 0; r < R; ++r) {
+            const int64_t t = tc.t0 - r;
+            if (tc.cok && t < g.T) {
+                const int64_t o = t * g.C + tc.c;
+                rg.xt[r].load(p.xt + o);
+                rg.uf[r].load(p.uf + o);
+                rg.ur[r].load(p.ur + o);
+                rg.x[r].load(p.x + o);
+                rg.c[r].load(p.c + o);
+                rg.dh[r].load(p.dh + o);
+                if (t > 0) rg.cp[r].load(p.c + o - g.C);
+                else if (p.c0 != nullptr) rg.cp[r].load(p.c0 + tc.c);
+                else rg.cp[r].ident(0.f);
+            } else {
+                rg.xt[r].ident(0.f);
+                rg.uf[r].ident(0.f);
+                rg.ur[r].ident(0.f);
+                rg.x[r].ident(0.f);
+                rg.c[r].ident(0.f);
+                rg.cp[r].ident(0.f);
+                rg.dh[r].ident(0.f);
+            }
+        }
     }
-    float F[R][VEC], E[R][VEC], XT[R][VEC], CP[R][VEC];
-    float sum_r[VEC], sum_f[VEC];
+    __device__ static void aggregate(const Params& p, const Geom& g, const TileCoord& tc,
+                                     const Regs& rg, Work& w, float (&A)[VEC], float (&B)[VEC],
+                                     bool side) {
+        float bfv[VEC], brv[VEC];
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) { sum_r[v] = 0.f; sum_f[v] = 0.f; }
+        for (int v = 0; v < VEC; ++v) { bfv[v] = 0.f; brv[v] = 0.f; w.sum_r[v] = 0.f; }
+        if (tc.cok) {
+            load_param<VEC>(p.bf + tc.c % g.D, bfv);
+            load_param<VEC>(p.br + tc.c % g.D, brv);
+        }
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int64_t t = tb - r;
-        if (cok && t < g.T) {
-            Pack<S, VEC> pxt, puf, pur, px, pc, pcp, pdh;
-            const int64_t o = t * g.C + ch;
-            pxt.load(xt + o);
-            puf.load(uf + o);
-            pur.load(ur + o);
-            px.load(x + o);
-            pc.load(cst + o);
-            pdh.load(dh + o);
-            if (t > 0) pcp.load(cst + o - g.C);
-            else if (c0 != nullptr) pcp.load(c0 + ch);
-            else pcp.ident(0.f);
+        for (int v = 0; v < VEC; ++v) { A[v] = 1.f; B[v] = 0.f; }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int64_t t = tc.t0 - r;
+            const bool ok = tc.cok && t < g.T;
             float durv[VEC], dxv[VEC];
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
-                const float f = sigmoidf_(puf.get(v) + bfv[v]);
-                const float rg = sigmoidf_(pur.get(v) + brv[v]);
-                const float th = tanhf(pc.get(v));
-                const float g_ = pdh.get(v);
-                durv[v] = g_ * (th - px.get(v)) * rg * (1.f - rg);
-                dxv[v] = g_ * (1.f - rg);
-                sum_r[v] += durv[v];
-                F[r][v] = f;
-                E[r][v] = g_ * rg * (1.f - th * th);
-                XT[r][v] = pxt.get(v);
-                CP[r][v] = pcp.get(v);
+                const float f = sigmoidf_(rg.uf[r].get(v) + bfv[v]);
+                const float rg_ = sigmoidf_(rg.ur[r].get(v) + brv[v]);
+                const float th = tanhf(rg.c[r].get(v));
+                const float gv = rg.dh[r].get(v);
+                durv[v] = gv * (th - rg.x[r].get(v)) * rg_ * (1.f - rg_);
+                dxv[v] = gv * (1.f - rg_);
+                if (ok) w.sum_r[v] += durv[v];
+                w.F[r][v] = ok ? f : 1.f;
+                w.E[r][v] = ok ? gv * rg_ * (1.f - th * th) : 0.f;
+                w.XT[r][v] = rg.xt[r].get(v);
+                w.CP[r][v] = rg.cp[r].get(v);
+                B[v] = w.F[r][v] * (w.E[r][v] + B[v]);
+                A[v] *= w.F[r][v];
             }
-            store_vec<S, VEC>(dur + o, durv);
-            store_vec<S, VEC>(dx + o, dxv);
-        } else {
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) { F[r][v] = 1.f; E[r][v] = 0.f; XT[r][v] = 0.f; CP[r][v] = 0.f; }
+            if (ok && side) {
+                store_vec<S, VEC>(p.dur + t * g.C + tc.c, durv);
+                store_vec<S, VEC>(p.dx + t * g.C + tc.c, dxv);
+            }
         }
     }
-    float A[VEC], Bs[VEC];
+    __device__ static void finish(const Params& p, const Geom& g, const TileCoord& tc,
+                                  const Regs&, Work& w, float (&s)[VEC], Smem& xs, Acc&) {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        float sum_f[VEC];
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) { A[v] = 1.f; Bs[v] = 0.f; }
+        for (int v = 0; v < VEC; ++v) sum_f[v] = 0.f;
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+        for (int r = 0; r < R; ++r) {
+            const int64_t t = tc.t0 - r;
+            const bool ok = tc.cok && t < g.T;
+            float dxtv[VEC], dufv[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                const float dc = w.E[r][v] + s[v];
+                const float f = w.F[r][v];
+                dxtv[v] = dc * (1.f - f);
+                dufv[v] = dc * (w.CP[r][v] - w.XT[r][v]) * f * (1.f - f);
+                s[v] = f * dc;
+                if (ok) sum_f[v] += dufv[v];
+            }
+            if (ok) {
+                store_vec<S, VEC>(p.dxt + t * g.C + tc.c, dxtv);
+                store_vec<S, VEC>(p.duf + t * g.C + tc.c, dufv);
+            }
+        }
+        if (tc.tchunk == 0 && warp == NW - 1 && p.dc0 != nullptr && tc.cok)
+            store_vec<S, VEC>(p.dc0 + tc.c, s);
+        // bias-gradient partials of this tile: sum over its rows, fixed warp order
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
-            Bs[v] = F[r][v] * (E[r][v] + Bs[v]);
-            A[v] *= F[r][v];
+            xs.pf[warp][lane][v] = sum_f[v];
+            xs.pr[warp][lane][v] = w.sum_r[v];
         }
-    float init[VEC];
+        __syncthreads();
+        if (warp == 0 && tc.cok) {
+            float pf[VEC], pr[VEC];
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) init[v] = 0.f;
-
-    float s[VEC];
-    tile_carry<VEC, NW>(sm, A, Bs, init, s, lb, q, j, g.n_ct);
-
+            for (int v = 0; v < VEC; ++v) { pf[v] = 0.f; pr[v] = 0.f; }
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int64_t t = tb - r;
-        const bool ok = cok && t < g.T;
-        float dxtv[VEC], dufv[VEC];
+            for (int ww = 0; ww < NW; ++ww)
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            const float dc = E[r][v] + s[v];
-            const float f = F[r][v];
-            dxtv[v] = dc * (1.f - f);
-            dufv[v] = dc * (CP[r][v] - XT[r][v]) * f * (1.f - f);
-            s[v] = f * dc;
-            if (ok) sum_f[v] += dufv[v];
-        }
-        if (ok) {
-            store_vec<S, VEC>(dxt + t * g.C + ch, dxtv);
-            store_vec<S, VEC>(duf + t * g.C + ch, dufv);
+                for (int v = 0; v < VEC; ++v) { pf[v] += xs.pf[ww][lane][v]; pr[v] += xs.pr[ww][lane][v]; }
+            float* pfp = p.partials + tc.tchunk * g.C + tc.c;
+            float* prp = p.partials + (g.n_chunks + tc.tchunk) * g.C + tc.c;
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) { pfp[v] = pf[v]; prp[v] = pr[v]; }
         }
     }
-    if (tchunk == 0 && warp == NW - 1 && dc0 != nullptr && cok) store_vec<S, VEC>(dc0 + ch, s);
+    __device__ static void at_exit(const Params&, Smem&, Acc&) {}
+};
 
-    // bias-gradient partials of this tile: sum over its rows, fixed warp order
-    __syncthreads();  // the carry smem is free again
-#pragma unroll
-    for (int v = 0; v < VEC; ++v) {
-        sm.a[warp][lane][v] = sum_f[v];
-        sm.b[warp][lane][v] = sum_r[v];
-    }
-    __syncthreads();
-    if (warp == 0 && cok) {
-        float pf[VEC], pr[VEC];
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) { pf[v] = 0.f; pr[v] = 0.f; }
-#pragma unroll
-        for (int w = 0; w < NW; ++w)
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) { pf[v] += sm.a[w][lane][v]; pr[v] += sm.b[w][lane][v]; }
-        float* pfp = partials + tchunk * g.C + ch;
-        float* prp = partials + (g.n_chunks + tchunk) * g.C + ch;
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) { pfp[v] = pf[v]; prp[v] = pr[v]; }
-    }
-}
-
-// dbf[d] = sum_k sum_b partials_f[k][b*D + d] (likewise dbr), in a fixed order:
-// a block owns 32 consecutive features; its 8 warps each sum a fixed slice of
-// the (chunk, batch) pairs; the slices are added in warp order.
+// Bias gradients from the per-tile partials, in a fixed order (deterministic):
+// stage 1 sums every channel over the time chunks (one thread per channel,
+// loads issued eight chunks ahead), stage 2 sums the batch rows of each
+// feature.  partials: [2][n_chunks][C] (forget, reset); colsum: [2][C].
 __global__ void __launch_bounds__(256)
-    k_bias_reduce(const float* __restrict__ partials, int64_t n_chunks, int64_t B, int64_t D,
-                  float* __restrict__ dbf, float* __restrict__ dbr) {
-    __shared__ float sf[8][32], sr[8][32];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t d = (int64_t)blockIdx.x * 32 + lane;
-    const int64_t C = B * D, n = n_chunks * B;
-    const int64_t per = (n + 7) / 8, lo = warp * per, hi = lo + per < n ? lo + per : n;
-    float af = 0.f, ar = 0.f;
-    if (d < D)
-        for (int64_t i = lo; i < hi; ++i) {
-            const int64_t k = i / B, b = i % B;
-            af += partials[k * C + b * D + d];
-            ar += partials[(n_chunks + k) * C + b * D + d];
-        }
-    sf[warp][lane] = af;
-    sr[warp][lane] = ar;
-    __syncthreads();
-    if (warp == 0 && d < D) {
-        float tf = 0.f, tr = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) { tf += sf[w][lane]; tr += sr[w][lane]; }
-        dbf[d] = tf;
-        dbr[d] = tr;
-    }
+    k_bias_colsum(const float* __restrict__ partials, int64_t n_chunks, int64_t C,
+                  float* __restrict__ colsum) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= 2 * C) return;
+    const int64_t which = i / C, c = i % C;
+    const float* p = partials + which * n_chunks * C + c;
+    float acc = 0.f;
+#pragma unroll 8
+    for (int64_t k = 0; k < n_chunks; ++k) acc += __ldg(p + k * C);
+    colsum[i] = acc;
 }
+
+__global__ void __launch_bounds__(256)
+    k_bias_batch(const float* __restrict__ colsum, int64_t B, int64_t D,
+                 float* __restrict__ dbf, float* __restrict__ dbr) {
+    const int64_t d = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (d >= D) return;
+    const int64_t C = B * D;
+    float sf = 0.f, sr = 0.f;
+    for (int64_t b = 0; b < B; ++b) {
+        sf += __ldg(colsum + b * D + d);
+        sr += __ldg(colsum + C + b * D + d);
+    }
+    dbf[d] = sf;
+    dbr[d] = sr;
+}
+
+template <typename S, bool VP>
+using SruFwdOpT = SruFwdOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_SRU_FWD, sizeof(S) == 2).NW,
+                           kcfg(OP_SRU_FWD, sizeof(S) == 2).R>;
+template <typename S, bool VP>
+using SruBwdOpT = SruBwdOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_SRU_BWD, sizeof(S) == 2).NW,
+                           kcfg(OP_SRU_BWD, sizeof(S) == 2).R>;
 
 template <typename S, bool VP>
 static cudaError_t sru_fwd_t(const void* xt, const void* uf, const void* ur, const void* x,
                              const float* bf, const float* br, const void* c0, void* h, void* c,
-                             const Geom& g, const Lookback& lb, cudaStream_t s) {
-    constexpr int DT = sizeof(S) == 2 ? 1 : 0;
-    constexpr KCfg k = kcfg(OP_SRU_FWD, DT);
-    constexpr int VEC = kvec(DT, VP);
-    k_sru_fwd<S, VEC, k.NW, k.R><<<g.n_launch, 32 * k.NW, 0, s>>>(
-        (const S*)xt, (const S*)uf, (const S*)ur, (const S*)x, bf, br, (const S*)c0, (S*)h,
-        (S*)c, g, lb);
-    return cudaGetLastError();
+                             const Geom& g, const Carry& cr, cudaStream_t s) {
+    return launch_persist<SruFwdOpT<S, VP>>({(const S*)xt, (const S*)uf, (const S*)ur,
+                                             (const S*)x, bf, br, (const S*)c0, (S*)h, (S*)c},
+                                            g, cr, s);
 }
 
 template <typename S, bool VP>
 static cudaError_t sru_bwd_t(const void* xt, const void* uf, const void* ur, const void* x,
                              const float* bf, const float* br, const void* c0, const void* c,
                              const void* dh, void* dxt, void* duf, void* dur, void* dx, void* dc0,
-                             float* partials, const Geom& g, const Lookback& lb, cudaStream_t s) {
-    constexpr int DT = sizeof(S) == 2 ? 1 : 0;
-    constexpr KCfg k = kcfg(OP_SRU_BWD, DT);
-    constexpr int VEC = kvec(DT, VP);
-    k_sru_bwd<S, VEC, k.NW, k.R><<<g.n_launch, 32 * k.NW, 0, s>>>(
-        (const S*)xt, (const S*)uf, (const S*)ur, (const S*)x, bf, br, (const S*)c0,
-        (const S*)c, (const S*)dh, (S*)dxt, (S*)duf, (S*)dur, (S*)dx, (S*)dc0, partials, g, lb);
-    return cudaGetLastError();
+                             float* partials, const Geom& g, const Carry& cr, cudaStream_t s) {
+    return launch_persist<SruBwdOpT<S, VP>>(
+        {(const S*)xt, (const S*)uf, (const S*)ur, (const S*)x, bf, br, (const S*)c0, (const S*)c,
+         (const S*)dh, (S*)dxt, (S*)duf, (S*)dur, (S*)dx, (S*)dc0, partials},
+        g, cr, s);
 }
 
 cudaError_t launch_sru_fwd(int dtype, bool vec, const void* xt, const void* uf, const void* ur,
                            const void* x, const float* bf, const float* br, const void* c0,
-                           void* h, void* c, const Geom& g, const Lookback& lb, cudaStream_t s) {
+                           void* h, void* c, const Geom& g, const Carry& cr, cudaStream_t s) {
     if (dtype == 0)
-        return vec ? sru_fwd_t<float, true>(xt, uf, ur, x, bf, br, c0, h, c, g, lb, s)
-                   : sru_fwd_t<float, false>(xt, uf, ur, x, bf, br, c0, h, c, g, lb, s);
-    return vec ? sru_fwd_t<__nv_bfloat16, true>(xt, uf, ur, x, bf, br, c0, h, c, g, lb, s)
-               : sru_fwd_t<__nv_bfloat16, false>(xt, uf, ur, x, bf, br, c0, h, c, g, lb, s);
+        return vec ? sru_fwd_t<float, true>(xt, uf, ur, x, bf, br, c0, h, c, g, cr, s)
+                   : sru_fwd_t<float, false>(xt, uf, ur, x, bf, br, c0, h, c, g, cr, s);
+    return vec ? sru_fwd_t<__nv_bfloat16, true>(xt, uf, ur, x, bf, br, c0, h, c, g, cr, s)
+               : sru_fwd_t<__nv_bfloat16, false>(xt, uf, ur, x, bf, br, c0, h, c, g, cr, s);
 }
 
 cudaError_t launch_sru_bwd(int dtype, bool vec, const void* xt, const void* uf, const void* ur,
                            const void* x, const float* bf, const float* br, const void* c0,
                            const void* c, const void* dh, void* dxt, void* duf, void* dur,
                            void* dx, void* dc0, float* partials, const Geom& g,
-                           const Lookback& lb, cudaStream_t s) {
+                           const Carry& cr, cudaStream_t s) {
     if (dtype == 0)
         return vec ? sru_bwd_t<float, true>(xt, uf, ur, x, bf, br, c0, c, dh, dxt, duf, dur, dx,
-                                            dc0, partials, g, lb, s)
+                                            dc0, partials, g, cr, s)
                    : sru_bwd_t<float, false>(xt, uf, ur, x, bf, br, c0, c, dh, dxt, duf, dur, dx,
-                                             dc0, partials, g, lb, s);
+                                             dc0, partials, g, cr, s);
     return vec ? sru_bwd_t<__nv_bfloat16, true>(xt, uf, ur, x, bf, br, c0, c, dh, dxt, duf, dur,
-                                                dx, dc0, partials, g, lb, s)
+                                                dx, dc0, partials, g, cr, s)
                : sru_bwd_t<__nv_bfloat16, false>(xt, uf, ur, x, bf, br, c0, c, dh, dxt, duf, dur,
-                                                 dx, dc0, partials, g, lb, s);
+                                                 dx, dc0, partials, g, cr, s);
 }
 
 cudaError_t launch_bias_reduce(const float* partials, int64_t n_chunks, int64_t B, int64_t D,
                                float* dbf, float* dbr, cudaStream_t s) {
-    const unsigned blocks = (unsigned)((D + 31) / 32);
-    k_bias_reduce<<<blocks, 256, 0, s>>>(partials, n_chunks, B, D, dbf, dbr);
+    const int64_t C = B * D;
+    float* colsum = const_cast<float*>(partials) + 2 * n_chunks * C;
+    k_bias_colsum<<<(unsigned)((2 * C + 255) / 256), 256, 0, s>>>(partials, n_chunks, C, colsum);
+    k_bias_batch<<<(unsigned)((D + 255) / 256), 256, 0, s>>>(colsum, B, D, dbf, dbr);
     return cudaGetLastError();
 }
 
