@@ -19,20 +19,23 @@
 
 namespace lrs {
 
+template <typename S>
+struct DeerParams {
+    const float* w;
+    const S* u;
+    const S* h0;
+    const S* yold;
+    S* ynew;
+    uint32_t* resid;
+};
+
 template <typename S_, int VEC_, int NW_, int R_>
 struct DeerOp {
     using S = S_;
     static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
     static constexpr bool REV = false;
     static constexpr int IN_ARRAYS = 2;  // u, previous iterate
-    struct Params {
-        const float* w;
-        const S* u;
-        const S* h0;
-        const S* yold;
-        S* ynew;
-        uint32_t* resid;
-    };
+    using Params = DeerParams<S>;
     struct Regs {
         Pack<S, VEC> u[R];
         Pack<S, VEC> yo[R + 1];  // previous iterate at rows t0-1 .. t0+R-1 (row -1 is h0)
@@ -130,29 +133,26 @@ struct DeerOp {
     }
 };
 
+template <typename S, bool VP, int M>
+using DeerOpT = DeerOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_DEER, sizeof(S) == 2, M).NW,
+                       kcfg(OP_DEER, sizeof(S) == 2, M).R>;
+
 template <typename S, bool VP>
-using DeerOpT = DeerOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_DEER, sizeof(S) == 2).NW,
-                       kcfg(OP_DEER, sizeof(S) == 2).R>;
+static cudaError_t deer_t(const float* w, const void* u, const void* h0, const void* yold,
+                          void* ynew, uint32_t* resid, const Geom& g, const Carry& cr,
+                          cudaStream_t s) {
+    return launch_persist<DeerOpT<S, VP, CARRY_CHAIN>, DeerOpT<S, VP, CARRY_WALK>>(
+        {w, (const S*)u, (const S*)h0, (const S*)yold, (S*)ynew, resid}, g, cr, s);
+}
 
 cudaError_t launch_deer_iter(int dtype, bool vec, const float* w, const void* u, const void* h0,
                              const void* yold, void* ynew, uint32_t* resid, const Geom& g,
                              const Carry& cr, cudaStream_t s) {
-    if (dtype == 0) {
-        const typename DeerOpT<float, true>::Params p{w, (const float*)u, (const float*)h0,
-                                                       (const float*)yold, (float*)ynew, resid};
-        return vec ? launch_persist<DeerOpT<float, true>>(p, g, cr, s)
-                   : launch_persist<DeerOpT<float, false>>(
-                         {w, (const float*)u, (const float*)h0, (const float*)yold, (float*)ynew,
-                          resid},
-                         g, cr, s);
-    }
-    using B16 = __nv_bfloat16;
-    return vec ? launch_persist<DeerOpT<B16, true>>(
-                     {w, (const B16*)u, (const B16*)h0, (const B16*)yold, (B16*)ynew, resid}, g,
-                     cr, s)
-               : launch_persist<DeerOpT<B16, false>>(
-                     {w, (const B16*)u, (const B16*)h0, (const B16*)yold, (B16*)ynew, resid}, g,
-                     cr, s);
+    if (dtype == 0)
+        return vec ? deer_t<float, true>(w, u, h0, yold, ynew, resid, g, cr, s)
+                   : deer_t<float, false>(w, u, h0, yold, ynew, resid, g, cr, s);
+    return vec ? deer_t<__nv_bfloat16, true>(w, u, h0, yold, ynew, resid, g, cr, s)
+               : deer_t<__nv_bfloat16, false>(w, u, h0, yold, ynew, resid, g, cr, s);
 }
 
 }  // namespace lrs

@@ -100,16 +100,16 @@ int leave(DevWS& ws, cudaStream_t s) {
 // Geometry + carry state for one launch of `op`.
 int plan(DevWS& ws, Op op, int dtype, bool vec, int64_t T, int64_t C, int64_t D, Geom* g,
          Carry* cr, cudaStream_t s) {
-    const TileShape ts = tile_shape(op, dtype, vec);
+    const CarryPlan cp = carry_plan(op, dtype, vec, T, C);
+    const TileShape ts = cp.ts;
     g->T = T;
     g->C = C;
     g->D = D;
-    g->n_chunks = (T + ts.L - 1) / ts.L;
-    g->n_ct = (int)((C + ts.CW - 1) / ts.CW);
+    g->n_chunks = cp.n_chunks;
     if ((C + ts.CW - 1) / ts.CW > INT32_MAX) return LR_ERR_TOO_LARGE;
+    g->n_ct = (int)((C + ts.CW - 1) / ts.CW);
     const int64_t tiles = g->n_chunks * (int64_t)g->n_ct;
-    const CarryPlan cp = carry_plan(op, dtype, g->n_chunks, C);
-    if (tiles + cp.n_walk > INT32_MAX / 2) return LR_ERR_TOO_LARGE;
+    if (tiles + cp.n_walk > INT32_MAX / 4) return LR_ERR_TOO_LARGE;
     g->n_tiles = (uint32_t)tiles;
     g->n_draws = 0;  // set by the launcher from the grid it picks
     g->ticket_base = 0;
@@ -372,7 +372,7 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
     cudaStream_t s = (cudaStream_t)stream;
     DevWS* ws;
     TRY(get_ws(&ws));
-    const TileShape ts = tile_shape(OP_SCAN_FWD, LR_F32, true);
+    const TileShape ts = tile_shape(OP_SCAN_FWD, LR_F32, true, CARRY_CHAIN);
     const int64_t T = 2 * ts.L, C = ts.CW;
     if (!ws->test_buf) {
         CK(cudaMalloc(&ws->test_buf, (size_t)(3 * T * C) * sizeof(float)));

@@ -108,6 +108,14 @@ __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
                  : "l"(p));
     return r;
 }
+__device__ __forceinline__ uint2 ld_stream_u2(const void* p) {
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ void st_u2(void* p, uint2 v) {
+    asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
 __device__ __forceinline__ void st_u4(void* p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)
@@ -144,6 +152,14 @@ struct Pack<float, VEC> {
             v[0] = __ldg(p);
         }
     }
+    __device__ __forceinline__ void load_shared(const float* p) {
+        if constexpr (VEC == 4) {
+            const float4 f = *reinterpret_cast<const float4*>(p);
+            v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+        } else {
+            v[0] = *p;
+        }
+    }
     __device__ __forceinline__ float get(int i) const { return v[i]; }
     __device__ __forceinline__ void ident(float x) {
 #pragma unroll
@@ -153,25 +169,36 @@ struct Pack<float, VEC> {
 
 template <int VEC>
 struct Pack<__nv_bfloat16, VEC> {
-    static_assert(VEC == 8 || VEC == 1, "bf16 packs hold 8 or 1 elements");
-    static constexpr int NW_ = VEC == 8 ? 4 : 1;
+    static_assert(VEC == 8 || VEC == 4 || VEC == 1, "bf16 packs hold 8, 4 or 1 elements");
+    static constexpr int NW_ = VEC == 1 ? 1 : VEC / 2;
     uint32_t w[NW_];
     __device__ __forceinline__ void load(const __nv_bfloat16* p) {
         if constexpr (VEC == 8) {
             uint4 r = ld_stream_u4(p);
             w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
+        } else if constexpr (VEC == 4) {
+            const uint2 r = ld_stream_u2(p);
+            w[0] = r.x; w[1] = r.y;
         } else {
             w[0] = (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p));
         }
     }
+    __device__ __forceinline__ void load_shared(const __nv_bfloat16* p) {
+        if constexpr (VEC == 8) {
+            const uint4 r = *reinterpret_cast<const uint4*>(p);
+            w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
+        } else {
+            w[0] = (uint32_t)*reinterpret_cast<const unsigned short*>(p);
+        }
+    }
     __device__ __forceinline__ float get(int i) const {
-        if constexpr (VEC == 8) return (i & 1) ? bf_hi(w[i >> 1]) : bf_lo(w[i >> 1]);
+        if constexpr (VEC > 1) return (i & 1) ? bf_hi(w[i >> 1]) : bf_lo(w[i >> 1]);
         else return bf_lo(w[0]);
     }
     __device__ __forceinline__ void ident(float x) {
         uint32_t b = bf_bits(x);
 #pragma unroll
-        for (int i = 0; i < NW_; ++i) w[i] = VEC == 8 ? (b | (b << 16)) : b;
+        for (int i = 0; i < NW_; ++i) w[i] = VEC > 1 ? (b | (b << 16)) : b;
     }
 };
 
@@ -188,6 +215,8 @@ __device__ __forceinline__ void store_vec(S* p, const float (&x)[VEC]) {
         if constexpr (VEC == 8)
             st_u4(p, make_uint4(bf_pack(x[0], x[1]), bf_pack(x[2], x[3]), bf_pack(x[4], x[5]),
                                 bf_pack(x[6], x[7])));
+        else if constexpr (VEC == 4)
+            st_u2(p, make_uint2(bf_pack(x[0], x[1]), bf_pack(x[2], x[3])));
         else
             *reinterpret_cast<unsigned short*>(p) = (unsigned short)bf_bits(x[0]);
     }
@@ -486,13 +515,14 @@ struct CarrySmem {
 // Whole CTA.  (A, B): this thread's aggregate over its R rows (scan order).
 // init: state before the whole scan (used by warp 0 when q == 0).  c: first
 // channel of this lane, cok: it is inside the problem.  Returns in `start` the
-// state entering this thread's first row.
+// state entering this thread's first row.  Chain protocol: publishes the
+// state after this chunk, INC(q).  Walker protocol: the tile's aggregate was
+// published by tile_publish_agg; the entering state comes from the walkers.
 template <int VEC, int NW>
 __device__ __forceinline__ void tile_carry(CarrySmem<VEC, NW>& sm, const float (&A)[VEC],
                                            const float (&B)[VEC], const float (&init)[VEC],
                                            float (&start)[VEC], const Carry& cr, const Geom& g,
-                                           int64_t q, int64_t c, bool cok,
-                                           bool publish_agg = true) {
+                                           int64_t q, int64_t c, bool cok) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
     for (int v = 0; v < VEC; ++v) {
@@ -519,12 +549,6 @@ __device__ __forceinline__ void tile_carry(CarrySmem<VEC, NW>& sm, const float (
         const bool more = q < g.n_chunks - 1;  // a later chunk needs this one's state
         const int64_t base = q * g.C + c;
         const bool walk = cr.mode == CARRY_WALK;
-        if (cok && walk && more && publish_agg) {
-#pragma unroll
-            for (int v = 0; v < VEC; ++v)
-                st_pkt2(cr.agg + 2 * ((c + v) * g.n_chunks + q), pkt(TA[v], cr.epoch),
-                        pkt(TB[v], cr.epoch));
-        }
         if (q == 0) {
             if (cok) {
 #pragma unroll
@@ -542,8 +566,10 @@ __device__ __forceinline__ void tile_carry(CarrySmem<VEC, NW>& sm, const float (
             const u64* rep = walk ? cr.inc + c_rep * g.n_chunks + q - 1 : cr.inc + (q - 1) * g.C + c_rep;
             uint32_t spins = 0, sleep_ns = 0;
             while (true) {
-                bool rep_ok = false;
-                if (lane == 0) rep_ok = pkt_ok(ld_pkt(rep), cr.epoch);
+                // chain: the states are one contiguous row, read directly (one
+                // round trip when they are there already, the common case)
+                bool rep_ok = !walk;
+                if (walk && lane == 0) rep_ok = pkt_ok(ld_pkt(rep), cr.epoch);
                 if (__shfl_sync(0xffffffffu, rep_ok, 0)) {
                     const bool ok =
                         !cok || (walk ? get_states_strided<VEC>(cr.inc + c * g.n_chunks + q - 1,

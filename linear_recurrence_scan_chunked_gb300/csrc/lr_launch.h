@@ -9,6 +9,11 @@
 
 #include "lr_common.cuh"
 
+// Consume lag of the walker-protocol kernel, in rounds of tickets.
+#ifndef LR_STREAM_LAG
+#define LR_STREAM_LAG 2
+#endif
+
 namespace lrs {
 
 struct TileShape {
@@ -21,35 +26,47 @@ enum Op { OP_SCAN_FWD = 0, OP_SCAN_BWD, OP_SRU_FWD, OP_SRU_BWD, OP_DEER, OP_COUN
 
 // Launch configuration of every kernel: NW warps per CTA, R rows per thread
 // (tile = NW*R rows), VEC channels per lane (16-byte vectors on the vector
-// path, one element on the scalar path).  R is sized so that two tiles (the
-// one being processed and the one being loaded) fit in the registers of a
-// thread at two CTAs per SM.  One table, used both to instantiate the
-// kernels and to size the workspace.
+// path, one element on the scalar path).  The chain protocol keeps two tiles
+// in registers (the one being processed and the one being loaded), the walker
+// protocol one; R is sized so that they fit in the registers of a thread at
+// two CTAs per SM.  One table, used both to instantiate the kernels and to
+// size the workspace.
 struct KCfg {
     int NW;
     int R;
 };
-constexpr KCfg kcfg(Op op, int dtype) {
-    return op == OP_SCAN_FWD ? KCfg{8, 4}
-         : op == OP_SCAN_BWD ? KCfg{8, 2}
-         : op == OP_SRU_FWD  ? KCfg{8, 2}
-         : op == OP_SRU_BWD  ? KCfg{8, 1}
-         :                     KCfg{8, 2};
+constexpr KCfg kcfg(Op op, int dtype, int mode) {
+    // bf16 holds two elements per register: twice the rows of fp32
+    return mode == CARRY_CHAIN
+               ? (op == OP_SCAN_FWD ? KCfg{8, dtype == 1 ? 8 : 4}
+                  : op == OP_SCAN_BWD ? KCfg{8, dtype == 1 ? 4 : 2}
+                  : op == OP_SRU_FWD  ? KCfg{8, dtype == 1 ? 4 : 2}
+                  : op == OP_SRU_BWD  ? KCfg{8, dtype == 1 ? 2 : 1}
+                  :                     KCfg{8, dtype == 1 ? 4 : 2})
+               : (op == OP_SCAN_FWD ? KCfg{8, 8}
+                  : op == OP_SCAN_BWD ? KCfg{8, dtype == 1 ? 8 : 4}
+                  : op == OP_SRU_FWD  ? KCfg{8, dtype == 1 ? 8 : 4}
+                  : op == OP_SRU_BWD  ? KCfg{8, dtype == 1 ? 4 : 2}
+                  :                     KCfg{8, dtype == 1 ? 8 : 4});
 }
-constexpr int kvec(int dtype, bool vec) { return vec ? (dtype == 1 ? 8 : 4) : 1; }
+// 4 channels per lane: 16-byte fp32 / 8-byte bf16 accesses, 128 channels per tile
+constexpr int kvec(int dtype, bool vec) { return vec ? 4 : 1; }
 
-inline TileShape tile_shape(Op op, int dtype, bool vec) {
-    const KCfg k = kcfg(op, dtype);
+inline TileShape tile_shape(Op op, int dtype, bool vec, int mode) {
+    const KCfg k = kcfg(op, dtype, mode);
     return TileShape{k.NW * k.R, 32 * kvec(dtype, vec), 32 * k.NW};
 }
 
-// Which carry protocol a launch uses, and the packet storage it needs.
-// WALK pays off once the chunk chain is long (a round trip per chunk would
-// dominate) and the channels are few enough for a handful of walker CTAs;
-// otherwise CHAIN.  The choice depends on the shape only, so a given problem
-// always gets the same association of its floating-point operations.
+// Which carry protocol a launch uses, its tile shape, and the packet storage
+// it needs.  WALK pays off once the chunk chain is long (a round trip per
+// chunk level would dominate) and the channels are few enough for a handful
+// of walker CTAs; otherwise CHAIN.  The choice depends on the shape only, so a
+// given problem always gets the same association of its floating-point
+// operations.
 struct CarryPlan {
     int mode;          // CARRY_CHAIN / CARRY_WALK
+    TileShape ts;      // tile shape of that protocol
+    int64_t n_chunks;  // ceil(T / ts.L)
     uint32_t n_walk;   // walker CTAs
     int wv;            // channels per walker warp
     size_t inc_elems;  // state packets: n_chunks * C
@@ -58,19 +75,33 @@ struct CarryPlan {
 constexpr int64_t kWalkMinChunks = 128;
 constexpr int64_t kWalkMaxCtas = 32;
 
-inline CarryPlan carry_plan(Op op, int dtype, int64_t n_chunks, int64_t C) {
-    CarryPlan p{CARRY_CHAIN, 0u, 0, (size_t)(n_chunks * C), 0};
-    if (n_chunks >= kWalkMinChunks) {
+inline CarryPlan carry_plan(Op op, int dtype, bool vec, int64_t T, int64_t C) {
+    CarryPlan p{};
+    const TileShape tw = tile_shape(op, dtype, vec, CARRY_WALK);
+    const int64_t nw = (T + tw.L - 1) / tw.L;
+    if (nw >= kWalkMinChunks) {
         const int wv = C <= 256 ? 1 : WALK_MAX_WV;  // spread the walkers' reads over more SMs
         const int64_t warps = (C + wv - 1) / wv;
-        const int64_t ctas = (warps + kcfg(op, dtype).NW - 1) / kcfg(op, dtype).NW;
+        const int nwarp = kcfg(op, dtype, CARRY_WALK).NW;
+        const int64_t ctas = (warps + nwarp - 1) / nwarp;
         if (ctas <= kWalkMaxCtas) {
             p.mode = CARRY_WALK;
+            p.ts = tw;
+            p.n_chunks = nw;
             p.n_walk = (uint32_t)ctas;
             p.wv = wv;
-            p.agg_elems = (size_t)(2 * n_chunks * C);
+            p.inc_elems = (size_t)(nw * C);
+            p.agg_elems = (size_t)(2 * nw * C);
+            return p;
         }
     }
+    p.mode = CARRY_CHAIN;
+    p.ts = tile_shape(op, dtype, vec, CARRY_CHAIN);
+    p.n_chunks = (T + p.ts.L - 1) / p.ts.L;
+    p.n_walk = 0;
+    p.wv = 0;
+    p.inc_elems = (size_t)(p.n_chunks * C);
+    p.agg_elems = 0;
     return p;
 }
 

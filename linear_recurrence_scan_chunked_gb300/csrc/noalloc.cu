@@ -73,14 +73,13 @@ extern "C" int lr_scan_fwd_noalloc(const void* a, const void* b, const void* h0,
     }
     if (err_dev && ((uintptr_t)err_dev % 4)) return LR_ERR_ALIGN;
 
-    const TileShape ts = tile_shape(OP_SCAN_FWD, dtype, vec);
     const int64_t C = B * D;
-    const int64_t n_chunks = (T + ts.L - 1) / ts.L;
+    const CarryPlan cp = carry_plan(OP_SCAN_FWD, dtype, vec, T, C);
+    const TileShape ts = cp.ts;
+    const int64_t n_chunks = cp.n_chunks;
     const int64_t n_ct = (C + ts.CW - 1) / ts.CW;
-    if (n_ct > INT32_MAX || n_chunks > INT32_MAX / n_ct) return LR_ERR_TOO_LARGE;
-    const CarryPlan cp = carry_plan(OP_SCAN_FWD, dtype, n_chunks, C);
+    if (n_ct > INT32_MAX || n_chunks > INT32_MAX / 4 / n_ct) return LR_ERR_TOO_LARGE;
     const size_t tiles = (size_t)(n_chunks * n_ct);
-    if (tiles + cp.n_walk > INT32_MAX / 2) return LR_ERR_TOO_LARGE;
     const size_t pk_bytes = (cp.inc_elems + cp.agg_elems) * sizeof(u64);
     if (kHeaderBytes + pk_bytes > kScratchBytes) return LR_ERR_TOO_LARGE;
 

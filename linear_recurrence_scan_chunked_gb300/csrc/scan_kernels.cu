@@ -22,18 +22,21 @@
 
 namespace lrs {
 
+template <typename S>
+struct ScanFwdParams {
+    const S* a;
+    const S* b;
+    const S* h0;
+    S* h;
+};
+
 template <typename S_, int VEC_, int NW_, int R_>
 struct ScanFwdOp {
     using S = S_;
     static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
     static constexpr bool REV = false;
     static constexpr int IN_ARRAYS = 2;  // a, b
-    struct Params {
-        const S* a;
-        const S* b;
-        const S* h0;
-        S* h;
-    };
+    using Params = ScanFwdParams<S>;
     struct Regs {
         Pack<S, VEC> a[R], b[R];
     };
@@ -84,21 +87,24 @@ struct ScanFwdOp {
     __device__ static void at_exit(const Params&, Smem&, Acc&) {}
 };
 
+template <typename S>
+struct ScanBwdParams {
+    const S* a;
+    const S* h;
+    const S* h0;
+    const S* dh;
+    S* da;
+    S* db;
+    S* dh0;
+};
+
 template <typename S_, int VEC_, int NW_, int R_>
 struct ScanBwdOp {
     using S = S_;
     static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
     static constexpr bool REV = true;
     static constexpr int IN_ARRAYS = 3;  // a, dh, h
-    struct Params {
-        const S* a;
-        const S* h;
-        const S* h0;
-        const S* dh;
-        S* da;
-        S* db;
-        S* dh0;
-    };
+    using Params = ScanBwdParams<S>;
     struct Regs {
         Pack<S, VEC> a[R], g[R], hp[R];  // a_t, dh_t, h_{t-1}
     };
@@ -165,24 +171,24 @@ struct ScanBwdOp {
     __device__ static void at_exit(const Params&, Smem&, Acc&) {}
 };
 
-template <typename S, bool VP>
-using FwdOpT = ScanFwdOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_SCAN_FWD, sizeof(S) == 2).NW,
-                         kcfg(OP_SCAN_FWD, sizeof(S) == 2).R>;
-template <typename S, bool VP>
-using BwdOpT = ScanBwdOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_SCAN_BWD, sizeof(S) == 2).NW,
-                         kcfg(OP_SCAN_BWD, sizeof(S) == 2).R>;
+template <typename S, bool VP, int M>
+using FwdOpT = ScanFwdOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_SCAN_FWD, sizeof(S) == 2, M).NW,
+                         kcfg(OP_SCAN_FWD, sizeof(S) == 2, M).R>;
+template <typename S, bool VP, int M>
+using BwdOpT = ScanBwdOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_SCAN_BWD, sizeof(S) == 2, M).NW,
+                         kcfg(OP_SCAN_BWD, sizeof(S) == 2, M).R>;
 
 template <typename S, bool VP>
 static cudaError_t scan_fwd_t(const void* a, const void* b, const void* h0, void* h, const Geom& g,
                               const Carry& cr, cudaStream_t s) {
-    return launch_persist<FwdOpT<S, VP>>({(const S*)a, (const S*)b, (const S*)h0, (S*)h}, g, cr, s);
+    return launch_persist<FwdOpT<S, VP, CARRY_CHAIN>, FwdOpT<S, VP, CARRY_WALK>>({(const S*)a, (const S*)b, (const S*)h0, (S*)h}, g, cr, s);
 }
 
 template <typename S, bool VP>
 static cudaError_t scan_bwd_t(const void* a, const void* h, const void* h0, const void* dh,
                               void* da, void* db, void* dh0, const Geom& g, const Carry& cr,
                               cudaStream_t s) {
-    return launch_persist<BwdOpT<S, VP>>({(const S*)a, (const S*)h, (const S*)h0, (const S*)dh,
+    return launch_persist<BwdOpT<S, VP, CARRY_CHAIN>, BwdOpT<S, VP, CARRY_WALK>>({(const S*)a, (const S*)h, (const S*)h0, (const S*)dh,
                                           (S*)da, (S*)db, (S*)dh0},
                                          g, cr, s);
 }

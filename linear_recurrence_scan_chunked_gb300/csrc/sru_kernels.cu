@@ -22,23 +22,26 @@ namespace lrs {
 
 __device__ __forceinline__ float sigmoidf_(float z) { return 1.f / (1.f + expf(-z)); }
 
+template <typename S>
+struct SruFwdParams {
+    const S* xt;
+    const S* uf;
+    const S* ur;
+    const S* x;
+    const float* bf;
+    const float* br;
+    const S* c0;
+    S* h;
+    S* c;
+};
+
 template <typename S_, int VEC_, int NW_, int R_>
 struct SruFwdOp {
     using S = S_;
     static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
     static constexpr bool REV = false;
     static constexpr int IN_ARRAYS = 4;  // xt, uf, ur, x
-    struct Params {
-        const S* xt;
-        const S* uf;
-        const S* ur;
-        const S* x;
-        const float* bf;
-        const float* br;
-        const S* c0;
-        S* h;
-        S* c;
-    };
+    using Params = SruFwdParams<S>;
     struct Regs {
         Pack<S, VEC> xt[R], uf[R], ur[R], x[R];
     };
@@ -117,29 +120,32 @@ struct SruFwdOp {
     __device__ static void at_exit(const Params&, Smem&, Acc&) {}
 };
 
+template <typename S>
+struct SruBwdParams {
+    const S* xt;
+    const S* uf;
+    const S* ur;
+    const S* x;
+    const float* bf;
+    const float* br;
+    const S* c0;
+    const S* c;
+    const S* dh;
+    S* dxt;
+    S* duf;
+    S* dur;
+    S* dx;
+    S* dc0;
+    float* partials;  // [2][n_chunks][C]
+};
+
 template <typename S_, int VEC_, int NW_, int R_>
 struct SruBwdOp {
     using S = S_;
     static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
     static constexpr bool REV = true;
     static constexpr int IN_ARRAYS = 7;  // xt, uf, ur, x, c, c_{t-1}, dh
-    struct Params {
-        const S* xt;
-        const S* uf;
-        const S* ur;
-        const S* x;
-        const float* bf;
-        const float* br;
-        const S* c0;
-        const S* c;
-        const S* dh;
-        S* dxt;
-        S* duf;
-        S* dur;
-        S* dx;
-        S* dc0;
-        float* partials;  // [2][n_chunks][C]
-    };
+    using Params = SruBwdParams<S>;
     struct Regs {
         Pack<S, VEC> xt[R], uf[R], ur[R], x[R], c[R], cp[R], dh[R];
     };
@@ -303,18 +309,18 @@ __global__ void __launch_bounds__(256)
     dbr[d] = sr;
 }
 
-template <typename S, bool VP>
-using SruFwdOpT = SruFwdOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_SRU_FWD, sizeof(S) == 2).NW,
-                           kcfg(OP_SRU_FWD, sizeof(S) == 2).R>;
-template <typename S, bool VP>
-using SruBwdOpT = SruBwdOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_SRU_BWD, sizeof(S) == 2).NW,
-                           kcfg(OP_SRU_BWD, sizeof(S) == 2).R>;
+template <typename S, bool VP, int M>
+using SruFwdOpT = SruFwdOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_SRU_FWD, sizeof(S) == 2, M).NW,
+                           kcfg(OP_SRU_FWD, sizeof(S) == 2, M).R>;
+template <typename S, bool VP, int M>
+using SruBwdOpT = SruBwdOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_SRU_BWD, sizeof(S) == 2, M).NW,
+                           kcfg(OP_SRU_BWD, sizeof(S) == 2, M).R>;
 
 template <typename S, bool VP>
 static cudaError_t sru_fwd_t(const void* xt, const void* uf, const void* ur, const void* x,
                              const float* bf, const float* br, const void* c0, void* h, void* c,
                              const Geom& g, const Carry& cr, cudaStream_t s) {
-    return launch_persist<SruFwdOpT<S, VP>>({(const S*)xt, (const S*)uf, (const S*)ur,
+    return launch_persist<SruFwdOpT<S, VP, CARRY_CHAIN>, SruFwdOpT<S, VP, CARRY_WALK>>({(const S*)xt, (const S*)uf, (const S*)ur,
                                              (const S*)x, bf, br, (const S*)c0, (S*)h, (S*)c},
                                             g, cr, s);
 }
@@ -324,7 +330,7 @@ static cudaError_t sru_bwd_t(const void* xt, const void* uf, const void* ur, con
                              const float* bf, const float* br, const void* c0, const void* c,
                              const void* dh, void* dxt, void* duf, void* dur, void* dx, void* dc0,
                              float* partials, const Geom& g, const Carry& cr, cudaStream_t s) {
-    return launch_persist<SruBwdOpT<S, VP>>(
+    return launch_persist<SruBwdOpT<S, VP, CARRY_CHAIN>, SruBwdOpT<S, VP, CARRY_WALK>>(
         {(const S*)xt, (const S*)uf, (const S*)ur, (const S*)x, bf, br, (const S*)c0, (const S*)c,
          (const S*)dh, (S*)dxt, (S*)duf, (S*)dur, (S*)dx, (S*)dc0, partials},
         g, cr, s);
