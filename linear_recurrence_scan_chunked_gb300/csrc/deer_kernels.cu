@@ -52,7 +52,17 @@ struct DeerOp {
     __device__ static void acc_init(Acc& a) { a.mx = 0; }
     __device__ static const S* init_ptr(const Params& p) { return p.h0; }
 
-    __device__ static void load(const Params& p, const Geom& g, const TileCoord& tc, Regs& rg) {
+    static constexpr int TMA_N = 2;  // staged: u, previous iterate (rows t0-1 .. t0+L-1)
+    __host__ __device__ static constexpr int tma_shift(int k) { return k == 1 ? -1 : 0; }
+    __host__ __device__ static constexpr int tma_extra(int k) { return k == 1 ? 1 : 0; }
+    static void tma_arrays(const Params& p, const void** ptr) {
+        ptr[0] = p.u;
+        ptr[1] = p.yold;  // nullptr on the first iteration: not staged
+    }
+
+    template <class Src>
+    __device__ static void load(const Src& src, const Params& p, const Geom& g,
+                                const TileCoord& tc, Regs& rg) {
 #pragma unroll
         for (int i = 0; i <= R; ++i) {
             const int64_t t = tc.t0 - 1 + i;
@@ -60,13 +70,13 @@ struct DeerOp {
             else if (t < 0) {
                 if (p.h0 != nullptr) rg.yo[i].load(p.h0 + tc.c);
                 else rg.yo[i].ident(0.f);
-            } else if (p.yold != nullptr) rg.yo[i].load(p.yold + t * g.C + tc.c);
+            } else if (p.yold != nullptr) src.ld(rg.yo[i], 1, p.yold, t);
             else rg.yo[i].ident(0.f);
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int64_t t = tc.t0 + r;
-            if (tc.cok && t < g.T) rg.u[r].load(p.u + t * g.C + tc.c);
+            if (tc.cok && t < g.T) src.ld(rg.u[r], 0, p.u, t);
             else rg.u[r].ident(0.f);
         }
     }
@@ -123,7 +133,7 @@ struct DeerOp {
             mx = o > mx ? o : mx;
         }
         if (lane == 0) xs.mx[warp] = mx;
-        __syncthreads();
+        csync<NW>();
         if (threadIdx.x == 0) {
             uint32_t m = 0;
 #pragma unroll
@@ -141,7 +151,8 @@ template <typename S, bool VP>
 static cudaError_t deer_t(const float* w, const void* u, const void* h0, const void* yold,
                           void* ynew, uint32_t* resid, const Geom& g, const Carry& cr,
                           cudaStream_t s) {
-    return launch_persist<DeerOpT<S, VP, CARRY_CHAIN>, DeerOpT<S, VP, CARRY_WALK>>(
+    return launch_persist<DeerOpT<S, VP, CARRY_CHAIN>, DeerOpT<S, VP, CARRY_WALK>,
+                          DeerOpT<S, VP, TILE_TMA>, kcfg(OP_DEER, sizeof(S) == 2, TILE_TMA).ST>(
         {w, (const S*)u, (const S*)h0, (const S*)yold, (S*)ynew, resid}, g, cr, s);
 }
 

@@ -9,7 +9,42 @@
 #include <vector>
 
 #include "lr_launch.h"
+#include "lr_tma.cuh"
 #include "lrscan.h"
+
+namespace lrs {
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link-time
+// dependency on the driver library).
+bool tma_encode(CUtensorMap* m, const void* ptr, int dtype, int64_t T, int64_t C, int box_c,
+                int box_rows) {
+    typedef CUresult (*encode_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static encode_fn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (encode_fn)f;
+    });
+    if (!fn) return false;
+    const size_t es = dtype == 1 ? 2 : 4;
+    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)(C * es)};
+    const cuuint32_t box[2] = {(cuuint32_t)box_c, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+              const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace lrs
 
 namespace {
 
@@ -98,9 +133,12 @@ int leave(DevWS& ws, cudaStream_t s) {
 }
 
 // Geometry + carry state for one launch of `op`.
+// tma: -1 picks the TMA-staged chain kernel whenever it applies; 0 / 1 force
+// the choice (the timeout test covers both kernels).
 int plan(DevWS& ws, Op op, int dtype, bool vec, int64_t T, int64_t C, int64_t D, Geom* g,
-         Carry* cr, cudaStream_t s) {
-    const CarryPlan cp = carry_plan(op, dtype, vec, T, C);
+         Carry* cr, cudaStream_t s, int tma = -1) {
+    const bool want_tma = tma < 0 ? use_tma(dtype, vec, T, C) : (tma == 1);
+    const CarryPlan cp = carry_plan(op, dtype, vec, want_tma, T, C);
     const TileShape ts = cp.ts;
     g->T = T;
     g->C = C;
@@ -129,6 +167,7 @@ int plan(DevWS& ws, Op op, int dtype, bool vec, int64_t T, int64_t C, int64_t D,
     cr->mode = cp.mode;
     cr->n_walk = cp.n_walk;
     cr->wv = cp.wv;
+    cr->tma = cp.tma ? 1 : 0;
     return LR_OK;
 }
 
@@ -339,6 +378,9 @@ int lr_last_error(void) {
     uint32_t bits = 0;
     CK(cudaMemcpy(&bits, ws->words + 1, sizeof bits, cudaMemcpyDeviceToHost));
     CK(cudaMemset(ws->words + 1, 0, sizeof(uint32_t)));
+    // a launch that gave up may have stopped drawing tickets before the
+    // drawer that resets the counter: reset it here (nothing is in flight)
+    if (bits) CK(cudaMemset(ws->words, 0, sizeof(uint32_t)));
     if (bits & ERRBIT_TIMEOUT) return LR_ERR_TIMEOUT;
     return LR_OK;
 }
@@ -372,26 +414,33 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
     cudaStream_t s = (cudaStream_t)stream;
     DevWS* ws;
     TRY(get_ws(&ws));
-    const TileShape ts = tile_shape(OP_SCAN_FWD, LR_F32, true, CARRY_CHAIN);
-    const int64_t T = 2 * ts.L, C = ts.CW;
+    // Both chain kernels (register and TMA-staged) on a problem of two time
+    // chunks and one channel tile, each with one CTA that is handed tile 1: it
+    // waits for the state after tile 0, which nobody publishes.
+    const int64_t C = tile_shape(OP_SCAN_FWD, LR_F32, true, CARRY_CHAIN).CW;
+    int64_t Tmax = 0;
+    for (int tma = 0; tma < 2; ++tma) {
+        const int64_t L = tile_shape(OP_SCAN_FWD, LR_F32, true, tma ? TILE_TMA : CARRY_CHAIN).L;
+        if (2 * L > Tmax) Tmax = 2 * L;
+    }
     if (!ws->test_buf) {
-        CK(cudaMalloc(&ws->test_buf, (size_t)(3 * T * C) * sizeof(float)));
-        CK(cudaMemset(ws->test_buf, 0, (size_t)(3 * T * C) * sizeof(float)));
-        ws->bytes += 3 * T * C * (int64_t)sizeof(float);
+        CK(cudaMalloc(&ws->test_buf, (size_t)(3 * Tmax * C) * sizeof(float)));
+        CK(cudaMemset(ws->test_buf, 0, (size_t)(3 * Tmax * C) * sizeof(float)));
+        ws->bytes += 3 * Tmax * C * (int64_t)sizeof(float);
     }
     float* a = (float*)ws->test_buf;
-    Geom g;
-    Carry cr;
     TRY(enter(*ws, s));
-    TRY(plan(*ws, OP_SCAN_FWD, LR_F32, true, T, C, C, &g, &cr, s));
-    // One CTA, handed tile 1: it waits for the state after tile 0, which
-    // nobody publishes.
-    g.max_grid = 1;
-    g.ticket_base = 1;
-    cr.mode = CARRY_CHAIN;
-    cr.n_walk = 0;
-    cr.spin_limit = spin_limit;
-    CK(launch_scan_fwd(LR_F32, true, a, a + T * C, nullptr, a + 2 * T * C, g, cr, s));
+    for (int tma = 0; tma < 2; ++tma) {
+        const int64_t T = 2 * tile_shape(OP_SCAN_FWD, LR_F32, true, tma ? TILE_TMA : CARRY_CHAIN).L;
+        Geom g;
+        Carry cr;
+        TRY(plan(*ws, OP_SCAN_FWD, LR_F32, true, T, C, C, &g, &cr, s, tma));
+        if (cr.mode != CARRY_CHAIN || cr.tma != tma) return LR_ERR_INVALID_ARG;
+        g.max_grid = 1;
+        g.ticket_base = 1;
+        cr.spin_limit = spin_limit;
+        CK(launch_scan_fwd(LR_F32, true, a, a + Tmax * C, nullptr, a + 2 * Tmax * C, g, cr, s));
+    }
     return leave(*ws, s);
 }
 

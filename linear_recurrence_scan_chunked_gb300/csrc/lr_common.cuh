@@ -70,6 +70,7 @@ struct Carry {
     int mode;             // CARRY_CHAIN or CARRY_WALK
     uint32_t n_walk;      // walker CTAs (first tickets); 0 in CHAIN mode
     int wv;               // channels per walker warp (WALK)
+    int tma;              // CHAIN: tiles are staged by TMA (k_tchain)
 };
 
 struct Geom {
@@ -83,6 +84,14 @@ struct Geom {
     uint32_t ticket_base; // added to every ticket (the timeout test starts past tile 0)
     uint32_t max_grid;    // 0, or an upper bound on the CTAs launched (timeout test)
 };
+
+// Barrier of the NW consumer warps of a CTA (named barrier 1).  The scan
+// kernels that stage tiles with TMA add a producer warp that never takes part
+// in the tile arithmetic; in the other kernels NW*32 is the whole CTA.
+template <int NW>
+__device__ __forceinline__ void csync() {
+    asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
+}
 
 // ------------------------------------------------------------- memory ops
 
@@ -187,6 +196,9 @@ struct Pack<__nv_bfloat16, VEC> {
         if constexpr (VEC == 8) {
             const uint4 r = *reinterpret_cast<const uint4*>(p);
             w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
+        } else if constexpr (VEC == 4) {
+            const uint2 r = *reinterpret_cast<const uint2*>(p);
+            w[0] = r.x; w[1] = r.y;
         } else {
             w[0] = (uint32_t)*reinterpret_cast<const unsigned short*>(p);
         }
@@ -529,7 +541,7 @@ __device__ __forceinline__ void tile_carry(CarrySmem<VEC, NW>& sm, const float (
         sm.a[warp][lane][v] = A[v];
         sm.b[warp][lane][v] = B[v];
     }
-    __syncthreads();
+    csync<NW>();
     if (warp == 0) {
         float TA[VEC], TB[VEC];
 #pragma unroll
@@ -594,7 +606,7 @@ __device__ __forceinline__ void tile_carry(CarrySmem<VEC, NW>& sm, const float (
 #pragma unroll
         for (int v = 0; v < VEC; ++v) sm.carry[lane][v] = cin[v];
     }
-    __syncthreads();
+    csync<NW>();
     float PA[VEC], PB[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) { PA[v] = 1.f; PB[v] = 0.f; }
@@ -613,6 +625,51 @@ __device__ __forceinline__ void tile_carry(CarrySmem<VEC, NW>& sm, const float (
     for (int v = 0; v < VEC; ++v) start[v] = __fmaf_rn(PA[v], sm.carry[lane][v], PB[v]);
 }
 
+// Shared memory of the strip kernel's carry: every warp's aggregate and the
+// state entering every warp's first row.
+template <int VEC, int NW>
+struct StripSmem {
+    float a[NW][32][VEC];
+    float b[NW][32][VEC];
+    float start[NW][32][VEC];
+};
+
+// Whole CTA, strip kernel.  (A, B): this thread's aggregate over its R rows.
+// The state before this chunk is `init` (first chunk) or this CTA's state
+// after the previous chunk of the same channel strip (`carry`, [32][VEC] in
+// shared memory); warp 0 folds the warp aggregates into it in row order,
+// leaving each warp's entering state in shared memory and the state after
+// the chunk in `carry`.  Returns in `start` the state entering this thread's
+// first row.  The association is fixed by position: bitwise reproducible.
+template <int VEC, int NW>
+__device__ __forceinline__ void strip_carry(StripSmem<VEC, NW>& sm, const float (&A)[VEC],
+                                            const float (&B)[VEC], const float (&init)[VEC],
+                                            float (&start)[VEC], float (*carry)[VEC], bool first,
+                                            bool cok) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+        sm.a[warp][lane][v] = A[v];
+        sm.b[warp][lane][v] = B[v];
+    }
+    csync<NW>();
+    if (warp == 0) {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            float st = first ? (cok ? init[v] : 0.f) : carry[lane][v];
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                sm.start[w][lane][v] = st;
+                st = __fmaf_rn(sm.a[w][lane][v], st, sm.b[w][lane][v]);
+            }
+            carry[lane][v] = st;
+        }
+    }
+    csync<NW>();
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) start[v] = sm.start[warp][lane][v];
+}
+
 // Whole CTA, walker protocol, look-ahead phase: combine the warp aggregates
 // of a tile and publish the tile aggregate (no wait, no output).
 template <int VEC, int NW>
@@ -625,7 +682,7 @@ __device__ __forceinline__ void tile_publish_agg(CarrySmem<VEC, NW>& sm, const f
         sm.a[warp][lane][v] = A[v];
         sm.b[warp][lane][v] = B[v];
     }
-    __syncthreads();
+    csync<NW>();
     if (warp == 0 && cok && q < g.n_chunks - 1) {
         float TA[VEC], TB[VEC];
 #pragma unroll
@@ -643,7 +700,7 @@ __device__ __forceinline__ void tile_publish_agg(CarrySmem<VEC, NW>& sm, const f
             st_pkt2(cr.agg + 2 * ((c + v) * g.n_chunks + q), pkt(TA[v], cr.epoch),
                     pkt(TB[v], cr.epoch));
     }
-    __syncthreads();  // the smem is reused by the next phase
+    csync<NW>();  // the smem is reused by the next phase
 }
 
 }  // namespace lrs

@@ -14,6 +14,11 @@
 #define LR_STREAM_LAG 2
 #endif
 
+// Register cap of the TMA-staged kernel: two CTAs of NW+1 = 9 warps per SM.
+#ifndef LR_TMA_MAXNREG
+#define LR_TMA_MAXNREG 112
+#endif
+
 namespace lrs {
 
 struct TileShape {
@@ -26,35 +31,57 @@ enum Op { OP_SCAN_FWD = 0, OP_SCAN_BWD, OP_SRU_FWD, OP_SRU_BWD, OP_DEER, OP_COUN
 
 // Launch configuration of every kernel: NW warps per CTA, R rows per thread
 // (tile = NW*R rows), VEC channels per lane (16-byte vectors on the vector
-// path, one element on the scalar path).  The chain protocol keeps two tiles
-// in registers (the one being processed and the one being loaded), the walker
-// protocol one; R is sized so that they fit in the registers of a thread at
-// two CTAs per SM.  One table, used both to instantiate the kernels and to
-// size the workspace.
+// path, one element on the scalar path), and for the TMA-staged chain kernel
+// ST shared-memory stages.  The register chain kernel keeps two tiles in
+// registers (the one being processed and the one being loaded), the walker
+// kernel one; R is sized so that they fit in the registers of a thread at two
+// CTAs per SM.  The TMA kernel keeps one tile in registers and ST in shared
+// memory (about 96 KB of stages per CTA, two CTAs per SM).  One table, used
+// both to instantiate the kernels and to size the workspace.
+constexpr int TILE_TMA = 2;  // kcfg row of the TMA-staged chain kernel
 struct KCfg {
     int NW;
     int R;
+    int ST;
 };
 constexpr KCfg kcfg(Op op, int dtype, int mode) {
     // bf16 holds two elements per register: twice the rows of fp32
     return mode == CARRY_CHAIN
-               ? (op == OP_SCAN_FWD ? KCfg{8, dtype == 1 ? 8 : 4}
-                  : op == OP_SCAN_BWD ? KCfg{8, dtype == 1 ? 4 : 2}
-                  : op == OP_SRU_FWD  ? KCfg{8, dtype == 1 ? 4 : 2}
-                  : op == OP_SRU_BWD  ? KCfg{8, dtype == 1 ? 2 : 1}
-                  :                     KCfg{8, dtype == 1 ? 4 : 2})
-               : (op == OP_SCAN_FWD ? KCfg{8, 8}
-                  : op == OP_SCAN_BWD ? KCfg{8, dtype == 1 ? 8 : 4}
-                  : op == OP_SRU_FWD  ? KCfg{8, dtype == 1 ? 8 : 4}
-                  : op == OP_SRU_BWD  ? KCfg{8, dtype == 1 ? 4 : 2}
-                  :                     KCfg{8, dtype == 1 ? 8 : 4});
+               ? (op == OP_SCAN_FWD ? KCfg{8, dtype == 1 ? 8 : 4, 0}
+                  : op == OP_SCAN_BWD ? KCfg{8, dtype == 1 ? 4 : 2, 0}
+                  : op == OP_SRU_FWD  ? KCfg{8, dtype == 1 ? 4 : 2, 0}
+                  : op == OP_SRU_BWD  ? KCfg{8, dtype == 1 ? 2 : 1, 0}
+                  :                     KCfg{8, dtype == 1 ? 4 : 2, 0})
+           : mode == CARRY_WALK
+               ? (op == OP_SCAN_FWD ? KCfg{8, 8, 0}
+                  : op == OP_SCAN_BWD ? KCfg{8, dtype == 1 ? 8 : 4, 0}
+                  : op == OP_SRU_FWD  ? KCfg{8, dtype == 1 ? 8 : 4, 0}
+                  : op == OP_SRU_BWD  ? KCfg{8, dtype == 1 ? 4 : 2, 0}
+                  :                     KCfg{8, dtype == 1 ? 8 : 4, 0})
+               : (op == OP_SCAN_FWD ? KCfg{8, dtype == 1 ? 8 : 4, 3}
+                  : op == OP_SCAN_BWD ? KCfg{8, dtype == 1 ? 8 : 4, 2}
+                  : op == OP_SRU_FWD  ? KCfg{8, dtype == 1 ? 4 : 2, 3}
+                  : op == OP_SRU_BWD  ? KCfg{8, dtype == 1 ? 2 : 1, 3}
+                  :                     KCfg{8, dtype == 1 ? 8 : 4, 3});
 }
 // 4 channels per lane: 16-byte fp32 / 8-byte bf16 accesses, 128 channels per tile
 constexpr int kvec(int dtype, bool vec) { return vec ? 4 : 1; }
 
+// mode: CARRY_CHAIN, CARRY_WALK or TILE_TMA (chain protocol, TMA staging)
 inline TileShape tile_shape(Op op, int dtype, bool vec, int mode) {
     const KCfg k = kcfg(op, dtype, mode);
     return TileShape{k.NW * k.R, 32 * kvec(dtype, vec), 32 * k.NW};
+}
+
+// The chain protocol stages its tiles with TMA when the vector path applies
+// and the rows of the [T, C] sequence are 16-byte multiples (tensor-map
+// strides) and at least one channel tile wide, with coordinates inside int32.  The tile height of the TMA kernel
+// can differ from the register kernel's, so this choice, like the protocol,
+// is fixed by the shape and the buffers' alignment of a call.
+inline bool use_tma(int dtype, bool vec, int64_t T, int64_t C) {
+    const int64_t es = dtype == 1 ? 2 : 4;
+    return vec && (C * es) % 16 == 0 && C >= 128 && T < ((int64_t)1 << 30) &&
+           C < ((int64_t)1 << 30);
 }
 
 // Which carry protocol a launch uses, its tile shape, and the packet storage
@@ -65,6 +92,7 @@ inline TileShape tile_shape(Op op, int dtype, bool vec, int mode) {
 // operations.
 struct CarryPlan {
     int mode;          // CARRY_CHAIN / CARRY_WALK
+    bool tma;          // CHAIN: the TMA-staged kernel runs it
     TileShape ts;      // tile shape of that protocol
     int64_t n_chunks;  // ceil(T / ts.L)
     uint32_t n_walk;   // walker CTAs
@@ -73,9 +101,13 @@ struct CarryPlan {
     size_t agg_elems;  // aggregate packets (WALK): 2 * n_chunks * C
 };
 constexpr int64_t kWalkMinChunks = 128;
+// Channel strips from which the strip kernel runs a chain-protocol launch
+// (one CTA per strip or more strips per CTA; fewer strips would leave SMs
+// idle, and the chain kernel spreads the chunks of few strips over all SMs).
+constexpr int64_t kStripMinStrips = 128;
 constexpr int64_t kWalkMaxCtas = 32;
 
-inline CarryPlan carry_plan(Op op, int dtype, bool vec, int64_t T, int64_t C) {
+inline CarryPlan carry_plan(Op op, int dtype, bool vec, bool tma, int64_t T, int64_t C) {
     CarryPlan p{};
     const TileShape tw = tile_shape(op, dtype, vec, CARRY_WALK);
     const int64_t nw = (T + tw.L - 1) / tw.L;
@@ -96,7 +128,8 @@ inline CarryPlan carry_plan(Op op, int dtype, bool vec, int64_t T, int64_t C) {
         }
     }
     p.mode = CARRY_CHAIN;
-    p.ts = tile_shape(op, dtype, vec, CARRY_CHAIN);
+    p.tma = tma && vec;
+    p.ts = tile_shape(op, dtype, vec, p.tma ? TILE_TMA : CARRY_CHAIN);
     p.n_chunks = (T + p.ts.L - 1) / p.ts.L;
     p.n_walk = 0;
     p.wv = 0;

@@ -19,9 +19,12 @@
 //   at_exit(p, sm, acc)           once per tile CTA after its last tile
 #pragma once
 
+#include <string.h>
+
 #include <type_traits>
 
 #include "lr_launch.h"
+#include "lr_tma.cuh"
 
 namespace lrs {
 
@@ -51,6 +54,14 @@ __device__ __forceinline__ TileCoord tile_coord(const Geom& g, uint32_t tile) {
 template <class Op>
 __device__ __forceinline__ int64_t row_t(const TileCoord& tc, int r) {
     return Op::REV ? tc.t0 - r : tc.t0 + r;
+}
+
+// Issue the global loads of one tile (register kernels).
+template <class Op>
+__device__ __forceinline__ void gload(const typename Op::Params& p, const Geom& g, uint32_t tile,
+                                      typename Op::Regs& rg) {
+    const TileCoord tc = tile_coord<Op>(g, tile);
+    Op::load(GlobalSrc{g.C, tc.c}, p, g, tc, rg);
 }
 
 // The streaming kernel of the walker protocol.  Every CTA draws tickets; the
@@ -97,14 +108,14 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
         typename Op::Work w;
         if (x < g.n_tiles) {  // reduce: publish the aggregate
             const TileCoord tc = tile_coord<Op>(g, x);
-            Op::load(p, g, tc, regs);
+            Op::load(GlobalSrc{g.C, tc.c}, p, g, tc, regs);
             float A[VEC], B[VEC];
             Op::aggregate(p, g, tc, regs, w, A, B, false);
             tile_publish_agg<VEC, Op::NW>(sm, A, B, cr, g, tc.q, tc.c, tc.cok);
         }
         if (x >= d_con && x - d_con < g.n_tiles) {  // consume
             const TileCoord tc = tile_coord<Op>(g, x - d_con);
-            Op::load(p, g, tc, regs);
+            Op::load(GlobalSrc{g.C, tc.c}, p, g, tc, regs);
             float A[VEC], B[VEC];
             Op::aggregate(p, g, tc, regs, w, A, B, true);
             float init[VEC];
@@ -127,17 +138,15 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
 // loads of tile i+1 are in flight and the ticket of tile i+2 is being drawn.
 // The chunk chain costs about one round trip per chunk level, hidden behind
 // the tiles of the other channel tiles.
+// Whole consumer CTA: one tile whose data is in registers -- local scan,
+// state entering the tile (chain protocol), output pass.
 template <class Op>
-__device__ __forceinline__ uint32_t chain_tile(const typename Op::Params& p, const Geom& g,
-                                               const Carry& cr, uint32_t tile,
-                                               const typename Op::Regs& regs,
-                                               CarrySmem<Op::VEC, Op::NW>& sm,
-                                               typename Op::Smem& xs, typename Op::Acc& acc,
-                                               bool draw, uint32_t* s_ticket) {
+__device__ __forceinline__ void tile_process(const typename Op::Params& p, const Geom& g,
+                                             const Carry& cr, const TileCoord& tc,
+                                             const typename Op::Regs& regs,
+                                             CarrySmem<Op::VEC, Op::NW>& sm,
+                                             typename Op::Smem& xs, typename Op::Acc& acc) {
     constexpr int VEC = Op::VEC;
-    uint32_t next = 0;
-    if (draw && threadIdx.x == 0) next = atomicAdd(cr.ticket, 1u);  // latency hidden by the tile
-    const TileCoord tc = tile_coord<Op>(g, tile);
     float A[VEC], B[VEC];
     typename Op::Work w;
     Op::aggregate(p, g, tc, regs, w, A, B, true);
@@ -150,6 +159,18 @@ __device__ __forceinline__ uint32_t chain_tile(const typename Op::Params& p, con
     float s[VEC];
     tile_carry<VEC, Op::NW>(sm, A, B, init, s, cr, g, tc.q, tc.c, tc.cok);
     Op::finish(p, g, tc, regs, w, s, xs, acc);
+}
+
+template <class Op>
+__device__ __forceinline__ uint32_t chain_tile(const typename Op::Params& p, const Geom& g,
+                                               const Carry& cr, uint32_t tile,
+                                               const typename Op::Regs& regs,
+                                               CarrySmem<Op::VEC, Op::NW>& sm,
+                                               typename Op::Smem& xs, typename Op::Acc& acc,
+                                               bool draw, uint32_t* s_ticket) {
+    uint32_t next = 0;
+    if (draw && threadIdx.x == 0) next = atomicAdd(cr.ticket, 1u);  // latency hidden by the tile
+    tile_process<Op>(p, g, cr, tile_coord<Op>(g, tile), regs, sm, xs, acc);
     if (draw && threadIdx.x == 0) {
         if (next == g.n_draws - 1) atomicExch(cr.ticket, 0u);
         *s_ticket = next + g.ticket_base;
@@ -177,7 +198,7 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
     Op::acc_init(acc);
     typename Op::Regs r0, r1;
     uint32_t t0 = tk;
-    Op::load(p, g, tile_coord<Op>(g, t0), r0);
+    gload<Op>(p, g, t0, r0);
     __syncthreads();
     if (threadIdx.x == 0) {
         const uint32_t t = atomicAdd(cr.ticket, 1u);
@@ -190,20 +211,221 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
         // tile t0 is loaded (r0); tk is the ticket of the next tile
         bool more = tk < limit;
         const uint32_t t1 = tk;
-        if (more) {
-            Op::load(p, g, tile_coord<Op>(g, t1), r1);
-        }
+        if (more) gload<Op>(p, g, t1, r1);
         tk = chain_tile<Op>(p, g, cr, t0, r0, sm, xs, acc, more, &s_ticket);
         if (!more) break;
         more = tk < limit;
         t0 = tk;
-        if (more) {
-                    Op::load(p, g, tile_coord<Op>(g, t0), r0);
-        }
+        if (more) gload<Op>(p, g, t0, r0);
         tk = chain_tile<Op>(p, g, cr, t1, r1, sm, xs, acc, more, &s_ticket);
         if (!more) break;
     }
     Op::at_exit(p, xs, acc);
+}
+
+// Chain protocol with TMA staging.  Warp NW is the producer: its lane 0 draws
+// the tickets (in order) and, for each tile, issues one box load per input
+// array into the next free stage of a ring of ST stages.  Warps 0 .. NW-1
+// consume the stages in the same order: copy the tile from shared memory into
+// registers, hand the stage back, then scan it as the register kernel does.
+// The consumers release a stage before they wait for the tile's carry, so up
+// to ST tiles stream in while one waits.
+//
+// Every CTA consumes its tickets in ticket order and every drawn ticket
+// belongs to a resident CTA, so the smallest unfinished tile can always
+// finish: no wait is circular.  Every wait is bounded: a consumer that gives
+// up on a stage sets the shared abort flag, and the consumers decide to stop
+// together, after a barrier; the producer waits for its copies in flight
+// before it exits.
+template <class Op, int ST>
+__device__ __forceinline__ void tma_produce(const Geom& g, const Carry& cr, const TmaDesc& td,
+                                            unsigned char* ring, uint64_t* full, uint64_t* empty,
+                                            uint32_t* s_tile) {
+    constexpr int L = Op::NW * Op::R, CW = 32 * Op::VEC;
+    constexpr uint32_t SB = tma_stage_bytes<Op>();
+    uint32_t k = 0;          // stage uses so far
+    bool last_plain = false; // use k was the final (tile-less) arrival
+    for (;; ++k) {
+        const uint32_t st = k % ST;
+        const uint32_t t = atomicAdd(cr.ticket, 1u);  // latency overlaps the wait below
+        if (t == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+        if (k >= ST && !mbar_wait(&empty[st], ((k / ST) - 1u) & 1u, cr.err)) {
+            atomicOr(cr.err, ERRBIT_TIMEOUT);
+            break;
+        }
+        const uint32_t tile = t + g.ticket_base;
+        s_tile[st] = tile;
+        if (tile >= g.n_tiles) {
+            mbar_arrive(&full[st]);
+            last_plain = true;
+            break;
+        }
+        mbar_arrive_tx(&full[st], td.tx_bytes);
+        const int64_t q = tile / g.n_ct, j = tile % g.n_ct;
+        const int64_t tchunk = Op::REV ? g.n_chunks - 1 - q : q;
+        const int32_t x = (int32_t)(j * CW), y0 = (int32_t)(tchunk * L);
+        unsigned char* dst = ring + st * SB;
+#pragma unroll
+        for (int a = 0; a < Op::TMA_N; ++a)
+            if (td.present & (1u << a))
+                tma_load_2d(dst + tma_off<Op>(a), &td.map[a], x, y0 + Op::tma_shift(a), &full[st]);
+    }
+    // Uses [k - ST + last_plain, k) may still have copies in flight (the stage
+    // of use k - ST was handed back before a final arrival on it).
+    const uint32_t lo = k + (last_plain ? 1u : 0u) > ST ? k + (last_plain ? 1u : 0u) - ST : 0u;
+    for (uint32_t i = lo; i < k; ++i) mbar_wait(&full[i % ST], (i / ST) & 1u, cr.err);
+}
+
+template <class Op, int ST>
+__global__ void __maxnreg__(LR_TMA_MAXNREG)
+    k_tchain(typename Op::Params p, Geom g, Carry cr, const __grid_constant__ TmaDesc td) {
+    constexpr int NW = Op::NW, VEC = Op::VEC, L = Op::NW * Op::R;
+    constexpr uint32_t SB = tma_stage_bytes<Op>();
+    extern __shared__ unsigned char dyn_smem[];
+    // TMA destinations: 128-byte aligned (the launch adds 128 bytes of slack)
+    unsigned char* ring = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~(uintptr_t)127);
+    __shared__ CarrySmem<VEC, NW> sm;
+    __shared__ typename Op::Smem xs;
+    __shared__ __align__(8) uint64_t full[ST], empty[ST];
+    __shared__ uint32_t s_tile[ST];
+    __shared__ uint32_t s_abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < ST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NW);
+        }
+        s_abort = 0;
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (warp == NW) {
+        if (lane == 0) tma_produce<Op, ST>(g, cr, td, ring, full, empty, s_tile);
+        return;
+    }
+    typename Op::Acc acc;
+    Op::acc_init(acc);
+    for (uint32_t k = 0;; ++k) {
+        const uint32_t st = k % ST;
+        if (!mbar_wait(&full[st], (k / ST) & 1u, cr.err)) {
+            s_abort = 1;
+            atomicOr(cr.err, ERRBIT_TIMEOUT);
+        }
+        csync<NW>();  // the decision below is the same in every consumer
+        const uint32_t tile = s_tile[st];
+        if (s_abort != 0 || tile >= g.n_tiles) break;
+        const TileCoord tc = tile_coord<Op>(g, tile);
+        typename Op::Regs regs;
+        Op::load(SmemSrc<Op>{ring + st * SB, tc.tchunk * L, lane * VEC}, p, g, tc, regs);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+        tile_process<Op>(p, g, cr, tc, regs, sm, xs, acc);
+    }
+    Op::at_exit(p, xs, acc);
+}
+
+// Strip kernel (chain protocol, wide problems): CTA b owns the channel
+// strips j = b, b + G, b + 2G, ... (G CTAs) and walks them through time,
+// chunk level by chunk level: (0, j1), (0, j2), ..., (1, j1), ...  The state
+// after each chunk of a strip stays in this CTA's shared memory, so no tile
+// waits for another CTA and nothing is drawn or polled; the tile sequence of
+// every CTA is fixed in advance.  Thread 0 keeps ST - 1 tiles of that
+// sequence streaming in through the TMA ring: at the top of each iteration,
+// after the barrier that also tells it that every warp has copied the
+// previous tile into registers, it re-arms that tile's stage with the tile ST
+// - 1 ahead.  All warps compute (no producer warp), so two CTAs of 8 warps
+// fit an SM with up to 128 registers a thread.
+constexpr int STRIP_MAX = 64;  // strips per CTA (state kept in shared memory)
+
+template <class Op>
+__device__ __forceinline__ uint32_t strip_tile(const Geom& g, uint32_t G, uint32_t m, uint32_t it) {
+    const uint32_t q = it / m, i = it % m;
+    return q * (uint32_t)g.n_ct + blockIdx.x + i * G;
+}
+
+// Thread 0: stage `it % ST` <- the tiles of use `it` (one box per array).
+template <class Op, int ST>
+__device__ __forceinline__ void strip_issue(const Geom& g, const TmaDesc& td, unsigned char* ring,
+                                            uint64_t* full, uint32_t G, uint32_t m, uint32_t it) {
+    constexpr int L = Op::NW * Op::R, CW = 32 * Op::VEC;
+    constexpr uint32_t SB = tma_stage_bytes<Op>();
+    const uint32_t st = it % ST;
+    const uint32_t tile = strip_tile<Op>(g, G, m, it);
+    const int64_t q = tile / g.n_ct, j = tile % g.n_ct;
+    const int64_t tchunk = Op::REV ? g.n_chunks - 1 - q : q;
+    const int32_t x = (int32_t)(j * CW), y0 = (int32_t)(tchunk * L);
+    mbar_arrive_tx(&full[st], td.tx_bytes);
+    unsigned char* dst = ring + st * SB;
+#pragma unroll
+    for (int a = 0; a < Op::TMA_N; ++a)
+        if (td.present & (1u << a))
+            tma_load_2d(dst + tma_off<Op>(a), &td.map[a], x, y0 + Op::tma_shift(a), &full[st]);
+}
+
+template <class Op, int ST>
+__global__ void __launch_bounds__(Op::NW * 32, 2)
+    k_strip(typename Op::Params p, Geom g, uint32_t* err, uint32_t G,
+            const __grid_constant__ TmaDesc td) {
+    constexpr int NW = Op::NW, VEC = Op::VEC, L = Op::NW * Op::R;
+    constexpr uint32_t SB = tma_stage_bytes<Op>();
+    extern __shared__ unsigned char dyn_smem[];
+    unsigned char* ring = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~(uintptr_t)127);
+    __shared__ StripSmem<VEC, NW> sm;
+    __shared__ typename Op::Smem xs;
+    __shared__ __align__(8) uint64_t full[ST];
+    __shared__ uint32_t s_abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // strips of this CTA: j = blockIdx.x + i*G < n_ct; their states follow the ring
+    const uint32_t m = ((uint32_t)g.n_ct - blockIdx.x + G - 1) / G;
+    const uint32_t n_it = m * (uint32_t)g.n_chunks;
+    float(*carry)[32][VEC] = reinterpret_cast<float(*)[32][VEC]>(ring + ST * SB);
+    uint32_t issued = 0;  // thread 0: uses whose loads were issued
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < ST; ++i) mbar_init(&full[i], 1);
+        s_abort = 0;
+        mbar_init_fence();
+        for (; issued < (uint32_t)ST && issued < n_it; ++issued)
+            strip_issue<Op, ST>(g, td, ring, full, G, m, issued);
+    }
+    __syncthreads();
+    typename Op::Acc acc;
+    Op::acc_init(acc);
+    uint32_t it = 0;
+    for (; it < n_it; ++it) {
+        const uint32_t st = it % ST;
+        if (!mbar_wait(&full[st], (it / ST) & 1u, err)) {
+            s_abort = 1;
+            atomicOr(err, ERRBIT_TIMEOUT);
+        }
+        // every warp is done with the previous tile (its stage is free), and
+        // the stop decision below is the same in every warp
+        csync<NW>();
+        if (s_abort != 0) break;
+        if (threadIdx.x == 0 && it > 0 && issued < n_it) {
+            strip_issue<Op, ST>(g, td, ring, full, G, m, issued);  // into stage (it-1) % ST
+            ++issued;
+        }
+        const TileCoord tc = tile_coord<Op>(g, strip_tile<Op>(g, G, m, it));
+        typename Op::Regs regs;
+        Op::load(SmemSrc<Op>{ring + st * SB, tc.tchunk * L, lane * VEC}, p, g, tc, regs);
+        float A[VEC], B[VEC];
+        typename Op::Work w;
+        Op::aggregate(p, g, tc, regs, w, A, B, true);
+        float init[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) init[v] = 0.f;
+        const typename Op::S* ip = Op::init_ptr(p);
+        if (tc.q == 0 && warp == 0 && ip != nullptr && tc.cok)
+            load_vec<typename Op::S, VEC>(ip + tc.c, init);
+        float s[VEC];
+        strip_carry<VEC, NW>(sm, A, B, init, s, carry[it % m], tc.q == 0, tc.cok);
+        Op::finish(p, g, tc, regs, w, s, xs, acc);
+    }
+    Op::at_exit(p, xs, acc);
+    if (threadIdx.x == 0)  // after an early stop: copies still in flight land first
+        for (uint32_t i = it; i < issued; ++i) mbar_wait(&full[i % ST], (i / ST) & 1u, err);
 }
 
 template <class Op>
@@ -269,14 +491,118 @@ cudaError_t launch_stream(const typename Op::Params& p, Geom g, const Carry& cr,
     return cudaGetLastError();
 }
 
-// Host: launch the kernel of the launch's carry protocol; OpC / OpW are the
-// operation instantiated with the chain / walker tile shapes.
-template <class OpC, class OpW>
+// Host: launch k_tchain<Op, ST> (chain protocol, TMA staging).  One tensor
+// map per staged array; the ring takes ST stages of dynamic shared memory.
+template <class Op, int ST>
+cudaError_t launch_tchain(const typename Op::Params& p, Geom g, const Carry& cr, cudaStream_t s) {
+    constexpr int L = Op::NW * Op::R, CW = 32 * Op::VEC;
+    constexpr size_t dyn = (size_t)ST * tma_stage_bytes<Op>() + 128;
+    static_assert(Op::TMA_N <= TMA_MAX_ARR, "too many staged arrays");
+    static_assert(L + 1 <= 256 && CW <= 256, "a TMA box holds at most 256 rows and columns");
+    TmaDesc td;
+    memset(&td, 0, sizeof td);
+    const void* ptr[TMA_MAX_ARR] = {};
+    Op::tma_arrays(p, ptr);
+    for (int a = 0; a < Op::TMA_N; ++a) {
+        if (!ptr[a]) continue;
+        if (!tma_encode(&td.map[a], ptr[a], sizeof(typename Op::S) == 2 ? 1 : 0, g.T, g.C, CW,
+                        L + Op::tma_extra(a)))
+            return cudaErrorInvalidValue;
+        td.present |= 1u << a;
+        td.tx_bytes += tma_arr_bytes<Op>(a);
+    }
+    static int occ[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int& o = occ[dev & 63];
+    if (o <= 0) {
+        cudaError_t e = cudaFuncSetAttribute(k_tchain<Op, ST>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k_tchain<Op, ST>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_tchain<Op, ST>, 32 * (Op::NW + 1),
+                                                          dyn) != cudaSuccess ||
+            n <= 0)
+            n = 1;
+        o = n;
+    }
+    const uint32_t grid = persist_grid(g, cr, o);
+    g.n_draws = g.n_tiles + grid - g.ticket_base;
+    k_tchain<Op, ST><<<grid, 32 * (Op::NW + 1), dyn, s>>>(p, g, cr, td);
+    return cudaGetLastError();
+}
+
+// Host: launch k_strip<Op, ST> when the problem has enough channel strips to
+// give every resident CTA the same number of them (at most STRIP_MAX);
+// returns cudaErrorNotSupported otherwise (the caller takes the chain kernel).
+template <class Op, int ST>
+cudaError_t launch_strip(const typename Op::Params& p, const Geom& g, const Carry& cr,
+                         cudaStream_t s) {
+    constexpr int L = Op::NW * Op::R, CW = 32 * Op::VEC;
+    constexpr size_t ring = (size_t)ST * tma_stage_bytes<Op>() + 128;
+    constexpr size_t strip_bytes = 32 * Op::VEC * sizeof(float);
+    static int occ[64] = {0}, n_sm[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int& o = occ[dev & 63];
+    if (o <= 0) {
+        cudaError_t e = cudaFuncSetAttribute(k_strip<Op, ST>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(ring + STRIP_MAX * strip_bytes));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k_strip<Op, ST>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        int n = 0;  // residency for up to two strips per CTA
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_strip<Op, ST>, 32 * Op::NW,
+                                                          ring + 2 * strip_bytes) != cudaSuccess ||
+            n <= 0)
+            n = 1;
+        o = n;
+        cudaDeviceGetAttribute(&n_sm[dev & 63], cudaDevAttrMultiProcessorCount, dev);
+    }
+    const int64_t slots = (int64_t)o * (n_sm[dev & 63] > 0 ? n_sm[dev & 63] : 1);
+    if (g.n_ct < kStripMinStrips || g.n_ct > slots * STRIP_MAX || g.max_grid != 0)
+        return cudaErrorNotSupported;
+    const int64_t m = (g.n_ct + slots - 1) / slots;
+    const uint32_t G = (uint32_t)((g.n_ct + m - 1) / m);
+    TmaDesc td;
+    memset(&td, 0, sizeof td);
+    const void* ptr[TMA_MAX_ARR] = {};
+    Op::tma_arrays(p, ptr);
+    for (int a = 0; a < Op::TMA_N; ++a) {
+        if (!ptr[a]) continue;
+        if (!tma_encode(&td.map[a], ptr[a], sizeof(typename Op::S) == 2 ? 1 : 0, g.T, g.C, CW,
+                        L + Op::tma_extra(a)))
+            return cudaErrorInvalidValue;
+        td.present |= 1u << a;
+        td.tx_bytes += tma_arr_bytes<Op>(a);
+    }
+    // no CTA waits for another, so the grid need not be co-resident
+    k_strip<Op, ST><<<G, 32 * Op::NW, ring + (size_t)m * strip_bytes, s>>>(p, g, cr.err, G, td);
+    return cudaGetLastError();
+}
+
+// Host: launch the kernel of the launch's carry protocol; OpC / OpW / OpT are
+// the operation instantiated with the tile shapes of the register chain, the
+// walker and the TMA chain kernels.
+template <class OpC, class OpW, class OpT, int ST>
 cudaError_t launch_persist(const typename OpC::Params& p, const Geom& g, const Carry& cr,
                            cudaStream_t s) {
-    static_assert(std::is_same<typename OpC::Params, typename OpW::Params>::value,
-                  "both instantiations take the same arguments");
-    if (cr.mode == CARRY_CHAIN) return launch_chain<OpC>(p, g, cr, s);
+    static_assert(std::is_same<typename OpC::Params, typename OpW::Params>::value &&
+                      std::is_same<typename OpC::Params, typename OpT::Params>::value,
+                  "all instantiations take the same arguments");
+    if (cr.mode == CARRY_CHAIN) {
+        if (cr.tma) {
+            const cudaError_t e = launch_strip<OpT, ST>(p, g, cr, s);
+            if (e != cudaErrorNotSupported) return e;
+            return launch_tchain<OpT, ST>(p, g, cr, s);
+        }
+        return launch_chain<OpC>(p, g, cr, s);
+    }
     return launch_stream<OpW>(p, g, cr, s);
 }
 

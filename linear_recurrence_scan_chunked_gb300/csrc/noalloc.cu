@@ -74,7 +74,7 @@ extern "C" int lr_scan_fwd_noalloc(const void* a, const void* b, const void* h0,
     if (err_dev && ((uintptr_t)err_dev % 4)) return LR_ERR_ALIGN;
 
     const int64_t C = B * D;
-    const CarryPlan cp = carry_plan(OP_SCAN_FWD, dtype, vec, T, C);
+    const CarryPlan cp = carry_plan(OP_SCAN_FWD, dtype, vec, use_tma(dtype, vec, T, C), T, C);
     const TileShape ts = cp.ts;
     const int64_t n_chunks = cp.n_chunks;
     const int64_t n_ct = (C + ts.CW - 1) / ts.CW;
@@ -122,6 +122,7 @@ extern "C" int lr_scan_fwd_noalloc(const void* a, const void* b, const void* h0,
     cr.mode = cp.mode;
     cr.n_walk = cp.n_walk;
     cr.wv = cp.wv;
+    cr.tma = cp.tma ? 1 : 0;
     if (launch_scan_fwd(dtype, vec, a, b, h0, h, g, cr, s) != cudaSuccess) return LR_ERR_CUDA;
     return LR_OK;
 }

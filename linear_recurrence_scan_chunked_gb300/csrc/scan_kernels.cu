@@ -48,13 +48,23 @@ struct ScanFwdOp {
     __device__ static void acc_init(Acc&) {}
     __device__ static const S* init_ptr(const Params& p) { return p.h0; }
 
-    __device__ static void load(const Params& p, const Geom& g, const TileCoord& tc, Regs& rg) {
+    static constexpr int TMA_N = 2;  // staged: a, b
+    __host__ __device__ static constexpr int tma_shift(int) { return 0; }
+    __host__ __device__ static constexpr int tma_extra(int) { return 0; }
+    static void tma_arrays(const Params& p, const void** ptr) {
+        ptr[0] = p.a;
+        ptr[1] = p.b;
+    }
+
+    template <class Src>
+    __device__ static void load(const Src& src, const Params& p, const Geom& g,
+                                const TileCoord& tc, Regs& rg) {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int64_t t = tc.t0 + r;
             if (tc.cok && t < g.T) {
-                rg.a[r].load(p.a + t * g.C + tc.c);
-                rg.b[r].load(p.b + t * g.C + tc.c);
+                src.ld(rg.a[r], 0, p.a, t);
+                src.ld(rg.b[r], 1, p.b, t);
             } else {  // identity element (1, 0) outside the problem
                 rg.a[r].ident(1.f);
                 rg.b[r].ident(0.f);
@@ -116,14 +126,25 @@ struct ScanBwdOp {
     __device__ static void acc_init(Acc&) {}
     __device__ static const S* init_ptr(const Params&) { return nullptr; }  // u_T = 0
 
-    __device__ static void load(const Params& p, const Geom& g, const TileCoord& tc, Regs& rg) {
+    static constexpr int TMA_N = 3;  // staged: a, dh, h (rows shifted by one: h_{t-1})
+    __host__ __device__ static constexpr int tma_shift(int k) { return k == 2 ? -1 : 0; }
+    __host__ __device__ static constexpr int tma_extra(int) { return 0; }
+    static void tma_arrays(const Params& p, const void** ptr) {
+        ptr[0] = p.a;
+        ptr[1] = p.dh;
+        ptr[2] = p.h;
+    }
+
+    template <class Src>
+    __device__ static void load(const Src& src, const Params& p, const Geom& g,
+                                const TileCoord& tc, Regs& rg) {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int64_t t = tc.t0 - r;
             if (tc.cok && t < g.T) {
-                rg.a[r].load(p.a + t * g.C + tc.c);
-                rg.g[r].load(p.dh + t * g.C + tc.c);
-                if (t > 0) rg.hp[r].load(p.h + (t - 1) * g.C + tc.c);
+                src.ld(rg.a[r], 0, p.a, t);
+                src.ld(rg.g[r], 1, p.dh, t);
+                if (t > 0) src.ld(rg.hp[r], 2, p.h, t - 1);
                 else if (p.h0 != nullptr) rg.hp[r].load(p.h0 + tc.c);
                 else rg.hp[r].ident(0.f);
             } else {
@@ -181,16 +202,18 @@ using BwdOpT = ScanBwdOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_SCAN_BWD, sizeof(S
 template <typename S, bool VP>
 static cudaError_t scan_fwd_t(const void* a, const void* b, const void* h0, void* h, const Geom& g,
                               const Carry& cr, cudaStream_t s) {
-    return launch_persist<FwdOpT<S, VP, CARRY_CHAIN>, FwdOpT<S, VP, CARRY_WALK>>({(const S*)a, (const S*)b, (const S*)h0, (S*)h}, g, cr, s);
+    return launch_persist<FwdOpT<S, VP, CARRY_CHAIN>, FwdOpT<S, VP, CARRY_WALK>,
+                          FwdOpT<S, VP, TILE_TMA>, kcfg(OP_SCAN_FWD, sizeof(S) == 2, TILE_TMA).ST>(
+        {(const S*)a, (const S*)b, (const S*)h0, (S*)h}, g, cr, s);
 }
 
 template <typename S, bool VP>
 static cudaError_t scan_bwd_t(const void* a, const void* h, const void* h0, const void* dh,
                               void* da, void* db, void* dh0, const Geom& g, const Carry& cr,
                               cudaStream_t s) {
-    return launch_persist<BwdOpT<S, VP, CARRY_CHAIN>, BwdOpT<S, VP, CARRY_WALK>>({(const S*)a, (const S*)h, (const S*)h0, (const S*)dh,
-                                          (S*)da, (S*)db, (S*)dh0},
-                                         g, cr, s);
+    return launch_persist<BwdOpT<S, VP, CARRY_CHAIN>, BwdOpT<S, VP, CARRY_WALK>,
+                          BwdOpT<S, VP, TILE_TMA>, kcfg(OP_SCAN_BWD, sizeof(S) == 2, TILE_TMA).ST>(
+        {(const S*)a, (const S*)h, (const S*)h0, (const S*)dh, (S*)da, (S*)db, (S*)dh0}, g, cr, s);
 }
 
 cudaError_t launch_scan_fwd(int dtype, bool vec, const void* a, const void* b, const void* h0,

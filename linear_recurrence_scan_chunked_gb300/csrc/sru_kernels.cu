@@ -55,16 +55,27 @@ struct SruFwdOp {
     __device__ static void acc_init(Acc&) {}
     __device__ static const S* init_ptr(const Params& p) { return p.c0; }
 
-    __device__ static void load(const Params& p, const Geom& g, const TileCoord& tc, Regs& rg) {
+    static constexpr int TMA_N = 4;  // staged: xt, uf, ur, x
+    __host__ __device__ static constexpr int tma_shift(int) { return 0; }
+    __host__ __device__ static constexpr int tma_extra(int) { return 0; }
+    static void tma_arrays(const Params& p, const void** ptr) {
+        ptr[0] = p.xt;
+        ptr[1] = p.uf;
+        ptr[2] = p.ur;
+        ptr[3] = p.x;
+    }
+
+    template <class Src>
+    __device__ static void load(const Src& src, const Params& p, const Geom& g,
+                                const TileCoord& tc, Regs& rg) {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int64_t t = tc.t0 + r;
             if (tc.cok && t < g.T) {
-                const int64_t o = t * g.C + tc.c;
-                rg.xt[r].load(p.xt + o);
-                rg.uf[r].load(p.uf + o);
-                rg.ur[r].load(p.ur + o);
-                rg.x[r].load(p.x + o);
+                src.ld(rg.xt[r], 0, p.xt, t);
+                src.ld(rg.uf[r], 1, p.uf, t);
+                src.ld(rg.ur[r], 2, p.ur, t);
+                src.ld(rg.x[r], 3, p.x, t);
             } else {
                 rg.xt[r].ident(0.f);
                 rg.uf[r].ident(0.f);
@@ -161,19 +172,32 @@ struct SruBwdOp {
     __device__ static void acc_init(Acc&) {}
     __device__ static const S* init_ptr(const Params&) { return nullptr; }  // u_T = 0
 
-    __device__ static void load(const Params& p, const Geom& g, const TileCoord& tc, Regs& rg) {
+    static constexpr int TMA_N = 6;  // staged: xt, uf, ur, x, dh, c (rows t0-1 .. t0+L-1)
+    __host__ __device__ static constexpr int tma_shift(int k) { return k == 5 ? -1 : 0; }
+    __host__ __device__ static constexpr int tma_extra(int k) { return k == 5 ? 1 : 0; }
+    static void tma_arrays(const Params& p, const void** ptr) {
+        ptr[0] = p.xt;
+        ptr[1] = p.uf;
+        ptr[2] = p.ur;
+        ptr[3] = p.x;
+        ptr[4] = p.dh;
+        ptr[5] = p.c;
+    }
+
+    template <class Src>
+    __device__ static void load(const Src& src, const Params& p, const Geom& g,
+                                const TileCoord& tc, Regs& rg) {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int64_t t = tc.t0 - r;
             if (tc.cok && t < g.T) {
-                const int64_t o = t * g.C + tc.c;
-                rg.xt[r].load(p.xt + o);
-                rg.uf[r].load(p.uf + o);
-                rg.ur[r].load(p.ur + o);
-                rg.x[r].load(p.x + o);
-                rg.c[r].load(p.c + o);
-                rg.dh[r].load(p.dh + o);
-                if (t > 0) rg.cp[r].load(p.c + o - g.C);
+                src.ld(rg.xt[r], 0, p.xt, t);
+                src.ld(rg.uf[r], 1, p.uf, t);
+                src.ld(rg.ur[r], 2, p.ur, t);
+                src.ld(rg.x[r], 3, p.x, t);
+                src.ld(rg.dh[r], 4, p.dh, t);
+                src.ld(rg.c[r], 5, p.c, t);
+                if (t > 0) src.ld(rg.cp[r], 5, p.c, t - 1);
                 else if (p.c0 != nullptr) rg.cp[r].load(p.c0 + tc.c);
                 else rg.cp[r].ident(0.f);
             } else {
@@ -259,7 +283,7 @@ struct SruBwdOp {
             xs.pf[warp][lane][v] = sum_f[v];
             xs.pr[warp][lane][v] = w.sum_r[v];
         }
-        __syncthreads();
+        csync<NW>();
         if (warp == 0 && tc.cok) {
             float pf[VEC], pr[VEC];
 #pragma unroll
@@ -320,9 +344,10 @@ template <typename S, bool VP>
 static cudaError_t sru_fwd_t(const void* xt, const void* uf, const void* ur, const void* x,
                              const float* bf, const float* br, const void* c0, void* h, void* c,
                              const Geom& g, const Carry& cr, cudaStream_t s) {
-    return launch_persist<SruFwdOpT<S, VP, CARRY_CHAIN>, SruFwdOpT<S, VP, CARRY_WALK>>({(const S*)xt, (const S*)uf, (const S*)ur,
-                                             (const S*)x, bf, br, (const S*)c0, (S*)h, (S*)c},
-                                            g, cr, s);
+    return launch_persist<SruFwdOpT<S, VP, CARRY_CHAIN>, SruFwdOpT<S, VP, CARRY_WALK>,
+                          SruFwdOpT<S, VP, TILE_TMA>, kcfg(OP_SRU_FWD, sizeof(S) == 2, TILE_TMA).ST>(
+        {(const S*)xt, (const S*)uf, (const S*)ur, (const S*)x, bf, br, (const S*)c0, (S*)h, (S*)c},
+        g, cr, s);
 }
 
 template <typename S, bool VP>
@@ -330,7 +355,8 @@ static cudaError_t sru_bwd_t(const void* xt, const void* uf, const void* ur, con
                              const float* bf, const float* br, const void* c0, const void* c,
                              const void* dh, void* dxt, void* duf, void* dur, void* dx, void* dc0,
                              float* partials, const Geom& g, const Carry& cr, cudaStream_t s) {
-    return launch_persist<SruBwdOpT<S, VP, CARRY_CHAIN>, SruBwdOpT<S, VP, CARRY_WALK>>(
+    return launch_persist<SruBwdOpT<S, VP, CARRY_CHAIN>, SruBwdOpT<S, VP, CARRY_WALK>,
+                          SruBwdOpT<S, VP, TILE_TMA>, kcfg(OP_SRU_BWD, sizeof(S) == 2, TILE_TMA).ST>(
         {(const S*)xt, (const S*)uf, (const S*)ur, (const S*)x, bf, br, (const S*)c0, (const S*)c,
          (const S*)dh, (S*)dxt, (S*)duf, (S*)dur, (S*)dx, (S*)dc0, partials},
         g, cr, s);

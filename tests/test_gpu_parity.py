@@ -17,6 +17,10 @@ pytestmark = pytest.mark.gpu
 SHAPES = [(1, 1, 4), (5, 2, 8), (64, 1, 128), (65, 1, 128), (200, 3, 96), (1000, 2, 64),
           (333, 4, 40), (77, 3, 5), (513, 1, 129), (2048, 2, 256), (3, 1, 1)]
 LONG = [(100003, 1, 4), (20000, 1, 128)]
+# wide problems (at least 128 channel tiles) run the strip kernel: one strip
+# per CTA with a ragged last strip, and two strips per CTA (more strips than
+# resident CTAs)
+WIDE = [(70, 33, 520), (45, 40, 1000)]
 
 
 def _scan_case(cuda, T, B, D, dtype, seed=0):
@@ -34,13 +38,13 @@ def _scan_case(cuda, T, B, D, dtype, seed=0):
     assert_close("dh0", to_f64(dh0), rdh0, dtype)
 
 
-@pytest.mark.parametrize("shape", SHAPES + LONG)
+@pytest.mark.parametrize("shape", SHAPES + LONG + WIDE)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_scan_fwd_bwd(cuda, shape, dtype):
     _scan_case(cuda, *shape, dtype)
 
 
-@pytest.mark.parametrize("shape", SHAPES[:9])
+@pytest.mark.parametrize("shape", SHAPES[:9] + WIDE)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_sru_fwd_bwd(cuda, shape, dtype):
     T, B, D = shape
@@ -62,7 +66,8 @@ def test_sru_fwd_bwd(cuda, shape, dtype):
         assert_close(k, to_f64(g[k]), r, dtype)
 
 
-@pytest.mark.parametrize("shape", [(1, 1, 4), (64, 2, 8), (300, 3, 40), (77, 2, 5), (5000, 1, 128)])
+@pytest.mark.parametrize("shape", [(1, 1, 4), (64, 2, 8), (300, 3, 40), (77, 2, 5), (5000, 1, 128)]
+                         + WIDE)
 @pytest.mark.parametrize("dtype", ["f32"])
 def test_deer(cuda, shape, dtype):
     T, B, D = shape
@@ -146,8 +151,9 @@ def test_empty_problems(cuda):
     assert (k, st) == (0, cuda.LR_OK)
 
 
-def test_repeat_is_bitwise_deterministic(cuda):
-    T, B, D = 2048, 4, 256
+@pytest.mark.parametrize("shape", [(2048, 4, 256), (64, 40, 1000)])
+def test_repeat_is_bitwise_deterministic(cuda, shape):
+    T, B, D = shape
     wl = W.like(W.SRU, T, B, D, "f32")
     inp = W.make_inputs(wl, 4)
     dv = dev_inputs(inp, "f32")
