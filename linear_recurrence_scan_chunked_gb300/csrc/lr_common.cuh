@@ -70,7 +70,7 @@ struct Carry {
     int mode;             // CARRY_CHAIN or CARRY_WALK
     uint32_t n_walk;      // walker CTAs (first tickets); 0 in CHAIN mode
     int wv;               // channels per walker warp (WALK)
-    int tma;              // CHAIN: tiles are staged by TMA (k_tchain)
+    int tma;              // CHAIN: tiles are staged by TMA (k_strip / k_tchain)
 };
 
 struct Geom {
@@ -122,6 +122,43 @@ __device__ __forceinline__ uint2 ld_stream_u2(const void* p) {
     asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
     return r;
 }
+// L2 eviction-priority policies (createpolicy) and loads that carry one: the
+// walker-protocol kernel reads every tile twice, and the second read should
+// find it in L2.
+__device__ __forceinline__ uint64_t l2_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint4 ld_hint_u4(const void* p, uint64_t pol) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p), "l"(pol));
+    return r;
+}
+__device__ __forceinline__ uint2 ld_hint_u2(const void* p, uint64_t pol) {
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
+                 : "=r"(r.x), "=r"(r.y)
+                 : "l"(p), "l"(pol));
+    return r;
+}
+__device__ __forceinline__ uint32_t ld_hint_b32(const void* p, uint64_t pol) {
+    uint32_t r;
+    asm volatile("ld.global.nc.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(r) : "l"(p), "l"(pol));
+    return r;
+}
+__device__ __forceinline__ uint32_t ld_hint_u16(const void* p, uint64_t pol) {
+    unsigned short r;
+    asm volatile("ld.global.nc.L2::cache_hint.u16 %0, [%1], %2;" : "=h"(r) : "l"(p), "l"(pol));
+    return (uint32_t)r;
+}
 __device__ __forceinline__ void st_u2(void* p, uint2 v) {
     asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
@@ -161,6 +198,15 @@ struct Pack<float, VEC> {
             v[0] = __ldg(p);
         }
     }
+    __device__ __forceinline__ void load_hint(const float* p, uint64_t pol) {
+        if constexpr (VEC == 4) {
+            uint4 r = ld_hint_u4(p, pol);
+            v[0] = __uint_as_float(r.x); v[1] = __uint_as_float(r.y);
+            v[2] = __uint_as_float(r.z); v[3] = __uint_as_float(r.w);
+        } else {
+            v[0] = __uint_as_float(ld_hint_b32(p, pol));
+        }
+    }
     __device__ __forceinline__ void load_shared(const float* p) {
         if constexpr (VEC == 4) {
             const float4 f = *reinterpret_cast<const float4*>(p);
@@ -190,6 +236,17 @@ struct Pack<__nv_bfloat16, VEC> {
             w[0] = r.x; w[1] = r.y;
         } else {
             w[0] = (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p));
+        }
+    }
+    __device__ __forceinline__ void load_hint(const __nv_bfloat16* p, uint64_t pol) {
+        if constexpr (VEC == 8) {
+            uint4 r = ld_hint_u4(p, pol);
+            w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
+        } else if constexpr (VEC == 4) {
+            const uint2 r = ld_hint_u2(p, pol);
+            w[0] = r.x; w[1] = r.y;
+        } else {
+            w[0] = ld_hint_u16(p, pol);
         }
     }
     __device__ __forceinline__ void load_shared(const __nv_bfloat16* p) {

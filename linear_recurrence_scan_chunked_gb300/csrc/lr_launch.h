@@ -92,7 +92,7 @@ inline bool use_tma(int dtype, bool vec, int64_t T, int64_t C) {
 // operations.
 struct CarryPlan {
     int mode;          // CARRY_CHAIN / CARRY_WALK
-    bool tma;          // CHAIN: the TMA-staged kernel runs it
+    bool tma;          // CHAIN: a TMA-staged kernel runs it (strip / TMA chain)
     TileShape ts;      // tile shape of that protocol
     int64_t n_chunks;  // ceil(T / ts.L)
     uint32_t n_walk;   // walker CTAs
@@ -109,6 +109,7 @@ constexpr int64_t kWalkMaxCtas = 32;
 
 inline CarryPlan carry_plan(Op op, int dtype, bool vec, bool tma, int64_t T, int64_t C) {
     CarryPlan p{};
+    tma = tma && vec;
     const TileShape tw = tile_shape(op, dtype, vec, CARRY_WALK);
     const int64_t nw = (T + tw.L - 1) / tw.L;
     if (nw >= kWalkMinChunks) {
@@ -118,6 +119,7 @@ inline CarryPlan carry_plan(Op op, int dtype, bool vec, bool tma, int64_t T, int
         const int64_t ctas = (warps + nwarp - 1) / nwarp;
         if (ctas <= kWalkMaxCtas) {
             p.mode = CARRY_WALK;
+            p.tma = false;  // the walker kernel loads through the registers
             p.ts = tw;
             p.n_chunks = nw;
             p.n_walk = (uint32_t)ctas;
@@ -128,7 +130,7 @@ inline CarryPlan carry_plan(Op op, int dtype, bool vec, bool tma, int64_t T, int
         }
     }
     p.mode = CARRY_CHAIN;
-    p.tma = tma && vec;
+    p.tma = tma;
     p.ts = tile_shape(op, dtype, vec, p.tma ? TILE_TMA : CARRY_CHAIN);
     p.n_chunks = (T + p.ts.L - 1) / p.ts.L;
     p.n_walk = 0;

@@ -88,15 +88,19 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
     Op::acc_init(acc);
     const uint32_t limit = cr.n_walk + g.n_tiles + d_con;
     bool tile_role = false;
+    if (threadIdx.x == 0) {
+        const uint32_t t = atomicAdd(cr.ticket, 1u);
+        if (t == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+        s_ticket = t + g.ticket_base;
+    }
+    __syncthreads();
+    uint32_t tk = s_ticket;
     while (true) {
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const uint32_t t = atomicAdd(cr.ticket, 1u);
-            if (t == g.n_draws - 1) atomicExch(cr.ticket, 0u);
-            s_ticket = t + g.ticket_base;
-        }
-        __syncthreads();
-        const uint32_t tk = s_ticket;
+        // the next ticket is drawn now and read after this one's work (a tile
+        // CTA; a walker returns before it draws again)
+        uint32_t next = 0;
+        const bool draw = tk >= cr.n_walk && tk < limit;
+        if (draw && threadIdx.x == 0) next = atomicAdd(cr.ticket, 1u);
         if (tk < cr.n_walk) {  // walker role
             walker<typename Op::S, Op::NW>(cr, g, tk, Op::init_ptr(p));
             return;
@@ -108,14 +112,14 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
         typename Op::Work w;
         if (x < g.n_tiles) {  // reduce: publish the aggregate
             const TileCoord tc = tile_coord<Op>(g, x);
-            Op::load(GlobalSrc{g.C, tc.c}, p, g, tc, regs);
+            Op::load(GlobalSrcHint{g.C, tc.c, l2_evict_last()}, p, g, tc, regs);
             float A[VEC], B[VEC];
             Op::aggregate(p, g, tc, regs, w, A, B, false);
             tile_publish_agg<VEC, Op::NW>(sm, A, B, cr, g, tc.q, tc.c, tc.cok);
         }
-        if (x >= d_con && x - d_con < g.n_tiles) {  // consume
+        if (x >= d_con && x - d_con < g.n_tiles) {  // consume (the tile's last read)
             const TileCoord tc = tile_coord<Op>(g, x - d_con);
-            Op::load(GlobalSrc{g.C, tc.c}, p, g, tc, regs);
+            Op::load(GlobalSrcHint{g.C, tc.c, l2_evict_first()}, p, g, tc, regs);
             float A[VEC], B[VEC];
             Op::aggregate(p, g, tc, regs, w, A, B, true);
             float init[VEC];
@@ -128,6 +132,12 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
             tile_carry<VEC, Op::NW>(sm, A, B, init, s, cr, g, tc.q, tc.c, tc.cok);
             Op::finish(p, g, tc, regs, w, s, xs, acc);
         }
+        if (draw && threadIdx.x == 0) {
+            if (next == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+            s_ticket = next + g.ticket_base;
+        }
+        __syncthreads();
+        tk = s_ticket;
     }
     if (tile_role) Op::at_exit(p, xs, acc);
 }
@@ -588,7 +598,7 @@ cudaError_t launch_strip(const typename Op::Params& p, const Geom& g, const Carr
 
 // Host: launch the kernel of the launch's carry protocol; OpC / OpW / OpT are
 // the operation instantiated with the tile shapes of the register chain, the
-// walker and the TMA chain kernels.
+// walker and the TMA-staged kernels (strip, TMA chain).
 template <class OpC, class OpW, class OpT, int ST>
 cudaError_t launch_persist(const typename OpC::Params& p, const Geom& g, const Carry& cr,
                            cudaStream_t s) {

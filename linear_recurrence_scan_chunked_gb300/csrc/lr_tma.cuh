@@ -138,6 +138,17 @@ struct GlobalSrc {
     }
 };
 
+// Global loads carrying an L2 eviction-priority policy.
+struct GlobalSrcHint {
+    int64_t C;
+    int64_t c;
+    uint64_t pol;
+    template <class P, typename S>
+    __device__ __forceinline__ void ld(P& pk, int, const S* base, int64_t t) const {
+        pk.load_hint(base + t * C + c, pol);
+    }
+};
+
 template <class Op>
 struct SmemSrc {
     const unsigned char* stage;

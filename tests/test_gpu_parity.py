@@ -44,7 +44,7 @@ def test_scan_fwd_bwd(cuda, shape, dtype):
     _scan_case(cuda, *shape, dtype)
 
 
-@pytest.mark.parametrize("shape", SHAPES[:9] + WIDE)
+@pytest.mark.parametrize("shape", SHAPES[:9] + WIDE + [(6001, 1, 256)])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_sru_fwd_bwd(cuda, shape, dtype):
     T, B, D = shape
@@ -66,8 +66,8 @@ def test_sru_fwd_bwd(cuda, shape, dtype):
         assert_close(k, to_f64(g[k]), r, dtype)
 
 
-@pytest.mark.parametrize("shape", [(1, 1, 4), (64, 2, 8), (300, 3, 40), (77, 2, 5), (5000, 1, 128)]
-                         + WIDE)
+@pytest.mark.parametrize("shape", [(1, 1, 4), (64, 2, 8), (300, 3, 40), (77, 2, 5), (5000, 1, 128),
+                                   (9000, 2, 512)] + WIDE)
 @pytest.mark.parametrize("dtype", ["f32"])
 def test_deer(cuda, shape, dtype):
     T, B, D = shape
