@@ -38,21 +38,28 @@
  *  - All pointers are DEVICE pointers owned by the caller; the library never
  *    frees or retains them.  Inputs are read-only.  No output may alias an
  *    input or another output.  Pointers must be aligned to the element size;
- *    16-byte alignment plus D a multiple of 4 (fp32) or 8 (bf16) selects the
- *    128-bit vector path, anything else the scalar path.
+ *    16-byte alignment plus D a multiple of 4 selects the vector path (4
+ *    channels per lane: 16-byte fp32 / 8-byte bf16 accesses), anything else
+ *    the scalar path.  On the vector path, when a time row (B*D elements) is
+ *    a multiple of 16 bytes and at least 128 channels wide, tiles are staged
+ *    through shared memory by the Tensor Memory Accelerator.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
  *    asynchronous on it except deer_diag_solve, which synchronises the stream
  *    once per Newton iteration to read the residual.
  *  - Sizes: B, T, D >= 0 with B*T*D < 2^62; an empty problem is a no-op
  *    (gradients of the initial state are zeroed).
- *  - The library keeps one internal workspace per device (look-back tile
- *    descriptors, a tile ticket, an error word, DEER's second iterate buffer,
- *    SRU bias partials), grown on demand with cudaMalloc.  Calls on different
- *    streams are serialised through it with CUDA events.
+ *  - The library keeps one internal workspace per device (carry packets of
+ *    the chunk states and aggregates, a tile ticket, an error word, DEER's
+ *    second iterate buffer, SRU bias partials), grown on demand with
+ *    cudaMalloc.  Calls on different streams are serialised through it with
+ *    CUDA events.
  *  - Return value: LR_OK, or an lr_status describing an argument or launch
  *    error detected before or while enqueuing the work.  Errors detected on
- *    the device while the kernels run (a look-back wait that ran out) are
+ *    the device while the kernels run (a carry or copy wait that ran out) are
  *    recorded in a sticky device error word read by lr_last_error().
+ *  - Results are bitwise reproducible from run to run: every floating-point
+ *    association depends on the shape and on which kernel the alignment
+ *    selects, never on timing.
  */
 #ifndef LRSCAN_H
 #define LRSCAN_H
@@ -197,10 +204,11 @@ const char* lr_cuda_error_string(void);
 int64_t lr_workspace_bytes(void);
 
 /*
- * Test hook for the bounded look-back wait: launches the forward scan kernel
- * on a private 2-chunk problem whose first chunk is never published, with the
- * wait limited to `spin_limit` polls, so the second chunk's wait runs out.
- * It leaves LR_ERR_TIMEOUT in the device error word.  Nothing faults or hangs.
+ * Test hook for the bounded carry wait: launches both chain-protocol forward
+ * scan kernels (register and TMA-staged) on a private 2-chunk problem whose
+ * first chunk is never published, one CTA each, with the wait limited to
+ * `spin_limit` polls, so the second chunk's wait runs out.  It leaves
+ * LR_ERR_TIMEOUT in the device error word.  Nothing faults or hangs.
  */
 int lr_test_lookback_timeout(uint32_t spin_limit, void* stream);
 
