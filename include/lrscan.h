@@ -212,6 +212,18 @@ int64_t lr_workspace_bytes(void);
  */
 int lr_test_lookback_timeout(uint32_t spin_limit, void* stream);
 
+/*
+ * Test hook for the activations of the fused kernels: tanh_out[i] = tanh(x[i])
+ * and sigmoid_out[i] = 1 / (1 + exp(-x[i])) as the SRU and DEER kernels
+ * evaluate them (exponential forms on the hardware exponential; the pages
+ * name the functions -- [P1] SRU paragraph, [P4] "核心原理" -- not how to
+ * evaluate them).  x, tanh_out, sigmoid_out: n fp32 device values each,
+ * caller-owned.  Asynchronous on `stream`.  Returns LR_ERR_INVALID_ARG for
+ * n < 0 or a null pointer with n > 0.
+ */
+int lr_test_activations(const float* x, float* tanh_out, float* sigmoid_out, int64_t n,
+                        void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -60,8 +60,9 @@ def load():
     lib.lr_cuda_error_string.restype = ctypes.c_char_p
     lib.lr_workspace_bytes.restype = I64
     lib.lr_test_lookback_timeout.argtypes = [ctypes.c_uint32, P]
+    lib.lr_test_activations.argtypes = [P, P, P, I64, P]
     for f in ("lr_scan_fwd", "lr_scan_bwd", "sru_fwd", "sru_bwd", "deer_diag_solve",
-              "lr_last_error", "lr_test_lookback_timeout"):
+              "lr_last_error", "lr_test_lookback_timeout", "lr_test_activations"):
         getattr(lib, f).restype = I
     _lib = lib
     return lib
@@ -224,6 +225,16 @@ def last_error() -> int:
 
 def workspace_bytes() -> int:
     return int(load().lr_workspace_bytes())
+
+
+def test_activations(x, stream=None):
+    """tanh and sigmoid of a contiguous fp32 CUDA tensor as the fused kernels
+    evaluate them. Returns (tanh, sigmoid)."""
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous fp32 CUDA tensor")
+    th, sg = torch.empty_like(x), torch.empty_like(x)
+    _check(load().lr_test_activations(_p(x), _p(th), _p(sg), x.numel(), _stream(stream)))
+    return th, sg
 
 
 def test_lookback_timeout(spin_limit: int = 1000, stream=None) -> int:

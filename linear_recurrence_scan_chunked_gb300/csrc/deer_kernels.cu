@@ -14,6 +14,7 @@
 // folds max |y_t - yold_t| into one residual word (the stopping test of the
 // section "工程实现": ||y^(i+1) - y^(i)|| < eps, here the max-abs norm).
 // yold == nullptr is the all-zero initial guess (not read).
+#include "lr_act.cuh"
 #include "lr_launch.h"
 #include "lr_persist.cuh"
 
@@ -95,7 +96,7 @@ struct DeerOp {
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
                 const float yt = rg.yo[r].get(v);
-                const float th = tanhf(wv[v] * yt + rg.u[r].get(v));
+                const float th = act_tanh(wv[v] * yt + rg.u[r].get(v));
                 const float jac = wv[v] * (1.f - th * th);
                 w.J[r][v] = ok ? jac : 1.f;
                 w.Rh[r][v] = ok ? th - jac * yt : 0.f;

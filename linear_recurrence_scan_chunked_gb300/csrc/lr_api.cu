@@ -8,6 +8,7 @@
 #include <mutex>
 #include <vector>
 
+#include "lr_act.cuh"
 #include "lr_launch.h"
 #include "lr_tma.cuh"
 #include "lrscan.h"
@@ -42,6 +43,16 @@ bool tma_encode(CUtensorMap* m, const void* ptr, int dtype, int64_t T, int64_t C
               const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Test hook kernel: the activations the fused kernels use, elementwise.
+__global__ void k_test_act(const float* __restrict__ x, float* __restrict__ th,
+                           float* __restrict__ sg, int64_t n) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        th[i] = act_tanh(x[i]);
+        sg[i] = act_sigmoid(x[i]);
+    }
 }
 
 }  // namespace lrs
@@ -407,6 +418,17 @@ int64_t lr_workspace_bytes(void) {
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if ((int)g_ws.size() <= dev || !g_ws[dev]) return 0;
     return g_ws[dev]->bytes;
+}
+
+int lr_test_activations(const float* x, float* tanh_out, float* sigmoid_out, int64_t n,
+                        void* stream) {
+    GUARD;
+    if (n < 0 || (n > 0 && (!x || !tanh_out || !sigmoid_out))) return LR_ERR_INVALID_ARG;
+    if (n == 0) return LR_OK;
+    const int64_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+    k_test_act<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(x, tanh_out, sigmoid_out, n);
+    CK(cudaGetLastError());
+    return LR_OK;
 }
 
 int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {

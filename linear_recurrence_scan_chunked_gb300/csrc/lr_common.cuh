@@ -686,7 +686,7 @@ __device__ __forceinline__ void tile_carry(CarrySmem<VEC, NW>& sm, const float (
 // state entering every warp's first row.
 template <int VEC, int NW>
 struct StripSmem {
-    float a[NW][32][VEC];
+    float a[NW][32][VEC];  // a and b are contiguous: the op's scratch overlays them
     float b[NW][32][VEC];
     float start[NW][32][VEC];
 };

@@ -61,7 +61,7 @@ constexpr KCfg kcfg(Op op, int dtype, int mode) {
                : (op == OP_SCAN_FWD ? KCfg{8, dtype == 1 ? 8 : 4, 3}
                   : op == OP_SCAN_BWD ? KCfg{8, dtype == 1 ? 8 : 4, 2}
                   : op == OP_SRU_FWD  ? KCfg{8, dtype == 1 ? 4 : 2, 3}
-                  : op == OP_SRU_BWD  ? KCfg{8, dtype == 1 ? 2 : 1, 3}
+                  : op == OP_SRU_BWD  ? KCfg{8, dtype == 1 ? 4 : 2, 2}
                   :                     KCfg{8, dtype == 1 ? 8 : 4, 3});
 }
 // 4 channels per lane: 16-byte fp32 / 8-byte bf16 accesses, 128 channels per tile

@@ -36,18 +36,23 @@ struct TileCoord {
     int64_t t0;      // time of this thread's first row (scan order)
 };
 
+// Coordinates of the tile of chunk q (scan order) and channel tile j.
 template <class Op>
-__device__ __forceinline__ TileCoord tile_coord(const Geom& g, uint32_t tile) {
+__device__ __forceinline__ TileCoord tile_coord_qj(const Geom& g, uint32_t q, uint32_t j) {
     constexpr int L = Op::NW * Op::R, CW = 32 * Op::VEC;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     TileCoord tc;
-    tc.q = tile / g.n_ct;
-    const int64_t j = tile % g.n_ct;
-    tc.c = j * CW + lane * Op::VEC;
+    tc.q = q;
+    tc.c = (int64_t)j * CW + lane * Op::VEC;
     tc.cok = tc.c < g.C;
     tc.tchunk = Op::REV ? g.n_chunks - 1 - tc.q : tc.q;
     tc.t0 = Op::REV ? tc.tchunk * L + (L - 1) - warp * Op::R : tc.tchunk * L + warp * Op::R;
     return tc;
+}
+
+template <class Op>
+__device__ __forceinline__ TileCoord tile_coord(const Geom& g, uint32_t tile) {
+    return tile_coord_qj<Op>(g, tile / (uint32_t)g.n_ct, tile % (uint32_t)g.n_ct);
 }
 
 // Time of row r (scan order) of this thread.
@@ -348,10 +353,11 @@ __global__ void __maxnreg__(LR_TMA_MAXNREG)
 // fit an SM with up to 128 registers a thread.
 constexpr int STRIP_MAX = 64;  // strips per CTA (state kept in shared memory)
 
-template <class Op>
-__device__ __forceinline__ uint32_t strip_tile(const Geom& g, uint32_t G, uint32_t m, uint32_t it) {
-    const uint32_t q = it / m, i = it % m;
-    return q * (uint32_t)g.n_ct + blockIdx.x + i * G;
+// Use `it` of this CTA: chunk q = it / m of its strip i = it % m, j = b + i*G.
+__device__ __forceinline__ void strip_qj(uint32_t G, uint32_t m, uint32_t it, uint32_t& q,
+                                         uint32_t& j) {
+    q = it / m;
+    j = blockIdx.x + (it - q * m) * G;
 }
 
 // Thread 0: stage `it % ST` <- the tiles of use `it` (one box per array).
@@ -361,8 +367,8 @@ __device__ __forceinline__ void strip_issue(const Geom& g, const TmaDesc& td, un
     constexpr int L = Op::NW * Op::R, CW = 32 * Op::VEC;
     constexpr uint32_t SB = tma_stage_bytes<Op>();
     const uint32_t st = it % ST;
-    const uint32_t tile = strip_tile<Op>(g, G, m, it);
-    const int64_t q = tile / g.n_ct, j = tile % g.n_ct;
+    uint32_t q, j;
+    strip_qj(G, m, it, q, j);
     const int64_t tchunk = Op::REV ? g.n_chunks - 1 - q : q;
     const int32_t x = (int32_t)(j * CW), y0 = (int32_t)(tchunk * L);
     mbar_arrive_tx(&full[st], td.tx_bytes);
@@ -383,7 +389,10 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
     unsigned char* ring = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~(uintptr_t)127);
     __shared__ StripSmem<VEC, NW> sm;
-    __shared__ typename Op::Smem xs;
+    // the op's scratch (bias partials, residual maxima) is only used after
+    // strip_carry has finished with the warp aggregates: it shares their space
+    static_assert(sizeof(typename Op::Smem) <= sizeof(sm.a) + sizeof(sm.b), "op scratch too large");
+    typename Op::Smem& xs = *reinterpret_cast<typename Op::Smem*>(&sm.a[0][0][0]);
     __shared__ __align__(8) uint64_t full[ST];
     __shared__ uint32_t s_abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -417,7 +426,9 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
             strip_issue<Op, ST>(g, td, ring, full, G, m, issued);  // into stage (it-1) % ST
             ++issued;
         }
-        const TileCoord tc = tile_coord<Op>(g, strip_tile<Op>(g, G, m, it));
+        uint32_t q, j;
+        strip_qj(G, m, it, q, j);
+        const TileCoord tc = tile_coord_qj<Op>(g, q, j);
         typename Op::Regs regs;
         Op::load(SmemSrc<Op>{ring + st * SB, tc.tchunk * L, lane * VEC}, p, g, tc, regs);
         float A[VEC], B[VEC];

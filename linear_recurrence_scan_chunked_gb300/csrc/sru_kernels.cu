@@ -15,12 +15,11 @@
 //   before the carry is known),
 //   dbf, dbr: per-tile channel sums -> [2][n_chunks][C] partials -> a
 //   fixed-order reduction over chunks, then over the batch (deterministic).
+#include "lr_act.cuh"
 #include "lr_launch.h"
 #include "lr_persist.cuh"
 
 namespace lrs {
-
-__device__ __forceinline__ float sigmoidf_(float z) { return 1.f / (1.f + expf(-z)); }
 
 template <typename S>
 struct SruFwdParams {
@@ -98,7 +97,7 @@ struct SruFwdOp {
             const bool ok = tc.cok && tc.t0 + r < g.T;
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
-                const float f = sigmoidf_(rg.uf[r].get(v) + bfv[v]);
+                const float f = act_sigmoid(rg.uf[r].get(v) + bfv[v]);
                 w.fa[r][v] = ok ? f : 1.f;
                 w.fb[r][v] = ok ? (1.f - f) * rg.xt[r].get(v) : 0.f;
                 B[v] = w.fa[r][v] * B[v] + w.fb[r][v];
@@ -119,8 +118,8 @@ struct SruFwdOp {
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
                 s[v] = w.fa[r][v] * s[v] + w.fb[r][v];
-                const float rg_ = sigmoidf_(rg.ur[r].get(v) + brv[v]);
-                hv[v] = rg_ * tanhf(s[v]) + (1.f - rg_) * rg.x[r].get(v);
+                const float rg_ = act_sigmoid(rg.ur[r].get(v) + brv[v]);
+                hv[v] = rg_ * act_tanh(s[v]) + (1.f - rg_) * rg.x[r].get(v);
             }
             if (tc.cok && t < g.T) {
                 store_vec<S, VEC>(p.c + t * g.C + tc.c, s);
@@ -230,9 +229,9 @@ struct SruBwdOp {
             float durv[VEC], dxv[VEC];
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
-                const float f = sigmoidf_(rg.uf[r].get(v) + bfv[v]);
-                const float rg_ = sigmoidf_(rg.ur[r].get(v) + brv[v]);
-                const float th = tanhf(rg.c[r].get(v));
+                const float f = act_sigmoid(rg.uf[r].get(v) + bfv[v]);
+                const float rg_ = act_sigmoid(rg.ur[r].get(v) + brv[v]);
+                const float th = act_tanh(rg.c[r].get(v));
                 const float gv = rg.dh[r].get(v);
                 durv[v] = gv * (th - rg.x[r].get(v)) * rg_ * (1.f - rg_);
                 dxv[v] = gv * (1.f - rg_);

@@ -219,3 +219,23 @@ def test_argument_errors(cuda):
     st = lib.lr_scan_fwd(ctypes.c_void_p(bad.data_ptr()), ctypes.c_void_p(a.data_ptr()), None,
                          ctypes.c_void_p(a.data_ptr()), 1, 1, 1, 0, None)
     assert st == cuda.LR_ERR_ALIGN
+
+
+def test_activations_error_bound(cuda):
+    """The kernels' tanh and sigmoid (exponential forms on the hardware
+    exponential) against fp64 on a dense grid, the saturated tails, signed
+    zeros, infinities and NaN: absolute error below 1e-6 everywhere."""
+    grid = np.concatenate([np.linspace(-30, 30, 600001), np.linspace(-1e-3, 1e-3, 20001),
+                           np.array([0.0, -0.0, 88.0, -88.0, 200.0, -200.0, np.inf, -np.inf])])
+    x = grid.astype(np.float32)
+    th, sg = cuda.test_activations(torch.from_numpy(x).cuda())
+    th, sg = th.cpu().numpy().astype(np.float64), sg.cpu().numpy().astype(np.float64)
+    xd = x.astype(np.float64)
+    with np.errstate(over="ignore"):
+        ref_sg = 1.0 / (1.0 + np.exp(-xd))
+    assert np.max(np.abs(th - np.tanh(xd))) < 1e-6
+    assert np.max(np.abs(sg - ref_sg)) < 1e-6
+    assert np.all(th * xd >= 0)  # odd: never the wrong sign
+    assert th[-2] == 1.0 and th[-1] == -1.0 and sg[-2] == 1.0 and sg[-1] == 0.0
+    nan_th, nan_sg = cuda.test_activations(torch.tensor([float("nan")], device="cuda"))
+    assert torch.isnan(nan_th).all() and torch.isnan(nan_sg).all()
