@@ -430,10 +430,141 @@ constexpr uint32_t kTileMaxSleepNs = 64;
 // index only, so the states are bitwise reproducible.  States are published
 // as soon as the aggregates before them are visible -- a lane whose later
 // chunks are not visible yet still publishes its leading ones -- so no tile
-// ever waits for a tile with a larger ticket.
-template <typename S, int NW>
-__device__ void walker(const Carry& cr, const Geom& g, uint32_t wid, const S* __restrict__ init) {
-    constexpr int P = WALK_P, MV = WALK_MAX_WV;
+// ever waits for a tile with a larger ticket.  A warp of one channel (MV = 1)
+// loads the next window's aggregates while it folds the current one, so its
+// windows cost compute, not a round trip each.
+
+// Issue the loads of one window's aggregate packets (not-yet-published ones
+// come back with an old epoch and are polled again).
+template <int MV>
+__device__ __forceinline__ void walk_load(const Carry& cr, const Geom& g, int64_t c0,
+                                          const bool (&chan)[MV], int64_t q0, int n_lane,
+                                          u64 (&pk)[WALK_P][MV][2]) {
+#pragma unroll
+    for (int k = 0; k < WALK_P; ++k)
+#pragma unroll
+        for (int v = 0; v < MV; ++v) {
+            pk[k][v][0] = pk[k][v][1] = 0;
+            if (chan[v] && k < n_lane)
+                ld_pkt2_cg(cr.agg + 2 * ((c0 + v) * g.n_chunks + q0 + k), pk[k][v][0], pk[k][v][1]);
+        }
+}
+
+// Fold and publish one window [w0, w0 + n_win); s_in: state before it, on
+// return the state after it.
+template <int MV>
+__device__ __forceinline__ void walk_window(const Carry& cr, const Geom& g, int64_t c0,
+                                            const bool (&chan)[MV], int wv, int64_t w0, int n_win,
+                                            u64 (&pk)[WALK_P][MV][2], float (&s_in)[MV],
+                                            bool& dead) {
+    constexpr int P = WALK_P;
+    const int lane = threadIdx.x & 31;
+    const int64_t q0 = w0 + (int64_t)lane * P;  // this lane's first chunk
+    uint32_t spins = 0, sleep_ns = 0;
+    bool okk[P];
+#pragma unroll
+    for (int k = 0; k < P; ++k) okk[k] = false;
+    int pub = 0;  // chunks of this window already published (a prefix)
+    while (true) {
+        // vp: leading chunks of this lane whose aggregates are visible (chunks
+        // past the end of the problem count as visible)
+        int vp = 0;
+        bool run = true;
+#pragma unroll
+        for (int k = 0; k < P; ++k) {
+            bool ok = okk[k] || lane * P + k >= n_win;
+            if (!ok) {
+                ok = true;
+#pragma unroll
+                for (int v = 0; v < MV; ++v)
+                    if (chan[v]) ok = ok && pkt_ok(pk[k][v][0], cr.epoch) && pkt_ok(pk[k][v][1], cr.epoch);
+                okk[k] = ok;
+            }
+            run = run && ok;
+            vp += run ? 1 : 0;
+        }
+        const unsigned notfull = ~__ballot_sync(0xffffffffu, vp == P);
+        const int npre = notfull ? __ffs(notfull) - 1 : 32;  // leading complete lanes
+        const int vp_part = __shfl_sync(0xffffffffu, vp, npre < 32 ? npre : 31);
+        int limit = npre * P + (npre < 32 ? vp_part : 0);
+        if (limit > n_win) limit = n_win;
+        if (dead) limit = n_win;
+        float s_end[MV];
+        if (limit > pub) {
+            float A[MV], B[MV];
+#pragma unroll
+            for (int v = 0; v < MV; ++v) { A[v] = 1.f; B[v] = 0.f; }
+            if (lane < npre) {  // left fold over this lane's chunks
+#pragma unroll
+                for (int k = 0; k < P; ++k)
+#pragma unroll
+                    for (int v = 0; v < MV; ++v)
+                        if (chan[v] && lane * P + k < n_win) {
+                            const float a = pkt_val(pk[k][v][0]);
+                            B[v] = __fmaf_rn(a, B[v], pkt_val(pk[k][v][1]));
+                            A[v] *= a;
+                        }
+            }
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+#pragma unroll
+                for (int v = 0; v < MV; ++v) {
+                    if (v >= wv) continue;
+                    const float pa = __shfl_up_sync(0xffffffffu, A[v], off);
+                    const float pb = __shfl_up_sync(0xffffffffu, B[v], off);
+                    if (lane >= off) {
+                        B[v] = __fmaf_rn(A[v], pb, B[v]);
+                        A[v] = pa * A[v];
+                    }
+                }
+            }
+            float st[MV];
+#pragma unroll
+            for (int v = 0; v < MV; ++v) {  // exclusive prefix -> entering state
+                const float ea = __shfl_up_sync(0xffffffffu, A[v], 1);
+                const float eb = __shfl_up_sync(0xffffffffu, B[v], 1);
+                st[v] = lane == 0 ? s_in[v] : __fmaf_rn(ea, s_in[v], eb);
+            }
+#pragma unroll
+            for (int k = 0; k < P; ++k) {
+                const int rel = lane * P + k;
+#pragma unroll
+                for (int v = 0; v < MV; ++v) {
+                    if (!chan[v]) continue;
+                    if (rel < limit)
+                        st[v] = dead ? __int_as_float(0x7fc00000)
+                                     : __fmaf_rn(pkt_val(pk[k][v][0]), st[v], pkt_val(pk[k][v][1]));
+                    if (rel >= pub && rel < limit)
+                        st_pkt_cg(cr.inc + (c0 + v) * g.n_chunks + q0 + k, pkt(st[v], cr.epoch));
+                }
+            }
+#pragma unroll
+            for (int v = 0; v < MV; ++v) s_end[v] = st[v];
+            pub = limit;
+        }
+        if (pub == n_win) {  // state after the window's last chunk -> next window
+            const int owner = (n_win - 1) / P;
+#pragma unroll
+            for (int v = 0; v < MV; ++v) s_in[v] = __shfl_sync(0xffffffffu, s_end[v], owner);
+            return;
+        }
+        if (__any_sync(0xffffffffu, wait_step(cr, spins, sleep_ns, 0))) {
+            if (lane == 0) atomicOr(cr.err, ERRBIT_TIMEOUT);
+            dead = true;  // publish NaN for the rest so no tile keeps waiting
+            continue;
+        }
+#pragma unroll
+        for (int k = 0; k < P; ++k)  // re-poll what was not visible
+#pragma unroll
+            for (int v = 0; v < MV; ++v)
+                if (chan[v] && !okk[k] && lane * P + k < n_win)
+                    ld_pkt2_cg(cr.agg + 2 * ((c0 + v) * g.n_chunks + q0 + k), pk[k][v][0], pk[k][v][1]);
+    }
+}
+
+template <typename S, int NW, int MV>
+__device__ void walker_mv(const Carry& cr, const Geom& g, uint32_t wid, const S* __restrict__ init) {
+    constexpr int P = WALK_P, WIN = 32 * WALK_P;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t c0 = ((int64_t)wid * NW + warp) * cr.wv;
     const int64_t last = g.n_chunks - 1;  // states are needed for chunks 0 .. last-1
@@ -452,123 +583,38 @@ __device__ void walker(const Carry& cr, const Geom& g, uint32_t wid, const S* __
             s_in[v] = pk.get(0);
         }
     }
-    const u64* agg = cr.agg;
-    uint32_t spins = 0, sleep_ns = 0;
     bool dead = false;  // a wait ran out: every remaining state is published as NaN
-    for (int64_t w0 = 0; w0 < last; w0 += 32 * P) {
-        const int n_win = (int)((last - w0) < 32 * P ? (last - w0) : 32 * P);  // chunks here
-        const int64_t q0 = w0 + (int64_t)lane * P;  // this lane's first chunk
+    auto n_of = [&](int64_t w0) { return (int)((last - w0) < WIN ? (last - w0) : WIN); };
+    auto lane_n = [&](int n_win) {
+        const int r = n_win - lane * P;
+        return r < 0 ? 0 : (r > P ? P : r);
+    };
+    if constexpr (MV == 1) {
+        // two windows in flight: the next one's loads overlap this one's fold
+        u64 pa[P][MV][2], pb[P][MV][2];
+        walk_load<MV>(cr, g, c0, chan, (int64_t)lane * P, lane_n(n_of(0)), pa);
+        for (int64_t w0 = 0; w0 < last; w0 += 2 * WIN) {
+            const int64_t w1 = w0 + WIN;
+            if (w1 < last) walk_load<MV>(cr, g, c0, chan, w1 + (int64_t)lane * P, lane_n(n_of(w1)), pb);
+            walk_window<MV>(cr, g, c0, chan, wv, w0, n_of(w0), pa, s_in, dead);
+            if (w1 >= last) break;
+            const int64_t w2 = w1 + WIN;
+            if (w2 < last) walk_load<MV>(cr, g, c0, chan, w2 + (int64_t)lane * P, lane_n(n_of(w2)), pa);
+            walk_window<MV>(cr, g, c0, chan, wv, w1, n_of(w1), pb, s_in, dead);
+        }
+    } else {
         u64 pk[P][MV][2];
-        bool okk[P];
-#pragma unroll
-        for (int k = 0; k < P; ++k) {
-            okk[k] = false;
-#pragma unroll
-            for (int v = 0; v < MV; ++v) {
-                pk[k][v][0] = pk[k][v][1] = 0;
-                if (chan[v] && lane * P + k < n_win)
-                    ld_pkt2_cg(agg + 2 * ((c0 + v) * g.n_chunks + q0 + k), pk[k][v][0], pk[k][v][1]);
-            }
+        for (int64_t w0 = 0; w0 < last; w0 += WIN) {
+            walk_load<MV>(cr, g, c0, chan, w0 + (int64_t)lane * P, lane_n(n_of(w0)), pk);
+            walk_window<MV>(cr, g, c0, chan, wv, w0, n_of(w0), pk, s_in, dead);
         }
-        int pub = 0;  // chunks of this window already published (a prefix)
-        while (true) {
-            // vp: leading chunks of this lane whose aggregates are visible (chunks
-            // past the end of the problem count as visible)
-            int vp = 0;
-            bool run = true;
-#pragma unroll
-            for (int k = 0; k < P; ++k) {
-                bool ok = okk[k] || lane * P + k >= n_win;
-                if (!ok) {
-                    ok = true;
-#pragma unroll
-                    for (int v = 0; v < MV; ++v)
-                        if (chan[v]) ok = ok && pkt_ok(pk[k][v][0], cr.epoch) && pkt_ok(pk[k][v][1], cr.epoch);
-                    okk[k] = ok;
-                }
-                run = run && ok;
-                vp += run ? 1 : 0;
-            }
-            const unsigned notfull = ~__ballot_sync(0xffffffffu, vp == P);
-            const int npre = notfull ? __ffs(notfull) - 1 : 32;  // leading complete lanes
-            const int vp_part = __shfl_sync(0xffffffffu, vp, npre < 32 ? npre : 31);
-            int limit = npre * P + (npre < 32 ? vp_part : 0);
-            if (limit > n_win) limit = n_win;
-            if (dead) limit = n_win;
-            float s_end[MV];
-            if (limit > pub) {
-                float A[MV], B[MV];
-#pragma unroll
-                for (int v = 0; v < MV; ++v) { A[v] = 1.f; B[v] = 0.f; }
-                if (lane < npre) {  // left fold over this lane's chunks
-#pragma unroll
-                    for (int k = 0; k < P; ++k)
-#pragma unroll
-                        for (int v = 0; v < MV; ++v)
-                            if (chan[v] && lane * P + k < n_win) {
-                                const float a = pkt_val(pk[k][v][0]);
-                                B[v] = __fmaf_rn(a, B[v], pkt_val(pk[k][v][1]));
-                                A[v] *= a;
-                            }
-                }
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-#pragma unroll
-                    for (int v = 0; v < MV; ++v) {
-                        if (v >= wv) continue;
-                        const float pa = __shfl_up_sync(0xffffffffu, A[v], off);
-                        const float pb = __shfl_up_sync(0xffffffffu, B[v], off);
-                        if (lane >= off) {
-                            B[v] = __fmaf_rn(A[v], pb, B[v]);
-                            A[v] = pa * A[v];
-                        }
-                    }
-                }
-                float st[MV];
-#pragma unroll
-                for (int v = 0; v < MV; ++v) {  // exclusive prefix -> entering state
-                    const float ea = __shfl_up_sync(0xffffffffu, A[v], 1);
-                    const float eb = __shfl_up_sync(0xffffffffu, B[v], 1);
-                    st[v] = lane == 0 ? s_in[v] : __fmaf_rn(ea, s_in[v], eb);
-                }
-#pragma unroll
-                for (int k = 0; k < P; ++k) {
-                    const int rel = lane * P + k;
-#pragma unroll
-                    for (int v = 0; v < MV; ++v) {
-                        if (!chan[v]) continue;
-                        if (rel < limit)
-                            st[v] = dead ? __int_as_float(0x7fc00000)
-                                         : __fmaf_rn(pkt_val(pk[k][v][0]), st[v], pkt_val(pk[k][v][1]));
-                        if (rel >= pub && rel < limit)
-                            st_pkt_cg(cr.inc + (c0 + v) * g.n_chunks + q0 + k, pkt(st[v], cr.epoch));
-                    }
-                }
-#pragma unroll
-                for (int v = 0; v < MV; ++v) s_end[v] = st[v];
-                pub = limit;
-            }
-            if (pub == n_win) {  // state after the window's last chunk -> next window
-                const int owner = (n_win - 1) / P;
-#pragma unroll
-                for (int v = 0; v < MV; ++v) s_in[v] = __shfl_sync(0xffffffffu, s_end[v], owner);
-                break;
-            }
-            if (__any_sync(0xffffffffu, wait_step(cr, spins, sleep_ns, 0))) {
-                if (lane == 0) atomicOr(cr.err, ERRBIT_TIMEOUT);
-                dead = true;  // publish NaN for the rest so no tile keeps waiting
-                continue;
-            }
-#pragma unroll
-            for (int k = 0; k < P; ++k)  // re-poll what was not visible
-#pragma unroll
-                for (int v = 0; v < MV; ++v)
-                    if (chan[v] && !okk[k] && lane * P + k < n_win)
-                        ld_pkt2_cg(agg + 2 * ((c0 + v) * g.n_chunks + q0 + k), pk[k][v][0], pk[k][v][1]);
-        }
-        spins = 0;
-        sleep_ns = 0;
     }
+}
+
+template <typename S, int NW>
+__device__ void walker(const Carry& cr, const Geom& g, uint32_t wid, const S* __restrict__ init) {
+    if (cr.wv == 1) walker_mv<S, NW, 1>(cr, g, wid, init);
+    else walker_mv<S, NW, WALK_MAX_WV>(cr, g, wid, init);
 }
 
 // -------------------------------------------------------------- the tile
@@ -591,7 +637,8 @@ template <int VEC, int NW>
 __device__ __forceinline__ void tile_carry(CarrySmem<VEC, NW>& sm, const float (&A)[VEC],
                                            const float (&B)[VEC], const float (&init)[VEC],
                                            float (&start)[VEC], const Carry& cr, const Geom& g,
-                                           int64_t q, int64_t c, bool cok) {
+                                           int64_t q, int64_t c, bool cok,
+                                           const u64* pre = nullptr) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
     for (int v = 0; v < VEC; ++v) {
@@ -624,6 +671,18 @@ __device__ __forceinline__ void tile_carry(CarrySmem<VEC, NW>& sm, const float (
                 for (int v = 0; v < VEC; ++v) cin[v] = init[v];
             }
         } else {
+            // Packets loaded early by the caller (warp 0, this lane's channels of
+            // chunk q-1): when they all carry this launch's epoch, no poll at all.
+            bool have = false;
+            if (pre != nullptr) {
+                bool ok = true;
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    ok = ok && (!cok || pkt_ok(pre[v], cr.epoch));
+                    cin[v] = pkt_val(pre[v]);
+                }
+                have = __all_sync(0xffffffffu, ok);
+            }
             // Lane 0 polls one packet, the state of one channel of the tile; once it
             // is there every lane reads its own.  One 8-byte poll per tile keeps the
             // L2 free for the data, and the polled channel rotates with the chunk
@@ -634,7 +693,7 @@ __device__ __forceinline__ void tile_carry(CarrySmem<VEC, NW>& sm, const float (
             const int64_t c_rep = c_first + (int64_t)((q * 37) % n_tile_ch);
             const u64* rep = walk ? cr.inc + c_rep * g.n_chunks + q - 1 : cr.inc + (q - 1) * g.C + c_rep;
             uint32_t spins = 0, sleep_ns = 0;
-            while (true) {
+            while (!have) {
                 // chain: the states are one contiguous row, read directly (one
                 // round trip when they are there already, the common case)
                 bool rep_ok = !walk;

@@ -9,9 +9,13 @@
 
 #include "lr_common.cuh"
 
-// Consume lag of the walker-protocol kernel, in rounds of tickets.
+// Consume lag of the walker-protocol kernel, in rounds of tickets, and the
+// L2 budget (MB) for the tiles parked between their two reads.
 #ifndef LR_STREAM_LAG
 #define LR_STREAM_LAG 2
+#endif
+#ifndef LR_STREAM_L2MB
+#define LR_STREAM_L2MB 32
 #endif
 
 // Register cap of the TMA-staged kernel: two CTAs of NW+1 = 9 warps per SM.

@@ -113,6 +113,18 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
         if (tk >= limit) break;
         tile_role = true;
         const uint32_t x = tk - cr.n_walk;
+        const bool consume = x >= d_con && x - d_con < g.n_tiles;
+        // the states entering the consumed tile, loaded now: usually they are
+        // published long before the consume needs them, and then the carry
+        // costs no round trip of its own
+        u64 pre[VEC];
+        if (consume && (threadIdx.x >> 5) == 0) {
+            const TileCoord tc = tile_coord<Op>(g, x - d_con);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v)
+                pre[v] = (tc.q > 0 && tc.cok) ? ld_pkt(cr.inc + (tc.c + v) * g.n_chunks + tc.q - 1)
+                                              : 0ull;
+        }
         typename Op::Regs regs;
         typename Op::Work w;
         if (x < g.n_tiles) {  // reduce: publish the aggregate
@@ -122,7 +134,7 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
             Op::aggregate(p, g, tc, regs, w, A, B, false);
             tile_publish_agg<VEC, Op::NW>(sm, A, B, cr, g, tc.q, tc.c, tc.cok);
         }
-        if (x >= d_con && x - d_con < g.n_tiles) {  // consume (the tile's last read)
+        if (consume) {  // the tile's last read
             const TileCoord tc = tile_coord<Op>(g, x - d_con);
             Op::load(GlobalSrcHint{g.C, tc.c, l2_evict_first()}, p, g, tc, regs);
             float A[VEC], B[VEC];
@@ -134,7 +146,7 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
             if (tc.q == 0 && (threadIdx.x >> 5) == 0 && ip != nullptr && tc.cok)
                 load_vec<typename Op::S, VEC>(ip + tc.c, init);
             float s[VEC];
-            tile_carry<VEC, Op::NW>(sm, A, B, init, s, cr, g, tc.q, tc.c, tc.cok);
+            tile_carry<VEC, Op::NW>(sm, A, B, init, s, cr, g, tc.q, tc.c, tc.cok, pre);
             Op::finish(p, g, tc, regs, w, s, xs, acc);
         }
         if (draw && threadIdx.x == 0) {
@@ -505,7 +517,7 @@ cudaError_t launch_stream(const typename Op::Params& p, Geom g, const Carry& cr,
     const uint64_t tile_bytes =
         (uint64_t)Op::NW * Op::R * 32 * Op::VEC * sizeof(typename Op::S) * Op::IN_ARRAYS;
     uint64_t d_con = LR_STREAM_LAG * tile_ctas;
-    const uint64_t cap = (32ull << 20) / (tile_bytes ? tile_bytes : 1);
+    const uint64_t cap = ((uint64_t)LR_STREAM_L2MB << 20) / (tile_bytes ? tile_bytes : 1);
     if (d_con > cap) d_con = cap > 1 ? cap : 1;
     g.n_draws = g.n_tiles + (uint32_t)d_con + grid - g.ticket_base;
     k_stream<Op><<<grid, 32 * Op::NW, 0, s>>>(p, g, cr, (uint32_t)d_con);
