@@ -17,6 +17,10 @@
 #ifndef LR_STREAM_L2MB
 #define LR_STREAM_L2MB 32
 #endif
+// L2 budget (MB) of the segmented walker kernel: segments read twice.
+#ifndef LR_SEG_L2MB
+#define LR_SEG_L2MB 160
+#endif
 
 // Register cap of the TMA-staged kernel: two CTAs of NW+1 = 9 warps per SM.
 #ifndef LR_TMA_MAXNREG
@@ -82,6 +86,14 @@ inline TileShape tile_shape(Op op, int dtype, bool vec, int mode) {
 // strides) and at least one channel tile wide, with coordinates inside int32.  The tile height of the TMA kernel
 // can differ from the register kernel's, so this choice, like the protocol,
 // is fixed by the shape and the buffers' alignment of a call.
+// The walker protocol runs the segmented TMA kernel when its tile is at least
+// as tall as the register walker kernel's (per-chunk costs are paid twice
+// there, once per pass); otherwise the register kernel with its taller tile.
+constexpr bool seg_walk(Op op, int dtype) {
+    return kcfg(op, dtype, TILE_TMA).NW * kcfg(op, dtype, TILE_TMA).R >=
+           kcfg(op, dtype, CARRY_WALK).NW * kcfg(op, dtype, CARRY_WALK).R;
+}
+
 inline bool use_tma(int dtype, bool vec, int64_t T, int64_t C) {
     const int64_t es = dtype == 1 ? 2 : 4;
     return vec && (C * es) % 16 == 0 && C >= 128 && T < ((int64_t)1 << 30) &&
@@ -114,16 +126,18 @@ constexpr int64_t kWalkMaxCtas = 32;
 inline CarryPlan carry_plan(Op op, int dtype, bool vec, bool tma, int64_t T, int64_t C) {
     CarryPlan p{};
     tma = tma && vec;
-    const TileShape tw = tile_shape(op, dtype, vec, CARRY_WALK);
+    // the TMA kernels (segmented walker, strip, TMA chain) use the TMA tile shape
+    const int wmode = tma && seg_walk(op, dtype) ? TILE_TMA : CARRY_WALK;
+    const TileShape tw = tile_shape(op, dtype, vec, wmode);
     const int64_t nw = (T + tw.L - 1) / tw.L;
     if (nw >= kWalkMinChunks) {
         const int wv = C <= 256 ? 1 : WALK_MAX_WV;  // spread the walkers' reads over more SMs
         const int64_t warps = (C + wv - 1) / wv;
-        const int nwarp = kcfg(op, dtype, CARRY_WALK).NW;
+        const int nwarp = kcfg(op, dtype, wmode).NW;
         const int64_t ctas = (warps + nwarp - 1) / nwarp;
         if (ctas <= kWalkMaxCtas) {
             p.mode = CARRY_WALK;
-            p.tma = false;  // the walker kernel loads through the registers
+            p.tma = wmode == TILE_TMA;  // segmented walker kernel, else the register one
             p.ts = tw;
             p.n_chunks = nw;
             p.n_walk = (uint32_t)ctas;

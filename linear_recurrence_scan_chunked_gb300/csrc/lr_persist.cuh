@@ -461,6 +461,255 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         for (uint32_t i = it; i < issued; ++i) mbar_wait(&full[i % ST], (i / ST) & 1u, err);
 }
 
+// Segmented walker kernel (walker protocol, TMA staging; long, narrow
+// problems).  The unit of work (ticket) is a segment: SEG consecutive chunks
+// of one channel strip, streamed through the TMA ring twice.  At its own
+// iteration i a CTA
+//   1. reduces the segment of its ticket i (from HBM, kept in L2): folds the
+//      chunk aggregates into the segment's aggregate and publishes it;
+//   2. consumes the segment of its ticket i-1 (from L2): one wait for the
+//      state entering that segment, which the walker CTAs (the first tickets)
+//      fold from the segment aggregates, then the state is carried from chunk
+//      to chunk in shared memory, as in the strip kernel, and the outputs are
+//      written.
+// The one-segment lag gives the walkers a segment's time to produce every
+// entering state.  Tickets, aggregate packets, walker work and the carry wait
+// are paid once per segment rather than once per tile, and every load is
+// issued ST - 1 uses ahead by thread 0 (tickets are drawn one iteration
+// early).  A consume only waits for reduces of smaller tickets, and every CTA
+// reduces before it consumes: every wait ends.
+struct SegGeom {
+    uint32_t seg;      // chunks per segment
+    uint32_t n_seg;    // segments per strip: ceil(n_chunks / seg)
+    uint32_t n_units;  // n_seg * n_ct
+};
+
+template <class Op, int ST>
+__device__ __forceinline__ void seg_issue(const Geom& g, const TmaDesc& td, unsigned char* ring,
+                                          uint64_t* full, uint32_t st, uint32_t q, uint32_t j,
+                                          uint64_t pol) {
+    constexpr int L = Op::NW * Op::R, CW = 32 * Op::VEC;
+    const int64_t tchunk = Op::REV ? g.n_chunks - 1 - (int64_t)q : (int64_t)q;
+    const int32_t x = (int32_t)((int64_t)j * CW), y0 = (int32_t)(tchunk * L);
+    mbar_arrive_tx(&full[st], td.tx_bytes);
+    unsigned char* dst = ring + st * tma_stage_bytes<Op>();
+#pragma unroll
+    for (int a = 0; a < Op::TMA_N; ++a)
+        if (td.present & (1u << a))
+            tma_load_2d_hint(dst + tma_off<Op>(a), &td.map[a], x, y0 + Op::tma_shift(a), &full[st],
+                             pol);
+}
+
+template <class Op, int ST>
+__global__ void __launch_bounds__(Op::NW * 32, 2)
+    k_seg(typename Op::Params p, Geom g, Carry cr, SegGeom sg,
+          const __grid_constant__ TmaDesc td) {
+    constexpr int NW = Op::NW, VEC = Op::VEC, L = Op::NW * Op::R;
+    constexpr uint32_t SB = tma_stage_bytes<Op>();
+    extern __shared__ unsigned char dyn_smem[];
+    unsigned char* ring = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~(uintptr_t)127);
+    __shared__ StripSmem<VEC, NW> sm;
+    static_assert(sizeof(typename Op::Smem) <= sizeof(sm.a) + sizeof(sm.b), "op scratch too large");
+    typename Op::Smem& xs = *reinterpret_cast<typename Op::Smem*>(&sm.a[0][0][0]);
+    __shared__ float carry[32][VEC];
+    __shared__ __align__(8) uint64_t full[ST];
+    __shared__ uint32_t s_tk[2], s_abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t limit = cr.n_walk + sg.n_units;
+    const uint32_t uses = 2 * sg.seg;  // per iteration: reduce pass, consume pass
+    if (threadIdx.x == 0) {
+        const uint32_t t = atomicAdd(cr.ticket, 1u);
+        if (t == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+        s_tk[0] = t;
+        s_abort = 0;
+    }
+    __syncthreads();
+    uint32_t cur = s_tk[0];
+    if (cur < cr.n_walk) {  // walker role: its chunks are the segments
+        Geom gw = g;
+        gw.n_chunks = sg.n_seg;
+        walker<typename Op::S, NW>(cr, gw, cur, Op::init_ptr(p));
+        return;
+    }
+    if (cur >= limit) return;
+    // thread 0 state: tickets drawn ahead, loads issued ahead
+    bool drawing = true;
+    uint32_t pend = 0;
+    uint32_t inflight = 0;  // stages with a box in flight
+    uint64_t pol_keep = 0, pol_drop = 0;
+    // Thread 0: issue use u into stage u % ST.  Use u is chunk k of the reduce
+    // pass of ticket `red` (k < SEG) or chunk k - SEG of the consume pass of
+    // ticket `con`; tickets >= limit have no segment.
+    auto issue = [&](uint32_t u, uint32_t red, uint32_t con) {
+        const uint32_t k = u % uses;
+        const uint32_t tk = k < sg.seg ? red : con, c = k < sg.seg ? k : k - sg.seg;
+        if (tk >= limit) return;
+        const uint32_t x = tk - cr.n_walk, seg = x / (uint32_t)g.n_ct;
+        const uint32_t j = x - seg * (uint32_t)g.n_ct, q = seg * sg.seg + c;
+        if (q >= (uint32_t)g.n_chunks) return;
+        const uint32_t st = u % ST;
+        seg_issue<Op, ST>(g, td, ring, full, st, q, j, k < sg.seg ? pol_keep : pol_drop);
+        inflight |= 1u << st;
+    };
+    uint32_t prev = limit;  // ticket whose segment this iteration consumes
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < ST; ++i) mbar_init(&full[i], 1);
+        mbar_init_fence();
+        pol_keep = l2_evict_last();
+        pol_drop = l2_evict_first();
+        const uint32_t t1 = atomicAdd(cr.ticket, 1u);
+        if (t1 == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+        if (t1 >= limit) drawing = false;
+        s_tk[1] = t1;
+        // uses 0 .. ST-1 (ST <= SEG + 1: the reduce pass of `cur` and at most
+        // the first chunk of the empty consume pass)
+        for (uint32_t u = 0; u < (uint32_t)ST; ++u) issue(u, cur, prev);
+        if (drawing) pend = atomicAdd(cr.ticket, 1u);
+    }
+    __syncthreads();
+    uint32_t nxt = s_tk[1];
+    uint32_t phase = 0;  // parity of the next completion of each stage's barrier
+    uint32_t it = 0;     // uses consumed
+    typename Op::Acc acc;
+    Op::acc_init(acc);
+    bool stop = false;
+    // Top of use `it`: wait for its box, then a barrier after which the stage
+    // of use it-1 is free and the stop decision is uniform; refill that stage
+    // with use it-1+ST (this iteration's tickets, or the next iteration's).
+    auto top = [&](bool valid) {
+        const uint32_t st = it % ST;
+        if (valid && !mbar_wait(&full[st], (phase >> st) & 1u, cr.err)) s_abort = 1;
+        csync<NW>();
+        if (s_abort != 0) return false;
+        if (threadIdx.x == 0 && it > 0) {
+            const uint32_t u = it - 1 + ST;
+            if (u / uses == it / uses) issue(u, cur, prev);
+            else issue(u, nxt, cur);
+        }
+        if (valid) {
+            phase ^= 1u << st;
+            if (threadIdx.x == 0) inflight &= ~(1u << st);
+        }
+        return true;
+    };
+    while ((cur < limit || prev < limit) && !stop) {
+        // ---- pass 1: the aggregate of the segment of `cur`
+        const bool has_red = cur < limit;
+        const uint32_t xr = has_red ? cur - cr.n_walk : 0u;
+        const uint32_t seg_r = xr / (uint32_t)g.n_ct, j_r = xr - seg_r * (uint32_t)g.n_ct;
+        float SA[VEC], SBv[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { SA[v] = 1.f; SBv[v] = 0.f; }
+        for (uint32_t c = 0; c < sg.seg; ++c, ++it) {
+            const uint32_t q = seg_r * sg.seg + c;
+            const bool valid = has_red && q < (uint32_t)g.n_chunks;
+            if (!top(valid)) { stop = true; break; }
+            if (!valid) continue;
+            const TileCoord tc = tile_coord_qj<Op>(g, q, j_r);
+            typename Op::Regs regs;
+            typename Op::Work w;
+            Op::load(SmemSrc<Op>{ring + (it % ST) * SB, tc.tchunk * L, lane * VEC}, p, g, tc, regs);
+            float A[VEC], B[VEC];
+            Op::aggregate(p, g, tc, regs, w, A, B, false);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                sm.a[warp][lane][v] = A[v];
+                sm.b[warp][lane][v] = B[v];
+            }
+            csync<NW>();
+            if (warp == 0) {  // fold the warps (row order), then into the segment
+#pragma unroll
+                for (int w2 = 0; w2 < NW; ++w2)
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) {
+                        const float a = sm.a[w2][lane][v];
+                        SBv[v] = __fmaf_rn(a, SBv[v], sm.b[w2][lane][v]);
+                        SA[v] *= a;
+                    }
+            }
+        }
+        if (stop) break;
+        if (warp == 0 && has_red) {  // the segment's aggregate, for the walkers
+            const TileCoord tc = tile_coord_qj<Op>(g, seg_r * sg.seg, j_r);
+            if (tc.cok && seg_r + 1 < sg.n_seg) {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v)
+                    st_pkt2(cr.agg + 2 * ((tc.c + v) * sg.n_seg + seg_r), pkt(SA[v], cr.epoch),
+                            pkt(SBv[v], cr.epoch));
+            }
+        }
+        // ---- pass 2: the outputs of the segment of `prev`
+        const bool has_con = prev < limit;
+        const uint32_t xc = has_con ? prev - cr.n_walk : 0u;
+        const uint32_t seg_c = xc / (uint32_t)g.n_ct, j_c = xc - seg_c * (uint32_t)g.n_ct;
+        if (warp == 0 && has_con) {  // the state entering that segment
+            const TileCoord tc = tile_coord_qj<Op>(g, seg_c * sg.seg, j_c);
+            float cin[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) cin[v] = 0.f;
+            const typename Op::S* ip = Op::init_ptr(p);
+            if (seg_c == 0) {
+                if (tc.cok && ip != nullptr) load_vec<typename Op::S, VEC>(ip + tc.c, cin);
+            } else {
+                uint32_t spins = 0, sleep_ns = 0;
+                while (true) {
+                    const bool ok = !tc.cok || get_states_strided<VEC>(
+                                                   cr.inc + tc.c * sg.n_seg + seg_c - 1, sg.n_seg,
+                                                   cin, cr.epoch);
+                    if (__all_sync(0xffffffffu, ok)) break;
+                    if (__any_sync(0xffffffffu, wait_step(cr, spins, sleep_ns, kTileMaxSleepNs))) {
+                        if (lane == 0) atomicOr(cr.err, ERRBIT_TIMEOUT);
+#pragma unroll
+                        for (int v = 0; v < VEC; ++v) cin[v] = __int_as_float(0x7fc00000);
+                        break;
+                    }
+                }
+            }
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) carry[lane][v] = cin[v];
+        }
+        for (uint32_t c = 0; c < sg.seg; ++c, ++it) {
+            const uint32_t q = seg_c * sg.seg + c;
+            const bool valid = has_con && q < (uint32_t)g.n_chunks;
+            if (!top(valid)) { stop = true; break; }
+            if (!valid) continue;
+            const TileCoord tc = tile_coord_qj<Op>(g, q, j_c);
+            typename Op::Regs regs;
+            typename Op::Work w;
+            Op::load(SmemSrc<Op>{ring + (it % ST) * SB, tc.tchunk * L, lane * VEC}, p, g, tc, regs);
+            float A[VEC], B[VEC];
+            Op::aggregate(p, g, tc, regs, w, A, B, true);
+            float s0[VEC], st[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) s0[v] = 0.f;
+            strip_carry<VEC, NW>(sm, A, B, s0, st, carry, false, tc.cok);
+            Op::finish(p, g, tc, regs, w, st, xs, acc);
+        }
+        if (stop) break;
+        // ---- next iteration: prev <- cur <- nxt <- drawn
+        if (threadIdx.x == 0) {
+            uint32_t t2 = limit;
+            if (drawing) {
+                t2 = pend;
+                if (t2 == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+                if (t2 >= limit) drawing = false;
+                else pend = atomicAdd(cr.ticket, 1u);
+            }
+            s_tk[0] = t2;
+        }
+        __syncthreads();
+        prev = cur;
+        cur = nxt;
+        nxt = s_tk[0];
+    }
+    if (stop && threadIdx.x == 0) atomicOr(cr.err, ERRBIT_TIMEOUT);
+    Op::at_exit(p, xs, acc);
+    if (threadIdx.x == 0)  // after an early stop: boxes still in flight land first
+        for (int st = 0; st < ST; ++st)
+            if (inflight & (1u << st)) mbar_wait(&full[st], (phase >> st) & 1u, cr.err);
+}
+
 template <class Op>
 int chain_occupancy() {
     static int occ[64] = {0};
@@ -619,6 +868,62 @@ cudaError_t launch_strip(const typename Op::Params& p, const Geom& g, const Carr
     return cudaGetLastError();
 }
 
+// Host: launch k_seg<Op, ST> (walker protocol, segmented, TMA staging).  The
+// segment length keeps the tiles between their two reads (about two segments
+// per CTA) within an L2 budget.
+template <class Op, int ST>
+cudaError_t launch_seg(const typename Op::Params& p, Geom g, const Carry& cr, cudaStream_t s) {
+    constexpr int L = Op::NW * Op::R, CW = 32 * Op::VEC;
+    constexpr uint32_t SB = tma_stage_bytes<Op>();
+    constexpr size_t dyn = (size_t)ST * SB + 128;
+    static_assert(L + 1 <= 256 && CW <= 256, "a TMA box holds at most 256 rows and columns");
+    TmaDesc td;
+    memset(&td, 0, sizeof td);
+    const void* ptr[TMA_MAX_ARR] = {};
+    Op::tma_arrays(p, ptr);
+    for (int a = 0; a < Op::TMA_N; ++a) {
+        if (!ptr[a]) continue;
+        if (!tma_encode(&td.map[a], ptr[a], sizeof(typename Op::S) == 2 ? 1 : 0, g.T, g.C, CW,
+                        L + Op::tma_extra(a)))
+            return cudaErrorInvalidValue;
+        td.present |= 1u << a;
+        td.tx_bytes += tma_arr_bytes<Op>(a);
+    }
+    static int occ[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int& o = occ[dev & 63];
+    if (o <= 0) {
+        cudaError_t e = cudaFuncSetAttribute(k_seg<Op, ST>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k_seg<Op, ST>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_seg<Op, ST>, 32 * Op::NW, dyn) !=
+                cudaSuccess ||
+            n <= 0)
+            n = 1;
+        o = n;
+    }
+    const uint32_t grid = persist_grid(g, cr, o);
+    const uint64_t tile_ctas = grid > cr.n_walk ? grid - cr.n_walk : 1;
+    // two segments per CTA are in L2 at a time (one reduced, one consumed)
+    uint64_t seg = ((uint64_t)LR_SEG_L2MB << 20) / (2 * tile_ctas * SB);
+    if (seg < (uint64_t)ST) seg = ST;  // the ring's look-ahead stays within one iteration
+    if (seg < 2) seg = 2;
+    if (seg > 64) seg = 64;
+    SegGeom sg;
+    sg.seg = (uint32_t)seg;
+    sg.n_seg = (uint32_t)((g.n_chunks + seg - 1) / seg);
+    sg.n_units = sg.n_seg * (uint32_t)g.n_ct;
+    // walkers draw once; a segment CTA draws until one past the end
+    g.n_draws = sg.n_units + grid - g.ticket_base;
+    k_seg<Op, ST><<<grid, 32 * Op::NW, dyn, s>>>(p, g, cr, sg, td);
+    return cudaGetLastError();
+}
+
 // Host: launch the kernel of the launch's carry protocol; OpC / OpW / OpT are
 // the operation instantiated with the tile shapes of the register chain, the
 // walker and the TMA-staged kernels (strip, TMA chain).
@@ -636,6 +941,8 @@ cudaError_t launch_persist(const typename OpC::Params& p, const Geom& g, const C
         }
         return launch_chain<OpC>(p, g, cr, s);
     }
+    if constexpr (OpT::NW * OpT::R >= OpW::NW * OpW::R)  // as seg_walk()
+        if (cr.tma) return launch_seg<OpT, ST>(p, g, cr, s);
     return launch_stream<OpW>(p, g, cr, s);
 }
 

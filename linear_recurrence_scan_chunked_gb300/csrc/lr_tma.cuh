@@ -125,6 +125,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int
         : "memory");
 }
 
+// As tma_load_2d, with an L2 eviction-priority policy (createpolicy) for the
+// lines it reads.
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m, int32_t x,
+                                                 int32_t y, uint64_t* b, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(b)), "l"(pol)
+        : "memory");
+}
+
 // ---------------------------------------------------------- tile sources
 // Where Op::load takes the rows of its arrays from: global memory (register
 // kernels) or the staged tile in shared memory (TMA kernels).
