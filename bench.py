@@ -180,7 +180,9 @@ class Bench:
                 if st != L.LR_OK:
                     raise RuntimeError(f"DEER did not converge (status {st})")
                 self.k_last = k
-                launches += k
+                # iterations are enqueued four at a time; those after the
+                # stopping test return at once but are still launches
+                launches += min(KMAX, -(-k // 4) * 4)
             if ev is not None:
                 ev[(name, p)][1].record()
             k = self.k_last if p == "solve" else 1

@@ -44,8 +44,10 @@
  *    a multiple of 16 bytes and at least 128 channels wide, tiles are staged
  *    through shared memory by the Tensor Memory Accelerator.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
- *    asynchronous on it except deer_diag_solve, which synchronises the stream
- *    once per Newton iteration to read the residual.
+ *    asynchronous on it except deer_diag_solve, which enqueues its Newton
+ *    iterations four at a time and synchronises the stream once per four to
+ *    read their residuals (an iteration enqueued after the stopping test was
+ *    met does no work).
  *  - Sizes: B, T, D >= 0 with B*T*D < 2^62; an empty problem is a no-op
  *    (gradients of the initial state are zeroed).
  *  - The library keeps one internal workspace per device (carry packets of

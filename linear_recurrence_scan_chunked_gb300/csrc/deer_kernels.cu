@@ -28,6 +28,8 @@ struct DeerParams {
     const S* yold;
     S* ynew;
     uint32_t* resid;
+    const uint32_t* prev_resid;  // residual of the previous iteration (nullptr: first)
+    float eps;
 };
 
 template <typename S_, int VEC_, int NW_, int R_>
@@ -51,6 +53,17 @@ struct DeerOp {
         uint32_t mx;  // max |y - yold| as bits: fp32 order of non-negative values, NaN on top
     };
     __device__ static void acc_init(Acc& a) { a.mx = 0; }
+    // The iterations of a solve are enqueued in batches; one whose predecessor
+    // already stopped the solve (residual below eps, or not finite) does
+    // nothing but pass that residual on, so that its own successor stops too.
+    __device__ static bool skip(const Params& p) {
+        if (p.prev_resid == nullptr) return false;
+        const uint32_t bits = *(volatile const uint32_t*)p.prev_resid;
+        const float rho = __uint_as_float(bits);
+        const bool stop = rho < p.eps || !(rho <= 3.4e38f);
+        if (stop && blockIdx.x == 0 && threadIdx.x == 0) *p.resid = bits;
+        return stop;
+    }
     __device__ static const S* init_ptr(const Params& p) { return p.h0; }
 
     static constexpr int TMA_N = 2;  // staged: u, previous iterate (rows t0-1 .. t0+L-1)
@@ -150,21 +163,23 @@ using DeerOpT = DeerOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_DEER, sizeof(S) == 2
 
 template <typename S, bool VP>
 static cudaError_t deer_t(const float* w, const void* u, const void* h0, const void* yold,
-                          void* ynew, uint32_t* resid, const Geom& g, const Carry& cr,
-                          cudaStream_t s) {
+                          void* ynew, uint32_t* resid, const uint32_t* prev_resid, float eps,
+                          const Geom& g, const Carry& cr, cudaStream_t s) {
     return launch_persist<DeerOpT<S, VP, CARRY_CHAIN>, DeerOpT<S, VP, CARRY_WALK>,
                           DeerOpT<S, VP, TILE_TMA>, kcfg(OP_DEER, sizeof(S) == 2, TILE_TMA).ST>(
-        {w, (const S*)u, (const S*)h0, (const S*)yold, (S*)ynew, resid}, g, cr, s);
+        {w, (const S*)u, (const S*)h0, (const S*)yold, (S*)ynew, resid, prev_resid, eps}, g, cr, s);
 }
 
 cudaError_t launch_deer_iter(int dtype, bool vec, const float* w, const void* u, const void* h0,
-                             const void* yold, void* ynew, uint32_t* resid, const Geom& g,
-                             const Carry& cr, cudaStream_t s) {
+                             const void* yold, void* ynew, uint32_t* resid,
+                             const uint32_t* prev_resid, float eps, const Geom& g, const Carry& cr,
+                             cudaStream_t s) {
     if (dtype == 0)
-        return vec ? deer_t<float, true>(w, u, h0, yold, ynew, resid, g, cr, s)
-                   : deer_t<float, false>(w, u, h0, yold, ynew, resid, g, cr, s);
-    return vec ? deer_t<__nv_bfloat16, true>(w, u, h0, yold, ynew, resid, g, cr, s)
-               : deer_t<__nv_bfloat16, false>(w, u, h0, yold, ynew, resid, g, cr, s);
+        return vec ? deer_t<float, true>(w, u, h0, yold, ynew, resid, prev_resid, eps, g, cr, s)
+                   : deer_t<float, false>(w, u, h0, yold, ynew, resid, prev_resid, eps, g, cr, s);
+    return vec ? deer_t<__nv_bfloat16, true>(w, u, h0, yold, ynew, resid, prev_resid, eps, g, cr, s)
+               : deer_t<__nv_bfloat16, false>(w, u, h0, yold, ynew, resid, prev_resid, eps, g, cr,
+                                              s);
 }
 
 }  // namespace lrs

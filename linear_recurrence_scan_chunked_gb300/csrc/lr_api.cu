@@ -63,6 +63,7 @@ using namespace lrs;
 
 constexpr uint32_t kSpinLimit = 1u << 21;  // polls (backing off to ~1 us each): ~2 s
 constexpr int kMaxIters = 4096;            // DEER kmax bound (residual slots)
+constexpr int kDeerBatch = 4;              // DEER iterations enqueued per residual read-back
 
 thread_local char g_cuda_msg[256] = "";
 
@@ -84,7 +85,7 @@ struct DevWS {
     uint32_t* words = nullptr;   // [0] ticket, [1] error bits, [2..] DEER residual slots
     float* partials = nullptr;   size_t partials_cap = 0; // floats
     void* ybuf = nullptr;        size_t ybuf_cap = 0;     // bytes
-    uint32_t* host_word = nullptr;                        // pinned, for residual reads
+    uint32_t* host_word = nullptr;                        // pinned [kMaxIters], residual reads
     void* test_buf = nullptr;                             // timeout-test problem
     uint32_t epoch = 0;
     cudaEvent_t done = nullptr;
@@ -104,7 +105,7 @@ int get_ws(DevWS** out) {
         DevWS* w = new DevWS();
         CK(cudaMalloc(&w->words, sizeof(uint32_t) * (2 + kMaxIters)));
         CK(cudaMemset(w->words, 0, sizeof(uint32_t) * (2 + kMaxIters)));
-        CK(cudaHostAlloc(&w->host_word, sizeof(uint32_t), cudaHostAllocDefault));
+        CK(cudaHostAlloc(&w->host_word, sizeof(uint32_t) * kMaxIters, cudaHostAllocDefault));
         CK(cudaEventCreateWithFlags(&w->done, cudaEventDisableTiming));
         w->bytes = sizeof(uint32_t) * (2 + kMaxIters);
         g_ws[dev] = w;
@@ -354,24 +355,37 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y, int6
     TRY(enter(*ws, s));
     uint32_t* slots = ws->words + 2;
     CK(cudaMemsetAsync(slots, 0, sizeof(uint32_t) * kmax, s));
-    // iterate k writes buf[k % 2]; buf[1] is the caller's y
+    // iterate k writes buf[k % 2]; buf[1] is the caller's y.  Iterations are
+    // enqueued kDeerBatch at a time with one residual read-back per batch;
+    // an iteration enqueued after the solve stopped returns at once (it sees
+    // its predecessor's residual on the device).
     void* buf[2] = {ws->ybuf, y};
     int k = 0, status = LR_ERR_NOT_CONVERGED;
     float rho = 0.f;
-    for (k = 1; k <= kmax; ++k) {
-        Geom g;
-        Carry cr;
-        TRY(plan(*ws, OP_DEER, dtype, vec, T, B * D, D, &g, &cr, s));
-        CK(launch_deer_iter(dtype, vec, w, u, h0, k == 1 ? nullptr : buf[(k - 1) & 1], buf[k & 1],
-                            slots + (k - 1), g, cr, s));
-        CK(cudaMemcpyAsync(ws->host_word, slots + (k - 1), sizeof(uint32_t),
+    int launched = 0;
+    bool done = false;
+    while (!done && launched < kmax) {
+        const int first = launched;
+        const int nb = kmax - launched < kDeerBatch ? kmax - launched : kDeerBatch;
+        for (int i = 0; i < nb; ++i) {
+            const int kk = ++launched;
+            Geom g;
+            Carry cr;
+            TRY(plan(*ws, OP_DEER, dtype, vec, T, B * D, D, &g, &cr, s));
+            CK(launch_deer_iter(dtype, vec, w, u, h0, kk == 1 ? nullptr : buf[(kk - 1) & 1],
+                                buf[kk & 1], slots + (kk - 1), kk == 1 ? nullptr : slots + (kk - 2),
+                                eps, g, cr, s));
+        }
+        CK(cudaMemcpyAsync(ws->host_word + first, slots + first, sizeof(uint32_t) * nb,
                            cudaMemcpyDeviceToHost, s));
         CK(cudaStreamSynchronize(s));
-        uint32_t bits = *ws->host_word;
-        memcpy(&rho, &bits, sizeof rho);
-        if (resid_hist) resid_hist[k - 1] = rho;
-        if (!(rho <= 3.4e38f)) { status = LR_ERR_NONFINITE; break; }
-        if (rho < eps) { status = LR_OK; break; }
+        for (k = first + 1; k <= launched; ++k) {
+            const uint32_t bits = ws->host_word[k - 1];
+            memcpy(&rho, &bits, sizeof rho);
+            if (resid_hist) resid_hist[k - 1] = rho;
+            if (!(rho <= 3.4e38f)) { status = LR_ERR_NONFINITE; done = true; break; }
+            if (rho < eps) { status = LR_OK; done = true; break; }
+        }
     }
     if (k > kmax) k = kmax;
     if ((k & 1) == 0) CK(cudaMemcpyAsync(y, ws->ybuf, nbytes, cudaMemcpyDeviceToDevice, s));

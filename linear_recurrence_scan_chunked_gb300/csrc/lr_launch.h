@@ -201,7 +201,8 @@ cudaError_t launch_bias_reduce(const float* partials, int64_t n_chunks, int64_t 
 
 // resid: one fp32 slot (as bits), zeroed before the launch, receives max|ynew-yold|
 cudaError_t launch_deer_iter(int dtype, bool vec, const float* w, const void* u, const void* h0,
-                             const void* yold, void* ynew, uint32_t* resid, const Geom& g,
-                             const Carry& cr, cudaStream_t s);
+                             const void* yold, void* ynew, uint32_t* resid,
+                             const uint32_t* prev_resid, float eps, const Geom& g, const Carry& cr,
+                             cudaStream_t s);
 
 }  // namespace lrs

@@ -85,6 +85,7 @@ __device__ __forceinline__ void gload(const typename Op::Params& p, const Geom& 
 template <class Op>
 __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
     k_stream(typename Op::Params p, Geom g, Carry cr, uint32_t d_con) {
+    if (Op::skip(p)) return;  // whole launch: before any ticket or barrier
     constexpr int VEC = Op::VEC;
     __shared__ CarrySmem<VEC, Op::NW> sm;
     __shared__ typename Op::Smem xs;
@@ -209,6 +210,7 @@ __device__ __forceinline__ uint32_t chain_tile(const typename Op::Params& p, con
 template <class Op>
 __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
     k_chain(typename Op::Params p, Geom g, Carry cr) {
+    if (Op::skip(p)) return;  // whole launch: before any ticket or barrier
     __shared__ CarrySmem<Op::VEC, Op::NW> sm;
     __shared__ typename Op::Smem xs;
     __shared__ uint32_t s_ticket;
@@ -306,6 +308,7 @@ __device__ __forceinline__ void tma_produce(const Geom& g, const Carry& cr, cons
 template <class Op, int ST>
 __global__ void __maxnreg__(LR_TMA_MAXNREG)
     k_tchain(typename Op::Params p, Geom g, Carry cr, const __grid_constant__ TmaDesc td) {
+    if (Op::skip(p)) return;  // whole launch: before any ticket or barrier
     constexpr int NW = Op::NW, VEC = Op::VEC, L = Op::NW * Op::R;
     constexpr uint32_t SB = tma_stage_bytes<Op>();
     extern __shared__ unsigned char dyn_smem[];
@@ -395,6 +398,7 @@ template <class Op, int ST>
 __global__ void __launch_bounds__(Op::NW * 32, 2)
     k_strip(typename Op::Params p, Geom g, uint32_t* err, uint32_t G,
             const __grid_constant__ TmaDesc td) {
+    if (Op::skip(p)) return;  // whole launch: before any ticket or barrier
     constexpr int NW = Op::NW, VEC = Op::VEC, L = Op::NW * Op::R;
     constexpr uint32_t SB = tma_stage_bytes<Op>();
     extern __shared__ unsigned char dyn_smem[];
@@ -504,6 +508,7 @@ template <class Op, int ST>
 __global__ void __launch_bounds__(Op::NW * 32, 2)
     k_seg(typename Op::Params p, Geom g, Carry cr, SegGeom sg,
           const __grid_constant__ TmaDesc td) {
+    if (Op::skip(p)) return;  // whole launch: before any ticket or barrier
     constexpr int NW = Op::NW, VEC = Op::VEC, L = Op::NW * Op::R;
     constexpr uint32_t SB = tma_stage_bytes<Op>();
     extern __shared__ unsigned char dyn_smem[];

@@ -46,6 +46,7 @@ struct ScanFwdOp {
     };
     struct Acc {};
     __device__ static void acc_init(Acc&) {}
+    __device__ static bool skip(const Params&) { return false; }
     __device__ static const S* init_ptr(const Params& p) { return p.h0; }
 
     static constexpr int TMA_N = 2;  // staged: a, b
@@ -124,6 +125,7 @@ struct ScanBwdOp {
     };
     struct Acc {};
     __device__ static void acc_init(Acc&) {}
+    __device__ static bool skip(const Params&) { return false; }
     __device__ static const S* init_ptr(const Params&) { return nullptr; }  // u_T = 0
 
     static constexpr int TMA_N = 3;  // staged: a, dh, h (rows shifted by one: h_{t-1})

@@ -52,6 +52,7 @@ struct SruFwdOp {
     };
     struct Acc {};
     __device__ static void acc_init(Acc&) {}
+    __device__ static bool skip(const Params&) { return false; }
     __device__ static const S* init_ptr(const Params& p) { return p.c0; }
 
     static constexpr int TMA_N = 4;  // staged: xt, uf, ur, x
@@ -169,6 +170,7 @@ struct SruBwdOp {
     };
     struct Acc {};
     __device__ static void acc_init(Acc&) {}
+    __device__ static bool skip(const Params&) { return false; }
     __device__ static const S* init_ptr(const Params&) { return nullptr; }  // u_T = 0
 
     static constexpr int TMA_N = 6;  // staged: xt, uf, ur, x, dh, c (rows t0-1 .. t0+L-1)
