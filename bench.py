@@ -27,6 +27,7 @@ import json
 import os
 import statistics
 import subprocess
+import threading
 import sys
 import time
 
@@ -243,23 +244,38 @@ class Clocks:
         self.index, self.p, self.lines = index, None, []
 
     def __enter__(self):
+        # sample every 20 ms; the timed region starts once the first sample is
+        # in (nvidia-smi takes a while to start)
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                       "--format=csv,noheader,nounits", "-lms", "20"],
                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.p = None
+            return self
+        self.first = threading.Event()
+
+        def reader():
+            for line in self.p.stdout:
+                if line.strip():
+                    self.lines.append(line)
+                    self.first.set()
+            self.first.set()
+
+        self.t = threading.Thread(target=reader, daemon=True)
+        self.t.start()
+        self.first.wait(timeout=10)
+        self.lines.clear()  # keep samples from the timed region only
         return self
 
     def __exit__(self, *a):
         if self.p is not None:
             self.p.terminate()
             try:
-                out, _ = self.p.communicate(timeout=5)
+                self.p.wait(timeout=5)
             except Exception:
                 self.p.kill()
-                out, _ = self.p.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+            self.t.join(timeout=5)
 
     def summary(self):
         sm, mx, reasons = [], [], set()
@@ -437,7 +453,7 @@ def run_reference(args, ws, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=2)

@@ -471,17 +471,23 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
 // iteration i a CTA
 //   1. reduces the segment of its ticket i (from HBM, kept in L2): folds the
 //      chunk aggregates into the segment's aggregate and publishes it;
-//   2. consumes the segment of its ticket i-1 (from L2): one wait for the
-//      state entering that segment, which the walker CTAs (the first tickets)
-//      fold from the segment aggregates, then the state is carried from chunk
-//      to chunk in shared memory, as in the strip kernel, and the outputs are
-//      written.
-// The one-segment lag gives the walkers a segment's time to produce every
-// entering state.  Tickets, aggregate packets, walker work and the carry wait
+//   2. consumes the segment of its ticket i-SEG_LAG (from L2): one wait for
+//      the state entering that segment, which the walker CTAs (the first
+//      tickets) fold from the segment aggregates, then the state is carried
+//      from chunk to chunk in shared memory, as in the strip kernel, and the
+//      outputs are written.
+// The lag of SEG_LAG segments gives the walkers that many segments' time to
+// produce every entering state, while SEG_LAG + 1 short segments per CTA stay
+// within the L2.  Tickets, aggregate packets, walker work and the carry wait
 // are paid once per segment rather than once per tile, and every load is
 // issued ST - 1 uses ahead by thread 0 (tickets are drawn one iteration
 // early).  A consume only waits for reduces of smaller tickets, and every CTA
 // reduces before it consumes: every wait ends.
+#ifndef LR_SEG_LAG
+#define LR_SEG_LAG 2
+#endif
+constexpr int SEG_LAG = LR_SEG_LAG;  // iterations between a segment's two passes
+
 struct SegGeom {
     uint32_t seg;      // chunks per segment
     uint32_t n_seg;    // segments per strip: ceil(n_chunks / seg)
@@ -557,7 +563,12 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         seg_issue<Op, ST>(g, td, ring, full, st, q, j, k < sg.seg ? pol_keep : pol_drop);
         inflight |= 1u << st;
     };
-    uint32_t prev = limit;  // ticket whose segment this iteration consumes
+    // tq[0]: ticket consumed this iteration, tq[SEG_LAG]: reduced this
+    // iteration, tq[SEG_LAG + 1]: reduced next iteration
+    uint32_t tq[SEG_LAG + 2];
+#pragma unroll
+    for (int i = 0; i < SEG_LAG; ++i) tq[i] = limit;
+    tq[SEG_LAG] = cur;
     if (threadIdx.x == 0) {
         for (int i = 0; i < ST; ++i) mbar_init(&full[i], 1);
         mbar_init_fence();
@@ -569,11 +580,11 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         s_tk[1] = t1;
         // uses 0 .. ST-1 (ST <= SEG + 1: the reduce pass of `cur` and at most
         // the first chunk of the empty consume pass)
-        for (uint32_t u = 0; u < (uint32_t)ST; ++u) issue(u, cur, prev);
+        for (uint32_t u = 0; u < (uint32_t)ST; ++u) issue(u, cur, limit);
         if (drawing) pend = atomicAdd(cr.ticket, 1u);
     }
     __syncthreads();
-    uint32_t nxt = s_tk[1];
+    tq[SEG_LAG + 1] = s_tk[1];
     uint32_t phase = 0;  // parity of the next completion of each stage's barrier
     uint32_t it = 0;     // uses consumed
     typename Op::Acc acc;
@@ -589,8 +600,8 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         if (s_abort != 0) return false;
         if (threadIdx.x == 0 && it > 0) {
             const uint32_t u = it - 1 + ST;
-            if (u / uses == it / uses) issue(u, cur, prev);
-            else issue(u, nxt, cur);
+            if (u / uses == it / uses) issue(u, tq[SEG_LAG], tq[0]);
+            else issue(u, tq[SEG_LAG + 1], tq[1]);
         }
         if (valid) {
             phase ^= 1u << st;
@@ -598,7 +609,14 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         }
         return true;
     };
-    while ((cur < limit || prev < limit) && !stop) {
+    auto active = [&]() {
+        bool a = false;
+#pragma unroll
+        for (int i = 0; i <= SEG_LAG; ++i) a = a || tq[i] < limit;
+        return a;
+    };
+    while (active() && !stop) {
+        const uint32_t cur = tq[SEG_LAG], prev = tq[0];
         // ---- pass 1: the aggregate of the segment of `cur`
         const bool has_red = cur < limit;
         const uint32_t xr = has_red ? cur - cr.n_walk : 0u;
@@ -692,7 +710,7 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
             Op::finish(p, g, tc, regs, w, st, xs, acc);
         }
         if (stop) break;
-        // ---- next iteration: prev <- cur <- nxt <- drawn
+        // ---- next iteration: shift the ticket queue, append the one drawn
         if (threadIdx.x == 0) {
             uint32_t t2 = limit;
             if (drawing) {
@@ -704,9 +722,9 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
             s_tk[0] = t2;
         }
         __syncthreads();
-        prev = cur;
-        cur = nxt;
-        nxt = s_tk[0];
+#pragma unroll
+        for (int i = 0; i <= SEG_LAG; ++i) tq[i] = tq[i + 1];
+        tq[SEG_LAG + 1] = s_tk[0];
     }
     if (stop && threadIdx.x == 0) atomicOr(cr.err, ERRBIT_TIMEOUT);
     Op::at_exit(p, xs, acc);
@@ -874,8 +892,8 @@ cudaError_t launch_strip(const typename Op::Params& p, const Geom& g, const Carr
 }
 
 // Host: launch k_seg<Op, ST> (walker protocol, segmented, TMA staging).  The
-// segment length keeps the tiles between their two reads (about two segments
-// per CTA) within an L2 budget.
+// segment length keeps the tiles between their two reads (SEG_LAG + 1
+// segments per CTA) within an L2 budget.
 template <class Op, int ST>
 cudaError_t launch_seg(const typename Op::Params& p, Geom g, const Carry& cr, cudaStream_t s) {
     constexpr int L = Op::NW * Op::R, CW = 32 * Op::VEC;
@@ -914,8 +932,8 @@ cudaError_t launch_seg(const typename Op::Params& p, Geom g, const Carry& cr, cu
     }
     const uint32_t grid = persist_grid(g, cr, o);
     const uint64_t tile_ctas = grid > cr.n_walk ? grid - cr.n_walk : 1;
-    // two segments per CTA are in L2 at a time (one reduced, one consumed)
-    uint64_t seg = ((uint64_t)LR_SEG_L2MB << 20) / (2 * tile_ctas * SB);
+    // SEG_LAG + 1 segments per CTA are in L2 at a time
+    uint64_t seg = ((uint64_t)LR_SEG_L2MB << 20) / ((SEG_LAG + 1) * tile_ctas * SB);
     if (seg < (uint64_t)ST) seg = ST;  // the ring's look-ahead stays within one iteration
     if (seg < 2) seg = 2;
     if (seg > 64) seg = 64;

@@ -239,3 +239,32 @@ def test_activations_error_bound(cuda):
     assert th[-2] == 1.0 and th[-1] == -1.0 and sg[-2] == 1.0 and sg[-1] == 0.0
     nan_th, nan_sg = cuda.test_activations(torch.tensor([float("nan")], device="cuda"))
     assert torch.isnan(nan_th).all() and torch.isnan(nan_sg).all()
+
+
+@pytest.mark.parametrize("kmax", [1, 3, 4, 5, 6])
+def test_deer_kmax_across_launch_batches(cuda, kmax):
+    """Iterations are enqueued four at a time and those past the stopping test
+    do nothing: stopping at kmax inside, at the end of and past a batch gives
+    the oracle's iterate, count, status and residual history."""
+    T, B, D = 3001, 2, 128
+    wl = W.like(W.DEER, T, B, D, "f32")
+    inp = W.make_inputs(wl, 21)
+    dv, f = dev_inputs(inp, "f32"), f64_inputs(inp, "f32")
+    y, k, resid, hist, st = cuda.deer_diag_solve(dv["w"], dv["u"], None, eps=1e-5, kmax=kmax)
+    ry, rk, rhist, rst = oracle.deer(f["w"], f["u"], None, eps=1e-5, kmax=kmax)
+    assert (k, st == cuda.LR_OK) == (rk, rst == oracle.DEER_CONVERGED), (k, st, rk, rst)
+    assert_close("y", to_f64(y), ry, "f32")
+    np.testing.assert_allclose(hist[:k], rhist, rtol=1e-3, atol=1e-6)
+
+
+def test_deer_nonfinite_stops_the_batch(cuda):
+    """A NaN input makes the first residual non-finite: the solve stops there
+    (the rest of the batch returns at once) and reports LR_ERR_NONFINITE."""
+    T, B, D = 2000, 1, 128
+    wl = W.like(W.DEER, T, B, D, "f32")
+    inp = W.make_inputs(wl, 22)
+    dv = dev_inputs(inp, "f32")
+    dv["u"][100, 0, 7] = float("nan")
+    y, k, resid, hist, st = cuda.deer_diag_solve(dv["w"], dv["u"], None, eps=1e-5, kmax=20)
+    assert st == cuda.LR_ERR_NONFINITE and k == 1
+    assert cuda.last_error() == cuda.LR_OK
