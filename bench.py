@@ -45,8 +45,11 @@ EPS, KMAX = 1e-5, 20
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture, keyed by operation; valid only while the kernel sources hash to
-# `src`.  Filled from the committed ncu summaries under profiles/.
-NCU_TRAFFIC = {}
+# `src`.  Filled from the committed ncu summaries under profiles/.  deer.solve:
+# DRAM bytes read + written per launch, averaged over the K = 6 launches of a
+# solve (first iteration + 5 x second iteration, both captured at full size,
+# profiles/dram_traffic.md).
+NCU_TRAFFIC = {"deer.solve": {"bytes": 1175074603, "src": "af9c4b88ef5049cb"}}
 
 
 def src_hash() -> str:
