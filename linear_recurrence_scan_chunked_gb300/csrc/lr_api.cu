@@ -450,21 +450,20 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
     cudaStream_t s = (cudaStream_t)stream;
     DevWS* ws;
     TRY(get_ws(&ws));
-    // Both chain kernels (register and TMA-staged) on a problem of two time
-    // chunks and one channel tile, each with one CTA that is handed tile 1: it
-    // waits for the state after tile 0, which nobody publishes.
+    // Chain protocol: both chain kernels (register and TMA-staged) on a problem
+    // of two time chunks and one channel tile, each with one CTA that is handed
+    // tile 1: it waits for the state after tile 0, which nobody publishes.
+    // Walker protocol: the register and the segmented walker kernels on a long
+    // one-strip problem launched without walker CTAs: no entering state is ever
+    // published, so every consume's wait runs out.
     const int64_t C = tile_shape(OP_SCAN_FWD, LR_F32, true, CARRY_CHAIN).CW;
-    int64_t Tmax = 0;
-    for (int tma = 0; tma < 2; ++tma) {
-        const int64_t L = tile_shape(OP_SCAN_FWD, LR_F32, true, tma ? TILE_TMA : CARRY_CHAIN).L;
-        if (2 * L > Tmax) Tmax = 2 * L;
-    }
+    const int64_t Tw = 8192;  // >= 128 chunks of both walker tile shapes
     if (!ws->test_buf) {
-        CK(cudaMalloc(&ws->test_buf, (size_t)(3 * Tmax * C) * sizeof(float)));
-        CK(cudaMemset(ws->test_buf, 0, (size_t)(3 * Tmax * C) * sizeof(float)));
-        ws->bytes += 3 * Tmax * C * (int64_t)sizeof(float);
+        CK(cudaMalloc(&ws->test_buf, (size_t)(3 * Tw * C) * sizeof(float)));
+        CK(cudaMemset(ws->test_buf, 0, (size_t)(3 * Tw * C) * sizeof(float)));
+        ws->bytes += 3 * Tw * C * (int64_t)sizeof(float);
     }
-    float* a = (float*)ws->test_buf;
+    char* buf = (char*)ws->test_buf;
     TRY(enter(*ws, s));
     for (int tma = 0; tma < 2; ++tma) {
         const int64_t T = 2 * tile_shape(OP_SCAN_FWD, LR_F32, true, tma ? TILE_TMA : CARRY_CHAIN).L;
@@ -475,7 +474,20 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
         g.max_grid = 1;
         g.ticket_base = 1;
         cr.spin_limit = spin_limit;
-        CK(launch_scan_fwd(LR_F32, true, a, a + Tmax * C, nullptr, a + 2 * Tmax * C, g, cr, s));
+        const float* a = (const float*)buf;
+        CK(launch_scan_fwd(LR_F32, true, a, a + Tw * C, nullptr, (float*)buf + 2 * Tw * C, g, cr,
+                           s));
+    }
+    for (int dt = 0; dt < 2; ++dt) {  // fp32: register walker; bf16: segmented walker
+        const size_t es = dt ? 2 : 4;
+        Geom g;
+        Carry cr;
+        TRY(plan(*ws, OP_SCAN_FWD, dt, true, Tw, C, C, &g, &cr, s, 1));
+        if (cr.mode != CARRY_WALK || cr.tma != dt) return LR_ERR_INVALID_ARG;
+        cr.n_walk = 0;
+        cr.spin_limit = spin_limit;
+        CK(launch_scan_fwd(dt, true, buf, buf + Tw * C * es, nullptr, buf + 2 * Tw * C * es, g, cr,
+                           s));
     }
     return leave(*ws, s);
 }
