@@ -79,7 +79,7 @@ typedef enum {
     LR_ERR_INVALID_ARG = 1,   /* NULL required pointer, negative size, bad dtype */
     LR_ERR_ALIGN = 2,         /* pointer not aligned to its element size */
     LR_ERR_CUDA = 3,          /* a CUDA runtime call failed (message: lr_cuda_error_string) */
-    LR_ERR_TIMEOUT = 4,       /* device: a look-back wait ran out; outputs are NaN */
+    LR_ERR_TIMEOUT = 4,       /* device: a carry wait ran out; outputs are NaN */
     LR_ERR_NONFINITE = 5,     /* DEER: a residual was NaN or Inf */
     LR_ERR_NOT_CONVERGED = 6, /* DEER: kmax iterations without residual < eps */
     LR_ERR_TOO_LARGE = 7      /* sizes beyond the supported range */
@@ -182,7 +182,7 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y,
  *   - The first call on a device looks up the array's address; make it before
  *     any stream capture.
  *   - err_dev: optional device word (4-byte aligned) into which device-side
- *     errors are OR-ed (bit 0: a look-back wait ran out; h is then NaN); NULL
+ *     errors are OR-ed (bit 0: a carry wait ran out; h is then NaN); NULL
  *     keeps them inside the scratch array.  lr_last_error() does not see them.
  */
 int lr_scan_fwd_noalloc(const void* a, const void* b, const void* h0, void* h,

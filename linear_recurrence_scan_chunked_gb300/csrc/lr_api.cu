@@ -416,7 +416,7 @@ const char* lr_status_str(int st) {
         case LR_ERR_INVALID_ARG: return "invalid argument";
         case LR_ERR_ALIGN: return "pointer not aligned to its element size";
         case LR_ERR_CUDA: return "CUDA runtime error";
-        case LR_ERR_TIMEOUT: return "look-back wait ran out on the device";
+        case LR_ERR_TIMEOUT: return "a carry wait ran out on the device";
         case LR_ERR_NONFINITE: return "non-finite residual";
         case LR_ERR_NOT_CONVERGED: return "not converged within kmax iterations";
         case LR_ERR_TOO_LARGE: return "problem size beyond the supported range";

@@ -1,6 +1,6 @@
 // lr_launch.h -- host-side interface between the C ABI (lr_api.cu) and the
 // kernel translation units.  Each operation exposes its tile shape (so the
-// API can size the look-back workspace) and a launcher that picks the
+// API can size the carry workspace) and a launcher that picks the
 // template instance for the storage type and the vector / scalar path.
 #pragma once
 

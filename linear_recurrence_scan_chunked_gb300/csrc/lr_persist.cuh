@@ -1,5 +1,10 @@
-// lr_persist.cuh -- the persistent streaming kernel shared by all five
-// operations (see k_stream below).
+// lr_persist.cuh -- the persistent kernels shared by all five operations:
+//   k_strip  (wide problems: channel strips walked through time, TMA-staged),
+//   k_seg    (long, narrow problems: walker protocol over segments, TMA-staged),
+//   k_tchain (chain protocol, TMA-staged, for what is neither),
+//   k_stream (walker protocol through registers),
+//   k_chain  (chain protocol through registers: scalar / unaligned paths),
+// and launch_persist, which picks one for a call.
 //
 // An operation is a policy struct `Op` providing:
 //   S, VEC, NW, R, REV, MINB      storage type, channels per lane, warps, rows
@@ -11,7 +16,12 @@
 //                                 finish(), extra shared memory, per-thread
 //                                 accumulators kept across tiles
 //   init_ptr(p)                   state before the scan (nullable)
-//   load(p, g, tc, regs)          issue the loads of one tile
+//   skip(p)                       the whole launch has nothing to do (checked
+//                                 first by every CTA)
+//   load(src, p, g, tc, regs)     the loads of one tile, from global memory or
+//                                 from a TMA-staged tile (GlobalSrc / SmemSrc)
+//   TMA_N, tma_shift, tma_extra, tma_arrays   the arrays staged by TMA
+//                                 (lr_tma.cuh)
 //   aggregate(p, g, tc, regs, w, A, B, side)  this thread's (A, B) over its R
 //                                 rows in scan order; with side = true it also
 //                                 writes the outputs that need no carry
@@ -53,12 +63,6 @@ __device__ __forceinline__ TileCoord tile_coord_qj(const Geom& g, uint32_t q, ui
 template <class Op>
 __device__ __forceinline__ TileCoord tile_coord(const Geom& g, uint32_t tile) {
     return tile_coord_qj<Op>(g, tile / (uint32_t)g.n_ct, tile % (uint32_t)g.n_ct);
-}
-
-// Time of row r (scan order) of this thread.
-template <class Op>
-__device__ __forceinline__ int64_t row_t(const TileCoord& tc, int r) {
-    return Op::REV ? tc.t0 - r : tc.t0 + r;
 }
 
 // Issue the global loads of one tile (register kernels).

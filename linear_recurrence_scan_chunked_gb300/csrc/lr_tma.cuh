@@ -3,10 +3,11 @@
 // A tile of every input array (L time rows x CW channels of the [T, C]
 // sequence, C = B*D contiguous) is one 2-D box of a tensor map: one
 // cp.async.bulk.tensor per array per tile moves it from HBM into a stage of a
-// shared-memory ring, and an mbarrier counts its bytes in.  A producer warp
-// keeps STAGES tiles in flight per CTA without holding registers, so the
-// bytes in flight per SM no longer depend on the registers of the arithmetic
-// warps (in the register-double-buffered kernels they do).
+// shared-memory ring, and an mbarrier counts its bytes in.  One thread (or, in
+// the TMA chain kernel, a producer warp) keeps the ring's stages in flight per
+// CTA without holding registers, so the bytes in flight per SM no longer depend
+// on the registers of the arithmetic warps (in the register-double-buffered
+// kernels they do).
 //
 // Shared-memory layout of one stage: array k of the operation at byte offset
 // tma_off<Op>(k) (128-byte aligned), rows in time order, row pitch CW *

@@ -168,8 +168,8 @@ def test_repeat_is_bitwise_deterministic(cuda, shape):
 
 
 def test_long_scan_is_bitwise_deterministic(cuda):
-    """Many chunks along time: the look-back sees different inclusive
-    predecessors from run to run, yet the carry is folded in a fixed order."""
+    """Many chunks along time: tiles and walkers interleave differently from
+    run to run, yet every carry is folded in an order fixed by position."""
     T, B, D = 300000, 1, 128
     wl = W.like(W.SCAN_LONG, T, B, D)
     dv = dev_inputs(W.make_inputs(wl, 13), "f32")
