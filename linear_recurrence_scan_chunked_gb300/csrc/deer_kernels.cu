@@ -38,6 +38,7 @@ struct DeerOp {
     static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
     static constexpr bool REV = false;
     static constexpr int IN_ARRAYS = 2;  // u, previous iterate
+    static constexpr bool SCRATCH_IN_CARRY = false;
     using Params = DeerParams<S>;
     struct Regs {
         Pack<S, VEC> u[R];

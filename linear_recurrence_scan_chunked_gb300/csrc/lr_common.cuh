@@ -733,27 +733,28 @@ __device__ __forceinline__ void tile_carry(CarrySmem<VEC, NW>& sm, const float (
     for (int v = 0; v < VEC; ++v) start[v] = __fmaf_rn(PA[v], sm.carry[lane][v], PB[v]);
 }
 
-// Shared memory of the strip kernel's carry: every warp's aggregate and the
-// state entering every warp's first row.
+// Shared memory of the strip kernel's carry: every warp's aggregate.
 template <int VEC, int NW>
 struct StripSmem {
-    float a[NW][32][VEC];  // a and b are contiguous: the op's scratch overlays them
+    float a[NW][32][VEC];
     float b[NW][32][VEC];
-    float start[NW][32][VEC];
 };
 
 // Whole CTA, strip kernel.  (A, B): this thread's aggregate over its R rows.
-// The state before this chunk is `init` (first chunk) or this CTA's state
-// after the previous chunk of the same channel strip (`carry`, [32][VEC] in
-// shared memory); warp 0 folds the warp aggregates into it in row order,
-// leaving each warp's entering state in shared memory and the state after
-// the chunk in `carry`.  Returns in `start` the state entering this thread's
-// first row.  The association is fixed by position: bitwise reproducible.
+// The state before this chunk is `init` (first chunk; every warp passes it) or
+// this CTA's state after the previous chunk of the same channel strip,
+// carry[par] ([32][VEC] in shared memory, par = chunk parity).  After one
+// barrier every warp folds the aggregates of the warps before it, in row
+// order, into that state -- the state entering its rows -- and the last warp
+// continues with its own aggregate and leaves the state after the chunk in
+// carry[par ^ 1].  Every warp applies the same operations in the same order,
+// so the bits are fixed by position.  Returns in `start` the state entering
+// this thread's first row.
 template <int VEC, int NW>
 __device__ __forceinline__ void strip_carry(StripSmem<VEC, NW>& sm, const float (&A)[VEC],
                                             const float (&B)[VEC], const float (&init)[VEC],
-                                            float (&start)[VEC], float (*carry)[VEC], bool first,
-                                            bool cok) {
+                                            float (&start)[VEC], float (*carry)[32][VEC], int par,
+                                            bool first, bool cok) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
     for (int v = 0; v < VEC; ++v) {
@@ -761,21 +762,19 @@ __device__ __forceinline__ void strip_carry(StripSmem<VEC, NW>& sm, const float 
         sm.b[warp][lane][v] = B[v];
     }
     csync<NW>();
-    if (warp == 0) {
+    float st[VEC];
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            float st = first ? (cok ? init[v] : 0.f) : carry[lane][v];
+    for (int v = 0; v < VEC; ++v) st[v] = first ? (cok ? init[v] : 0.f) : carry[par][lane][v];
+#pragma unroll 1
+    for (int w = 0; w < warp; ++w)
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                sm.start[w][lane][v] = st;
-                st = __fmaf_rn(sm.a[w][lane][v], st, sm.b[w][lane][v]);
-            }
-            carry[lane][v] = st;
-        }
+        for (int v = 0; v < VEC; ++v) st[v] = __fmaf_rn(sm.a[w][lane][v], st[v], sm.b[w][lane][v]);
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) start[v] = st[v];
+    if (warp == NW - 1) {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) carry[par ^ 1][lane][v] = __fmaf_rn(A[v], st[v], B[v]);
     }
-    csync<NW>();
-#pragma unroll
-    for (int v = 0; v < VEC; ++v) start[v] = sm.start[warp][lane][v];
 }
 
 // Whole CTA, walker protocol, look-ahead phase: combine the warp aggregates

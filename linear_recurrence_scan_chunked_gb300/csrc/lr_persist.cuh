@@ -370,6 +370,18 @@ __global__ void __maxnreg__(LR_TMA_MAXNREG)
 // previous tile into registers, it re-arms that tile's stage with the tile ST
 // - 1 ahead.  All warps compute (no producer warp), so two CTAs of 8 warps
 // fit an SM with up to 128 registers a thread.
+template <class Op>
+using OpScratch = typename std::conditional<Op::SCRATCH_IN_CARRY, int, typename Op::Smem>::type;
+template <class Op, class SM>
+__device__ __forceinline__ typename Op::Smem& scratch(SM& sm, OpScratch<Op>& own) {
+    if constexpr (Op::SCRATCH_IN_CARRY) {
+        static_assert(sizeof(typename Op::Smem) <= sizeof(sm.a) + sizeof(sm.b), "op scratch too large");
+        return *reinterpret_cast<typename Op::Smem*>(&sm.a[0][0][0]);
+    } else {
+        return own;
+    }
+}
+
 constexpr int STRIP_MAX = 64;  // strips per CTA (state kept in shared memory)
 
 // Use `it` of this CTA: chunk q = it / m of its strip i = it % m, j = b + i*G.
@@ -409,17 +421,18 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
     unsigned char* ring = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~(uintptr_t)127);
     __shared__ StripSmem<VEC, NW> sm;
-    // the op's scratch (bias partials, residual maxima) is only used after
-    // strip_carry has finished with the warp aggregates: it shares their space
-    static_assert(sizeof(typename Op::Smem) <= sizeof(sm.a) + sizeof(sm.b), "op scratch too large");
-    typename Op::Smem& xs = *reinterpret_cast<typename Op::Smem*>(&sm.a[0][0][0]);
+    // the op's scratch: its own space, or over the warp aggregates when the op
+    // says it synchronises before using it
+    __shared__ OpScratch<Op> xs_own;
+    typename Op::Smem& xs = scratch<Op>(sm, xs_own);
     __shared__ __align__(8) uint64_t full[ST];
     __shared__ uint32_t s_abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // strips of this CTA: j = blockIdx.x + i*G < n_ct; their states follow the ring
+    // strips of this CTA: j = blockIdx.x + i*G < n_ct; their states (two
+    // slots each, by chunk parity) follow the ring
     const uint32_t m = ((uint32_t)g.n_ct - blockIdx.x + G - 1) / G;
     const uint32_t n_it = m * (uint32_t)g.n_chunks;
-    float(*carry)[32][VEC] = reinterpret_cast<float(*)[32][VEC]>(ring + ST * SB);
+    float(*carry)[2][32][VEC] = reinterpret_cast<float(*)[2][32][VEC]>(ring + ST * SB);
     uint32_t issued = 0;  // thread 0: uses whose loads were issued
     if (threadIdx.x == 0) {
         for (int i = 0; i < ST; ++i) mbar_init(&full[i], 1);
@@ -458,10 +471,9 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
 #pragma unroll
         for (int v = 0; v < VEC; ++v) init[v] = 0.f;
         const typename Op::S* ip = Op::init_ptr(p);
-        if (tc.q == 0 && warp == 0 && ip != nullptr && tc.cok)
-            load_vec<typename Op::S, VEC>(ip + tc.c, init);
+        if (tc.q == 0 && ip != nullptr && tc.cok) load_vec<typename Op::S, VEC>(ip + tc.c, init);
         float s[VEC];
-        strip_carry<VEC, NW>(sm, A, B, init, s, carry[it % m], tc.q == 0, tc.cok);
+        strip_carry<VEC, NW>(sm, A, B, init, s, carry[it % m], (int)(q & 1u), tc.q == 0, tc.cok);
         Op::finish(p, g, tc, regs, w, s, xs, acc);
     }
     Op::at_exit(p, xs, acc);
@@ -525,9 +537,11 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
     unsigned char* ring = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~(uintptr_t)127);
     __shared__ StripSmem<VEC, NW> sm;
-    static_assert(sizeof(typename Op::Smem) <= sizeof(sm.a) + sizeof(sm.b), "op scratch too large");
-    typename Op::Smem& xs = *reinterpret_cast<typename Op::Smem*>(&sm.a[0][0][0]);
-    __shared__ float carry[32][VEC];
+    // the op's scratch: its own space, or over the warp aggregates when the op
+    // says it synchronises before using it
+    __shared__ OpScratch<Op> xs_own;
+    typename Op::Smem& xs = scratch<Op>(sm, xs_own);
+    __shared__ float carry[2][32][VEC];  // by chunk parity
     __shared__ __align__(8) uint64_t full[ST];
     __shared__ uint32_t s_tk[2], s_abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -694,7 +708,7 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
                 }
             }
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) carry[lane][v] = cin[v];
+            for (int v = 0; v < VEC; ++v) carry[0][lane][v] = cin[v];
         }
         for (uint32_t c = 0; c < sg.seg; ++c, ++it) {
             const uint32_t q = seg_c * sg.seg + c;
@@ -710,7 +724,7 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
             float s0[VEC], st[VEC];
 #pragma unroll
             for (int v = 0; v < VEC; ++v) s0[v] = 0.f;
-            strip_carry<VEC, NW>(sm, A, B, s0, st, carry, false, tc.cok);
+            strip_carry<VEC, NW>(sm, A, B, s0, st, carry, (int)(c & 1u), false, tc.cok);
             Op::finish(p, g, tc, regs, w, st, xs, acc);
         }
         if (stop) break;
@@ -852,7 +866,7 @@ cudaError_t launch_strip(const typename Op::Params& p, const Geom& g, const Carr
                          cudaStream_t s) {
     constexpr int L = Op::NW * Op::R, CW = 32 * Op::VEC;
     constexpr size_t ring = (size_t)ST * tma_stage_bytes<Op>() + 128;
-    constexpr size_t strip_bytes = 32 * Op::VEC * sizeof(float);
+    constexpr size_t strip_bytes = 2 * 32 * Op::VEC * sizeof(float);  // two carry slots
     static int occ[64] = {0}, n_sm[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);

@@ -36,6 +36,7 @@ struct ScanFwdOp {
     static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
     static constexpr bool REV = false;
     static constexpr int IN_ARRAYS = 2;  // a, b
+    static constexpr bool SCRATCH_IN_CARRY = false;
     using Params = ScanFwdParams<S>;
     struct Regs {
         Pack<S, VEC> a[R], b[R];
@@ -115,6 +116,7 @@ struct ScanBwdOp {
     static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
     static constexpr bool REV = true;
     static constexpr int IN_ARRAYS = 3;  // a, dh, h
+    static constexpr bool SCRATCH_IN_CARRY = false;
     using Params = ScanBwdParams<S>;
     struct Regs {
         Pack<S, VEC> a[R], g[R], hp[R];  // a_t, dh_t, h_{t-1}

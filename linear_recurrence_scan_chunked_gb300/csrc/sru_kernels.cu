@@ -40,6 +40,7 @@ struct SruFwdOp {
     static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
     static constexpr bool REV = false;
     static constexpr int IN_ARRAYS = 4;  // xt, uf, ur, x
+    static constexpr bool SCRATCH_IN_CARRY = false;
     using Params = SruFwdParams<S>;
     struct Regs {
         Pack<S, VEC> xt[R], uf[R], ur[R], x[R];
@@ -168,6 +169,10 @@ struct SruBwdOp {
         float pf[NW][32][VEC];
         float pr[NW][32][VEC];
     };
+    // The 8 KB of partial sums may overlay the carry's warp aggregates (the
+    // TMA kernels do that to keep two CTAs per SM): finish() writes them only
+    // after a barrier that every warp reaches once it is done with those.
+    static constexpr bool SCRATCH_IN_CARRY = true;
     struct Acc {};
     __device__ static void acc_init(Acc&) {}
     __device__ static bool skip(const Params&) { return false; }
@@ -279,6 +284,7 @@ struct SruBwdOp {
         if (tc.tchunk == 0 && warp == NW - 1 && p.dc0 != nullptr && tc.cok)
             store_vec<S, VEC>(p.dc0 + tc.c, s);
         // bias-gradient partials of this tile: sum over its rows, fixed warp order
+        csync<NW>();  // every warp is past its reads of the carry smem
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
             xs.pf[warp][lane][v] = sum_f[v];
