@@ -268,3 +268,20 @@ def test_deer_nonfinite_stops_the_batch(cuda):
     y, k, resid, hist, st = cuda.deer_diag_solve(dv["w"], dv["u"], None, eps=1e-5, kmax=20)
     assert st == cuda.LR_ERR_NONFINITE and k == 1
     assert cuda.last_error() == cuda.LR_OK
+
+
+@pytest.mark.parametrize("shape", [(300, 3, 40), (9000, 2, 512), (45, 40, 1000)])
+def test_deer_bf16(cuda, shape):
+    """bf16 storage (the iterates are stored in bf16, so the stopping test sees
+    bf16 iterates): converges, and the solution matches the fp64 fixed point
+    within the bf16 tolerance.  The iteration count can differ from the fp64
+    oracle's by the rounding of the stored iterate; fp32 checks it exactly."""
+    T, B, D = shape
+    wl = W.like(W.DEER, T, B, D, "bf16")
+    inp = W.make_inputs(wl, 23)
+    dv, f = dev_inputs(inp, "bf16"), f64_inputs(inp, "bf16")
+    y, k, resid, hist, st = cuda.deer_diag_solve(dv["w"], dv["u"], None, eps=1e-2, kmax=20)
+    ry, rk, rhist, rst = oracle.deer(f["w"], f["u"], None, eps=1e-2, kmax=20)
+    assert st == cuda.LR_OK and rst == oracle.DEER_CONVERGED
+    assert abs(k - rk) <= 1, (k, rk, hist, list(rhist))
+    assert_close("y", to_f64(y), ry, "bf16")

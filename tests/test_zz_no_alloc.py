@@ -40,7 +40,10 @@ def _p(t):
 
 
 @pytest.mark.parametrize("dtype,shape", [("f32", (1024, 4, 256)), ("f32", (3001, 2, 100)),
-                                         ("bf16", (777, 3, 512))])
+                                         ("bf16", (777, 3, 512)),
+                                         # strip kernel; walker kernels (register, segmented)
+                                         ("f32", (40, 40, 1000)), ("f32", (20000, 1, 128)),
+                                         ("bf16", (20000, 1, 128))])
 def test_noalloc_matches_allocating_scan_twice(cuda, dtype, shape):
     T, B, D = shape
     wl = W.like(W.SCAN_TINY, T, B, D, dtype)
