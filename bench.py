@@ -49,17 +49,21 @@ EPS, KMAX = 1e-5, 20
 # DRAM bytes read + written per launch, averaged over the K = 6 launches of a
 # solve (first iteration + 5 x second iteration, both captured at full size,
 # profiles/dram_traffic.md).
-NCU_TRAFFIC = {"deer.solve": {"bytes": 1174852011, "src": "66c0298c3aee7065"}}
+NCU_TRAFFIC = {"deer.solve": {"bytes": 1174852011, "src": "cc0c561d98f6cd4c"}}
 
 
 def src_hash() -> str:
-    """Hash of the sources the kernels are compiled from (device code and the
-    launch configuration; the host-only C-ABI files do not change a kernel)."""
+    """Hash of the code the kernels are compiled from (device code and the
+    launch configuration, comments and blank lines left out; the host-only
+    C-ABI files do not change a kernel)."""
     h = hashlib.sha256()
     cdir = os.path.join(ROOT, "linear_recurrence_scan_chunked_gb300", "csrc")
     for n in sorted(os.listdir(cdir)):
         if n.endswith((".cuh", "_kernels.cu")) or n == "lr_launch.h":
-            h.update(open(os.path.join(cdir, n), "rb").read())
+            for line in open(os.path.join(cdir, n)):
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -164,12 +164,6 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
     if (tile_role) Op::at_exit(p, xs, acc);
 }
 
-// Chain protocol (many channel tiles, few chunks): persistent CTAs walk their
-// tiles in ticket order with two register sets.  While tile i is processed
-// (local scan, wait for the state after the previous chunk, output pass) the
-// loads of tile i+1 are in flight and the ticket of tile i+2 is being drawn.
-// The chunk chain costs about one round trip per chunk level, hidden behind
-// the tiles of the other channel tiles.
 // Whole consumer CTA: one tile whose data is in registers -- local scan,
 // state entering the tile (chain protocol), output pass.
 template <class Op>
@@ -211,6 +205,12 @@ __device__ __forceinline__ uint32_t chain_tile(const typename Op::Params& p, con
     return draw ? *s_ticket : 0xffffffffu;
 }
 
+// Chain protocol through registers (scalar and unaligned paths): persistent
+// CTAs walk their tiles in ticket order with two register sets.  While tile i
+// is processed (local scan, wait for the state after the previous chunk,
+// output pass) the loads of tile i+1 are in flight and the ticket of tile i+2
+// is being drawn.  The chunk chain costs about one round trip per chunk level,
+// hidden behind the tiles of the other channel tiles.
 template <class Op>
 __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
     k_chain(typename Op::Params p, Geom g, Carry cr) {
@@ -359,17 +359,9 @@ __global__ void __maxnreg__(LR_TMA_MAXNREG)
     Op::at_exit(p, xs, acc);
 }
 
-// Strip kernel (chain protocol, wide problems): CTA b owns the channel
-// strips j = b, b + G, b + 2G, ... (G CTAs) and walks them through time,
-// chunk level by chunk level: (0, j1), (0, j2), ..., (1, j1), ...  The state
-// after each chunk of a strip stays in this CTA's shared memory, so no tile
-// waits for another CTA and nothing is drawn or polled; the tile sequence of
-// every CTA is fixed in advance.  Thread 0 keeps ST - 1 tiles of that
-// sequence streaming in through the TMA ring: at the top of each iteration,
-// after the barrier that also tells it that every warp has copied the
-// previous tile into registers, it re-arms that tile's stage with the tile ST
-// - 1 ahead.  All warps compute (no producer warp), so two CTAs of 8 warps
-// fit an SM with up to 128 registers a thread.
+// The op's scratch in the TMA strip and segmented kernels: its own space, or
+// over the warp aggregates when the op synchronises before using it
+// (SCRATCH_IN_CARRY; it keeps the shared memory of two CTAs within an SM).
 template <class Op>
 using OpScratch = typename std::conditional<Op::SCRATCH_IN_CARRY, int, typename Op::Smem>::type;
 template <class Op, class SM>
@@ -382,6 +374,17 @@ __device__ __forceinline__ typename Op::Smem& scratch(SM& sm, OpScratch<Op>& own
     }
 }
 
+// Strip kernel (chain protocol, wide problems): CTA b owns the channel
+// strips j = b, b + G, b + 2G, ... (G CTAs) and walks them through time,
+// chunk level by chunk level: (0, j1), (0, j2), ..., (1, j1), ...  The state
+// after each chunk of a strip stays in this CTA's shared memory, so no tile
+// waits for another CTA and nothing is drawn or polled; the tile sequence of
+// every CTA is fixed in advance.  Thread 0 keeps ST - 1 tiles of that
+// sequence streaming in through the TMA ring: at the top of each iteration,
+// after the barrier that also tells it that every warp has copied the
+// previous tile into registers, it re-arms that tile's stage with the tile ST
+// - 1 ahead.  All warps compute (no producer warp), so two CTAs of 8 warps
+// fit an SM with up to 128 registers a thread.
 constexpr int STRIP_MAX = 64;  // strips per CTA (state kept in shared memory)
 
 // Use `it` of this CTA: chunk q = it / m of its strip i = it % m, j = b + i*G.
@@ -421,8 +424,6 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
     unsigned char* ring = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~(uintptr_t)127);
     __shared__ StripSmem<VEC, NW> sm;
-    // the op's scratch: its own space, or over the warp aggregates when the op
-    // says it synchronises before using it
     __shared__ OpScratch<Op> xs_own;
     typename Op::Smem& xs = scratch<Op>(sm, xs_own);
     __shared__ __align__(8) uint64_t full[ST];
@@ -537,8 +538,6 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
     unsigned char* ring = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~(uintptr_t)127);
     __shared__ StripSmem<VEC, NW> sm;
-    // the op's scratch: its own space, or over the warp aggregates when the op
-    // says it synchronises before using it
     __shared__ OpScratch<Op> xs_own;
     typename Op::Smem& xs = scratch<Op>(sm, xs_own);
     __shared__ float carry[2][32][VEC];  // by chunk parity
