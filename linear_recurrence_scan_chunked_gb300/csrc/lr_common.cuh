@@ -13,24 +13,25 @@
 // GB300 layout of the work:
 //   * the sequence is [T, C] with C = B*D channels contiguous;
 //   * a tile is L = NW*R time rows x CW = 32*VEC channels;  lane l of every warp
-//     owns channels [l*VEC, l*VEC+VEC) of the tile (one 16-byte vector per row,
-//     so one warp row is a 512-byte coalesced segment), warp w owns the R
-//     consecutive rows [w*R, w*R+R) in scan order;
+//     owns channels [l*VEC, l*VEC+VEC) of the tile (4 channels: a 16-byte fp32
+//     or 8-byte bf16 vector per row, so one warp row is one contiguous 512 /
+//     256-byte segment), warp w owns the R consecutive rows [w*R, w*R+R) in
+//     scan order;
 //   * each thread scans its R rows sequentially in registers (depth R), the NW
 //     warp aggregates are combined through shared memory (depth NW), and the
-//     carry between time chunks comes from one of two single-pass protocols:
+//     state between time chunks comes from one of three single-pass schemes:
+//       STRIP -- a CTA owns whole channel strips and walks them through time:
+//                the state stays in its shared memory (wide problems);
 //       CHAIN -- tile q waits for the state after chunk q-1 and publishes the
-//                state after chunk q.  One L2 round trip per chunk level: best
-//                when there are many channel tiles and few chunks, because the
-//                tiles of one chunk level stream while the chain advances;
-//       WALK  -- tile q publishes its aggregate (A, B) and waits for the state
-//                after chunk q-1, which dedicated walker CTAs compute: a warp
-//                owns a few channels, its lanes own 32 consecutive chunks, and a
-//                Kogge-Stone prefix over the 32 aggregates plus the carried
-//                block state gives 32 states at once.  Best for long sequences
-//                with few channels (the chain would cost one round trip per
-//                chunk; here it costs one per 32 chunks, overlapped).
-//     Both fix the association of every floating-point operation by position
+//                state after chunk q.  One L2 round trip per chunk level;
+//       WALK  -- tiles (or segments of tiles) publish their aggregate (A, B)
+//                and wait for the state before them, which dedicated walker
+//                CTAs compute: a warp owns a few channels, its lanes own
+//                WALK_P consecutive chunks each, and a Kogge-Stone prefix over
+//                the lanes' folds plus the carried state gives a window of
+//                32*WALK_P states at once.  For long sequences with few
+//                channels (the chain would cost one round trip per chunk).
+//     All fix the association of every floating-point operation by position
 //     alone, so results are bitwise reproducible run to run.
 //   * every published value is a self-validating 64-bit packet (value << 32 |
 //     epoch): no memory fence sits on the critical path, and packets left by

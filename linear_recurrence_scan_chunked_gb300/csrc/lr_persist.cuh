@@ -595,8 +595,8 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         if (t1 == g.n_draws - 1) atomicExch(cr.ticket, 0u);
         if (t1 >= limit) drawing = false;
         s_tk[1] = t1;
-        // uses 0 .. ST-1 (ST <= SEG + 1: the reduce pass of `cur` and at most
-        // the first chunk of the empty consume pass)
+        // uses 0 .. ST-1: the first chunks of the reduce pass of `cur` (the
+        // launch keeps SEG >= ST)
         for (uint32_t u = 0; u < (uint32_t)ST; ++u) issue(u, cur, limit);
         if (drawing) pend = atomicAdd(cr.ticket, 1u);
     }
@@ -633,10 +633,10 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         return a;
     };
     while (active() && !stop) {
-        const uint32_t cur = tq[SEG_LAG], prev = tq[0];
-        // ---- pass 1: the aggregate of the segment of `cur`
-        const bool has_red = cur < limit;
-        const uint32_t xr = has_red ? cur - cr.n_walk : 0u;
+        const uint32_t tk_red = tq[SEG_LAG], tk_con = tq[0];
+        // ---- pass 1: the aggregate of the segment of `tk_red`
+        const bool has_red = tk_red < limit;
+        const uint32_t xr = has_red ? tk_red - cr.n_walk : 0u;
         const uint32_t seg_r = xr / (uint32_t)g.n_ct, j_r = xr - seg_r * (uint32_t)g.n_ct;
         float SA[VEC], SBv[VEC];
 #pragma unroll
@@ -679,9 +679,9 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
                             pkt(SBv[v], cr.epoch));
             }
         }
-        // ---- pass 2: the outputs of the segment of `prev`
-        const bool has_con = prev < limit;
-        const uint32_t xc = has_con ? prev - cr.n_walk : 0u;
+        // ---- pass 2: the outputs of the segment of `tk_con`
+        const bool has_con = tk_con < limit;
+        const uint32_t xc = has_con ? tk_con - cr.n_walk : 0u;
         const uint32_t seg_c = xc / (uint32_t)g.n_ct, j_c = xc - seg_c * (uint32_t)g.n_ct;
         if (warp == 0 && has_con) {  // the state entering that segment
             const TileCoord tc = tile_coord_qj<Op>(g, seg_c * sg.seg, j_c);
