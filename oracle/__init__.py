@@ -59,6 +59,7 @@ def _load():
         lib.lro_rollout_tanh.argtypes = [I64, I64, I64, P, P, P, P]
         lib.lro_deer_step.argtypes = [I64, I64, I64, P, P, P, P, P, P]
         lib.lro_deer.argtypes = [I64, I64, I64, P, P, P, ctypes.c_double, ctypes.c_int, P, P, P]
+        lib.lro_deer_bwd.argtypes = [I64, I64, I64] + [P] * 7
         lib.lro_deer.restype = ctypes.c_int
         lib.lro_num_threads.restype = ctypes.c_int
         lib.lro_set_num_threads.argtypes = [ctypes.c_int]
@@ -151,6 +152,19 @@ def deer_step(w, u, yprev=None, h0=None):
     _load().lro_deer_step(T, C, w.shape[0], _p(w), _p(u), _p(h0), _p(yprev), _p(y),
                           ctypes.byref(rho))
     return y, rho.value
+
+
+def deer_bwd(w, y, g, h0=None):
+    """Gradient through the DEER solution y (the tanh-RNN rollout) for the
+    upstream dL/dy = g. Returns (du, dw, dh0)."""
+    w, y, g, h0 = _f64(w), _f64(y), _f64(g), _f64(h0)
+    T, C = _tc(y)
+    D = w.shape[0]
+    du = np.empty_like(y)
+    dw = np.zeros(D)
+    dh0 = np.empty(y.shape[1:]) if y.ndim == 3 else np.empty(C)
+    _load().lro_deer_bwd(T, C, D, _p(w), _p(y), _p(h0), _p(g), _p(du), _p(dw), _p(dh0))
+    return du, dw, dh0
 
 
 DEER_CONVERGED, DEER_NOT_CONVERGED, DEER_NONFINITE = 0, 1, 2

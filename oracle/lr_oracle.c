@@ -293,3 +293,43 @@ int lro_deer(int64_t T, int64_t C, int64_t D, const double* w, const double* u,
     free(prev);
     return status;
 }
+
+/* ------------------------------------- DEER backward (next row), tanh RNN */
+/*
+ * Gradient through the solution y of h_t = tanh(w (.) h_{t-1} + u_t)
+ * ([P4] "核心原理": at the fixed point y is the rollout, so the gradient is
+ * back-propagation through the rollout evaluated at y):
+ *   s_t = w y_{t-1} + u_t, y_t = tanh(s_t), dy_t/dy_{t-1} = w (1 - y_t^2);
+ *   delta_{T-1} = g_{T-1},  delta_t = g_t + w (1 - y_{t+1}^2) delta_{t+1}
+ *     (delta_t: total derivative of L = sum g.y with respect to y_t);
+ *   du_t = delta_t (1 - y_t^2);  dw_d = sum over t and the channels of
+ *   feature d of du_t y_{t-1} (y_{-1} = h0);  dh0 = w (1 - y_0^2) delta_0.
+ * g is the upstream gradient dL/dy.  dh0 may be NULL.
+ */
+void lro_deer_bwd(int64_t T, int64_t C, int64_t D, const double* w,
+                  const double* y, const double* h0, const double* g, double* du,
+                  double* dw, double* dh0) {
+    double* sw = (double*)calloc((size_t)(C > 0 ? C : 1), sizeof(double));
+    if (!sw) {
+        for (int64_t d = 0; d < D; ++d) dw[d] = NAN;
+        return;
+    }
+    PAR_BEGIN
+    for (int64_t k = c0_; k < c1_; ++k) {
+        const double wk = w[k % D];
+        double delta = 0.0;
+        for (int64_t t = T - 1; t >= 0; --t) {
+            const int64_t i = t * C + k;
+            if (t == T - 1) delta = g[i];
+            else delta = g[i] + wk * (1.0 - y[i + C] * y[i + C]) * delta;
+            du[i] = delta * (1.0 - y[i] * y[i]);
+            const double yprev = t > 0 ? y[i - C] : (h0 ? h0[k] : 0.0);
+            sw[k] += du[i] * yprev;
+        }
+        if (dh0) dh0[k] = T > 0 ? wk * (1.0 - y[k] * y[k]) * delta : 0.0;
+    }
+    PAR_END
+    for (int64_t d = 0; d < D; ++d) dw[d] = 0.0;
+    for (int64_t k = 0; k < C; ++k) dw[k % D] += sw[k];
+    free(sw);
+}

@@ -338,6 +338,52 @@ def test_deer_stopping_rule_edges():
     assert (k, st, len(hist)) == (5, oracle.DEER_NOT_CONVERGED, 5)
 
 
+# ----------------------------------------------------------- DEER backward
+
+def test_deer_bwd_finite_differences_of_the_rollout():
+    """The gradient through the solution, against central differences of
+    L = sum g . rollout(w, u, h0) -- the quantity the gradient is of, computed
+    by the direct sequential tanh RNN, not by the backward code."""
+    T, B, D = 6, 2, 3
+    r = np.random.default_rng(21)
+    p = {"w": r.uniform(-0.9, 0.9, D), "u": r.standard_normal((T, B, D)),
+         "h0": r.standard_normal((B, D))}
+    g = r.standard_normal((T, B, D))
+    loss = lambda: float(np.sum(g * oracle.rollout_tanh(**p)))
+    y = oracle.rollout_tanh(**p)
+    du, dw, dh0 = oracle.deer_bwd(p["w"], y, g, p["h0"])
+    for got, key in ((du, "u"), (dw, "w"), (dh0, "h0")):
+        np.testing.assert_allclose(got, _fd(loss, p[key]), rtol=1e-6, atol=1e-8, err_msg=key)
+
+
+def test_deer_bwd_w_zero_is_tanh_derivative():
+    """w = 0: no time coupling, du = g tanh'(u) (numpy's tanh), dh0 = 0."""
+    T, B, D = 30, 2, 4
+    u = rng.standard_normal((T, B, D))
+    g = rng.standard_normal((T, B, D))
+    y = np.tanh(u)
+    du, dw, dh0 = oracle.deer_bwd(np.zeros(D), y, g, rng.standard_normal((B, D)))
+    np.testing.assert_allclose(du, g * (1.0 - np.tanh(u) ** 2), rtol=1e-14, atol=1e-15)
+    np.testing.assert_array_equal(dh0, np.zeros((B, D)))
+
+
+def test_deer_bwd_small_signal_is_linear_scan_backward():
+    """At amplitude 1e-6 tanh is the identity to O(1e-12), so the gradient is
+    the linear scan's (coefficient w): du ~ db and dh0 ~ dh0 of the transposed
+    bidiagonal solve."""
+    T, D = 120, 4
+    w = rng.uniform(-0.9, 0.9, D)
+    u = 1e-6 * rng.standard_normal((T, 1, D))
+    y = oracle.rollout_tanh(w, u)
+    g = rng.standard_normal((T, 1, D))
+    du, dw, dh0 = oracle.deer_bwd(w, y, g)
+    for d in range(D):
+        a = np.full(T, w[d])
+        delta = _bidiag_solve_T(a, g[:, 0, d])
+        np.testing.assert_allclose(du[:, 0, d], delta, rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(dh0[0, d], w[d] * delta[0], rtol=1e-9, atol=1e-12)
+
+
 def test_oracle_threads_do_not_change_results():
     a = rng.uniform(-1, 1, (300, 33))
     b = rng.standard_normal((300, 33))
