@@ -207,6 +207,32 @@ class Bench:
             tot = [a + b for a, b in zip(tot, r)]
         return tot
 
+    def time_deer_bwd(self, peak, reps=10):
+        """deer_diag_bwd on the DEER workload: mean event time over `reps`
+        launches after 3 warm-up launches (inputs larger than L2)."""
+        t, L, o = self.torch, self.lrs, self.d["deer"]
+        wl = W.DEER
+        if "dy" not in o:
+            o["dy"] = t.from_numpy(W.normal(0, 90, (wl.T, wl.B, wl.D))).to(self.dev)
+            o["du"] = t.empty_like(o["dy"])
+            o["dw"] = t.empty(wl.D, device=self.dev)
+        run = lambda: L.deer_diag_bwd(o["w"], o["y"], o["dy"], o["h0"], o["du"], o["dw"],
+                                      want_dh0=False)
+        for _ in range(3):
+            run()
+        e0, e1 = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+        t.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            run()
+        e1.record()
+        t.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        byt = 12 * wl.N + 8 * wl.D  # read y, dy; write du; w, dw
+        return {"ms": round(ms, 4), "launches": 3, "GBps": round(byt / (ms / 1e3) / 1e9, 1),
+                "frac": round(byt / (ms / 1e3) / 1e9 / peak, 3),
+                "workload": f"deer fp32 T={wl.T} B={wl.B} D={wl.D}, gradient through the solution"}
+
     # ---- end to end: host buffers, copies inside the timed region
     def setup_e2e(self):
         t = self.torch
@@ -555,6 +581,10 @@ def main():
             "data": "synthetic", "config": config_dict(),
             "hbm_GBps": round(gbs, 1), "hbm_frac": round(gbs / peak, 4), "deer_iters": k_med,
             "gpu_launches": launches, "clocks": clk.summary(), "roofline": roof, "ops": ops}
+
+    # the next row on the same scan, outside the step: the gradient through the
+    # DEER solution at the DEER workload's size, from the step's own solution
+    line["next_ops"] = {"deer.bwd": b.time_deer_bwd(peak)}
 
     if not args.no_e2e:
         b.setup_e2e()

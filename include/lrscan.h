@@ -164,6 +164,25 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y,
                     int dtype, void* stream);
 
 /*
+ * Gradient through the DEER solution (the next row on the same scan):
+ * [P4] "核心原理": at the fixed point y is the rollout of
+ * h_t = tanh(w (.) h_{t-1} + u_t), so the gradient of a loss L with upstream
+ * g = dL/dy is back-propagation through it, one reverse scan with coefficient
+ * J_{t+1} = w (1 - y_{t+1}^2):
+ *   delta_t = g_t + J_{t+1} delta_{t+1}  (delta_{T-1} = g_{T-1}),
+ *   du_t = delta_t (1 - y_t^2),  dw_d = sum over t and batch of du_t y_{t-1},
+ *   dh0 = w (1 - y_0^2) delta_0  (y_{-1} = h0).
+ *   w      : [D] fp32 in;   y : [T,B,D] in, the solution (deer_diag_solve)
+ *   h0     : [B,D] in (NULL = zeros);  dy : [T,B,D] in, the upstream gradient
+ *   du     : [T,B,D] out;  dw : [D] fp32 out;  dh0 : [B,D] out (NULL = skip)
+ * Asynchronous on `stream`.  Uses the workspace's per-tile partial sums for dw
+ * (a fixed-order reduction: bitwise reproducible).
+ */
+int deer_diag_bwd(const float* w, const void* y, const void* h0, const void* dy, void* du,
+                  float* dw, void* dh0, int64_t B, int64_t T, int64_t D, int dtype,
+                  void* stream);
+
+/*
  * Forward scan that allocates nothing (no counterpart in the pages: this is a
  * deployment variant of lr_scan_fwd, same arguments and results).
  * For callers that may not allocate device memory: code running under an

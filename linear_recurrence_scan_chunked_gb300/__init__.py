@@ -54,6 +54,7 @@ def load():
     lib.sru_fwd.argtypes = [P] * 9 + [I64, I64, I64, I, P]
     lib.sru_bwd.argtypes = [P] * 16 + [I64, I64, I64, I, P]
     lib.deer_diag_solve.argtypes = [P, P, P, P, I64, I64, I64, ctypes.c_float, I, P, P, P, I, P]
+    lib.deer_diag_bwd.argtypes = [P] * 7 + [I64, I64, I64, I, P]
     lib.lr_last_error.argtypes = []
     lib.lr_status_str.argtypes = [I]
     lib.lr_status_str.restype = ctypes.c_char_p
@@ -61,7 +62,7 @@ def load():
     lib.lr_workspace_bytes.restype = I64
     lib.lr_test_lookback_timeout.argtypes = [ctypes.c_uint32, P]
     lib.lr_test_activations.argtypes = [P, P, P, I64, P]
-    for f in ("lr_scan_fwd", "lr_scan_bwd", "sru_fwd", "sru_bwd", "deer_diag_solve",
+    for f in ("lr_scan_fwd", "lr_scan_bwd", "sru_fwd", "sru_bwd", "deer_diag_solve", "deer_diag_bwd",
               "lr_last_error", "lr_test_lookback_timeout", "lr_test_activations"):
         getattr(lib, f).restype = I
     _lib = lib
@@ -216,6 +217,24 @@ def deer_diag_solve(w, u, h0=None, y=None, eps=1e-5, kmax=20, stream=None):
         _check(st)
     k = iters.value
     return y, k, resid.value, [hist[i] for i in range(k)], st
+
+
+def deer_diag_bwd(w, y, dy, h0=None, du=None, dw=None, dh0=None, want_dh0=True, stream=None):
+    """Gradient through the DEER solution y for the upstream dy = dL/dy.
+    Returns (du, dw, dh0 or None)."""
+    _seq("y", y)
+    _seq("dy", dy, y)
+    T, B, D = y.shape
+    _param("w", w, D)
+    _state("h0", h0, y)
+    du = torch.empty_like(y) if du is None else _seq("du", du, y)
+    dw = torch.empty(D, dtype=torch.float32, device=y.device) if dw is None else _param("dw", dw, D)
+    if dh0 is None and want_dh0:
+        dh0 = torch.empty((B, D), dtype=y.dtype, device=y.device)
+    _state("dh0", dh0, y)
+    _check(load().deer_diag_bwd(_p(w), _p(y), _p(h0), _p(dy), _p(du), _p(dw), _p(dh0), B, T, D,
+                                _code(y), _stream(stream)))
+    return du, dw, dh0
 
 
 def last_error() -> int:

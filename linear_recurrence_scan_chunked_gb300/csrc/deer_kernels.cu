@@ -158,6 +158,146 @@ struct DeerOp {
     }
 };
 
+// DEER backward (next row of the same scan): the gradient through the
+// solution y of h_t = tanh(w h_{t-1} + u_t).  At the fixed point y is the
+// rollout ([P4] "核心原理"), so the gradient is back-propagation through it:
+// with the upstream g = dL/dy and J_t = dy_t/dy_{t-1} = w (1 - y_t^2),
+//     delta_t = g_t + J_{t+1} delta_{t+1}   (reverse scan, as the linear BPTT,
+//                                           on u_t = J_t delta_t),
+//     du_t = delta_t (1 - y_t^2),   dw = sum_{t,b} du_t y_{t-1},
+//     dh0 = u_0 = J_0 delta_0      (y_{-1} = h0).
+// dw: per-tile channel sums, then the fixed-order reduction of the SRU bias
+// gradients.
+template <typename S>
+struct DeerBwdParams {
+    const float* w;
+    const S* y;
+    const S* h0;
+    const S* dy;
+    S* du;
+    S* dh0;
+    float* partials;  // [n_chunks][C]
+};
+
+template <typename S_, int VEC_, int NW_, int R_>
+struct DeerBwdOp {
+    using S = S_;
+    static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
+    static constexpr bool REV = true;
+    static constexpr int IN_ARRAYS = 2;  // y (rows t and t-1), dy
+    using Params = DeerBwdParams<S>;
+    struct Regs {
+        Pack<S, VEC> y[R + 1];  // y at times t0, t0-1, ..., t0-R (row -1 is h0)
+        Pack<S, VEC> g[R];
+    };
+    struct Work {
+        float J[R][VEC], D1[R][VEC];  // J_t and 1 - y_t^2
+    };
+    struct Smem {
+        float pw[NW][32][VEC];
+    };
+    // the partial sums may overlay the carry's warp aggregates: finish() writes
+    // them only after a barrier that every warp reaches once done with those
+    static constexpr bool SCRATCH_IN_CARRY = true;
+    struct Acc {};
+    __device__ static void acc_init(Acc&) {}
+    __device__ static bool skip(const Params&) { return false; }
+    __device__ static const S* init_ptr(const Params&) { return nullptr; }  // u_T = 0
+
+    static constexpr int TMA_N = 2;  // staged: dy, y (rows t0-1 .. t0+L-1 of the chunk)
+    __host__ __device__ static constexpr int tma_shift(int k) { return k == 1 ? -1 : 0; }
+    __host__ __device__ static constexpr int tma_extra(int k) { return k == 1 ? 1 : 0; }
+    static void tma_arrays(const Params& p, const void** ptr) {
+        ptr[0] = p.dy;
+        ptr[1] = p.y;
+    }
+
+    template <class Src>
+    __device__ static void load(const Src& src, const Params& p, const Geom& g,
+                                const TileCoord& tc, Regs& rg) {
+#pragma unroll
+        for (int i = 0; i <= R; ++i) {
+            const int64_t t = tc.t0 - i;
+            if (!tc.cok || t >= g.T) rg.y[i].ident(0.f);
+            else if (t < 0) {
+                if (p.h0 != nullptr) rg.y[i].load(p.h0 + tc.c);
+                else rg.y[i].ident(0.f);
+            } else src.ld(rg.y[i], 1, p.y, t);
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int64_t t = tc.t0 - r;
+            if (tc.cok && t < g.T) src.ld(rg.g[r], 0, p.dy, t);
+            else rg.g[r].ident(0.f);
+        }
+    }
+    __device__ static void aggregate(const Params& p, const Geom& g, const TileCoord& tc,
+                                     const Regs& rg, Work& w, float (&A)[VEC], float (&B)[VEC],
+                                     bool) {
+        float wv[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) wv[v] = 0.f;
+        if (tc.cok) load_param<VEC>(p.w + tc.c % g.D, wv);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { A[v] = 1.f; B[v] = 0.f; }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const bool ok = tc.cok && tc.t0 - r < g.T;
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                const float yt = rg.y[r].get(v);
+                const float d1 = 1.f - yt * yt;
+                w.D1[r][v] = d1;
+                w.J[r][v] = ok ? wv[v] * d1 : 1.f;
+                B[v] = w.J[r][v] * (rg.g[r].get(v) + B[v]);
+                A[v] *= w.J[r][v];
+            }
+        }
+    }
+    __device__ static void finish(const Params& p, const Geom& g, const TileCoord& tc,
+                                  const Regs& rg, Work& w, float (&s)[VEC], Smem& xs, Acc&) {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        float sum[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) sum[v] = 0.f;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int64_t t = tc.t0 - r;
+            const bool ok = tc.cok && t < g.T;
+            float du[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                const float delta = rg.g[r].get(v) + s[v];
+                du[v] = delta * w.D1[r][v];
+                s[v] = w.J[r][v] * delta;
+                if (ok) sum[v] += du[v] * rg.y[r + 1].get(v);
+            }
+            if (ok) store_vec<S, VEC>(p.du + t * g.C + tc.c, du);
+        }
+        // row 0 is the last row of the last warp of time chunk 0: s = u_0 = dh0
+        if (tc.tchunk == 0 && warp == NW - 1 && p.dh0 != nullptr && tc.cok)
+            store_vec<S, VEC>(p.dh0 + tc.c, s);
+        // dw partials of this tile: sum over its rows, fixed warp order
+        csync<NW>();  // every warp is past its reads of the carry smem
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) xs.pw[warp][lane][v] = sum[v];
+        csync<NW>();
+        if (warp == 0 && tc.cok) {
+            float pw[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) pw[v] = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < NW; ++ww)
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) pw[v] += xs.pw[ww][lane][v];
+            float* pp = p.partials + tc.tchunk * g.C + tc.c;
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) pp[v] = pw[v];
+        }
+    }
+    __device__ static void at_exit(const Params&, Smem&, Acc&) {}
+};
+
 template <typename S, bool VP, int M>
 using DeerOpT = DeerOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_DEER, sizeof(S) == 2, M).NW,
                        kcfg(OP_DEER, sizeof(S) == 2, M).R>;
@@ -181,6 +321,29 @@ cudaError_t launch_deer_iter(int dtype, bool vec, const float* w, const void* u,
     return vec ? deer_t<__nv_bfloat16, true>(w, u, h0, yold, ynew, resid, prev_resid, eps, g, cr, s)
                : deer_t<__nv_bfloat16, false>(w, u, h0, yold, ynew, resid, prev_resid, eps, g, cr,
                                               s);
+}
+
+template <typename S, bool VP, int M>
+using DeerBwdOpT = DeerBwdOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_DEER_BWD, sizeof(S) == 2, M).NW,
+                             kcfg(OP_DEER_BWD, sizeof(S) == 2, M).R>;
+
+template <typename S, bool VP>
+static cudaError_t deer_bwd_t(const float* w, const void* y, const void* h0, const void* dy,
+                              void* du, void* dh0, float* partials, const Geom& g, const Carry& cr,
+                              cudaStream_t s) {
+    return launch_persist<DeerBwdOpT<S, VP, CARRY_CHAIN>, DeerBwdOpT<S, VP, CARRY_WALK>,
+                          DeerBwdOpT<S, VP, TILE_TMA>, kcfg(OP_DEER_BWD, sizeof(S) == 2, TILE_TMA).ST>(
+        {w, (const S*)y, (const S*)h0, (const S*)dy, (S*)du, (S*)dh0, partials}, g, cr, s);
+}
+
+cudaError_t launch_deer_bwd(int dtype, bool vec, const float* w, const void* y, const void* h0,
+                            const void* dy, void* du, void* dh0, float* partials, const Geom& g,
+                            const Carry& cr, cudaStream_t s) {
+    if (dtype == 0)
+        return vec ? deer_bwd_t<float, true>(w, y, h0, dy, du, dh0, partials, g, cr, s)
+                   : deer_bwd_t<float, false>(w, y, h0, dy, du, dh0, partials, g, cr, s);
+    return vec ? deer_bwd_t<__nv_bfloat16, true>(w, y, h0, dy, du, dh0, partials, g, cr, s)
+               : deer_bwd_t<__nv_bfloat16, false>(w, y, h0, dy, du, dh0, partials, g, cr, s);
 }
 
 }  // namespace lrs

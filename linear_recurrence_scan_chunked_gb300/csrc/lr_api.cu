@@ -324,7 +324,7 @@ int sru_bwd(const void* xt, const void* uf, const void* ur, const void* x, const
     TRY(grow(*ws, &ws->partials, &ws->partials_cap, (size_t)(2 * g.n_chunks * g.C + 2 * g.C), false));
     CK(launch_sru_bwd(dtype, vec, xt, uf, ur, x, bf, br, c0, c, dh, dxt, duf, dur, dx, dc0,
                       ws->partials, g, cr, s));
-    CK(launch_bias_reduce(ws->partials, g.n_chunks, B, D, dbf, dbr, s));
+    CK(launch_bias_reduce(ws->partials, g.n_chunks, 2, B, D, dbf, dbr, s));
     return leave(*ws, s);
 }
 
@@ -393,6 +393,33 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y, int6
     if (resid_out) *resid_out = rho;
     TRY(leave(*ws, s));
     return status;
+}
+
+int deer_diag_bwd(const float* w, const void* y, const void* h0, const void* dy, void* du,
+                  float* dw, void* dh0, int64_t B, int64_t T, int64_t D, int dtype, void* stream) {
+    TRY(check_sizes(B, T, D, dtype));
+    cudaStream_t s = (cudaStream_t)stream;
+    if (B * T * D == 0) {
+        if (D > 0) {
+            if (!dw) return LR_ERR_INVALID_ARG;
+            CK(cudaMemsetAsync(dw, 0, (size_t)D * 4, s));
+        }
+        if (dh0 && B * D > 0) CK(cudaMemsetAsync(dh0, 0, (size_t)(B * D) * esize(dtype), s));
+        return LR_OK;
+    }
+    bool vec;
+    TRY(check_ptrs({y, dy, du}, {h0, dh0}, {w, dw}, dtype, D, &vec));
+    GUARD;
+    DevWS* ws;
+    TRY(get_ws(&ws));
+    Geom g;
+    Carry cr;
+    TRY(enter(*ws, s));
+    TRY(plan(*ws, OP_DEER_BWD, dtype, vec, T, B * D, D, &g, &cr, s));
+    TRY(grow(*ws, &ws->partials, &ws->partials_cap, (size_t)(g.n_chunks * g.C + g.C), false));
+    CK(launch_deer_bwd(dtype, vec, w, y, h0, dy, du, dh0, ws->partials, g, cr, s));
+    CK(launch_bias_reduce(ws->partials, g.n_chunks, 1, B, D, dw, nullptr, s));
+    return leave(*ws, s);
 }
 
 int lr_last_error(void) {

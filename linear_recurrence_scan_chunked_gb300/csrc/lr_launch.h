@@ -35,7 +35,7 @@ struct TileShape {
     int threads;
 };
 
-enum Op { OP_SCAN_FWD = 0, OP_SCAN_BWD, OP_SRU_FWD, OP_SRU_BWD, OP_DEER, OP_COUNT };
+enum Op { OP_SCAN_FWD = 0, OP_SCAN_BWD, OP_SRU_FWD, OP_SRU_BWD, OP_DEER, OP_DEER_BWD, OP_COUNT };
 
 // Launch configuration of every kernel: NW warps per CTA, R rows per thread
 // (tile = NW*R rows), VEC channels per lane (16-byte vectors on the vector
@@ -53,8 +53,11 @@ struct KCfg {
     int ST;
 };
 constexpr KCfg kcfg(Op op, int dtype, int mode) {
-    // bf16 holds two elements per register: twice the rows of fp32
-    return mode == CARRY_CHAIN
+    // bf16 holds two elements per register: twice the rows of fp32 (but the
+    // DEER backward keeps two fp32 values per element between its passes: the
+    // rows of fp32 for both)
+    return op == OP_DEER_BWD ? KCfg{8, mode == CARRY_CHAIN ? 2 : 4, mode == TILE_TMA ? 3 : 0}
+           : mode == CARRY_CHAIN
                ? (op == OP_SCAN_FWD ? KCfg{8, dtype == 1 ? 8 : 4, 0}
                   : op == OP_SCAN_BWD ? KCfg{8, dtype == 1 ? 4 : 2, 0}
                   : op == OP_SRU_FWD  ? KCfg{8, dtype == 1 ? 4 : 2, 0}
@@ -196,13 +199,19 @@ cudaError_t launch_sru_bwd(int dtype, bool vec, const void* xt, const void* uf, 
                            void* dx, void* dc0, float* partials, const Geom& g,
                            const Carry& cr, cudaStream_t s);
 
-cudaError_t launch_bias_reduce(const float* partials, int64_t n_chunks, int64_t B, int64_t D,
-                               float* dbf, float* dbr, cudaStream_t s);
+cudaError_t launch_bias_reduce(const float* partials, int64_t n_chunks, int n_arr, int64_t B,
+                               int64_t D, float* out0, float* out1, cudaStream_t s);
 
 // resid: one fp32 slot (as bits), zeroed before the launch, receives max|ynew-yold|
 cudaError_t launch_deer_iter(int dtype, bool vec, const float* w, const void* u, const void* h0,
                              const void* yold, void* ynew, uint32_t* resid,
                              const uint32_t* prev_resid, float eps, const Geom& g, const Carry& cr,
                              cudaStream_t s);
+
+// DEER backward: partials is [n_chunks][C] fp32 scratch (dw per tile),
+// followed by C floats that launch_bias_reduce uses for its per-channel sums
+cudaError_t launch_deer_bwd(int dtype, bool vec, const float* w, const void* y, const void* h0,
+                            const void* dy, void* du, void* dh0, float* partials, const Geom& g,
+                            const Carry& cr, cudaStream_t s);
 
 }  // namespace lrs

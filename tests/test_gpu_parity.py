@@ -285,3 +285,24 @@ def test_deer_bf16(cuda, shape):
     assert st == cuda.LR_OK and rst == oracle.DEER_CONVERGED
     assert abs(k - rk) <= 1, (k, rk, hist, list(rhist))
     assert_close("y", to_f64(y), ry, "bf16")
+
+
+@pytest.mark.parametrize("shape", SHAPES[:9] + WIDE + [(20000, 1, 128)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_deer_bwd(cuda, shape, dtype):
+    """Gradient through the DEER solution: du, dw, dh0 against the oracle on
+    the same stored solution y and upstream gradient."""
+    T, B, D = shape
+    wl = W.like(W.DEER, T, B, D, dtype)
+    inp = W.make_inputs(wl, 31)
+    h0 = W.store(W.normal(31, 44, (B, D)), dtype)
+    y = W.store(oracle.rollout_tanh(np.asarray(inp["w"], np.float64), W.to_f64(inp["u"], dtype),
+                                    W.to_f64(h0, dtype)), dtype)
+    g = W.store(W.normal(31, 45, (T, B, D)), dtype)
+    dv = dev_inputs({"w": inp["w"], "y": y, "h0": h0, "g": g}, dtype)
+    f = f64_inputs({"w": inp["w"], "y": y, "h0": h0, "g": g}, dtype)
+    du, dw, dh0 = cuda.deer_diag_bwd(dv["w"], dv["y"], dv["g"], dv["h0"])
+    rdu, rdw, rdh0 = oracle.deer_bwd(f["w"], f["y"], f["g"], f["h0"])
+    assert_close("du", to_f64(du), rdu, dtype)
+    assert_close("dw", to_f64(dw), rdw, dtype)
+    assert_close("dh0", to_f64(dh0), rdh0, dtype)
