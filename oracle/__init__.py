@@ -9,6 +9,7 @@ ctypes and converts numpy arrays to contiguous fp64.
 Every function here follows the pages cited in ``lr_oracle.c``:
   scan_fwd / scan_bwd  -- the diagonal linear recurrence and its BPTT gradient
   sru_fwd / sru_bwd    -- the linear-form SRU layer and its gradient
+  lstm_fwd / lstm_bwd  -- the LSTM cell-state scan with its gates, and its gradient
   deer / deer_step     -- DEER Newton iteration on a diagonal tanh RNN
   rollout_tanh         -- the direct sequential tanh RNN
 Each is pinned by tests in ``tests/test_oracle_pins.py`` against closed forms,
@@ -56,6 +57,9 @@ def _load():
         lib.lro_scan_bwd.argtypes = [I64, I64, P, P, P, P, P, P, P]
         lib.lro_sru_fwd.argtypes = [I64, I64, I64] + [P] * 9
         lib.lro_sru_bwd.argtypes = [I64, I64, I64] + [P] * 15
+        lib.lro_lstm_fwd.argtypes = [I64, I64, I64] + [P] * 11
+        lib.lro_lstm_bwd.argtypes = [I64, I64, I64] + [P] * 20
+        lib.lro_lstm_bwd.restype = ctypes.c_int
         lib.lro_rollout_tanh.argtypes = [I64, I64, I64, P, P, P, P]
         lib.lro_deer_step.argtypes = [I64, I64, I64, P, P, P, P, P, P]
         lib.lro_deer.argtypes = [I64, I64, I64, P, P, P, ctypes.c_double, ctypes.c_int, P, P, P]
@@ -132,6 +136,34 @@ def sru_bwd(xt, uf, ur, x, bf, br, c, dh, c0=None):
     _load().lro_sru_bwd(T, C, D, *map(_p, (xt, uf, ur, x, bf, br, c0, c, dh,
                                             dxt, duf, dur, dx, dbf, dbr, dc0)))
     return dxt, duf, dur, dx, dbf, dbr, dc0
+
+
+def lstm_fwd(zf, zi, zc, zo, bf, bi, bc, bo, c0=None):
+    """LSTM cell-state scan with its gates; returns (h, c).  Pre-activations
+    [T, B, D]; biases [D]; c0 [B, D] (None = zeros)."""
+    zf, zi, zc, zo, bf, bi, bc, bo, c0 = map(_f64, (zf, zi, zc, zo, bf, bi, bc, bo, c0))
+    T, C = _tc(zf)
+    D = bf.shape[0]
+    h, c = np.empty_like(zf), np.empty_like(zf)
+    _load().lro_lstm_fwd(T, C, D, *map(_p, (zf, zi, zc, zo, bf, bi, bc, bo, c0, h, c)))
+    return h, c
+
+
+def lstm_bwd(zf, zi, zc, zo, bf, bi, bc, bo, c, dh, c0=None):
+    """Gradient of sum(dh * h) for lstm_fwd given its cell states c.
+    Returns (dzf, dzi, dzc, dzo, dbf, dbi, dbc, dbo, dc0)."""
+    zf, zi, zc, zo, bf, bi, bc, bo, c, dh, c0 = map(
+        _f64, (zf, zi, zc, zo, bf, bi, bc, bo, c, dh, c0))
+    T, C = _tc(zf)
+    D = bf.shape[0]
+    dz = [np.empty_like(zf) for _ in range(4)]
+    db = [np.empty(D) for _ in range(4)]
+    dc0 = np.empty(zf.shape[1:]) if zf.ndim == 3 else np.empty(C)
+    st = _load().lro_lstm_bwd(T, C, D, *map(_p, (zf, zi, zc, zo, bf, bi, bc, bo, c0, c, dh,
+                                                 *dz, *db, dc0)))
+    if st < 0:
+        raise MemoryError("oracle lstm_bwd: allocation failed")
+    return (*dz, *db, dc0)
 
 
 def rollout_tanh(w, u, h0=None):

@@ -204,6 +204,111 @@ void lro_sru_bwd(int64_t T, int64_t C, int64_t D, const double* xt,
     free(sr);
 }
 
+/* ------------------------------------------- LSTM cell-state scan (next) */
+/*
+ * [P2] LSTM paragraph: the cell state of a standard LSTM unit evolves by
+ *   C_t = f_t * C_{t-1} + i_t * C~_t,
+ * a linear recurrence in C whose coefficients f_t (forget gate) and i_t
+ * (input gate) vary with t, and C~_t is the candidate state; the input,
+ * forget and output gates are sigmoids and the candidate a tanh of their
+ * pre-activations.  The plain reading taken here (the GILR-style cell of
+ * [P2] checklist item 1): the pre-activations zf, zi, zc, zo come
+ * precomputed from the input only (no h_{t-1} term), so the gates do not
+ * depend on the state and the recurrence is linear:
+ *   f = sigma(zf + bf),  i = sigma(zi + bi),  C~ = tanh(zc + bc),
+ *   o = sigma(zo + bo),
+ *   C_t = f_t C_{t-1} + i_t C~_t,   C_{-1} = c0,
+ *   h_t = o_t tanh(C_t)             (the LSTM output).
+ * zf..zo are [T, C]; bf..bo are [D].
+ */
+void lro_lstm_fwd(int64_t T, int64_t C, int64_t D, const double* zf,
+                  const double* zi, const double* zc, const double* zo,
+                  const double* bf, const double* bi, const double* bc,
+                  const double* bo, const double* c0, double* h, double* c) {
+    PAR_BEGIN
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t k = c0_; k < c1_; ++k) {
+            int64_t n = t * C + k, d = k % D;
+            double cprev = t > 0 ? c[n - C] : (c0 ? c0[k] : 0.0);
+            double f = sigm(zf[n] + bf[d]);
+            double i = sigm(zi[n] + bi[d]);
+            double g = tanh(zc[n] + bc[d]);
+            double o = sigm(zo[n] + bo[d]);
+            c[n] = f * cprev + i * g;
+            h[n] = o * tanh(c[n]);
+        }
+    PAR_END
+}
+
+/*
+ * Gradients of lro_lstm_fwd given the cell states c and the upstream
+ * dh = dL/dh_t (back-propagation through time, the reverse-time form of the
+ * same linear recurrence):
+ *   dC_t  = dh_t o_t (1 - tanh^2 C_t) + f_{t+1} dC_{t+1}     (reverse in t)
+ *   dzf_t = dC_t C_{t-1} f_t (1 - f_t)
+ *   dzi_t = dC_t C~_t i_t (1 - i_t)
+ *   dzc_t = dC_t i_t (1 - C~_t^2)
+ *   dzo_t = dh_t tanh(C_t) o_t (1 - o_t)
+ *   dc0   = f_0 dC_0
+ *   db*[d] = sum over t and batch of dz*.
+ * dc0 may be NULL.  Returns -1 when scratch allocation fails.
+ */
+int lro_lstm_bwd(int64_t T, int64_t C, int64_t D, const double* zf,
+                 const double* zi, const double* zc, const double* zo,
+                 const double* bf, const double* bi, const double* bc,
+                 const double* bo, const double* c0, const double* c,
+                 const double* dh, double* dzf, double* dzi, double* dzc,
+                 double* dzo, double* dbf, double* dbi, double* dbc,
+                 double* dbo, double* dc0) {
+    double* dc = (double*)malloc(sizeof(double) * (size_t)(T * C > 0 ? T * C : 1));
+    double* sum = (double*)calloc((size_t)(4 * C > 0 ? 4 * C : 1), sizeof(double));
+    if (!dc || !sum) {
+        free(dc);
+        free(sum);
+        return -1;
+    }
+    PAR_BEGIN
+    for (int64_t t = T - 1; t >= 0; --t)
+        for (int64_t k = c0_; k < c1_; ++k) {
+            int64_t n = t * C + k, d = k % D;
+            double o = sigm(zo[n] + bo[d]);
+            double th = tanh(c[n]);
+            double carry = 0.0;
+            if (t + 1 < T) carry = sigm(zf[n + C] + bf[d]) * dc[n + C];
+            dc[n] = dh[n] * o * (1.0 - th * th) + carry;
+        }
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t k = c0_; k < c1_; ++k) {
+            int64_t n = t * C + k, d = k % D;
+            double cprev = t > 0 ? c[n - C] : (c0 ? c0[k] : 0.0);
+            double f = sigm(zf[n] + bf[d]);
+            double i = sigm(zi[n] + bi[d]);
+            double g = tanh(zc[n] + bc[d]);
+            double o = sigm(zo[n] + bo[d]);
+            dzf[n] = dc[n] * cprev * f * (1.0 - f);
+            dzi[n] = dc[n] * g * i * (1.0 - i);
+            dzc[n] = dc[n] * i * (1.0 - g * g);
+            dzo[n] = dh[n] * tanh(c[n]) * o * (1.0 - o);
+            sum[k] += dzf[n];
+            sum[C + k] += dzi[n];
+            sum[2 * C + k] += dzc[n];
+            sum[3 * C + k] += dzo[n];
+        }
+    if (dc0)
+        for (int64_t k = c0_; k < c1_; ++k) dc0[k] = sigm(zf[k] + bf[k % D]) * dc[k];
+    PAR_END
+    for (int64_t d = 0; d < D; ++d) { dbf[d] = 0.0; dbi[d] = 0.0; dbc[d] = 0.0; dbo[d] = 0.0; }
+    for (int64_t k = 0; k < C; ++k) {
+        dbf[k % D] += sum[k];
+        dbi[k % D] += sum[C + k];
+        dbc[k % D] += sum[2 * C + k];
+        dbo[k % D] += sum[3 * C + k];
+    }
+    free(dc);
+    free(sum);
+    return 0;
+}
+
 /* -------------------------------------------------- DEER (row a5), tanh RNN */
 /*
  * Target recurrence: h_t = tanh(w (.) h_{t-1} + u_t), h_{-1} = h0, w in [D].

@@ -252,6 +252,110 @@ def test_sru_bwd_finite_differences():
         np.testing.assert_allclose(got, _fd(loss, p[key]), rtol=1e-6, atol=1e-8, err_msg=key)
 
 
+# ---------------------------------------------------- LSTM cell-state scan
+
+def _lstm_inputs(T, B, D, seed=21):
+    r = np.random.default_rng(seed)
+    p = {k: r.standard_normal((T, B, D)) for k in ("zf", "zi", "zc", "zo")}
+    p.update({k: r.standard_normal(D) for k in ("bf", "bi", "bc", "bo")})
+    p["c0"] = r.standard_normal((B, D))
+    return p
+
+
+def _gilr(p):
+    """Tie the input gate to the forget gate: i = sigma(-(zf + bf)) = 1 - f."""
+    q = dict(p)
+    q["zi"], q["bi"] = -p["zf"], -p["bf"]
+    return q
+
+
+def test_lstm_gilr_tie_is_the_sru_cell():
+    # with i = 1 - f and the candidate as SRU's xt, the cell is SRU's memory
+    # c_t = f c_{t-1} + (1 - f) xt, and h = o tanh(c) is SRU's output with
+    # reset gate o and highway input x = 0
+    p = _gilr(_lstm_inputs(40, 2, 3))
+    h, c = oracle.lstm_fwd(**p)
+    xt = np.tanh(p["zc"] + p["bc"])
+    zero = np.zeros_like(xt)
+    hs, cs = oracle.sru_fwd(xt, p["zf"], p["zo"], zero, p["bf"], p["bo"], p["c0"])
+    np.testing.assert_allclose(c, cs, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(h, hs, rtol=0, atol=1e-13)
+
+
+def test_lstm_bwd_gilr_tie_is_the_sru_gradient():
+    # chain rule through the tie zi = -zf: SRU's duf = dzf - dzi, its dxt
+    # times (1 - xt^2) is dzc (xt = tanh(zc + bc)), its dur is dzo
+    T, B, D = 30, 2, 3
+    p = _gilr(_lstm_inputs(T, B, D))
+    dh = np.random.default_rng(4).standard_normal((T, B, D))
+    h, c = oracle.lstm_fwd(**p)
+    dzf, dzi, dzc, dzo, dbf, dbi, dbc, dbo, dc0 = oracle.lstm_bwd(c=c, dh=dh, **p)
+    xt = np.tanh(p["zc"] + p["bc"])
+    zero = np.zeros_like(xt)
+    dxt, duf, dur, _, sbf, sbr, sc0 = oracle.sru_bwd(xt, p["zf"], p["zo"], zero, p["bf"],
+                                                     p["bo"], c, dh, p["c0"])
+    tol = dict(rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dzf - dzi, duf, **tol)
+    np.testing.assert_allclose(dzc, dxt * (1 - xt * xt), **tol)
+    np.testing.assert_allclose(dzo, dur, **tol)
+    np.testing.assert_allclose(dbf - dbi, sbf, **tol)
+    np.testing.assert_allclose(dbo, sbr, **tol)
+    np.testing.assert_allclose(dc0, sc0, **tol)
+
+
+def test_lstm_gates_open_is_running_sum():
+    # f = i = o = 1 exactly (sigmoid of +1000 rounds to 1): C = c0 + cumsum(C~)
+    p = _lstm_inputs(50, 2, 3)
+    for k in ("zf", "zi", "zo"):
+        p[k][:] = 1000.0
+    h, c = oracle.lstm_fwd(**p)
+    ref = p["c0"][None] + np.cumsum(np.tanh(p["zc"] + p["bc"]), axis=0)
+    np.testing.assert_allclose(c, ref, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(h, np.tanh(ref), rtol=1e-13, atol=1e-13)
+
+
+def test_lstm_forget_closed_has_no_memory():
+    # f = 0 exactly (sigmoid of -1000 is 0): every row is its own one-step
+    # problem whatever came before
+    T, B, D = 12, 2, 3
+    p = _lstm_inputs(T, B, D)
+    p["zf"][:] = -1000.0
+    h, c = oracle.lstm_fwd(**p)
+    for t in range(T):
+        row = {k: (v[t:t + 1] if v.ndim == 3 else v) for k, v in p.items() if k != "c0"}
+        c0 = np.random.default_rng(t).standard_normal((B, D))
+        ht, ct = oracle.lstm_fwd(**row, c0=c0)
+        np.testing.assert_array_equal(ct[0], c[t])
+        np.testing.assert_array_equal(ht[0], h[t])
+
+
+def test_lstm_cell_is_linear_recurrence_solve():
+    T, B, D = 80, 2, 3
+    p = _lstm_inputs(T, B, D)
+    h, c = oracle.lstm_fwd(**p)
+    sig = lambda z: 1.0 / (1.0 + np.exp(-z))
+    f = sig(p["zf"] + p["bf"])
+    ig = sig(p["zi"] + p["bi"]) * np.tanh(p["zc"] + p["bc"])
+    for bb in range(B):
+        for d in range(D):
+            rhs = ig[:, bb, d].copy()
+            rhs[0] += f[0, bb, d] * p["c0"][bb, d]
+            np.testing.assert_allclose(c[:, bb, d], _bidiag_solve(f[:, bb, d], rhs),
+                                       rtol=1e-11, atol=1e-12)
+
+
+def test_lstm_bwd_finite_differences():
+    T, B, D = 7, 2, 3
+    p = _lstm_inputs(T, B, D)
+    dh = np.random.default_rng(9).standard_normal((T, B, D))
+    loss = lambda: float(np.sum(dh * oracle.lstm_fwd(**p)[0]))
+    h, c = oracle.lstm_fwd(**p)
+    got = oracle.lstm_bwd(c=c, dh=dh, **p)
+    keys = ("zf", "zi", "zc", "zo", "bf", "bi", "bc", "bo", "c0")
+    for g, key in zip(got, keys):
+        np.testing.assert_allclose(g, _fd(loss, p[key]), rtol=1e-6, atol=1e-8, err_msg=key)
+
+
 # -------------------------------------------------------------------- DEER
 
 def test_rollout_w_zero_is_tanh():
