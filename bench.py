@@ -233,6 +233,49 @@ class Bench:
                 "frac": round(byt / (ms / 1e3) / 1e9 / peak, 3),
                 "workload": f"deer fp32 T={wl.T} B={wl.B} D={wl.D}, gradient through the solution"}
 
+    def _mean_ms(self, run, reps):
+        t = self.torch
+        for _ in range(3):
+            run()
+        e0, e1 = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+        t.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            run()
+        e1.record()
+        t.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    def time_lstm(self, peak, reps=10):
+        """lstm_cell_fwd and lstm_cell_bwd on the LSTM cell workload (the SRU
+        layer's size): mean event time over `reps` launches after 3 warm-up
+        launches (every array larger than L2).  Device buffers are freed
+        afterwards."""
+        t, L, wl = self.torch, self.lrs, W.LSTM
+        inp = W.make_inputs(wl, 0)
+        d = {k: t.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to(self.dev)
+             for k, v in inp.items()}
+        z = [d[k] for k in ("zf", "zi", "zc", "zo", "bf", "bi", "bc", "bo")]
+        h, c = t.empty_like(d["zf"]), t.empty_like(d["zf"])
+        grad = {k: t.empty_like(d["zf"]) for k in ("dzf", "dzi", "dzc", "dzo")}
+        grad.update({k: t.empty(wl.D, device=self.dev) for k in ("dbf", "dbi", "dbc", "dbo")})
+        grad["dc0"] = t.empty((wl.B, wl.D), device=self.dev)
+        N, C, D = wl.N, wl.C, wl.D
+        out = {}
+        for p, run, byt, launches in (
+                ("fwd", lambda: L.lstm_cell_fwd(*z, d["c0"], h, c),
+                 24 * N + 4 * C + 16 * D, 1),  # read 4 gates, write h, c; c0; 4 biases
+                ("bwd", lambda: L.lstm_cell_bwd(*z, c, d["dh"], d["c0"], out=grad),
+                 40 * N + 8 * C + 32 * D, 3)):  # read 4 gates, c, dh, write 4; c0, dc0; biases
+            ms = self._mean_ms(run, reps)
+            gbs = byt / (ms / 1e3) / 1e9
+            out[f"lstm.{p}"] = {"ms": round(ms, 4), "launches": launches, "GBps": round(gbs, 1),
+                                "frac": round(gbs / peak, 3),
+                                "workload": f"lstm cell fp32 T={wl.T} B={wl.B} D={wl.D}, {p}"}
+        del d, z, h, c, grad
+        t.cuda.empty_cache()
+        return out
+
     # ---- end to end: host buffers, copies inside the timed region
     def setup_e2e(self):
         t = self.torch
@@ -582,9 +625,12 @@ def main():
             "hbm_GBps": round(gbs, 1), "hbm_frac": round(gbs / peak, 4), "deer_iters": k_med,
             "gpu_launches": launches, "clocks": clk.summary(), "roofline": roof, "ops": ops}
 
-    # the next row on the same scan, outside the step: the gradient through the
-    # DEER solution at the DEER workload's size, from the step's own solution
-    line["next_ops"] = {"deer.bwd": b.time_deer_bwd(peak)}
+    # the next rows on the same scan, outside the step: the gradient through
+    # the DEER solution at the DEER workload's size (from the step's own
+    # solution), and the LSTM cell forward and backward
+    nxt = {"deer.bwd": b.time_deer_bwd(peak)} if "deer" in b.d else {}
+    nxt.update(b.time_lstm(peak))
+    line["next_ops"] = nxt
 
     if not args.no_e2e:
         b.setup_e2e()

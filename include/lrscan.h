@@ -8,7 +8,8 @@
  *
  * along the sequence axis as a parallel prefix scan over the associative
  * operator (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2) (earlier element on the
- * left, identity (1, 0)), and four computations built on that scan.
+ * left, identity (1, 0)), and the computations built on that scan (SRU and
+ * LSTM cells, forward and backward; DEER solve and its gradient).
  *
  * Sources (blog.hotdry.top, all dated 2025-09-21):
  *   [P1] "CUDA并行化RNN训练：从O(T)到O(log T)的工程实践与参数调优":
@@ -30,8 +31,8 @@
  * ---------------------------------------
  *  - Sequence tensors are [T, B, D] row-major with D contiguous (channel
  *    c = b*D + d, element (t, c) at offset t*B*D + c).  Per-step state tensors
- *    (h0, dh0, c0, dc0) are [B, D].  Per-feature parameters (w, bf, br and
- *    their gradients) are [D] and always fp32.
+ *    (h0, dh0, c0, dc0) are [B, D].  Per-feature parameters (w and the
+ *    biases bf, br, bi, bc, bo, and their gradients) are [D] and always fp32.
  *  - `dtype` is the storage type of every sequence and state tensor:
  *    LR_F32 (fp32) or LR_BF16 (bfloat16).  All arithmetic is fp32; bf16
  *    results are rounded to nearest-even when stored.
@@ -52,7 +53,7 @@
  *    (gradients of the initial state are zeroed).
  *  - The library keeps one internal workspace per device (carry packets of
  *    the chunk states and aggregates, a tile ticket, an error word, DEER's
- *    second iterate buffer, SRU bias partials), grown on demand with
+ *    second iterate buffer, bias-gradient partials), grown on demand with
  *    cudaMalloc.  Calls on different streams are serialised through it with
  *    CUDA events.
  *  - Return value: LR_OK, or an lr_status describing an argument or launch
@@ -181,6 +182,44 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y,
 int deer_diag_bwd(const float* w, const void* y, const void* h0, const void* dy, void* du,
                   float* dw, void* dh0, int64_t B, int64_t T, int64_t D, int dtype,
                   void* stream);
+
+/*
+ * LSTM cell-state scan with a fused gate producer (the next row on the same
+ * scan).  [P2] LSTM paragraph: the cell update C_t = f_t C_{t-1} + i_t C~_t is
+ * a linear recurrence in C with time-varying coefficients; checklist item 1:
+ * the GILR-style cell, whose gate pre-activations come from the input only
+ * (precomputed projections, no h_{t-1} term), keeps it linear.  One launch:
+ *   f = sigmoid(zf + bf),  i = sigmoid(zi + bi),  C~ = tanh(zc + bc),
+ *   o = sigmoid(zo + bo),
+ *   C_t = f_t C_{t-1} + i_t C~_t   (C_{-1} = c0),   h_t = o_t tanh(C_t).
+ *   zf, zi, zc, zo : [T,B,D] in   gate pre-activations (forget, input,
+ *                                 candidate, output)
+ *   bf, bi, bc, bo : [D] fp32 in  their biases
+ *   c0             : [B,D]   in   NULL means zeros
+ *   h, c           : [T,B,D] out  (c is kept for lstm_cell_bwd)
+ * The GILR cell is the case zi = -zf, bi = -bf (i = 1 - f).
+ */
+int lstm_cell_fwd(const void* zf, const void* zi, const void* zc, const void* zo,
+                  const float* bf, const float* bi, const float* bc, const float* bo,
+                  const void* c0, void* h, void* c,
+                  int64_t B, int64_t T, int64_t D, int dtype, void* stream);
+
+/*
+ * LSTM cell backward, given the forward c and the upstream dh = dL/dh_t
+ * (back-propagation through time; the cell gradient is the reverse scan):
+ *   dC_t = dh_t o_t (1 - tanh^2 C_t) + f_{t+1} dC_{t+1},
+ *   dzf = dC C_{t-1} f (1-f),  dzi = dC C~ i (1-i),  dzc = dC i (1 - C~^2),
+ *   dzo = dh tanh(C) o (1-o),  dc0 = f_0 dC_0,
+ *   db*[d] = sum over t and batch of dz* (deterministic order).
+ *   dzf, dzi, dzc, dzo : [T,B,D] out;  dbf, dbi, dbc, dbo : [D] fp32 out
+ *   (overwritten);  dc0 : [B,D] out, may be NULL.
+ */
+int lstm_cell_bwd(const void* zf, const void* zi, const void* zc, const void* zo,
+                  const float* bf, const float* bi, const float* bc, const float* bo,
+                  const void* c0, const void* c, const void* dh,
+                  void* dzf, void* dzi, void* dzc, void* dzo,
+                  float* dbf, float* dbi, float* dbc, float* dbo, void* dc0,
+                  int64_t B, int64_t T, int64_t D, int dtype, void* stream);
 
 /*
  * Forward scan that allocates nothing (no counterpart in the pages: this is a

@@ -53,6 +53,8 @@ def load():
     lib.lr_scan_bwd.argtypes = [P] * 7 + [I64, I64, I64, I, P]
     lib.sru_fwd.argtypes = [P] * 9 + [I64, I64, I64, I, P]
     lib.sru_bwd.argtypes = [P] * 16 + [I64, I64, I64, I, P]
+    lib.lstm_cell_fwd.argtypes = [P] * 11 + [I64, I64, I64, I, P]
+    lib.lstm_cell_bwd.argtypes = [P] * 20 + [I64, I64, I64, I, P]
     lib.deer_diag_solve.argtypes = [P, P, P, P, I64, I64, I64, ctypes.c_float, I, P, P, P, I, P]
     lib.deer_diag_bwd.argtypes = [P] * 7 + [I64, I64, I64, I, P]
     lib.lr_last_error.argtypes = []
@@ -194,6 +196,49 @@ def sru_bwd(xt, uf, ur, x, bf, br, c, dh, c0=None, out=None, want_dc0=True, stre
     _check(load().sru_bwd(_p(xt), _p(uf), _p(ur), _p(x), _p(bf), _p(br), _p(c0), _p(c), _p(dh),
                           _p(o["dxt"]), _p(o["duf"]), _p(o["dur"]), _p(o["dx"]), _p(o["dbf"]),
                           _p(o["dbr"]), _p(o.get("dc0")), B, T, D, _code(xt), _stream(stream)))
+    return o
+
+
+def lstm_cell_fwd(zf, zi, zc, zo, bf, bi, bc, bo, c0=None, h=None, c=None, stream=None):
+    """LSTM cell-state scan with its gates (forget, input, candidate, output
+    pre-activations [T, B, D]; biases [D] fp32). Returns (h, c)."""
+    _seq("zf", zf)
+    for n, t in (("zi", zi), ("zc", zc), ("zo", zo)):
+        _seq(n, t, zf)
+    T, B, D = zf.shape
+    for n, t in (("bf", bf), ("bi", bi), ("bc", bc), ("bo", bo)):
+        _param(n, t, D)
+    _state("c0", c0, zf)
+    h = torch.empty_like(zf) if h is None else _seq("h", h, zf)
+    c = torch.empty_like(zf) if c is None else _seq("c", c, zf)
+    _check(load().lstm_cell_fwd(_p(zf), _p(zi), _p(zc), _p(zo), _p(bf), _p(bi), _p(bc), _p(bo),
+                                _p(c0), _p(h), _p(c), B, T, D, _code(zf), _stream(stream)))
+    return h, c
+
+
+def lstm_cell_bwd(zf, zi, zc, zo, bf, bi, bc, bo, c, dh, c0=None, out=None, want_dc0=True,
+                  stream=None):
+    """LSTM cell backward. Returns dict dzf, dzi, dzc, dzo, dbf, dbi, dbc, dbo, dc0."""
+    _seq("zf", zf)
+    for n, t in (("zi", zi), ("zc", zc), ("zo", zo), ("c", c), ("dh", dh)):
+        _seq(n, t, zf)
+    T, B, D = zf.shape
+    for n, t in (("bf", bf), ("bi", bi), ("bc", bc), ("bo", bo)):
+        _param(n, t, D)
+    _state("c0", c0, zf)
+    o = dict(out or {})
+    for k in ("dzf", "dzi", "dzc", "dzo"):
+        o[k] = torch.empty_like(zf) if o.get(k) is None else _seq(k, o[k], zf)
+    for k in ("dbf", "dbi", "dbc", "dbo"):
+        o[k] = torch.empty(D, dtype=torch.float32, device=zf.device) if o.get(k) is None else _param(k, o[k], D)
+    if o.get("dc0") is None and want_dc0:
+        o["dc0"] = torch.empty((B, D), dtype=zf.dtype, device=zf.device)
+    _state("dc0", o.get("dc0"), zf)
+    _check(load().lstm_cell_bwd(_p(zf), _p(zi), _p(zc), _p(zo), _p(bf), _p(bi), _p(bc), _p(bo),
+                                _p(c0), _p(c), _p(dh), _p(o["dzf"]), _p(o["dzi"]), _p(o["dzc"]),
+                                _p(o["dzo"]), _p(o["dbf"]), _p(o["dbi"]), _p(o["dbc"]),
+                                _p(o["dbo"]), _p(o.get("dc0")), B, T, D, _code(zf),
+                                _stream(stream)))
     return o
 
 

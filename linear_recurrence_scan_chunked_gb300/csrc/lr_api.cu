@@ -324,7 +324,62 @@ int sru_bwd(const void* xt, const void* uf, const void* ur, const void* x, const
     TRY(grow(*ws, &ws->partials, &ws->partials_cap, (size_t)(2 * g.n_chunks * g.C + 2 * g.C), false));
     CK(launch_sru_bwd(dtype, vec, xt, uf, ur, x, bf, br, c0, c, dh, dxt, duf, dur, dx, dc0,
                       ws->partials, g, cr, s));
-    CK(launch_bias_reduce(ws->partials, g.n_chunks, 2, B, D, dbf, dbr, s));
+    CK(launch_bias_reduce(ws->partials, g.n_chunks, 2, B, D, BiasOut{{dbf, dbr}}, s));
+    return leave(*ws, s);
+}
+
+int lstm_cell_fwd(const void* zf, const void* zi, const void* zc, const void* zo,
+                  const float* bf, const float* bi, const float* bc, const float* bo,
+                  const void* c0, void* h, void* c, int64_t B, int64_t T, int64_t D, int dtype,
+                  void* stream) {
+    TRY(check_sizes(B, T, D, dtype));
+    if (B * T * D == 0) return LR_OK;
+    bool vec;
+    TRY(check_ptrs({zf, zi, zc, zo, h, c}, {c0}, {bf, bi, bc, bo}, dtype, D, &vec));
+    GUARD;
+    cudaStream_t s = (cudaStream_t)stream;
+    DevWS* ws;
+    TRY(get_ws(&ws));
+    Geom g;
+    Carry cr;
+    TRY(enter(*ws, s));
+    TRY(plan(*ws, OP_LSTM_FWD, dtype, vec, T, B * D, D, &g, &cr, s));
+    CK(launch_lstm_fwd(dtype, vec, LstmGates{zf, zi, zc, zo}, LstmBias{bf, bi, bc, bo}, c0, h, c,
+                       g, cr, s));
+    return leave(*ws, s);
+}
+
+int lstm_cell_bwd(const void* zf, const void* zi, const void* zc, const void* zo,
+                  const float* bf, const float* bi, const float* bc, const float* bo,
+                  const void* c0, const void* c, const void* dh, void* dzf, void* dzi, void* dzc,
+                  void* dzo, float* dbf, float* dbi, float* dbc, float* dbo, void* dc0, int64_t B,
+                  int64_t T, int64_t D, int dtype, void* stream) {
+    TRY(check_sizes(B, T, D, dtype));
+    cudaStream_t s = (cudaStream_t)stream;
+    if (B * T * D == 0) {
+        if (D > 0) {
+            for (float* db : {dbf, dbi, dbc, dbo}) {
+                if (!db) return LR_ERR_INVALID_ARG;
+                CK(cudaMemsetAsync(db, 0, (size_t)D * 4, s));
+            }
+        }
+        if (dc0 && B * D > 0) CK(cudaMemsetAsync(dc0, 0, (size_t)(B * D) * esize(dtype), s));
+        return LR_OK;
+    }
+    bool vec;
+    TRY(check_ptrs({zf, zi, zc, zo, c, dh, dzf, dzi, dzc, dzo}, {c0, dc0},
+                   {bf, bi, bc, bo, dbf, dbi, dbc, dbo}, dtype, D, &vec));
+    GUARD;
+    DevWS* ws;
+    TRY(get_ws(&ws));
+    Geom g;
+    Carry cr;
+    TRY(enter(*ws, s));
+    TRY(plan(*ws, OP_LSTM_BWD, dtype, vec, T, B * D, D, &g, &cr, s));
+    TRY(grow(*ws, &ws->partials, &ws->partials_cap, (size_t)(4 * g.n_chunks * g.C + 4 * g.C), false));
+    CK(launch_lstm_bwd(dtype, vec, LstmGates{zf, zi, zc, zo}, LstmBias{bf, bi, bc, bo}, c0, c, dh,
+                       LstmGates{dzf, dzi, dzc, dzo}, dc0, ws->partials, g, cr, s));
+    CK(launch_bias_reduce(ws->partials, g.n_chunks, 4, B, D, BiasOut{{dbf, dbi, dbc, dbo}}, s));
     return leave(*ws, s);
 }
 
@@ -418,7 +473,7 @@ int deer_diag_bwd(const float* w, const void* y, const void* h0, const void* dy,
     TRY(plan(*ws, OP_DEER_BWD, dtype, vec, T, B * D, D, &g, &cr, s));
     TRY(grow(*ws, &ws->partials, &ws->partials_cap, (size_t)(g.n_chunks * g.C + g.C), false));
     CK(launch_deer_bwd(dtype, vec, w, y, h0, dy, du, dh0, ws->partials, g, cr, s));
-    CK(launch_bias_reduce(ws->partials, g.n_chunks, 1, B, D, dw, nullptr, s));
+    CK(launch_bias_reduce(ws->partials, g.n_chunks, 1, B, D, BiasOut{{dw}}, s));
     return leave(*ws, s);
 }
 

@@ -35,7 +35,17 @@ struct TileShape {
     int threads;
 };
 
-enum Op { OP_SCAN_FWD = 0, OP_SCAN_BWD, OP_SRU_FWD, OP_SRU_BWD, OP_DEER, OP_DEER_BWD, OP_COUNT };
+enum Op {
+    OP_SCAN_FWD = 0,
+    OP_SCAN_BWD,
+    OP_SRU_FWD,
+    OP_SRU_BWD,
+    OP_DEER,
+    OP_DEER_BWD,
+    OP_LSTM_FWD,
+    OP_LSTM_BWD,
+    OP_COUNT
+};
 
 // Launch configuration of every kernel: NW warps per CTA, R rows per thread
 // (tile = NW*R rows), VEC channels per lane (16-byte vectors on the vector
@@ -55,8 +65,11 @@ struct KCfg {
 constexpr KCfg kcfg(Op op, int dtype, int mode) {
     // bf16 holds two elements per register: twice the rows of fp32 (but the
     // DEER backward keeps two fp32 values per element between its passes: the
-    // rows of fp32 for both)
-    return op == OP_DEER_BWD ? KCfg{8, mode == CARRY_CHAIN ? 2 : 4, mode == TILE_TMA ? 3 : 0}
+    // rows of fp32 for both).  The LSTM cell stages as many arrays per
+    // direction as the SRU cell and takes its rows.
+    return op == OP_LSTM_FWD   ? kcfg(OP_SRU_FWD, dtype, mode)
+           : op == OP_LSTM_BWD ? kcfg(OP_SRU_BWD, dtype, mode)
+           : op == OP_DEER_BWD ? KCfg{8, mode == CARRY_CHAIN ? 2 : 4, mode == TILE_TMA ? 3 : 0}
            : mode == CARRY_CHAIN
                ? (op == OP_SCAN_FWD ? KCfg{8, dtype == 1 ? 8 : 4, 0}
                   : op == OP_SCAN_BWD ? KCfg{8, dtype == 1 ? 4 : 2, 0}
@@ -199,14 +212,44 @@ cudaError_t launch_sru_bwd(int dtype, bool vec, const void* xt, const void* uf, 
                            void* dx, void* dc0, float* partials, const Geom& g,
                            const Carry& cr, cudaStream_t s);
 
+// Per-feature sums of the per-tile partials [n_arr][n_chunks][C] (n_arr <= 4)
+// into out[k] ([D] each), in a fixed order; the partials buffer must hold
+// n_arr * C more floats after them for the per-channel sums.
+struct BiasOut {
+    float* o[4];
+};
 cudaError_t launch_bias_reduce(const float* partials, int64_t n_chunks, int n_arr, int64_t B,
-                               int64_t D, float* out0, float* out1, cudaStream_t s);
+                               int64_t D, BiasOut out, cudaStream_t s);
 
 // resid: one fp32 slot (as bits), zeroed before the launch, receives max|ynew-yold|
 cudaError_t launch_deer_iter(int dtype, bool vec, const float* w, const void* u, const void* h0,
                              const void* yold, void* ynew, uint32_t* resid,
                              const uint32_t* prev_resid, float eps, const Geom& g, const Carry& cr,
                              cudaStream_t s);
+
+// LSTM cell: the four gate pre-activations (or their gradients), [T, C]
+// each, and the four per-feature biases, [D] each.
+struct LstmGates {
+    const void* f;
+    const void* i;
+    const void* c;
+    const void* o;
+};
+struct LstmBias {
+    const float* f;
+    const float* i;
+    const float* c;
+    const float* o;
+};
+cudaError_t launch_lstm_fwd(int dtype, bool vec, const LstmGates& z, const LstmBias& b,
+                            const void* c0, void* h, void* c, const Geom& g, const Carry& cr,
+                            cudaStream_t s);
+// partials: [4][n_chunks][C] fp32 scratch (forget, input, candidate, output),
+// followed by 4*C floats for launch_bias_reduce
+cudaError_t launch_lstm_bwd(int dtype, bool vec, const LstmGates& z, const LstmBias& b,
+                            const void* c0, const void* c, const void* dh, const LstmGates& dz,
+                            void* dc0, float* partials, const Geom& g, const Carry& cr,
+                            cudaStream_t s);
 
 // DEER backward: partials is [n_chunks][C] fp32 scratch (dw per tile),
 // followed by C floats that launch_bias_reduce uses for its per-channel sums

@@ -308,11 +308,11 @@ struct SruBwdOp {
     __device__ static void at_exit(const Params&, Smem&, Acc&) {}
 };
 
-// Per-feature parameter gradients (SRU biases, DEER's w) from per-tile
-// partials, in a fixed order (deterministic): stage 1 sums every channel over
-// the time chunks (one thread per channel, loads issued eight chunks ahead),
-// stage 2 sums the batch rows of each feature.  partials: [n_arr][n_chunks][C];
-// colsum: [n_arr][C]; out0 / out1: [D] (out1 only when n_arr == 2).
+// Per-feature parameter gradients (SRU and LSTM biases, DEER's w) from
+// per-tile partials, in a fixed order (deterministic): stage 1 sums every
+// channel over the time chunks (one thread per channel, loads issued eight
+// chunks ahead), stage 2 sums the batch rows of each feature.  partials:
+// [n_arr][n_chunks][C]; colsum: [n_arr][C]; out.o[k]: [D] for k < n_arr.
 __global__ void __launch_bounds__(256)
     k_bias_colsum(const float* __restrict__ partials, int64_t n_chunks, int64_t C, int n_arr,
                   float* __restrict__ colsum) {
@@ -327,18 +327,14 @@ __global__ void __launch_bounds__(256)
 }
 
 __global__ void __launch_bounds__(256)
-    k_bias_batch(const float* __restrict__ colsum, int64_t B, int64_t D, int n_arr,
-                 float* __restrict__ out0, float* __restrict__ out1) {
-    const int64_t d = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (d >= D) return;
-    const int64_t C = B * D;
-    float s0 = 0.f, s1 = 0.f;
-    for (int64_t b = 0; b < B; ++b) {
-        s0 += __ldg(colsum + b * D + d);
-        if (n_arr == 2) s1 += __ldg(colsum + C + b * D + d);
-    }
-    out0[d] = s0;
-    if (n_arr == 2) out1[d] = s1;
+    k_bias_batch(const float* __restrict__ colsum, int64_t B, int64_t D, int n_arr, BiasOut out) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n_arr * D) return;
+    const int64_t which = i / D, d = i % D;
+    const float* cs = colsum + which * B * D + d;
+    float s = 0.f;
+    for (int64_t b = 0; b < B; ++b) s += __ldg(cs + b * D);
+    out.o[which][d] = s;
 }
 
 template <typename S, bool VP, int M>
@@ -397,12 +393,13 @@ cudaError_t launch_sru_bwd(int dtype, bool vec, const void* xt, const void* uf, 
 }
 
 cudaError_t launch_bias_reduce(const float* partials, int64_t n_chunks, int n_arr, int64_t B,
-                               int64_t D, float* out0, float* out1, cudaStream_t s) {
+                               int64_t D, BiasOut out, cudaStream_t s) {
+    if (n_arr < 1 || n_arr > 4) return cudaErrorInvalidValue;
     const int64_t C = B * D;
     float* colsum = const_cast<float*>(partials) + n_arr * n_chunks * C;
     k_bias_colsum<<<(unsigned)((n_arr * C + 255) / 256), 256, 0, s>>>(partials, n_chunks, C, n_arr,
                                                                         colsum);
-    k_bias_batch<<<(unsigned)((D + 255) / 256), 256, 0, s>>>(colsum, B, D, n_arr, out0, out1);
+    k_bias_batch<<<(unsigned)((n_arr * D + 255) / 256), 256, 0, s>>>(colsum, B, D, n_arr, out);
     return cudaGetLastError();
 }
 

@@ -8,6 +8,9 @@ import torch
 import oracle
 import workloads as W
 
+# per-feature parameters: always fp32, whatever the storage type
+PARAMS = ("w", "bf", "br", "bi", "bc", "bo")
+
 # max|gpu - oracle| / max(1, max|oracle|) per output tensor
 TOL = {"f32": 1e-5, "bf16": 2e-2}
 
@@ -28,7 +31,7 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
 def dev_inputs(inp: dict, dtype: str) -> dict:
     out = {}
     for k, v in inp.items():
-        if k in ("w", "bf", "br"):
+        if k in PARAMS:
             out[k] = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).cuda()
         else:
             out[k] = to_dev(v, dtype)
@@ -36,7 +39,7 @@ def dev_inputs(inp: dict, dtype: str) -> dict:
 
 
 def f64_inputs(inp: dict, dtype: str) -> dict:
-    return {k: (np.asarray(v, np.float64) if k in ("w", "bf", "br") else W.to_f64(v, dtype))
+    return {k: (np.asarray(v, np.float64) if k in PARAMS else W.to_f64(v, dtype))
             for k, v in inp.items()}
 
 

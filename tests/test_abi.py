@@ -17,6 +17,7 @@ def lib():
 def test_every_declared_function_is_exported(lib):
     names = lrs.declared_functions()
     for required in ("lr_scan_fwd", "lr_scan_bwd", "sru_fwd", "sru_bwd", "deer_diag_solve",
+                     "deer_diag_bwd", "lstm_cell_fwd", "lstm_cell_bwd", "lr_scan_fwd_noalloc",
                      "lr_last_error", "lr_status_str"):
         assert required in names
     for n in names:
@@ -38,6 +39,9 @@ def test_argument_errors_before_cuda(lib):
     assert lib.lr_scan_bwd(P, P, P, P, P, P, P, 2, 3, 4, 0, P) == lrs.LR_ERR_INVALID_ARG
     assert lib.sru_fwd(*([P] * 9), 2, 3, 4, 0, P) == lrs.LR_ERR_INVALID_ARG
     assert lib.sru_bwd(*([P] * 16), 2, 3, 4, 0, P) == lrs.LR_ERR_INVALID_ARG
+    assert lib.lstm_cell_fwd(*([P] * 11), 2, 3, 4, 0, P) == lrs.LR_ERR_INVALID_ARG
+    assert lib.lstm_cell_bwd(*([P] * 20), 2, 3, 4, 0, P) == lrs.LR_ERR_INVALID_ARG
+    assert lib.lstm_cell_fwd(*([P] * 11), 2, 3, 4, 1, P) == lrs.LR_ERR_INVALID_ARG
     iters = ctypes.c_int(0)
     assert lib.deer_diag_solve(P, P, P, P, 2, 3, 4, ctypes.c_float(1e-5), 20, ctypes.byref(iters),
                                P, P, 0, P) == lrs.LR_ERR_INVALID_ARG
@@ -55,6 +59,7 @@ def test_empty_problem_is_a_no_op(lib):
     # B*T*D == 0 returns before touching the device
     assert lib.lr_scan_fwd(None, None, None, None, 0, 5, 4, 0, None) == lrs.LR_OK
     assert lib.sru_fwd(*([None] * 9), 3, 0, 4, 0, None) == lrs.LR_OK
+    assert lib.lstm_cell_fwd(*([None] * 11), 3, 0, 4, 0, None) == lrs.LR_OK
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -66,6 +66,64 @@ def test_sru_fwd_bwd(cuda, shape, dtype):
         assert_close(k, to_f64(g[k]), r, dtype)
 
 
+def _lstm_case(cuda, T, B, D, dtype, seed=6):
+    wl = W.like(W.LSTM, T, B, D, dtype)
+    inp = W.make_inputs(wl, seed)
+    inp["c0"] = W.store(W.normal(seed, 44, (B, D)), dtype)  # nonzero initial state
+    dv, f = dev_inputs(inp, dtype), f64_inputs(inp, dtype)
+    z = [dv[k] for k in ("zf", "zi", "zc", "zo")]
+    bias = [dv[k] for k in ("bf", "bi", "bc", "bo")]
+    zr = [f[k] for k in ("zf", "zi", "zc", "zo")]
+    br = [f[k] for k in ("bf", "bi", "bc", "bo")]
+    h, c = cuda.lstm_cell_fwd(*z, *bias, dv["c0"])
+    rh, rc = oracle.lstm_fwd(*zr, *br, f["c0"])
+    assert_close("h", to_f64(h), rh, dtype)
+    assert_close("c", to_f64(c), rc, dtype)
+    g = cuda.lstm_cell_bwd(*z, *bias, c, dv["dh"], dv["c0"])
+    ref = oracle.lstm_bwd(*zr, *br, rc, f["dh"], f["c0"])
+    for k, r in zip(("dzf", "dzi", "dzc", "dzo", "dbf", "dbi", "dbc", "dbo", "dc0"), ref):
+        assert_close(k, to_f64(g[k]), r, dtype)
+    return g
+
+
+@pytest.mark.parametrize("shape", SHAPES[:9] + WIDE + [(6001, 1, 256), (20000, 1, 128)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_lstm_cell_fwd_bwd(cuda, shape, dtype):
+    _lstm_case(cuda, *shape, dtype)
+
+
+def test_lstm_cell_gilr_tie_matches_sru(cuda):
+    """i = 1 - f (zi = -zf, bi = -bf) and the candidate as SRU's input with
+    a zero highway input: the LSTM cell's c and h are the SRU layer's, on the
+    GPU, up to the rounding of sigmoid(-z) against 1 - sigmoid(z)."""
+    T, B, D = 3000, 2, 256
+    r = np.random.default_rng(17)
+    zf = torch.from_numpy(r.standard_normal((T, B, D)).astype(np.float32)).cuda()
+    zc = torch.from_numpy(r.standard_normal((T, B, D)).astype(np.float32)).cuda()
+    zo = torch.from_numpy(r.standard_normal((T, B, D)).astype(np.float32)).cuda()
+    bf, bc, bo = (torch.from_numpy(r.standard_normal(D).astype(np.float32)).cuda() for _ in range(3))
+    c0 = torch.from_numpy(r.standard_normal((B, D)).astype(np.float32)).cuda()
+    h, c = cuda.lstm_cell_fwd(zf, -zf, zc, zo, bf, -bf, bc, bo, c0)
+    xt = torch.tanh(zc + bc)
+    hs, cs = cuda.sru_fwd(xt, zf, zo, torch.zeros_like(zf), bf, bo, c0)
+    assert float((c - cs).abs().max()) < 1e-4
+    assert float((h - hs).abs().max()) < 1e-4
+
+
+def test_lstm_cell_bwd_is_deterministic(cuda):
+    T, B, D = 4000, 8, 256
+    wl = W.like(W.LSTM, T, B, D, "f32")
+    dv = dev_inputs(W.make_inputs(wl, 2), "f32")
+    z = [dv[k] for k in ("zf", "zi", "zc", "zo")]
+    bias = [dv[k] for k in ("bf", "bi", "bc", "bo")]
+    h, c = cuda.lstm_cell_fwd(*z, *bias)
+    g1 = cuda.lstm_cell_bwd(*z, *bias, c, dv["dh"])
+    g2 = cuda.lstm_cell_bwd(*z, *bias, c, dv["dh"])
+    for k in g1:
+        if g1[k] is not None:
+            assert torch.equal(g1[k], g2[k]), k
+
+
 @pytest.mark.parametrize("shape", [(1, 1, 4), (64, 2, 8), (300, 3, 40), (77, 2, 5), (5000, 1, 128),
                                    (9000, 2, 512)] + WIDE)
 @pytest.mark.parametrize("dtype", ["f32"])
@@ -149,6 +207,33 @@ def test_empty_problems(cuda):
     assert torch.count_nonzero(dh0) == 0
     y, k, resid, hist, st = cuda.deer_diag_solve(torch.zeros(8, device="cuda"), e)
     assert (k, st) == (0, cuda.LR_OK)
+    # LSTM cell: the bias gradients and dc0 of an empty sequence are zero
+    bias = [torch.zeros(8, device="cuda") for _ in range(4)]
+    h, c = cuda.lstm_cell_fwd(e, e, e, e, *bias)
+    assert h.shape == (0, 3, 8)
+    out = {k: torch.full((8,), 7.0, device="cuda") for k in ("dbf", "dbi", "dbc", "dbo")}
+    out["dc0"] = torch.full((3, 8), 7.0, device="cuda")
+    g = cuda.lstm_cell_bwd(e, e, e, e, *bias, e, e, out=out)
+    torch.cuda.synchronize()
+    for k in ("dbf", "dbi", "dbc", "dbo", "dc0"):
+        assert torch.count_nonzero(g[k]) == 0, k
+
+
+def test_lstm_cell_null_initial_state(cuda):
+    T, B, D = 130, 2, 16
+    wl = W.like(W.LSTM, T, B, D, "f32")
+    inp = W.make_inputs(wl, 9)
+    dv, f = dev_inputs(inp, "f32"), f64_inputs(inp, "f32")
+    z = [dv[k] for k in ("zf", "zi", "zc", "zo")] + [dv[k] for k in ("bf", "bi", "bc", "bo")]
+    zr = [f[k] for k in ("zf", "zi", "zc", "zo")] + [f[k] for k in ("bf", "bi", "bc", "bo")]
+    h, c = cuda.lstm_cell_fwd(*z, None)
+    rh, rc = oracle.lstm_fwd(*zr)
+    assert_close("h", to_f64(h), rh, "f32")
+    g = cuda.lstm_cell_bwd(*z, c, dv["dh"], None, want_dc0=False)
+    assert g.get("dc0") is None
+    ref = oracle.lstm_bwd(*zr, rc, f["dh"])
+    assert_close("dzf", to_f64(g["dzf"]), ref[0], "f32")
+    assert_close("dbf", to_f64(g["dbf"]), ref[4], "f32")
 
 
 @pytest.mark.parametrize("shape", [(2048, 4, 256), (64, 40, 1000)])

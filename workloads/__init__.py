@@ -26,7 +26,8 @@ BLOCK = 1 << 22
 
 # fixed ids of the tensor roles (part of the input recipe)
 TID = {"a": 1, "b": 2, "h0": 3, "g": 4, "xt": 5, "uf": 6, "ur": 7, "x": 8,
-       "dh": 9, "w": 10, "u": 11}
+       "dh": 9, "w": 10, "u": 11, "zf": 12, "zi": 13, "zc": 14, "zo": 15,
+       "bf": 16, "bi": 17, "bc": 18, "bo": 19}
 
 
 def _threads() -> int:
@@ -109,7 +110,7 @@ def store(x: np.ndarray, dtype: str) -> np.ndarray:
 @dataclass
 class Workload:
     name: str
-    kind: str               # "scan" | "sru" | "deer"
+    kind: str               # "scan" | "sru" | "deer" | "lstm"
     T: int
     B: int
     D: int
@@ -140,6 +141,9 @@ SCAN_BF16 = Workload("scan_large_bf16", "scan", 8192, 16, 4096, "bf16", True,
 DEER = Workload("deer_tanh_f32", "deer", 65536, 4, 256, "f32", False,
                 {"eps": 1e-5, "kmax": 20})
 FULL = [SCAN_TINY, SRU, SCAN_LONG, SCAN_BF16, DEER]
+# The LSTM cell-state scan at the SRU layer's size (the pages give no LSTM
+# sizes; same [T, B, D] and the same number of gate projections per element).
+LSTM = Workload("lstm_cell_f32", "lstm", 2048, 32, 1024, "f32", True)
 
 
 def like(base: Workload, T=None, B=None, D=None, dtype=None, name=None) -> Workload:
@@ -172,6 +176,16 @@ def make_inputs(wl: Workload, seed: int = 0) -> dict:
             out[k] = st(normal(seed, TID[k], shp))
         out["bf"] = np.full(wl.D, wl.extra.get("bf", 1.0), np.float32)
         out["br"] = np.full(wl.D, wl.extra.get("br", -1.0), np.float32)
+        out["c0"] = st(np.zeros((wl.B, wl.D), np.float32))
+        if wl.backward:
+            out["dh"] = st(normal(seed, TID["dh"], shp))
+    elif wl.kind == "lstm":
+        for k in ("zf", "zi", "zc", "zo"):
+            out[k] = st(normal(seed, TID[k], shp))
+        # biases: forget gate biased open (mean 1), the others around 0
+        out["bf"] = normal(seed, TID["bf"], (wl.D,), 1.0, 0.5)
+        for k in ("bi", "bc", "bo"):
+            out[k] = normal(seed, TID[k], (wl.D,), 0.0, 0.5)
         out["c0"] = st(np.zeros((wl.B, wl.D), np.float32))
         if wl.backward:
             out["dh"] = st(normal(seed, TID["dh"], shp))
