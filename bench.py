@@ -44,22 +44,25 @@ FALLBACK_HBM_GBS = 6800.0
 EPS, KMAX = 1e-5, 20
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
-# ncu capture, keyed by operation; valid only while the kernel sources hash to
-# `src`.  Filled from the committed ncu summaries under profiles/.  deer.solve:
-# DRAM bytes read + written per launch, averaged over the K = 6 launches of a
-# solve (first iteration + 5 x second iteration, both captured at full size,
+# ncu capture, keyed by operation; valid only while the kernel's sources (the
+# shared device headers and its own kernel file) hash to `src`.  Filled from
+# the committed ncu summaries under profiles/.  deer.solve: DRAM bytes read +
+# written per launch, averaged over the K = 6 launches of a solve (first
+# iteration + 5 x second iteration, both captured at full size,
 # profiles/dram_traffic.md).
-NCU_TRAFFIC = {"deer.solve": {"bytes": 1174852011, "src": "cc0c561d98f6cd4c"}}
+NCU_TRAFFIC = {"deer.solve": {"bytes": 1174852011, "src": "cc0c561d98f6cd4c",
+                              "file": "deer_kernels.cu"}}
 
 
-def src_hash() -> str:
-    """Hash of the code the kernels are compiled from (device code and the
-    launch configuration, comments and blank lines left out; the host-only
-    C-ABI files do not change a kernel)."""
+def src_hash(kernel_file: str = "deer_kernels.cu") -> str:
+    """Hash of the code one operation's kernels are compiled from: the shared
+    device headers, the launch configuration and that operation's kernel
+    file, comments and blank lines left out (the host-only C-ABI files and
+    the other operations' kernel files do not change its kernel)."""
     h = hashlib.sha256()
     cdir = os.path.join(ROOT, "linear_recurrence_scan_chunked_gb300", "csrc")
     for n in sorted(os.listdir(cdir)):
-        if n.endswith((".cuh", "_kernels.cu")) or n == "lr_launch.h":
+        if n.endswith(".cuh") or n in ("lr_launch.h", kernel_file):
             for line in open(os.path.join(cdir, n)):
                 code = line.split("//", 1)[0].rstrip()
                 if code:
@@ -612,7 +615,7 @@ def main():
     bytes_per_launch = pass_bytes(dwl, dp, k) / ops[dom]["launches"]
     achieved = bytes_per_launch / (launch_ms / 1e3) / 1e9
     tr = NCU_TRAFFIC.get(dom)
-    traffic = tr["bytes"] if tr and tr.get("src") == src_hash() else None
+    traffic = tr["bytes"] if tr and tr.get("src") == src_hash(tr["file"]) else None
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": dom,
             "peak_source": f"{peak_kind} HBM copy bandwidth",
