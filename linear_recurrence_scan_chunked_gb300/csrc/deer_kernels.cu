@@ -14,6 +14,12 @@
 // folds max |y_t - yold_t| into one residual word (the stopping test of the
 // section "工程实现": ||y^(i+1) - y^(i)|| < eps, here the max-abs norm).
 // yold == nullptr is the all-zero initial guess (not read).
+//
+// On the segmented walker kernel the epilogue also builds the next
+// iteration's J and rhs at row t from the value just computed at row t-1 (as
+// stored: bf16-rounded for bf16 storage) and u_t, exactly what the next
+// iteration would read, and folds them into the next iteration's segment
+// aggregates; the next iteration then needs no reduce pass (NextAgg).
 #include "lr_act.cuh"
 #include "lr_launch.h"
 #include "lr_persist.cuh"
@@ -30,6 +36,7 @@ struct DeerParams {
     uint32_t* resid;
     const uint32_t* prev_resid;  // residual of the previous iteration (nullptr: first)
     float eps;
+    NextAgg nx;  // next iteration's aggregates (segmented walker kernel only)
 };
 
 template <typename S_, int VEC_, int NW_, int R_>
@@ -39,6 +46,7 @@ struct DeerOp {
     static constexpr bool REV = false;
     static constexpr int IN_ARRAYS = 2;  // u, previous iterate
     static constexpr bool SCRATCH_IN_CARRY = false;
+    static constexpr bool NEXT_AGG = true;
     using Params = DeerParams<S>;
     struct Regs {
         Pack<S, VEC> u[R];
@@ -46,10 +54,12 @@ struct DeerOp {
     };
     struct Work {
         float J[R][VEC], Rh[R][VEC];
+        float NA[VEC], NB[VEC];  // next iteration's aggregate of this thread's rows
     };
     struct Smem {
         uint32_t mx[NW];
     };
+    __device__ static NextAgg next_agg(const Params& p) { return p.nx; }
     struct Acc {
         uint32_t mx;  // max |y - yold| as bits: fp32 order of non-negative values, NaN on top
     };
@@ -121,9 +131,26 @@ struct DeerOp {
     }
     __device__ static void finish(const Params& p, const Geom& g, const TileCoord& tc,
                                   const Regs& rg, Work& w, float (&s)[VEC], Smem&, Acc& acc) {
+        const bool nxt = p.nx.agg != nullptr;
+        float wv[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { wv[v] = 0.f; w.NA[v] = 1.f; w.NB[v] = 0.f; }
+        if (nxt && tc.cok) load_param<VEC>(p.w + tc.c % g.D, wv);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int64_t t = tc.t0 + r;
+            if (nxt && tc.cok && t < g.T) {
+                // next iteration, row t: from y_{t-1} (s, as stored) and u_t
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    float yp = s[v];
+                    if constexpr (sizeof(S) == 2) yp = bf_lo(bf_bits(yp));
+                    const float th = act_tanh(wv[v] * yp + rg.u[r].get(v));
+                    const float jac = wv[v] * (1.f - th * th);
+                    w.NB[v] = jac * w.NB[v] + (th - jac * yp);
+                    w.NA[v] *= jac;
+                }
+            }
 #pragma unroll
             for (int v = 0; v < VEC; ++v) s[v] = w.J[r][v] * s[v] + w.Rh[r][v];
             if (tc.cok && t < g.T) {
@@ -305,22 +332,25 @@ using DeerOpT = DeerOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_DEER, sizeof(S) == 2
 template <typename S, bool VP>
 static cudaError_t deer_t(const float* w, const void* u, const void* h0, const void* yold,
                           void* ynew, uint32_t* resid, const uint32_t* prev_resid, float eps,
-                          const Geom& g, const Carry& cr, cudaStream_t s) {
+                          const NextAgg& nx, const Geom& g, const Carry& cr, cudaStream_t s) {
     return launch_persist<DeerOpT<S, VP, CARRY_CHAIN>, DeerOpT<S, VP, CARRY_WALK>,
                           DeerOpT<S, VP, TILE_TMA>, kcfg(OP_DEER, sizeof(S) == 2, TILE_TMA).ST>(
-        {w, (const S*)u, (const S*)h0, (const S*)yold, (S*)ynew, resid, prev_resid, eps}, g, cr, s);
+        {w, (const S*)u, (const S*)h0, (const S*)yold, (S*)ynew, resid, prev_resid, eps, nx}, g,
+        cr, s);
 }
 
 cudaError_t launch_deer_iter(int dtype, bool vec, const float* w, const void* u, const void* h0,
                              const void* yold, void* ynew, uint32_t* resid,
-                             const uint32_t* prev_resid, float eps, const Geom& g, const Carry& cr,
-                             cudaStream_t s) {
+                             const uint32_t* prev_resid, float eps, const NextAgg& nx,
+                             const Geom& g, const Carry& cr, cudaStream_t s) {
     if (dtype == 0)
-        return vec ? deer_t<float, true>(w, u, h0, yold, ynew, resid, prev_resid, eps, g, cr, s)
-                   : deer_t<float, false>(w, u, h0, yold, ynew, resid, prev_resid, eps, g, cr, s);
-    return vec ? deer_t<__nv_bfloat16, true>(w, u, h0, yold, ynew, resid, prev_resid, eps, g, cr, s)
-               : deer_t<__nv_bfloat16, false>(w, u, h0, yold, ynew, resid, prev_resid, eps, g, cr,
-                                              s);
+        return vec ? deer_t<float, true>(w, u, h0, yold, ynew, resid, prev_resid, eps, nx, g, cr, s)
+                   : deer_t<float, false>(w, u, h0, yold, ynew, resid, prev_resid, eps, nx, g, cr,
+                                          s);
+    return vec ? deer_t<__nv_bfloat16, true>(w, u, h0, yold, ynew, resid, prev_resid, eps, nx, g,
+                                             cr, s)
+               : deer_t<__nv_bfloat16, false>(w, u, h0, yold, ynew, resid, prev_resid, eps, nx, g,
+                                              cr, s);
 }
 
 template <typename S, bool VP, int M>

@@ -408,6 +408,19 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y, int6
         ws->ybuf_cap = cap;
     }
     TRY(enter(*ws, s));
+    // On the segmented walker kernel each iteration also publishes the next
+    // one's segment aggregates (two buffers after the packets plan() lays
+    // out, alternating), tagged with the next launch's epoch; from the second
+    // iteration on a launch has no reduce pass.
+    const CarryPlan cp = carry_plan(OP_DEER, dtype, vec, use_tma(dtype, vec, T, B * D), T, B * D);
+    const bool onepass = cp.mode == CARRY_WALK && cp.tma;
+    if (onepass) {
+        TRY(grow(*ws, &ws->pk, &ws->pk_cap, cp.inc_elems + 2 * cp.agg_elems, true));
+        if (ws->epoch > 0xFFFFFFFFu - (uint32_t)(kmax + 8)) {  // no epoch wrap inside the solve
+            CK(cudaMemsetAsync(ws->pk, 0, ws->pk_cap * sizeof(u64), s));
+            ws->epoch = 0;
+        }
+    }
     uint32_t* slots = ws->words + 2;
     CK(cudaMemsetAsync(slots, 0, sizeof(uint32_t) * kmax, s));
     // iterate k writes buf[k % 2]; buf[1] is the caller's y.  Iterations are
@@ -427,9 +440,17 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y, int6
             Geom g;
             Carry cr;
             TRY(plan(*ws, OP_DEER, dtype, vec, T, B * D, D, &g, &cr, s));
+            NextAgg nx{nullptr, 0u, 0u};
+            if (onepass) {
+                u64* agg0 = ws->pk + cp.inc_elems;  // where plan() put cr.agg
+                cr.agg = (kk & 1) ? agg0 : agg0 + cp.agg_elems;
+                nx.agg = (kk & 1) ? agg0 + cp.agg_elems : agg0;
+                nx.epoch = cr.epoch + 1;  // the next plan() call's
+                nx.pre = kk > 1 ? 1u : 0u;
+            }
             CK(launch_deer_iter(dtype, vec, w, u, h0, kk == 1 ? nullptr : buf[(kk - 1) & 1],
                                 buf[kk & 1], slots + (kk - 1), kk == 1 ? nullptr : slots + (kk - 2),
-                                eps, g, cr, s));
+                                eps, nx, g, cr, s));
         }
         CK(cudaMemcpyAsync(ws->host_word + first, slots + first, sizeof(uint32_t) * nb,
                            cudaMemcpyDeviceToHost, s));

@@ -47,6 +47,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace lrs {
 
 constexpr uint32_t ERRBIT_TIMEOUT = 1u;
@@ -73,6 +75,23 @@ struct Carry {
     int wv;               // channels per walker warp (WALK)
     int tma;              // CHAIN: tiles are staged by TMA (k_strip / k_tchain)
 };
+
+// Aggregates published one launch ahead, for operations whose next launch
+// builds its coefficients from this launch's outputs (segmented walker
+// kernel only).
+struct NextAgg {
+    u64* agg;        // [C][n_seg][2] (A, B) packets of the next launch; nullptr: none
+    uint32_t epoch;  // the next launch's epoch
+    uint32_t pre;    // this launch's aggregates were published by the previous launch
+};
+// Op::NEXT_AGG (optional, default false): the operation computes the next
+// launch's per-thread aggregate in finish() (Work::NA, Work::NB) and exposes
+// its NextAgg through Op::next_agg(params).
+template <class Op, class = void>
+struct has_next_agg : std::false_type {};
+template <class Op>
+struct has_next_agg<Op, std::void_t<decltype(Op::NEXT_AGG)>>
+    : std::integral_constant<bool, Op::NEXT_AGG> {};
 
 struct Geom {
     int64_t T;            // rows

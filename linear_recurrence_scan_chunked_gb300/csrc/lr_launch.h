@@ -221,11 +221,14 @@ struct BiasOut {
 cudaError_t launch_bias_reduce(const float* partials, int64_t n_chunks, int n_arr, int64_t B,
                                int64_t D, BiasOut out, cudaStream_t s);
 
-// resid: one fp32 slot (as bits), zeroed before the launch, receives max|ynew-yold|
+// resid: one fp32 slot (as bits), zeroed before the launch, receives max|ynew-yold|.
+// nx: the next iteration's segment aggregates (segmented walker kernel only;
+// nx.agg == nullptr otherwise), and whether this launch's were published by
+// the previous one (then cr.agg must point at them).
 cudaError_t launch_deer_iter(int dtype, bool vec, const float* w, const void* u, const void* h0,
                              const void* yold, void* ynew, uint32_t* resid,
-                             const uint32_t* prev_resid, float eps, const Geom& g, const Carry& cr,
-                             cudaStream_t s);
+                             const uint32_t* prev_resid, float eps, const NextAgg& nx,
+                             const Geom& g, const Carry& cr, cudaStream_t s);
 
 // LSTM cell: the four gate pre-activations (or their gradients), [T, C]
 // each, and the four per-feature biases, [D] each.

@@ -500,6 +500,15 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
 // issued ST - 1 uses ahead by thread 0 (tickets are drawn one iteration
 // early).  A consume only waits for reduces of smaller tickets, and every CTA
 // reduces before it consumes: every wait ends.
+//
+// Operations whose next launch's coefficients are built from this launch's
+// outputs (DEER: iteration k+1's Jacobian and right-hand side at row t come
+// from y^(k)_{t-1} and u_t) also fold, in the consume pass, the segment
+// aggregates of the next launch and publish them with its epoch
+// (NEXT_AGG, NextAgg::agg).  A launch whose aggregates were published that way
+// (NextAgg::pre) has no reduce pass: each ticket is consumed at once, its
+// tiles read from HBM once, while the walkers fold aggregates that are all
+// visible from the start.
 #ifndef LR_SEG_LAG
 #define LR_SEG_LAG 2
 #endif
@@ -527,6 +536,19 @@ __device__ __forceinline__ void seg_issue(const Geom& g, const TmaDesc& td, unsi
                              pol);
 }
 
+// Per-warp partials of the next launch's aggregate of the chunk just
+// finished (k_seg, NEXT_AGG operations).  They live in that chunk's ring
+// stage: its tile is in registers by then, and the stage is refilled only
+// after the next barrier, once warp 0 has folded them.
+template <int VEC, int NW>
+struct NextPart {
+    float a[NW][32][VEC];
+    float b[NW][32][VEC];
+};
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 template <class Op, int ST>
 __global__ void __launch_bounds__(Op::NW * 32, 2)
     k_seg(typename Op::Params p, Geom g, Carry cr, SegGeom sg,
@@ -534,6 +556,7 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
     if (Op::skip(p)) return;  // whole launch: before any ticket or barrier
     constexpr int NW = Op::NW, VEC = Op::VEC, L = Op::NW * Op::R;
     constexpr uint32_t SB = tma_stage_bytes<Op>();
+    constexpr bool NXT = has_next_agg<Op>::value;
     extern __shared__ unsigned char dyn_smem[];
     unsigned char* ring = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~(uintptr_t)127);
@@ -545,7 +568,13 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
     __shared__ uint32_t s_tk[2], s_abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t limit = cr.n_walk + sg.n_units;
-    const uint32_t uses = 2 * sg.seg;  // per iteration: reduce pass, consume pass
+    NextAgg nx{nullptr, 0u, 0u};
+    if constexpr (NXT) nx = Op::next_agg(p);
+    const bool pre = nx.pre != 0;
+    static_assert(!NXT || sizeof(NextPart<VEC, NW>) <= SB, "partials must fit in a stage");
+    // uses per iteration: the reduce pass (none when pre), the consume pass
+    const uint32_t nred = pre ? 0u : sg.seg;
+    const uint32_t uses = nred + sg.seg;
     if (threadIdx.x == 0) {
         const uint32_t t = atomicAdd(cr.ticket, 1u);
         if (t == g.n_draws - 1) atomicExch(cr.ticket, 0u);
@@ -567,21 +596,23 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
     uint32_t inflight = 0;  // stages with a box in flight
     uint64_t pol_keep = 0, pol_drop = 0;
     // Thread 0: issue use u into stage u % ST.  Use u is chunk k of the reduce
-    // pass of ticket `red` (k < SEG) or chunk k - SEG of the consume pass of
+    // pass of ticket `red` (k < nred) or chunk k - nred of the consume pass of
     // ticket `con`; tickets >= limit have no segment.
     auto issue = [&](uint32_t u, uint32_t red, uint32_t con) {
         const uint32_t k = u % uses;
-        const uint32_t tk = k < sg.seg ? red : con, c = k < sg.seg ? k : k - sg.seg;
+        const uint32_t tk = k < nred ? red : con, c = k < nred ? k : k - nred;
         if (tk >= limit) return;
         const uint32_t x = tk - cr.n_walk, seg = x / (uint32_t)g.n_ct;
         const uint32_t j = x - seg * (uint32_t)g.n_ct, q = seg * sg.seg + c;
         if (q >= (uint32_t)g.n_chunks) return;
         const uint32_t st = u % ST;
-        seg_issue<Op, ST>(g, td, ring, full, st, q, j, k < sg.seg ? pol_keep : pol_drop);
+        seg_issue<Op, ST>(g, td, ring, full, st, q, j, k < nred ? pol_keep : pol_drop);
         inflight |= 1u << st;
     };
     // tq[0]: ticket consumed this iteration, tq[SEG_LAG]: reduced this
-    // iteration, tq[SEG_LAG + 1]: reduced next iteration
+    // iteration, tq[SEG_LAG + 1]: reduced next iteration.  Without a reduce
+    // pass (pre) tq[SEG_LAG] is consumed this iteration and tq[SEG_LAG + 1]
+    // the next.
     uint32_t tq[SEG_LAG + 2];
 #pragma unroll
     for (int i = 0; i < SEG_LAG; ++i) tq[i] = limit;
@@ -595,9 +626,9 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         if (t1 == g.n_draws - 1) atomicExch(cr.ticket, 0u);
         if (t1 >= limit) drawing = false;
         s_tk[1] = t1;
-        // uses 0 .. ST-1: the first chunks of the reduce pass of `cur` (the
-        // launch keeps SEG >= ST)
-        for (uint32_t u = 0; u < (uint32_t)ST; ++u) issue(u, cur, limit);
+        // uses 0 .. ST-1: the first chunks of the reduce pass of `cur`, or of
+        // its consume pass when pre (the launch keeps SEG >= ST)
+        for (uint32_t u = 0; u < (uint32_t)ST; ++u) issue(u, cur, pre ? cur : limit);
         if (drawing) pend = atomicAdd(cr.ticket, 1u);
     }
     __syncthreads();
@@ -607,6 +638,30 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
     typename Op::Acc acc;
     Op::acc_init(acc);
     bool stop = false;
+    // Next launch's aggregate of the segment being consumed: warp 0 folds the
+    // chunks' warp partials (written into a chunk's stage after its finish,
+    // read after the next barrier, before that stage is refilled) in row order.
+    float NA[VEC], NB[VEC];
+    bool nx_pend = false;  // partials of the previous chunk await the fold
+    uint32_t nx_st = 0;    // the stage holding them
+    auto nx_fold = [&]() {
+        if constexpr (NXT) {
+            if (warp == 0 && nx_pend) {
+                const NextPart<VEC, NW>& np =
+                    *reinterpret_cast<const NextPart<VEC, NW>*>(ring + nx_st * SB);
+#pragma unroll
+                for (int w2 = 0; w2 < NW; ++w2)
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) {
+                        const float a = np.a[w2][lane][v];
+                        NB[v] = __fmaf_rn(a, NB[v], np.b[w2][lane][v]);
+                        NA[v] *= a;
+                    }
+                __syncwarp();  // every lane has read them before thread 0 refills the stage
+            }
+        }
+        nx_pend = false;
+    };
     // Top of use `it`: wait for its box, then a barrier after which the stage
     // of use it-1 is free and the stop decision is uniform; refill that stage
     // with use it-1+ST (this iteration's tickets, or the next iteration's).
@@ -615,10 +670,11 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         if (valid && !mbar_wait(&full[st], (phase >> st) & 1u, cr.err)) s_abort = 1;
         csync<NW>();
         if (s_abort != 0) return false;
+        nx_fold();  // the previous chunk's partials, in the stage refilled next
         if (threadIdx.x == 0 && it > 0) {
             const uint32_t u = it - 1 + ST;
-            if (u / uses == it / uses) issue(u, tq[SEG_LAG], tq[0]);
-            else issue(u, tq[SEG_LAG + 1], tq[1]);
+            if (u / uses == it / uses) issue(u, tq[SEG_LAG], pre ? tq[SEG_LAG] : tq[0]);
+            else issue(u, tq[SEG_LAG + 1], pre ? tq[SEG_LAG + 1] : tq[1]);
         }
         if (valid) {
             phase ^= 1u << st;
@@ -627,13 +683,13 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         return true;
     };
     auto active = [&]() {
-        bool a = false;
+        bool a = tq[SEG_LAG] < limit;
 #pragma unroll
-        for (int i = 0; i <= SEG_LAG; ++i) a = a || tq[i] < limit;
+        for (int i = 0; i < SEG_LAG; ++i) a = a || (!pre && tq[i] < limit);
         return a;
     };
     while (active() && !stop) {
-        const uint32_t tk_red = tq[SEG_LAG], tk_con = tq[0];
+        const uint32_t tk_red = pre ? limit : tq[SEG_LAG], tk_con = pre ? tq[SEG_LAG] : tq[0];
         // ---- pass 1: the aggregate of the segment of `tk_red`
         const bool has_red = tk_red < limit;
         const uint32_t xr = has_red ? tk_red - cr.n_walk : 0u;
@@ -641,7 +697,7 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         float SA[VEC], SBv[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { SA[v] = 1.f; SBv[v] = 0.f; }
-        for (uint32_t c = 0; c < sg.seg; ++c, ++it) {
+        for (uint32_t c = 0; c < nred; ++c, ++it) {
             const uint32_t q = seg_r * sg.seg + c;
             const bool valid = has_red && q < (uint32_t)g.n_chunks;
             if (!top(valid)) { stop = true; break; }
@@ -709,6 +765,8 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
 #pragma unroll
             for (int v = 0; v < VEC; ++v) carry[0][lane][v] = cin[v];
         }
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { NA[v] = 1.f; NB[v] = 0.f; }
         for (uint32_t c = 0; c < sg.seg; ++c, ++it) {
             const uint32_t q = seg_c * sg.seg + c;
             const bool valid = has_con && q < (uint32_t)g.n_chunks;
@@ -725,8 +783,38 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
             for (int v = 0; v < VEC; ++v) s0[v] = 0.f;
             strip_carry<VEC, NW>(sm, A, B, s0, st, carry, (int)(c & 1u), false, tc.cok);
             Op::finish(p, g, tc, regs, w, st, xs, acc);
+            if constexpr (NXT) {
+                if (nx.agg != nullptr) {
+                    // into this chunk's stage: every warp copied its tile out
+                    // of it before the barrier inside strip_carry
+                    NextPart<VEC, NW>& np = *reinterpret_cast<NextPart<VEC, NW>*>(ring + (it % ST) * SB);
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) {
+                        np.a[warp][lane][v] = w.NA[v];
+                        np.b[warp][lane][v] = w.NB[v];
+                    }
+                    fence_proxy_async_smem();  // ordered before the copy that refills the stage
+                    nx_pend = true;
+                    nx_st = it % ST;
+                }
+            }
         }
         if (stop) break;
+        if constexpr (NXT) {
+            if (nx.agg != nullptr && has_con) {
+                csync<NW>();
+                nx_fold();
+                const TileCoord tc = tile_coord_qj<Op>(g, seg_c * sg.seg, j_c);
+                if (warp == 0 && tc.cok && seg_c + 1 < sg.n_seg) {
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v)
+                        st_pkt2(nx.agg + 2 * ((tc.c + v) * sg.n_seg + seg_c), pkt(NA[v], nx.epoch),
+                                pkt(NB[v], nx.epoch));
+                }
+                // the ticket step below ends with a block barrier before any
+                // warp writes partials again
+            }
+        }
         // ---- next iteration: shift the ticket queue, append the one drawn
         if (threadIdx.x == 0) {
             uint32_t t2 = limit;
