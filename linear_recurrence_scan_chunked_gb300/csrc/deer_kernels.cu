@@ -59,7 +59,7 @@ struct DeerOp {
     struct Smem {
         uint32_t mx[NW];
     };
-    __device__ static NextAgg next_agg(const Params& p) { return p.nx; }
+    __host__ __device__ static NextAgg next_agg(const Params& p) { return p.nx; }
     struct Acc {
         uint32_t mx;  // max |y - yold| as bits: fp32 order of non-negative values, NaN on top
     };

@@ -838,6 +838,221 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
             if (inflight & (1u << st)) mbar_wait(&full[st], (phase >> st) & 1u, cr.err);
 }
 
+// Segmented walker kernel, consume only: a launch whose segment aggregates
+// the previous launch published (NEXT_AGG operations with NextAgg::pre: DEER
+// iterations after the first).  Each ticket (segment) is consumed as soon as
+// it is drawn, its tiles read from HBM once.  One barrier per chunk: the warp
+// aggregates and the next launch's per-warp partials alternate between two
+// buffers by chunk parity (a warp may start the next chunk while another is
+// still folding this one), the stop decision is read after that barrier, and
+// a chunk's stage is refilled right after it -- every warp has copied its tile
+// out by then -- so two stages keep two tiles in flight during the fold and
+// the epilogue.
+template <class Op, int ST>
+__global__ void __launch_bounds__(Op::NW * 32, 2)
+    k_seg1(typename Op::Params p, Geom g, Carry cr, SegGeom sg,
+           const __grid_constant__ TmaDesc td) {
+    static_assert(has_next_agg<Op>::value, "a consume-only launch publishes the next aggregates");
+    if (Op::skip(p)) return;  // whole launch: before any ticket or barrier
+    constexpr int NW = Op::NW, VEC = Op::VEC, L = Op::NW * Op::R;
+    constexpr uint32_t SB = tma_stage_bytes<Op>();
+    extern __shared__ unsigned char dyn_smem[];
+    unsigned char* ring = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~(uintptr_t)127);
+    __shared__ StripSmem<VEC, NW> sm[2];
+    __shared__ NextPart<VEC, NW> part[2];
+    __shared__ typename Op::Smem xs;
+    __shared__ float carry[2][32][VEC];  // by chunk parity
+    __shared__ __align__(8) uint64_t full[ST];
+    __shared__ uint32_t s_tk[2], s_abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t limit = cr.n_walk + sg.n_units;
+    const NextAgg nx = Op::next_agg(p);
+    if (threadIdx.x == 0) {
+        const uint32_t t = atomicAdd(cr.ticket, 1u);
+        if (t == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+        s_tk[0] = t;
+        s_abort = 0;
+    }
+    __syncthreads();
+    const uint32_t cur = s_tk[0];
+    if (cur < cr.n_walk) {  // walker role: its chunks are the segments
+        Geom gw = g;
+        gw.n_chunks = sg.n_seg;
+        walker<typename Op::S, NW>(cr, gw, cur, Op::init_ptr(p));
+        return;
+    }
+    if (cur >= limit) return;
+    // thread 0 state: the ticket drawn ahead, loads issued ahead
+    bool drawing = true;
+    uint32_t pend = 0;
+    uint32_t inflight = 0;  // stages with a box in flight
+    uint64_t pol = 0;
+    uint32_t tk = cur, tk_next = limit;
+    // Thread 0: issue use u (chunk u % SEG of the ticket whose uses it is
+    // part of: every ticket has SEG uses) into stage u % ST.
+    auto issue = [&](uint32_t u, uint32_t t) {
+        if (t >= limit) return;
+        const uint32_t x = t - cr.n_walk, seg = x / (uint32_t)g.n_ct;
+        const uint32_t j = x - seg * (uint32_t)g.n_ct, q = seg * sg.seg + u % sg.seg;
+        if (q >= (uint32_t)g.n_chunks) return;
+        const uint32_t st = u % ST;
+        seg_issue<Op, ST>(g, td, ring, full, st, q, j, pol);
+        inflight |= 1u << st;
+    };
+    // Thread 0, once use u's stage is free: issue use u + ST (the same
+    // ticket's, or the next one's; SEG >= ST).
+    auto refill = [&](uint32_t u) {
+        if (threadIdx.x == 0) {
+            const uint32_t v = u + ST;
+            issue(v, v / sg.seg == u / sg.seg ? tk : tk_next);
+        }
+    };
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < ST; ++i) mbar_init(&full[i], 1);
+        mbar_init_fence();
+        pol = l2_evict_first();  // every tile is read once
+        const uint32_t t1 = atomicAdd(cr.ticket, 1u);
+        if (t1 == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+        if (t1 >= limit) drawing = false;
+        s_tk[1] = t1;
+        tk_next = t1;
+        for (uint32_t u = 0; u < (uint32_t)ST; ++u) issue(u, cur);
+        if (drawing) pend = atomicAdd(cr.ticket, 1u);
+    }
+    __syncthreads();
+    tk_next = s_tk[1];
+    uint32_t phase = 0;  // parity of the next completion of each stage's barrier
+    uint32_t it = 0;     // uses consumed
+    typename Op::Acc acc;
+    Op::acc_init(acc);
+    bool stop = false;
+    while (tk < limit) {
+        const uint32_t x = tk - cr.n_walk;
+        const uint32_t seg_c = x / (uint32_t)g.n_ct, j_c = x - seg_c * (uint32_t)g.n_ct;
+        if (warp == 0) {  // the state entering the segment, from the walkers
+            const TileCoord tc = tile_coord_qj<Op>(g, seg_c * sg.seg, j_c);
+            float cin[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) cin[v] = 0.f;
+            const typename Op::S* ip = Op::init_ptr(p);
+            if (seg_c == 0) {
+                if (tc.cok && ip != nullptr) load_vec<typename Op::S, VEC>(ip + tc.c, cin);
+            } else {
+                uint32_t spins = 0, sleep_ns = 0;
+                while (true) {
+                    const bool ok = !tc.cok || get_states_strided<VEC>(
+                                                   cr.inc + tc.c * sg.n_seg + seg_c - 1, sg.n_seg,
+                                                   cin, cr.epoch);
+                    if (__all_sync(0xffffffffu, ok)) break;
+                    if (__any_sync(0xffffffffu, wait_step(cr, spins, sleep_ns, kTileMaxSleepNs))) {
+                        if (lane == 0) atomicOr(cr.err, ERRBIT_TIMEOUT);
+#pragma unroll
+                        for (int v = 0; v < VEC; ++v) cin[v] = __int_as_float(0x7fc00000);
+                        break;
+                    }
+                }
+            }
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) carry[0][lane][v] = cin[v];
+        }
+        float NA[VEC], NB[VEC];  // warp 0: the next launch's aggregate of this segment
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { NA[v] = 1.f; NB[v] = 0.f; }
+        int pend_buf = -1;  // part[] buffer whose partials await warp 0's fold
+        auto fold_part = [&]() {
+            if (warp == 0 && pend_buf >= 0) {
+#pragma unroll
+                for (int w2 = 0; w2 < NW; ++w2)
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) {
+                        const float a = part[pend_buf].a[w2][lane][v];
+                        NB[v] = __fmaf_rn(a, NB[v], part[pend_buf].b[w2][lane][v]);
+                        NA[v] *= a;
+                    }
+            }
+            pend_buf = -1;
+        };
+        for (uint32_t c = 0; c < sg.seg; ++c, ++it) {
+            const uint32_t q = seg_c * sg.seg + c;
+            const uint32_t st = it % ST;
+            if (q >= (uint32_t)g.n_chunks) {  // past the strip's end: no box, stage idle
+                refill(it);
+                continue;
+            }
+            if (!mbar_wait(&full[st], (phase >> st) & 1u, cr.err)) s_abort = 1;
+            phase ^= 1u << st;
+            const TileCoord tc = tile_coord_qj<Op>(g, q, j_c);
+            typename Op::Regs regs;
+            typename Op::Work w;
+            Op::load(SmemSrc<Op>{ring + st * SB, tc.tchunk * L, lane * VEC}, p, g, tc, regs);
+            float A[VEC], B[VEC];
+            Op::aggregate(p, g, tc, regs, w, A, B, true);
+            const int par = (int)(c & 1u);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                sm[par].a[warp][lane][v] = A[v];
+                sm[par].b[warp][lane][v] = B[v];
+            }
+            csync<NW>();  // the chunk's one barrier
+            if (s_abort != 0) { stop = true; break; }
+            if (threadIdx.x == 0) inflight &= ~(1u << st);
+            refill(it);  // every warp has copied its tile out of stage st
+            fold_part();  // the previous chunk's partials
+            float s0[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) s0[v] = carry[par][lane][v];
+#pragma unroll 1
+            for (int w2 = 0; w2 < warp; ++w2)
+#pragma unroll
+                for (int v = 0; v < VEC; ++v)
+                    s0[v] = __fmaf_rn(sm[par].a[w2][lane][v], s0[v], sm[par].b[w2][lane][v]);
+            if (warp == NW - 1) {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) carry[par ^ 1][lane][v] = __fmaf_rn(A[v], s0[v], B[v]);
+            }
+            Op::finish(p, g, tc, regs, w, s0, xs, acc);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                part[par].a[warp][lane][v] = w.NA[v];
+                part[par].b[warp][lane][v] = w.NB[v];
+            }
+            pend_buf = par;
+        }
+        if (stop) break;
+        csync<NW>();  // the last chunk's partials are visible
+        fold_part();
+        {
+            const TileCoord tc = tile_coord_qj<Op>(g, seg_c * sg.seg, j_c);
+            if (warp == 0 && tc.cok && seg_c + 1 < sg.n_seg) {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v)
+                    st_pkt2(nx.agg + 2 * ((tc.c + v) * sg.n_seg + seg_c), pkt(NA[v], nx.epoch),
+                            pkt(NB[v], nx.epoch));
+            }
+        }
+        // next ticket (drawn one ahead)
+        if (threadIdx.x == 0) {
+            uint32_t t2 = limit;
+            if (drawing) {
+                t2 = pend;
+                if (t2 == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+                if (t2 >= limit) drawing = false;
+                else pend = atomicAdd(cr.ticket, 1u);
+            }
+            s_tk[0] = t2;
+        }
+        __syncthreads();  // also: no warp writes sm / part / carry of the next segment early
+        tk = tk_next;
+        tk_next = s_tk[0];
+    }
+    if (stop && threadIdx.x == 0) atomicOr(cr.err, ERRBIT_TIMEOUT);
+    Op::at_exit(p, xs, acc);
+    if (threadIdx.x == 0)  // after an early stop: boxes still in flight land first
+        for (int st = 0; st < ST; ++st)
+            if (inflight & (1u << st)) mbar_wait(&full[st], (phase >> st) & 1u, cr.err);
+}
+
 template <class Op>
 int chain_occupancy() {
     static int occ[64] = {0};
@@ -996,6 +1211,37 @@ cudaError_t launch_strip(const typename Op::Params& p, const Geom& g, const Carr
     return cudaGetLastError();
 }
 
+// Host: launch k_seg1<Op, 2> (consume only) on the segments sg.
+template <class Op>
+cudaError_t launch_seg1(const typename Op::Params& p, Geom g, const Carry& cr, const SegGeom& sg,
+                        const TmaDesc& td, cudaStream_t s) {
+    constexpr int ST = 2;
+    constexpr size_t dyn = (size_t)ST * tma_stage_bytes<Op>() + 128;
+    static_assert(ST <= 2, "the launch keeps SEG >= 2 >= ST");
+    static int occ[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int& o = occ[dev & 63];
+    if (o <= 0) {
+        cudaError_t e = cudaFuncSetAttribute(k_seg1<Op, ST>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k_seg1<Op, ST>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_seg1<Op, ST>, 32 * Op::NW, dyn) !=
+                cudaSuccess ||
+            n <= 0)
+            n = 1;
+        o = n;
+    }
+    const uint32_t grid = persist_grid(g, cr, o);
+    g.n_draws = sg.n_units + grid - g.ticket_base;
+    k_seg1<Op, ST><<<grid, 32 * Op::NW, dyn, s>>>(p, g, cr, sg, td);
+    return cudaGetLastError();
+}
+
 // Host: launch k_seg<Op, ST> (walker protocol, segmented, TMA staging).  The
 // segment length keeps the tiles between their two reads (SEG_LAG + 1
 // segments per CTA) within an L2 budget.
@@ -1046,6 +1292,10 @@ cudaError_t launch_seg(const typename Op::Params& p, Geom g, const Carry& cr, cu
     sg.seg = (uint32_t)seg;
     sg.n_seg = (uint32_t)((g.n_chunks + seg - 1) / seg);
     sg.n_units = sg.n_seg * (uint32_t)g.n_ct;
+    // The consume-only kernel takes the segments this geometry gives (the
+    // previous launch published its aggregates for them), its own grid.
+    if constexpr (has_next_agg<Op>::value)
+        if (Op::next_agg(p).pre) return launch_seg1<Op>(p, g, cr, sg, td, s);
     // walkers draw once; a segment CTA draws until one past the end
     g.n_draws = sg.n_units + grid - g.ticket_base;
     k_seg<Op, ST><<<grid, 32 * Op::NW, dyn, s>>>(p, g, cr, sg, td);
