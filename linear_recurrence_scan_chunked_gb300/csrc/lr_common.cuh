@@ -93,6 +93,15 @@ template <class Op>
 struct has_next_agg<Op, std::void_t<decltype(Op::NEXT_AGG)>>
     : std::integral_constant<bool, Op::NEXT_AGG> {};
 
+// Op::STRIP_ONE_BARRIER (optional, default false): the strip kernel runs the
+// operation with one barrier per tile (two stages, double-buffered warp
+// aggregates) -- for operations whose per-tile work, not HBM, bounds a CTA.
+template <class Op, class = void>
+struct strip_one_barrier : std::false_type {};
+template <class Op>
+struct strip_one_barrier<Op, std::void_t<decltype(Op::STRIP_ONE_BARRIER)>>
+    : std::integral_constant<bool, Op::STRIP_ONE_BARRIER> {};
+
 struct Geom {
     int64_t T;            // rows
     int64_t C;            // channels (B*D)

@@ -22,6 +22,13 @@
 #define LR_SEG_L2MB 160
 #endif
 
+// The fused forward cells (SRU, LSTM) run the strip kernel with one barrier
+// per tile (their backward kernels would not keep two CTAs per SM with the
+// second buffer of warp aggregates).
+#ifndef LR_STRIP_ONEB
+#define LR_STRIP_ONEB 1
+#endif
+
 // Register cap of the TMA-staged kernel: two CTAs of NW+1 = 9 warps per SM.
 #ifndef LR_TMA_MAXNREG
 #define LR_TMA_MAXNREG 112

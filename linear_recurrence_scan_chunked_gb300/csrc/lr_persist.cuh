@@ -413,7 +413,14 @@ __device__ __forceinline__ void strip_issue(const Geom& g, const TmaDesc& td, un
             tma_load_2d(dst + tma_off<Op>(a), &td.map[a], x, y0 + Op::tma_shift(a), &full[st]);
 }
 
-template <class Op, int ST>
+// ONEB: one barrier per tile.  The warp aggregates (and an op scratch that
+// overlays them) alternate between two buffers by use parity, so a warp may
+// start the next tile while another still folds this one; the stop decision
+// is read after the carry barrier, and the tile's stage is refilled right
+// after it (every warp has copied its tile out by then): two stages keep two
+// tiles in flight during the fold and the epilogue.  Otherwise a barrier at
+// the top of each tile frees the previous stage.
+template <class Op, int ST, bool ONEB>
 __global__ void __launch_bounds__(Op::NW * 32, 2)
     k_strip(typename Op::Params p, Geom g, uint32_t* err, uint32_t G,
             const __grid_constant__ TmaDesc td) {
@@ -423,7 +430,8 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
     extern __shared__ unsigned char dyn_smem[];
     unsigned char* ring = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~(uintptr_t)127);
-    __shared__ StripSmem<VEC, NW> sm;
+    __shared__ StripSmem<VEC, NW> smb[ONEB ? 2 : 1];
+    StripSmem<VEC, NW>& sm = smb[0];
     __shared__ OpScratch<Op> xs_own;
     typename Op::Smem& xs = scratch<Op>(sm, xs_own);
     __shared__ __align__(8) uint64_t full[ST];
@@ -452,13 +460,15 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
             s_abort = 1;
             atomicOr(err, ERRBIT_TIMEOUT);
         }
-        // every warp is done with the previous tile (its stage is free), and
-        // the stop decision below is the same in every warp
-        csync<NW>();
-        if (s_abort != 0) break;
-        if (threadIdx.x == 0 && it > 0 && issued < n_it) {
-            strip_issue<Op, ST>(g, td, ring, full, G, m, issued);  // into stage (it-1) % ST
-            ++issued;
+        if constexpr (!ONEB) {
+            // every warp is done with the previous tile (its stage is free), and
+            // the stop decision below is the same in every warp
+            csync<NW>();
+            if (s_abort != 0) break;
+            if (threadIdx.x == 0 && it > 0 && issued < n_it) {
+                strip_issue<Op, ST>(g, td, ring, full, G, m, issued);  // into stage (it-1) % ST
+                ++issued;
+            }
         }
         uint32_t q, j;
         strip_qj(G, m, it, q, j);
@@ -474,8 +484,41 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         const typename Op::S* ip = Op::init_ptr(p);
         if (tc.q == 0 && ip != nullptr && tc.cok) load_vec<typename Op::S, VEC>(ip + tc.c, init);
         float s[VEC];
-        strip_carry<VEC, NW>(sm, A, B, init, s, carry[it % m], (int)(q & 1u), tc.q == 0, tc.cok);
-        Op::finish(p, g, tc, regs, w, s, xs, acc);
+        if constexpr (ONEB) {
+            const int pb = (int)(it & 1u);
+            StripSmem<VEC, NW>& sb = smb[pb];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                sb.a[warp][lane][v] = A[v];
+                sb.b[warp][lane][v] = B[v];
+            }
+            csync<NW>();  // the tile's one barrier
+            if (s_abort != 0) break;
+            if (threadIdx.x == 0 && issued < n_it) {
+                strip_issue<Op, ST>(g, td, ring, full, G, m, issued);  // into stage st
+                ++issued;
+            }
+            float(*cs)[32][VEC] = carry[it % m];
+            const int par = (int)(q & 1u);
+            float stt[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v)
+                stt[v] = tc.q == 0 ? (tc.cok ? init[v] : 0.f) : cs[par][lane][v];
+#pragma unroll 1
+            for (int w2 = 0; w2 < warp; ++w2)
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) stt[v] = __fmaf_rn(sb.a[w2][lane][v], stt[v], sb.b[w2][lane][v]);
+            if (warp == NW - 1) {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) cs[par ^ 1][lane][v] = __fmaf_rn(A[v], stt[v], B[v]);
+            }
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) s[v] = stt[v];
+            Op::finish(p, g, tc, regs, w, s, scratch<Op>(sb, xs_own), acc);
+        } else {
+            strip_carry<VEC, NW>(sm, A, B, init, s, carry[it % m], (int)(q & 1u), tc.q == 0, tc.cok);
+            Op::finish(p, g, tc, regs, w, s, xs, acc);
+        }
     }
     Op::at_exit(p, xs, acc);
     if (threadIdx.x == 0)  // after an early stop: copies still in flight land first
@@ -1163,7 +1206,7 @@ cudaError_t launch_tchain(const typename Op::Params& p, Geom g, const Carry& cr,
 // Host: launch k_strip<Op, ST> when the problem has enough channel strips to
 // give every resident CTA the same number of them (at most STRIP_MAX);
 // returns cudaErrorNotSupported otherwise (the caller takes the chain kernel).
-template <class Op, int ST>
+template <class Op, int ST, bool ONEB>
 cudaError_t launch_strip(const typename Op::Params& p, const Geom& g, const Carry& cr,
                          cudaStream_t s) {
     constexpr int L = Op::NW * Op::R, CW = 32 * Op::VEC;
@@ -1174,15 +1217,16 @@ cudaError_t launch_strip(const typename Op::Params& p, const Geom& g, const Carr
     cudaGetDevice(&dev);
     int& o = occ[dev & 63];
     if (o <= 0) {
-        cudaError_t e = cudaFuncSetAttribute(k_strip<Op, ST>,
+        cudaError_t e = cudaFuncSetAttribute(k_strip<Op, ST, ONEB>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)(ring + STRIP_MAX * strip_bytes));
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k_strip<Op, ST>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        e = cudaFuncSetAttribute(k_strip<Op, ST, ONEB>,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         int n = 0;  // residency for up to two strips per CTA
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_strip<Op, ST>, 32 * Op::NW,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_strip<Op, ST, ONEB>, 32 * Op::NW,
                                                           ring + 2 * strip_bytes) != cudaSuccess ||
             n <= 0)
             n = 1;
@@ -1207,7 +1251,8 @@ cudaError_t launch_strip(const typename Op::Params& p, const Geom& g, const Carr
         td.tx_bytes += tma_arr_bytes<Op>(a);
     }
     // no CTA waits for another, so the grid need not be co-resident
-    k_strip<Op, ST><<<G, 32 * Op::NW, ring + (size_t)m * strip_bytes, s>>>(p, g, cr.err, G, td);
+    k_strip<Op, ST, ONEB><<<G, 32 * Op::NW, ring + (size_t)m * strip_bytes, s>>>(p, g, cr.err, G,
+                                                                                 td);
     return cudaGetLastError();
 }
 
@@ -1313,7 +1358,9 @@ cudaError_t launch_persist(const typename OpC::Params& p, const Geom& g, const C
                   "all instantiations take the same arguments");
     if (cr.mode == CARRY_CHAIN) {
         if (cr.tma) {
-            const cudaError_t e = launch_strip<OpT, ST>(p, g, cr, s);
+            cudaError_t e;
+            if constexpr (strip_one_barrier<OpT>::value) e = launch_strip<OpT, 2, true>(p, g, cr, s);
+            else e = launch_strip<OpT, ST, false>(p, g, cr, s);
             if (e != cudaErrorNotSupported) return e;
             return launch_tchain<OpT, ST>(p, g, cr, s);
         }

@@ -42,6 +42,7 @@ struct LstmFwdParams {
 template <typename S_, int VEC_, int NW_, int R_>
 struct LstmFwdOp {
     using S = S_;
+    static constexpr bool STRIP_ONE_BARRIER = LR_STRIP_ONEB != 0;
     static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
     static constexpr bool REV = false;
     static constexpr int IN_ARRAYS = 4;  // zf, zi, zc, zo

@@ -37,6 +37,7 @@ struct SruFwdParams {
 template <typename S_, int VEC_, int NW_, int R_>
 struct SruFwdOp {
     using S = S_;
+    static constexpr bool STRIP_ONE_BARRIER = LR_STRIP_ONEB != 0;
     static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
     static constexpr bool REV = false;
     static constexpr int IN_ARRAYS = 4;  // xt, uf, ur, x
