@@ -50,7 +50,7 @@ EPS, KMAX = 1e-5, 20
 # written per launch, averaged over the K = 6 launches of a solve (first
 # iteration + 5 x second iteration, both captured at full size,
 # profiles/dram_traffic.md).
-NCU_TRAFFIC = {"deer.solve": {"bytes": 1174852011, "src": "cc0c561d98f6cd4c",
+NCU_TRAFFIC = {"deer.solve": {"bytes": 753902805, "src": "25108ce5e842ac8a",
                               "file": "deer_kernels.cu"}}
 
 
@@ -531,6 +531,57 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+# Small programs of the bench's kernels for ncu captures: one short launch per
+# kernel of interest, inputs still larger than the 129 MB L2, the public
+# binding on the seeded inputs of `workloads`.  Launch order per case:
+#   deer   DEER fp32 4x65536x256 (full size), three Newton iterations (eps = 0):
+#          k_seg (iteration 1, reduce + consume), then k_seg1 twice (consume only)
+#   large  scan_large bf16 16x2048x4096 (T reduced from 8192): fwd, bwd
+#   long   scan_long fp32 1x262144x128 (T reduced from 2^20): fwd
+#   sru    SRU fp32 32x512x1024 (T reduced from 2048): fwd, bwd, 2 bias kernels
+#   lstm   LSTM cell fp32 32x512x1024 (T reduced from 2048): fwd, bwd, 2 bias kernels
+PROFILE_CASES = ("deer", "large", "long", "sru", "lstm")
+
+
+def profile_case(name):
+    import dataclasses
+    import torch
+    import linear_recurrence_scan_chunked_gb300 as L
+    L.load()
+
+    def dev(inp, k):
+        v = inp[k]
+        if v.dtype == np.uint16:
+            return torch.from_numpy(v.view(np.int16)).cuda().view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).cuda()
+
+    if name == "deer":
+        inp = W.make_inputs(W.DEER, 0)
+        L.deer_diag_solve(dev(inp, "w"), dev(inp, "u"), None, None, eps=0.0, kmax=3)
+    elif name == "large":
+        inp = W.make_inputs(dataclasses.replace(W.SCAN_BF16, T=2048), 0)
+        a, b, g = dev(inp, "a"), dev(inp, "b"), dev(inp, "g")
+        L.lr_scan_bwd(a, L.lr_scan_fwd(a, b, None), g, None)
+    elif name == "long":
+        inp = W.make_inputs(dataclasses.replace(W.SCAN_LONG, T=1 << 18), 0)
+        L.lr_scan_fwd(dev(inp, "a"), dev(inp, "b"), dev(inp, "h0"))
+    elif name == "sru":
+        inp = W.make_inputs(dataclasses.replace(W.SRU, T=512), 0)
+        d = {k: dev(inp, k) for k in inp}
+        h, c = L.sru_fwd(d["xt"], d["uf"], d["ur"], d["x"], d["bf"], d["br"], d["c0"])
+        L.sru_bwd(d["xt"], d["uf"], d["ur"], d["x"], d["bf"], d["br"], c, d["dh"], d["c0"])
+    elif name == "lstm":
+        inp = W.make_inputs(dataclasses.replace(W.LSTM, T=512), 0)
+        d = {k: dev(inp, k) for k in inp}
+        z = [d[k] for k in ("zf", "zi", "zc", "zo", "bf", "bi", "bc", "bo")]
+        h, c = L.lstm_cell_fwd(*z, d["c0"])
+        L.lstm_cell_bwd(*z, c, d["dh"], d["c0"])
+    torch.cuda.synchronize()
+    if L.last_error() != L.LR_OK:
+        raise RuntimeError("device error in the profiling case")
+    print(f"profile case {name}: ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -544,7 +595,12 @@ def main():
     ap.add_argument("--only", action="append", default=[],
                     help="run only these operations (e.g. scan_large.bwd); for profiling cases")
     ap.add_argument("--T", type=int, default=0, help="override T of the selected rows (profiling cases)")
+    ap.add_argument("--profile-case", choices=PROFILE_CASES,
+                    help="run one small program of the bench's kernels (for ncu) and exit")
     args = ap.parse_args()
+    if args.profile_case:
+        profile_case(args.profile_case)
+        return
     select_rows(args.only, args.T)
     ws, rank, local = dist_init(args)
     if args.impl == "reference":
