@@ -10,7 +10,9 @@ Every function here follows the pages cited in ``lr_oracle.c``:
   scan_fwd / scan_bwd  -- the diagonal linear recurrence and its BPTT gradient
   sru_fwd / sru_bwd    -- the linear-form SRU layer and its gradient
   lstm_fwd / lstm_bwd  -- the LSTM cell-state scan with its gates, and its gradient
-  deer / deer_step     -- DEER Newton iteration on a diagonal tanh RNN
+  deer / deer_step     -- DEER Newton iteration on a diagonal tanh RNN (from a
+                          given initial guess or zeros)
+  deer_per_sequence    -- the same with each batch sequence stopping on its own
   rollout_tanh         -- the direct sequential tanh RNN
 Each is pinned by tests in ``tests/test_oracle_pins.py`` against closed forms,
 library linear solves, finite differences and brute-force evaluation orders.
@@ -62,7 +64,7 @@ def _load():
         lib.lro_lstm_bwd.restype = ctypes.c_int
         lib.lro_rollout_tanh.argtypes = [I64, I64, I64, P, P, P, P]
         lib.lro_deer_step.argtypes = [I64, I64, I64, P, P, P, P, P, P]
-        lib.lro_deer.argtypes = [I64, I64, I64, P, P, P, ctypes.c_double, ctypes.c_int, P, P, P]
+        lib.lro_deer.argtypes = [I64, I64, I64, P, P, P, P, ctypes.c_double, ctypes.c_int, P, P, P]
         lib.lro_deer_bwd.argtypes = [I64, I64, I64] + [P] * 7
         lib.lro_deer.restype = ctypes.c_int
         lib.lro_num_threads.restype = ctypes.c_int
@@ -202,18 +204,37 @@ def deer_bwd(w, y, g, h0=None):
 DEER_CONVERGED, DEER_NOT_CONVERGED, DEER_NONFINITE = 0, 1, 2
 
 
-def deer(w, u, h0=None, eps=1e-5, kmax=20):
-    """Returns (y, iters, rho_history, status) -- status 0 converged, 1 hit kmax."""
-    w, u, h0 = _f64(w), _f64(u), _f64(h0)
+def deer(w, u, h0=None, eps=1e-5, kmax=20, y_init=None):
+    """Returns (y, iters, rho_history, status) -- status 0 converged, 1 hit kmax,
+    2 not finite.  y_init: the initial guess (None = zeros)."""
+    w, u, h0, y_init = _f64(w), _f64(u), _f64(h0), _f64(y_init)
     T, C = _tc(u)
     y = np.empty_like(u)
     hist = np.zeros(kmax, dtype=np.float64)
     iters = ctypes.c_int(0)
-    st = _load().lro_deer(T, C, w.shape[0], _p(w), _p(u), _p(h0), float(eps), int(kmax),
-                          _p(y), _p(hist), ctypes.byref(iters))
+    st = _load().lro_deer(T, C, w.shape[0], _p(w), _p(u), _p(h0), _p(y_init), float(eps),
+                          int(kmax), _p(y), _p(hist), ctypes.byref(iters))
     if st < 0:
         raise MemoryError("oracle deer: allocation failed")
     return y, int(iters.value), hist[: iters.value].copy(), int(st)
+
+
+def deer_per_sequence(w, u, h0=None, eps=1e-5, kmax=20, y_init=None):
+    """Per-sequence stopping: every batch sequence u[:, b] is its own DEER
+    problem with its own stopping test.  Returns (y, iters[B], status[B],
+    rho_histories[B])."""
+    u = _f64(u)
+    T, B, D = u.shape
+    y = np.empty_like(u)
+    iters, status, hists = [], [], []
+    for b in range(B):
+        yb, kb, hb, sb = deer(w, u[:, b:b + 1], None if h0 is None else _f64(h0)[b:b + 1], eps, kmax,
+                              None if y_init is None else _f64(y_init)[:, b:b + 1])
+        y[:, b:b + 1] = yb
+        iters.append(kb)
+        status.append(sb)
+        hists.append(hb)
+    return y, iters, status, hists
 
 
 def rel_err(got, ref) -> float:

@@ -372,23 +372,27 @@ void lro_deer_step(int64_t T, int64_t C, int64_t D, const double* w,
 }
 
 /*
- * DEER fixed-point iteration from the all-zero guess ([P4] "工程实现": stop
- * when ||y^(i+1) - y^(i)|| < eps, here the max-abs norm over all entries, or
- * after kmax iterations).  K counts the scans performed, including the one
- * whose residual fell below eps.  rho_hist[k-1] = residual of iteration k.
- * Returns 0 when converged, 1 when kmax was reached without convergence,
- * 2 when a residual was not finite, -1 on allocation failure.
+ * DEER fixed-point iteration ([P4] "工程实现": stop when
+ * ||y^(i+1) - y^(i)|| < eps, here the max-abs norm over all entries, or after
+ * kmax iterations) from the initial guess y_init, NULL meaning the all-zero
+ * guess ([P4] "核心原理": a guess close to the solution -- in training, the
+ * previous step's -- keeps the iteration count small; the residual of
+ * iteration 1 is measured against the guess).  K counts the scans performed,
+ * including the one whose residual fell below eps.  rho_hist[k-1] = residual
+ * of iteration k.  Returns 0 when converged, 1 when kmax was reached without
+ * convergence, 2 when a residual was not finite, -1 on allocation failure.
  */
 int lro_deer(int64_t T, int64_t C, int64_t D, const double* w, const double* u,
-             const double* h0, double eps, int kmax, double* y,
-             double* rho_hist, int* iters) {
+             const double* h0, const double* y_init, double eps, int kmax,
+             double* y, double* rho_hist, int* iters) {
     size_t n = (size_t)(T * C);
-    double* prev = (double*)malloc(sizeof(double) * n);
+    double* prev = (double*)malloc(sizeof(double) * (n ? n : 1));
     if (!prev) return -1;
     int status = 1, k;
     for (k = 1; k <= kmax; ++k) {
         double rho = 0.0;
-        lro_deer_step(T, C, D, w, u, h0, k == 1 ? NULL : prev, y, &rho);
+        /* iteration 1 starts from the initial guess: y_init, or zeros */
+        lro_deer_step(T, C, D, w, u, h0, k == 1 ? y_init : prev, y, &rho);
         rho_hist[k - 1] = rho;
         if (!isfinite(rho)) { status = 2; break; }
         if (rho < eps) { status = 0; break; }

@@ -433,6 +433,58 @@ def test_deer_w_zero_takes_two_iterations():
     np.testing.assert_allclose(y, np.tanh(u), rtol=0, atol=1e-15)
 
 
+def test_deer_warm_start_from_the_solution_takes_one_iteration():
+    # Newton's method started at the root returns it: one scan, residual ~0
+    T, B, D = 400, 2, 5
+    r = np.random.default_rng(31)
+    w, u, h0 = r.uniform(-0.9, 0.9, D), r.standard_normal((T, B, D)), r.standard_normal((B, D))
+    ystar = oracle.rollout_tanh(w, u, h0)
+    y, k, hist, st = oracle.deer(w, u, h0, eps=1e-10, kmax=20, y_init=ystar)
+    assert (k, st) == (1, oracle.DEER_CONVERGED)
+    assert hist[0] < 1e-13
+    np.testing.assert_allclose(y, ystar, rtol=0, atol=1e-13)
+
+
+def test_deer_warm_start_first_iteration_is_newton_from_the_guess():
+    T, B, D = 200, 2, 4
+    r = np.random.default_rng(32)
+    w, u = r.uniform(-0.9, 0.9, D), r.standard_normal((T, B, D))
+    guess = r.standard_normal((T, B, D))
+    y, k, hist, st = oracle.deer(w, u, eps=0.0, kmax=1, y_init=guess)
+    ystep, rho = oracle.deer_step(w, u, guess)
+    np.testing.assert_array_equal(y, ystep)
+    assert hist[0] == rho == np.max(np.abs(ystep - guess))
+
+
+def test_deer_warm_start_zero_is_the_cold_start():
+    r = np.random.default_rng(33)
+    w, u = r.uniform(-0.9, 0.9, 3), r.standard_normal((300, 2, 3))
+    a = oracle.deer(w, u, eps=1e-8, kmax=30)
+    b = oracle.deer(w, u, eps=1e-8, kmax=30, y_init=np.zeros_like(u))
+    np.testing.assert_array_equal(a[0], b[0])
+    assert a[1] == b[1] and a[3] == b[3]
+    np.testing.assert_array_equal(a[2], b[2])
+
+
+def test_deer_per_sequence_stopping():
+    # a quiet sequence (small u: nearly linear, converges fast), a loud one,
+    # and a copy of the loud one
+    T, D = 2000, 6
+    r = np.random.default_rng(34)
+    w = r.uniform(-0.9, 0.9, D)
+    loud = r.standard_normal((T, D)) * 2.0
+    u = np.stack([1e-3 * r.standard_normal((T, D)), loud, loud], axis=1)
+    y, ks, sts, hists = oracle.deer_per_sequence(w, u, eps=1e-9, kmax=40)
+    assert sts == [oracle.DEER_CONVERGED] * 3
+    assert ks[0] < ks[1] == ks[2]
+    # each sequence reached its own rollout; the global stopping test takes as
+    # many iterations as the slowest sequence
+    np.testing.assert_allclose(y, oracle.rollout_tanh(w, u), rtol=0, atol=1e-8)
+    yg, kg, hg, stg = oracle.deer(w, u, eps=1e-9, kmax=40)
+    assert kg == max(ks)
+    np.testing.assert_array_equal(y[:, 1:], yg[:, 1:])
+
+
 def test_deer_stopping_rule_edges():
     w = rng.uniform(-0.9, 0.9, 3)
     u = rng.standard_normal((64, 1, 3))
