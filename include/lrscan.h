@@ -165,6 +165,37 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y,
                     int dtype, void* stream);
 
 /*
+ * DEER solve with an initial guess and a choice of stopping test (the next
+ * row on the same scan).  [P4] "核心原理": the Newton iteration needs few steps
+ * when the initial guess is close to the solution (in training, the previous
+ * step's); [P4] "工程实现": stop at ||y^(i+1) - y^(i)|| < eps or K_max.
+ *   y_init       : [T,B,D] in, the initial guess y^(0) (NULL = zeros); iteration 1
+ *                  builds J and rhs from it and its residual is max|y^(1) - y^(0)|.
+ *                  It may be y itself (the guess is copied first); no other
+ *                  overlap with y is allowed.
+ *   per_sequence : 0 = one stopping test over the whole batch (deer_diag_solve);
+ *                  1 = each batch sequence b stops at its own first K_b with
+ *                  max over (t, d) |y^(K_b) - y^(K_b - 1)| < eps (or a non-finite
+ *                  residual, or kmax); y[:, b] is its iterate K_b.  Iterations
+ *                  continue until every sequence stopped; a stopped sequence is
+ *                  no longer written.
+ *   iters_out    : host int out, the largest K_b (per_sequence) or K
+ *   resid_out    : host float out (may be NULL): the largest final residual
+ *   resid_hist   : host float[kmax] out (may be NULL): residual of every
+ *                  iteration (per_sequence: the largest over the sequences that
+ *                  ran it)
+ *   seq_iters    : host int[B] out (may be NULL): K_b (K for every b when
+ *                  per_sequence = 0)
+ *   seq_resid    : host float[B] out (may be NULL): each sequence's residual at K_b
+ * Status as deer_diag_solve: LR_ERR_NONFINITE if any sequence's residual was not
+ * finite, else LR_ERR_NOT_CONVERGED if any sequence reached kmax without eps.
+ */
+int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void* y_init,
+                       void* y, int64_t B, int64_t T, int64_t D, float eps, int kmax,
+                       int per_sequence, int* iters_out, float* resid_out, float* resid_hist,
+                       int* seq_iters, float* seq_resid, int dtype, void* stream);
+
+/*
  * Gradient through the DEER solution (the next row on the same scan):
  * [P4] "核心原理": at the fixed point y is the rollout of
  * h_t = tanh(w (.) h_{t-1} + u_t), so the gradient of a loss L with upstream

@@ -56,6 +56,8 @@ def load():
     lib.lstm_cell_fwd.argtypes = [P] * 11 + [I64, I64, I64, I, P]
     lib.lstm_cell_bwd.argtypes = [P] * 20 + [I64, I64, I64, I, P]
     lib.deer_diag_solve.argtypes = [P, P, P, P, I64, I64, I64, ctypes.c_float, I, P, P, P, I, P]
+    lib.deer_diag_solve_ex.argtypes = [P, P, P, P, P, I64, I64, I64, ctypes.c_float, I, I, P, P,
+                                       P, P, P, I, P]
     lib.deer_diag_bwd.argtypes = [P] * 7 + [I64, I64, I64, I, P]
     lib.lr_last_error.argtypes = []
     lib.lr_status_str.argtypes = [I]
@@ -262,6 +264,35 @@ def deer_diag_solve(w, u, h0=None, y=None, eps=1e-5, kmax=20, stream=None):
         _check(st)
     k = iters.value
     return y, k, resid.value, [hist[i] for i in range(k)], st
+
+
+def deer_diag_solve_ex(w, u, h0=None, y=None, y_init=None, eps=1e-5, kmax=20,
+                       per_sequence=False, stream=None):
+    """DEER solve from an initial guess (None = zeros; it may be y itself) with
+    one stopping test for the batch or one per sequence.  Returns a dict: y,
+    iters (largest K), resid, hist (per iteration), status, seq_iters[B],
+    seq_resid[B]."""
+    _seq("u", u)
+    T, B, D = u.shape
+    _param("w", w, D)
+    _state("h0", h0, u)
+    if y_init is not None:
+        _seq("y_init", y_init, u)
+    y = torch.empty_like(u) if y is None else _seq("y", y, u)
+    it = ctypes.c_int(0)
+    rho = ctypes.c_float(0.0)
+    hist = (ctypes.c_float * int(kmax))()
+    sk = (ctypes.c_int * max(1, B))()
+    sr = (ctypes.c_float * max(1, B))()
+    st = load().deer_diag_solve_ex(_p(w), _p(u), _p(h0), _p(y_init), _p(y), B, T, D,
+                                   ctypes.c_float(eps), int(kmax), 1 if per_sequence else 0,
+                                   ctypes.byref(it), ctypes.byref(rho), hist, sk, sr, _code(u),
+                                   _stream(stream))
+    if st not in (LR_OK, LR_ERR_NOT_CONVERGED, LR_ERR_NONFINITE):
+        _check(st)
+    k = int(it.value)
+    return {"y": y, "iters": k, "resid": float(rho.value), "hist": list(hist)[:k], "status": int(st),
+            "seq_iters": list(sk)[:B], "seq_resid": list(sr)[:B]}
 
 
 def deer_diag_bwd(w, y, dy, h0=None, du=None, dw=None, dh0=None, want_dh0=True, stream=None):

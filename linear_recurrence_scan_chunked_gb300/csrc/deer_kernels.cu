@@ -37,6 +37,10 @@ struct DeerParams {
     const uint32_t* prev_resid;  // residual of the previous iteration (nullptr: first)
     float eps;
     NextAgg nx;  // next iteration's aggregates (segmented walker kernel only)
+    // Per-sequence stopping (nullptr: one stopping test for the whole batch).
+    uint32_t* seq_resid;        // [B] this iteration's residual bits, per sequence
+    const uint32_t* seq_done;   // [B] nonzero: the sequence stopped (its y is not written)
+    const uint32_t* all_done;   // nonzero: every sequence stopped (the launch does nothing)
 };
 
 template <typename S_, int VEC_, int NW_, int R_>
@@ -68,6 +72,7 @@ struct DeerOp {
     // already stopped the solve (residual below eps, or not finite) does
     // nothing but pass that residual on, so that its own successor stops too.
     __device__ static bool skip(const Params& p) {
+        if (p.all_done != nullptr) return *(volatile const uint32_t*)p.all_done != 0;
         if (p.prev_resid == nullptr) return false;
         const uint32_t bits = *(volatile const uint32_t*)p.prev_resid;
         const float rho = __uint_as_float(bits);
@@ -132,6 +137,16 @@ struct DeerOp {
     __device__ static void finish(const Params& p, const Geom& g, const TileCoord& tc,
                                   const Regs& rg, Work& w, float (&s)[VEC], Smem&, Acc& acc) {
         const bool nxt = p.nx.agg != nullptr;
+        // per-sequence stopping: the lane's channels belong to one sequence
+        // (VEC divides D); a stopped sequence keeps its iterate
+        const bool per_seq = p.seq_done != nullptr;
+        uint32_t seq = 0;
+        bool live = true;
+        if (per_seq && tc.cok) {
+            seq = (uint32_t)(tc.c / g.D);
+            live = p.seq_done[seq] == 0;
+        }
+        uint32_t mx = 0;  // this tile's residual bits (per-sequence stopping)
         float wv[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { wv[v] = 0.f; w.NA[v] = 1.f; w.NB[v] = 0.f; }
@@ -153,7 +168,7 @@ struct DeerOp {
             }
 #pragma unroll
             for (int v = 0; v < VEC; ++v) s[v] = w.J[r][v] * s[v] + w.Rh[r][v];
-            if (tc.cok && t < g.T) {
+            if (tc.cok && t < g.T && live) {
                 store_vec<S, VEC>(p.ynew + t * g.C + tc.c, s);
 #pragma unroll
                 for (int v = 0; v < VEC; ++v) {
@@ -161,8 +176,24 @@ struct DeerOp {
                     float yv = s[v];
                     if constexpr (sizeof(S) == 2) yv = bf_lo(bf_bits(yv));
                     const uint32_t bits = __float_as_uint(fabsf(yv - rg.yo[r + 1].get(v)));
-                    acc.mx = bits > acc.mx ? bits : acc.mx;
+                    mx = bits > mx ? bits : mx;
                 }
+            }
+        }
+        acc.mx = mx > acc.mx ? mx : acc.mx;
+        if (per_seq) {
+            // one atomic per warp when its lanes share a sequence, else per lane
+            const uint32_t key = tc.cok && live ? seq : 0xffffffffu;
+            const uint32_t k0 = __shfl_sync(0xffffffffu, key, 0);
+            if (__all_sync(0xffffffffu, key == k0)) {
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const uint32_t o = __shfl_xor_sync(0xffffffffu, mx, off);
+                    mx = o > mx ? o : mx;
+                }
+                if ((threadIdx.x & 31) == 0 && k0 != 0xffffffffu && mx) atomicMax(p.seq_resid + k0, mx);
+            } else if (key != 0xffffffffu && mx) {
+                atomicMax(p.seq_resid + key, mx);
             }
         }
     }
@@ -332,25 +363,86 @@ using DeerOpT = DeerOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_DEER, sizeof(S) == 2
 template <typename S, bool VP>
 static cudaError_t deer_t(const float* w, const void* u, const void* h0, const void* yold,
                           void* ynew, uint32_t* resid, const uint32_t* prev_resid, float eps,
-                          const NextAgg& nx, const Geom& g, const Carry& cr, cudaStream_t s) {
+                          const NextAgg& nx, const DeerSeq& sq, const Geom& g, const Carry& cr,
+                          cudaStream_t s) {
     return launch_persist<DeerOpT<S, VP, CARRY_CHAIN>, DeerOpT<S, VP, CARRY_WALK>,
                           DeerOpT<S, VP, TILE_TMA>, kcfg(OP_DEER, sizeof(S) == 2, TILE_TMA).ST>(
-        {w, (const S*)u, (const S*)h0, (const S*)yold, (S*)ynew, resid, prev_resid, eps, nx}, g,
-        cr, s);
+        {w, (const S*)u, (const S*)h0, (const S*)yold, (S*)ynew, resid, prev_resid, eps, nx,
+         sq.resid, sq.done, sq.all_done},
+        g, cr, s);
 }
 
 cudaError_t launch_deer_iter(int dtype, bool vec, const float* w, const void* u, const void* h0,
                              const void* yold, void* ynew, uint32_t* resid,
                              const uint32_t* prev_resid, float eps, const NextAgg& nx,
-                             const Geom& g, const Carry& cr, cudaStream_t s) {
+                             const DeerSeq& sq, const Geom& g, const Carry& cr, cudaStream_t s) {
     if (dtype == 0)
-        return vec ? deer_t<float, true>(w, u, h0, yold, ynew, resid, prev_resid, eps, nx, g, cr, s)
-                   : deer_t<float, false>(w, u, h0, yold, ynew, resid, prev_resid, eps, nx, g, cr,
-                                          s);
-    return vec ? deer_t<__nv_bfloat16, true>(w, u, h0, yold, ynew, resid, prev_resid, eps, nx, g,
-                                             cr, s)
-               : deer_t<__nv_bfloat16, false>(w, u, h0, yold, ynew, resid, prev_resid, eps, nx, g,
-                                              cr, s);
+        return vec ? deer_t<float, true>(w, u, h0, yold, ynew, resid, prev_resid, eps, nx, sq, g,
+                                         cr, s)
+                   : deer_t<float, false>(w, u, h0, yold, ynew, resid, prev_resid, eps, nx, sq, g,
+                                          cr, s);
+    return vec ? deer_t<__nv_bfloat16, true>(w, u, h0, yold, ynew, resid, prev_resid, eps, nx, sq,
+                                             g, cr, s)
+               : deer_t<__nv_bfloat16, false>(w, u, h0, yold, ynew, resid, prev_resid, eps, nx,
+                                              sq, g, cr, s);
+}
+
+// Per-sequence stopping, after iteration k: a running sequence whose residual
+// of iteration k is below eps (or not finite) stops at K = k; all_done is set
+// when no sequence runs.  One block.
+__global__ void __launch_bounds__(1024)
+    k_deer_seq_update(const uint32_t* __restrict__ resid, uint32_t* done, int32_t* iters,
+                      uint32_t* all_done, int64_t B, float eps, int k) {
+    __shared__ int any_live;
+    if (threadIdx.x == 0) any_live = 0;
+    __syncthreads();
+    int live = 0;
+    for (int64_t b = threadIdx.x; b < B; b += blockDim.x) {
+        if (done[b]) continue;
+        const float rho = __uint_as_float(resid[b]);
+        if (rho < eps || !(rho <= 3.4e38f)) {
+            done[b] = 1u;
+            iters[b] = k;
+        } else {
+            live = 1;
+        }
+    }
+    if (live) atomicOr(&any_live, 1);
+    __syncthreads();
+    if (threadIdx.x == 0) *all_done = any_live ? 0u : 1u;
+}
+
+// Per-sequence solve, at the end: sequence b's last iterate (K_b, or
+// `launched` when it never stopped) is in the second buffer when K_b is even;
+// copy those channels into y.  Threads own channels, blocks stride over rows.
+template <typename S>
+__global__ void __launch_bounds__(256)
+    k_deer_seq_gather(const S* __restrict__ ybuf, S* __restrict__ y, const int32_t* __restrict__ iters,
+                      int launched, int64_t T, int64_t C, int64_t D) {
+    const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= C) return;
+    const int kb = iters[c / D] > 0 ? iters[c / D] : launched;
+    if (kb & 1) return;
+    for (int64_t t = blockIdx.y; t < T; t += gridDim.y) y[t * C + c] = ybuf[t * C + c];
+}
+
+cudaError_t launch_deer_seq_gather(const void* ybuf, void* y, const int32_t* iters, int launched,
+                                   int64_t T, int64_t C, int64_t D, int dtype, cudaStream_t s) {
+    const dim3 grid((unsigned)((C + 255) / 256), (unsigned)(T < 1024 ? T : 1024));
+    if (dtype == 0)
+        k_deer_seq_gather<float><<<grid, 256, 0, s>>>((const float*)ybuf, (float*)y, iters, launched,
+                                                      T, C, D);
+    else
+        k_deer_seq_gather<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            (const __nv_bfloat16*)ybuf, (__nv_bfloat16*)y, iters, launched, T, C, D);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_deer_seq_update(const uint32_t* resid, uint32_t* done, int32_t* iters,
+                                   uint32_t* all_done, int64_t B, float eps, int k,
+                                   cudaStream_t s) {
+    k_deer_seq_update<<<1, 1024, 0, s>>>(resid, done, iters, all_done, B, eps, k);
+    return cudaGetLastError();
 }
 
 template <typename S, bool VP, int M>

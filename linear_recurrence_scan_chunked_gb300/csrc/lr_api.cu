@@ -87,6 +87,8 @@ struct DevWS {
     void* ybuf = nullptr;        size_t ybuf_cap = 0;     // bytes
     uint32_t* host_word = nullptr;                        // pinned [kMaxIters], residual reads
     void* test_buf = nullptr;                             // timeout-test problem
+    uint32_t* seq = nullptr;     size_t seq_cap = 0;      // DEER per-sequence state (words)
+    uint32_t* seq_host = nullptr; size_t seq_host_cap = 0;  // pinned mirror of its residuals
     uint32_t epoch = 0;
     cudaEvent_t done = nullptr;
     cudaStream_t last_stream = nullptr;
@@ -383,29 +385,72 @@ int lstm_cell_bwd(const void* zf, const void* zi, const void* zc, const void* zo
     return leave(*ws, s);
 }
 
-int deer_diag_solve(const float* w, const void* u, const void* h0, void* y, int64_t B, int64_t T,
-                    int64_t D, float eps, int kmax, int* iters_out, float* resid_out,
-                    float* resid_hist, int dtype, void* stream) {
+static int grow_host(DevWS& ws, size_t need) {
+    if (need <= ws.seq_host_cap) return LR_OK;
+    const size_t n = need + need / 4;
+    if (ws.seq_host) CK(cudaFreeHost(ws.seq_host));
+    ws.seq_host = nullptr;
+    ws.seq_host_cap = 0;
+    CK(cudaHostAlloc(&ws.seq_host, n * sizeof(uint32_t), cudaHostAllocDefault));
+    ws.seq_host_cap = n;
+    return LR_OK;
+}
+
+static bool ranges_overlap(const void* a, const void* b, size_t n) {
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + n && y < x + n;
+}
+
+static float bits_f(uint32_t b) {
+    float f;
+    memcpy(&f, &b, sizeof f);
+    return f;
+}
+
+int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void* y_init, void* y,
+                       int64_t B, int64_t T, int64_t D, float eps, int kmax, int per_sequence,
+                       int* iters_out, float* resid_out, float* resid_hist, int* seq_iters,
+                       float* seq_resid, int dtype, void* stream) {
     TRY(check_sizes(B, T, D, dtype));
     if (!iters_out || kmax < 1 || kmax > kMaxIters || !(eps >= 0.f)) return LR_ERR_INVALID_ARG;
+    if (per_sequence != 0 && per_sequence != 1) return LR_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     if (B * T * D == 0) {
         *iters_out = 0;
         if (resid_out) *resid_out = 0.f;
+        for (int64_t b = 0; b < B; ++b) {
+            if (seq_iters) seq_iters[b] = 0;
+            if (seq_resid) seq_resid[b] = 0.f;
+        }
         return LR_OK;
     }
     bool vec;
-    TRY(check_ptrs({u, y}, {h0}, {w}, dtype, D, &vec));
+    TRY(check_ptrs({u, y}, {h0, y_init}, {w}, dtype, D, &vec));
+    const size_t nbytes = (size_t)(B * T * D) * esize(dtype);
+    if (y_init && y_init != y && ranges_overlap(y_init, y, nbytes)) return LR_ERR_INVALID_ARG;
     GUARD;
     DevWS* ws;
     TRY(get_ws(&ws));
-    const size_t nbytes = (size_t)(B * T * D) * esize(dtype);
     {
         size_t cap = ws->ybuf_cap;
         char* p = (char*)ws->ybuf;
         TRY(grow(*ws, &p, &cap, nbytes, false));
         ws->ybuf = p;
         ws->ybuf_cap = cap;
+    }
+    // per-sequence state: [kmax][B] residual slots, [B] stop flags, [B]
+    // iteration counts, the all-done word
+    uint32_t *sq_slots = nullptr, *sq_done = nullptr, *sq_all = nullptr;
+    int32_t* sq_iters = nullptr;
+    const size_t sq_words = (size_t)kmax * (size_t)B + 2 * (size_t)B + 1;
+    if (per_sequence) {
+        TRY(grow(*ws, &ws->seq, &ws->seq_cap, sq_words, false));
+        // pinned mirror: the residual slots, the all-done word, the counts
+        TRY(grow_host(*ws, (size_t)kmax * (size_t)B + 1 + (size_t)B));
+        sq_slots = ws->seq;
+        sq_done = sq_slots + (size_t)kmax * B;
+        sq_iters = reinterpret_cast<int32_t*>(sq_done + B);
+        sq_all = reinterpret_cast<uint32_t*>(sq_iters + B);
     }
     TRY(enter(*ws, s));
     // On the segmented walker kernel each iteration also publishes the next
@@ -421,13 +466,21 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y, int6
             ws->epoch = 0;
         }
     }
+    if (per_sequence) CK(cudaMemsetAsync(ws->seq, 0, sq_words * sizeof(uint32_t), s));
     uint32_t* slots = ws->words + 2;
     CK(cudaMemsetAsync(slots, 0, sizeof(uint32_t) * kmax, s));
-    // iterate k writes buf[k % 2]; buf[1] is the caller's y.  Iterations are
-    // enqueued kDeerBatch at a time with one residual read-back per batch;
-    // an iteration enqueued after the solve stopped returns at once (it sees
-    // its predecessor's residual on the device).
+    // iterate k writes buf[k % 2]; buf[1] is the caller's y.  Iteration 1
+    // reads the initial guess (a guess passed in y itself is first copied to
+    // buf[0]).  Iterations are enqueued kDeerBatch at a time with one residual
+    // read-back per batch; an iteration enqueued after the solve stopped
+    // returns at once (it sees its predecessor's residual, or the all-done
+    // word, on the device).
     void* buf[2] = {ws->ybuf, y};
+    const void* y0 = y_init;
+    if (y_init != nullptr && y_init == y) {
+        CK(cudaMemcpyAsync(ws->ybuf, y_init, nbytes, cudaMemcpyDeviceToDevice, s));
+        y0 = ws->ybuf;
+    }
     int k = 0, status = LR_ERR_NOT_CONVERGED;
     float rho = 0.f;
     int launched = 0;
@@ -448,27 +501,82 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y, int6
                 nx.epoch = cr.epoch + 1;  // the next plan() call's
                 nx.pre = kk > 1 ? 1u : 0u;
             }
-            CK(launch_deer_iter(dtype, vec, w, u, h0, kk == 1 ? nullptr : buf[(kk - 1) & 1],
-                                buf[kk & 1], slots + (kk - 1), kk == 1 ? nullptr : slots + (kk - 2),
-                                eps, nx, g, cr, s));
+            DeerSeq sq{nullptr, nullptr, nullptr};
+            if (per_sequence) sq = DeerSeq{sq_slots + (size_t)(kk - 1) * B, sq_done, sq_all};
+            CK(launch_deer_iter(dtype, vec, w, u, h0, kk == 1 ? y0 : buf[(kk - 1) & 1],
+                                buf[kk & 1], slots + (kk - 1),
+                                kk == 1 || per_sequence ? nullptr : slots + (kk - 2), eps, nx, sq, g,
+                                cr, s));
+            if (per_sequence)
+                CK(launch_deer_seq_update(sq_slots + (size_t)(kk - 1) * B, sq_done, sq_iters, sq_all,
+                                          B, eps, kk, s));
         }
-        CK(cudaMemcpyAsync(ws->host_word + first, slots + first, sizeof(uint32_t) * nb,
-                           cudaMemcpyDeviceToHost, s));
-        CK(cudaStreamSynchronize(s));
-        for (k = first + 1; k <= launched; ++k) {
-            const uint32_t bits = ws->host_word[k - 1];
-            memcpy(&rho, &bits, sizeof rho);
-            if (resid_hist) resid_hist[k - 1] = rho;
-            if (!(rho <= 3.4e38f)) { status = LR_ERR_NONFINITE; done = true; break; }
-            if (rho < eps) { status = LR_OK; done = true; break; }
+        if (!per_sequence) {
+            CK(cudaMemcpyAsync(ws->host_word + first, slots + first, sizeof(uint32_t) * nb,
+                               cudaMemcpyDeviceToHost, s));
+            CK(cudaStreamSynchronize(s));
+            for (k = first + 1; k <= launched; ++k) {
+                rho = bits_f(ws->host_word[k - 1]);
+                if (resid_hist) resid_hist[k - 1] = rho;
+                if (!(rho <= 3.4e38f)) { status = LR_ERR_NONFINITE; done = true; break; }
+                if (rho < eps) { status = LR_OK; done = true; break; }
+            }
+        } else {
+            uint32_t* hs = ws->seq_host;
+            CK(cudaMemcpyAsync(hs + (size_t)first * B, sq_slots + (size_t)first * B,
+                               sizeof(uint32_t) * (size_t)nb * B, cudaMemcpyDeviceToHost, s));
+            CK(cudaMemcpyAsync(hs + (size_t)kmax * B, sq_all, sizeof(uint32_t),
+                               cudaMemcpyDeviceToHost, s));
+            CK(cudaStreamSynchronize(s));
+            for (int kk = first + 1; kk <= launched; ++kk) {  // max over the sequences still running
+                uint32_t m = 0;
+                for (int64_t b = 0; b < B; ++b) m = hs[(size_t)(kk - 1) * B + b] > m ? hs[(size_t)(kk - 1) * B + b] : m;
+                if (resid_hist) resid_hist[kk - 1] = bits_f(m);
+            }
+            done = hs[(size_t)kmax * B] != 0;
         }
     }
-    if (k > kmax) k = kmax;
-    if ((k & 1) == 0) CK(cudaMemcpyAsync(y, ws->ybuf, nbytes, cudaMemcpyDeviceToDevice, s));
-    *iters_out = k;
-    if (resid_out) *resid_out = rho;
+    if (!per_sequence) {
+        if (k > kmax) k = kmax;
+        if ((k & 1) == 0) CK(cudaMemcpyAsync(y, ws->ybuf, nbytes, cudaMemcpyDeviceToDevice, s));
+        *iters_out = k;
+        if (resid_out) *resid_out = rho;
+        for (int64_t b = 0; b < B; ++b) {
+            if (seq_iters) seq_iters[b] = k;
+            if (seq_resid) seq_resid[b] = rho;
+        }
+    } else {
+        // every sequence's last iterate into y; counts and final residuals
+        CK(launch_deer_seq_gather(ws->ybuf, y, sq_iters, launched, T, B * D, D, dtype, s));
+        int32_t* hi = reinterpret_cast<int32_t*>(ws->seq_host + (size_t)kmax * B + 1);
+        CK(cudaMemcpyAsync(hi, sq_iters, sizeof(int32_t) * (size_t)B, cudaMemcpyDeviceToHost, s));
+        CK(cudaStreamSynchronize(s));
+        int kmx = 0;
+        float rmx = 0.f;
+        bool nonfinite = false, open = false;
+        for (int64_t b = 0; b < B; ++b) {
+            const int kb = hi[b] > 0 ? hi[b] : launched;  // never stopped: ran every iteration
+            const float rb = bits_f(ws->seq_host[(size_t)(kb - 1) * B + b]);
+            if (!(rb <= 3.4e38f)) nonfinite = true;
+            else if (!(rb < eps)) open = true;
+            if (seq_iters) seq_iters[b] = kb;
+            if (seq_resid) seq_resid[b] = rb;
+            kmx = kb > kmx ? kb : kmx;
+            rmx = rb > rmx || !(rb <= 3.4e38f) ? rb : rmx;
+        }
+        status = nonfinite ? LR_ERR_NONFINITE : open ? LR_ERR_NOT_CONVERGED : LR_OK;
+        *iters_out = kmx;
+        if (resid_out) *resid_out = rmx;
+    }
     TRY(leave(*ws, s));
     return status;
+}
+
+int deer_diag_solve(const float* w, const void* u, const void* h0, void* y, int64_t B, int64_t T,
+                    int64_t D, float eps, int kmax, int* iters_out, float* resid_out,
+                    float* resid_hist, int dtype, void* stream) {
+    return deer_diag_solve_ex(w, u, h0, nullptr, y, B, T, D, eps, kmax, 0, iters_out, resid_out,
+                              resid_hist, nullptr, nullptr, dtype, stream);
 }
 
 int deer_diag_bwd(const float* w, const void* y, const void* h0, const void* dy, void* du,

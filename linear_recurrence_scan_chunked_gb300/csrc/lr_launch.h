@@ -228,6 +228,12 @@ struct BiasOut {
 cudaError_t launch_bias_reduce(const float* partials, int64_t n_chunks, int n_arr, int64_t B,
                                int64_t D, BiasOut out, cudaStream_t s);
 
+// DEER per-sequence stopping state (all nullptr: one test for the batch).
+struct DeerSeq {
+    uint32_t* resid;           // [B] this iteration's residual bits per sequence, zeroed
+    const uint32_t* done;      // [B] nonzero: stopped
+    const uint32_t* all_done;  // nonzero: every sequence stopped
+};
 // resid: one fp32 slot (as bits), zeroed before the launch, receives max|ynew-yold|.
 // nx: the next iteration's segment aggregates (segmented walker kernel only;
 // nx.agg == nullptr otherwise), and whether this launch's were published by
@@ -235,7 +241,17 @@ cudaError_t launch_bias_reduce(const float* partials, int64_t n_chunks, int n_ar
 cudaError_t launch_deer_iter(int dtype, bool vec, const float* w, const void* u, const void* h0,
                              const void* yold, void* ynew, uint32_t* resid,
                              const uint32_t* prev_resid, float eps, const NextAgg& nx,
-                             const Geom& g, const Carry& cr, cudaStream_t s);
+                             const DeerSeq& sq, const Geom& g, const Carry& cr, cudaStream_t s);
+// After iteration k of a per-sequence solve: stop the sequences whose residual
+// fell below eps (or is not finite), record K = k for them, set all_done when
+// none runs.
+cudaError_t launch_deer_seq_update(const uint32_t* resid, uint32_t* done, int32_t* iters,
+                                   uint32_t* all_done, int64_t B, float eps, int k,
+                                   cudaStream_t s);
+// At the end of a per-sequence solve: copy into y the sequences whose last
+// iterate is in ybuf (even K; `launched` for those that never stopped).
+cudaError_t launch_deer_seq_gather(const void* ybuf, void* y, const int32_t* iters, int launched,
+                                   int64_t T, int64_t C, int64_t D, int dtype, cudaStream_t s);
 
 // LSTM cell: the four gate pre-activations (or their gradients), [T, C]
 // each, and the four per-feature biases, [D] each.

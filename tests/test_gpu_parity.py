@@ -140,6 +140,85 @@ def test_deer(cuda, shape, dtype):
     np.testing.assert_allclose(hist, rhist, rtol=1e-3, atol=1e-6)
 
 
+def _deer_case(shape, seed, scales=None):
+    """DEER inputs in fp32; scales[b] multiplies sequence b's u and h0."""
+    T, B, D = shape
+    wl = W.like(W.DEER, T, B, D, "f32")
+    inp = W.make_inputs(wl, seed)
+    inp["h0"] = W.normal(seed, 43, (B, D))
+    if scales is not None:
+        sc = np.asarray(scales, np.float32)
+        inp["u"] = (inp["u"] * sc[None, :, None]).astype(np.float32)
+        inp["h0"] = (inp["h0"] * sc[:, None]).astype(np.float32)
+    return inp, dev_inputs(inp, "f32"), f64_inputs(inp, "f32")
+
+
+DEER_SHAPES = [(300, 3, 40), (2000, 2, 256), (9000, 2, 512), (5000, 1, 128)]
+
+
+@pytest.mark.parametrize("shape", DEER_SHAPES)
+def test_deer_warm_start(cuda, shape):
+    """Warm start from the solution of a nearby problem (the previous step's):
+    same K, status and residuals as the oracle from the same guess, fewer
+    iterations than the cold start; the guess may be y itself."""
+    inp, dv, f = _deer_case(shape, 7)
+    near = oracle.rollout_tanh(f["w"], f["u"] + 1e-3 * np.sin(np.arange(f["u"].size)).reshape(f["u"].shape),
+                               f["h0"]).astype(np.float32)
+    guess = torch.from_numpy(near).cuda()
+    r = cuda.deer_diag_solve_ex(dv["w"], dv["u"], dv["h0"], y_init=guess, eps=1e-5, kmax=20)
+    ry, rk, rhist, rst = oracle.deer(f["w"], f["u"], f["h0"], eps=1e-5, kmax=20,
+                                     y_init=near.astype(np.float64))
+    assert (r["iters"], r["status"]) == (rk, rst), (r["hist"], list(rhist))
+    assert_close("y", to_f64(r["y"]), ry, "f32")
+    np.testing.assert_allclose(r["hist"], rhist, rtol=1e-3, atol=1e-6)
+    _, kc, _, _ = oracle.deer(f["w"], f["u"], f["h0"], eps=1e-5, kmax=20)
+    assert rk < kc
+    # in place: the guess in the output buffer
+    y = guess.clone()
+    r2 = cuda.deer_diag_solve_ex(dv["w"], dv["u"], dv["h0"], y=y, y_init=y, eps=1e-5, kmax=20)
+    assert r2["iters"] == rk and torch.equal(y, r["y"])
+
+
+@pytest.mark.parametrize("shape", DEER_SHAPES)
+def test_deer_per_sequence_stopping(cuda, shape):
+    """Per-sequence stopping against the oracle's per-sequence solve: each
+    sequence's K, final residual and iterate; a quiet sequence stops early."""
+    T, B, D = shape
+    scales = [0.01] + [1.5] * (B - 1) if B > 1 else [1.5]
+    inp, dv, f = _deer_case(shape, 8, scales)
+    r = cuda.deer_diag_solve_ex(dv["w"], dv["u"], dv["h0"], eps=1e-5, kmax=20, per_sequence=True)
+    ry, rks, rsts, rhists = oracle.deer_per_sequence(f["w"], f["u"], f["h0"], eps=1e-5, kmax=20)
+    assert r["seq_iters"] == rks, (r["seq_iters"], rks)
+    assert r["status"] == (cuda.LR_OK if all(s == 0 for s in rsts) else r["status"])
+    assert r["iters"] == max(rks)
+    for b in range(B):
+        np.testing.assert_allclose(r["seq_resid"][b], rhists[b][-1], rtol=1e-3, atol=1e-6)
+    assert_close("y", to_f64(r["y"]), ry, "f32")
+    if B > 1:
+        assert rks[0] < max(rks)
+
+
+def test_deer_per_sequence_kmax(cuda):
+    """kmax reached by the loud sequences, not by the quiet one: NOT_CONVERGED,
+    and each sequence's iterate is its own last one."""
+    shape = (9000, 3, 256)
+    inp, dv, f = _deer_case(shape, 9, [0.01, 1.5, 1.5])
+    r = cuda.deer_diag_solve_ex(dv["w"], dv["u"], dv["h0"], eps=1e-5, kmax=3, per_sequence=True)
+    ry, rks, rsts, rhists = oracle.deer_per_sequence(f["w"], f["u"], f["h0"], eps=1e-5, kmax=3)
+    assert rsts[1] == oracle.DEER_NOT_CONVERGED and rsts[0] == oracle.DEER_CONVERGED
+    assert r["status"] == cuda.LR_ERR_NOT_CONVERGED
+    assert r["seq_iters"] == rks
+    assert_close("y", to_f64(r["y"]), ry, "f32")
+
+
+def test_deer_ex_global_matches_deer_diag_solve(cuda):
+    inp, dv, f = _deer_case((9000, 2, 512), 10)
+    y, k, resid, hist, st = cuda.deer_diag_solve(dv["w"], dv["u"], dv["h0"], eps=1e-5, kmax=20)
+    r = cuda.deer_diag_solve_ex(dv["w"], dv["u"], dv["h0"], eps=1e-5, kmax=20)
+    assert (r["iters"], r["status"]) == (k, st) and torch.equal(r["y"], y)
+    assert r["seq_iters"] == [k, k]
+
+
 def test_scan_integer_valued_is_bit_exact(cuda):
     """a in {0, +1, -1}, b small integers: every association order is exact,
     so the chunked scan must equal the sequential oracle bit for bit."""
