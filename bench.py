@@ -299,18 +299,38 @@ class Bench:
                                   for k, v in outs.items()}
             self.h2d += sum(v.numel() * v.element_size() for v in self.pin_in[name].values())
             self.d2h += sum(v.numel() * v.element_size() for v, _ in self.pin_out[name].values())
+        self.s_in, self.s_out = t.cuda.Stream(), t.cuda.Stream()
 
     def e2e_step(self):
+        """One step from pinned host buffers: every row's inputs stream in on
+        one copy stream, a row's kernels run on the current stream once its
+        own inputs have landed, and its outputs stream out on a second copy
+        stream, so the host link carries both directions at once, overlapped
+        with the kernels.  Returns after every copy has completed."""
+        t = self.torch
+        comp = t.cuda.current_stream()
+        ready = {}
+        with t.cuda.stream(self.s_in):
+            for name, wl, passes in ROWS:
+                o = self.d[name]
+                for k, hv in self.pin_in[name].items():
+                    o[k].copy_(hv, non_blocking=True)
+                ready[name] = t.cuda.Event()
+                ready[name].record(self.s_in)
         elems = 0
         for name, wl, passes in ROWS:
-            o = self.d[name]
-            for k, hv in self.pin_in[name].items():
-                o[k].copy_(hv, non_blocking=True)
+            comp.wait_event(ready[name])
             e, _, _ = self.run_row(name, wl, passes)
             elems += e
-            for k, (dv, hv) in self.pin_out[name].items():
-                hv.copy_(dv, non_blocking=True)
-        self.torch.cuda.current_stream().synchronize()
+            done = t.cuda.Event()
+            done.record(comp)
+            self.s_out.wait_event(done)
+            with t.cuda.stream(self.s_out):
+                for k, (dv, hv) in self.pin_out[name].items():
+                    hv.copy_(dv, non_blocking=True)
+        self.s_in.synchronize()
+        comp.synchronize()
+        self.s_out.synchronize()
         return elems
 
 
