@@ -13,6 +13,9 @@ Every function here follows the pages cited in ``lr_oracle.c``:
   deer / deer_step     -- DEER Newton iteration on a diagonal tanh RNN (from a
                           given initial guess or zeros)
   deer_per_sequence    -- the same with each batch sequence stopping on its own
+  deer_ode / deer_ode_step / rollout_ode -- DEER's ODE form (exp(-G dt)
+                          coefficients, G clamped) and its exponential-Euler
+                          fixed point
   rollout_tanh         -- the direct sequential tanh RNN
 Each is pinned by tests in ``tests/test_oracle_pins.py`` against closed forms,
 library linear solves, finite differences and brute-force evaluation orders.
@@ -66,6 +69,11 @@ def _load():
         lib.lro_deer_step.argtypes = [I64, I64, I64, P, P, P, P, P, P]
         lib.lro_deer.argtypes = [I64, I64, I64, P, P, P, P, ctypes.c_double, ctypes.c_int, P, P, P]
         lib.lro_deer_bwd.argtypes = [I64, I64, I64] + [P] * 7
+        lib.lro_rollout_ode.argtypes = [I64, I64, I64] + [P] * 6
+        lib.lro_deer_ode_step.argtypes = [I64, I64, I64] + [P] * 8
+        lib.lro_deer_ode.argtypes = [I64, I64, I64, P, P, P, P, ctypes.c_double, ctypes.c_int,
+                                     P, P, P, P]
+        lib.lro_deer_ode.restype = ctypes.c_int
         lib.lro_deer.restype = ctypes.c_int
         lib.lro_num_threads.restype = ctypes.c_int
         lib.lro_set_num_threads.argtypes = [ctypes.c_int]
@@ -235,6 +243,44 @@ def deer_per_sequence(w, u, h0=None, eps=1e-5, kmax=20, y_init=None):
         status.append(sb)
         hists.append(hb)
     return y, iters, status, hists
+
+
+def rollout_ode(w, u, dt, h0=None):
+    """Exponential-Euler rollout of dy/dt = -y + tanh(w y + u) on steps dt[t]
+    (G clamped to [-10, 10]).  Returns (y, clamps)."""
+    w, u, dt, h0 = _f64(w), _f64(u), _f64(dt), _f64(h0)
+    T, C = _tc(u)
+    y = np.empty_like(u)
+    n = ctypes.c_int64(0)
+    _load().lro_rollout_ode(T, C, w.shape[0], _p(w), _p(u), _p(dt), _p(h0), _p(y), ctypes.byref(n))
+    return y, int(n.value)
+
+
+def deer_ode_step(w, u, dt, yprev=None, h0=None):
+    """One ODE-form DEER iteration from yprev (None = zeros): (ynew, rho, clamps)."""
+    w, u, dt, yprev, h0 = _f64(w), _f64(u), _f64(dt), _f64(yprev), _f64(h0)
+    T, C = _tc(u)
+    y = np.empty_like(u)
+    rho = ctypes.c_double(0.0)
+    n = ctypes.c_int64(0)
+    _load().lro_deer_ode_step(T, C, w.shape[0], _p(w), _p(u), _p(dt), _p(h0), _p(yprev), _p(y),
+                              ctypes.byref(rho), ctypes.byref(n))
+    return y, rho.value, int(n.value)
+
+
+def deer_ode(w, u, dt, h0=None, eps=1e-5, kmax=20):
+    """ODE-form DEER: (y, iters, rho_history, status, clamps of the last iteration)."""
+    w, u, dt, h0 = _f64(w), _f64(u), _f64(dt), _f64(h0)
+    T, C = _tc(u)
+    y = np.empty_like(u)
+    hist = np.zeros(kmax, dtype=np.float64)
+    iters = ctypes.c_int(0)
+    n = ctypes.c_int64(0)
+    st = _load().lro_deer_ode(T, C, w.shape[0], _p(w), _p(u), _p(dt), _p(h0), float(eps), int(kmax),
+                              _p(y), _p(hist), ctypes.byref(iters), ctypes.byref(n))
+    if st < 0:
+        raise MemoryError("oracle deer_ode: allocation failed")
+    return y, int(iters.value), hist[: iters.value].copy(), int(st), int(n.value)
 
 
 def rel_err(got, ref) -> float:

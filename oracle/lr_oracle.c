@@ -309,6 +309,122 @@ int lro_lstm_bwd(int64_t T, int64_t C, int64_t D, const double* zf,
     return 0;
 }
 
+/* ------------------------------------------- DEER, ODE form (next row) */
+/*
+ * [P4] "监控与调优", third check: in the ODE form of DEER the linear inverse
+ * operator's coefficients are exp(-G_i Delta_i), which overflow when G_i is
+ * large, so the elements of G_i are clamped to [-10, 10] (and the clamps
+ * counted).  Reading: the continuous-time form of the same diagonal tanh RNN,
+ *     dy/dt = f(y, u) = -y + tanh(w y + u),
+ * on steps of length dt[t] with the input held at u_t over step t and
+ * y_{-1} = h0.  Each iteration linearises f at the previous iterate at the
+ * start of the step,
+ *     G_t = -df/dy = 1 - w (1 - tanh^2(w ytil_{t-1} + u_t)),  clamped to [-10, 10],
+ *     z_t = f(ytil_{t-1}, u_t) + G_t ytil_{t-1},
+ * and solves dy/dt + G_t y = z_t exactly over the step,
+ *     y_t = exp(-G_t dt_t) y_{t-1} + (1 - exp(-G_t dt_t)) / G_t z_t
+ * (dt_t z_t when G_t = 0): a linear recurrence, the scan.  At the fixed point
+ * (ytil = y) this is the exponential-Euler rollout
+ *     y_t = y_{t-1} + (1 - exp(-G_t dt_t)) / G_t f(y_{t-1}, u_t).
+ * (1 - exp(-x)) is evaluated as -expm1(-x).  The clamp counts are of the
+ * evaluations where G left [-10, 10].
+ */
+static double ode_g(double wk, double th, int64_t* ncl) {
+    double g = 1.0 - wk * (1.0 - th * th);
+    if (g > 10.0) { g = 10.0; ++*ncl; }
+    else if (g < -10.0) { g = -10.0; ++*ncl; }
+    return g;
+}
+
+/* (1 - exp(-g dt)) / g, and its g = 0 limit dt */
+static double ode_phi(double g, double dt) { return g != 0.0 ? -expm1(-g * dt) / g : dt; }
+
+void lro_rollout_ode(int64_t T, int64_t C, int64_t D, const double* w,
+                     const double* u, const double* dt, const double* h0,
+                     double* y, int64_t* clamps) {
+    int64_t ncl = 0;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(lro_num_threads()) reduction(+ : ncl)
+#endif
+    {
+        int64_t c0_ = 0, c1_ = C;
+#ifdef _OPENMP
+        chan_range(C, omp_get_thread_num(), omp_get_num_threads(), &c0_, &c1_);
+#endif
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t k = c0_; k < c1_; ++k) {
+                int64_t i = t * C + k;
+                double wk = w[k % D];
+                double yp = t > 0 ? y[i - C] : (h0 ? h0[k] : 0.0);
+                double th = tanh(wk * yp + u[i]);
+                double g = ode_g(wk, th, &ncl);
+                y[i] = yp + ode_phi(g, dt[t]) * (th - yp);
+            }
+    }
+    if (clamps) *clamps = ncl;
+}
+
+/* One iteration from yprev (NULL = the all-zero guess); rho = max |ynew - yprev|. */
+void lro_deer_ode_step(int64_t T, int64_t C, int64_t D, const double* w,
+                       const double* u, const double* dt, const double* h0,
+                       const double* yprev, double* ynew, double* rho,
+                       int64_t* clamps) {
+    double best = 0.0;
+    int64_t ncl = 0;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(lro_num_threads()) reduction(max : best) reduction(+ : ncl)
+#endif
+    {
+        int64_t c0_ = 0, c1_ = C;
+#ifdef _OPENMP
+        chan_range(C, omp_get_thread_num(), omp_get_num_threads(), &c0_, &c1_);
+#endif
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t k = c0_; k < c1_; ++k) {
+                int64_t i = t * C + k;
+                double wk = w[k % D];
+                double init = h0 ? h0[k] : 0.0;
+                double ytil = t > 0 ? (yprev ? yprev[i - C] : 0.0) : init;
+                double th = tanh(wk * ytil + u[i]);
+                double g = ode_g(wk, th, &ncl);
+                double z = (th - ytil) + g * ytil;
+                double a = exp(-g * dt[t]);
+                double b = ode_phi(g, dt[t]) * z;
+                double ylast = t > 0 ? ynew[i - C] : init;
+                ynew[i] = a * ylast + b;
+                double diff = fabs(ynew[i] - (yprev ? yprev[i] : 0.0));
+                if (diff > best) best = diff;
+            }
+    }
+    *rho = best;
+    if (clamps) *clamps = ncl;
+}
+
+/*
+ * The ODE-form iteration from the all-zero guess with the stopping rule of
+ * lro_deer; clamps: the clamp count of the last iteration.  Returns as
+ * lro_deer.
+ */
+int lro_deer_ode(int64_t T, int64_t C, int64_t D, const double* w, const double* u,
+                 const double* dt, const double* h0, double eps, int kmax,
+                 double* y, double* rho_hist, int* iters, int64_t* clamps) {
+    size_t n = (size_t)(T * C);
+    double* prev = (double*)malloc(sizeof(double) * (n ? n : 1));
+    if (!prev) return -1;
+    int status = 1, k;
+    for (k = 1; k <= kmax; ++k) {
+        double rho = 0.0;
+        lro_deer_ode_step(T, C, D, w, u, dt, h0, k == 1 ? NULL : prev, y, &rho, clamps);
+        rho_hist[k - 1] = rho;
+        if (!isfinite(rho)) { status = 2; break; }
+        if (rho < eps) { status = 0; break; }
+        memcpy(prev, y, sizeof(double) * n);
+    }
+    *iters = k > kmax ? kmax : k;
+    free(prev);
+    return status;
+}
+
 /* -------------------------------------------------- DEER (row a5), tanh RNN */
 /*
  * Target recurrence: h_t = tanh(w (.) h_{t-1} + u_t), h_{-1} = h0, w in [D].

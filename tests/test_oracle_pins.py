@@ -542,6 +542,100 @@ def test_deer_bwd_small_signal_is_linear_scan_backward():
         np.testing.assert_allclose(dh0[0, d], w[d] * delta[0], rtol=0, atol=1e-10 * scale)
 
 
+# --------------------------------------------------------- DEER, ODE form
+
+def _ode_exact_piecewise(w, u, dt, h0, fun):
+    """Integrate dy/dt = fun(y, u_t) step by step with scipy (DOP853, tight
+    tolerances), the input held over each step."""
+    import scipy.integrate
+    T, C = u.shape
+    y = np.empty_like(u)
+    cur = h0.copy()
+    for t in range(T):
+        sol = scipy.integrate.solve_ivp(lambda _, yy: fun(yy, u[t]), (0.0, dt[t]), cur,
+                                        method="DOP853", rtol=1e-13, atol=1e-15)
+        cur = sol.y[:, -1]
+        y[t] = cur
+    return y
+
+
+def test_deer_ode_linear_case_is_exact():
+    # w = 0: f = -y + tanh(u) is linear in y, so the exponential step is the
+    # exact solution over each step and DEER is exact after one iteration
+    T, C = 40, 3
+    r = np.random.default_rng(41)
+    u, h0 = r.standard_normal((T, C)), r.standard_normal(C)
+    dt = r.uniform(0.05, 2.0, T)
+    ref = _ode_exact_piecewise(np.zeros(C), u, dt, h0, lambda yy, ut: -yy + np.tanh(ut))
+    y, clamps = oracle.rollout_ode(np.zeros(C), u, dt, h0)
+    np.testing.assert_allclose(y, ref, rtol=0, atol=1e-11)
+    yd, k, hist, st, _ = oracle.deer_ode(np.zeros(C), u, dt, h0, eps=1e-12, kmax=10)
+    assert (k, st) == (2, oracle.DEER_CONVERGED) and hist[1] < 1e-15
+    np.testing.assert_allclose(yd, ref, rtol=0, atol=1e-11)
+
+
+def test_deer_ode_small_signal_is_the_linearised_ode():
+    # at amplitude 1e-6 tanh(x) = x to 1e-18: f = -(1 - w) y + u, linear, so
+    # the exponential step with G = 1 - w is exact (a wrong sign or a dropped
+    # term in G's w part is first order in dt here)
+    T, C = 30, 4
+    r = np.random.default_rng(42)
+    w = r.uniform(-0.9, 0.9, C)
+    u, h0 = 1e-6 * r.standard_normal((T, C)), 1e-6 * r.standard_normal(C)
+    dt = r.uniform(0.1, 1.5, T)
+    ref = _ode_exact_piecewise(w, u, dt, h0, lambda yy, ut: -(1.0 - w) * yy + ut)
+    y, _ = oracle.rollout_ode(w, u, dt, h0)
+    np.testing.assert_allclose(y, ref, rtol=0, atol=1e-16)
+
+
+def test_deer_ode_small_step_is_forward_euler():
+    # dt -> 0: the exponential step is y + dt f(y) + O(dt^2)
+    T, C = 100, 3
+    r = np.random.default_rng(43)
+    w = r.uniform(-0.9, 0.9, C)
+    u, h0 = r.standard_normal((T, C)), r.standard_normal(C)
+    dt = np.full(T, 1e-5)
+    y, _ = oracle.rollout_ode(w, u, dt, h0)
+    fe = np.empty_like(u)
+    cur = h0.copy()
+    for t in range(T):
+        cur = cur + dt[t] * (-cur + np.tanh(w * cur + u[t]))
+        fe[t] = cur
+    np.testing.assert_allclose(y, fe, rtol=0, atol=1e-7)
+
+
+def test_deer_ode_converges_to_the_rollout():
+    T, B, D = 2000, 2, 5
+    r = np.random.default_rng(44)
+    w = r.uniform(-0.9, 0.9, D)
+    u, h0 = r.standard_normal((T, B, D)), r.standard_normal((B, D))
+    dt = r.uniform(0.1, 1.0, T)
+    y, k, hist, st, _ = oracle.deer_ode(w, u, dt, h0, eps=1e-12, kmax=60)
+    assert st == oracle.DEER_CONVERGED
+    np.testing.assert_allclose(y, oracle.rollout_ode(w, u, dt, h0)[0], rtol=0, atol=1e-11)
+    # iteration 1 from zeros is one step of the iteration
+    y1, rho1, _ = oracle.deer_ode_step(w, u, dt)
+    assert abs(rho1 - np.max(np.abs(y1))) == 0.0
+
+
+def test_deer_ode_clamp():
+    # w = -12: G = 1 + 12 (1 - tanh^2) reaches 13 where the pre-activation is
+    # small; clamped to 10 and counted (the count is that of the rollout, at
+    # the fixed point), every value finite
+    T, C = 500, 4
+    r = np.random.default_rng(45)
+    w = np.full(C, -12.0)
+    u, dt = 0.3 * r.standard_normal((T, C)), np.full(T, 0.2)
+    y, clamps = oracle.rollout_ode(w, u, dt, np.zeros(C))
+    assert np.all(np.isfinite(y))
+    prev = np.vstack([np.zeros((1, C)), y[:-1]])
+    g = 1.0 - w * (1.0 - np.tanh(w * prev + u) ** 2)
+    assert clamps == int(np.sum(np.abs(g) > 10.0)) > 0
+    yd, k, hist, st, cl = oracle.deer_ode(w, u, dt, np.zeros(C), eps=1e-10, kmax=60)
+    assert st == oracle.DEER_CONVERGED and cl == clamps
+    np.testing.assert_allclose(yd, y, rtol=0, atol=1e-9)
+
+
 def test_oracle_threads_do_not_change_results():
     a = rng.uniform(-1, 1, (300, 33))
     b = rng.standard_normal((300, 33))
