@@ -196,6 +196,28 @@ int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void
                        int* seq_iters, float* seq_resid, int dtype, void* stream);
 
 /*
+ * DEER solve in the ODE form (the next row on the same scan).  [P4] "监控与调优":
+ * the coefficients of the linear inverse operator are exp(-G_i dt_i), with the
+ * elements of G_i clamped to [-10, 10] and the clamps counted.  The ODE is the
+ * continuous-time diagonal tanh RNN dy/dt = -y + tanh(w (.) y + u) on steps
+ * dt[t], the input held at u_t over step t, y_{-1} = h0.  Iteration k
+ * linearises at the previous iterate ytil (ytil_{-1} = h0; zeros before the
+ * first iteration):
+ *   G_t = 1 - w (1 - tanh^2(w ytil_{t-1} + u_t)) clamped to [-10, 10],
+ *   z_t = (tanh(w ytil_{t-1} + u_t) - ytil_{t-1}) + G_t ytil_{t-1},
+ *   y_t = exp(-G_t dt_t) y_{t-1} + (1 - exp(-G_t dt_t)) / G_t z_t  (dt_t z_t if G_t = 0),
+ * one scan per iteration; the fixed point is the exponential-Euler rollout.
+ * Stopping rule, outputs and statuses as deer_diag_solve.
+ *   dt          : [T] fp32 in, step lengths (device)
+ *   clamps_out  : host int64 out (may be NULL): clamped G evaluations of the
+ *                 last iteration
+ */
+int deer_ode_solve(const float* w, const void* u, const float* dt, const void* h0, void* y,
+                   int64_t B, int64_t T, int64_t D, float eps, int kmax, int* iters_out,
+                   float* resid_out, float* resid_hist, int64_t* clamps_out, int dtype,
+                   void* stream);
+
+/*
  * Gradient through the DEER solution (the next row on the same scan):
  * [P4] "核心原理": at the fixed point y is the rollout of
  * h_t = tanh(w (.) h_{t-1} + u_t), so the gradient of a loss L with upstream

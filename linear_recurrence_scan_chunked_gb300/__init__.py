@@ -58,6 +58,8 @@ def load():
     lib.deer_diag_solve.argtypes = [P, P, P, P, I64, I64, I64, ctypes.c_float, I, P, P, P, I, P]
     lib.deer_diag_solve_ex.argtypes = [P, P, P, P, P, I64, I64, I64, ctypes.c_float, I, I, P, P,
                                        P, P, P, I, P]
+    lib.deer_ode_solve.argtypes = [P, P, P, P, P, I64, I64, I64, ctypes.c_float, I, P, P, P, P,
+                                   I, P]
     lib.deer_diag_bwd.argtypes = [P] * 7 + [I64, I64, I64, I, P]
     lib.lr_last_error.argtypes = []
     lib.lr_status_str.argtypes = [I]
@@ -293,6 +295,29 @@ def deer_diag_solve_ex(w, u, h0=None, y=None, y_init=None, eps=1e-5, kmax=20,
     k = int(it.value)
     return {"y": y, "iters": k, "resid": float(rho.value), "hist": list(hist)[:k], "status": int(st),
             "seq_iters": list(sk)[:B], "seq_resid": list(sr)[:B]}
+
+
+def deer_ode_solve(w, u, dt, h0=None, y=None, eps=1e-5, kmax=20, stream=None):
+    """DEER in the ODE form (dy/dt = -y + tanh(w y + u) on steps dt[T], G
+    clamped to [-10, 10]).  Returns (y, iters, resid, resid_history, status,
+    clamps of the last iteration)."""
+    _seq("u", u)
+    T, B, D = u.shape
+    _param("w", w, D)
+    _param("dt", dt, T)
+    _state("h0", h0, u)
+    y = torch.empty_like(u) if y is None else _seq("y", y, u)
+    iters = ctypes.c_int(0)
+    resid = ctypes.c_float(0.0)
+    clamps = ctypes.c_int64(0)
+    hist = (ctypes.c_float * max(1, int(kmax)))()
+    st = load().deer_ode_solve(_p(w), _p(u), _p(dt), _p(h0), _p(y), B, T, D, ctypes.c_float(eps),
+                               int(kmax), ctypes.byref(iters), ctypes.byref(resid), hist,
+                               ctypes.byref(clamps), _code(u), _stream(stream))
+    if st not in (LR_OK, LR_ERR_NOT_CONVERGED, LR_ERR_NONFINITE):
+        _check(st)
+    k = iters.value
+    return y, k, resid.value, [hist[i] for i in range(k)], st, int(clamps.value)
 
 
 def deer_diag_bwd(w, y, dy, h0=None, du=None, dw=None, dh0=None, want_dh0=True, stream=None):

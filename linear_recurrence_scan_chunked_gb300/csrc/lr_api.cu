@@ -88,6 +88,7 @@ struct DevWS {
     uint32_t* host_word = nullptr;                        // pinned [kMaxIters], residual reads
     void* test_buf = nullptr;                             // timeout-test problem
     uint32_t* seq = nullptr;     size_t seq_cap = 0;      // DEER per-sequence state (words)
+    unsigned long long* clamps = nullptr;                 // DEER ODE form: [kMaxIters] clamp counts
     uint32_t* seq_host = nullptr; size_t seq_host_cap = 0;  // pinned mirror of its residuals
     uint32_t epoch = 0;
     cudaEvent_t done = nullptr;
@@ -108,6 +109,7 @@ int get_ws(DevWS** out) {
         CK(cudaMalloc(&w->words, sizeof(uint32_t) * (2 + kMaxIters)));
         CK(cudaMemset(w->words, 0, sizeof(uint32_t) * (2 + kMaxIters)));
         CK(cudaHostAlloc(&w->host_word, sizeof(uint32_t) * kMaxIters, cudaHostAllocDefault));
+        CK(cudaMalloc(&w->clamps, sizeof(unsigned long long) * kMaxIters));
         CK(cudaEventCreateWithFlags(&w->done, cudaEventDisableTiming));
         w->bytes = sizeof(uint32_t) * (2 + kMaxIters);
         g_ws[dev] = w;
@@ -577,6 +579,80 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y, int6
                     float* resid_hist, int dtype, void* stream) {
     return deer_diag_solve_ex(w, u, h0, nullptr, y, B, T, D, eps, kmax, 0, iters_out, resid_out,
                               resid_hist, nullptr, nullptr, dtype, stream);
+}
+
+int deer_ode_solve(const float* w, const void* u, const float* dt, const void* h0, void* y,
+                   int64_t B, int64_t T, int64_t D, float eps, int kmax, int* iters_out,
+                   float* resid_out, float* resid_hist, int64_t* clamps_out, int dtype,
+                   void* stream) {
+    TRY(check_sizes(B, T, D, dtype));
+    if (!iters_out || kmax < 1 || kmax > kMaxIters || !(eps >= 0.f)) return LR_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (B * T * D == 0) {
+        *iters_out = 0;
+        if (resid_out) *resid_out = 0.f;
+        if (clamps_out) *clamps_out = 0;
+        return LR_OK;
+    }
+    bool vec;
+    TRY(check_ptrs({u, y}, {h0}, {w, dt}, dtype, D, &vec));
+    GUARD;
+    DevWS* ws;
+    TRY(get_ws(&ws));
+    const size_t nbytes = (size_t)(B * T * D) * esize(dtype);
+    {
+        size_t cap = ws->ybuf_cap;
+        char* p = (char*)ws->ybuf;
+        TRY(grow(*ws, &p, &cap, nbytes, false));
+        ws->ybuf = p;
+        ws->ybuf_cap = cap;
+    }
+    TRY(enter(*ws, s));
+    uint32_t* slots = ws->words + 2;
+    CK(cudaMemsetAsync(slots, 0, sizeof(uint32_t) * kmax, s));
+    CK(cudaMemsetAsync(ws->clamps, 0, sizeof(unsigned long long) * kmax, s));
+    // as deer_diag_solve: iterate k writes buf[k % 2] (buf[1] is y), batches
+    // of kDeerBatch launches with one residual read-back each
+    void* buf[2] = {ws->ybuf, y};
+    int k = 0, status = LR_ERR_NOT_CONVERGED;
+    float rho = 0.f;
+    int launched = 0;
+    bool done = false;
+    while (!done && launched < kmax) {
+        const int first = launched;
+        const int nb = kmax - launched < kDeerBatch ? kmax - launched : kDeerBatch;
+        for (int i = 0; i < nb; ++i) {
+            const int kk = ++launched;
+            Geom g;
+            Carry cr;
+            TRY(plan(*ws, OP_DEER_ODE, dtype, vec, T, B * D, D, &g, &cr, s));
+            CK(launch_deer_ode_iter(dtype, vec, w, u, dt, h0, kk == 1 ? nullptr : buf[(kk - 1) & 1],
+                                    buf[kk & 1], slots + (kk - 1),
+                                    kk == 1 ? nullptr : slots + (kk - 2), eps,
+                                    ws->clamps + (kk - 1), g, cr, s));
+        }
+        CK(cudaMemcpyAsync(ws->host_word + first, slots + first, sizeof(uint32_t) * nb,
+                           cudaMemcpyDeviceToHost, s));
+        CK(cudaStreamSynchronize(s));
+        for (k = first + 1; k <= launched; ++k) {
+            rho = bits_f(ws->host_word[k - 1]);
+            if (resid_hist) resid_hist[k - 1] = rho;
+            if (!(rho <= 3.4e38f)) { status = LR_ERR_NONFINITE; done = true; break; }
+            if (rho < eps) { status = LR_OK; done = true; break; }
+        }
+    }
+    if (k > kmax) k = kmax;
+    if ((k & 1) == 0) CK(cudaMemcpyAsync(y, ws->ybuf, nbytes, cudaMemcpyDeviceToDevice, s));
+    if (clamps_out) {
+        unsigned long long n = 0;
+        CK(cudaMemcpyAsync(&n, ws->clamps + (k - 1), sizeof n, cudaMemcpyDeviceToHost, s));
+        CK(cudaStreamSynchronize(s));
+        *clamps_out = (int64_t)n;
+    }
+    *iters_out = k;
+    if (resid_out) *resid_out = rho;
+    TRY(leave(*ws, s));
+    return status;
 }
 
 int deer_diag_bwd(const float* w, const void* y, const void* h0, const void* dy, void* du,

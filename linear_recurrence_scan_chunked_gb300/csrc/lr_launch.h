@@ -51,6 +51,7 @@ enum Op {
     OP_DEER_BWD,
     OP_LSTM_FWD,
     OP_LSTM_BWD,
+    OP_DEER_ODE,
     OP_COUNT
 };
 
@@ -73,8 +74,10 @@ constexpr KCfg kcfg(Op op, int dtype, int mode) {
     // bf16 holds two elements per register: twice the rows of fp32 (but the
     // DEER backward keeps two fp32 values per element between its passes: the
     // rows of fp32 for both).  The LSTM cell stages as many arrays per
-    // direction as the SRU cell and takes its rows.
-    return op == OP_LSTM_FWD   ? kcfg(OP_SRU_FWD, dtype, mode)
+    // direction as the SRU cell and takes its rows; DEER's ODE form takes the
+    // tanh form's.
+    return op == OP_DEER_ODE   ? kcfg(OP_DEER, dtype, mode)
+           : op == OP_LSTM_FWD ? kcfg(OP_SRU_FWD, dtype, mode)
            : op == OP_LSTM_BWD ? kcfg(OP_SRU_BWD, dtype, mode)
            : op == OP_DEER_BWD ? KCfg{8, mode == CARRY_CHAIN ? 2 : 4, mode == TILE_TMA ? 3 : 0}
            : mode == CARRY_CHAIN
@@ -276,6 +279,14 @@ cudaError_t launch_lstm_bwd(int dtype, bool vec, const LstmGates& z, const LstmB
                             const void* c0, const void* c, const void* dh, const LstmGates& dz,
                             void* dc0, float* partials, const Geom& g, const Carry& cr,
                             cudaStream_t s);
+
+// DEER, ODE form: one iteration (dt: [T] step lengths; clamps: the
+// iteration's clamp counter, zeroed before the launch).
+cudaError_t launch_deer_ode_iter(int dtype, bool vec, const float* w, const void* u,
+                                 const float* dt, const void* h0, const void* yold, void* ynew,
+                                 uint32_t* resid, const uint32_t* prev_resid, float eps,
+                                 unsigned long long* clamps, const Geom& g, const Carry& cr,
+                                 cudaStream_t s);
 
 // DEER backward: partials is [n_chunks][C] fp32 scratch (dw per tile),
 // followed by C floats that launch_bias_reduce uses for its per-channel sums

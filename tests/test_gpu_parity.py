@@ -219,6 +219,44 @@ def test_deer_ex_global_matches_deer_diag_solve(cuda):
     assert r["seq_iters"] == [k, k]
 
 
+def _ode_case(shape, seed, w_value=None, u_scale=1.0, dt=None):
+    T, B, D = shape
+    wl = W.like(W.DEER, T, B, D, "f32")
+    inp = W.make_inputs(wl, seed)
+    inp["h0"] = W.normal(seed, 43, (B, D))
+    inp["u"] = (inp["u"] * np.float32(u_scale)).astype(np.float32)
+    if w_value is not None:
+        inp["w"] = np.full(D, w_value, np.float32)
+    dts = W.uniform(seed, 44, (T,), 0.1, 1.0) if dt is None else np.full(T, dt, np.float32)
+    dv, f = dev_inputs(inp, "f32"), f64_inputs(inp, "f32")
+    return dv, f, torch.from_numpy(dts).cuda(), dts.astype(np.float64)
+
+
+@pytest.mark.parametrize("shape", DEER_SHAPES)
+def test_deer_ode(cuda, shape):
+    """ODE form against the oracle: K, status, residual history, iterate."""
+    dv, f, dt, dtf = _ode_case(shape, 11)
+    y, k, resid, hist, st, cl = cuda.deer_ode_solve(dv["w"], dv["u"], dt, dv["h0"], eps=1e-5, kmax=20)
+    ry, rk, rhist, rst, rcl = oracle.deer_ode(f["w"], f["u"], dtf, f["h0"], eps=1e-5, kmax=20)
+    assert (k, st) == (rk, rst), (hist, list(rhist))
+    assert_close("y", to_f64(y), ry, "f32")
+    np.testing.assert_allclose(hist, rhist, rtol=1e-3, atol=1e-6)
+    assert cl == rcl == 0
+
+
+def test_deer_ode_clamp(cuda):
+    """w = -12: G = 1 + 12 (1 - tanh^2) exceeds 10 for small pre-activations
+    and is clamped.  The count decides, per element, G > 10 in fp32 on the
+    GPU and in fp64 in the oracle from iterates that differ by ~1e-6: the
+    elements within that band of the bound may fall either way."""
+    dv, f, dt, dtf = _ode_case((3000, 2, 128), 12, w_value=-12.0, u_scale=0.3, dt=0.2)
+    y, k, resid, hist, st, cl = cuda.deer_ode_solve(dv["w"], dv["u"], dt, dv["h0"], eps=1e-5, kmax=60)
+    ry, rk, rhist, rst, rcl = oracle.deer_ode(f["w"], f["u"], dtf, f["h0"], eps=1e-5, kmax=60)
+    assert st == rst == cuda.LR_OK and abs(k - rk) <= 1
+    assert_close("y", to_f64(y), ry, "f32")
+    assert rcl > 0 and abs(cl - rcl) <= max(4, rcl // 10000), (cl, rcl)
+
+
 def test_scan_integer_valued_is_bit_exact(cuda):
     """a in {0, +1, -1}, b small integers: every association order is exact,
     so the chunked scan must equal the sequential oracle bit for bit."""
