@@ -236,6 +236,45 @@ class Bench:
                 "frac": round(byt / (ms / 1e3) / 1e9 / peak, 3),
                 "workload": f"deer fp32 T={wl.T} B={wl.B} D={wl.D}, gradient through the solution"}
 
+    def time_deer_variants(self, peak, reps=5):
+        """At the DEER workload's size: the ODE form (steps dt ~ U(0.1, 1))
+        and a warm-started solve (the guess is the solution for u + 1e-3 sin,
+        a nearby problem, as the previous training step's would be): mean
+        solve time, K, algorithmic GB/s per iteration."""
+        t, L, wl = self.torch, self.lrs, W.DEER
+        o = self.d["deer"]
+        N, D = wl.N, wl.D
+        out = {}
+        dt = t.from_numpy(W.uniform(0, 44, (wl.T,), 0.1, 1.0)).to(self.dev)
+        y = t.empty_like(o["u"])
+        res = {}
+
+        def ode():
+            res["k"] = L.deer_ode_solve(o["w"], o["u"], dt, o["h0"], y, eps=EPS, kmax=KMAX)[1]
+
+        ms = self._mean_ms(ode, reps)
+        k = res["k"]
+        byt = (8 + 12 * (k - 1)) * N + 4 * D * k + 4 * wl.T * k
+        out["deer_ode.solve"] = {"ms": round(ms, 4), "iters": k, "GBps": round(byt / (ms / 1e3) / 1e9, 1),
+                                 "frac": round(byt / (ms / 1e3) / 1e9 / peak, 3),
+                                 "workload": f"deer ODE form fp32 T={wl.T} B={wl.B} D={wl.D}, dt ~ U(0.1, 1)"}
+        u2 = o["u"] + 1e-3 * t.sin(t.arange(N, device=self.dev, dtype=t.float32)).view_as(o["u"])
+        guess = t.empty_like(o["u"])
+        L.deer_diag_solve(o["w"], u2, o["h0"], guess, eps=EPS, kmax=KMAX)
+
+        def warm():
+            res["k"] = L.deer_diag_solve_ex(o["w"], o["u"], o["h0"], y, y_init=guess, eps=EPS,
+                                           kmax=KMAX)["iters"]
+
+        ms = self._mean_ms(warm, reps)
+        k = res["k"]
+        byt = 12 * N * k + 4 * D * k
+        out["deer.warm"] = {"ms": round(ms, 4), "iters": k, "GBps": round(byt / (ms / 1e3) / 1e9, 1),
+                            "frac": round(byt / (ms / 1e3) / 1e9 / peak, 3),
+                            "workload": f"deer fp32 T={wl.T} B={wl.B} D={wl.D} from a nearby problem's solution"}
+        del dt, y, u2, guess
+        return out
+
     def _mean_ms(self, run, reps):
         t = self.torch
         for _ in range(3):
@@ -706,8 +745,12 @@ def main():
 
     # the next rows on the same scan, outside the step: the gradient through
     # the DEER solution at the DEER workload's size (from the step's own
-    # solution), and the LSTM cell forward and backward
-    nxt = {"deer.bwd": b.time_deer_bwd(peak)} if "deer" in b.d else {}
+    # solution), DEER's ODE form and a warm-started solve there, and the LSTM
+    # cell forward and backward
+    nxt = {}
+    if "deer" in b.d:
+        nxt["deer.bwd"] = b.time_deer_bwd(peak)
+        nxt.update(b.time_deer_variants(peak))
     nxt.update(b.time_lstm(peak))
     line["next_ops"] = nxt
 
