@@ -60,6 +60,14 @@ constexpr int WALK_P = 4;       // consecutive chunks per walker lane
 typedef unsigned long long u64;
 
 // Carry-protocol state of one launch.
+// Unroll factor of the warp-aggregate folds (a warp folds the aggregates of
+// the warps before it: a dependent chain whose shared-memory loads an unrolled
+// loop issues ahead).
+#ifndef LR_FOLD_UNROLL
+#define LR_FOLD_UNROLL 1
+#endif
+constexpr int kFoldUnroll = LR_FOLD_UNROLL;
+
 struct Carry {
     u64* agg;             // WALK: [C][n_chunks][2] packets (A, B) of every tile
     u64* inc;             // packets: state after chunk q (scan order); CHAIN stores
@@ -794,7 +802,7 @@ __device__ __forceinline__ void strip_carry(StripSmem<VEC, NW>& sm, const float 
     float st[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) st[v] = first ? (cok ? init[v] : 0.f) : carry[par][lane][v];
-#pragma unroll 1
+#pragma unroll kFoldUnroll
     for (int w = 0; w < warp; ++w)
 #pragma unroll
         for (int v = 0; v < VEC; ++v) st[v] = __fmaf_rn(sm.a[w][lane][v], st[v], sm.b[w][lane][v]);

@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
 #pragma unroll
             for (int v = 0; v < VEC; ++v)
                 stt[v] = tc.q == 0 ? (tc.cok ? init[v] : 0.f) : cs[par][lane][v];
-#pragma unroll 1
+#pragma unroll kFoldUnroll
             for (int w2 = 0; w2 < warp; ++w2)
 #pragma unroll
                 for (int v = 0; v < VEC; ++v) stt[v] = __fmaf_rn(sb.a[w2][lane][v], stt[v], sb.b[w2][lane][v]);
@@ -1045,7 +1045,7 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
             float s0[VEC];
 #pragma unroll
             for (int v = 0; v < VEC; ++v) s0[v] = carry[par][lane][v];
-#pragma unroll 1
+#pragma unroll kFoldUnroll
             for (int w2 = 0; w2 < warp; ++w2)
 #pragma unroll
                 for (int v = 0; v < VEC; ++v)

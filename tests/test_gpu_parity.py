@@ -211,6 +211,32 @@ def test_deer_per_sequence_kmax(cuda):
     assert_close("y", to_f64(r["y"]), ry, "f32")
 
 
+@pytest.mark.parametrize("shape", [(2000, 2, 256), (9000, 2, 512)])
+def test_deer_bf16_warm_start_and_per_sequence(cuda, shape):
+    """bf16 storage: the warm start converges in fewer iterations than the
+    cold start, per-sequence stopping stops the quiet sequence first, and both
+    solutions match the fp64 fixed point within the bf16 tolerance (the
+    iteration counts can differ from the oracle's by the stored rounding)."""
+    T, B, D = shape
+    wl = W.like(W.DEER, T, B, D, "bf16")
+    inp = W.make_inputs(wl, 24)
+    sc = np.asarray([0.01] + [1.5] * (B - 1), np.float32)
+    inp["u"] = W.store(W.to_f64(inp["u"], "bf16").astype(np.float32) * sc[None, :, None], "bf16")
+    dv, f = dev_inputs(inp, "bf16"), f64_inputs(inp, "bf16")
+    star = oracle.rollout_tanh(f["w"], f["u"])
+    near = W.store(oracle.rollout_tanh(f["w"], f["u"] * 1.001).astype(np.float32), "bf16")
+    guess = dev_inputs({"y": near}, "bf16")["y"]
+    warm = cuda.deer_diag_solve_ex(dv["w"], dv["u"], None, y_init=guess, eps=1e-2, kmax=20)
+    cold = cuda.deer_diag_solve_ex(dv["w"], dv["u"], None, eps=1e-2, kmax=20)
+    assert warm["status"] == cold["status"] == cuda.LR_OK
+    assert warm["iters"] < cold["iters"]
+    assert_close("y warm", to_f64(warm["y"]), star, "bf16")
+    seq = cuda.deer_diag_solve_ex(dv["w"], dv["u"], None, eps=1e-2, kmax=20, per_sequence=True)
+    assert seq["status"] == cuda.LR_OK
+    assert seq["seq_iters"][0] < max(seq["seq_iters"])
+    assert_close("y per sequence", to_f64(seq["y"]), star, "bf16")
+
+
 def test_deer_ex_global_matches_deer_diag_solve(cuda):
     inp, dv, f = _deer_case((9000, 2, 512), 10)
     y, k, resid, hist, st = cuda.deer_diag_solve(dv["w"], dv["u"], dv["h0"], eps=1e-5, kmax=20)
