@@ -44,6 +44,10 @@ struct TileCoord {
     int64_t c;       // first channel of this lane
     bool cok;        // the lane's channels are inside the problem
     int64_t t0;      // time of this thread's first row (scan order)
+    // The CTA walks one strip through every chunk in scan order (strip kernel,
+    // one strip per CTA): per-channel sums may run in registers across its
+    // tiles (Acc) and be reduced once, on the tile with q == n_chunks - 1.
+    bool acc_strip;
 };
 
 // Coordinates of the tile of chunk q (scan order) and channel tile j.
@@ -57,6 +61,7 @@ __device__ __forceinline__ TileCoord tile_coord_qj(const Geom& g, uint32_t q, ui
     tc.cok = tc.c < g.C;
     tc.tchunk = Op::REV ? g.n_chunks - 1 - tc.q : tc.q;
     tc.t0 = Op::REV ? tc.tchunk * L + (L - 1) - warp * Op::R : tc.tchunk * L + warp * Op::R;
+    tc.acc_strip = false;
     return tc;
 }
 
@@ -472,7 +477,8 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         }
         uint32_t q, j;
         strip_qj(G, m, it, q, j);
-        const TileCoord tc = tile_coord_qj<Op>(g, q, j);
+        TileCoord tc = tile_coord_qj<Op>(g, q, j);
+        tc.acc_strip = m == 1;
         typename Op::Regs regs;
         Op::load(SmemSrc<Op>{ring + st * SB, tc.tchunk * L, lane * VEC}, p, g, tc, regs);
         float A[VEC], B[VEC];

@@ -187,8 +187,13 @@ struct LstmBwdOp {
         float p1[NW][32][VEC];
     };
     static constexpr bool SCRATCH_IN_CARRY = true;
-    struct Acc {};
-    __device__ static void acc_init(Acc&) {}
+    struct Acc {
+        float sf[VEC], si[VEC], sc[VEC], so[VEC];  // bias sums over the CTA's strip (acc_strip)
+    };
+    __device__ static void acc_init(Acc& a) {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { a.sf[v] = 0.f; a.si[v] = 0.f; a.sc[v] = 0.f; a.so[v] = 0.f; }
+    }
     __device__ static bool skip(const Params&) { return false; }
     __device__ static const S* init_ptr(const Params&) { return nullptr; }  // u_T = 0
 
@@ -281,7 +286,7 @@ struct LstmBwdOp {
         for (int v = 0; v < VEC; ++v) { q0[v] = s0[v]; q1[v] = s1[v]; }
     }
     __device__ static void finish(const Params& p, const Geom& g, const TileCoord& tc,
-                                  const Regs& rg, Work& w, float (&s)[VEC], Smem& xs, Acc&) {
+                                  const Regs& rg, Work& w, float (&s)[VEC], Smem& xs, Acc& acc) {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
         float biv[VEC], bcv[VEC];
         float sum_f[VEC], sum_i[VEC], sum_c[VEC];
@@ -326,7 +331,37 @@ struct LstmBwdOp {
         }
         if (tc.tchunk == 0 && warp == NW - 1 && p.dc0 != nullptr && tc.cok)
             store_vec<S, VEC>(p.dc0 + tc.c, s);
-        // bias-gradient partials of this tile, two arrays per round
+        if (tc.acc_strip) {
+            // one strip per CTA: the sums run over its tiles in registers; a
+            // tile's partial rows are zeros and the strip's last tile writes
+            // the totals (the reduction over chunks is unchanged)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                acc.sf[v] += sum_f[v];
+                acc.si[v] += sum_i[v];
+                acc.sc[v] += sum_c[v];
+                acc.so[v] += w.sum_o[v];
+            }
+            if (tc.q != g.n_chunks - 1) {
+                if (warp == 0 && tc.cok) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        float* q = p.partials + ((int64_t)k * g.n_chunks + tc.tchunk) * g.C + tc.c;
+#pragma unroll
+                        for (int v = 0; v < VEC; ++v) q[v] = 0.f;
+                    }
+                }
+                return;
+            }
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                sum_f[v] = acc.sf[v];
+                sum_i[v] = acc.si[v];
+                sum_c[v] = acc.sc[v];
+                w.sum_o[v] = acc.so[v];
+            }
+        }
+        // bias-gradient partials of this tile (or strip), two arrays per round
         csync<NW>();  // every warp is past its reads of the carry smem
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {

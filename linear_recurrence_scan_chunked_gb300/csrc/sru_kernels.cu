@@ -174,8 +174,13 @@ struct SruBwdOp {
     // TMA kernels do that to keep two CTAs per SM): finish() writes them only
     // after a barrier that every warp reaches once it is done with those.
     static constexpr bool SCRATCH_IN_CARRY = true;
-    struct Acc {};
-    __device__ static void acc_init(Acc&) {}
+    struct Acc {
+        float sf[VEC], sr[VEC];  // bias sums over the tiles of the CTA's strip (acc_strip)
+    };
+    __device__ static void acc_init(Acc& a) {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { a.sf[v] = 0.f; a.sr[v] = 0.f; }
+    }
     __device__ static bool skip(const Params&) { return false; }
     __device__ static const S* init_ptr(const Params&) { return nullptr; }  // u_T = 0
 
@@ -258,7 +263,7 @@ struct SruBwdOp {
         }
     }
     __device__ static void finish(const Params& p, const Geom& g, const TileCoord& tc,
-                                  const Regs&, Work& w, float (&s)[VEC], Smem& xs, Acc&) {
+                                  const Regs&, Work& w, float (&s)[VEC], Smem& xs, Acc& acc) {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
         float sum_f[VEC];
 #pragma unroll
@@ -284,7 +289,25 @@ struct SruBwdOp {
         }
         if (tc.tchunk == 0 && warp == NW - 1 && p.dc0 != nullptr && tc.cok)
             store_vec<S, VEC>(p.dc0 + tc.c, s);
-        // bias-gradient partials of this tile: sum over its rows, fixed warp order
+        if (tc.acc_strip) {
+            // one strip per CTA: the sums run over its tiles in registers; a
+            // tile's partial rows are zeros and the strip's last tile writes
+            // the totals (the reduction over chunks is unchanged)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) { acc.sf[v] += sum_f[v]; acc.sr[v] += w.sum_r[v]; }
+            if (tc.q != g.n_chunks - 1) {
+                if (warp == 0 && tc.cok) {
+                    float* pfp = p.partials + tc.tchunk * g.C + tc.c;
+                    float* prp = p.partials + (g.n_chunks + tc.tchunk) * g.C + tc.c;
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) { pfp[v] = 0.f; prp[v] = 0.f; }
+                }
+                return;
+            }
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) { sum_f[v] = acc.sf[v]; w.sum_r[v] = acc.sr[v]; }
+        }
+        // bias-gradient partials of this tile (or strip): fixed warp order
         csync<NW>();  // every warp is past its reads of the carry smem
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
