@@ -257,8 +257,13 @@ struct DeerBwdOp {
     // the partial sums may overlay the carry's warp aggregates: finish() writes
     // them only after a barrier that every warp reaches once done with those
     static constexpr bool SCRATCH_IN_CARRY = true;
-    struct Acc {};
-    __device__ static void acc_init(Acc&) {}
+    struct Acc {
+        float sw[VEC];  // dw sums over a run of tiles (acc_run)
+    };
+    __device__ static void acc_init(Acc& a) {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) a.sw[v] = 0.f;
+    }
     __device__ static bool skip(const Params&) { return false; }
     __device__ static const S* init_ptr(const Params&) { return nullptr; }  // u_T = 0
 
@@ -313,7 +318,7 @@ struct DeerBwdOp {
         }
     }
     __device__ static void finish(const Params& p, const Geom& g, const TileCoord& tc,
-                                  const Regs& rg, Work& w, float (&s)[VEC], Smem& xs, Acc&) {
+                                  const Regs& rg, Work& w, float (&s)[VEC], Smem& xs, Acc& acc) {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
         float sum[VEC];
 #pragma unroll
@@ -335,7 +340,28 @@ struct DeerBwdOp {
         // row 0 is the last row of the last warp of time chunk 0: s = u_0 = dh0
         if (tc.tchunk == 0 && warp == NW - 1 && p.dh0 != nullptr && tc.cok)
             store_vec<S, VEC>(p.dh0 + tc.c, s);
-        // dw partials of this tile: sum over its rows, fixed warp order
+        if (tc.acc_run) {
+            // a run of tiles of these channels through this CTA: the sums run
+            // over it in registers; a tile's partial row is zeros and the
+            // run's last tile writes the total (the reduction over chunks is
+            // unchanged)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) acc.sw[v] += sum[v];
+            if (!tc.acc_flush) {
+                if (warp == 0 && tc.cok) {
+                    float* pp = p.partials + tc.tchunk * g.C + tc.c;
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) pp[v] = 0.f;
+                }
+                return;
+            }
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                sum[v] = acc.sw[v];
+                acc.sw[v] = 0.f;
+            }
+        }
+        // dw partials of this tile (or run): fixed warp order
         csync<NW>();  // every warp is past its reads of the carry smem
 #pragma unroll
         for (int v = 0; v < VEC; ++v) xs.pw[warp][lane][v] = sum[v];

@@ -44,10 +44,13 @@ struct TileCoord {
     int64_t c;       // first channel of this lane
     bool cok;        // the lane's channels are inside the problem
     int64_t t0;      // time of this thread's first row (scan order)
-    // The CTA walks one strip through every chunk in scan order (strip kernel,
-    // one strip per CTA): per-channel sums may run in registers across its
-    // tiles (Acc) and be reduced once, on the tile with q == n_chunks - 1.
-    bool acc_strip;
+    // A run of tiles of the same channels in scan order goes through this CTA
+    // (strip kernel with one strip per CTA: the whole strip; segmented walker
+    // kernel: a segment's consume pass): per-channel sums may run in registers
+    // across the run (Acc, acc_run) and be reduced once, on its last tile
+    // (acc_flush).
+    bool acc_run;
+    bool acc_flush;
 };
 
 // Coordinates of the tile of chunk q (scan order) and channel tile j.
@@ -61,7 +64,8 @@ __device__ __forceinline__ TileCoord tile_coord_qj(const Geom& g, uint32_t q, ui
     tc.cok = tc.c < g.C;
     tc.tchunk = Op::REV ? g.n_chunks - 1 - tc.q : tc.q;
     tc.t0 = Op::REV ? tc.tchunk * L + (L - 1) - warp * Op::R : tc.tchunk * L + warp * Op::R;
-    tc.acc_strip = false;
+    tc.acc_run = false;
+    tc.acc_flush = false;
     return tc;
 }
 
@@ -478,7 +482,8 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         uint32_t q, j;
         strip_qj(G, m, it, q, j);
         TileCoord tc = tile_coord_qj<Op>(g, q, j);
-        tc.acc_strip = m == 1;
+        tc.acc_run = m == 1;
+        tc.acc_flush = m == 1 && (int64_t)q == g.n_chunks - 1;
         typename Op::Regs regs;
         Op::load(SmemSrc<Op>{ring + st * SB, tc.tchunk * L, lane * VEC}, p, g, tc, regs);
         float A[VEC], B[VEC];
@@ -821,7 +826,9 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
             const bool valid = has_con && q < (uint32_t)g.n_chunks;
             if (!top(valid)) { stop = true; break; }
             if (!valid) continue;
-            const TileCoord tc = tile_coord_qj<Op>(g, q, j_c);
+            TileCoord tc = tile_coord_qj<Op>(g, q, j_c);
+            tc.acc_run = true;  // the segment's chunks, in scan order
+            tc.acc_flush = c + 1 == sg.seg || (int64_t)q + 1 == g.n_chunks;
             typename Op::Regs regs;
             typename Op::Work w;
             Op::load(SmemSrc<Op>{ring + (it % ST) * SB, tc.tchunk * L, lane * VEC}, p, g, tc, regs);

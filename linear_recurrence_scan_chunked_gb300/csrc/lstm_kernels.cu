@@ -188,7 +188,7 @@ struct LstmBwdOp {
     };
     static constexpr bool SCRATCH_IN_CARRY = true;
     struct Acc {
-        float sf[VEC], si[VEC], sc[VEC], so[VEC];  // bias sums over the CTA's strip (acc_strip)
+        float sf[VEC], si[VEC], sc[VEC], so[VEC];  // bias sums over a run of tiles (acc_run)
     };
     __device__ static void acc_init(Acc& a) {
 #pragma unroll
@@ -331,10 +331,11 @@ struct LstmBwdOp {
         }
         if (tc.tchunk == 0 && warp == NW - 1 && p.dc0 != nullptr && tc.cok)
             store_vec<S, VEC>(p.dc0 + tc.c, s);
-        if (tc.acc_strip) {
-            // one strip per CTA: the sums run over its tiles in registers; a
-            // tile's partial rows are zeros and the strip's last tile writes
-            // the totals (the reduction over chunks is unchanged)
+        if (tc.acc_run) {
+            // a run of tiles of these channels through this CTA: the sums run
+            // over it in registers; a tile's partial rows are zeros and the
+            // run's last tile writes the totals (the reduction over chunks is
+            // unchanged)
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
                 acc.sf[v] += sum_f[v];
@@ -342,7 +343,7 @@ struct LstmBwdOp {
                 acc.sc[v] += sum_c[v];
                 acc.so[v] += w.sum_o[v];
             }
-            if (tc.q != g.n_chunks - 1) {
+            if (!tc.acc_flush) {
                 if (warp == 0 && tc.cok) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -359,6 +360,7 @@ struct LstmBwdOp {
                 sum_i[v] = acc.si[v];
                 sum_c[v] = acc.sc[v];
                 w.sum_o[v] = acc.so[v];
+                acc.sf[v] = acc.si[v] = acc.sc[v] = acc.so[v] = 0.f;
             }
         }
         // bias-gradient partials of this tile (or strip), two arrays per round

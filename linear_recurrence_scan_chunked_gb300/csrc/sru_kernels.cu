@@ -175,7 +175,7 @@ struct SruBwdOp {
     // after a barrier that every warp reaches once it is done with those.
     static constexpr bool SCRATCH_IN_CARRY = true;
     struct Acc {
-        float sf[VEC], sr[VEC];  // bias sums over the tiles of the CTA's strip (acc_strip)
+        float sf[VEC], sr[VEC];  // bias sums over a run of tiles (acc_run)
     };
     __device__ static void acc_init(Acc& a) {
 #pragma unroll
@@ -289,13 +289,14 @@ struct SruBwdOp {
         }
         if (tc.tchunk == 0 && warp == NW - 1 && p.dc0 != nullptr && tc.cok)
             store_vec<S, VEC>(p.dc0 + tc.c, s);
-        if (tc.acc_strip) {
-            // one strip per CTA: the sums run over its tiles in registers; a
-            // tile's partial rows are zeros and the strip's last tile writes
-            // the totals (the reduction over chunks is unchanged)
+        if (tc.acc_run) {
+            // a run of tiles of these channels through this CTA: the sums run
+            // over it in registers; a tile's partial rows are zeros and the
+            // run's last tile writes the totals (the reduction over chunks is
+            // unchanged)
 #pragma unroll
             for (int v = 0; v < VEC; ++v) { acc.sf[v] += sum_f[v]; acc.sr[v] += w.sum_r[v]; }
-            if (tc.q != g.n_chunks - 1) {
+            if (!tc.acc_flush) {
                 if (warp == 0 && tc.cok) {
                     float* pfp = p.partials + tc.tchunk * g.C + tc.c;
                     float* prp = p.partials + (g.n_chunks + tc.tchunk) * g.C + tc.c;
@@ -305,7 +306,12 @@ struct SruBwdOp {
                 return;
             }
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) { sum_f[v] = acc.sf[v]; w.sum_r[v] = acc.sr[v]; }
+            for (int v = 0; v < VEC; ++v) {
+                sum_f[v] = acc.sf[v];
+                w.sum_r[v] = acc.sr[v];
+                acc.sf[v] = 0.f;
+                acc.sr[v] = 0.f;
+            }
         }
         // bias-gradient partials of this tile (or strip): fixed warp order
         csync<NW>();  // every warp is past its reads of the carry smem
