@@ -189,10 +189,12 @@ class Bench:
                           o["c0"], out=o["grad"])
                 launches += 3  # fused backward + two bias-reduction stages
             else:
-                _, k, _, _, st = L.deer_diag_solve(o["w"], o["u"], o["h0"], o["y"], eps=EPS, kmax=KMAX)
+                _, k, _, hist, st = L.deer_diag_solve(o["w"], o["u"], o["h0"], o["y"], eps=EPS,
+                                                      kmax=KMAX)
                 if st != L.LR_OK:
                     raise RuntimeError(f"DEER did not converge (status {st})")
                 self.k_last = k
+                self.hist_last = hist
                 # iterations are enqueued four at a time; those after the
                 # stopping test return at once but are still launches
                 launches += min(KMAX, -(-k // 4) * 4)
@@ -494,6 +496,30 @@ class OracleSampler:
             el += sub.N * k
         return el, time.perf_counter() - t0, k
 
+    def run_single_thread(self):
+        """The same rows on one thread, each sample cut to 1/threads of its
+        channels (about the same wall time): elements/s per row."""
+        rates = {}
+        n0 = self.oracle.num_threads()
+        self.oracle.set_num_threads(1)
+        try:
+            for name, wl, passes in ROWS:
+                sub, inp = self.subs[name]
+                if wl.kind == "sru":
+                    nb = max(1, sub.B // self.nth)
+                    cut = W.like(sub, B=nb)
+                    ci = {k: (v if np.ndim(v) == 1 else v[:, :nb] if np.ndim(v) == 3 else v[:nb])
+                          for k, v in inp.items()}
+                else:
+                    nd = max(1, sub.D // self.nth)
+                    cut = W.like(sub, D=nd)
+                    ci = {k: (v[:nd] if k == "w" else v[..., :nd]) for k, v in inp.items()}
+                el, dt, _ = self._run(wl, passes, (cut, ci))
+                rates[name] = el / dt
+        finally:
+            self.oracle.set_num_threads(n0)
+        return rates
+
     def run(self):
         """One pass over the samples: (elements/s per row, description, DEER K)."""
         rates, desc, kd = {}, [], 1
@@ -599,7 +625,9 @@ def run_reference(args, ws, rank):
 #   long   scan_long fp32 1x262144x128 (T reduced from 2^20): fwd
 #   sru    SRU fp32 32x512x1024 (T reduced from 2048): fwd, bwd, 2 bias kernels
 #   lstm   LSTM cell fp32 32x512x1024 (T reduced from 2048): fwd, bwd, 2 bias kernels
-PROFILE_CASES = ("deer", "large", "long", "sru", "lstm")
+#   deerbwd  DEER backward fp32 4x65536x256 (full size) from a 3-iteration solve:
+#          k_seg + k_seg1 x 2 (the solve), then k_seg (backward) and 2 dw kernels
+PROFILE_CASES = ("deer", "large", "long", "sru", "lstm", "deerbwd")
 
 
 def profile_case(name):
@@ -617,6 +645,12 @@ def profile_case(name):
     if name == "deer":
         inp = W.make_inputs(W.DEER, 0)
         L.deer_diag_solve(dev(inp, "w"), dev(inp, "u"), None, None, eps=0.0, kmax=3)
+    elif name == "deerbwd":
+        inp = W.make_inputs(W.DEER, 0)
+        w, u = dev(inp, "w"), dev(inp, "u")
+        y = L.deer_diag_solve(w, u, None, None, eps=0.0, kmax=3)[0]
+        dy = torch.from_numpy(W.normal(0, 90, u.shape)).cuda()
+        L.deer_diag_bwd(w, y, dy, None)
     elif name == "large":
         inp = W.make_inputs(dataclasses.replace(W.SCAN_BF16, T=2048), 0)
         a, b, g = dev(inp, "a"), dev(inp, "b"), dev(inp, "g")
@@ -741,6 +775,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "f32 compute (f32 and bf16 storage)",
             "data": "synthetic", "config": config_dict(),
             "hbm_GBps": round(gbs, 1), "hbm_frac": round(gbs / peak, 4), "deer_iters": k_med,
+            "deer_resid_history": [float(f"{r:.3e}") for r in getattr(b, "hist_last", [])],
             "gpu_launches": launches, "clocks": clk.summary(), "roofline": roof, "ops": ops}
 
     # the next rows on the same scan, outside the step: the gradient through
@@ -772,9 +807,14 @@ def main():
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         smp = OracleSampler(args.cpu_budget)
         rates, desc, _ = smp.run()
+        r1 = smp.run_single_thread()
         line["cpu_baseline"] = {"value": step_rate_from_rows(rates, k_med), "unit": UNIT,
                                 "cores": smp.nth, "kind": "oracle",
-                                "sample": desc + f"; extrapolated to the step mix with K={k_med}"}
+                                "sample": desc + f"; extrapolated to the step mix with K={k_med}",
+                                "single_thread": {"value": step_rate_from_rows(r1, k_med),
+                                                  "unit": UNIT, "cores": 1,
+                                                  "sample": "the same samples cut to 1/"
+                                                            f"{smp.nth} of their channels"}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     barrier(ws)
