@@ -1,6 +1,9 @@
-// lr_persist.cuh -- the persistent kernels shared by all five operations:
-//   k_strip  (wide problems: channel strips walked through time, TMA-staged),
+// lr_persist.cuh -- the persistent kernels shared by every operation:
+//   k_strip  (wide problems: channel strips walked through time, TMA-staged;
+//             a one-barrier-per-tile variant for operations that opt in),
 //   k_seg    (long, narrow problems: walker protocol over segments, TMA-staged),
+//   k_seg1   (k_seg's consume pass alone, for launches whose segment
+//             aggregates the previous launch published: DEER iterations),
 //   k_tchain (chain protocol, TMA-staged, for what is neither),
 //   k_stream (walker protocol through registers),
 //   k_chain  (chain protocol through registers: scalar / unaligned paths),
@@ -26,7 +29,11 @@
 //                                 rows in scan order; with side = true it also
 //                                 writes the outputs that need no carry
 //   finish(p, g, tc, regs, w, s, sm, acc)  output pass from the entering state s
+//                                 (tc.acc_run / acc_flush: per-channel sums may
+//                                 run in acc across a run of tiles, see TileCoord)
 //   at_exit(p, sm, acc)           once per tile CTA after its last tile
+// and optionally NEXT_AGG / next_agg(p) (lr_common.cuh: the next launch's
+// aggregates, folded in finish) and STRIP_ONE_BARRIER.
 #pragma once
 
 #include <string.h>
