@@ -328,16 +328,18 @@ int64_t lr_workspace_bytes(void);
 int lr_test_lookback_timeout(uint32_t spin_limit, void* stream);
 
 /*
- * Test hook for the activations of the fused kernels: tanh_out[i] = tanh(x[i])
- * and sigmoid_out[i] = 1 / (1 + exp(-x[i])) as the SRU and DEER kernels
- * evaluate them (exponential forms on the hardware exponential; the pages
- * name the functions -- [P1] SRU paragraph, [P4] "核心原理" -- not how to
- * evaluate them).  x, tanh_out, sigmoid_out: n fp32 device values each,
- * caller-owned.  Asynchronous on `stream`.  Returns LR_ERR_INVALID_ARG for
- * n < 0 or a null pointer with n > 0.
+ * Test hook for the activations of the fused kernels: tanh_out[i] = tanh(x[i]),
+ * sigmoid_out[i] = 1 / (1 + exp(-x[i])) and expm1_out[i] = exp(x[i]) - 1 as the
+ * SRU, LSTM and DEER kernels evaluate them (tanh and sigmoid in exponential
+ * forms on the hardware exponential; e^x - 1 by its Taylor series near 0 and
+ * the hardware exponential elsewhere -- the pages name the functions, [P1]
+ * SRU paragraph, [P4] "核心原理" and "监控与调优", not how to evaluate them).
+ * x, tanh_out, sigmoid_out: n fp32 device values each, caller-owned;
+ * expm1_out likewise or NULL (not computed).  Asynchronous on `stream`.
+ * Returns LR_ERR_INVALID_ARG for n < 0 or a null required pointer with n > 0.
  */
-int lr_test_activations(const float* x, float* tanh_out, float* sigmoid_out, int64_t n,
-                        void* stream);
+int lr_test_activations(const float* x, float* tanh_out, float* sigmoid_out, float* expm1_out,
+                        int64_t n, void* stream);
 
 #ifdef __cplusplus
 }

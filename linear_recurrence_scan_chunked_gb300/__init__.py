@@ -67,7 +67,7 @@ def load():
     lib.lr_cuda_error_string.restype = ctypes.c_char_p
     lib.lr_workspace_bytes.restype = I64
     lib.lr_test_lookback_timeout.argtypes = [ctypes.c_uint32, P]
-    lib.lr_test_activations.argtypes = [P, P, P, I64, P]
+    lib.lr_test_activations.argtypes = [P, P, P, P, I64, P]
     for f in ("lr_scan_fwd", "lr_scan_bwd", "sru_fwd", "sru_bwd", "deer_diag_solve", "deer_diag_bwd",
               "lr_last_error", "lr_test_lookback_timeout", "lr_test_activations"):
         getattr(lib, f).restype = I
@@ -347,14 +347,16 @@ def workspace_bytes() -> int:
     return int(load().lr_workspace_bytes())
 
 
-def test_activations(x, stream=None):
-    """tanh and sigmoid of a contiguous fp32 CUDA tensor as the fused kernels
-    evaluate them. Returns (tanh, sigmoid)."""
+def test_activations(x, stream=None, with_expm1=False):
+    """tanh and sigmoid (and e^x - 1) of a contiguous fp32 CUDA tensor as the
+    fused kernels evaluate them. Returns (tanh, sigmoid) or (tanh, sigmoid,
+    expm1)."""
     if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
         raise ValueError("x must be a contiguous fp32 CUDA tensor")
     th, sg = torch.empty_like(x), torch.empty_like(x)
-    _check(load().lr_test_activations(_p(x), _p(th), _p(sg), x.numel(), _stream(stream)))
-    return th, sg
+    em = torch.empty_like(x) if with_expm1 else None
+    _check(load().lr_test_activations(_p(x), _p(th), _p(sg), _p(em), x.numel(), _stream(stream)))
+    return (th, sg, em) if with_expm1 else (th, sg)
 
 
 def test_lookback_timeout(spin_limit: int = 1000, stream=None) -> int:

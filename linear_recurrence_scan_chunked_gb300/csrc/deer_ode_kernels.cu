@@ -13,8 +13,11 @@
 //     z_t = f(ytil_{t-1}, u_t) + G_t ytil_{t-1},
 // and solves dy/dt + G_t y = z_t exactly over the step: the scan element is
 //     (a_t, b_t) = (exp(-G_t dt_t), (1 - exp(-G_t dt_t)) / G_t z_t)
-// (b_t = dt_t z_t when G_t = 0), both from one expm1f.  The epilogue writes y
-// and folds max |y - yold| as the tanh form does.
+// (b_t = dt_t z_t when G_t = 0), both from one e^x - 1 (act_expm1).  The
+// epilogue writes y and folds max |y - yold| as the tanh form does, and on the
+// segmented walker kernel also builds the next iteration's coefficients at
+// row t from the y_{t-1} just computed (as stored) and folds them into the next
+// iteration's aggregates, which then needs no reduce pass (NextAgg).
 #include "lr_act.cuh"
 #include "lr_launch.h"
 #include "lr_persist.cuh"
@@ -33,6 +36,7 @@ struct DeerOdeParams {
     const uint32_t* prev_resid;  // residual of the previous iteration (nullptr: first)
     float eps;
     unsigned long long* clamps;  // clamped G evaluations of this iteration
+    NextAgg nx;                  // next iteration's aggregates (segmented walker kernel only)
 };
 
 constexpr float kOdeGClamp = 10.f;
@@ -44,6 +48,7 @@ struct DeerOdeOp {
     static constexpr bool REV = false;
     static constexpr int IN_ARRAYS = 2;  // u, previous iterate
     static constexpr bool SCRATCH_IN_CARRY = false;
+    static constexpr bool NEXT_AGG = true;
     using Params = DeerOdeParams<S>;
     struct Regs {
         Pack<S, VEC> u[R];
@@ -51,7 +56,9 @@ struct DeerOdeOp {
     };
     struct Work {
         float J[R][VEC], Rh[R][VEC];  // (a_t, b_t)
+        float DT[R];                  // step lengths of the rows
         uint32_t ncl;                 // clamps among this thread's rows (counted once per element)
+        float NA[VEC], NB[VEC];       // next iteration's aggregate of this thread's rows
     };
     struct Smem {
         uint32_t mx[NW];
@@ -71,6 +78,26 @@ struct DeerOdeOp {
         return stop;
     }
     __device__ static const S* init_ptr(const Params& p) { return p.h0; }
+    __host__ __device__ static NextAgg next_agg(const Params& p) { return p.nx; }
+
+    // The step's coefficients from the linearisation point yt (the state
+    // entering the step), the input and the step length: clamps G, counts it.
+    __device__ static void coeffs(float wv, float yt, float uv, float dtt, float& a, float& b,
+                                  uint32_t& ncl) {
+        const float th = act_tanh(wv * yt + uv);
+        float gv = 1.f - wv * (1.f - th * th);
+        if (gv > kOdeGClamp) {  // (a NaN fails both tests and stays NaN)
+            gv = kOdeGClamp;
+            ++ncl;
+        } else if (gv < -kOdeGClamp) {
+            gv = -kOdeGClamp;
+            ++ncl;
+        }
+        const float z = (th - yt) + gv * yt;
+        const float em = act_expm1(-gv * dtt);  // exp(-G dt) - 1
+        a = 1.f + em;
+        b = (gv != 0.f ? __fdividef(-em, gv) : dtt) * z;
+    }
 
     static constexpr int TMA_N = 2;  // staged: u, previous iterate (rows t0-1 .. t0+L-1)
     __host__ __device__ static constexpr int tma_shift(int k) { return k == 1 ? -1 : 0; }
@@ -115,23 +142,15 @@ struct DeerOdeOp {
             const int64_t t = tc.t0 + r;
             const bool ok = tc.cok && t < g.T;
             const float dtt = ok ? __ldg(p.dt + t) : 0.f;
+            w.DT[r] = dtt;
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
-                const float yt = rg.yo[r].get(v);
-                const float th = act_tanh(wv[v] * yt + rg.u[r].get(v));
-                float gv = 1.f - wv[v] * (1.f - th * th);
-                if (gv > kOdeGClamp) {  // (a NaN fails both tests and stays NaN)
-                    gv = kOdeGClamp;
-                    ncl += ok ? 1u : 0u;
-                } else if (gv < -kOdeGClamp) {
-                    gv = -kOdeGClamp;
-                    ncl += ok ? 1u : 0u;
-                }
-                const float z = (th - yt) + gv * yt;
-                const float em = expm1f(-gv * dtt);  // exp(-G dt) - 1
-                const float phi = gv != 0.f ? -em / gv : dtt;
-                w.J[r][v] = ok ? 1.f + em : 1.f;
-                w.Rh[r][v] = ok ? phi * z : 0.f;
+                float a, b;
+                uint32_t n = 0;
+                coeffs(wv[v], rg.yo[r].get(v), rg.u[r].get(v), dtt, a, b, n);
+                ncl += ok ? n : 0u;
+                w.J[r][v] = ok ? a : 1.f;
+                w.Rh[r][v] = ok ? b : 0.f;
                 B[v] = w.J[r][v] * B[v] + w.Rh[r][v];
                 A[v] *= w.J[r][v];
             }
@@ -140,9 +159,27 @@ struct DeerOdeOp {
     }
     __device__ static void finish(const Params& p, const Geom& g, const TileCoord& tc,
                                   const Regs& rg, Work& w, float (&s)[VEC], Smem&, Acc& acc) {
+        const bool nxt = p.nx.agg != nullptr;
+        float wv[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { wv[v] = 0.f; w.NA[v] = 1.f; w.NB[v] = 0.f; }
+        if (nxt && tc.cok) load_param<VEC>(p.w + tc.c % g.D, wv);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int64_t t = tc.t0 + r;
+            if (nxt && tc.cok && t < g.T) {
+                // next iteration, row t: linearised at y_{t-1} (s, as stored)
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    float yp = s[v];
+                    if constexpr (sizeof(S) == 2) yp = bf_lo(bf_bits(yp));
+                    float a, b;
+                    uint32_t n = 0;  // counted by the next iteration itself
+                    coeffs(wv[v], yp, rg.u[r].get(v), w.DT[r], a, b, n);
+                    w.NB[v] = a * w.NB[v] + b;
+                    w.NA[v] *= a;
+                }
+            }
 #pragma unroll
             for (int v = 0; v < VEC; ++v) s[v] = w.J[r][v] * s[v] + w.Rh[r][v];
             if (tc.cok && t < g.T) {
@@ -197,21 +234,21 @@ template <typename S>
 static cudaError_t deer_ode_s(bool vec, const float* w, const void* u, const float* dt,
                               const void* h0, const void* yold, void* ynew, uint32_t* resid,
                               const uint32_t* prev_resid, float eps, unsigned long long* clamps,
-                              const Geom& g, const Carry& cr, cudaStream_t s) {
+                              const NextAgg& nx, const Geom& g, const Carry& cr, cudaStream_t s) {
     const DeerOdeParams<S> p{w, (const S*)u, dt, (const S*)h0, (const S*)yold, (S*)ynew,
-                             resid, prev_resid, eps, clamps};
+                             resid, prev_resid, eps, clamps, nx};
     return vec ? deer_ode_t<S, true>(p, g, cr, s) : deer_ode_t<S, false>(p, g, cr, s);
 }
 
 cudaError_t launch_deer_ode_iter(int dtype, bool vec, const float* w, const void* u,
                                  const float* dt, const void* h0, const void* yold, void* ynew,
                                  uint32_t* resid, const uint32_t* prev_resid, float eps,
-                                 unsigned long long* clamps, const Geom& g, const Carry& cr,
-                                 cudaStream_t s) {
+                                 unsigned long long* clamps, const NextAgg& nx, const Geom& g,
+                                 const Carry& cr, cudaStream_t s) {
     return dtype == 0 ? deer_ode_s<float>(vec, w, u, dt, h0, yold, ynew, resid, prev_resid, eps,
-                                          clamps, g, cr, s)
+                                          clamps, nx, g, cr, s)
                       : deer_ode_s<__nv_bfloat16>(vec, w, u, dt, h0, yold, ynew, resid,
-                                                  prev_resid, eps, clamps, g, cr, s);
+                                                  prev_resid, eps, clamps, nx, g, cr, s);
 }
 
 }  // namespace lrs

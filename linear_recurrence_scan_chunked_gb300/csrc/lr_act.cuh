@@ -1,7 +1,9 @@
 // lr_act.cuh -- the activations of the fused producers and epilogues: the
 // logistic sigmoid (SRU gates, page [P1] "CUDA并行化RNN训练：从O(T)到O(log T)的
-// 工程实践与参数调优", SRU paragraph) and tanh (SRU output and cell gradient;
-// DEER's diagonal tanh RNN, page [P4], section "核心原理").
+// 工程实践与参数调优", SRU paragraph; LSTM gates), tanh (SRU output and cell
+// gradient; LSTM candidate and output; DEER's diagonal tanh RNN, page [P4],
+// section "核心原理") and e^x - 1 (DEER's ODE form, page [P4], section
+// "监控与调优").
 //
 // Both are written from their exponential forms,
 //     sigmoid(z) = 1 / (1 + e^{-z}),
@@ -29,6 +31,26 @@ __device__ __forceinline__ float act_sigmoid(float z) {
 __device__ __forceinline__ float act_tanh(float x) {
     const float t = 1.f - __fdividef(2.f, __expf(2.f * fabsf(x)) + 1.f);
     return copysignf(t, x);
+}
+
+// e^x - 1 without the cancellation of e^x - 1 near 0 (DEER's ODE form,
+// exp(-G dt) and (1 - exp(-G dt)) / G): below |x| = 1/4 the Taylor series
+// x (1 + x/2 (1 + x/3 (... (1 + x/8)))) -- its first omitted term, x^9/9!, is
+// under 1e-11 |x| there -- and elsewhere e^x - 1 from the hardware
+// exponential, where |e^x - 1| > 0.22 keeps the subtraction exact to a few
+// ulp.  NaN stays NaN, -inf gives -1, +inf gives +inf.
+__device__ __forceinline__ float act_expm1(float x) {
+    if (fabsf(x) < 0.25f) {
+        float p = fmaf(x, 0.125f, 1.f);
+        p = fmaf(x * (1.f / 7.f), p, 1.f);
+        p = fmaf(x * (1.f / 6.f), p, 1.f);
+        p = fmaf(x * 0.2f, p, 1.f);
+        p = fmaf(x * 0.25f, p, 1.f);
+        p = fmaf(x * (1.f / 3.f), p, 1.f);
+        p = fmaf(x * 0.5f, p, 1.f);
+        return x * p;
+    }
+    return __expf(x) - 1.f;
 }
 
 }  // namespace lrs

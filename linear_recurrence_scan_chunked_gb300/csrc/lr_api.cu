@@ -47,11 +47,12 @@ bool tma_encode(CUtensorMap* m, const void* ptr, int dtype, int64_t T, int64_t C
 
 // Test hook kernel: the activations the fused kernels use, elementwise.
 __global__ void k_test_act(const float* __restrict__ x, float* __restrict__ th,
-                           float* __restrict__ sg, int64_t n) {
+                           float* __restrict__ sg, float* __restrict__ em, int64_t n) {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
         th[i] = act_tanh(x[i]);
         sg[i] = act_sigmoid(x[i]);
+        if (em) em[i] = act_expm1(x[i]);
     }
 }
 
@@ -409,6 +410,33 @@ static float bits_f(uint32_t b) {
     return f;
 }
 
+// One-pass iterations (operations with next-launch aggregates on the
+// segmented walker kernel): every launch also publishes the next one's
+// segment aggregates, with the next launch's epoch, into the second of two
+// aggregate buffers after the packets plan() lays out; from the second
+// iteration on a launch has no reduce pass.  onepass_begin sizes the packets
+// and keeps the epoch from wrapping inside the solve (plan() adds one per
+// launch); onepass_args points launch kk at its two buffers.
+static int onepass_begin(DevWS& ws, Op op, int dtype, bool vec, int64_t T, int64_t C, int kmax,
+                         cudaStream_t s, CarryPlan* cp, bool* on) {
+    *cp = carry_plan(op, dtype, vec, use_tma(dtype, vec, T, C), T, C);
+    *on = cp->mode == CARRY_WALK && cp->tma;
+    if (!*on) return LR_OK;
+    TRY(grow(ws, &ws.pk, &ws.pk_cap, cp->inc_elems + 2 * cp->agg_elems, true));
+    if (ws.epoch > 0xFFFFFFFFu - (uint32_t)(kmax + 8)) {
+        CK(cudaMemsetAsync(ws.pk, 0, ws.pk_cap * sizeof(u64), s));
+        ws.epoch = 0;
+    }
+    return LR_OK;
+}
+
+static NextAgg onepass_args(DevWS& ws, const CarryPlan& cp, int kk, Carry& cr) {
+    u64* agg0 = ws.pk + cp.inc_elems;  // where plan() put cr.agg
+    cr.agg = (kk & 1) ? agg0 : agg0 + cp.agg_elems;
+    return NextAgg{(kk & 1) ? agg0 + cp.agg_elems : agg0, cr.epoch + 1 /* the next plan()'s */,
+                   kk > 1 ? 1u : 0u};
+}
+
 int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void* y_init, void* y,
                        int64_t B, int64_t T, int64_t D, float eps, int kmax, int per_sequence,
                        int* iters_out, float* resid_out, float* resid_hist, int* seq_iters,
@@ -455,19 +483,9 @@ int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void
         sq_all = reinterpret_cast<uint32_t*>(sq_iters + B);
     }
     TRY(enter(*ws, s));
-    // On the segmented walker kernel each iteration also publishes the next
-    // one's segment aggregates (two buffers after the packets plan() lays
-    // out, alternating), tagged with the next launch's epoch; from the second
-    // iteration on a launch has no reduce pass.
-    const CarryPlan cp = carry_plan(OP_DEER, dtype, vec, use_tma(dtype, vec, T, B * D), T, B * D);
-    const bool onepass = cp.mode == CARRY_WALK && cp.tma;
-    if (onepass) {
-        TRY(grow(*ws, &ws->pk, &ws->pk_cap, cp.inc_elems + 2 * cp.agg_elems, true));
-        if (ws->epoch > 0xFFFFFFFFu - (uint32_t)(kmax + 8)) {  // no epoch wrap inside the solve
-            CK(cudaMemsetAsync(ws->pk, 0, ws->pk_cap * sizeof(u64), s));
-            ws->epoch = 0;
-        }
-    }
+    CarryPlan cp;
+    bool onepass;
+    TRY(onepass_begin(*ws, OP_DEER, dtype, vec, T, B * D, kmax, s, &cp, &onepass));
     if (per_sequence) CK(cudaMemsetAsync(ws->seq, 0, sq_words * sizeof(uint32_t), s));
     uint32_t* slots = ws->words + 2;
     CK(cudaMemsetAsync(slots, 0, sizeof(uint32_t) * kmax, s));
@@ -495,14 +513,7 @@ int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void
             Geom g;
             Carry cr;
             TRY(plan(*ws, OP_DEER, dtype, vec, T, B * D, D, &g, &cr, s));
-            NextAgg nx{nullptr, 0u, 0u};
-            if (onepass) {
-                u64* agg0 = ws->pk + cp.inc_elems;  // where plan() put cr.agg
-                cr.agg = (kk & 1) ? agg0 : agg0 + cp.agg_elems;
-                nx.agg = (kk & 1) ? agg0 + cp.agg_elems : agg0;
-                nx.epoch = cr.epoch + 1;  // the next plan() call's
-                nx.pre = kk > 1 ? 1u : 0u;
-            }
+            const NextAgg nx = onepass ? onepass_args(*ws, cp, kk, cr) : NextAgg{nullptr, 0u, 0u};
             DeerSeq sq{nullptr, nullptr, nullptr};
             if (per_sequence) sq = DeerSeq{sq_slots + (size_t)(kk - 1) * B, sq_done, sq_all};
             CK(launch_deer_iter(dtype, vec, w, u, h0, kk == 1 ? y0 : buf[(kk - 1) & 1],
@@ -608,6 +619,9 @@ int deer_ode_solve(const float* w, const void* u, const float* dt, const void* h
         ws->ybuf_cap = cap;
     }
     TRY(enter(*ws, s));
+    CarryPlan cp;
+    bool onepass;
+    TRY(onepass_begin(*ws, OP_DEER_ODE, dtype, vec, T, B * D, kmax, s, &cp, &onepass));
     uint32_t* slots = ws->words + 2;
     CK(cudaMemsetAsync(slots, 0, sizeof(uint32_t) * kmax, s));
     CK(cudaMemsetAsync(ws->clamps, 0, sizeof(unsigned long long) * kmax, s));
@@ -626,10 +640,11 @@ int deer_ode_solve(const float* w, const void* u, const float* dt, const void* h
             Geom g;
             Carry cr;
             TRY(plan(*ws, OP_DEER_ODE, dtype, vec, T, B * D, D, &g, &cr, s));
+            const NextAgg nx = onepass ? onepass_args(*ws, cp, kk, cr) : NextAgg{nullptr, 0u, 0u};
             CK(launch_deer_ode_iter(dtype, vec, w, u, dt, h0, kk == 1 ? nullptr : buf[(kk - 1) & 1],
                                     buf[kk & 1], slots + (kk - 1),
                                     kk == 1 ? nullptr : slots + (kk - 2), eps,
-                                    ws->clamps + (kk - 1), g, cr, s));
+                                    ws->clamps + (kk - 1), nx, g, cr, s));
         }
         CK(cudaMemcpyAsync(ws->host_word + first, slots + first, sizeof(uint32_t) * nb,
                            cudaMemcpyDeviceToHost, s));
@@ -721,13 +736,14 @@ int64_t lr_workspace_bytes(void) {
     return g_ws[dev]->bytes;
 }
 
-int lr_test_activations(const float* x, float* tanh_out, float* sigmoid_out, int64_t n,
-                        void* stream) {
+int lr_test_activations(const float* x, float* tanh_out, float* sigmoid_out, float* expm1_out,
+                        int64_t n, void* stream) {
     GUARD;
     if (n < 0 || (n > 0 && (!x || !tanh_out || !sigmoid_out))) return LR_ERR_INVALID_ARG;
     if (n == 0) return LR_OK;
     const int64_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
-    k_test_act<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(x, tanh_out, sigmoid_out, n);
+    k_test_act<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(x, tanh_out, sigmoid_out,
+                                                                    expm1_out, n);
     CK(cudaGetLastError());
     return LR_OK;
 }

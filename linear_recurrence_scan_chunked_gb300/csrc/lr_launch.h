@@ -285,8 +285,8 @@ cudaError_t launch_lstm_bwd(int dtype, bool vec, const LstmGates& z, const LstmB
 cudaError_t launch_deer_ode_iter(int dtype, bool vec, const float* w, const void* u,
                                  const float* dt, const void* h0, const void* yold, void* ynew,
                                  uint32_t* resid, const uint32_t* prev_resid, float eps,
-                                 unsigned long long* clamps, const Geom& g, const Carry& cr,
-                                 cudaStream_t s);
+                                 unsigned long long* clamps, const NextAgg& nx, const Geom& g,
+                                 const Carry& cr, cudaStream_t s);
 
 // DEER backward: partials is [n_chunks][C] fp32 scratch (dw per tile),
 // followed by C floats that launch_bias_reduce uses for its per-channel sums
