@@ -319,9 +319,10 @@ int64_t lr_workspace_bytes(void);
 /*
  * Test hook for the bounded carry waits: launches both chain-protocol
  * forward scan kernels (register and TMA-staged) on a private 2-chunk problem
- * whose first chunk is never published, one CTA each, and both walker-protocol
- * kernels (register, fp32; segmented, bf16) on a private long problem with no
- * walker CTAs, so no entering state is ever published.  Every wait is limited
+ * whose first chunk is never published, one CTA each, and the walker-protocol
+ * kernels (register, fp32; segmented, bf16; consume-only segmented, a fp32
+ * DEER iteration whose aggregates count as published) on a private long
+ * problem with no walker CTAs, so no entering state is ever published.  Every wait is limited
  * to `spin_limit` polls and runs out.  It leaves LR_ERR_TIMEOUT in the device
  * error word.  Nothing faults or hangs.
  */

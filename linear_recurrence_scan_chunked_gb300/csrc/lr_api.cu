@@ -756,9 +756,10 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
     // Chain protocol: both chain kernels (register and TMA-staged) on a problem
     // of two time chunks and one channel tile, each with one CTA that is handed
     // tile 1: it waits for the state after tile 0, which nobody publishes.
-    // Walker protocol: the register and the segmented walker kernels on a long
-    // one-strip problem launched without walker CTAs: no entering state is ever
-    // published, so every consume's wait runs out.
+    // Walker protocol: the register and the segmented walker kernels, and the
+    // consume-only segmented kernel, on a long one-strip problem launched
+    // without walker CTAs: no entering state is ever published, so every
+    // consume's wait runs out.
     const int64_t C = tile_shape(OP_SCAN_FWD, LR_F32, true, CARRY_CHAIN).CW;
     const int64_t Tw = 8192;  // >= 128 chunks of both walker tile shapes
     if (!ws->test_buf) {
@@ -791,6 +792,20 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
         cr.spin_limit = spin_limit;
         CK(launch_scan_fwd(dt, true, buf, buf + Tw * C * es, nullptr, buf + 2 * Tw * C * es, g, cr,
                            s));
+    }
+    {  // the consume-only segmented kernel: a DEER iteration whose aggregates
+       // count as published, again without walker CTAs
+        Geom g;
+        Carry cr;
+        TRY(plan(*ws, OP_DEER, LR_F32, true, Tw, C, C, &g, &cr, s, 1));
+        if (cr.mode != CARRY_WALK || !cr.tma) return LR_ERR_INVALID_ARG;
+        cr.n_walk = 0;
+        cr.spin_limit = spin_limit;
+        const float* z = (const float*)buf;  // zeros: w, u and the previous iterate
+        const NextAgg nx{cr.agg, cr.epoch + 1, 1u};
+        CK(launch_deer_iter(LR_F32, true, z, z, nullptr, z + Tw * C, (float*)buf + 2 * Tw * C,
+                            ws->words + 2, nullptr, 0.f, nx, DeerSeq{nullptr, nullptr, nullptr}, g,
+                            cr, s));
     }
     return leave(*ws, s);
 }
