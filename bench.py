@@ -239,10 +239,10 @@ class Bench:
                 "workload": f"deer fp32 T={wl.T} B={wl.B} D={wl.D}, gradient through the solution"}
 
     def time_deer_variants(self, peak, reps=5):
-        """At the DEER workload's size: the ODE form (steps dt ~ U(0.1, 1))
-        and a warm-started solve (the guess is the solution for u + 1e-3 sin,
-        a nearby problem, as the previous training step's would be): mean
-        solve time, K, algorithmic GB/s per iteration."""
+        """At the DEER workload's size: the ODE form (steps dt ~ U(0.1, 1)), a
+        warm-started solve (the guess is the solution for u + 1e-3 sin, a
+        nearby problem, as the previous training step's would be) and the
+        per-sequence stopping test: mean solve time, K, algorithmic GB/s."""
         t, L, wl = self.torch, self.lrs, W.DEER
         o = self.d["deer"]
         N, D = wl.N, wl.D
@@ -274,6 +274,19 @@ class Bench:
         out["deer.warm"] = {"ms": round(ms, 4), "iters": k, "GBps": round(byt / (ms / 1e3) / 1e9, 1),
                             "frac": round(byt / (ms / 1e3) / 1e9 / peak, 3),
                             "workload": f"deer fp32 T={wl.T} B={wl.B} D={wl.D} from a nearby problem's solution"}
+
+        def per_seq():
+            r = L.deer_diag_solve_ex(o["w"], o["u"], o["h0"], y, eps=EPS, kmax=KMAX, per_sequence=True)
+            res["k"], res["ks"] = r["iters"], r["seq_iters"]
+
+        ms = self._mean_ms(per_seq, reps)
+        k = res["k"]
+        byt = (8 + 12 * (k - 1)) * N + 4 * D * k
+        out["deer.per_sequence"] = {"ms": round(ms, 4), "iters": k, "seq_iters": res["ks"],
+                                    "GBps": round(byt / (ms / 1e3) / 1e9, 1),
+                                    "frac": round(byt / (ms / 1e3) / 1e9 / peak, 3),
+                                    "workload": f"deer fp32 T={wl.T} B={wl.B} D={wl.D}, "
+                                                "one stopping test per sequence"}
         del dt, y, u2, guess
         return out
 
