@@ -340,20 +340,33 @@ struct SruBwdOp {
 
 // Per-feature parameter gradients (SRU and LSTM biases, DEER's w) from
 // per-tile partials, in a fixed order (deterministic): stage 1 sums every
-// channel over the time chunks (one thread per channel, loads issued eight
-// chunks ahead), stage 2 sums the batch rows of each feature.  partials:
-// [n_arr][n_chunks][C]; colsum: [n_arr][C]; out.o[k]: [D] for k < n_arr.
-__global__ void __launch_bounds__(256)
-    k_bias_colsum(const float* __restrict__ partials, int64_t n_chunks, int64_t C, int n_arr,
+// channel over the time chunks, stage 2 sums the batch rows of each feature.
+// partials: [n_arr][n_chunks][C]; colsum: [n_arr][C]; out.o[k]: [D] for
+// k < n_arr.  Stage 1: a block owns 32 channels (x) and kColLanes chunk lanes
+// (y); lane y sums chunks y, y + kColLanes, ... (each step one coalesced row
+// segment), then lane 0 adds the lanes' sums in lane order -- so a channel's
+// chain of dependent loads is n_chunks / kColLanes long, not n_chunks.
+constexpr int kColLanes = 32;
+__global__ void __launch_bounds__(32 * kColLanes)
+    k_bias_colsum(const float* __restrict__ partials, int64_t n_chunks, int64_t C,
                   float* __restrict__ colsum) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n_arr * C) return;
-    const int64_t which = i / C, c = i % C;
-    const float* p = partials + which * n_chunks * C + c;
+    __shared__ float part[kColLanes][33];
+    const int64_t c = (int64_t)blockIdx.x * 32 + threadIdx.x;
+    const int64_t which = blockIdx.y;
     float acc = 0.f;
-#pragma unroll 8
-    for (int64_t k = 0; k < n_chunks; ++k) acc += __ldg(p + k * C);
-    colsum[i] = acc;
+    if (c < C) {
+        const float* p = partials + which * n_chunks * C + c;
+#pragma unroll 4
+        for (int64_t k = threadIdx.y; k < n_chunks; k += kColLanes) acc += __ldg(p + k * C);
+    }
+    part[threadIdx.y][threadIdx.x] = acc;
+    __syncthreads();
+    if (threadIdx.y == 0 && c < C) {
+        float sum = 0.f;
+#pragma unroll
+        for (int l = 0; l < kColLanes; ++l) sum += part[l][threadIdx.x];
+        colsum[which * C + c] = sum;
+    }
 }
 
 __global__ void __launch_bounds__(256)
@@ -427,8 +440,8 @@ cudaError_t launch_bias_reduce(const float* partials, int64_t n_chunks, int n_ar
     if (n_arr < 1 || n_arr > 4) return cudaErrorInvalidValue;
     const int64_t C = B * D;
     float* colsum = const_cast<float*>(partials) + n_arr * n_chunks * C;
-    k_bias_colsum<<<(unsigned)((n_arr * C + 255) / 256), 256, 0, s>>>(partials, n_chunks, C, n_arr,
-                                                                        colsum);
+    k_bias_colsum<<<dim3((unsigned)((C + 31) / 32), (unsigned)n_arr), dim3(32, kColLanes), 0, s>>>(
+        partials, n_chunks, C, colsum);
     k_bias_batch<<<(unsigned)((n_arr * D + 255) / 256), 256, 0, s>>>(colsum, B, D, n_arr, out);
     return cudaGetLastError();
 }
