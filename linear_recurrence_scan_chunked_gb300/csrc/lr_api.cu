@@ -90,6 +90,10 @@ struct DevWS {
     void* test_buf = nullptr;                             // timeout-test problem
     uint32_t* seq = nullptr;     size_t seq_cap = 0;      // DEER per-sequence state (words)
     unsigned long long* clamps = nullptr;                 // DEER ODE form: [kMaxIters] clamp counts
+    struct DeerLast {                                     // the last solve of each DEER form
+        int64_t T = -1, C = -1;
+        int dtype = -1, K = 0;
+    } deer_last[2];
     uint32_t* seq_host = nullptr; size_t seq_host_cap = 0;  // pinned mirror of its residuals
     uint32_t epoch = 0;
     cudaEvent_t done = nullptr;
@@ -416,7 +420,9 @@ static float bits_f(uint32_t b) {
 // aggregate buffers after the packets plan() lays out; from the second
 // iteration on a launch has no reduce pass.  onepass_begin sizes the packets
 // and keeps the epoch from wrapping inside the solve (plan() adds one per
-// launch); onepass_args points launch kk at its two buffers.
+// launch); onepass_args points launch kk at its two buffers; onepass_end
+// retires the epoch the solve's last launch tagged its next-aggregates with,
+// so that no later launch, of any operation, takes them for its own.
 static int onepass_begin(DevWS& ws, Op op, int dtype, bool vec, int64_t T, int64_t C, int kmax,
                          cudaStream_t s, CarryPlan* cp, bool* on) {
     *cp = carry_plan(op, dtype, vec, use_tma(dtype, vec, T, C), T, C);
@@ -427,7 +433,26 @@ static int onepass_begin(DevWS& ws, Op op, int dtype, bool vec, int64_t T, int64
         CK(cudaMemsetAsync(ws.pk, 0, ws.pk_cap * sizeof(u64), s));
         ws.epoch = 0;
     }
+    ++ws.epoch;  // also retired here, in case an earlier solve stopped on an error
     return LR_OK;
+}
+
+// The iteration count of the last solve of this DEER form (0: tanh, 1: ODE)
+// and shape, 0 if none.  A solve writes iterate k to buf[(k + flip) % 2]
+// (buf[1] is the caller's y) with flip chosen so that this count's iterate
+// lands in y, and enqueues that many iterations before its first residual
+// read-back; a wrong guess costs one copy or one more read-back, never a
+// different result.
+static int deer_predict(const DevWS& ws, int form, int64_t T, int64_t C, int dtype) {
+    const DevWS::DeerLast& d = ws.deer_last[form];
+    return d.T == T && d.C == C && d.dtype == dtype ? d.K : 0;
+}
+static void deer_remember(DevWS& ws, int form, int64_t T, int64_t C, int dtype, int K) {
+    ws.deer_last[form] = DevWS::DeerLast{T, C, dtype, K};
+}
+
+static void onepass_end(DevWS& ws, bool on) {
+    if (on) ++ws.epoch;  // onepass_begin left room: no wrap here
 }
 
 static NextAgg onepass_args(DevWS& ws, const CarryPlan& cp, int kk, Carry& cr) {
@@ -440,11 +465,12 @@ static NextAgg onepass_args(DevWS& ws, const CarryPlan& cp, int kk, Carry& cr) {
 int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void* y_init, void* y,
                        int64_t B, int64_t T, int64_t D, float eps, int kmax, int per_sequence,
                        int* iters_out, float* resid_out, float* resid_hist, int* seq_iters,
-                       float* seq_resid, int dtype, void* stream) {
+                       float* seq_resid, int* launched_out, int dtype, void* stream) {
     TRY(check_sizes(B, T, D, dtype));
     if (!iters_out || kmax < 1 || kmax > kMaxIters || !(eps >= 0.f)) return LR_ERR_INVALID_ARG;
     if (per_sequence != 0 && per_sequence != 1) return LR_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
+    if (launched_out) *launched_out = 0;
     if (B * T * D == 0) {
         *iters_out = 0;
         if (resid_out) *resid_out = 0.f;
@@ -489,25 +515,31 @@ int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void
     if (per_sequence) CK(cudaMemsetAsync(ws->seq, 0, sq_words * sizeof(uint32_t), s));
     uint32_t* slots = ws->words + 2;
     CK(cudaMemsetAsync(slots, 0, sizeof(uint32_t) * kmax, s));
-    // iterate k writes buf[k % 2]; buf[1] is the caller's y.  Iteration 1
-    // reads the initial guess (a guess passed in y itself is first copied to
-    // buf[0]).  Iterations are enqueued kDeerBatch at a time with one residual
-    // read-back per batch; an iteration enqueued after the solve stopped
-    // returns at once (it sees its predecessor's residual, or the all-done
-    // word, on the device).
+    // iterate k writes buf[(k + flip) % 2]; buf[1] is the caller's y.
+    // Iteration 1 reads the initial guess (a guess passed in y itself is first
+    // copied to buf[0], and then iteration 1 writes y: flip = 0).  The first
+    // batch is the last solve's iteration count (deer_predict), later ones
+    // kDeerBatch, with one residual read-back per batch; an iteration enqueued
+    // after the solve stopped returns at once (it sees its predecessor's
+    // residual, or the all-done word, on the device).
     void* buf[2] = {ws->ybuf, y};
     const void* y0 = y_init;
-    if (y_init != nullptr && y_init == y) {
+    const bool in_place = y_init != nullptr && y_init == y;
+    if (in_place) {
         CK(cudaMemcpyAsync(ws->ybuf, y_init, nbytes, cudaMemcpyDeviceToDevice, s));
         y0 = ws->ybuf;
     }
+    const int kp = per_sequence ? 0 : deer_predict(*ws, 0, T, B * D, dtype);
+    const int flip = kp > 0 && !in_place ? (kp + 1) & 1 : 0;
+    auto tgt = [&](int kk) { return buf[(kk + flip) & 1]; };
     int k = 0, status = LR_ERR_NOT_CONVERGED;
     float rho = 0.f;
     int launched = 0;
     bool done = false;
     while (!done && launched < kmax) {
         const int first = launched;
-        const int nb = kmax - launched < kDeerBatch ? kmax - launched : kDeerBatch;
+        const int want = first == 0 && kp > 0 ? kp : kDeerBatch;
+        const int nb = kmax - launched < want ? kmax - launched : want;
         for (int i = 0; i < nb; ++i) {
             const int kk = ++launched;
             Geom g;
@@ -516,8 +548,8 @@ int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void
             const NextAgg nx = onepass ? onepass_args(*ws, cp, kk, cr) : NextAgg{nullptr, 0u, 0u};
             DeerSeq sq{nullptr, nullptr, nullptr};
             if (per_sequence) sq = DeerSeq{sq_slots + (size_t)(kk - 1) * B, sq_done, sq_all};
-            CK(launch_deer_iter(dtype, vec, w, u, h0, kk == 1 ? y0 : buf[(kk - 1) & 1],
-                                buf[kk & 1], slots + (kk - 1),
+            CK(launch_deer_iter(dtype, vec, w, u, h0, kk == 1 ? y0 : tgt(kk - 1), tgt(kk),
+                                slots + (kk - 1),
                                 kk == 1 || per_sequence ? nullptr : slots + (kk - 2), eps, nx, sq, g,
                                 cr, s));
             if (per_sequence)
@@ -549,9 +581,12 @@ int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void
             done = hs[(size_t)kmax * B] != 0;
         }
     }
+    onepass_end(*ws, onepass);
+    if (launched_out) *launched_out = launched;
     if (!per_sequence) {
         if (k > kmax) k = kmax;
-        if ((k & 1) == 0) CK(cudaMemcpyAsync(y, ws->ybuf, nbytes, cudaMemcpyDeviceToDevice, s));
+        if (tgt(k) != y) CK(cudaMemcpyAsync(y, ws->ybuf, nbytes, cudaMemcpyDeviceToDevice, s));
+        if (status != LR_ERR_NONFINITE) deer_remember(*ws, 0, T, B * D, dtype, k);
         *iters_out = k;
         if (resid_out) *resid_out = rho;
         for (int64_t b = 0; b < B; ++b) {
@@ -589,7 +624,7 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y, int6
                     int64_t D, float eps, int kmax, int* iters_out, float* resid_out,
                     float* resid_hist, int dtype, void* stream) {
     return deer_diag_solve_ex(w, u, h0, nullptr, y, B, T, D, eps, kmax, 0, iters_out, resid_out,
-                              resid_hist, nullptr, nullptr, dtype, stream);
+                              resid_hist, nullptr, nullptr, nullptr, dtype, stream);
 }
 
 int deer_ode_solve(const float* w, const void* u, const float* dt, const void* h0, void* y,
@@ -625,24 +660,28 @@ int deer_ode_solve(const float* w, const void* u, const float* dt, const void* h
     uint32_t* slots = ws->words + 2;
     CK(cudaMemsetAsync(slots, 0, sizeof(uint32_t) * kmax, s));
     CK(cudaMemsetAsync(ws->clamps, 0, sizeof(unsigned long long) * kmax, s));
-    // as deer_diag_solve: iterate k writes buf[k % 2] (buf[1] is y), batches
-    // of kDeerBatch launches with one residual read-back each
+    // as deer_diag_solve_ex: iterate k writes buf[(k + flip) % 2] (buf[1] is
+    // y), the first batch is the last solve's count, later ones kDeerBatch
     void* buf[2] = {ws->ybuf, y};
+    const int kp = deer_predict(*ws, 1, T, B * D, dtype);
+    const int flip = kp > 0 ? (kp + 1) & 1 : 0;
+    auto tgt = [&](int kk) { return buf[(kk + flip) & 1]; };
     int k = 0, status = LR_ERR_NOT_CONVERGED;
     float rho = 0.f;
     int launched = 0;
     bool done = false;
     while (!done && launched < kmax) {
         const int first = launched;
-        const int nb = kmax - launched < kDeerBatch ? kmax - launched : kDeerBatch;
+        const int want = first == 0 && kp > 0 ? kp : kDeerBatch;
+        const int nb = kmax - launched < want ? kmax - launched : want;
         for (int i = 0; i < nb; ++i) {
             const int kk = ++launched;
             Geom g;
             Carry cr;
             TRY(plan(*ws, OP_DEER_ODE, dtype, vec, T, B * D, D, &g, &cr, s));
             const NextAgg nx = onepass ? onepass_args(*ws, cp, kk, cr) : NextAgg{nullptr, 0u, 0u};
-            CK(launch_deer_ode_iter(dtype, vec, w, u, dt, h0, kk == 1 ? nullptr : buf[(kk - 1) & 1],
-                                    buf[kk & 1], slots + (kk - 1),
+            CK(launch_deer_ode_iter(dtype, vec, w, u, dt, h0, kk == 1 ? nullptr : tgt(kk - 1), tgt(kk),
+                                    slots + (kk - 1),
                                     kk == 1 ? nullptr : slots + (kk - 2), eps,
                                     ws->clamps + (kk - 1), nx, g, cr, s));
         }
@@ -656,8 +695,10 @@ int deer_ode_solve(const float* w, const void* u, const float* dt, const void* h
             if (rho < eps) { status = LR_OK; done = true; break; }
         }
     }
+    onepass_end(*ws, onepass);
     if (k > kmax) k = kmax;
-    if ((k & 1) == 0) CK(cudaMemcpyAsync(y, ws->ybuf, nbytes, cudaMemcpyDeviceToDevice, s));
+    if (tgt(k) != y) CK(cudaMemcpyAsync(y, ws->ybuf, nbytes, cudaMemcpyDeviceToDevice, s));
+    if (status != LR_ERR_NONFINITE) deer_remember(*ws, 1, T, B * D, dtype, k);
     if (clamps_out) {
         unsigned long long n = 0;
         CK(cudaMemcpyAsync(&n, ws->clamps + (k - 1), sizeof n, cudaMemcpyDeviceToHost, s));
