@@ -189,15 +189,14 @@ class Bench:
                           o["c0"], out=o["grad"])
                 launches += 3  # fused backward + two bias-reduction stages
             else:
-                _, k, _, hist, st = L.deer_diag_solve(o["w"], o["u"], o["h0"], o["y"], eps=EPS,
-                                                      kmax=KMAX)
-                if st != L.LR_OK:
-                    raise RuntimeError(f"DEER did not converge (status {st})")
-                self.k_last = k
-                self.hist_last = hist
-                # iterations are enqueued four at a time; those after the
-                # stopping test return at once but are still launches
-                launches += min(KMAX, -(-k // 4) * 4)
+                r = L.deer_diag_solve_ex(o["w"], o["u"], o["h0"], o["y"], eps=EPS, kmax=KMAX)
+                if r["status"] != L.LR_OK:
+                    raise RuntimeError(f"DEER did not converge (status {r['status']})")
+                self.k_last = r["iters"]
+                self.hist_last = r["hist"]
+                # iterations are enqueued in batches; those after the stopping
+                # test return at once but are still launches
+                launches += r["launches"]
             if ev is not None:
                 ev[(name, p)][1].record()
             k = self.k_last if p == "solve" else 1

@@ -45,10 +45,11 @@
  *    a multiple of 16 bytes and at least 128 channels wide, tiles are staged
  *    through shared memory by the Tensor Memory Accelerator.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
- *    asynchronous on it except deer_diag_solve, which enqueues its Newton
- *    iterations four at a time and synchronises the stream once per four to
- *    read their residuals (an iteration enqueued after the stopping test was
- *    met does no work).
+ *    asynchronous on it except the DEER solves, which enqueue their Newton
+ *    iterations in batches -- the first as long as the previous solve of the
+ *    same form and shape took, then four -- and synchronise the stream once
+ *    per batch to read the residuals (an iteration enqueued after the
+ *    stopping test was met does no work).
  *  - Sizes: B, T, D >= 0 with B*T*D < 2^62; an empty problem is a no-op
  *    (gradients of the initial state are zeroed).
  *  - The library keeps one internal workspace per device (carry packets of
@@ -187,13 +188,16 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y,
  *   seq_iters    : host int[B] out (may be NULL): K_b (K for every b when
  *                  per_sequence = 0)
  *   seq_resid    : host float[B] out (may be NULL): each sequence's residual at K_b
+ *   launched_out : host int out (may be NULL): iteration kernels enqueued,
+ *                  including those that returned at once after the solve stopped
  * Status as deer_diag_solve: LR_ERR_NONFINITE if any sequence's residual was not
  * finite, else LR_ERR_NOT_CONVERGED if any sequence reached kmax without eps.
  */
 int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void* y_init,
                        void* y, int64_t B, int64_t T, int64_t D, float eps, int kmax,
                        int per_sequence, int* iters_out, float* resid_out, float* resid_hist,
-                       int* seq_iters, float* seq_resid, int dtype, void* stream);
+                       int* seq_iters, float* seq_resid, int* launched_out, int dtype,
+                       void* stream);
 
 /*
  * DEER solve in the ODE form (the next row on the same scan).  [P4] "监控与调优":

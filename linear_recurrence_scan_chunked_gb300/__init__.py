@@ -57,7 +57,7 @@ def load():
     lib.lstm_cell_bwd.argtypes = [P] * 20 + [I64, I64, I64, I, P]
     lib.deer_diag_solve.argtypes = [P, P, P, P, I64, I64, I64, ctypes.c_float, I, P, P, P, I, P]
     lib.deer_diag_solve_ex.argtypes = [P, P, P, P, P, I64, I64, I64, ctypes.c_float, I, I, P, P,
-                                       P, P, P, I, P]
+                                       P, P, P, P, I, P]
     lib.deer_ode_solve.argtypes = [P, P, P, P, P, I64, I64, I64, ctypes.c_float, I, P, P, P, P,
                                    I, P]
     lib.deer_diag_bwd.argtypes = [P] * 7 + [I64, I64, I64, I, P]
@@ -273,7 +273,7 @@ def deer_diag_solve_ex(w, u, h0=None, y=None, y_init=None, eps=1e-5, kmax=20,
     """DEER solve from an initial guess (None = zeros; it may be y itself) with
     one stopping test for the batch or one per sequence.  Returns a dict: y,
     iters (largest K), resid, hist (per iteration), status, seq_iters[B],
-    seq_resid[B]."""
+    seq_resid[B], launches (iteration kernels enqueued)."""
     _seq("u", u)
     T, B, D = u.shape
     _param("w", w, D)
@@ -286,15 +286,16 @@ def deer_diag_solve_ex(w, u, h0=None, y=None, y_init=None, eps=1e-5, kmax=20,
     hist = (ctypes.c_float * int(kmax))()
     sk = (ctypes.c_int * max(1, B))()
     sr = (ctypes.c_float * max(1, B))()
+    nl = ctypes.c_int(0)
     st = load().deer_diag_solve_ex(_p(w), _p(u), _p(h0), _p(y_init), _p(y), B, T, D,
                                    ctypes.c_float(eps), int(kmax), 1 if per_sequence else 0,
-                                   ctypes.byref(it), ctypes.byref(rho), hist, sk, sr, _code(u),
-                                   _stream(stream))
+                                   ctypes.byref(it), ctypes.byref(rho), hist, sk, sr,
+                                   ctypes.byref(nl), _code(u), _stream(stream))
     if st not in (LR_OK, LR_ERR_NOT_CONVERGED, LR_ERR_NONFINITE):
         _check(st)
     k = int(it.value)
     return {"y": y, "iters": k, "resid": float(rho.value), "hist": list(hist)[:k], "status": int(st),
-            "seq_iters": list(sk)[:B], "seq_resid": list(sr)[:B]}
+            "seq_iters": list(sk)[:B], "seq_resid": list(sr)[:B], "launches": int(nl.value)}
 
 
 def deer_ode_solve(w, u, dt, h0=None, y=None, eps=1e-5, kmax=20, stream=None):

@@ -237,6 +237,32 @@ def test_deer_bf16_warm_start_and_per_sequence(cuda, shape):
     assert_close("y per sequence", to_f64(seq["y"]), star, "bf16")
 
 
+@pytest.mark.parametrize("shape", [(300, 3, 40), (9000, 2, 512)])
+def test_deer_repeat_uses_the_last_count(cuda, shape):
+    """A solve remembers its K: the next solve of the same shape enqueues K
+    iterations before its first read-back and writes iterate K straight into
+    y.  Solves that stop later (eps 1e-5 after 1e-2) or earlier (1e-2 after
+    1e-5) than the remembered count match the oracle; a repeat takes exactly
+    K launches and gives the same bits."""
+    inp, dv, f = _deer_case(shape, 14)
+
+    def solve_and_check(eps):
+        r = cuda.deer_diag_solve_ex(dv["w"], dv["u"], dv["h0"], eps=eps, kmax=20)
+        ry, rk, rhist, rst = oracle.deer(f["w"], f["u"], f["h0"], eps=eps, kmax=20)
+        assert (r["iters"], r["status"]) == (rk, rst), (eps, r["hist"], list(rhist))
+        assert_close(f"y eps={eps}", to_f64(r["y"]), ry, "f32")
+        return r
+
+    short = solve_and_check(1e-2)
+    long_ = solve_and_check(1e-5)  # later than remembered
+    assert long_["iters"] > short["iters"]
+    y1 = long_["y"].clone()
+    again = cuda.deer_diag_solve_ex(dv["w"], dv["u"], dv["h0"], eps=1e-5, kmax=20)
+    assert again["iters"] == long_["iters"] == again["launches"]
+    assert torch.equal(again["y"], y1)
+    solve_and_check(1e-2)  # earlier than remembered
+
+
 def test_deer_ex_global_matches_deer_diag_solve(cuda):
     inp, dv, f = _deer_case((9000, 2, 512), 10)
     y, k, resid, hist, st = cuda.deer_diag_solve(dv["w"], dv["u"], dv["h0"], eps=1e-5, kmax=20)
