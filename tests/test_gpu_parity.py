@@ -296,6 +296,32 @@ def test_deer_ode(cuda, shape):
     assert cl == rcl == 0
 
 
+def test_deer_ode_repeat_and_bf16(cuda):
+    """A repeated ODE solve (the remembered count: iterate K written straight
+    into y) gives the same bits; bf16 storage converges to the fp64 fixed point
+    within the bf16 tolerance."""
+    dv, f, dt, dtf = _ode_case((9000, 2, 512), 13)
+    a = cuda.deer_ode_solve(dv["w"], dv["u"], dt, dv["h0"], eps=1e-5, kmax=20)
+    ya = a[0].clone()
+    b = cuda.deer_ode_solve(dv["w"], dv["u"], dt, dv["h0"], eps=1e-5, kmax=20)
+    assert (b[1], b[4]) == (a[1], a[4]) and torch.equal(b[0], ya)
+    ry, rk, rhist, rst, _ = oracle.deer_ode(f["w"], f["u"], dtf, f["h0"], eps=1e-5, kmax=20)
+    assert (a[1], a[4]) == (rk, rst)
+    assert_close("y", to_f64(ya), ry, "f32")
+    T, B, D = 4000, 2, 256
+    wl = W.like(W.DEER, T, B, D, "bf16")
+    inp = W.make_inputs(wl, 15)
+    dvb, fb = dev_inputs(inp, "bf16"), f64_inputs(inp, "bf16")
+    dts = W.uniform(15, 44, (T,), 0.1, 1.0)
+    y, k, resid, hist, st, cl = cuda.deer_ode_solve(dvb["w"], dvb["u"], torch.from_numpy(dts).cuda(),
+                                                    None, eps=1e-2, kmax=20)
+    ry, rk, rhist, rst, _ = oracle.deer_ode(fb["w"], fb["u"], dts.astype(np.float64), None, eps=1e-2,
+                                            kmax=20)
+    assert st == cuda.LR_OK and rst == oracle.DEER_CONVERGED and abs(k - rk) <= 1
+    assert_close("y bf16", to_f64(y), oracle.rollout_ode(fb["w"], fb["u"], dts.astype(np.float64))[0],
+                 "bf16")
+
+
 def test_deer_ode_clamp(cuda):
     """w = -12: G = 1 + 12 (1 - tanh^2) exceeds 10 for small pre-activations
     and is clamped.  The count decides, per element, G > 10 in fp32 on the
