@@ -54,9 +54,10 @@
  *    (gradients of the initial state are zeroed).
  *  - The library keeps one internal workspace per device (carry packets of
  *    the chunk states and aggregates, a tile ticket, an error word, DEER's
- *    second iterate buffer, bias-gradient partials), grown on demand with
- *    cudaMalloc.  Calls on different streams are serialised through it with
- *    CUDA events.
+ *    second iterate buffer, residual slots, per-sequence stop state, clamp
+ *    counters and the last iteration count of each DEER form and shape,
+ *    bias-gradient partials), grown on demand with cudaMalloc.  Calls on
+ *    different streams are serialised through it with CUDA events.
  *  - Return value: LR_OK, or an lr_status describing an argument or launch
  *    error detected before or while enqueuing the work.  Errors detected on
  *    the device while the kernels run (a carry or copy wait that ran out) are
