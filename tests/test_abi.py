@@ -47,6 +47,21 @@ def test_argument_errors_before_cuda(lib):
                                P, P, 0, P) == lrs.LR_ERR_INVALID_ARG
     assert lib.deer_diag_solve(P, P, P, P, 2, 3, 4, ctypes.c_float(1e-5), 0, ctypes.byref(iters),
                                P, P, 0, P) == lrs.LR_ERR_INVALID_ARG
+    # the DEER variants: null required pointers, kmax out of range, a bad mode
+    it, nl = ctypes.c_int(0), ctypes.c_int(0)
+    eps = ctypes.c_float(1e-5)
+    assert lib.deer_diag_solve_ex(P, P, P, P, P, 2, 3, 4, eps, 20, 0, ctypes.byref(it), P, P, P, P,
+                                  ctypes.byref(nl), 0, P) == lrs.LR_ERR_INVALID_ARG
+    assert lib.deer_diag_solve_ex(P, P, P, P, P, 2, 3, 4, eps, 20, 2, ctypes.byref(it), P, P, P, P,
+                                  P, 0, P) == lrs.LR_ERR_INVALID_ARG
+    assert lib.deer_diag_solve_ex(P, P, P, P, P, 2, 3, 4, eps, 0, 0, ctypes.byref(it), P, P, P, P,
+                                  P, 0, P) == lrs.LR_ERR_INVALID_ARG
+    assert lib.deer_ode_solve(P, P, P, P, P, 2, 3, 4, eps, 20, ctypes.byref(it), P, P, P, 0,
+                              P) == lrs.LR_ERR_INVALID_ARG
+    assert lib.deer_ode_solve(P, P, P, P, P, 2, 3, 4, ctypes.c_float(-1.0), 20, ctypes.byref(it), P,
+                              P, P, 0, P) == lrs.LR_ERR_INVALID_ARG
+    assert lib.deer_diag_bwd(*([P] * 7), 2, 3, 4, 0, P) == lrs.LR_ERR_INVALID_ARG
+    assert lib.lr_test_activations(P, P, P, P, -1, P) == lrs.LR_ERR_INVALID_ARG
     # sizes beyond 2^62 elements
     assert lib.lr_scan_fwd(P, P, P, P, 1 << 31, 1 << 31, 4, 0, P) == lrs.LR_ERR_TOO_LARGE
     # misaligned (odd byte address) fp32 pointer
@@ -60,6 +75,22 @@ def test_empty_problem_is_a_no_op(lib):
     assert lib.lr_scan_fwd(None, None, None, None, 0, 5, 4, 0, None) == lrs.LR_OK
     assert lib.sru_fwd(*([None] * 9), 3, 0, 4, 0, None) == lrs.LR_OK
     assert lib.lstm_cell_fwd(*([None] * 11), 3, 0, 4, 0, None) == lrs.LR_OK
+
+
+def test_binding_checks_tensors_before_the_library():
+    """The binding rejects host tensors, wrong shapes and wrong dtypes with
+    ValueError before any call into the library (no device needed)."""
+    import torch
+    u = torch.zeros(5, 2, 4)
+    w = torch.zeros(4)
+    with pytest.raises(ValueError):
+        lrs.deer_ode_solve(w, u, torch.zeros(5))
+    with pytest.raises(ValueError):
+        lrs.deer_diag_solve_ex(w, u)
+    with pytest.raises(ValueError):
+        lrs.lstm_cell_fwd(u, u, u, u, w, w, w, w)
+    with pytest.raises(ValueError):
+        lrs.test_activations(torch.zeros(3))
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
