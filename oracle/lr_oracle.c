@@ -364,15 +364,17 @@ void lro_rollout_ode(int64_t T, int64_t C, int64_t D, const double* w,
     if (clamps) *clamps = ncl;
 }
 
-/* One iteration from yprev (NULL = the all-zero guess); rho = max |ynew - yprev|. */
+/* One iteration from yprev (NULL = the all-zero guess); rho = max |ynew - yprev|,
+ * NaN when any difference is NaN (as lro_deer_step). */
 void lro_deer_ode_step(int64_t T, int64_t C, int64_t D, const double* w,
                        const double* u, const double* dt, const double* h0,
                        const double* yprev, double* ynew, double* rho,
                        int64_t* clamps) {
     double best = 0.0;
     int64_t ncl = 0;
+    int nan_seen = 0;
 #ifdef _OPENMP
-#pragma omp parallel num_threads(lro_num_threads()) reduction(max : best) reduction(+ : ncl)
+#pragma omp parallel num_threads(lro_num_threads()) reduction(max : best) reduction(+ : ncl) reduction(| : nan_seen)
 #endif
     {
         int64_t c0_ = 0, c1_ = C;
@@ -393,10 +395,11 @@ void lro_deer_ode_step(int64_t T, int64_t C, int64_t D, const double* w,
                 double ylast = t > 0 ? ynew[i - C] : init;
                 ynew[i] = a * ylast + b;
                 double diff = fabs(ynew[i] - (yprev ? yprev[i] : 0.0));
-                if (diff > best) best = diff;
+                if (isnan(diff)) nan_seen = 1;
+                else if (diff > best) best = diff;
             }
     }
-    *rho = best;
+    *rho = nan_seen ? NAN : best;
     if (clamps) *clamps = ncl;
 }
 
@@ -454,14 +457,17 @@ void lro_rollout_tanh(int64_t T, int64_t C, int64_t D, const double* w,
  *   rhs_t = tanh(s_t) - J_t ytil_{t-1}
  *   ynew_t = J_t ynew_{t-1} + rhs_t,   ynew_{-1} = h0     (sequential here)
  * yprev == NULL means the all-zero initial guess.  Returns, through *rho,
- * max |ynew - yprev| over all B*T*D entries.
+ * max |ynew - yprev| over all B*T*D entries; NaN when any entry's difference
+ * is NaN (the max-abs norm of a vector holding a NaN is NaN, so the stopping
+ * test sees it as not finite).
  */
 void lro_deer_step(int64_t T, int64_t C, int64_t D, const double* w,
                    const double* u, const double* h0, const double* yprev,
                    double* ynew, double* rho) {
     double best = 0.0;
+    int nan_seen = 0;
 #ifdef _OPENMP
-#pragma omp parallel num_threads(lro_num_threads()) reduction(max : best)
+#pragma omp parallel num_threads(lro_num_threads()) reduction(max : best) reduction(| : nan_seen)
 #endif
     {
         int64_t c0_ = 0, c1_ = C;
@@ -481,10 +487,11 @@ void lro_deer_step(int64_t T, int64_t C, int64_t D, const double* w,
                 double ylast = t > 0 ? ynew[i - C] : init;
                 ynew[i] = J * ylast + rhs;
                 double diff = fabs(ynew[i] - (yprev ? yprev[i] : 0.0));
-                if (diff > best) best = diff;
+                if (isnan(diff)) nan_seen = 1;
+                else if (diff > best) best = diff;
             }
     }
-    *rho = best;
+    *rho = nan_seen ? NAN : best;
 }
 
 /*

@@ -485,6 +485,32 @@ def test_deer_per_sequence_stopping():
     np.testing.assert_array_equal(y[:, 1:], yg[:, 1:])
 
 
+def test_deer_per_sequence_nonfinite_sequence_stops_alone():
+    # a NaN in one sequence's input makes its first residual NaN: that
+    # sequence stops (not finite) at K = 1, the other converges untouched
+    T, D = 500, 4
+    r = np.random.default_rng(35)
+    w = r.uniform(-0.9, 0.9, D)
+    u = r.standard_normal((T, 2, D))
+    u[100, 1, 2] = np.nan
+    y, ks, sts, hists = oracle.deer_per_sequence(w, u, eps=1e-9, kmax=30)
+    assert sts[1] == oracle.DEER_NONFINITE and ks[1] == 1
+    assert sts[0] == oracle.DEER_CONVERGED
+    np.testing.assert_allclose(y[:, 0], oracle.rollout_tanh(w, u[:, :1])[:, 0], rtol=0, atol=1e-8)
+
+
+def test_deer_ode_nonfinite_input_stops_at_once():
+    # the ODE form's residual carries a NaN through the max-abs norm as well
+    T, D = 300, 4
+    r = np.random.default_rng(36)
+    w = r.uniform(-0.9, 0.9, D)
+    u = r.standard_normal((T, 1, D))
+    u[50, 0, 1] = np.nan
+    dt = np.full(T, 0.1)
+    y, k, hist, st, ncl = oracle.deer_ode(w, u, dt, eps=1e-9, kmax=30)
+    assert st == oracle.DEER_NONFINITE and k == 1 and np.isnan(hist[0])
+
+
 def test_deer_stopping_rule_edges():
     w = rng.uniform(-0.9, 0.9, 3)
     u = rng.standard_normal((64, 1, 3))
