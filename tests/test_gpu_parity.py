@@ -211,6 +211,30 @@ def test_deer_per_sequence_kmax(cuda):
     assert_close("y", to_f64(r["y"]), ry, "f32")
 
 
+def test_deer_per_sequence_nonfinite_sequence(cuda):
+    """A NaN input stops its own sequence at K = 1 (not finite) and the solve
+    reports LR_ERR_NONFINITE, while the other sequences run to their own
+    convergence and match the oracle's per-sequence solve."""
+    shape = (9000, 3, 256)
+    inp, dv, f = _deer_case(shape, 10, [0.01, 1.5, 1.5])
+    dv["u"][4000, 2, 17] = float("nan")
+    u = f["u"].copy()
+    u[4000, 2, 17] = np.nan
+    r = cuda.deer_diag_solve_ex(dv["w"], dv["u"], dv["h0"], eps=1e-5, kmax=20, per_sequence=True)
+    ry, rks, rsts, rhists = oracle.deer_per_sequence(f["w"], u, f["h0"], eps=1e-5, kmax=20)
+    assert rsts == [oracle.DEER_CONVERGED, oracle.DEER_CONVERGED, oracle.DEER_NONFINITE]
+    assert r["status"] == cuda.LR_ERR_NONFINITE
+    assert r["seq_iters"] == rks and rks[2] == 1
+    assert np.isnan(r["seq_resid"][2])
+    y = to_f64(r["y"])
+    assert_close("y of the finite sequences", y[:, :2], ry[:, :2], "f32")
+    # sequence 2 holds its first iterate: NaN from the bad step on, in its channel only
+    bad = np.zeros(shape, bool)
+    bad[4000:, 2, 17] = True
+    assert np.isnan(y[bad]).all() and np.isfinite(y[~bad]).all()
+    assert_close("y of the stopped sequence", np.where(bad, 0.0, y)[:, 2], np.where(bad, 0.0, ry)[:, 2], "f32")
+
+
 @pytest.mark.parametrize("shape", [(2000, 2, 256), (9000, 2, 512)])
 def test_deer_bf16_warm_start_and_per_sequence(cuda, shape):
     """bf16 storage: the warm start converges in fewer iterations than the
