@@ -320,6 +320,32 @@ def test_deer_ode(cuda, shape):
     assert cl == rcl == 0
 
 
+def test_deer_ode_nonfinite_stops(cuda):
+    """A NaN input makes the ODE form's first residual NaN: the solve stops at
+    K = 1 with LR_ERR_NONFINITE, as the oracle does, and y holds iterate 1
+    (NaN from the bad step on, in its channel only).  A clean solve of the
+    same shape runs first, so the remembered count enqueues several iterations
+    and the later ones must pass the residual on."""
+    shape = (2000, 2, 256)
+    dv, f, dt, dtf = _ode_case(shape, 14)
+    _, k0, _, _, st0, _ = cuda.deer_ode_solve(dv["w"], dv["u"], dt, dv["h0"], eps=1e-5, kmax=20)
+    assert st0 == cuda.LR_OK and k0 > 2
+    dv["u"][700, 1, 33] = float("nan")
+    u = f["u"].copy()
+    u[700, 1, 33] = np.nan
+    y, k, resid, hist, st, cl = cuda.deer_ode_solve(dv["w"], dv["u"], dt, dv["h0"], eps=1e-5, kmax=20)
+    ry, rk, rhist, rst, rcl = oracle.deer_ode(f["w"], u, dtf, f["h0"], eps=1e-5, kmax=20)
+    assert (rk, rst) == (1, oracle.DEER_NONFINITE)
+    assert (k, st) == (1, cuda.LR_ERR_NONFINITE)
+    assert np.isnan(resid) and np.isnan(hist[0]) and np.isnan(rhist[0])
+    assert cl == rcl == 0
+    y = to_f64(y)
+    bad = np.zeros(shape, bool)
+    bad[700:, 1, 33] = True
+    assert np.isnan(y[bad]).all() and np.isfinite(y[~bad]).all()
+    assert_close("y", np.where(bad, 0.0, y), np.where(bad, 0.0, ry), "f32")
+
+
 def test_deer_ode_repeat_and_bf16(cuda):
     """A repeated ODE solve (the remembered count: iterate K written straight
     into y) gives the same bits; bf16 storage converges to the fp64 fixed point
