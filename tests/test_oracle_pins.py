@@ -365,15 +365,20 @@ def test_rollout_w_zero_is_tanh():
 
 
 def test_rollout_small_signal_is_linear_recurrence():
-    """tanh(z) = z + O(z^3): at amplitude 1e-6 the rollout equals the linear
-    recurrence y_t = w y_{t-1} + u_t to ~1e-18 absolute."""
+    """|tanh z - z| <= |z|^3 / 3: at amplitude 1e-6 the rollout equals the
+    linear recurrence y_t = w y_{t-1} + u_t within that term, carried through
+    the recurrence (a factor 1 / (1 - max|w|)), plus rounding."""
     T, D = 200, 5
-    w = rng.uniform(-0.9, 0.9, D)
-    u = 1e-6 * rng.standard_normal((T, 1, D))
+    r = np.random.default_rng(38)
+    w = r.uniform(-0.9, 0.9, D)
+    u = 1e-6 * r.standard_normal((T, 1, D))
     y = oracle.rollout_tanh(w, u)
     for d in range(D):
         lin = _bidiag_solve(np.full(T, w[d]), u[:, 0, d])
-        np.testing.assert_allclose(y[:, 0, d], lin, rtol=0, atol=1e-16)
+        zmax = np.abs(w[d] * np.concatenate([[0.0], lin[:-1]]) + u[:, 0, d]).max()
+        bound = 2 * zmax ** 3 / 3 / (1 - abs(w[d])) + 1e-19
+        assert bound < 1e-3 * np.abs(lin).max()
+        np.testing.assert_allclose(y[:, 0, d], lin, rtol=0, atol=bound)
 
 
 def test_deer_step_is_newton_on_residual():
@@ -520,6 +525,20 @@ def test_deer_stopping_rule_edges():
     assert (k, st, len(hist)) == (5, oracle.DEER_NOT_CONVERGED, 5)
 
 
+def test_deer_stopping_test_is_strict():
+    # the test is rho < eps: a residual equal to eps does not stop.  With
+    # w = 0 iteration 2 repeats iteration 1 exactly (rho_2 = 0), so eps = 0
+    # never stops; with eps = rho_2 of a random problem, iteration 2 goes on
+    _, k, hist, st = oracle.deer(np.zeros(3), rng.standard_normal((40, 1, 3)), eps=0.0, kmax=4)
+    assert hist[1] == 0.0 and (k, st) == (4, oracle.DEER_NOT_CONVERGED)
+    w = rng.uniform(-0.9, 0.9, 3)
+    u = rng.standard_normal((64, 1, 3))
+    _, _, hist, _ = oracle.deer(w, u, eps=0.0, kmax=3)
+    assert hist[2] < hist[1]
+    _, k, _, st = oracle.deer(w, u, eps=hist[1], kmax=20)
+    assert k > 2 and st == oracle.DEER_CONVERGED
+
+
 # ----------------------------------------------------------- DEER backward
 
 def test_deer_bwd_finite_differences_of_the_rollout():
@@ -642,6 +661,19 @@ def test_deer_ode_converges_to_the_rollout():
     # iteration 1 from zeros is one step of the iteration
     y1, rho1, _ = oracle.deer_ode_step(w, u, dt)
     assert abs(rho1 - np.max(np.abs(y1))) == 0.0
+
+
+def test_deer_ode_stopping_test_is_strict():
+    # as the tanh form: a residual equal to eps does not stop the iteration
+    T, D = 300, 4
+    r = np.random.default_rng(45)
+    w = r.uniform(-0.9, 0.9, D)
+    u = r.standard_normal((T, 1, D))
+    dt = r.uniform(0.1, 1.0, T)
+    _, _, hist, _, _ = oracle.deer_ode(w, u, dt, eps=0.0, kmax=3)
+    assert hist[2] < hist[1]
+    _, k, _, st, _ = oracle.deer_ode(w, u, dt, eps=hist[1], kmax=20)
+    assert k > 2 and st == oracle.DEER_CONVERGED
 
 
 def test_deer_ode_clamp():
