@@ -62,6 +62,7 @@ def _load():
         lib.lro_scan_bwd.argtypes = [I64, I64, P, P, P, P, P, P, P]
         lib.lro_sru_fwd.argtypes = [I64, I64, I64] + [P] * 9
         lib.lro_sru_bwd.argtypes = [I64, I64, I64] + [P] * 15
+        lib.lro_sru_bwd.restype = ctypes.c_int
         lib.lro_lstm_fwd.argtypes = [I64, I64, I64] + [P] * 11
         lib.lro_lstm_bwd.argtypes = [I64, I64, I64] + [P] * 20
         lib.lro_lstm_bwd.restype = ctypes.c_int
@@ -69,6 +70,7 @@ def _load():
         lib.lro_deer_step.argtypes = [I64, I64, I64, P, P, P, P, P, P]
         lib.lro_deer.argtypes = [I64, I64, I64, P, P, P, P, ctypes.c_double, ctypes.c_int, P, P, P]
         lib.lro_deer_bwd.argtypes = [I64, I64, I64] + [P] * 7
+        lib.lro_deer_bwd.restype = ctypes.c_int
         lib.lro_rollout_ode.argtypes = [I64, I64, I64] + [P] * 6
         lib.lro_deer_ode_step.argtypes = [I64, I64, I64] + [P] * 8
         lib.lro_deer_ode.argtypes = [I64, I64, I64, P, P, P, P, ctypes.c_double, ctypes.c_int,
@@ -143,8 +145,10 @@ def sru_bwd(xt, uf, ur, x, bf, br, c, dh, c0=None):
     dxt, duf, dur, dx = (np.empty_like(xt) for _ in range(4))
     dbf, dbr = np.empty(D), np.empty(D)
     dc0 = np.empty(xt.shape[1:], dtype=np.float64)
-    _load().lro_sru_bwd(T, C, D, *map(_p, (xt, uf, ur, x, bf, br, c0, c, dh,
-                                            dxt, duf, dur, dx, dbf, dbr, dc0)))
+    st = _load().lro_sru_bwd(T, C, D, *map(_p, (xt, uf, ur, x, bf, br, c0, c, dh,
+                                                 dxt, duf, dur, dx, dbf, dbr, dc0)))
+    if st != 0:
+        raise MemoryError("oracle sru_bwd: allocation failed")
     return dxt, duf, dur, dx, dbf, dbr, dc0
 
 
@@ -205,7 +209,9 @@ def deer_bwd(w, y, g, h0=None):
     du = np.empty_like(y)
     dw = np.zeros(D)
     dh0 = np.empty(y.shape[1:]) if y.ndim == 3 else np.empty(C)
-    _load().lro_deer_bwd(T, C, D, _p(w), _p(y), _p(h0), _p(g), _p(du), _p(dw), _p(dh0))
+    st = _load().lro_deer_bwd(T, C, D, _p(w), _p(y), _p(h0), _p(g), _p(du), _p(dw), _p(dh0))
+    if st != 0:
+        raise MemoryError("oracle deer_bwd: allocation failed")
     return du, dw, dh0
 
 

@@ -155,17 +155,23 @@ void lro_sru_fwd(int64_t T, int64_t C, int64_t D, const double* xt,
  *   dU_f,t = dc_t (c_{t-1} - xt_t) f_t (1 - f_t)
  *   dc0    = f_0 dc_0
  *   db_f[d] = sum over t and batch of dU_f,  db_r[d] likewise of dU_r.
- * dc0 may be NULL.
+ * dc0 may be NULL.  Returns -1 when scratch allocation fails.
  */
-void lro_sru_bwd(int64_t T, int64_t C, int64_t D, const double* xt,
-                 const double* uf, const double* ur, const double* x,
-                 const double* bf, const double* br, const double* c0,
-                 const double* c, const double* dh, double* dxt, double* duf,
-                 double* dur, double* dx, double* dbf, double* dbr,
-                 double* dc0) {
-    double* dc = (double*)malloc(sizeof(double) * (size_t)(T * C));
-    double* sf = (double*)calloc((size_t)C, sizeof(double));
-    double* sr = (double*)calloc((size_t)C, sizeof(double));
+int lro_sru_bwd(int64_t T, int64_t C, int64_t D, const double* xt,
+                const double* uf, const double* ur, const double* x,
+                const double* bf, const double* br, const double* c0,
+                const double* c, const double* dh, double* dxt, double* duf,
+                double* dur, double* dx, double* dbf, double* dbr,
+                double* dc0) {
+    double* dc = (double*)malloc(sizeof(double) * (size_t)(T * C > 0 ? T * C : 1));
+    double* sf = (double*)calloc((size_t)(C > 0 ? C : 1), sizeof(double));
+    double* sr = (double*)calloc((size_t)(C > 0 ? C : 1), sizeof(double));
+    if (!dc || !sf || !sr) {
+        free(dc);
+        free(sf);
+        free(sr);
+        return -1;
+    }
     PAR_BEGIN
     /* memory-state gradient, reverse in time */
     for (int64_t t = T - 1; t >= 0; --t)
@@ -202,6 +208,7 @@ void lro_sru_bwd(int64_t T, int64_t C, int64_t D, const double* xt,
     free(dc);
     free(sf);
     free(sr);
+    return 0;
 }
 
 /* ------------------------------------------- LSTM cell-state scan (next) */
@@ -536,16 +543,14 @@ int lro_deer(int64_t T, int64_t C, int64_t D, const double* w, const double* u,
  *     (delta_t: total derivative of L = sum g.y with respect to y_t);
  *   du_t = delta_t (1 - y_t^2);  dw_d = sum over t and the channels of
  *   feature d of du_t y_{t-1} (y_{-1} = h0);  dh0 = w (1 - y_0^2) delta_0.
- * g is the upstream gradient dL/dy.  dh0 may be NULL.
+ * g is the upstream gradient dL/dy.  dh0 may be NULL.  Returns -1 when
+ * scratch allocation fails.
  */
-void lro_deer_bwd(int64_t T, int64_t C, int64_t D, const double* w,
-                  const double* y, const double* h0, const double* g, double* du,
-                  double* dw, double* dh0) {
+int lro_deer_bwd(int64_t T, int64_t C, int64_t D, const double* w,
+                 const double* y, const double* h0, const double* g, double* du,
+                 double* dw, double* dh0) {
     double* sw = (double*)calloc((size_t)(C > 0 ? C : 1), sizeof(double));
-    if (!sw) {
-        for (int64_t d = 0; d < D; ++d) dw[d] = NAN;
-        return;
-    }
+    if (!sw) return -1;
     PAR_BEGIN
     for (int64_t k = c0_; k < c1_; ++k) {
         const double wk = w[k % D];
@@ -564,4 +569,5 @@ void lro_deer_bwd(int64_t T, int64_t C, int64_t D, const double* w,
     for (int64_t d = 0; d < D; ++d) dw[d] = 0.0;
     for (int64_t k = 0; k < C; ++k) dw[k % D] += sw[k];
     free(sw);
+    return 0;
 }
