@@ -57,7 +57,9 @@
  *    second iterate buffer, residual slots, per-sequence stop state, clamp
  *    counters and the last iteration count of each DEER form and shape,
  *    bias-gradient partials), grown on demand with cudaMalloc.  Calls on
- *    different streams are serialised through it with CUDA events.
+ *    different streams are serialised through it with CUDA events.  A call
+ *    that returns LR_ERR_CUDA after it began enqueueing does not record its
+ *    event: synchronise the device before the next call on another stream.
  *  - Return value: LR_OK, or an lr_status describing an argument or launch
  *    error detected before or while enqueuing the work.  Errors detected on
  *    the device while the kernels run (a carry or copy wait that ran out) are
