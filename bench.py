@@ -54,20 +54,33 @@ NCU_TRAFFIC = {"deer.solve": {"bytes": 753228544, "src": "67b92c8d6ee481ff",
                               "file": "deer_kernels.cu"}}
 
 
+def code_hash(texts) -> str:
+    """Hash of source texts (an iterable of strings, in a fixed order) with
+    line comments, trailing blanks and blank lines left out."""
+    h = hashlib.sha256()
+    for text in texts:
+        for line in text.splitlines():
+            code = line.split("//", 1)[0].rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
+    return h.hexdigest()[:16]
+
+
 def src_hash(kernel_file: str = "deer_kernels.cu") -> str:
     """Hash of the code one operation's kernels are compiled from: the shared
     device headers, the launch configuration and that operation's kernel
-    file, comments and blank lines left out (the host-only C-ABI files and
-    the other operations' kernel files do not change its kernel)."""
-    h = hashlib.sha256()
+    file (the host-only C-ABI files and the other operations' kernel files do
+    not change its kernel)."""
     cdir = os.path.join(ROOT, "linear_recurrence_scan_chunked_gb300", "csrc")
-    for n in sorted(os.listdir(cdir)):
-        if n.endswith(".cuh") or n in ("lr_launch.h", kernel_file):
-            for line in open(os.path.join(cdir, n)):
-                code = line.split("//", 1)[0].rstrip()
-                if code:
-                    h.update(code.encode() + b"\n")
-    return h.hexdigest()[:16]
+    names = [n for n in sorted(os.listdir(cdir)) if n.endswith(".cuh") or n in ("lr_launch.h", kernel_file)]
+    return code_hash(open(os.path.join(cdir, n)).read() for n in names)
+
+
+def recorded_traffic(op: str):
+    """NCU_TRAFFIC's DRAM bytes per launch for `op`, or None when there is no
+    record or the kernel's sources changed since it was captured."""
+    tr = NCU_TRAFFIC.get(op)
+    return tr["bytes"] if tr and tr.get("src") == src_hash(tr["file"]) else None
 
 
 def peak_hbm():
@@ -775,8 +788,7 @@ def main():
     launch_ms = ops[dom]["ms"] / ops[dom]["launches"]
     bytes_per_launch = pass_bytes(dwl, dp, k) / ops[dom]["launches"]
     achieved = bytes_per_launch / (launch_ms / 1e3) / 1e9
-    tr = NCU_TRAFFIC.get(dom)
-    traffic = tr["bytes"] if tr and tr.get("src") == src_hash(tr["file"]) else None
+    traffic = recorded_traffic(dom)
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": dom,
             "peak_source": f"{peak_kind} HBM copy bandwidth",

@@ -53,3 +53,38 @@ def test_two_rank_max_timing():
     out = mp.Manager().dict()
     mp.spawn(_worker, args=(port, out), nprocs=2, join=True)
     assert dict(out) == {0: 11.0, 1: 11.0}
+
+
+def test_code_hash_ignores_comments_and_blank_lines():
+    src = "int f(int x) {\n    return x + 1;  // one more\n}\n"
+    same = "// a header comment\nint f(int x) {\n\n    return x + 1;   \n}\n"
+    other = "int f(int x) {\n    return x + 2;\n}\n"
+    assert bench.code_hash([src]) == bench.code_hash([same])
+    assert bench.code_hash([src]) != bench.code_hash([other])
+    assert bench.code_hash([src, other]) != bench.code_hash([other, src])
+
+
+def test_recorded_traffic_needs_the_captured_sources(monkeypatch):
+    rec = bench.NCU_TRAFFIC["deer.solve"]
+    monkeypatch.setattr(bench, "NCU_TRAFFIC", {
+        "ok": dict(rec, src=bench.src_hash(rec["file"])),
+        "stale": dict(rec, src="0" * 16)})
+    assert bench.recorded_traffic("ok") == rec["bytes"]
+    assert bench.recorded_traffic("stale") is None
+    assert bench.recorded_traffic("absent") is None
+
+
+def test_clock_summary():
+    c = bench.Clocks(0)
+    na = "Not Active"
+    c.lines = [
+        f"0, 2070, 2070, 812.3, 0x0000000000000000, {na}, {na}, {na}, {na}\n",
+        f"0, 1965, 2070, 1390.0, 0x0000000000000004, {na}, {na}, {na}, Active\n",
+        f"0, 2070, 2070, 900.1, 0x0000000000000000, {na}, {na}, {na}, {na}\n",
+        "garbage line\n",
+        "0, [N/A], 2070, 1.0, 0x0, x, x, x, x\n",
+    ]
+    s = c.summary()
+    assert s == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    c.lines = []
+    assert bench.Clocks(0).summary()["samples"] == 0
