@@ -106,8 +106,16 @@ def _p(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream):
+def _stream(stream, ref=None):
+    """The stream handle for a call on `ref`'s tensors: those tensors must be on
+    the current CUDA device (the library launches there) and an explicit
+    stream must belong to it."""
+    if ref is not None and ref.device.index != torch.cuda.current_device():
+        raise ValueError(f"the tensors are on {ref.device} but the current CUDA device is "
+                         f"cuda:{torch.cuda.current_device()}: call under torch.cuda.device({ref.device})")
     s = stream if stream is not None else torch.cuda.current_stream()
+    if ref is not None and s.device != ref.device:
+        raise ValueError(f"the stream belongs to {s.device}, the tensors to {ref.device}")
     return ctypes.c_void_p(s.cuda_stream)
 
 
@@ -127,12 +135,16 @@ def _state(name, t, ref):
     T, B, D = ref.shape
     if tuple(t.shape) != (B, D) or t.dtype != ref.dtype or not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous [B, D] CUDA tensor of the storage dtype")
+    if t.device != ref.device:
+        raise ValueError(f"{name} is on {t.device}, the sequence tensors on {ref.device}")
     return t
 
 
-def _param(name, t, D):
+def _param(name, t, D, ref):
     if t.dtype != torch.float32 or tuple(t.shape) != (D,) or not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous fp32 [D] CUDA tensor")
+    if t.device != ref.device:
+        raise ValueError(f"{name} is on {t.device}, the sequence tensors on {ref.device}")
     return t
 
 
@@ -143,7 +155,7 @@ def lr_scan_fwd(a, b, h0=None, h=None, stream=None):
     _state("h0", h0, a)
     h = torch.empty_like(a) if h is None else _seq("h", h, a)
     T, B, D = a.shape
-    _check(load().lr_scan_fwd(_p(a), _p(b), _p(h0), _p(h), B, T, D, _code(a), _stream(stream)))
+    _check(load().lr_scan_fwd(_p(a), _p(b), _p(h0), _p(h), B, T, D, _code(a), _stream(stream, a)))
     return h
 
 
@@ -160,7 +172,7 @@ def lr_scan_bwd(a, h, dh, h0=None, da=None, db=None, dh0=None, want_dh0=True, st
         dh0 = torch.empty((B, D), dtype=a.dtype, device=a.device)
     _state("dh0", dh0, a)
     _check(load().lr_scan_bwd(_p(a), _p(h), _p(h0), _p(dh), _p(da), _p(db), _p(dh0), B, T, D,
-                              _code(a), _stream(stream)))
+                              _code(a), _stream(stream, a)))
     return da, db, dh0
 
 
@@ -170,13 +182,13 @@ def sru_fwd(xt, uf, ur, x, bf, br, c0=None, h=None, c=None, stream=None):
     for n, t in (("uf", uf), ("ur", ur), ("x", x)):
         _seq(n, t, xt)
     T, B, D = xt.shape
-    _param("bf", bf, D)
-    _param("br", br, D)
+    _param("bf", bf, D, xt)
+    _param("br", br, D, xt)
     _state("c0", c0, xt)
     h = torch.empty_like(xt) if h is None else _seq("h", h, xt)
     c = torch.empty_like(xt) if c is None else _seq("c", c, xt)
     _check(load().sru_fwd(_p(xt), _p(uf), _p(ur), _p(x), _p(bf), _p(br), _p(c0), _p(h), _p(c),
-                          B, T, D, _code(xt), _stream(stream)))
+                          B, T, D, _code(xt), _stream(stream, xt)))
     return h, c
 
 
@@ -186,20 +198,20 @@ def sru_bwd(xt, uf, ur, x, bf, br, c, dh, c0=None, out=None, want_dc0=True, stre
     for n, t in (("uf", uf), ("ur", ur), ("x", x), ("c", c), ("dh", dh)):
         _seq(n, t, xt)
     T, B, D = xt.shape
-    _param("bf", bf, D)
-    _param("br", br, D)
+    _param("bf", bf, D, xt)
+    _param("br", br, D, xt)
     _state("c0", c0, xt)
     o = dict(out or {})
     for k in ("dxt", "duf", "dur", "dx"):
         o[k] = torch.empty_like(xt) if o.get(k) is None else _seq(k, o[k], xt)
     for k in ("dbf", "dbr"):
-        o[k] = torch.empty(D, dtype=torch.float32, device=xt.device) if o.get(k) is None else _param(k, o[k], D)
+        o[k] = torch.empty(D, dtype=torch.float32, device=xt.device) if o.get(k) is None else _param(k, o[k], D, xt)
     if o.get("dc0") is None and want_dc0:
         o["dc0"] = torch.empty((B, D), dtype=xt.dtype, device=xt.device)
     _state("dc0", o.get("dc0"), xt)
     _check(load().sru_bwd(_p(xt), _p(uf), _p(ur), _p(x), _p(bf), _p(br), _p(c0), _p(c), _p(dh),
                           _p(o["dxt"]), _p(o["duf"]), _p(o["dur"]), _p(o["dx"]), _p(o["dbf"]),
-                          _p(o["dbr"]), _p(o.get("dc0")), B, T, D, _code(xt), _stream(stream)))
+                          _p(o["dbr"]), _p(o.get("dc0")), B, T, D, _code(xt), _stream(stream, xt)))
     return o
 
 
@@ -211,12 +223,12 @@ def lstm_cell_fwd(zf, zi, zc, zo, bf, bi, bc, bo, c0=None, h=None, c=None, strea
         _seq(n, t, zf)
     T, B, D = zf.shape
     for n, t in (("bf", bf), ("bi", bi), ("bc", bc), ("bo", bo)):
-        _param(n, t, D)
+        _param(n, t, D, zf)
     _state("c0", c0, zf)
     h = torch.empty_like(zf) if h is None else _seq("h", h, zf)
     c = torch.empty_like(zf) if c is None else _seq("c", c, zf)
     _check(load().lstm_cell_fwd(_p(zf), _p(zi), _p(zc), _p(zo), _p(bf), _p(bi), _p(bc), _p(bo),
-                                _p(c0), _p(h), _p(c), B, T, D, _code(zf), _stream(stream)))
+                                _p(c0), _p(h), _p(c), B, T, D, _code(zf), _stream(stream, zf)))
     return h, c
 
 
@@ -228,13 +240,13 @@ def lstm_cell_bwd(zf, zi, zc, zo, bf, bi, bc, bo, c, dh, c0=None, out=None, want
         _seq(n, t, zf)
     T, B, D = zf.shape
     for n, t in (("bf", bf), ("bi", bi), ("bc", bc), ("bo", bo)):
-        _param(n, t, D)
+        _param(n, t, D, zf)
     _state("c0", c0, zf)
     o = dict(out or {})
     for k in ("dzf", "dzi", "dzc", "dzo"):
         o[k] = torch.empty_like(zf) if o.get(k) is None else _seq(k, o[k], zf)
     for k in ("dbf", "dbi", "dbc", "dbo"):
-        o[k] = torch.empty(D, dtype=torch.float32, device=zf.device) if o.get(k) is None else _param(k, o[k], D)
+        o[k] = torch.empty(D, dtype=torch.float32, device=zf.device) if o.get(k) is None else _param(k, o[k], D, zf)
     if o.get("dc0") is None and want_dc0:
         o["dc0"] = torch.empty((B, D), dtype=zf.dtype, device=zf.device)
     _state("dc0", o.get("dc0"), zf)
@@ -242,7 +254,7 @@ def lstm_cell_bwd(zf, zi, zc, zo, bf, bi, bc, bo, c, dh, c0=None, out=None, want
                                 _p(c0), _p(c), _p(dh), _p(o["dzf"]), _p(o["dzi"]), _p(o["dzc"]),
                                 _p(o["dzo"]), _p(o["dbf"]), _p(o["dbi"]), _p(o["dbc"]),
                                 _p(o["dbo"]), _p(o.get("dc0")), B, T, D, _code(zf),
-                                _stream(stream)))
+                                _stream(stream, zf)))
     return o
 
 
@@ -253,7 +265,7 @@ def deer_diag_solve(w, u, h0=None, y=None, eps=1e-5, kmax=20, stream=None):
     LR_ERR_NOT_CONVERGED or LR_ERR_NONFINITE (other statuses raise)."""
     _seq("u", u)
     T, B, D = u.shape
-    _param("w", w, D)
+    _param("w", w, D, u)
     _state("h0", h0, u)
     y = torch.empty_like(u) if y is None else _seq("y", y, u)
     iters = ctypes.c_int(0)
@@ -261,7 +273,7 @@ def deer_diag_solve(w, u, h0=None, y=None, eps=1e-5, kmax=20, stream=None):
     hist = (ctypes.c_float * max(1, int(kmax)))()
     st = load().deer_diag_solve(_p(w), _p(u), _p(h0), _p(y), B, T, D, ctypes.c_float(eps),
                                 int(kmax), ctypes.byref(iters), ctypes.byref(resid), hist,
-                                _code(u), _stream(stream))
+                                _code(u), _stream(stream, u))
     if st not in (LR_OK, LR_ERR_NOT_CONVERGED, LR_ERR_NONFINITE):
         _check(st)
     k = iters.value
@@ -276,7 +288,7 @@ def deer_diag_solve_ex(w, u, h0=None, y=None, y_init=None, eps=1e-5, kmax=20,
     seq_resid[B], launches (iteration kernels enqueued)."""
     _seq("u", u)
     T, B, D = u.shape
-    _param("w", w, D)
+    _param("w", w, D, u)
     _state("h0", h0, u)
     if y_init is not None:
         _seq("y_init", y_init, u)
@@ -290,7 +302,7 @@ def deer_diag_solve_ex(w, u, h0=None, y=None, y_init=None, eps=1e-5, kmax=20,
     st = load().deer_diag_solve_ex(_p(w), _p(u), _p(h0), _p(y_init), _p(y), B, T, D,
                                    ctypes.c_float(eps), int(kmax), 1 if per_sequence else 0,
                                    ctypes.byref(it), ctypes.byref(rho), hist, sk, sr,
-                                   ctypes.byref(nl), _code(u), _stream(stream))
+                                   ctypes.byref(nl), _code(u), _stream(stream, u))
     if st not in (LR_OK, LR_ERR_NOT_CONVERGED, LR_ERR_NONFINITE):
         _check(st)
     k = int(it.value)
@@ -304,8 +316,8 @@ def deer_ode_solve(w, u, dt, h0=None, y=None, eps=1e-5, kmax=20, stream=None):
     clamps of the last iteration)."""
     _seq("u", u)
     T, B, D = u.shape
-    _param("w", w, D)
-    _param("dt", dt, T)
+    _param("w", w, D, u)
+    _param("dt", dt, T, u)
     _state("h0", h0, u)
     y = torch.empty_like(u) if y is None else _seq("y", y, u)
     iters = ctypes.c_int(0)
@@ -314,7 +326,7 @@ def deer_ode_solve(w, u, dt, h0=None, y=None, eps=1e-5, kmax=20, stream=None):
     hist = (ctypes.c_float * max(1, int(kmax)))()
     st = load().deer_ode_solve(_p(w), _p(u), _p(dt), _p(h0), _p(y), B, T, D, ctypes.c_float(eps),
                                int(kmax), ctypes.byref(iters), ctypes.byref(resid), hist,
-                               ctypes.byref(clamps), _code(u), _stream(stream))
+                               ctypes.byref(clamps), _code(u), _stream(stream, u))
     if st not in (LR_OK, LR_ERR_NOT_CONVERGED, LR_ERR_NONFINITE):
         _check(st)
     k = iters.value
@@ -327,15 +339,15 @@ def deer_diag_bwd(w, y, dy, h0=None, du=None, dw=None, dh0=None, want_dh0=True, 
     _seq("y", y)
     _seq("dy", dy, y)
     T, B, D = y.shape
-    _param("w", w, D)
+    _param("w", w, D, y)
     _state("h0", h0, y)
     du = torch.empty_like(y) if du is None else _seq("du", du, y)
-    dw = torch.empty(D, dtype=torch.float32, device=y.device) if dw is None else _param("dw", dw, D)
+    dw = torch.empty(D, dtype=torch.float32, device=y.device) if dw is None else _param("dw", dw, D, y)
     if dh0 is None and want_dh0:
         dh0 = torch.empty((B, D), dtype=y.dtype, device=y.device)
     _state("dh0", dh0, y)
     _check(load().deer_diag_bwd(_p(w), _p(y), _p(h0), _p(dy), _p(du), _p(dw), _p(dh0), B, T, D,
-                                _code(y), _stream(stream)))
+                                _code(y), _stream(stream, y)))
     return du, dw, dh0
 
 
@@ -356,7 +368,7 @@ def test_activations(x, stream=None, with_expm1=False):
         raise ValueError("x must be a contiguous fp32 CUDA tensor")
     th, sg = torch.empty_like(x), torch.empty_like(x)
     em = torch.empty_like(x) if with_expm1 else None
-    _check(load().lr_test_activations(_p(x), _p(th), _p(sg), _p(em), x.numel(), _stream(stream)))
+    _check(load().lr_test_activations(_p(x), _p(th), _p(sg), _p(em), x.numel(), _stream(stream, x)))
     return (th, sg, em) if with_expm1 else (th, sg)
 
 

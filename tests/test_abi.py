@@ -98,3 +98,37 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(lrs, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         lrs.load()
+
+
+def _fake_cuda_tensor(shape, dtype, device):
+    """Stands in for a CUDA tensor in the binding's checks (no device here)."""
+    import types
+    import torch
+    return types.SimpleNamespace(shape=torch.Size(shape), dtype=dtype, device=torch.device(device),
+                                 is_cuda=True, dim=lambda: len(shape), is_contiguous=lambda: True)
+
+
+def test_binding_rejects_tensors_on_another_device(monkeypatch):
+    """States, per-feature parameters and the stream must be on the sequence
+    tensors' device, and that device must be the current one (the library
+    launches on the current device)."""
+    import types
+    import torch
+    f32 = torch.float32
+    u = _fake_cuda_tensor((5, 2, 4), f32, "cuda:0")
+    assert lrs._state("h0", _fake_cuda_tensor((2, 4), f32, "cuda:0"), u) is not None
+    assert lrs._param("w", _fake_cuda_tensor((4,), f32, "cuda:0"), 4, u) is not None
+    with pytest.raises(ValueError, match="cuda:1"):
+        lrs._state("h0", _fake_cuda_tensor((2, 4), f32, "cuda:1"), u)
+    with pytest.raises(ValueError, match="cuda:1"):
+        lrs._param("w", _fake_cuda_tensor((4,), f32, "cuda:1"), 4, u)
+    with pytest.raises(ValueError, match="match"):
+        lrs._seq("b", _fake_cuda_tensor((5, 2, 4), f32, "cuda:1"), u)
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    s0 = types.SimpleNamespace(device=torch.device("cuda:0"), cuda_stream=0)
+    s1 = types.SimpleNamespace(device=torch.device("cuda:1"), cuda_stream=0)
+    assert lrs._stream(s0, u).value is None  # handle 0: the legacy default stream
+    with pytest.raises(ValueError, match="stream belongs"):
+        lrs._stream(s1, u)
+    with pytest.raises(ValueError, match="current CUDA device"):
+        lrs._stream(s1, _fake_cuda_tensor((5, 2, 4), f32, "cuda:1"))
