@@ -132,3 +132,48 @@ def test_binding_rejects_tensors_on_another_device(monkeypatch):
         lrs._stream(s1, u)
     with pytest.raises(ValueError, match="current CUDA device"):
         lrs._stream(s1, _fake_cuda_tensor((5, 2, 4), f32, "cuda:1"))
+
+
+def test_binding_call_paths_reach_the_library(lib, monkeypatch):
+    """Every public call marshals its arguments through the real library's
+    prototypes (ctypes checks their count and types).  With stand-in CUDA
+    tensors at address 0 the library answers LR_ERR_INVALID_ARG before any
+    CUDA call, and the binding raises it as LrError."""
+    import types
+    import torch
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    monkeypatch.setattr(torch.cuda, "current_stream",
+                        lambda *a, **k: types.SimpleNamespace(device=torch.device("cuda:0"), cuda_stream=0))
+    T, B, D = 5, 2, 4
+
+    def t(*shape):
+        x = _fake_cuda_tensor(shape, torch.float32, "cuda:0")
+        x.data_ptr = lambda: 0
+        return x
+
+    def seq():
+        return t(T, B, D)
+
+    calls = [
+        lambda: lrs.lr_scan_fwd(seq(), seq(), t(B, D), h=seq()),
+        lambda: lrs.lr_scan_bwd(seq(), seq(), seq(), t(B, D), da=seq(), db=seq(), dh0=t(B, D)),
+        lambda: lrs.sru_fwd(seq(), seq(), seq(), seq(), t(D), t(D), t(B, D), h=seq(), c=seq()),
+        lambda: lrs.sru_bwd(seq(), seq(), seq(), seq(), t(D), t(D), seq(), seq(), t(B, D),
+                            out={"dxt": seq(), "duf": seq(), "dur": seq(), "dx": seq(), "dbf": t(D),
+                                 "dbr": t(D), "dc0": t(B, D)}),
+        lambda: lrs.lstm_cell_fwd(seq(), seq(), seq(), seq(), t(D), t(D), t(D), t(D), t(B, D),
+                                  h=seq(), c=seq()),
+        lambda: lrs.lstm_cell_bwd(seq(), seq(), seq(), seq(), t(D), t(D), t(D), t(D), seq(), seq(),
+                                  t(B, D), out={"dzf": seq(), "dzi": seq(), "dzc": seq(), "dzo": seq(),
+                                                "dbf": t(D), "dbi": t(D), "dbc": t(D), "dbo": t(D),
+                                                "dc0": t(B, D)}),
+        lambda: lrs.deer_diag_solve(t(D), seq(), t(B, D), y=seq()),
+        lambda: lrs.deer_diag_solve_ex(t(D), seq(), t(B, D), y=seq(), y_init=seq()),
+        lambda: lrs.deer_diag_solve_ex(t(D), seq(), y=seq(), per_sequence=True),
+        lambda: lrs.deer_ode_solve(t(D), seq(), t(T), t(B, D), y=seq()),
+        lambda: lrs.deer_diag_bwd(t(D), seq(), seq(), t(B, D), du=seq(), dw=t(D), dh0=t(B, D)),
+    ]
+    for call in calls:
+        with pytest.raises(lrs.LrError) as e:
+            call()
+        assert e.value.status == lrs.LR_ERR_INVALID_ARG
