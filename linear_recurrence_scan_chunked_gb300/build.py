@@ -66,16 +66,20 @@ def build(force: bool = False, verbose: bool = False) -> str:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr[-4000:]}")
         return obj
 
-    with ThreadPoolExecutor(max(1, min(len(sources()), os.cpu_count() or 1))) as ex:
-        objs = list(ex.map(compile_one, sources()))
+    objs = [os.path.join(OUT_DIR, os.path.basename(s) + f".{tag}.o") for s in sources()]
     tmp = LIB + f".{tag}.tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    for o in objs:
-        os.remove(o)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stderr[-4000:]}")
-    os.replace(tmp, LIB)
+    try:
+        with ThreadPoolExecutor(max(1, min(len(sources()), os.cpu_count() or 1))) as ex:
+            list(ex.map(compile_one, sources()))
+        cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stderr[-4000:]}")
+        os.replace(tmp, LIB)
+    finally:  # no objects or partial library left behind, whatever failed
+        for f in objs + [tmp]:
+            if os.path.exists(f):
+                os.remove(f)
     if verbose:
         print("built", LIB)
     return LIB
