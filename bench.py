@@ -608,6 +608,7 @@ def config_dict():
     return {"workload": "; ".join(f"{n} {wl.dtype} T={wl.T} B={wl.B} D={wl.D} "
                                   f"{'+'.join(p)}" for n, wl, p in ROWS),
             "layout": "[T,B,D], D contiguous", "seed": 0,
+            "storage": "as each workload names it (f32 or bf16); arithmetic in f32",
             "l2": "inputs larger than the 129 MB L2 except scan_tiny (12.6 MB); each step streams ~18 GB",
             "deer": {"eps": EPS, "kmax": KMAX},
             "distributions": "see workloads/__init__.py (N(0,0.01) read as std 0.01)"}
@@ -796,7 +797,7 @@ def main():
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32 compute (f32 and bf16 storage)",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": config_dict(),
             "hbm_GBps": round(gbs, 1), "hbm_frac": round(gbs / peak, 4), "deer_iters": k_med,
             "deer_resid_history": [float(f"{r:.3e}") for r in getattr(b, "hist_last", [])],
