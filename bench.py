@@ -83,17 +83,34 @@ def recorded_traffic(op: str):
     return tr["bytes"] if tr and tr.get("src") == src_hash(tr["file"]) else None
 
 
+def hbm_peak_from(d):
+    """The measured HBM copy bandwidth (GB/s) in a parsed peaks file, or None:
+    a number under hbm_gbs / hbm_GBs / hbm, or that key's value, burst or
+    (failing both) sustained entry -- the kernels are timed on their own, so
+    the burst figure is the one that applies."""
+    if not isinstance(d, dict):
+        return None
+    for k in ("hbm_gbs", "hbm_GBs", "hbm"):
+        if k in d:
+            v = d[k]
+            if isinstance(v, dict):
+                v = v.get("value", v.get("burst", v.get("sustained")))
+            try:
+                v = float(v)
+            except (TypeError, ValueError):
+                return None
+            return v if v > 0 else None
+    return None
+
+
 def peak_hbm():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         try:
-            d = json.load(open(p))
-            for k in ("hbm_gbs", "hbm_GBs", "hbm"):
-                if k in d:
-                    v = d[k]
-                    v = v.get("value", v.get("burst")) if isinstance(v, dict) else v
-                    return float(v), "measured"
-        except Exception:
+            v = hbm_peak_from(json.load(open(p)))
+            if v is not None:
+                return v, "measured"
+        except (OSError, ValueError):
             pass
     return FALLBACK_HBM_GBS, "fallback"
 

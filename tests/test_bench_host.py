@@ -88,3 +88,15 @@ def test_clock_summary():
     assert s == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
     c.lines = []
     assert bench.Clocks(0).summary()["samples"] == 0
+
+
+def test_measured_peak_parsing():
+    assert bench.hbm_peak_from({"hbm_gbs": 7012.5}) == 7012.5
+    assert bench.hbm_peak_from({"hbm_gbs": {"value": 7100, "clock_mhz": 2070}}) == 7100.0
+    assert bench.hbm_peak_from({"hbm": {"burst": "7200"}}) == 7200.0
+    assert bench.hbm_peak_from({"bf16_tflops": 1900}) is None
+    assert bench.hbm_peak_from({"hbm_gbs": None}) is None
+    assert bench.hbm_peak_from({"hbm_gbs": {"burst": 7300, "sustained": 7000}}) == 7300.0
+    assert bench.hbm_peak_from({"hbm_gbs": {"sustained": 7000}}) == 7000.0
+    assert bench.hbm_peak_from(["hbm_gbs"]) is None
+    assert bench.hbm_peak_from({"hbm_gbs": 0}) is None
