@@ -84,10 +84,16 @@ def sigmoid_of_normal(seed, tid, shape, mean=0.0, std=1.0) -> np.ndarray:
 # ------------------------------------------------------------ storage formats
 
 def f32_to_bf16(x: np.ndarray) -> np.ndarray:
-    """Round float32 to bfloat16 (nearest-even); returns uint16 bit patterns."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    r = (u.astype(np.uint64) + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return r.astype(np.uint16)
+    """Round float32 to bfloat16 (nearest-even); returns uint16 bit patterns.
+    A NaN stays a NaN (the quiet NaN 0x7FC0, sign kept): adding the rounding
+    bias to a NaN with a small payload would carry into an infinity."""
+    x32 = np.ascontiguousarray(x, dtype=np.float32)
+    u = x32.view(np.uint32)
+    r = ((u.astype(np.uint64) + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    nan = np.isnan(x32)
+    if nan.any():
+        r = np.where(nan, ((u >> 16) & 0x8000).astype(np.uint16) | np.uint16(0x7FC0), r)
+    return r
 
 
 def bf16_to_f32(u16: np.ndarray) -> np.ndarray:
