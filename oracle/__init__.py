@@ -108,10 +108,33 @@ def _tc(x):
     return T, int(np.prod(x.shape[1:])) if x.ndim > 1 else 1
 
 
+def _shapes(ref, seqs=(), feats=(), states=(), steps=()):
+    """(T, C) of sequence tensor `ref`, after checking the shapes the C code
+    trusts: every other sequence tensor shaped like ref, the per-feature
+    arrays one length D dividing C, the initial states C values, the
+    per-step arrays T values (None = absent)."""
+    T, C = _tc(ref)
+    for x in seqs:
+        if x is not None and x.shape != ref.shape:
+            raise ValueError(f"sequence tensor of shape {x.shape}, expected {ref.shape}")
+    lens = {x.size for x in feats}
+    if feats and (len(lens) != 1 or any(x.ndim != 1 for x in feats)):
+        raise ValueError("per-feature arrays must be 1-D and of one length")
+    if feats and C and (next(iter(lens)) == 0 or C % next(iter(lens))):
+        raise ValueError(f"per-feature length {next(iter(lens))} does not divide {C} channels")
+    for x in states:
+        if x is not None and x.size != C:
+            raise ValueError(f"initial state of {x.size} values, expected {C}")
+    for x in steps:
+        if x.shape != (T,):
+            raise ValueError(f"per-step array of shape {x.shape}, expected ({T},)")
+    return T, C
+
+
 def scan_fwd(a, b, h0=None):
     """h_t = a_t h_{t-1} + b_t along axis 0; returns fp64 h shaped like a."""
     a, b, h0 = _f64(a), _f64(b), _f64(h0)
-    T, C = _tc(a)
+    T, C = _shapes(a, seqs=(b,), states=(h0,))
     h = np.empty_like(a)
     _load().lro_scan_fwd(T, C, _p(a), _p(b), _p(h0), _p(h))
     return h
@@ -120,7 +143,7 @@ def scan_fwd(a, b, h0=None):
 def scan_bwd(a, h, g, h0=None):
     """Returns (da, db, dh0) for loss sum(g * h), given the forward h."""
     a, h, g, h0 = _f64(a), _f64(h), _f64(g), _f64(h0)
-    T, C = _tc(a)
+    T, C = _shapes(a, seqs=(h, g), states=(h0,))
     da, db = np.empty_like(a), np.empty_like(a)
     dh0 = np.empty(a.shape[1:], dtype=np.float64)
     _load().lro_scan_bwd(T, C, _p(a), _p(h), _p(h0), _p(g), _p(da), _p(db), _p(dh0))
@@ -130,7 +153,7 @@ def scan_bwd(a, h, g, h0=None):
 def sru_fwd(xt, uf, ur, x, bf, br, c0=None):
     """Returns (h, c). Sequence tensors [T, B, D]; bf, br [D]."""
     xt, uf, ur, x, bf, br, c0 = map(_f64, (xt, uf, ur, x, bf, br, c0))
-    T, C = _tc(xt)
+    T, C = _shapes(xt, seqs=(uf, ur, x), feats=(bf, br), states=(c0,))
     D = bf.shape[0]
     h, c = np.empty_like(xt), np.empty_like(xt)
     _load().lro_sru_fwd(T, C, D, *map(_p, (xt, uf, ur, x, bf, br, c0, h, c)))
@@ -140,7 +163,7 @@ def sru_fwd(xt, uf, ur, x, bf, br, c0=None):
 def sru_bwd(xt, uf, ur, x, bf, br, c, dh, c0=None):
     """Returns (dxt, duf, dur, dx, dbf, dbr, dc0) given the forward c."""
     xt, uf, ur, x, bf, br, c, dh, c0 = map(_f64, (xt, uf, ur, x, bf, br, c, dh, c0))
-    T, C = _tc(xt)
+    T, C = _shapes(xt, seqs=(uf, ur, x, c, dh), feats=(bf, br), states=(c0,))
     D = bf.shape[0]
     dxt, duf, dur, dx = (np.empty_like(xt) for _ in range(4))
     dbf, dbr = np.empty(D), np.empty(D)
@@ -156,7 +179,7 @@ def lstm_fwd(zf, zi, zc, zo, bf, bi, bc, bo, c0=None):
     """LSTM cell-state scan with its gates; returns (h, c).  Pre-activations
     [T, B, D]; biases [D]; c0 [B, D] (None = zeros)."""
     zf, zi, zc, zo, bf, bi, bc, bo, c0 = map(_f64, (zf, zi, zc, zo, bf, bi, bc, bo, c0))
-    T, C = _tc(zf)
+    T, C = _shapes(zf, seqs=(zi, zc, zo), feats=(bf, bi, bc, bo), states=(c0,))
     D = bf.shape[0]
     h, c = np.empty_like(zf), np.empty_like(zf)
     _load().lro_lstm_fwd(T, C, D, *map(_p, (zf, zi, zc, zo, bf, bi, bc, bo, c0, h, c)))
@@ -168,7 +191,7 @@ def lstm_bwd(zf, zi, zc, zo, bf, bi, bc, bo, c, dh, c0=None):
     Returns (dzf, dzi, dzc, dzo, dbf, dbi, dbc, dbo, dc0)."""
     zf, zi, zc, zo, bf, bi, bc, bo, c, dh, c0 = map(
         _f64, (zf, zi, zc, zo, bf, bi, bc, bo, c, dh, c0))
-    T, C = _tc(zf)
+    T, C = _shapes(zf, seqs=(zi, zc, zo, c, dh), feats=(bf, bi, bc, bo), states=(c0,))
     D = bf.shape[0]
     dz = [np.empty_like(zf) for _ in range(4)]
     db = [np.empty(D) for _ in range(4)]
@@ -183,7 +206,7 @@ def lstm_bwd(zf, zi, zc, zo, bf, bi, bc, bo, c, dh, c0=None):
 def rollout_tanh(w, u, h0=None):
     """Direct sequential h_t = tanh(w h_{t-1} + u_t)."""
     w, u, h0 = _f64(w), _f64(u), _f64(h0)
-    T, C = _tc(u)
+    T, C = _shapes(u, feats=(w,), states=(h0,))
     y = np.empty_like(u)
     _load().lro_rollout_tanh(T, C, w.shape[0], _p(w), _p(u), _p(h0), _p(y))
     return y
@@ -192,7 +215,7 @@ def rollout_tanh(w, u, h0=None):
 def deer_step(w, u, yprev=None, h0=None):
     """One Newton step from yprev (None = all-zero guess); returns (ynew, rho)."""
     w, u, yprev, h0 = _f64(w), _f64(u), _f64(yprev), _f64(h0)
-    T, C = _tc(u)
+    T, C = _shapes(u, seqs=(yprev,), feats=(w,), states=(h0,))
     y = np.empty_like(u)
     rho = ctypes.c_double(0.0)
     _load().lro_deer_step(T, C, w.shape[0], _p(w), _p(u), _p(h0), _p(yprev), _p(y),
@@ -204,7 +227,7 @@ def deer_bwd(w, y, g, h0=None):
     """Gradient through the DEER solution y (the tanh-RNN rollout) for the
     upstream dL/dy = g. Returns (du, dw, dh0)."""
     w, y, g, h0 = _f64(w), _f64(y), _f64(g), _f64(h0)
-    T, C = _tc(y)
+    T, C = _shapes(y, seqs=(g,), feats=(w,), states=(h0,))
     D = w.shape[0]
     du = np.empty_like(y)
     dw = np.zeros(D)
@@ -222,7 +245,7 @@ def deer(w, u, h0=None, eps=1e-5, kmax=20, y_init=None):
     """Returns (y, iters, rho_history, status) -- status 0 converged, 1 hit kmax,
     2 not finite.  y_init: the initial guess (None = zeros)."""
     w, u, h0, y_init = _f64(w), _f64(u), _f64(h0), _f64(y_init)
-    T, C = _tc(u)
+    T, C = _shapes(u, seqs=(y_init,), feats=(w,), states=(h0,))
     y = np.empty_like(u)
     hist = np.zeros(kmax, dtype=np.float64)
     iters = ctypes.c_int(0)
@@ -255,7 +278,7 @@ def rollout_ode(w, u, dt, h0=None):
     """Exponential-Euler rollout of dy/dt = -y + tanh(w y + u) on steps dt[t]
     (G clamped to [-10, 10]).  Returns (y, clamps)."""
     w, u, dt, h0 = _f64(w), _f64(u), _f64(dt), _f64(h0)
-    T, C = _tc(u)
+    T, C = _shapes(u, feats=(w,), states=(h0,), steps=(dt,))
     y = np.empty_like(u)
     n = ctypes.c_int64(0)
     _load().lro_rollout_ode(T, C, w.shape[0], _p(w), _p(u), _p(dt), _p(h0), _p(y), ctypes.byref(n))
@@ -265,7 +288,7 @@ def rollout_ode(w, u, dt, h0=None):
 def deer_ode_step(w, u, dt, yprev=None, h0=None):
     """One ODE-form DEER iteration from yprev (None = zeros): (ynew, rho, clamps)."""
     w, u, dt, yprev, h0 = _f64(w), _f64(u), _f64(dt), _f64(yprev), _f64(h0)
-    T, C = _tc(u)
+    T, C = _shapes(u, seqs=(yprev,), feats=(w,), states=(h0,), steps=(dt,))
     y = np.empty_like(u)
     rho = ctypes.c_double(0.0)
     n = ctypes.c_int64(0)
@@ -277,7 +300,7 @@ def deer_ode_step(w, u, dt, yprev=None, h0=None):
 def deer_ode(w, u, dt, h0=None, eps=1e-5, kmax=20):
     """ODE-form DEER: (y, iters, rho_history, status, clamps of the last iteration)."""
     w, u, dt, h0 = _f64(w), _f64(u), _f64(dt), _f64(h0)
-    T, C = _tc(u)
+    T, C = _shapes(u, feats=(w,), states=(h0,), steps=(dt,))
     y = np.empty_like(u)
     hist = np.zeros(kmax, dtype=np.float64)
     iters = ctypes.c_int(0)

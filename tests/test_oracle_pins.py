@@ -703,3 +703,24 @@ def test_oracle_threads_do_not_change_results():
     h4 = oracle.scan_fwd(a, b)
     oracle.set_num_threads(0)
     assert np.array_equal(h1, h4)
+
+
+def test_oracle_rejects_shapes_it_would_misread():
+    # the C code trusts its sizes: the wrappers check them first
+    u = np.zeros((6, 2, 4))
+    w = np.zeros(4)
+    with pytest.raises(ValueError):
+        oracle.scan_fwd(u, np.zeros((6, 2, 3)))
+    with pytest.raises(ValueError):
+        oracle.scan_fwd(u, u, np.zeros(7))
+    with pytest.raises(ValueError):
+        oracle.deer(np.zeros(3), u)
+    with pytest.raises(ValueError):
+        oracle.deer(w, u, y_init=np.zeros((5, 2, 4)))
+    with pytest.raises(ValueError):
+        oracle.deer_ode(w, u, np.zeros(5))
+    with pytest.raises(ValueError):
+        oracle.sru_fwd(u, u, u, u, w, np.zeros(2))
+    # per-feature arrays shorter than the channel count repeat over the batch
+    y, _, _, _ = oracle.deer(np.zeros(2), np.zeros((6, 8)))
+    assert y.shape == (6, 8)
