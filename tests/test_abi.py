@@ -177,3 +177,52 @@ def test_binding_call_paths_reach_the_library(lib, monkeypatch):
         with pytest.raises(lrs.LrError) as e:
             call()
         assert e.value.status == lrs.LR_ERR_INVALID_ARG
+
+
+_C_CALLER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "lrscan.h"
+
+int main(void) {
+    int bad = 0, it = 0;
+    float eps = 1e-5f;
+    if (lr_scan_fwd(NULL, NULL, NULL, NULL, 2, 3, 4, LR_F32, NULL) != LR_ERR_INVALID_ARG) bad |= 1;
+    if (lr_scan_fwd(NULL, NULL, NULL, NULL, 0, 3, 4, LR_F32, NULL) != LR_OK) bad |= 2;
+    if (lr_scan_fwd(NULL, NULL, NULL, NULL, 2, 3, 4, 9, NULL) != LR_ERR_INVALID_ARG) bad |= 4;
+    if (deer_diag_solve(NULL, NULL, NULL, NULL, 2, 3, 4, eps, 0, &it, NULL, NULL, LR_F32, NULL)
+        != LR_ERR_INVALID_ARG) bad |= 8;
+    if (strcmp(lr_status_str(LR_OK), lr_status_str(LR_ERR_INVALID_ARG)) == 0) bad |= 16;
+    printf("%s\n", lr_status_str(LR_ERR_INVALID_ARG));
+    return bad;
+}
+"""
+
+
+def test_c_program_links_against_the_header_and_library(lib):
+    """The boundary as a C caller sees it: a C99 program includes the header,
+    links the shared library, and gets the documented status codes (argument
+    errors only: no device is needed)."""
+    import os
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(lrs.LIB_PATH)
+    root = os.path.dirname(os.path.dirname(os.path.abspath(lrs.__file__)))
+    src = os.path.join(libdir, f"c_caller.{os.getpid()}.c")
+    exe = src[:-2]
+    with open(src, "w") as f:
+        f.write(_C_CALLER)
+    try:
+        subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(root, "include"), src,
+                        "-o", exe, "-L", libdir, "-llrscan", f"-Wl,-rpath,{libdir}"],
+                       check=True, capture_output=True, text=True)
+        r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+        assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+        assert r.stdout.strip() == lrs.status_str(lrs.LR_ERR_INVALID_ARG)
+    finally:
+        for p in (src, exe):
+            if os.path.exists(p):
+                os.remove(p)
