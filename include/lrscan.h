@@ -180,9 +180,10 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y,
  *   per_sequence : 0 = one stopping test over the whole batch (deer_diag_solve);
  *                  1 = each batch sequence b stops at its own first K_b with
  *                  max over (t, d) |y^(K_b) - y^(K_b - 1)| < eps (or a non-finite
- *                  residual, or kmax); y[:, b] is its iterate K_b.  Iterations
- *                  continue until every sequence stopped; a stopped sequence is
- *                  no longer written.
+ *                  residual -- one NaN entry makes it NaN -- or kmax); y[:, b] is
+ *                  its iterate K_b.  Iterations continue until every sequence
+ *                  stopped; a stopped sequence is no longer written, so a
+ *                  sequence that turned non-finite stops alone.
  *   iters_out    : host int out, the largest K_b (per_sequence) or K
  *   resid_out    : host float out (may be NULL): the largest final residual
  *   resid_hist   : host float[kmax] out (may be NULL): residual of every
