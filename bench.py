@@ -14,7 +14,13 @@ Metric: scan elements per second (each element of each pass counts once; a
 DEER solve counts N*K) and the algorithmic HBM bytes per second.  Inputs are
 resident in HBM before the timed region; every input except scan_tiny's
 (12.6 MB) is larger than the 129 MB L2, and each step streams ~18 GB, so no
-step starts with its inputs cached.
+step starts with its inputs cached.  The scan_tiny passes are launch-bound
+(a few microseconds of device work each): the step replays them as CUDA
+graphs captured once after the warm-up, instead of calling through Python.
+
+`value` and `ms_per_step` come from exactly --steps timed steps.  The
+per-operation figures (`ops`) are medians over those steps and further steps
+run until --ops-seconds have passed (clocks are sampled over both).
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
 on a bounded sample of the same workload instead.
@@ -159,6 +165,11 @@ def pass_elems(wl, p, k=1):
     return wl.N * (k if p == "solve" else 1)
 
 
+# Rows run as CUDA graphs inside the step (launch-bound: microseconds of
+# device work per pass, less than the host's cost of a call through Python).
+GRAPH_ROWS = ("scan_tiny",)
+
+
 class Bench:
     def __init__(self, dev):
         import torch
@@ -187,6 +198,7 @@ class Bench:
             else:
                 o["y"] = e()
         self.k_last = 0
+        self.graphs = {}
         torch.cuda.synchronize()
 
     def _tdt(self, wl):
@@ -200,11 +212,28 @@ class Bench:
 
     # one row; returns (elements, bytes, launches)
     def run_row(self, name, wl, passes, ev=None):
-        L, o = self.lrs, self.d[name]
         elems = byts = launches = 0
         for p in passes:
             if ev is not None:
                 ev[(name, p)][0].record()
+            g = self.graphs.get((name, p))
+            if g is not None:
+                g.replay()
+                launches += 1
+            else:
+                launches += self.run_pass(name, wl, p)
+            if ev is not None:
+                ev[(name, p)][1].record()
+            k = self.k_last if p == "solve" else 1
+            elems += pass_elems(wl, p, k)
+            byts += pass_bytes(wl, p, k)
+        return elems, byts, launches
+
+    def run_pass(self, name, wl, p):
+        """One pass through the public binding; returns the kernel launches."""
+        L, o = self.lrs, self.d[name]
+        launches = 0
+        if True:
             if wl.kind == "scan" and p == "fwd":
                 L.lr_scan_fwd(o["a"], o["b"], o["h0"], o["h"])
                 launches += 1
@@ -227,12 +256,52 @@ class Bench:
                 # iterations are enqueued in batches; those after the stopping
                 # test return at once but are still launches
                 launches += r["launches"]
-            if ev is not None:
-                ev[(name, p)][1].record()
-            k = self.k_last if p == "solve" else 1
-            elems += pass_elems(wl, p, k)
-            byts += pass_bytes(wl, p, k)
-        return elems, byts, launches
+        return launches
+
+    def capture_graphs(self):
+        """After the warm-up (every row has sized the library's workspace):
+        capture each pass of the launch-bound rows as a CUDA graph."""
+        t = self.torch
+        for name, wl, passes in ROWS:
+            if name not in GRAPH_ROWS:
+                continue
+            for p in passes:
+                g = t.cuda.CUDAGraph()
+                with t.cuda.graph(g):
+                    self.run_pass(name, wl, p)
+                self.graphs[(name, p)] = g
+        t.cuda.synchronize()
+
+    def back_to_back_us(self, name, reps=64, rounds=5):
+        """Device time per launch of each pass of a launch-bound row, from a
+        graph of `reps` launches in a row (each starts when the previous one
+        ends): the kernel's own time, no host in between.  Median of
+        `rounds` replays."""
+        t = self.torch
+        wl = next(w for n, w, _ in ROWS if n == name)
+        passes = next(ps for n, _, ps in ROWS if n == name)
+        out = {}
+        for p in passes:
+            g = t.cuda.CUDAGraph()
+            with t.cuda.graph(g):
+                for _ in range(reps):
+                    self.run_pass(name, wl, p)
+            g.replay()
+            ts = []
+            for _ in range(rounds):
+                e0, e1 = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+                t.cuda.synchronize()
+                e0.record()
+                g.replay()
+                e1.record()
+                t.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3 / reps)
+            us = statistics.median(ts)
+            byt = pass_bytes(wl, p)
+            out[p] = {"us_per_launch": round(us, 3), "GBps": round(byt / (us / 1e6) / 1e9, 1),
+                      "launches_per_graph": reps}
+            del g
+        return out
 
     def step(self, ev=None):
         tot = [0, 0, 0]
@@ -383,6 +452,37 @@ class Bench:
             self.h2d += sum(v.numel() * v.element_size() for v in self.pin_in[name].values())
             self.d2h += sum(v.numel() * v.element_size() for v, _ in self.pin_out[name].values())
         self.s_in, self.s_out = t.cuda.Stream(), t.cuda.Stream()
+
+    def link_ceiling(self, nbytes=1 << 30, reps=3):
+        """Pinned host <-> device copy bandwidth on this machine, GB/s: H2D alone,
+        D2H alone, and both at once on two streams (as the e2e step runs
+        them).  Best of `reps`."""
+        t = self.torch
+        n = nbytes // 4
+        hin = t.empty(n, dtype=t.float32, pin_memory=True)
+        hout = t.empty(n, dtype=t.float32, pin_memory=True)
+        d1 = t.empty(n, dtype=t.float32, device=self.dev)
+        d2 = t.empty(n, dtype=t.float32, device=self.dev)
+        s1, s2 = t.cuda.Stream(), t.cuda.Stream()
+
+        def one(src, dst, st):
+            with t.cuda.stream(st):
+                dst.copy_(src, non_blocking=True)
+
+        res = {}
+        for key, fn, byt in (("h2d", lambda: one(hin, d1, s1), nbytes),
+                             ("d2h", lambda: one(d2, hout, s2), nbytes),
+                             ("both", lambda: (one(hin, d1, s1), one(d2, hout, s2)), 2 * nbytes)):
+            ts = []
+            for _ in range(reps):
+                t.cuda.synchronize()
+                t0 = time.perf_counter()
+                fn()
+                t.cuda.synchronize()
+                ts.append(time.perf_counter() - t0)
+            res[key + "_GBps"] = round(byt / min(ts) / 1e9, 1)
+        del hin, hout, d1, d2
+        return res
 
     def e2e_step(self):
         """One step from pinned host buffers: every row's inputs stream in on
@@ -670,7 +770,9 @@ def run_reference(args, ws, rank):
 #   lstm   LSTM cell fp32 32x512x1024 (T reduced from 2048): fwd, bwd, 2 bias kernels
 #   deerbwd  DEER backward fp32 4x65536x256 (full size) from a 3-iteration solve:
 #          k_seg + k_seg1 x 2 (the solve), then k_seg (backward) and 2 dw kernels
-PROFILE_CASES = ("deer", "large", "long", "sru", "lstm", "deerbwd")
+#   tiny   scan_tiny fp32 4x1024x256 (full size; 12.6 MB, L2-resident after the
+#          first launch): fwd, bwd, fwd, bwd
+PROFILE_CASES = ("deer", "large", "long", "sru", "lstm", "deerbwd", "tiny")
 
 
 def profile_case(name):
@@ -698,6 +800,11 @@ def profile_case(name):
         inp = W.make_inputs(dataclasses.replace(W.SCAN_BF16, T=2048), 0)
         a, b, g = dev(inp, "a"), dev(inp, "b"), dev(inp, "g")
         L.lr_scan_bwd(a, L.lr_scan_fwd(a, b, None), g, None)
+    elif name == "tiny":
+        inp = W.make_inputs(W.SCAN_TINY, 0)
+        a, b, g = dev(inp, "a"), dev(inp, "b"), dev(inp, "g")
+        for _ in range(2):
+            L.lr_scan_bwd(a, L.lr_scan_fwd(a, b, None), g, None)
     elif name == "long":
         inp = W.make_inputs(dataclasses.replace(W.SCAN_LONG, T=1 << 18), 0)
         L.lr_scan_fwd(dev(inp, "a"), dev(inp, "b"), dev(inp, "h0"))
@@ -728,6 +835,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ops-seconds", type=float, default=2.5,
+                    help="per-operation medians: steps after the timed ones until this much "
+                         "time has passed since the timed region began")
+    ap.add_argument("--no-next", action="store_true", help="skip the next rows (next_ops)")
     ap.add_argument("--only", action="append", default=[],
                     help="run only these operations (e.g. scan_large.bwd); for profiling cases")
     ap.add_argument("--T", type=int, default=0, help="override T of the selected rows (profiling cases)")
@@ -752,7 +863,9 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     b = Bench(dev)
-    for _ in range(args.warmup):
+    for i in range(args.warmup):
+        if i == args.warmup - 1:  # every shape has sized the workspace by now
+            b.capture_graphs()
         b.step()
     torch.cuda.synchronize()
     if lrs.last_error() != lrs.LR_OK:
@@ -766,7 +879,9 @@ def main():
     barrier(ws)
     torch.cuda.synchronize()
     elems = byts = launches = 0
+    n_ops_steps = 0
     with Clocks(local) as clk:
+        t_begin = time.perf_counter()
         start.record()
         for _ in range(args.steps):
             e, by, la = b.step(ev)
@@ -777,6 +892,14 @@ def main():
                 per[key].append(e0.elapsed_time(e1))
         end.record()
         torch.cuda.synchronize()
+        # more steps, for the per-operation medians only (not in `value`)
+        while time.perf_counter() - t_begin < args.ops_seconds:
+            b.step(ev)
+            torch.cuda.synchronize()
+            n_ops_steps += 1
+            for key, (e0, e1) in ev.items():
+                per[key].append(e0.elapsed_time(e1))
+        ops_wall = time.perf_counter() - t_begin
     barrier(ws)
     ms = start.elapsed_time(end)
     ms = max_over_ranks(ms, ws)
@@ -793,7 +916,7 @@ def main():
     for (n, p), ts in per.items():
         wl = next(w for nn, w, _ in ROWS if nn == n)
         k = k_med if p == "solve" else 1
-        t_ms = statistics.mean(ts)
+        t_ms = statistics.median(ts)
         launches_op = k if p == "solve" else 1
         byt = pass_bytes(wl, p, k)
         ops[f"{n}.{p}"] = {"ms": round(t_ms, 4), "launches": launches_op,
@@ -818,18 +941,30 @@ def main():
             "data": "synthetic", "config": config_dict(),
             "hbm_GBps": round(gbs, 1), "hbm_frac": round(gbs / peak, 4), "deer_iters": k_med,
             "deer_resid_history": [float(f"{r:.3e}") for r in getattr(b, "hist_last", [])],
-            "gpu_launches": launches, "clocks": clk.summary(), "roofline": roof, "ops": ops}
+            "gpu_launches": launches, "clocks": clk.summary(), "roofline": roof, "ops": ops,
+            "ops_timing": {"stat": "median", "steps": args.steps + n_ops_steps,
+                           "seconds": round(ops_wall, 2),
+                           "graph_rows": list(GRAPH_ROWS)}}
+    if "scan_tiny" in b.d:
+        # the tiny scan's kernels back to back (graph of 64 launches): their
+        # own device time, which the step's per-pass figure adds a graph
+        # launch to
+        bb = b.back_to_back_us("scan_tiny")
+        for p_, r in bb.items():
+            r["frac"] = round(r["GBps"] / peak, 3)
+        line["scan_tiny_back_to_back"] = bb
 
     # the next rows on the same scan, outside the step: the gradient through
     # the DEER solution at the DEER workload's size (from the step's own
     # solution), DEER's ODE form and a warm-started solve there, and the LSTM
     # cell forward and backward
-    nxt = {}
-    if "deer" in b.d:
-        nxt["deer.bwd"] = b.time_deer_bwd(peak)
-        nxt.update(b.time_deer_variants(peak))
-    nxt.update(b.time_lstm(peak))
-    line["next_ops"] = nxt
+    if not args.no_next:
+        nxt = {}
+        if "deer" in b.d:
+            nxt["deer.bwd"] = b.time_deer_bwd(peak)
+            nxt.update(b.time_deer_variants(peak))
+        nxt.update(b.time_lstm(peak))
+        line["next_ops"] = nxt
 
     if not args.no_e2e:
         b.setup_e2e()
@@ -846,6 +981,14 @@ def main():
         t = max_over_ranks(e0.elapsed_time(e1), ws)
         line["e2e"] = {"value": el * ws / (t / 1e3), "unit": UNIT, "h2d_bytes_per_step": b.h2d,
                        "d2h_bytes_per_step": b.d2h, "ms_per_step": t / args.e2e_steps}
+        # the host link's ceiling on this machine: the e2e step moves h2d + d2h
+        # bytes per step, both directions at once
+        lk = b.link_ceiling()
+        moved = (b.h2d + b.d2h) / (t / args.e2e_steps / 1e3) / 1e9
+        line["e2e"]["link"] = {**lk, "achieved_GBps": round(moved, 1),
+                               "frac_of_both": round(moved / lk["both_GBps"], 3),
+                               "how": "pinned 1 GiB copies, best of 3: H2D, D2H, both at once "
+                                      "on two streams"}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         smp = OracleSampler(args.cpu_budget)
         rates, desc, _ = smp.run()

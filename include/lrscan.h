@@ -57,9 +57,25 @@
  *    second iterate buffer, residual slots, per-sequence stop state, clamp
  *    counters and the last iteration count of each DEER form and shape,
  *    bias-gradient partials), grown on demand with cudaMalloc.  Calls on
- *    different streams are serialised through it with CUDA events.  A call
- *    that returns LR_ERR_CUDA after it began enqueueing does not record its
- *    event: synchronise the device before the next call on another stream.
+ *    different streams are serialised through it with CUDA events; every
+ *    call records its event on every return once it has begun enqueueing,
+ *    errors included, so a later call on another stream still waits for
+ *    whatever a failed call enqueued.
+ *  - CUDA graphs: the carry packets are tagged with an epoch that the kernels
+ *    take on the device from the workspace's ticket word (every launch takes
+ *    a fresh one), so a call of lr_scan_fwd, lr_scan_bwd, sru_fwd, sru_bwd,
+ *    lstm_cell_fwd, lstm_cell_bwd or deer_diag_bwd captured into a graph
+ *    gives the right result on every replay, with whatever the captured
+ *    buffers hold then.  Make one uncaptured call of the same shape first
+ *    (it sizes the workspace and sets up the kernels; capture fails if the
+ *    workspace would have to grow).  A graph keeps using the workspace
+ *    buffers it captured: the carry packets and the bias partials that a
+ *    later, larger call outgrows are kept, not freed, until the process
+ *    exits (lr_workspace_bytes counts the current ones only).  A captured
+ *    call is ordered, when the graph runs, by the stream the graph is
+ *    launched on only: do not run it concurrently with other calls on the
+ *    same device.  The DEER solves read residuals back on the host and
+ *    cannot be captured.
  *  - Return value: LR_OK, or an lr_status describing an argument or launch
  *    error detected before or while enqueuing the work.  Errors detected on
  *    the device while the kernels run (a carry or copy wait that ran out) are
@@ -93,6 +109,10 @@ typedef enum {
 /*
  * Forward scan (row a1): h_t = a_t * h_{t-1} + b_t for t = 0..T-1 with
  * h_{-1} = h0.  [P1] parallel-scan paragraph; [P2] LSTM paragraph.
+ * Chunks of time rows are scanned in parallel; the state entering each chunk
+ * comes from the chunk aggregates published before it (a look-back over all
+ * of them for short problems, walker CTAs for long ones, a CTA walking its
+ * channel strip through time for wide ones).
  *   a, b : [T,B,D] in   coefficients and inputs
  *   h0   : [B,D]   in   initial state; NULL means zeros
  *   h    : [T,B,D] out  states (h0 is not repeated in h)
@@ -289,20 +309,26 @@ int lstm_cell_bwd(const void* zf, const void* zi, const void* zc, const void* zo
  * engine or framework that owns every device byte (a hidden cudaMalloc can
  * fail at run time or fragment its pool) and latency-critical loops (the
  * cudaFree that grows lr_scan_fwd's cached workspace synchronises the device).
- * Its scratch (chunk-state packets, tile ticket) is one fixed 4 MiB
- * __device__ array that every GPU loading this library holds until the
- * process exits.
+ * Its scratch (chunk-state or chunk-aggregate packets, tile ticket) is one
+ * fixed 4 MiB __device__ array that every GPU loading this library holds
+ * until the process exits.
  *   - Problems needing more scratch than that return LR_ERR_TOO_LARGE: the
- *     array holds ~524 K channel-chunks (one chunk = 64 fp32 or 32 bf16 time
- *     steps; a third of that when the sequence is long enough for the walker
- *     protocol), e.g. B*D = 1024 channels up to T = 32 K fp32 steps.
+ *     array holds ~524 K 8-byte packets, one per channel per chunk of 32 fp32
+ *     or 64 bf16 time steps, two for short problems (look-back protocol),
+ *     three per chunk of 64 steps for long ones (walker protocol); e.g.
+ *     B*D = 1024 channels up to T = 8 K fp32 steps.
  *   - All calls share the array: calls whose kernels overlap on the GPU race
  *     and give wrong results; order them on one stream or with events.
+ *   - Every call clears the array's internal error word and tile counter
+ *     (one 8-byte memset on `stream`) before its launch.
  *   - The first call on a device looks up the array's address; make it before
  *     any stream capture.
  *   - err_dev: optional device word (4-byte aligned) into which device-side
- *     errors are OR-ed (bit 0: a carry wait ran out; h is then NaN); NULL
- *     keeps them inside the scratch array.  lr_last_error() does not see them.
+ *     errors are OR-ed (bit 0: a carry wait ran out; h is then NaN).  The
+ *     library never clears it: set it to zero before a call whose errors you
+ *     want to tell apart.  With err_dev == NULL the errors go to the array's
+ *     internal word, which nothing can read (lr_last_error() reads the other
+ *     workspace): pass err_dev whenever a timed-out wait must be detected.
  */
 int lr_scan_fwd_noalloc(const void* a, const void* b, const void* h0, void* h,
                         int64_t B, int64_t T, int64_t D, int dtype,
@@ -311,7 +337,9 @@ int lr_scan_fwd_noalloc(const void* a, const void* b, const void* h0, void* h,
 /*
  * Reads and clears the device error word of the current device (synchronises
  * the device).  Returns LR_OK or the first recorded device error
- * (LR_ERR_TIMEOUT).
+ * (LR_ERR_TIMEOUT).  After an error it also resets the tile ticket, which a
+ * launch that gave up leaves mid-count: call it after LR_ERR_TIMEOUT before
+ * any further call on that device.
  */
 int lr_last_error(void);
 
@@ -335,6 +363,18 @@ int64_t lr_workspace_bytes(void);
  * error word.  Nothing faults or hangs.
  */
 int lr_test_lookback_timeout(uint32_t spin_limit, void* stream);
+
+/*
+ * Test hook for the ordering of calls after an error: enters a call on
+ * `stream` as every entry point does, enqueues a kernel that sleeps about
+ * `sleep_ns` nanoseconds (bounded by the GPU's global timer) and then sets
+ * x[0..n) to `value` (x: n fp32 device values, caller-owned), and returns
+ * LR_ERR_CUDA as a call whose later launch failed would.  A following call
+ * on another stream must still be ordered after that kernel.  Returns
+ * LR_ERR_INVALID_ARG for n < 0 or x == NULL with n > 0.
+ */
+int lr_test_fail_after_enqueue(float* x, int64_t n, float value, uint64_t sleep_ns,
+                               void* stream);
 
 /*
  * Test hook for the activations of the fused kernels: tanh_out[i] = tanh(x[i]),

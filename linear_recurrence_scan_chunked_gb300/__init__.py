@@ -68,6 +68,8 @@ def load():
     lib.lr_workspace_bytes.restype = I64
     lib.lr_test_lookback_timeout.argtypes = [ctypes.c_uint32, P]
     lib.lr_test_activations.argtypes = [P, P, P, P, I64, P]
+    lib.lr_test_fail_after_enqueue.argtypes = [P, I64, ctypes.c_float, ctypes.c_uint64, P]
+    lib.lr_test_fail_after_enqueue.restype = I
     for f in ("lr_scan_fwd", "lr_scan_bwd", "sru_fwd", "sru_bwd", "deer_diag_solve", "deer_diag_bwd",
               "lr_last_error", "lr_test_lookback_timeout", "lr_test_activations"):
         getattr(lib, f).restype = I
@@ -375,3 +377,13 @@ def test_activations(x, stream=None, with_expm1=False):
 def test_lookback_timeout(spin_limit: int = 1000, stream=None) -> int:
     """Runs the bounded-wait test launch; returns its enqueue status."""
     return int(load().lr_test_lookback_timeout(ctypes.c_uint32(spin_limit), _stream(stream)))
+
+
+def test_fail_after_enqueue(x, value: float, sleep_ns: int, stream=None) -> int:
+    """Enqueues a kernel that sleeps ~sleep_ns and then fills the fp32 CUDA
+    tensor x with `value`, and returns the LR_ERR_CUDA of a call whose later
+    launch failed (the call-ordering test after an error)."""
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous fp32 CUDA tensor")
+    return int(load().lr_test_fail_after_enqueue(_p(x), x.numel(), ctypes.c_float(value),
+                                                  ctypes.c_uint64(sleep_ns), _stream(stream, x)))

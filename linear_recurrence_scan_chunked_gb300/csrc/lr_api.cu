@@ -45,6 +45,32 @@ bool tma_encode(CUtensorMap* m, const void* ptr, int dtype, int64_t T, int64_t C
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Retire the current epoch of a workspace (the ticket word's high half):
+// ends a DEER solve, whose last launch published the next launch's
+// aggregates tagged with the epoch after its own.
+__global__ void k_retire_epoch(u64* tk) {
+    atomicAdd(reinterpret_cast<unsigned long long*>(tk), 1ull << 32);
+}
+
+// Test hook kernel: sleeps about `ns` nanoseconds (bounded by the global
+// timer), then fills x[0..n) with `value`.
+__global__ void k_test_sleep_fill(float* x, int64_t n, float value, uint64_t ns) {
+    if (threadIdx.x == 0) {
+        uint64_t t0;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+        for (;;) {
+            uint64_t t;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+            if (t - t0 >= ns) break;
+            __nanosleep(10000);
+        }
+    }
+    __syncthreads();
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        x[i] = value;
+}
+
 // Test hook kernel: the activations the fused kernels use, elementwise.
 __global__ void k_test_act(const float* __restrict__ x, float* __restrict__ th,
                            float* __restrict__ sg, float* __restrict__ em, int64_t n) {
@@ -64,6 +90,13 @@ using namespace lrs;
 
 constexpr uint32_t kSpinLimit = 1u << 21;  // polls (backing off to ~1 us each): ~2 s
 constexpr int kMaxIters = 4096;            // DEER kmax bound (residual slots)
+// Launches counted on the host after which the packets and the ticket word
+// are cleared, so that the device's epochs never wrap into packets left by
+// earlier launches.
+constexpr uint64_t kEpochClear = 1ull << 31;
+// Workspace words: [0..1] the 64-bit ticket word (ticket counter, last retired
+// epoch), [2] the sticky error bits, [3] unused, [4 ..] DEER residual slots.
+constexpr int kWordErr = 2, kWordSlots = 4;
 constexpr int kDeerBatch = 4;              // DEER iterations enqueued per residual read-back
 
 thread_local char g_cuda_msg[256] = "";
@@ -83,7 +116,7 @@ int cuda_fail(cudaError_t e) {
 // error word, DEER residual slots and second iterate, SRU bias partials.
 struct DevWS {
     u64* pk = nullptr;           size_t pk_cap = 0;        // carry packets (state, aggregate)
-    uint32_t* words = nullptr;   // [0] ticket, [1] error bits, [2..] DEER residual slots
+    uint32_t* words = nullptr;   // ticket word, error bits, DEER residual slots (kWord*)
     float* partials = nullptr;   size_t partials_cap = 0; // floats
     void* ybuf = nullptr;        size_t ybuf_cap = 0;     // bytes
     uint32_t* host_word = nullptr;                        // pinned [kMaxIters], residual reads
@@ -95,7 +128,8 @@ struct DevWS {
         int dtype = -1, K = 0;
     } deer_last[2];
     uint32_t* seq_host = nullptr; size_t seq_host_cap = 0;  // pinned mirror of its residuals
-    uint32_t epoch = 0;
+    uint64_t launches = 0;                                // packet launches since the last clear
+    std::vector<void*> kept;                              // outgrown buffers graphs may still use
     cudaEvent_t done = nullptr;
     cudaStream_t last_stream = nullptr;
     bool has_last = false;
@@ -111,26 +145,33 @@ int get_ws(DevWS** out) {
     if ((int)g_ws.size() <= dev) g_ws.resize(dev + 1, nullptr);
     if (!g_ws[dev]) {
         DevWS* w = new DevWS();
-        CK(cudaMalloc(&w->words, sizeof(uint32_t) * (2 + kMaxIters)));
-        CK(cudaMemset(w->words, 0, sizeof(uint32_t) * (2 + kMaxIters)));
+        CK(cudaMalloc(&w->words, sizeof(uint32_t) * (kWordSlots + kMaxIters)));
+        CK(cudaMemset(w->words, 0, sizeof(uint32_t) * (kWordSlots + kMaxIters)));
         CK(cudaHostAlloc(&w->host_word, sizeof(uint32_t) * kMaxIters, cudaHostAllocDefault));
         CK(cudaMalloc(&w->clamps, sizeof(unsigned long long) * kMaxIters));
         CK(cudaEventCreateWithFlags(&w->done, cudaEventDisableTiming));
-        w->bytes = sizeof(uint32_t) * (2 + kMaxIters);
+        w->bytes = sizeof(uint32_t) * (kWordSlots + kMaxIters);
         g_ws[dev] = w;
     }
     *out = g_ws[dev];
     return LR_OK;
 }
 
+// Grow a workspace buffer to hold `need` elements.  keep: the outgrown buffer
+// is kept until the process exits instead of freed -- a CUDA graph that
+// captured a launch holds its address (the carry packets, the bias partials).
 template <typename T>
-int grow(DevWS& ws, T** p, size_t* cap, size_t need, bool zero) {
+int grow(DevWS& ws, T** p, size_t* cap, size_t need, bool zero, bool keep = false) {
     if (need <= *cap) return LR_OK;
     size_t n = need + need / 4;
     CK(cudaDeviceSynchronize());  // nothing in flight may still use the old buffer
     if (*p) {
-        CK(cudaFree(*p));
-        ws.bytes -= (int64_t)(*cap * sizeof(T));
+        if (keep) {
+            ws.kept.push_back(*p);
+        } else {
+            CK(cudaFree(*p));
+            ws.bytes -= (int64_t)(*cap * sizeof(T));
+        }
     }
     *p = nullptr;
     *cap = 0;
@@ -141,25 +182,62 @@ int grow(DevWS& ws, T** p, size_t* cap, size_t need, bool zero) {
     return LR_OK;
 }
 
-// Order this call after the previous call on any other stream.
+// Order this call after the previous call on any other stream.  A call
+// being captured into a CUDA graph is not ordered here: when the graph runs,
+// the stream it is launched on orders it.
+bool capturing(cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    return cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone;
+}
 int enter(DevWS& ws, cudaStream_t s) {
+    if (capturing(s)) return LR_OK;
     if (ws.has_last && ws.last_stream != s) CK(cudaStreamWaitEvent(s, ws.done, 0));
     return LR_OK;
 }
 int leave(DevWS& ws, cudaStream_t s) {
+    if (capturing(s)) return LR_OK;
     CK(cudaEventRecord(ws.done, s));
     ws.last_stream = s;
     ws.has_last = true;
     return LR_OK;
 }
+// From enter() on, every return of a call records the workspace event, the
+// error returns included: work the call already enqueued is then still
+// ordered before the next call on another stream.
+struct Leave {
+    DevWS& ws;
+    cudaStream_t s;
+    bool armed = true;
+    Leave(DevWS& w, cudaStream_t st) : ws(w), s(st) {}
+    int done() {
+        armed = false;
+        return leave(ws, s);
+    }
+    ~Leave() {
+        if (armed) (void)leave(ws, s);
+    }
+};
+u64* ticket_word(DevWS& ws) { return reinterpret_cast<u64*>(ws.words); }
+// Count one launch that uses packets; clears the packets and the ticket word
+// (epochs start again at 1) once every kEpochClear launches.
+int count_launch(DevWS& ws, cudaStream_t s, uint64_t n = 1) {
+    ws.launches += n;
+    if (ws.launches < kEpochClear) return LR_OK;
+    ws.launches = n;
+    if (ws.pk) CK(cudaMemsetAsync(ws.pk, 0, ws.pk_cap * sizeof(u64), s));
+    CK(cudaMemsetAsync(ws.words, 0, sizeof(u64), s));
+    return LR_OK;
+}
 
 // Geometry + carry state for one launch of `op`.
-// tma: -1 picks the TMA-staged chain kernel whenever it applies; 0 / 1 force
-// the choice (the timeout test covers both kernels).
+// tma: -1 picks the TMA-staged kernels whenever they apply; 0 / 1 force the
+// choice, and chain = true the chain protocol (the timeout test covers every
+// kernel).
 int plan(DevWS& ws, Op op, int dtype, bool vec, int64_t T, int64_t C, int64_t D, Geom* g,
-         Carry* cr, cudaStream_t s, int tma = -1) {
+         Carry* cr, cudaStream_t s, int tma = -1, bool chain = false) {
     const bool want_tma = tma < 0 ? use_tma(dtype, vec, T, C) : (tma == 1);
-    const CarryPlan cp = carry_plan(op, dtype, vec, want_tma, T, C);
+    const CarryPlan cp = chain ? chain_plan(op, dtype, vec, want_tma, T, C)
+                               : carry_plan(op, dtype, vec, want_tma, T, C);
     const TileShape ts = cp.ts;
     g->T = T;
     g->C = C;
@@ -173,17 +251,15 @@ int plan(DevWS& ws, Op op, int dtype, bool vec, int64_t T, int64_t C, int64_t D,
     g->n_draws = 0;  // set by the launcher from the grid it picks
     g->ticket_base = 0;
     g->max_grid = 0;
-    int st = grow(ws, &ws.pk, &ws.pk_cap, cp.inc_elems + cp.agg_elems, true);
+    int st = grow(ws, &ws.pk, &ws.pk_cap, cp.inc_elems + cp.agg_elems, true, true);
     if (st) return st;
-    if (++ws.epoch == 0) {  // 32-bit wrap: forget every packet once
-        ws.epoch = 1;
-        CK(cudaMemsetAsync(ws.pk, 0, ws.pk_cap * sizeof(u64), s));
-    }
+    st = count_launch(ws, s);
+    if (st) return st;
     cr->inc = ws.pk;
     cr->agg = ws.pk + cp.inc_elems;
-    cr->ticket = ws.words;
-    cr->err = ws.words + 1;
-    cr->epoch = ws.epoch;
+    cr->tk = ticket_word(ws);
+    cr->err = ws.words + kWordErr;
+    cr->epoch = 0;  // taken on the device from the ticket word
     cr->spin_limit = kSpinLimit;
     cr->mode = cp.mode;
     cr->n_walk = cp.n_walk;
@@ -257,9 +333,10 @@ int lr_scan_fwd(const void* a, const void* b, const void* h0, void* h, int64_t B
     Geom g;
     Carry cr;
     TRY(enter(*ws, s));
+    Leave lv(*ws, s);
     TRY(plan(*ws, OP_SCAN_FWD, dtype, vec, T, B * D, D, &g, &cr, s));
     CK(launch_scan_fwd(dtype, vec, a, b, h0, h, g, cr, s));
-    return leave(*ws, s);
+    return lv.done();
 }
 
 int lr_scan_bwd(const void* a, const void* h, const void* h0, const void* dh, void* da, void* db,
@@ -281,9 +358,10 @@ int lr_scan_bwd(const void* a, const void* h, const void* h0, const void* dh, vo
     Geom g;
     Carry cr;
     TRY(enter(*ws, s));
+    Leave lv(*ws, s);
     TRY(plan(*ws, OP_SCAN_BWD, dtype, vec, T, B * D, D, &g, &cr, s));
     CK(launch_scan_bwd(dtype, vec, a, h, h0, dh, da, db, dh0, g, cr, s));
-    return leave(*ws, s);
+    return lv.done();
 }
 
 int sru_fwd(const void* xt, const void* uf, const void* ur, const void* x, const float* bf,
@@ -300,9 +378,10 @@ int sru_fwd(const void* xt, const void* uf, const void* ur, const void* x, const
     Geom g;
     Carry cr;
     TRY(enter(*ws, s));
+    Leave lv(*ws, s);
     TRY(plan(*ws, OP_SRU_FWD, dtype, vec, T, B * D, D, &g, &cr, s));
     CK(launch_sru_fwd(dtype, vec, xt, uf, ur, x, bf, br, c0, h, c, g, cr, s));
-    return leave(*ws, s);
+    return lv.done();
 }
 
 int sru_bwd(const void* xt, const void* uf, const void* ur, const void* x, const float* bf,
@@ -329,12 +408,14 @@ int sru_bwd(const void* xt, const void* uf, const void* ur, const void* x, const
     Geom g;
     Carry cr;
     TRY(enter(*ws, s));
+    Leave lv(*ws, s);
     TRY(plan(*ws, OP_SRU_BWD, dtype, vec, T, B * D, D, &g, &cr, s));
-    TRY(grow(*ws, &ws->partials, &ws->partials_cap, (size_t)(2 * g.n_chunks * g.C + 2 * g.C), false));
+    TRY(grow(*ws, &ws->partials, &ws->partials_cap, (size_t)(2 * g.n_chunks * g.C + 2 * g.C), false,
+             true));
     CK(launch_sru_bwd(dtype, vec, xt, uf, ur, x, bf, br, c0, c, dh, dxt, duf, dur, dx, dc0,
                       ws->partials, g, cr, s));
     CK(launch_bias_reduce(ws->partials, g.n_chunks, 2, B, D, BiasOut{{dbf, dbr}}, s));
-    return leave(*ws, s);
+    return lv.done();
 }
 
 int lstm_cell_fwd(const void* zf, const void* zi, const void* zc, const void* zo,
@@ -352,10 +433,11 @@ int lstm_cell_fwd(const void* zf, const void* zi, const void* zc, const void* zo
     Geom g;
     Carry cr;
     TRY(enter(*ws, s));
+    Leave lv(*ws, s);
     TRY(plan(*ws, OP_LSTM_FWD, dtype, vec, T, B * D, D, &g, &cr, s));
     CK(launch_lstm_fwd(dtype, vec, LstmGates{zf, zi, zc, zo}, LstmBias{bf, bi, bc, bo}, c0, h, c,
                        g, cr, s));
-    return leave(*ws, s);
+    return lv.done();
 }
 
 int lstm_cell_bwd(const void* zf, const void* zi, const void* zc, const void* zo,
@@ -384,12 +466,14 @@ int lstm_cell_bwd(const void* zf, const void* zi, const void* zc, const void* zo
     Geom g;
     Carry cr;
     TRY(enter(*ws, s));
+    Leave lv(*ws, s);
     TRY(plan(*ws, OP_LSTM_BWD, dtype, vec, T, B * D, D, &g, &cr, s));
-    TRY(grow(*ws, &ws->partials, &ws->partials_cap, (size_t)(4 * g.n_chunks * g.C + 4 * g.C), false));
+    TRY(grow(*ws, &ws->partials, &ws->partials_cap, (size_t)(4 * g.n_chunks * g.C + 4 * g.C), false,
+             true));
     CK(launch_lstm_bwd(dtype, vec, LstmGates{zf, zi, zc, zo}, LstmBias{bf, bi, bc, bo}, c0, c, dh,
                        LstmGates{dzf, dzi, dzc, dzo}, dc0, ws->partials, g, cr, s));
     CK(launch_bias_reduce(ws->partials, g.n_chunks, 4, B, D, BiasOut{{dbf, dbi, dbc, dbo}}, s));
-    return leave(*ws, s);
+    return lv.done();
 }
 
 static int grow_host(DevWS& ws, size_t need) {
@@ -419,23 +503,34 @@ static float bits_f(uint32_t b) {
 // segment aggregates, with the next launch's epoch, into the second of two
 // aggregate buffers after the packets plan() lays out; from the second
 // iteration on a launch has no reduce pass.  onepass_begin sizes the packets
-// and keeps the epoch from wrapping inside the solve (plan() adds one per
-// launch); onepass_args points launch kk at its two buffers; onepass_end
-// retires the epoch the solve's last launch tagged its next-aggregates with,
-// so that no later launch, of any operation, takes them for its own.
+// and keeps the packet epochs from being cleared inside the solve;
+// onepass_args points launch kk at its two buffers; the solve's Retire
+// retires, on the device, the epoch that its last launch tagged the
+// next-aggregates with, so that no later launch, of any operation, takes them
+// for its own -- on every return once the first iteration was enqueued.
 static int onepass_begin(DevWS& ws, Op op, int dtype, bool vec, int64_t T, int64_t C, int kmax,
                          cudaStream_t s, CarryPlan* cp, bool* on) {
     *cp = carry_plan(op, dtype, vec, use_tma(dtype, vec, T, C), T, C);
     *on = cp->mode == CARRY_WALK && cp->tma;
     if (!*on) return LR_OK;
-    TRY(grow(ws, &ws.pk, &ws.pk_cap, cp->inc_elems + 2 * cp->agg_elems, true));
-    if (ws.epoch > 0xFFFFFFFFu - (uint32_t)(kmax + 8)) {
-        CK(cudaMemsetAsync(ws.pk, 0, ws.pk_cap * sizeof(u64), s));
-        ws.epoch = 0;
-    }
-    ++ws.epoch;  // also retired here, in case an earlier solve stopped on an error
+    TRY(grow(ws, &ws.pk, &ws.pk_cap, cp->inc_elems + 2 * cp->agg_elems, true, true));
+    if (ws.launches + (uint64_t)kmax + 8 >= kEpochClear) TRY(count_launch(ws, s, kEpochClear));
     return LR_OK;
 }
+struct Retire {
+    DevWS& ws;
+    cudaStream_t s;
+    bool armed;
+    Retire(DevWS& w, cudaStream_t st, bool on) : ws(w), s(st), armed(on) {}
+    int done() {
+        if (!armed) return LR_OK;
+        armed = false;
+        k_retire_epoch<<<1, 1, 0, s>>>(ticket_word(ws));
+        CK(cudaGetLastError());
+        return LR_OK;
+    }
+    ~Retire() { (void)done(); }
+};
 
 // The iteration count of the last solve of this DEER form (0: tanh, 1: ODE)
 // and shape, 0 if none.  A solve writes iterate k to buf[(k + flip) % 2]
@@ -451,14 +546,10 @@ static void deer_remember(DevWS& ws, int form, int64_t T, int64_t C, int dtype, 
     ws.deer_last[form] = DevWS::DeerLast{T, C, dtype, K};
 }
 
-static void onepass_end(DevWS& ws, bool on) {
-    if (on) ++ws.epoch;  // onepass_begin left room: no wrap here
-}
-
 static NextAgg onepass_args(DevWS& ws, const CarryPlan& cp, int kk, Carry& cr) {
     u64* agg0 = ws.pk + cp.inc_elems;  // where plan() put cr.agg
     cr.agg = (kk & 1) ? agg0 : agg0 + cp.agg_elems;
-    return NextAgg{(kk & 1) ? agg0 + cp.agg_elems : agg0, cr.epoch + 1 /* the next plan()'s */,
+    return NextAgg{(kk & 1) ? agg0 + cp.agg_elems : agg0, 0u /* the next launch's: on the device */,
                    kk > 1 ? 1u : 0u};
 }
 
@@ -509,11 +600,13 @@ int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void
         sq_all = reinterpret_cast<uint32_t*>(sq_iters + B);
     }
     TRY(enter(*ws, s));
+    Leave lv(*ws, s);
     CarryPlan cp;
     bool onepass;
     TRY(onepass_begin(*ws, OP_DEER, dtype, vec, T, B * D, kmax, s, &cp, &onepass));
+    Retire rt(*ws, s, onepass);
     if (per_sequence) CK(cudaMemsetAsync(ws->seq, 0, sq_words * sizeof(uint32_t), s));
-    uint32_t* slots = ws->words + 2;
+    uint32_t* slots = ws->words + kWordSlots;
     CK(cudaMemsetAsync(slots, 0, sizeof(uint32_t) * kmax, s));
     // iterate k writes buf[(k + flip) % 2]; buf[1] is the caller's y.
     // Iteration 1 reads the initial guess (a guess passed in y itself is first
@@ -581,7 +674,7 @@ int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void
             done = hs[(size_t)kmax * B] != 0;
         }
     }
-    onepass_end(*ws, onepass);
+    TRY(rt.done());
     if (launched_out) *launched_out = launched;
     if (!per_sequence) {
         if (k > kmax) k = kmax;
@@ -616,7 +709,7 @@ int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void
         *iters_out = kmx;
         if (resid_out) *resid_out = rmx;
     }
-    TRY(leave(*ws, s));
+    TRY(lv.done());
     return status;
 }
 
@@ -654,10 +747,12 @@ int deer_ode_solve(const float* w, const void* u, const float* dt, const void* h
         ws->ybuf_cap = cap;
     }
     TRY(enter(*ws, s));
+    Leave lv(*ws, s);
     CarryPlan cp;
     bool onepass;
     TRY(onepass_begin(*ws, OP_DEER_ODE, dtype, vec, T, B * D, kmax, s, &cp, &onepass));
-    uint32_t* slots = ws->words + 2;
+    Retire rt(*ws, s, onepass);
+    uint32_t* slots = ws->words + kWordSlots;
     CK(cudaMemsetAsync(slots, 0, sizeof(uint32_t) * kmax, s));
     CK(cudaMemsetAsync(ws->clamps, 0, sizeof(unsigned long long) * kmax, s));
     // as deer_diag_solve_ex: iterate k writes buf[(k + flip) % 2] (buf[1] is
@@ -695,7 +790,7 @@ int deer_ode_solve(const float* w, const void* u, const float* dt, const void* h
             if (rho < eps) { status = LR_OK; done = true; break; }
         }
     }
-    onepass_end(*ws, onepass);
+    TRY(rt.done());
     if (k > kmax) k = kmax;
     if (tgt(k) != y) CK(cudaMemcpyAsync(y, ws->ybuf, nbytes, cudaMemcpyDeviceToDevice, s));
     if (status != LR_ERR_NONFINITE) deer_remember(*ws, 1, T, B * D, dtype, k);
@@ -707,7 +802,7 @@ int deer_ode_solve(const float* w, const void* u, const float* dt, const void* h
     }
     *iters_out = k;
     if (resid_out) *resid_out = rho;
-    TRY(leave(*ws, s));
+    TRY(lv.done());
     return status;
 }
 
@@ -731,11 +826,12 @@ int deer_diag_bwd(const float* w, const void* y, const void* h0, const void* dy,
     Geom g;
     Carry cr;
     TRY(enter(*ws, s));
+    Leave lv(*ws, s);
     TRY(plan(*ws, OP_DEER_BWD, dtype, vec, T, B * D, D, &g, &cr, s));
-    TRY(grow(*ws, &ws->partials, &ws->partials_cap, (size_t)(g.n_chunks * g.C + g.C), false));
+    TRY(grow(*ws, &ws->partials, &ws->partials_cap, (size_t)(g.n_chunks * g.C + g.C), false, true));
     CK(launch_deer_bwd(dtype, vec, w, y, h0, dy, du, dh0, ws->partials, g, cr, s));
     CK(launch_bias_reduce(ws->partials, g.n_chunks, 1, B, D, BiasOut{{dw}}, s));
-    return leave(*ws, s);
+    return lv.done();
 }
 
 int lr_last_error(void) {
@@ -744,11 +840,17 @@ int lr_last_error(void) {
     TRY(get_ws(&ws));
     CK(cudaDeviceSynchronize());
     uint32_t bits = 0;
-    CK(cudaMemcpy(&bits, ws->words + 1, sizeof bits, cudaMemcpyDeviceToHost));
-    CK(cudaMemset(ws->words + 1, 0, sizeof(uint32_t)));
+    CK(cudaMemcpy(&bits, ws->words + kWordErr, sizeof bits, cudaMemcpyDeviceToHost));
+    CK(cudaMemset(ws->words + kWordErr, 0, sizeof(uint32_t)));
     // a launch that gave up may have stopped drawing tickets before the
-    // drawer that resets the counter: reset it here (nothing is in flight)
-    if (bits) CK(cudaMemset(ws->words, 0, sizeof(uint32_t)));
+    // drawer that resets the counter: reset it here (nothing is in flight),
+    // and retire its epoch
+    if (bits) {
+        u64 tw = 0;
+        CK(cudaMemcpy(&tw, ws->words, sizeof tw, cudaMemcpyDeviceToHost));
+        tw = (u64)epoch_after((uint32_t)(tw >> 32)) << 32;
+        CK(cudaMemcpy(ws->words, &tw, sizeof tw, cudaMemcpyHostToDevice));
+    }
     if (bits & ERRBIT_TIMEOUT) return LR_ERR_TIMEOUT;
     return LR_OK;
 }
@@ -777,6 +879,20 @@ int64_t lr_workspace_bytes(void) {
     return g_ws[dev]->bytes;
 }
 
+int lr_test_fail_after_enqueue(float* x, int64_t n, float value, uint64_t sleep_ns, void* stream) {
+    if (n < 0 || (n > 0 && !x)) return LR_ERR_INVALID_ARG;
+    GUARD;
+    cudaStream_t s = (cudaStream_t)stream;
+    DevWS* ws;
+    TRY(get_ws(&ws));
+    TRY(enter(*ws, s));
+    Leave lv(*ws, s);
+    k_test_sleep_fill<<<64, 256, 0, s>>>(x, n, value, sleep_ns);
+    CK(cudaGetLastError());
+    snprintf(g_cuda_msg, sizeof g_cuda_msg, "injected by lr_test_fail_after_enqueue");
+    return LR_ERR_CUDA;  // as if a later launch of the call had failed
+}
+
 int lr_test_activations(const float* x, float* tanh_out, float* sigmoid_out, float* expm1_out,
                         int64_t n, void* stream) {
     GUARD;
@@ -797,6 +913,7 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
     // Chain protocol: both chain kernels (register and TMA-staged) on a problem
     // of two time chunks and one channel tile, each with one CTA that is handed
     // tile 1: it waits for the state after tile 0, which nobody publishes.
+    // Look-back protocol: the same, tile 1 waits for tile 0's aggregate.
     // Walker protocol: the register and the segmented walker kernels, and the
     // consume-only segmented kernel, on a long one-strip problem launched
     // without walker CTAs: no entering state is ever published, so every
@@ -810,12 +927,26 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
     }
     char* buf = (char*)ws->test_buf;
     TRY(enter(*ws, s));
+    Leave lv(*ws, s);
     for (int tma = 0; tma < 2; ++tma) {
         const int64_t T = 2 * tile_shape(OP_SCAN_FWD, LR_F32, true, tma ? TILE_TMA : CARRY_CHAIN).L;
         Geom g;
         Carry cr;
-        TRY(plan(*ws, OP_SCAN_FWD, LR_F32, true, T, C, C, &g, &cr, s, tma));
+        TRY(plan(*ws, OP_SCAN_FWD, LR_F32, true, T, C, C, &g, &cr, s, tma, true));
         if (cr.mode != CARRY_CHAIN || cr.tma != tma) return LR_ERR_INVALID_ARG;
+        g.max_grid = 1;
+        g.ticket_base = 1;
+        cr.spin_limit = spin_limit;
+        const float* a = (const float*)buf;
+        CK(launch_scan_fwd(LR_F32, true, a, a + Tw * C, nullptr, (float*)buf + 2 * Tw * C, g, cr,
+                           s));
+    }
+    {  // look-back kernel
+        const int64_t T = 2 * tile_shape(OP_SCAN_FWD, LR_F32, true, TILE_TMA).L;
+        Geom g;
+        Carry cr;
+        TRY(plan(*ws, OP_SCAN_FWD, LR_F32, true, T, C, C, &g, &cr, s, 1));
+        if (cr.mode != CARRY_LOOK) return LR_ERR_INVALID_ARG;
         g.max_grid = 1;
         g.ticket_base = 1;
         cr.spin_limit = spin_limit;
@@ -843,12 +974,12 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
         cr.n_walk = 0;
         cr.spin_limit = spin_limit;
         const float* z = (const float*)buf;  // zeros: w, u and the previous iterate
-        const NextAgg nx{cr.agg, cr.epoch + 1, 1u};
+        const NextAgg nx{cr.agg, 0u, 1u};
         CK(launch_deer_iter(LR_F32, true, z, z, nullptr, z + Tw * C, (float*)buf + 2 * Tw * C,
-                            ws->words + 2, nullptr, 0.f, nx, DeerSeq{nullptr, nullptr, nullptr}, g,
+                            ws->words + kWordSlots, nullptr, 0.f, nx, DeerSeq{nullptr, nullptr, nullptr}, g,
                             cr, s));
     }
-    return leave(*ws, s);
+    return lv.done();
 }
 
 }  // extern "C"

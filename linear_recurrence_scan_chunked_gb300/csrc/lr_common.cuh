@@ -40,7 +40,13 @@
 //     atomic ticket, so every producer a CTA waits for is already running: the
 //     wait always ends.  Every wait is still bounded (spin_limit polls); when
 //     it runs out the CTA records LR_ERR_TIMEOUT and publishes NaN, so nothing
-//     downstream waits in turn.
+//     downstream waits in turn;
+//   * the launch's epoch lives on the device, in the high half of the 64-bit
+//     ticket word (the low half counts the tickets): every draw returns both,
+//     so a CTA learns its launch's epoch with its first ticket at no extra
+//     cost, and the last drawer retires the epoch as it resets the counter.
+//     A launch replayed from a CUDA graph therefore takes a fresh epoch, like
+//     one enqueued by the host.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -54,6 +60,7 @@ namespace lrs {
 constexpr uint32_t ERRBIT_TIMEOUT = 1u;
 constexpr int CARRY_CHAIN = 0;
 constexpr int CARRY_WALK = 1;
+constexpr int CARRY_LOOK = 2;
 constexpr int WALK_MAX_WV = 4;  // channels per walker warp (upper bound)
 constexpr int WALK_P = 4;       // consecutive chunks per walker lane
 
@@ -69,17 +76,21 @@ typedef unsigned long long u64;
 constexpr int kFoldUnroll = LR_FOLD_UNROLL;
 
 struct Carry {
-    u64* agg;             // WALK: [C][n_chunks][2] packets (A, B) of every tile
+    u64* agg;             // WALK: [C][n_chunks][2] packets (A, B) of every tile;
+                          // LOOK: [n_chunks][C][2] (chunk-major: a tile publishes
+                          // one contiguous row, a look-back reads whole rows)
     u64* inc;             // packets: state after chunk q (scan order); CHAIN stores
                           // them chunk-major [n_chunks][C] (a tile reads one row),
                           // WALK channel-major [C][n_chunks] (a walker warp reads
                           // and writes 32 consecutive chunks of one channel)
-    uint32_t* ticket;     // ticket counter (0 between launches)
+    u64* tk;              // ticket word: low 32 bits the ticket counter (0 between
+                          // launches), high 32 bits the last retired epoch
     uint32_t* err;        // sticky error bits
-    uint32_t epoch;       // 1 .. 2^32-1, one per launch
+    uint32_t epoch;       // this launch's epoch (1 .. 2^32-1): set on the device
+                          // from the ticket word by each CTA's first draw
     uint32_t spin_limit;  // polls before a wait gives up
-    int mode;             // CARRY_CHAIN or CARRY_WALK
-    uint32_t n_walk;      // walker CTAs (first tickets); 0 in CHAIN mode
+    int mode;             // CARRY_CHAIN, CARRY_WALK or CARRY_LOOK
+    uint32_t n_walk;      // walker CTAs (first tickets); 0 in CHAIN / LOOK mode
     int wv;               // channels per walker warp (WALK)
     int tma;              // CHAIN: tiles are staged by TMA (k_strip / k_tchain)
 };
@@ -136,6 +147,50 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+// ------------------------------------------------------ tickets and epochs
+// The epoch that follows the last retired one (0 is never an epoch: a packet
+// buffer cleared to zero holds no valid packet).
+__host__ __device__ __forceinline__ uint32_t epoch_after(uint32_t last) {
+    return last + 1u == 0u ? 1u : last + 1u;
+}
+// Draw one ticket: returns it, and sets c.epoch to the launch's epoch (every
+// draw of a launch sees the same high half, until the last drawer retires it).
+template <class Cr>
+__device__ __forceinline__ uint32_t draw_ticket(Cr& c) {
+    const unsigned long long v =
+        atomicAdd(reinterpret_cast<unsigned long long*>(c.tk), 1ull);
+    c.epoch = epoch_after((uint32_t)(v >> 32));
+    return (uint32_t)v;
+}
+// After ticket t was drawn: the launch's last draw resets the counter and
+// retires the epoch in one atomic (every CTA has drawn by then, so each has
+// read the epoch).  A maximum rather than an exchange: when a wait of this
+// launch ran out and already retired later epochs, the word keeps them (and
+// its counter, which lr_last_error resets) -- except at the wrap to epoch 1.
+template <class Cr, class G>
+__device__ __forceinline__ void ticket_drawn(const Cr& c, const G& g, uint32_t t) {
+    if (t == g.n_draws - 1) {
+        unsigned long long* w = reinterpret_cast<unsigned long long*>(c.tk);
+        const unsigned long long v = (unsigned long long)c.epoch << 32;
+        if (c.epoch == 1u) atomicExch(w, v);
+        else atomicMax(w, v);
+    }
+}
+// Retire the launch's epoch outside the normal end of a launch: a wait that
+// ran out (the launch will not complete its draws) or a launch with nothing
+// to do.  The counter half is left alone; a timed-out launch leaves it for
+// lr_last_error to reset.  Several callers in one launch only skip epochs.
+template <class Cr>
+__device__ __forceinline__ void retire_epoch(const Cr& c) {
+    atomicAdd(reinterpret_cast<unsigned long long*>(c.tk), 1ull << 32);
+}
+// A wait ran out: record the error, retire the epoch.
+template <class Cr>
+__device__ __forceinline__ void give_up(const Cr& c) {
+    atomicOr(c.err, ERRBIT_TIMEOUT);
+    retire_epoch(c);
 }
 
 // Streaming 16-byte loads of read-once inputs (no L1 allocation).
@@ -578,7 +633,7 @@ __device__ __forceinline__ void walk_window(const Carry& cr, const Geom& g, int6
             return;
         }
         if (__any_sync(0xffffffffu, wait_step(cr, spins, sleep_ns, 0))) {
-            if (lane == 0) atomicOr(cr.err, ERRBIT_TIMEOUT);
+            if (lane == 0) give_up(cr);
             dead = true;  // publish NaN for the rest so no tile keeps waiting
             continue;
         }
@@ -735,7 +790,7 @@ __device__ __forceinline__ void tile_carry(CarrySmem<VEC, NW>& sm, const float (
                     if (__all_sync(0xffffffffu, ok)) break;
                 }
                 if (__any_sync(0xffffffffu, wait_step(cr, spins, sleep_ns, kTileMaxSleepNs))) {
-                    if (lane == 0) atomicOr(cr.err, ERRBIT_TIMEOUT);
+                    if (lane == 0) give_up(cr);
 #pragma unroll
                     for (int v = 0; v < VEC; ++v) cin[v] = __int_as_float(0x7fc00000);
                     break;

@@ -29,6 +29,17 @@
 #define LR_STRIP_ONEB 1
 #endif
 
+// Walker-protocol tile of the forward scan (the register walker kernel runs
+// it): warps per CTA and rows per thread.  The kernel keeps 16 warps per SM
+// resident whatever the CTA width (narrower CTAs: more of them per SM, each
+// with its own ticket in flight).
+#ifndef LR_WALK_FWD_NW
+#define LR_WALK_FWD_NW 8
+#endif
+#ifndef LR_WALK_FWD_R
+#define LR_WALK_FWD_R 8
+#endif
+
 // Register cap of the TMA-staged kernel: two CTAs of NW+1 = 9 warps per SM.
 #ifndef LR_TMA_MAXNREG
 #define LR_TMA_MAXNREG 112
@@ -72,11 +83,13 @@ struct KCfg {
 };
 constexpr KCfg kcfg(Op op, int dtype, int mode) {
     // bf16 holds two elements per register: twice the rows of fp32 (but the
-    // DEER backward keeps two fp32 values per element between its passes: the
-    // rows of fp32 for both).  The LSTM cell stages as many arrays per
-    // direction as the SRU cell and takes its rows; DEER's ODE form takes the
-    // tanh form's.
+    // DEER forms keep two fp32 values per element between their passes, J and
+    // the right-hand side or the backward's two factors: the rows of fp32 for
+    // both storage types).  The LSTM cell stages as many arrays per direction
+    // as the SRU cell and takes its rows; DEER's ODE form takes the tanh
+    // form's.
     return op == OP_DEER_ODE   ? kcfg(OP_DEER, dtype, mode)
+           : op == OP_DEER && dtype == 1 ? kcfg(OP_DEER, 0, mode)
            : op == OP_LSTM_FWD ? kcfg(OP_SRU_FWD, dtype, mode)
            : op == OP_LSTM_BWD ? kcfg(OP_SRU_BWD, dtype, mode)
            : op == OP_DEER_BWD ? KCfg{8, mode == CARRY_CHAIN ? 2 : 4, mode == TILE_TMA ? 3 : 0}
@@ -87,7 +100,7 @@ constexpr KCfg kcfg(Op op, int dtype, int mode) {
                   : op == OP_SRU_BWD  ? KCfg{8, dtype == 1 ? 2 : 1, 0}
                   :                     KCfg{8, dtype == 1 ? 4 : 2, 0})
            : mode == CARRY_WALK
-               ? (op == OP_SCAN_FWD ? KCfg{8, 8, 0}
+               ? (op == OP_SCAN_FWD ? KCfg{LR_WALK_FWD_NW, LR_WALK_FWD_R, 0}
                   : op == OP_SCAN_BWD ? KCfg{8, dtype == 1 ? 8 : 4, 0}
                   : op == OP_SRU_FWD  ? KCfg{8, dtype == 1 ? 8 : 4, 0}
                   : op == OP_SRU_BWD  ? KCfg{8, dtype == 1 ? 4 : 2, 0}
@@ -129,25 +142,47 @@ inline bool use_tma(int dtype, bool vec, int64_t T, int64_t C) {
 // Which carry protocol a launch uses, its tile shape, and the packet storage
 // it needs.  WALK pays off once the chunk chain is long (a round trip per
 // chunk level would dominate) and the channels are few enough for a handful
-// of walker CTAs; otherwise CHAIN.  The choice depends on the shape only, so a
+// of walker CTAs; LOOK when the problem is short enough for every tile to
+// fold all the chunk aggregates before it (TMA path); otherwise CHAIN (the
+// strip kernel for wide problems).  The choice depends on the shape only, so a
 // given problem always gets the same association of its floating-point
 // operations.
 struct CarryPlan {
-    int mode;          // CARRY_CHAIN / CARRY_WALK
+    int mode;          // CARRY_CHAIN / CARRY_WALK / CARRY_LOOK
     bool tma;          // CHAIN: a TMA-staged kernel runs it (strip / TMA chain)
     TileShape ts;      // tile shape of that protocol
     int64_t n_chunks;  // ceil(T / ts.L)
     uint32_t n_walk;   // walker CTAs
     int wv;            // channels per walker warp
     size_t inc_elems;  // state packets: n_chunks * C
-    size_t agg_elems;  // aggregate packets (WALK): 2 * n_chunks * C
+    size_t agg_elems;  // aggregate packets (WALK, LOOK): 2 * n_chunks * C
 };
 constexpr int64_t kWalkMinChunks = 128;
+// The look-back protocol reads, for a tile of chunk q, q aggregate packets
+// per channel: about n_chunks^2 / 2 * 2 KB per channel tile in all.  It runs
+// while n_chunks^2 * n_ct stays within this bound (~32 MB of L2 reads), i.e.
+// where the chunk chain's one round trip per chunk level, not the bytes,
+// would bound the launch.
+constexpr int64_t kLookBudget = 32768;
 // Channel strips from which the strip kernel runs a chain-protocol launch
 // (one CTA per strip or more strips per CTA; fewer strips would leave SMs
 // idle, and the chain kernel spreads the chunks of few strips over all SMs).
 constexpr int64_t kStripMinStrips = 128;
 constexpr int64_t kWalkMaxCtas = 32;
+
+// The chain protocol's plan (TMA-staged or through registers).
+inline CarryPlan chain_plan(Op op, int dtype, bool vec, bool tma, int64_t T, int64_t C) {
+    CarryPlan p{};
+    p.mode = CARRY_CHAIN;
+    p.tma = tma && vec;
+    p.ts = tile_shape(op, dtype, vec, p.tma ? TILE_TMA : CARRY_CHAIN);
+    p.n_chunks = (T + p.ts.L - 1) / p.ts.L;
+    p.n_walk = 0;
+    p.wv = 0;
+    p.inc_elems = (size_t)(p.n_chunks * C);
+    p.agg_elems = 0;
+    return p;
+}
 
 inline CarryPlan carry_plan(Op op, int dtype, bool vec, bool tma, int64_t T, int64_t C) {
     CarryPlan p{};
@@ -173,15 +208,22 @@ inline CarryPlan carry_plan(Op op, int dtype, bool vec, bool tma, int64_t T, int
             return p;
         }
     }
-    p.mode = CARRY_CHAIN;
-    p.tma = tma;
-    p.ts = tile_shape(op, dtype, vec, p.tma ? TILE_TMA : CARRY_CHAIN);
-    p.n_chunks = (T + p.ts.L - 1) / p.ts.L;
-    p.n_walk = 0;
-    p.wv = 0;
-    p.inc_elems = (size_t)(p.n_chunks * C);
-    p.agg_elems = 0;
-    return p;
+    if (tma) {
+        const TileShape tt = tile_shape(op, dtype, vec, TILE_TMA);
+        const int64_t nc = (T + tt.L - 1) / tt.L, nct = (C + tt.CW - 1) / tt.CW;
+        if (nct < kStripMinStrips && nc <= 4096 && nc * nc * nct <= kLookBudget) {
+            p.mode = CARRY_LOOK;
+            p.tma = true;
+            p.ts = tt;
+            p.n_chunks = nc;
+            p.n_walk = 0;
+            p.wv = 0;
+            p.inc_elems = 0;
+            p.agg_elems = (size_t)(2 * nc * C);
+            return p;
+        }
+    }
+    return chain_plan(op, dtype, vec, tma, T, C);
 }
 
 // Grid of a persistent launch: every walker plus as many tile CTAs as can be

@@ -4,7 +4,10 @@
 //   k_seg    (long, narrow problems: walker protocol over segments, TMA-staged),
 //   k_seg1   (k_seg's consume pass alone, for launches whose segment
 //             aggregates the previous launch published: DEER iterations),
-//   k_tchain (chain protocol, TMA-staged, for what is neither),
+//   k_look   (short problems: every tile publishes its aggregate at once and
+//             folds those of the chunks before it -- one round trip, not one
+//             per chunk level; TMA-staged),
+//   k_tchain (chain protocol, TMA-staged, for what is none of these),
 //   k_stream (walker protocol through registers),
 //   k_chain  (chain protocol through registers: scalar / unaligned paths),
 // and launch_persist, which picks one for a call.
@@ -103,30 +106,36 @@ __device__ __forceinline__ void gload(const typename Op::Params& p, const Geom& 
 // inputs and one write of the outputs as long as the d_con tiles in flight fit
 // in L2.
 template <class Op>
-__global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
-    k_stream(typename Op::Params p, Geom g, Carry cr, uint32_t d_con) {
-    if (Op::skip(p)) return;  // whole launch: before any ticket or barrier
+__global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
+    k_stream(typename Op::Params p, Geom g, const Carry cr0, uint32_t d_con) {
+    if (Op::skip(p)) {  // whole launch: before any ticket or barrier
+        if (blockIdx.x == 0 && threadIdx.x == 0) retire_epoch(cr0);
+        return;
+    }
     constexpr int VEC = Op::VEC;
     __shared__ CarrySmem<VEC, Op::NW> sm;
     __shared__ typename Op::Smem xs;
-    __shared__ uint32_t s_ticket;
+    __shared__ uint32_t s_ticket, s_epoch;
+    Carry cr = cr0;
     typename Op::Acc acc;
     Op::acc_init(acc);
     const uint32_t limit = cr.n_walk + g.n_tiles + d_con;
     bool tile_role = false;
     if (threadIdx.x == 0) {
-        const uint32_t t = atomicAdd(cr.ticket, 1u);
-        if (t == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+        const uint32_t t = draw_ticket(cr);
+        ticket_drawn(cr, g, t);
         s_ticket = t + g.ticket_base;
+        s_epoch = cr.epoch;
     }
     __syncthreads();
+    cr.epoch = s_epoch;
     uint32_t tk = s_ticket;
     while (true) {
         // the next ticket is drawn now and read after this one's work (a tile
         // CTA; a walker returns before it draws again)
         uint32_t next = 0;
         const bool draw = tk >= cr.n_walk && tk < limit;
-        if (draw && threadIdx.x == 0) next = atomicAdd(cr.ticket, 1u);
+        if (draw && threadIdx.x == 0) next = draw_ticket(cr);
         if (tk < cr.n_walk) {  // walker role
             walker<typename Op::S, Op::NW>(cr, g, tk, Op::init_ptr(p));
             return;
@@ -171,7 +180,7 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
             Op::finish(p, g, tc, regs, w, s, xs, acc);
         }
         if (draw && threadIdx.x == 0) {
-            if (next == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+            ticket_drawn(cr, g, next);
             s_ticket = next + g.ticket_base;
         }
         __syncthreads();
@@ -211,10 +220,11 @@ __device__ __forceinline__ uint32_t chain_tile(const typename Op::Params& p, con
                                                typename Op::Smem& xs, typename Op::Acc& acc,
                                                bool draw, uint32_t* s_ticket) {
     uint32_t next = 0;
-    if (draw && threadIdx.x == 0) next = atomicAdd(cr.ticket, 1u);  // latency hidden by the tile
+    Carry c = cr;
+    if (draw && threadIdx.x == 0) next = draw_ticket(c);  // latency hidden by the tile
     tile_process<Op>(p, g, cr, tile_coord<Op>(g, tile), regs, sm, xs, acc);
     if (draw && threadIdx.x == 0) {
-        if (next == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+        ticket_drawn(cr, g, next);
         *s_ticket = next + g.ticket_base;
     }
     __syncthreads();  // publishes the ticket; frees the carry smem for the next tile
@@ -229,17 +239,23 @@ __device__ __forceinline__ uint32_t chain_tile(const typename Op::Params& p, con
 // hidden behind the tiles of the other channel tiles.
 template <class Op>
 __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
-    k_chain(typename Op::Params p, Geom g, Carry cr) {
-    if (Op::skip(p)) return;  // whole launch: before any ticket or barrier
+    k_chain(typename Op::Params p, Geom g, const Carry cr0) {
+    if (Op::skip(p)) {  // whole launch: before any ticket or barrier
+        if (blockIdx.x == 0 && threadIdx.x == 0) retire_epoch(cr0);
+        return;
+    }
     __shared__ CarrySmem<Op::VEC, Op::NW> sm;
     __shared__ typename Op::Smem xs;
-    __shared__ uint32_t s_ticket;
+    __shared__ uint32_t s_ticket, s_epoch;
+    Carry cr = cr0;
     if (threadIdx.x == 0) {
-        const uint32_t t = atomicAdd(cr.ticket, 1u);
-        if (t == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+        const uint32_t t = draw_ticket(cr);
+        ticket_drawn(cr, g, t);
         s_ticket = t + g.ticket_base;
+        s_epoch = cr.epoch;
     }
     __syncthreads();
+    cr.epoch = s_epoch;
     uint32_t tk = s_ticket;
     const uint32_t limit = g.n_tiles;
     if (tk >= limit) return;
@@ -250,8 +266,8 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
     gload<Op>(p, g, t0, r0);
     __syncthreads();
     if (threadIdx.x == 0) {
-        const uint32_t t = atomicAdd(cr.ticket, 1u);
-        if (t == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+        const uint32_t t = draw_ticket(cr);
+        ticket_drawn(cr, g, t);
         s_ticket = t + g.ticket_base;
     }
     __syncthreads();
@@ -286,20 +302,24 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
 // up on a stage sets the shared abort flag, and the consumers decide to stop
 // together, after a barrier; the producer waits for its copies in flight
 // before it exits.
+// The producer also hands the consumers the launch's epoch (s_epoch, written
+// before the first stage is armed: the consumers read it after their first
+// completed wait).
 template <class Op, int ST>
-__device__ __forceinline__ void tma_produce(const Geom& g, const Carry& cr, const TmaDesc& td,
+__device__ __forceinline__ void tma_produce(const Geom& g, Carry cr, const TmaDesc& td,
                                             unsigned char* ring, uint64_t* full, uint64_t* empty,
-                                            uint32_t* s_tile) {
+                                            uint32_t* s_tile, uint32_t* s_epoch) {
     constexpr int L = Op::NW * Op::R, CW = 32 * Op::VEC;
     constexpr uint32_t SB = tma_stage_bytes<Op>();
     uint32_t k = 0;          // stage uses so far
     bool last_plain = false; // use k was the final (tile-less) arrival
     for (;; ++k) {
         const uint32_t st = k % ST;
-        const uint32_t t = atomicAdd(cr.ticket, 1u);  // latency overlaps the wait below
-        if (t == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+        const uint32_t t = draw_ticket(cr);  // latency overlaps the wait below
+        ticket_drawn(cr, g, t);
+        if (k == 0) *s_epoch = cr.epoch;
         if (k >= ST && !mbar_wait(&empty[st], ((k / ST) - 1u) & 1u, cr.err)) {
-            atomicOr(cr.err, ERRBIT_TIMEOUT);
+            give_up(cr);
             break;
         }
         const uint32_t tile = t + g.ticket_base;
@@ -327,8 +347,11 @@ __device__ __forceinline__ void tma_produce(const Geom& g, const Carry& cr, cons
 
 template <class Op, int ST>
 __global__ void __maxnreg__(LR_TMA_MAXNREG)
-    k_tchain(typename Op::Params p, Geom g, Carry cr, const __grid_constant__ TmaDesc td) {
-    if (Op::skip(p)) return;  // whole launch: before any ticket or barrier
+    k_tchain(typename Op::Params p, Geom g, const Carry cr0, const __grid_constant__ TmaDesc td) {
+    if (Op::skip(p)) {  // whole launch: before any ticket or barrier
+        if (blockIdx.x == 0 && threadIdx.x == 0) retire_epoch(cr0);
+        return;
+    }
     constexpr int NW = Op::NW, VEC = Op::VEC, L = Op::NW * Op::R;
     constexpr uint32_t SB = tma_stage_bytes<Op>();
     extern __shared__ unsigned char dyn_smem[];
@@ -339,8 +362,9 @@ __global__ void __maxnreg__(LR_TMA_MAXNREG)
     __shared__ typename Op::Smem xs;
     __shared__ __align__(8) uint64_t full[ST], empty[ST];
     __shared__ uint32_t s_tile[ST];
-    __shared__ uint32_t s_abort;
+    __shared__ uint32_t s_abort, s_epoch;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Carry cr = cr0;
     if (threadIdx.x == 0) {
         for (int i = 0; i < ST; ++i) {
             mbar_init(&full[i], 1);
@@ -351,7 +375,7 @@ __global__ void __maxnreg__(LR_TMA_MAXNREG)
     }
     __syncthreads();
     if (warp == NW) {
-        if (lane == 0) tma_produce<Op, ST>(g, cr, td, ring, full, empty, s_tile);
+        if (lane == 0) tma_produce<Op, ST>(g, cr, td, ring, full, empty, s_tile, &s_epoch);
         return;
     }
     typename Op::Acc acc;
@@ -363,6 +387,7 @@ __global__ void __maxnreg__(LR_TMA_MAXNREG)
             atomicOr(cr.err, ERRBIT_TIMEOUT);
         }
         csync<NW>();  // the decision below is the same in every consumer
+        cr.epoch = s_epoch;
         const uint32_t tile = s_tile[st];
         if (s_abort != 0 || tile >= g.n_tiles) break;
         const TileCoord tc = tile_coord<Op>(g, tile);
@@ -371,6 +396,228 @@ __global__ void __maxnreg__(LR_TMA_MAXNREG)
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
         tile_process<Op>(p, g, cr, tc, regs, sm, xs, acc);
+    }
+    Op::at_exit(p, xs, acc);
+}
+
+// Look-back kernel (LOOK protocol; short problems whose chunk chain would
+// cost one L2 round trip per chunk level).  The tiles are staged by TMA as in
+// the TMA chain kernel (producer warp, tickets in scan order).  A tile
+//   1. folds its rows into its aggregate and publishes it at once (before it
+//      waits for anything): packets agg[q][c] = (A, B) of chunk q;
+//   2. looks back over every chunk before it: warp w folds the aggregates of
+//      its share [q*w/NW, q*(w+1)/NW) of chunks 0 .. q-1 (issued as one batch
+//      of loads per LOOK_PB chunks, polled until they carry this launch's
+//      epoch), and the state entering the tile is h0 carried through the NW
+//      shares in order;
+//   3. re-reads its rows from the stage and writes its outputs.
+// Every chunk's aggregate is published before its tile waits, so once the
+// tiles of a wave have reduced their rows, each wait costs one round trip to
+// L2 instead of one per chunk level, and no chunk waits for another's state.
+// The association of every operation is fixed by (q, NW): the result is
+// bitwise reproducible.  The look-back reads q * 16 bytes per channel, which
+// bounds the protocol to problems with few chunks (the launch plan).
+#ifndef LR_LOOK_PB
+#define LR_LOOK_PB 4
+#endif
+constexpr int LOOK_PB = LR_LOOK_PB;  // preceding chunks per warp per batch of loads
+
+// Warp-level: the fold of the aggregates of chunks [lo, hi) for this lane's
+// channels, in chunk order.  Polls until every packet carries the launch's
+// epoch; a wait that runs out gives NaN (and records the error).
+template <int VEC>
+__device__ __forceinline__ void look_fold(const Carry& cr, const Geom& g, uint32_t lo, uint32_t hi,
+                                          int64_t c, bool cok, float (&RA)[VEC], float (&RB)[VEC]) {
+    constexpr int PB = LOOK_PB;
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) { RA[v] = 1.f; RB[v] = 0.f; }
+    uint32_t spins = 0, sleep_ns = 0;
+    bool dead = false;
+    for (uint32_t p0 = lo; p0 < hi; p0 += PB) {
+        const uint32_t n = hi - p0 < (uint32_t)PB ? hi - p0 : (uint32_t)PB;
+        u64 pk[PB][VEC][2];
+        bool okk[PB];
+#pragma unroll
+        for (int k = 0; k < PB; ++k) {
+            okk[k] = !cok || (uint32_t)k >= n;
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                pk[k][v][0] = pk[k][v][1] = 0;
+                if (!okk[k]) ld_pkt2(cr.agg + 2 * ((int64_t)(p0 + k) * g.C + c + v), pk[k][v][0], pk[k][v][1]);
+            }
+        }
+        while (!dead) {
+            bool all = true;
+#pragma unroll
+            for (int k = 0; k < PB; ++k) {
+                if (!okk[k]) {
+                    bool ok = true;
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v)
+                        ok = ok && pkt_ok(pk[k][v][0], cr.epoch) && pkt_ok(pk[k][v][1], cr.epoch);
+                    okk[k] = ok;
+                }
+                all = all && okk[k];
+            }
+            if (__all_sync(0xffffffffu, all)) break;
+            if (__any_sync(0xffffffffu, wait_step(cr, spins, sleep_ns, kTileMaxSleepNs))) {
+                if ((threadIdx.x & 31) == 0) give_up(cr);
+                dead = true;
+                break;
+            }
+#pragma unroll
+            for (int k = 0; k < PB; ++k)  // re-poll what was not visible
+                if (!okk[k])
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v)
+                        ld_pkt2(cr.agg + 2 * ((int64_t)(p0 + k) * g.C + c + v), pk[k][v][0], pk[k][v][1]);
+        }
+        if (dead) break;
+#pragma unroll
+        for (int k = 0; k < PB; ++k)
+            if ((uint32_t)k < n)
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    const float a = pkt_val(pk[k][v][0]);
+                    RB[v] = __fmaf_rn(a, RB[v], pkt_val(pk[k][v][1]));
+                    RA[v] *= a;
+                }
+    }
+    if (dead) {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) RA[v] = RB[v] = __int_as_float(0x7fc00000);
+    }
+}
+
+template <class Op, int ST>
+__global__ void __maxnreg__(LR_TMA_MAXNREG)
+    k_look(typename Op::Params p, Geom g, const Carry cr0, const __grid_constant__ TmaDesc td) {
+    if (Op::skip(p)) {  // whole launch: before any ticket or barrier
+        if (blockIdx.x == 0 && threadIdx.x == 0) retire_epoch(cr0);
+        return;
+    }
+    constexpr int NW = Op::NW, VEC = Op::VEC, L = Op::NW * Op::R;
+    constexpr uint32_t SB = tma_stage_bytes<Op>();
+    extern __shared__ unsigned char dyn_smem[];
+    unsigned char* ring = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~(uintptr_t)127);
+    // warp aggregates of the tile, then (after a barrier) each warp's fold
+    // of its share of the preceding chunks
+    __shared__ StripSmem<VEC, NW> sm;
+    __shared__ typename Op::Smem xs;
+    __shared__ __align__(8) uint64_t full[ST], empty[ST];
+    __shared__ uint32_t s_tile[ST];
+    __shared__ uint32_t s_abort, s_epoch;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Carry cr = cr0;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < ST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NW);
+        }
+        s_abort = 0;
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (warp == NW) {
+        if (lane == 0) tma_produce<Op, ST>(g, cr, td, ring, full, empty, s_tile, &s_epoch);
+        return;
+    }
+    typename Op::Acc acc;
+    Op::acc_init(acc);
+    for (uint32_t k = 0;; ++k) {
+        const uint32_t st = k % ST;
+        if (!mbar_wait(&full[st], (k / ST) & 1u, cr.err)) {
+            s_abort = 1;
+            atomicOr(cr.err, ERRBIT_TIMEOUT);
+        }
+        csync<NW>();  // uniform stop decision; the previous tile is done with sm
+        cr.epoch = s_epoch;
+        const uint32_t tile = s_tile[st];
+        if (s_abort != 0 || tile >= g.n_tiles) break;
+        const TileCoord tc = tile_coord<Op>(g, tile);
+        const SmemSrc<Op> src{ring + st * SB, tc.tchunk * L, lane * VEC};
+        float A[VEC], B[VEC];
+        {
+            typename Op::Regs regs;
+            typename Op::Work w;
+            Op::load(src, p, g, tc, regs);
+            Op::aggregate(p, g, tc, regs, w, A, B, false);
+        }
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            sm.a[warp][lane][v] = A[v];
+            sm.b[warp][lane][v] = B[v];
+        }
+        csync<NW>();
+        // 1. the tile's aggregate, published before any wait
+        if (warp == 0 && tc.cok && tc.q < g.n_chunks - 1) {
+            float TA[VEC], TB[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) { TA[v] = 1.f; TB[v] = 0.f; }
+#pragma unroll
+            for (int w2 = 0; w2 < NW; ++w2)
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    const float a = sm.a[w2][lane][v];
+                    TB[v] = __fmaf_rn(a, TB[v], sm.b[w2][lane][v]);
+                    TA[v] *= a;
+                }
+#pragma unroll
+            for (int v = 0; v < VEC; ++v)
+                st_pkt2(cr.agg + 2 * (tc.q * g.C + tc.c + v), pkt(TA[v], cr.epoch), pkt(TB[v], cr.epoch));
+        }
+        // the warps before this one within the tile, as one affine map
+        float PA[VEC], PB[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { PA[v] = 1.f; PB[v] = 0.f; }
+#pragma unroll
+        for (int w2 = 0; w2 < NW - 1; ++w2)
+            if (w2 < warp)
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    const float a = sm.a[w2][lane][v];
+                    PB[v] = __fmaf_rn(a, PB[v], sm.b[w2][lane][v]);
+                    PA[v] *= a;
+                }
+        csync<NW>();  // sm is free for the look-back
+        // 2. this warp's share of the preceding chunks
+        const uint32_t q = (uint32_t)tc.q;
+        const uint32_t lo = (uint32_t)(((uint64_t)q * warp) / NW);
+        const uint32_t hi = (uint32_t)(((uint64_t)q * (warp + 1)) / NW);
+        {
+            float RA[VEC], RB[VEC];
+            look_fold<VEC>(cr, g, lo, hi, tc.c, tc.cok, RA, RB);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                sm.a[warp][lane][v] = RA[v];
+                sm.b[warp][lane][v] = RB[v];
+            }
+        }
+        csync<NW>();
+        float s[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) s[v] = 0.f;
+        const typename Op::S* ip = Op::init_ptr(p);
+        if (ip != nullptr && tc.cok) load_vec<typename Op::S, VEC>(ip + tc.c, s);
+#pragma unroll
+        for (int w2 = 0; w2 < NW; ++w2)
+            if ((uint64_t)q * (w2 + 1) / NW > (uint64_t)q * w2 / NW)  // a non-empty share
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) s[v] = __fmaf_rn(sm.a[w2][lane][v], s[v], sm.b[w2][lane][v]);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) s[v] = __fmaf_rn(PA[v], s[v], PB[v]);
+        // 3. the outputs, from the rows still in the stage
+        {
+            typename Op::Regs regs;
+            typename Op::Work w;
+            float A2[VEC], B2[VEC];
+            Op::load(src, p, g, tc, regs);
+            Op::aggregate(p, g, tc, regs, w, A2, B2, true);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
+            Op::finish(p, g, tc, regs, w, s, xs, acc);
+        }
     }
     Op::at_exit(p, xs, acc);
 }
@@ -612,9 +859,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 template <class Op, int ST>
 __global__ void __launch_bounds__(Op::NW * 32, 2)
-    k_seg(typename Op::Params p, Geom g, Carry cr, SegGeom sg,
+    k_seg(typename Op::Params p, Geom g, const Carry cr0, SegGeom sg,
           const __grid_constant__ TmaDesc td) {
-    if (Op::skip(p)) return;  // whole launch: before any ticket or barrier
+    if (Op::skip(p)) {  // whole launch: before any ticket or barrier
+        if (blockIdx.x == 0 && threadIdx.x == 0) retire_epoch(cr0);
+        return;
+    }
+    Carry cr = cr0;
     constexpr int NW = Op::NW, VEC = Op::VEC, L = Op::NW * Op::R;
     constexpr uint32_t SB = tma_stage_bytes<Op>();
     constexpr bool NXT = has_next_agg<Op>::value;
@@ -626,7 +877,7 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
     typename Op::Smem& xs = scratch<Op>(sm, xs_own);
     __shared__ float carry[2][32][VEC];  // by chunk parity
     __shared__ __align__(8) uint64_t full[ST];
-    __shared__ uint32_t s_tk[2], s_abort;
+    __shared__ uint32_t s_tk[2], s_abort, s_epoch;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t limit = cr.n_walk + sg.n_units;
     NextAgg nx{nullptr, 0u, 0u};
@@ -637,12 +888,15 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
     const uint32_t nred = pre ? 0u : sg.seg;
     const uint32_t uses = nred + sg.seg;
     if (threadIdx.x == 0) {
-        const uint32_t t = atomicAdd(cr.ticket, 1u);
-        if (t == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+        const uint32_t t = draw_ticket(cr);
+        ticket_drawn(cr, g, t);
         s_tk[0] = t;
         s_abort = 0;
+        s_epoch = cr.epoch;
     }
     __syncthreads();
+    cr.epoch = s_epoch;
+    nx.epoch = epoch_after(cr.epoch);  // the next launch's
     uint32_t cur = s_tk[0];
     if (cur < cr.n_walk) {  // walker role: its chunks are the segments
         Geom gw = g;
@@ -683,14 +937,14 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         mbar_init_fence();
         pol_keep = l2_evict_last();
         pol_drop = l2_evict_first();
-        const uint32_t t1 = atomicAdd(cr.ticket, 1u);
-        if (t1 == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+        const uint32_t t1 = draw_ticket(cr);
+        ticket_drawn(cr, g, t1);
         if (t1 >= limit) drawing = false;
         s_tk[1] = t1;
         // uses 0 .. ST-1: the first chunks of the reduce pass of `cur`, or of
         // its consume pass when pre (the launch keeps SEG >= ST)
         for (uint32_t u = 0; u < (uint32_t)ST; ++u) issue(u, cur, pre ? cur : limit);
-        if (drawing) pend = atomicAdd(cr.ticket, 1u);
+        if (drawing) pend = draw_ticket(cr);
     }
     __syncthreads();
     tq[SEG_LAG + 1] = s_tk[1];
@@ -816,7 +1070,7 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
                                                    cin, cr.epoch);
                     if (__all_sync(0xffffffffu, ok)) break;
                     if (__any_sync(0xffffffffu, wait_step(cr, spins, sleep_ns, kTileMaxSleepNs))) {
-                        if (lane == 0) atomicOr(cr.err, ERRBIT_TIMEOUT);
+                        if (lane == 0) give_up(cr);
 #pragma unroll
                         for (int v = 0; v < VEC; ++v) cin[v] = __int_as_float(0x7fc00000);
                         break;
@@ -883,9 +1137,9 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
             uint32_t t2 = limit;
             if (drawing) {
                 t2 = pend;
-                if (t2 == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+                ticket_drawn(cr, g, t2);
                 if (t2 >= limit) drawing = false;
-                else pend = atomicAdd(cr.ticket, 1u);
+                else pend = draw_ticket(cr);
             }
             s_tk[0] = t2;
         }
@@ -894,7 +1148,7 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         for (int i = 0; i <= SEG_LAG; ++i) tq[i] = tq[i + 1];
         tq[SEG_LAG + 1] = s_tk[0];
     }
-    if (stop && threadIdx.x == 0) atomicOr(cr.err, ERRBIT_TIMEOUT);
+    if (stop && threadIdx.x == 0) give_up(cr);
     Op::at_exit(p, xs, acc);
     if (threadIdx.x == 0)  // after an early stop: boxes still in flight land first
         for (int st = 0; st < ST; ++st)
@@ -913,10 +1167,14 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
 // the epilogue.
 template <class Op, int ST>
 __global__ void __launch_bounds__(Op::NW * 32, 2)
-    k_seg1(typename Op::Params p, Geom g, Carry cr, SegGeom sg,
+    k_seg1(typename Op::Params p, Geom g, const Carry cr0, SegGeom sg,
            const __grid_constant__ TmaDesc td) {
     static_assert(has_next_agg<Op>::value, "a consume-only launch publishes the next aggregates");
-    if (Op::skip(p)) return;  // whole launch: before any ticket or barrier
+    if (Op::skip(p)) {  // whole launch: before any ticket or barrier
+        if (blockIdx.x == 0 && threadIdx.x == 0) retire_epoch(cr0);
+        return;
+    }
+    Carry cr = cr0;
     constexpr int NW = Op::NW, VEC = Op::VEC, L = Op::NW * Op::R;
     constexpr uint32_t SB = tma_stage_bytes<Op>();
     extern __shared__ unsigned char dyn_smem[];
@@ -927,17 +1185,20 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
     __shared__ typename Op::Smem xs;
     __shared__ float carry[2][32][VEC];  // by chunk parity
     __shared__ __align__(8) uint64_t full[ST];
-    __shared__ uint32_t s_tk[2], s_abort;
+    __shared__ uint32_t s_tk[2], s_abort, s_epoch;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t limit = cr.n_walk + sg.n_units;
-    const NextAgg nx = Op::next_agg(p);
+    NextAgg nx = Op::next_agg(p);
     if (threadIdx.x == 0) {
-        const uint32_t t = atomicAdd(cr.ticket, 1u);
-        if (t == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+        const uint32_t t = draw_ticket(cr);
+        ticket_drawn(cr, g, t);
         s_tk[0] = t;
         s_abort = 0;
+        s_epoch = cr.epoch;
     }
     __syncthreads();
+    cr.epoch = s_epoch;
+    nx.epoch = epoch_after(cr.epoch);  // the next launch's
     const uint32_t cur = s_tk[0];
     if (cur < cr.n_walk) {  // walker role: its chunks are the segments
         Geom gw = g;
@@ -975,13 +1236,13 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         for (int i = 0; i < ST; ++i) mbar_init(&full[i], 1);
         mbar_init_fence();
         pol = l2_evict_first();  // every tile is read once
-        const uint32_t t1 = atomicAdd(cr.ticket, 1u);
-        if (t1 == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+        const uint32_t t1 = draw_ticket(cr);
+        ticket_drawn(cr, g, t1);
         if (t1 >= limit) drawing = false;
         s_tk[1] = t1;
         tk_next = t1;
         for (uint32_t u = 0; u < (uint32_t)ST; ++u) issue(u, cur);
-        if (drawing) pend = atomicAdd(cr.ticket, 1u);
+        if (drawing) pend = draw_ticket(cr);
     }
     __syncthreads();
     tk_next = s_tk[1];
@@ -1009,7 +1270,7 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
                                                    cin, cr.epoch);
                     if (__all_sync(0xffffffffu, ok)) break;
                     if (__any_sync(0xffffffffu, wait_step(cr, spins, sleep_ns, kTileMaxSleepNs))) {
-                        if (lane == 0) atomicOr(cr.err, ERRBIT_TIMEOUT);
+                        if (lane == 0) give_up(cr);
 #pragma unroll
                         for (int v = 0; v < VEC; ++v) cin[v] = __int_as_float(0x7fc00000);
                         break;
@@ -1099,9 +1360,9 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
             uint32_t t2 = limit;
             if (drawing) {
                 t2 = pend;
-                if (t2 == g.n_draws - 1) atomicExch(cr.ticket, 0u);
+                ticket_drawn(cr, g, t2);
                 if (t2 >= limit) drawing = false;
-                else pend = atomicAdd(cr.ticket, 1u);
+                else pend = draw_ticket(cr);
             }
             s_tk[0] = t2;
         }
@@ -1109,7 +1370,7 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         tk = tk_next;
         tk_next = s_tk[0];
     }
-    if (stop && threadIdx.x == 0) atomicOr(cr.err, ERRBIT_TIMEOUT);
+    if (stop && threadIdx.x == 0) give_up(cr);
     Op::at_exit(p, xs, acc);
     if (threadIdx.x == 0)  // after an early stop: boxes still in flight land first
         for (int st = 0; st < ST; ++st)
@@ -1220,6 +1481,53 @@ cudaError_t launch_tchain(const typename Op::Params& p, Geom g, const Carry& cr,
     const uint32_t grid = persist_grid(g, cr, o);
     g.n_draws = g.n_tiles + grid - g.ticket_base;
     k_tchain<Op, ST><<<grid, 32 * (Op::NW + 1), dyn, s>>>(p, g, cr, td);
+    return cudaGetLastError();
+}
+
+// Host: launch k_look<Op, 2> (look-back protocol, TMA staging).  Two stages:
+// a tile keeps its stage until its outputs are written (the rows are read
+// twice, before and after the look-back), the other one streams the CTA's
+// next tile in.
+template <class Op>
+cudaError_t launch_look(const typename Op::Params& p, Geom g, const Carry& cr, cudaStream_t s) {
+    constexpr int ST = 2;
+    constexpr int L = Op::NW * Op::R, CW = 32 * Op::VEC;
+    constexpr size_t dyn = (size_t)ST * tma_stage_bytes<Op>() + 128;
+    static_assert(Op::TMA_N <= TMA_MAX_ARR, "too many staged arrays");
+    static_assert(L + 1 <= 256 && CW <= 256, "a TMA box holds at most 256 rows and columns");
+    TmaDesc td;
+    memset(&td, 0, sizeof td);
+    const void* ptr[TMA_MAX_ARR] = {};
+    Op::tma_arrays(p, ptr);
+    for (int a = 0; a < Op::TMA_N; ++a) {
+        if (!ptr[a]) continue;
+        if (!tma_encode(&td.map[a], ptr[a], sizeof(typename Op::S) == 2 ? 1 : 0, g.T, g.C, CW,
+                        L + Op::tma_extra(a)))
+            return cudaErrorInvalidValue;
+        td.present |= 1u << a;
+        td.tx_bytes += tma_arr_bytes<Op>(a);
+    }
+    static int occ[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int& o = occ[dev & 63];
+    if (o <= 0) {
+        cudaError_t e = cudaFuncSetAttribute(k_look<Op, ST>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k_look<Op, ST>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_look<Op, ST>, 32 * (Op::NW + 1),
+                                                          dyn) != cudaSuccess ||
+            n <= 0)
+            n = 1;
+        o = n;
+    }
+    const uint32_t grid = persist_grid(g, cr, o);
+    g.n_draws = g.n_tiles + grid - g.ticket_base;
+    k_look<Op, ST><<<grid, 32 * (Op::NW + 1), dyn, s>>>(p, g, cr, td);
     return cudaGetLastError();
 }
 
@@ -1376,6 +1684,7 @@ cudaError_t launch_persist(const typename OpC::Params& p, const Geom& g, const C
     static_assert(std::is_same<typename OpC::Params, typename OpW::Params>::value &&
                       std::is_same<typename OpC::Params, typename OpT::Params>::value,
                   "all instantiations take the same arguments");
+    if (cr.mode == CARRY_LOOK) return launch_look<OpT>(p, g, cr, s);
     if (cr.mode == CARRY_CHAIN) {
         if (cr.tma) {
             cudaError_t e;

@@ -15,15 +15,17 @@
 //   * every GPU that loads the library holds kScratchBytes (4 MiB) of device
 //     memory until the process exits;
 //   * problems needing more carry packets than fit are rejected with
-//     LR_ERR_TOO_LARGE: one 8-byte state packet per channel per chunk of 64
-//     time steps (three per channel-chunk when the walker protocol is used),
-//     i.e. ~524 K channel-chunks, ~33 M elements in the common case;
+//     LR_ERR_TOO_LARGE: ~524 K 8-byte packets, one per channel per chunk of
+//     time steps (the chain protocol), two (look-back protocol, short
+//     problems) or three (walker protocol, long ones);
 //   * every call shares the one array: two calls whose kernels overlap on the
 //     GPU (different streams, no ordering between them) race on it and give
 //     wrong results.  Order such calls on one stream or with events.
-//   * the array keeps the last call's contents; packets are tagged with a
-//     per-call epoch so old ones are ignored, and the tile ticket is cleared
-//     (a 4-byte memset, not an allocation) before every launch.
+//   * the array keeps the last call's contents.  Packets are tagged with the
+//     launch's epoch, which the kernels take from the array's ticket word on
+//     the device, so packets of earlier calls are ignored; before every
+//     launch one 8-byte memset (not an allocation) clears the internal error
+//     word and the tile counter, and leaves the epoch alone.
 //   * the first call on a device looks up the array's device address with
 //     cudaGetSymbolAddress (host code cannot use the symbol itself); make that
 //     first call before any stream capture.
@@ -40,15 +42,22 @@ namespace {
 using namespace lrs;
 
 constexpr size_t kScratchBytes = size_t(4) << 20;
-constexpr size_t kHeaderBytes = 256;  // [0] ticket, [1] error word
+// Header: bytes 4..7 the internal error word, 8..15 the 64-bit ticket word
+// (bytes 8..11 the tile counter, 12..15 the last retired epoch); packets from
+// byte 256 on.  Bytes 4..11 are cleared before every launch.
+constexpr size_t kHeaderBytes = 256;
+constexpr size_t kErrOff = 4, kTicketOff = 8;
 constexpr uint32_t kSpinLimit = 1u << 21;
 constexpr int kMaxDevices = 64;
+// Launches after which the packets and the epoch are cleared (the device's
+// epochs never wrap into packets of earlier calls).
+constexpr uint64_t kEpochClear = 1ull << 31;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 struct NoAllocDev {
     unsigned char* base = nullptr;  // device address of g_scratch on this device
-    uint32_t epoch = 0;
+    uint64_t launches = 0;          // launches since the last clear
 };
 std::mutex g_na_mu;
 NoAllocDev g_na[kMaxDevices];
@@ -93,14 +102,14 @@ extern "C" int lr_scan_fwd_noalloc(const void* a, const void* b, const void* h0,
         if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return LR_ERR_CUDA;
         nd.base = (unsigned char*)p;
     }
-    uint32_t* words = (uint32_t*)nd.base;
     u64* pk = (u64*)(nd.base + kHeaderBytes);
-    if (++nd.epoch == 0) {  // 32-bit wrap: forget every old packet once
-        nd.epoch = 1;
-        if (cudaMemsetAsync(pk, 0, kScratchBytes - kHeaderBytes, s) != cudaSuccess)
-            return LR_ERR_CUDA;
+    if (++nd.launches >= kEpochClear) {  // forget every old packet; epochs restart at 1
+        nd.launches = 1;
+        if (cudaMemsetAsync(nd.base, 0, kScratchBytes, s) != cudaSuccess) return LR_ERR_CUDA;
     }
-    if (cudaMemsetAsync(words, 0, sizeof(uint32_t), s) != cudaSuccess) return LR_ERR_CUDA;
+    // the internal error word and the tile counter (a launch that gave up
+    // may have left it mid-count); not the epoch
+    if (cudaMemsetAsync(nd.base + kErrOff, 0, 8, s) != cudaSuccess) return LR_ERR_CUDA;
 
     Geom g;
     g.T = T;
@@ -115,9 +124,9 @@ extern "C" int lr_scan_fwd_noalloc(const void* a, const void* b, const void* h0,
     Carry cr;
     cr.inc = pk;
     cr.agg = pk + cp.inc_elems;
-    cr.ticket = words;
-    cr.err = err_dev ? err_dev : words + 1;
-    cr.epoch = nd.epoch;
+    cr.tk = (u64*)(nd.base + kTicketOff);
+    cr.err = err_dev ? err_dev : (uint32_t*)(nd.base + kErrOff);
+    cr.epoch = 0;  // taken on the device from the ticket word
     cr.spin_limit = kSpinLimit;
     cr.mode = cp.mode;
     cr.n_walk = cp.n_walk;
