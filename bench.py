@@ -339,8 +339,9 @@ class Bench:
     def time_deer_variants(self, peak, reps=5):
         """At the DEER workload's size: the ODE form (steps dt ~ U(0.1, 1)), a
         warm-started solve (the guess is the solution for u + 1e-3 sin, a
-        nearby problem, as the previous training step's would be) and the
-        per-sequence stopping test: mean solve time, K, algorithmic GB/s."""
+        nearby problem, as the previous training step's would be), the
+        per-sequence stopping test and bf16 storage: mean solve time, K,
+        algorithmic GB/s."""
         t, L, wl = self.torch, self.lrs, W.DEER
         o = self.d["deer"]
         N, D = wl.N, wl.D
@@ -385,7 +386,24 @@ class Bench:
                                     "frac": round(byt / (ms / 1e3) / 1e9 / peak, 3),
                                     "workload": f"deer fp32 T={wl.T} B={wl.B} D={wl.D}, "
                                                 "one stopping test per sequence"}
-        del dt, y, u2, guess
+        # bf16 storage: the same workload's u rounded to bf16; the iterates
+        # are stored in bf16, so the stopping test is taken at 1e-2 (bf16
+        # rounding of the iterate puts a floor of ~1e-3 under the residual)
+        ub = o["u"].to(t.bfloat16)
+        yb = t.empty_like(ub)
+
+        def bf16():
+            r = L.deer_diag_solve_ex(o["w"], ub, None, yb, eps=1e-2, kmax=KMAX)
+            res["k"], res["st"] = r["iters"], r["status"]
+
+        ms = self._mean_ms(bf16, reps)
+        k = res["k"]
+        byt = (4 + 6 * (k - 1)) * N + 4 * D * k
+        out["deer_bf16.solve"] = {"ms": round(ms, 4), "iters": k, "status": res["st"],
+                                  "GBps": round(byt / (ms / 1e3) / 1e9, 1),
+                                  "frac": round(byt / (ms / 1e3) / 1e9 / peak, 3),
+                                  "workload": f"deer bf16 storage T={wl.T} B={wl.B} D={wl.D}, eps 1e-2"}
+        del dt, y, u2, guess, ub, yb
         return out
 
     def _mean_ms(self, run, reps):

@@ -914,10 +914,10 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
     // of two time chunks and one channel tile, each with one CTA that is handed
     // tile 1: it waits for the state after tile 0, which nobody publishes.
     // Look-back protocol: the same, tile 1 waits for tile 0's aggregate.
-    // Walker protocol: the register and the segmented walker kernels, and the
-    // consume-only segmented kernel, on a long one-strip problem launched
-    // without walker CTAs: no entering state is ever published, so every
-    // consume's wait runs out.
+    // Walker protocol: the register walker kernel (vector and scalar paths),
+    // the segmented walker kernel and its consume-only form, on a long
+    // one-strip problem launched without walker CTAs: no entering state is
+    // ever published, so every consume's wait runs out.
     const int64_t C = tile_shape(OP_SCAN_FWD, LR_F32, true, CARRY_CHAIN).CW;
     const int64_t Tw = 8192;  // >= 128 chunks of both walker tile shapes
     if (!ws->test_buf) {
@@ -954,16 +954,26 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
         CK(launch_scan_fwd(LR_F32, true, a, a + Tw * C, nullptr, (float*)buf + 2 * Tw * C, g, cr,
                            s));
     }
-    for (int dt = 0; dt < 2; ++dt) {  // fp32: register walker; bf16: segmented walker
-        const size_t es = dt ? 2 : 4;
+    for (int vec = 0; vec < 2; ++vec) {  // fp32 forward: register walker, scalar and vector paths
         Geom g;
         Carry cr;
-        TRY(plan(*ws, OP_SCAN_FWD, dt, true, Tw, C, C, &g, &cr, s, 1));
-        if (cr.mode != CARRY_WALK || cr.tma != dt) return LR_ERR_INVALID_ARG;
+        TRY(plan(*ws, OP_SCAN_FWD, LR_F32, vec == 1, Tw, C, C, &g, &cr, s, 0));
+        if (cr.mode != CARRY_WALK || cr.tma) return LR_ERR_INVALID_ARG;
         cr.n_walk = 0;
         cr.spin_limit = spin_limit;
-        CK(launch_scan_fwd(dt, true, buf, buf + Tw * C * es, nullptr, buf + 2 * Tw * C * es, g, cr,
-                           s));
+        CK(launch_scan_fwd(LR_F32, vec == 1, buf, buf + Tw * C * 4, nullptr, buf + 2 * Tw * C * 4, g,
+                           cr, s));
+    }
+    {  // bf16 backward: the segmented walker
+        Geom g;
+        Carry cr;
+        TRY(plan(*ws, OP_SCAN_BWD, LR_BF16, true, Tw, C, C, &g, &cr, s, 1));
+        if (cr.mode != CARRY_WALK || !cr.tma) return LR_ERR_INVALID_ARG;
+        cr.n_walk = 0;
+        cr.spin_limit = spin_limit;
+        const size_t n = (size_t)(Tw * C) * 2;  // bytes of one bf16 array
+        CK(launch_scan_bwd(LR_BF16, true, buf, buf + n, nullptr, buf + 2 * n, buf + 3 * n, buf + 4 * n,
+                           nullptr, g, cr, s));
     }
     {  // the consume-only segmented kernel: a DEER iteration whose aggregates
        // count as published, again without walker CTAs

@@ -29,17 +29,6 @@
 #define LR_STRIP_ONEB 1
 #endif
 
-// Walker-protocol tile of the forward scan (the register walker kernel runs
-// it): warps per CTA and rows per thread.  The kernel keeps 16 warps per SM
-// resident whatever the CTA width (narrower CTAs: more of them per SM, each
-// with its own ticket in flight).
-#ifndef LR_WALK_FWD_NW
-#define LR_WALK_FWD_NW 8
-#endif
-#ifndef LR_WALK_FWD_R
-#define LR_WALK_FWD_R 8
-#endif
-
 // Register cap of the TMA-staged kernel: two CTAs of NW+1 = 9 warps per SM.
 #ifndef LR_TMA_MAXNREG
 #define LR_TMA_MAXNREG 112
@@ -100,7 +89,7 @@ constexpr KCfg kcfg(Op op, int dtype, int mode) {
                   : op == OP_SRU_BWD  ? KCfg{8, dtype == 1 ? 2 : 1, 0}
                   :                     KCfg{8, dtype == 1 ? 4 : 2, 0})
            : mode == CARRY_WALK
-               ? (op == OP_SCAN_FWD ? KCfg{LR_WALK_FWD_NW, LR_WALK_FWD_R, 0}
+               ? (op == OP_SCAN_FWD ? KCfg{8, 8, 0}
                   : op == OP_SCAN_BWD ? KCfg{8, dtype == 1 ? 8 : 4, 0}
                   : op == OP_SRU_FWD  ? KCfg{8, dtype == 1 ? 8 : 4, 0}
                   : op == OP_SRU_BWD  ? KCfg{8, dtype == 1 ? 4 : 2, 0}

@@ -48,6 +48,12 @@
 
 namespace lrs {
 
+// Order generic-proxy shared-memory accesses before later async-proxy (TMA)
+// accesses of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 struct TileCoord {
     int64_t q;       // chunk index in scan order
     int64_t tchunk;  // chunk index in time
@@ -400,6 +406,7 @@ __global__ void __maxnreg__(LR_TMA_MAXNREG)
     Op::at_exit(p, xs, acc);
 }
 
+
 // Look-back kernel (LOOK protocol; short problems whose chunk chain would
 // cost one L2 round trip per chunk level).  The tiles are staged by TMA as in
 // the TMA chain kernel (producer warp, tickets in scan order).  A tile
@@ -489,8 +496,34 @@ __device__ __forceinline__ void look_fold(const Carry& cr, const Geom& g, uint32
     }
 }
 
+// Thread 0 of a look-back CTA: draw the next ticket (tile, or past the end)
+// into s_tile[st] and, for a tile, issue its boxes into stage st.
+template <class Op>
+__device__ __forceinline__ void look_issue(Carry& cr, const Geom& g, const TmaDesc& td,
+                                           unsigned char* ring, uint64_t* full, uint32_t* s_tile,
+                                           uint32_t st) {
+    constexpr int L = Op::NW * Op::R, CW = 32 * Op::VEC;
+    const uint32_t t = draw_ticket(cr);
+    ticket_drawn(cr, g, t);
+    const uint32_t tile = t + g.ticket_base;
+    s_tile[st] = tile;
+    if (tile >= g.n_tiles) return;
+    const int64_t q = tile / g.n_ct, j = tile % g.n_ct;
+    const int64_t tchunk = Op::REV ? g.n_chunks - 1 - q : q;
+    const int32_t x = (int32_t)(j * CW), y0 = (int32_t)(tchunk * L);
+    mbar_arrive_tx(&full[st], td.tx_bytes);
+    unsigned char* dst = ring + st * tma_stage_bytes<Op>();
+#pragma unroll
+    for (int a = 0; a < Op::TMA_N; ++a)
+        if (td.present & (1u << a))
+            tma_load_2d(dst + tma_off<Op>(a), &td.map[a], x, y0 + Op::tma_shift(a), &full[st]);
+}
+
+// No producer warp: thread 0 draws the tickets (in order) and issues each
+// tile's boxes, ST stages ahead, so that two CTAs of NW warps fit an SM and a
+// problem of up to two tiles per SM runs in one wave.
 template <class Op, int ST>
-__global__ void __maxnreg__(LR_TMA_MAXNREG)
+__global__ void __launch_bounds__(Op::NW * 32, 2)
     k_look(typename Op::Params p, Geom g, const Carry cr0, const __grid_constant__ TmaDesc td) {
     if (Op::skip(p)) {  // whole launch: before any ticket or barrier
         if (blockIdx.x == 0 && threadIdx.x == 0) retire_epoch(cr0);
@@ -505,36 +538,36 @@ __global__ void __maxnreg__(LR_TMA_MAXNREG)
     // of its share of the preceding chunks
     __shared__ StripSmem<VEC, NW> sm;
     __shared__ typename Op::Smem xs;
-    __shared__ __align__(8) uint64_t full[ST], empty[ST];
+    __shared__ __align__(8) uint64_t full[ST];
     __shared__ uint32_t s_tile[ST];
     __shared__ uint32_t s_abort, s_epoch;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     Carry cr = cr0;
+    bool drawing = true;  // thread 0: no ticket past the end drawn yet
+    uint32_t issued = 0;  // thread 0: stage uses whose ticket was drawn
     if (threadIdx.x == 0) {
-        for (int i = 0; i < ST; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], NW);
-        }
+        for (int i = 0; i < ST; ++i) mbar_init(&full[i], 1);
         s_abort = 0;
         mbar_init_fence();
+        for (; issued < (uint32_t)ST && drawing; ++issued) {
+            look_issue<Op>(cr, g, td, ring, full, s_tile, issued);
+            if (s_tile[issued] >= g.n_tiles) drawing = false;
+        }
+        for (uint32_t i = issued; i < (uint32_t)ST; ++i) s_tile[i] = 0xffffffffu;
+        s_epoch = cr.epoch;
     }
     __syncthreads();
-    if (warp == NW) {
-        if (lane == 0) tma_produce<Op, ST>(g, cr, td, ring, full, empty, s_tile, &s_epoch);
-        return;
-    }
+    cr.epoch = s_epoch;
     typename Op::Acc acc;
     Op::acc_init(acc);
-    for (uint32_t k = 0;; ++k) {
+    uint32_t k = 0;
+    for (;; ++k) {
         const uint32_t st = k % ST;
-        if (!mbar_wait(&full[st], (k / ST) & 1u, cr.err)) {
-            s_abort = 1;
-            atomicOr(cr.err, ERRBIT_TIMEOUT);
-        }
-        csync<NW>();  // uniform stop decision; the previous tile is done with sm
-        cr.epoch = s_epoch;
         const uint32_t tile = s_tile[st];
-        if (s_abort != 0 || tile >= g.n_tiles) break;
+        if (tile >= g.n_tiles) break;  // uniform: s_tile is written before a barrier
+        if (!mbar_wait(&full[st], (k / ST) & 1u, cr.err)) s_abort = 1;
+        csync<NW>();  // uniform stop decision
+        if (s_abort != 0) break;
         const TileCoord tc = tile_coord<Op>(g, tile);
         const SmemSrc<Op> src{ring + st * SB, tc.tchunk * L, lane * VEC};
         float A[VEC], B[VEC];
@@ -614,12 +647,28 @@ __global__ void __maxnreg__(LR_TMA_MAXNREG)
             float A2[VEC], B2[VEC];
             Op::load(src, p, g, tc, regs);
             Op::aggregate(p, g, tc, regs, w, A2, B2, true);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
             Op::finish(p, g, tc, regs, w, s, xs, acc);
         }
+        // every warp has read the stage and sm: thread 0 refills the stage
+        // with the tile ST uses ahead (the next loop top reads s_tile after
+        // this barrier)
+        csync<NW>();
+        if (threadIdx.x == 0) {
+            if (drawing) {
+                fence_proxy_async_smem();  // the generic reads of the stage before the async refill
+                look_issue<Op>(cr, g, td, ring, full, s_tile, st);
+                if (s_tile[st] >= g.n_tiles) drawing = false;
+                ++issued;
+            } else {
+                s_tile[st] = 0xffffffffu;
+            }
+        }
+        csync<NW>();
     }
     Op::at_exit(p, xs, acc);
+    if (threadIdx.x == 0)  // after an early stop: copies still in flight land first
+        for (uint32_t i = k; i < issued; ++i)
+            if (s_tile[i % ST] < g.n_tiles) mbar_wait(&full[i % ST], (i / ST) & 1u, cr.err);
 }
 
 // The op's scratch in the TMA strip and segmented kernels: its own space, or
@@ -853,9 +902,6 @@ struct NextPart {
     float a[NW][32][VEC];
     float b[NW][32][VEC];
 };
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 template <class Op, int ST>
 __global__ void __launch_bounds__(Op::NW * 32, 2)
@@ -1519,15 +1565,15 @@ cudaError_t launch_look(const typename Op::Params& p, Geom g, const Carry& cr, c
                                  (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_look<Op, ST>, 32 * (Op::NW + 1),
-                                                          dyn) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_look<Op, ST>, 32 * Op::NW, dyn) !=
+                cudaSuccess ||
             n <= 0)
             n = 1;
         o = n;
     }
     const uint32_t grid = persist_grid(g, cr, o);
     g.n_draws = g.n_tiles + grid - g.ticket_base;
-    k_look<Op, ST><<<grid, 32 * (Op::NW + 1), dyn, s>>>(p, g, cr, td);
+    k_look<Op, ST><<<grid, 32 * Op::NW, dyn, s>>>(p, g, cr, td);
     return cudaGetLastError();
 }
 
