@@ -212,8 +212,13 @@ int deer_diag_solve(const float* w, const void* u, const void* h0, void* y,
  *   seq_iters    : host int[B] out (may be NULL): K_b (K for every b when
  *                  per_sequence = 0)
  *   seq_resid    : host float[B] out (may be NULL): each sequence's residual at K_b
- *   launched_out : host int out (may be NULL): iteration kernels enqueued,
- *                  including those that returned at once after the solve stopped
+ *   launched_out : host int out (may be NULL): the kernels the solve enqueued --
+ *                  the iterations, including those that returned at once after
+ *                  the solve stopped, and for long, narrow problems the pass that
+ *                  publishes iteration 1's segment aggregates before it and the
+ *                  one-thread kernel that closes the solve (per_sequence: also
+ *                  the stop-state update after every iteration and the final
+ *                  gather)
  * Status as deer_diag_solve: LR_ERR_NONFINITE if any sequence's residual was not
  * finite, else LR_ERR_NOT_CONVERGED if any sequence reached kmax without eps.
  */

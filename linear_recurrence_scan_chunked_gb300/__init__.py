@@ -287,7 +287,7 @@ def deer_diag_solve_ex(w, u, h0=None, y=None, y_init=None, eps=1e-5, kmax=20,
     """DEER solve from an initial guess (None = zeros; it may be y itself) with
     one stopping test for the batch or one per sequence.  Returns a dict: y,
     iters (largest K), resid, hist (per iteration), status, seq_iters[B],
-    seq_resid[B], launches (iteration kernels enqueued)."""
+    seq_resid[B], launches (kernels the solve enqueued)."""
     _seq("u", u)
     T, B, D = u.shape
     _param("w", w, D, u)

@@ -501,8 +501,9 @@ static float bits_f(uint32_t b) {
 // One-pass iterations (operations with next-launch aggregates on the
 // segmented walker kernel): every launch also publishes the next one's
 // segment aggregates, with the next launch's epoch, into the second of two
-// aggregate buffers after the packets plan() lays out; from the second
-// iteration on a launch has no reduce pass.  onepass_begin sizes the packets
+// aggregate buffers after the packets plan() lays out, and a reduce-only pass
+// before the first iteration publishes that one's: no iteration has a reduce
+// pass.  onepass_begin sizes the packets
 // and keeps the packet epochs from being cleared inside the solve;
 // onepass_args points launch kk at its two buffers; the solve's Retire
 // retires, on the device, the epoch that its last launch tagged the
@@ -546,11 +547,14 @@ static void deer_remember(DevWS& ws, int form, int64_t T, int64_t C, int dtype, 
     ws.deer_last[form] = DevWS::DeerLast{T, C, dtype, K};
 }
 
+// Launch kk >= 1 reads its aggregates from one buffer and publishes the next
+// launch's into the other; launch 0 is the reduce-only pass, which publishes
+// launch 1's.
 static NextAgg onepass_args(DevWS& ws, const CarryPlan& cp, int kk, Carry& cr) {
     u64* agg0 = ws.pk + cp.inc_elems;  // where plan() put cr.agg
     cr.agg = (kk & 1) ? agg0 : agg0 + cp.agg_elems;
     return NextAgg{(kk & 1) ? agg0 + cp.agg_elems : agg0, 0u /* the next launch's: on the device */,
-                   kk > 1 ? 1u : 0u};
+                   kk >= 1 ? 1u : 0u, kk == 0 ? 1u : 0u};
 }
 
 int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void* y_init, void* y,
@@ -628,7 +632,17 @@ int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void
     int k = 0, status = LR_ERR_NOT_CONVERGED;
     float rho = 0.f;
     int launched = 0;
+    int kernels = 0;  // every kernel the solve enqueues
     bool done = false;
+    if (onepass) {  // iteration 1's segment aggregates, from the initial guess
+        Geom g;
+        Carry cr;
+        TRY(plan(*ws, OP_DEER, dtype, vec, T, B * D, D, &g, &cr, s));
+        const NextAgg nx = onepass_args(*ws, cp, 0, cr);
+        CK(launch_deer_iter(dtype, vec, w, u, h0, y0, tgt(1), slots, nullptr, eps, nx,
+                            DeerSeq{nullptr, nullptr, nullptr}, g, cr, s));
+        ++kernels;
+    }
     while (!done && launched < kmax) {
         const int first = launched;
         const int want = first == 0 && kp > 0 ? kp : kDeerBatch;
@@ -638,16 +652,19 @@ int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void
             Geom g;
             Carry cr;
             TRY(plan(*ws, OP_DEER, dtype, vec, T, B * D, D, &g, &cr, s));
-            const NextAgg nx = onepass ? onepass_args(*ws, cp, kk, cr) : NextAgg{nullptr, 0u, 0u};
+            const NextAgg nx = onepass ? onepass_args(*ws, cp, kk, cr) : NextAgg{nullptr, 0u, 0u, 0u};
             DeerSeq sq{nullptr, nullptr, nullptr};
             if (per_sequence) sq = DeerSeq{sq_slots + (size_t)(kk - 1) * B, sq_done, sq_all};
             CK(launch_deer_iter(dtype, vec, w, u, h0, kk == 1 ? y0 : tgt(kk - 1), tgt(kk),
                                 slots + (kk - 1),
                                 kk == 1 || per_sequence ? nullptr : slots + (kk - 2), eps, nx, sq, g,
                                 cr, s));
-            if (per_sequence)
+            ++kernels;
+            if (per_sequence) {
                 CK(launch_deer_seq_update(sq_slots + (size_t)(kk - 1) * B, sq_done, sq_iters, sq_all,
                                           B, eps, kk, s));
+                ++kernels;
+            }
         }
         if (!per_sequence) {
             CK(cudaMemcpyAsync(ws->host_word + first, slots + first, sizeof(uint32_t) * nb,
@@ -674,8 +691,8 @@ int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void
             done = hs[(size_t)kmax * B] != 0;
         }
     }
+    if (onepass) ++kernels;  // the epoch retire below
     TRY(rt.done());
-    if (launched_out) *launched_out = launched;
     if (!per_sequence) {
         if (k > kmax) k = kmax;
         if (tgt(k) != y) CK(cudaMemcpyAsync(y, ws->ybuf, nbytes, cudaMemcpyDeviceToDevice, s));
@@ -689,6 +706,7 @@ int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void
     } else {
         // every sequence's last iterate into y; counts and final residuals
         CK(launch_deer_seq_gather(ws->ybuf, y, sq_iters, launched, T, B * D, D, dtype, s));
+        ++kernels;
         int32_t* hi = reinterpret_cast<int32_t*>(ws->seq_host + (size_t)kmax * B + 1);
         CK(cudaMemcpyAsync(hi, sq_iters, sizeof(int32_t) * (size_t)B, cudaMemcpyDeviceToHost, s));
         CK(cudaStreamSynchronize(s));
@@ -709,6 +727,7 @@ int deer_diag_solve_ex(const float* w, const void* u, const void* h0, const void
         *iters_out = kmx;
         if (resid_out) *resid_out = rmx;
     }
+    if (launched_out) *launched_out = kernels;
     TRY(lv.done());
     return status;
 }
@@ -765,6 +784,14 @@ int deer_ode_solve(const float* w, const void* u, const float* dt, const void* h
     float rho = 0.f;
     int launched = 0;
     bool done = false;
+    if (onepass) {  // iteration 1's segment aggregates, from the zero guess
+        Geom g;
+        Carry cr;
+        TRY(plan(*ws, OP_DEER_ODE, dtype, vec, T, B * D, D, &g, &cr, s));
+        const NextAgg nx = onepass_args(*ws, cp, 0, cr);
+        CK(launch_deer_ode_iter(dtype, vec, w, u, dt, h0, nullptr, tgt(1), slots, nullptr, eps,
+                                ws->clamps, nx, g, cr, s));
+    }
     while (!done && launched < kmax) {
         const int first = launched;
         const int want = first == 0 && kp > 0 ? kp : kDeerBatch;
@@ -774,7 +801,7 @@ int deer_ode_solve(const float* w, const void* u, const float* dt, const void* h
             Geom g;
             Carry cr;
             TRY(plan(*ws, OP_DEER_ODE, dtype, vec, T, B * D, D, &g, &cr, s));
-            const NextAgg nx = onepass ? onepass_args(*ws, cp, kk, cr) : NextAgg{nullptr, 0u, 0u};
+            const NextAgg nx = onepass ? onepass_args(*ws, cp, kk, cr) : NextAgg{nullptr, 0u, 0u, 0u};
             CK(launch_deer_ode_iter(dtype, vec, w, u, dt, h0, kk == 1 ? nullptr : tgt(kk - 1), tgt(kk),
                                     slots + (kk - 1),
                                     kk == 1 ? nullptr : slots + (kk - 2), eps,
@@ -984,7 +1011,7 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
         cr.n_walk = 0;
         cr.spin_limit = spin_limit;
         const float* z = (const float*)buf;  // zeros: w, u and the previous iterate
-        const NextAgg nx{cr.agg, 0u, 1u};
+        const NextAgg nx{cr.agg, 0u, 1u, 0u};
         CK(launch_deer_iter(LR_F32, true, z, z, nullptr, z + Tw * C, (float*)buf + 2 * Tw * C,
                             ws->words + kWordSlots, nullptr, 0.f, nx, DeerSeq{nullptr, nullptr, nullptr}, g,
                             cr, s));

@@ -99,9 +99,11 @@ struct Carry {
 // builds its coefficients from this launch's outputs (segmented walker
 // kernel only).
 struct NextAgg {
-    u64* agg;        // [C][n_seg][2] (A, B) packets of the next launch; nullptr: none
-    uint32_t epoch;  // the next launch's epoch
-    uint32_t pre;    // this launch's aggregates were published by the previous launch
+    u64* agg;              // [C][n_seg][2] (A, B) packets of the next launch; nullptr: none
+    uint32_t epoch;        // the next launch's epoch (set on the device)
+    uint32_t pre;          // this launch's aggregates were published by the previous launch
+    uint32_t reduce_only;  // this launch only publishes the next launch's aggregates (from its
+                           // own coefficients: the pass before a solve's first iteration)
 };
 // Op::NEXT_AGG (optional, default false): the operation computes the next
 // launch's per-thread aggregate in finish() (Work::NA, Work::NB) and exposes

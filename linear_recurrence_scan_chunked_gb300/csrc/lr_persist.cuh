@@ -850,6 +850,10 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
 //      tickets) fold from the segment aggregates, then the state is carried
 //      from chunk to chunk in shared memory, as in the strip kernel, and the
 //      outputs are written.
+// A reduce-only launch (NextAgg::reduce_only) has no walkers and no consume
+// pass: its reduce pass publishes the segment aggregates into NextAgg::agg
+// with the next launch's epoch -- the aggregates of a DEER solve's first
+// iteration, which then runs consume-only like the later ones.
 // The lag of SEG_LAG segments gives the walkers that many segments' time to
 // produce every entering state, while SEG_LAG + 1 short segments per CTA stay
 // within the L2.  Tickets, aggregate packets, walker work and the carry wait
@@ -925,14 +929,17 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
     __shared__ __align__(8) uint64_t full[ST];
     __shared__ uint32_t s_tk[2], s_abort, s_epoch;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t limit = cr.n_walk + sg.n_units;
-    NextAgg nx{nullptr, 0u, 0u};
+    NextAgg nx{nullptr, 0u, 0u, 0u};
     if constexpr (NXT) nx = Op::next_agg(p);
     const bool pre = nx.pre != 0;
+    const bool ronly = NXT && nx.reduce_only != 0;
+    if (ronly) cr.n_walk = 0;  // no walkers: nothing is consumed
+    const uint32_t limit = cr.n_walk + sg.n_units;
     static_assert(!NXT || sizeof(NextPart<VEC, NW>) <= SB, "partials must fit in a stage");
     // uses per iteration: the reduce pass (none when pre), the consume pass
+    // (none when reduce-only)
     const uint32_t nred = pre ? 0u : sg.seg;
-    const uint32_t uses = nred + sg.seg;
+    const uint32_t uses = nred + (ronly ? 0u : sg.seg);
     if (threadIdx.x == 0) {
         const uint32_t t = draw_ticket(cr);
         ticket_drawn(cr, g, t);
@@ -1046,7 +1053,7 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
     auto active = [&]() {
         bool a = tq[SEG_LAG] < limit;
 #pragma unroll
-        for (int i = 0; i < SEG_LAG; ++i) a = a || (!pre && tq[i] < limit);
+        for (int i = 0; i < SEG_LAG; ++i) a = a || (!pre && !ronly && tq[i] < limit);
         return a;
     };
     while (active() && !stop) {
@@ -1087,17 +1094,18 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
             }
         }
         if (stop) break;
-        if (warp == 0 && has_red) {  // the segment's aggregate, for the walkers
+        if (warp == 0 && has_red) {  // the segment's aggregate, for the walkers (or the next launch's)
             const TileCoord tc = tile_coord_qj<Op>(g, seg_r * sg.seg, j_r);
+            u64* dst = ronly ? nx.agg : cr.agg;
+            const uint32_t ep = ronly ? nx.epoch : cr.epoch;
             if (tc.cok && seg_r + 1 < sg.n_seg) {
 #pragma unroll
                 for (int v = 0; v < VEC; ++v)
-                    st_pkt2(cr.agg + 2 * ((tc.c + v) * sg.n_seg + seg_r), pkt(SA[v], cr.epoch),
-                            pkt(SBv[v], cr.epoch));
+                    st_pkt2(dst + 2 * ((tc.c + v) * sg.n_seg + seg_r), pkt(SA[v], ep), pkt(SBv[v], ep));
             }
         }
         // ---- pass 2: the outputs of the segment of `tk_con`
-        const bool has_con = tk_con < limit;
+        const bool has_con = !ronly && tk_con < limit;
         const uint32_t xc = has_con ? tk_con - cr.n_walk : 0u;
         const uint32_t seg_c = xc / (uint32_t)g.n_ct, j_c = xc - seg_c * (uint32_t)g.n_ct;
         if (warp == 0 && has_con) {  // the state entering that segment
@@ -1128,7 +1136,7 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
         }
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { NA[v] = 1.f; NB[v] = 0.f; }
-        for (uint32_t c = 0; c < sg.seg; ++c, ++it) {
+        for (uint32_t c = 0; c < (ronly ? 0u : sg.seg); ++c, ++it) {
             const uint32_t q = seg_c * sg.seg + c;
             const bool valid = has_con && q < (uint32_t)g.n_chunks;
             if (!top(valid)) { stop = true; break; }

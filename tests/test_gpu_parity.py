@@ -267,7 +267,7 @@ def test_deer_repeat_uses_the_last_count(cuda, shape):
     iterations before its first read-back and writes iterate K straight into
     y.  Solves that stop later (eps 1e-5 after 1e-2) or earlier (1e-2 after
     1e-5) than the remembered count match the oracle; a repeat takes exactly
-    K launches and gives the same bits."""
+    K iteration launches and gives the same bits."""
     inp, dv, f = _deer_case(shape, 14)
 
     def solve_and_check(eps):
@@ -282,7 +282,10 @@ def test_deer_repeat_uses_the_last_count(cuda, shape):
     assert long_["iters"] > short["iters"]
     y1 = long_["y"].clone()
     again = cuda.deer_diag_solve_ex(dv["w"], dv["u"], dv["h0"], eps=1e-5, kmax=20)
-    assert again["iters"] == long_["iters"] == again["launches"]
+    # the long, narrow shape adds two kernels to its K iterations: the pass that
+    # publishes iteration 1's segment aggregates and the one closing the solve
+    extra = 2 if shape == (9000, 2, 512) else 0
+    assert again["iters"] == long_["iters"] == again["launches"] - extra
     assert torch.equal(again["y"], y1)
     solve_and_check(1e-2)  # earlier than remembered
 
