@@ -52,11 +52,11 @@ EPS, KMAX = 1e-5, 20
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture, keyed by operation; valid only while the kernel's sources (the
 # shared device headers and its own kernel file) hash to `src`.  Filled from
-# the committed ncu summaries under profiles/.  deer.solve: DRAM bytes read +
-# written per launch, averaged over the K = 6 launches of a solve (first
-# iteration + 5 x second iteration, both captured at full size,
-# profiles/dram_traffic.md).
-NCU_TRAFFIC = {"deer.solve": {"bytes": 753228544, "src": "67b92c8d6ee481ff",
+# the committed ncu summaries under profiles/.  deer.solve: the DRAM bytes read
+# and written by a K = 6 solve -- the reduce-only pass, iteration 1 and five
+# later iterations, captured at full size (profiles/dram_traffic.md) -- over
+# its K iteration launches.
+NCU_TRAFFIC = {"deer.solve": {"bytes": 763311146, "src": "1a59a87e4feba3db",
                               "file": "deer_kernels.cu"}}
 
 
