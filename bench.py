@@ -56,7 +56,7 @@ EPS, KMAX = 1e-5, 20
 # and written by a K = 6 solve -- the reduce-only pass, iteration 1 and five
 # later iterations, captured at full size (profiles/dram_traffic.md) -- over
 # its K iteration launches.
-NCU_TRAFFIC = {"deer.solve": {"bytes": 763311146, "src": "1a59a87e4feba3db",
+NCU_TRAFFIC = {"deer.solve": {"bytes": 760960171, "src": "78c47023f9de522b",
                               "file": "deer_kernels.cu"}}
 
 
@@ -795,7 +795,7 @@ def run_reference(args, ws, rank):
 #          (as `deer`), then k_seg (backward) and 2 dw kernels
 #   tiny   scan_tiny fp32 4x1024x256 (full size; 12.6 MB, L2-resident after the
 #          first launch): fwd, bwd, fwd, bwd
-PROFILE_CASES = ("deer", "large", "long", "sru", "lstm", "deerbwd", "tiny")
+PROFILE_CASES = ("deer", "large", "long", "longfull", "sru", "lstm", "deerbwd", "tiny")
 
 
 def profile_case(name):
@@ -828,8 +828,9 @@ def profile_case(name):
         a, b, g = dev(inp, "a"), dev(inp, "b"), dev(inp, "g")
         for _ in range(2):
             L.lr_scan_bwd(a, L.lr_scan_fwd(a, b, None), g, None)
-    elif name == "long":
-        inp = W.make_inputs(dataclasses.replace(W.SCAN_LONG, T=1 << 18), 0)
+    elif name in ("long", "longfull"):
+        wl = W.SCAN_LONG if name == "longfull" else dataclasses.replace(W.SCAN_LONG, T=1 << 18)
+        inp = W.make_inputs(wl, 0)
         L.lr_scan_fwd(dev(inp, "a"), dev(inp, "b"), dev(inp, "h0"))
     elif name == "sru":
         inp = W.make_inputs(dataclasses.replace(W.SRU, T=512), 0)

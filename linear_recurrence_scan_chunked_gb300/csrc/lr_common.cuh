@@ -123,6 +123,14 @@ template <class Op>
 struct strip_one_barrier<Op, std::void_t<decltype(Op::STRIP_ONE_BARRIER)>>
     : std::integral_constant<bool, Op::STRIP_ONE_BARRIER> {};
 
+// Op::STREAM_WS: the walker protocol's streaming launches take the
+// warp-specialised TMA kernel (k_wstream) where it applies.
+template <class Op, class = void>
+struct stream_ws : std::false_type {};
+template <class Op>
+struct stream_ws<Op, std::void_t<decltype(Op::STREAM_WS)>>
+    : std::integral_constant<bool, Op::STREAM_WS> {};
+
 struct Geom {
     int64_t T;            // rows
     int64_t C;            // channels (B*D)
@@ -245,13 +253,30 @@ __device__ __forceinline__ uint32_t ld_hint_u16(const void* p, uint64_t pol) {
     asm volatile("ld.global.nc.L2::cache_hint.u16 %0, [%1], %2;" : "=h"(r) : "l"(p), "l"(pol));
     return (uint32_t)r;
 }
+// Output stores are streaming (.cs: evict-first in L2): outputs are not
+// read back by the launch that writes them, and tiles parked in L2 for a
+// second read (walker-protocol kernels) or the next iterate's inputs keep
+// their lines.  0: plain stores.
+#ifndef LR_ST_CS
+#define LR_ST_CS 1
+#endif
 __device__ __forceinline__ void st_u2(void* p, uint2 v) {
+#if LR_ST_CS
+    asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+#else
     asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+#endif
 }
 __device__ __forceinline__ void st_u4(void* p, uint4 v) {
+#if LR_ST_CS
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+#else
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)
                  : "memory");
+#endif
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -431,6 +456,11 @@ __device__ __forceinline__ void st_pkt(u64* p, u64 a) {
 __device__ __forceinline__ void ld_pkt2_cg(const u64* p, u64& a, u64& b) {
     asm volatile("ld.global.cg.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
+__device__ __forceinline__ u64 ld_pkt_cg(const u64* p) {
+    u64 a;
+    asm volatile("ld.global.cg.u64 %0, [%1];" : "=l"(a) : "l"(p) : "memory");
+    return a;
+}
 __device__ __forceinline__ void st_pkt_cg(u64* p, u64 a) {
     asm volatile("st.global.cg.u64 [%0], %1;" ::"l"(p), "l"(a) : "memory");
 }
@@ -484,8 +514,9 @@ __device__ __forceinline__ bool get_states_strided(const u64* p, int64_t stride,
 }
 
 // Bounded wait helper: returns true when the caller should give up.  Sleeps
-// grow to max_sleep_ns between polls (0: pure spin -- the walker, which is on
-// every tile's critical path, must notice new aggregates at once).
+// grow to max_sleep_ns between polls (0: pure spin -- a walker with an SM of its
+// own, which is on every tile's critical path, must notice new aggregates at
+// once).
 __device__ __forceinline__ bool wait_step(const Carry& cr, uint32_t& spins, uint32_t& sleep_ns,
                                           uint32_t max_sleep_ns) {
     ++spins;
@@ -542,7 +573,7 @@ template <int MV>
 __device__ __forceinline__ void walk_window(const Carry& cr, const Geom& g, int64_t c0,
                                             const bool (&chan)[MV], int wv, int64_t w0, int n_win,
                                             u64 (&pk)[WALK_P][MV][2], float (&s_in)[MV],
-                                            bool& dead) {
+                                            bool& dead, uint32_t max_sleep) {
     constexpr int P = WALK_P;
     const int lane = threadIdx.x & 31;
     const int64_t q0 = w0 + (int64_t)lane * P;  // this lane's first chunk
@@ -634,7 +665,7 @@ __device__ __forceinline__ void walk_window(const Carry& cr, const Geom& g, int6
             for (int v = 0; v < MV; ++v) s_in[v] = __shfl_sync(0xffffffffu, s_end[v], owner);
             return;
         }
-        if (__any_sync(0xffffffffu, wait_step(cr, spins, sleep_ns, 0))) {
+        if (__any_sync(0xffffffffu, wait_step(cr, spins, sleep_ns, max_sleep))) {
             if (lane == 0) give_up(cr);
             dead = true;  // publish NaN for the rest so no tile keeps waiting
             continue;
@@ -648,11 +679,13 @@ __device__ __forceinline__ void walk_window(const Carry& cr, const Geom& g, int6
     }
 }
 
-template <typename S, int NW, int MV>
-__device__ void walker_mv(const Carry& cr, const Geom& g, uint32_t wid, const S* __restrict__ init) {
+// Walker warp gw: channels [gw*wv, gw*wv + wv).
+template <typename S, int MV>
+__device__ void walker_mv(const Carry& cr, const Geom& g, int64_t gw, const S* __restrict__ init,
+                          uint32_t max_sleep) {
     constexpr int P = WALK_P, WIN = 32 * WALK_P;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t c0 = ((int64_t)wid * NW + warp) * cr.wv;
+    const int lane = threadIdx.x & 31;
+    const int64_t c0 = gw * cr.wv;
     const int64_t last = g.n_chunks - 1;  // states are needed for chunks 0 .. last-1
     if (c0 >= g.C || last <= 0) return;
     const int wv = cr.wv;
@@ -682,25 +715,31 @@ __device__ void walker_mv(const Carry& cr, const Geom& g, uint32_t wid, const S*
         for (int64_t w0 = 0; w0 < last; w0 += 2 * WIN) {
             const int64_t w1 = w0 + WIN;
             if (w1 < last) walk_load<MV>(cr, g, c0, chan, w1 + (int64_t)lane * P, lane_n(n_of(w1)), pb);
-            walk_window<MV>(cr, g, c0, chan, wv, w0, n_of(w0), pa, s_in, dead);
+            walk_window<MV>(cr, g, c0, chan, wv, w0, n_of(w0), pa, s_in, dead, max_sleep);
             if (w1 >= last) break;
             const int64_t w2 = w1 + WIN;
             if (w2 < last) walk_load<MV>(cr, g, c0, chan, w2 + (int64_t)lane * P, lane_n(n_of(w2)), pa);
-            walk_window<MV>(cr, g, c0, chan, wv, w1, n_of(w1), pb, s_in, dead);
+            walk_window<MV>(cr, g, c0, chan, wv, w1, n_of(w1), pb, s_in, dead, max_sleep);
         }
     } else {
         u64 pk[P][MV][2];
         for (int64_t w0 = 0; w0 < last; w0 += WIN) {
             walk_load<MV>(cr, g, c0, chan, w0 + (int64_t)lane * P, lane_n(n_of(w0)), pk);
-            walk_window<MV>(cr, g, c0, chan, wv, w0, n_of(w0), pk, s_in, dead);
+            walk_window<MV>(cr, g, c0, chan, wv, w0, n_of(w0), pk, s_in, dead, max_sleep);
         }
     }
 }
 
+template <typename S>
+__device__ void walker_warp(const Carry& cr, const Geom& g, int64_t gw, const S* __restrict__ init,
+                            uint32_t max_sleep = 0) {
+    if (cr.wv == 1) walker_mv<S, 1>(cr, g, gw, init, max_sleep);
+    else walker_mv<S, WALK_MAX_WV>(cr, g, gw, init, max_sleep);
+}
+// Warp w of walker CTA wid is walker warp wid*NW + w.
 template <typename S, int NW>
 __device__ void walker(const Carry& cr, const Geom& g, uint32_t wid, const S* __restrict__ init) {
-    if (cr.wv == 1) walker_mv<S, NW, 1>(cr, g, wid, init);
-    else walker_mv<S, NW, WALK_MAX_WV>(cr, g, wid, init);
+    walker_warp<S>(cr, g, (int64_t)wid * NW + (threadIdx.x >> 5), init);
 }
 
 // -------------------------------------------------------------- the tile

@@ -17,6 +17,11 @@
 #ifndef LR_STREAM_L2MB
 #define LR_STREAM_L2MB 32
 #endif
+// The fp32 / bf16 forward scan's walker-protocol launches take the
+// warp-specialised TMA kernel where it applies (0: the register kernel).
+#ifndef LR_STREAM_WS
+#define LR_STREAM_WS 1
+#endif
 // L2 budget (MB) of the segmented walker kernel: segments read twice.
 #ifndef LR_SEG_L2MB
 #define LR_SEG_L2MB 160
@@ -217,7 +222,7 @@ inline CarryPlan carry_plan(Op op, int dtype, bool vec, bool tma, int64_t T, int
 
 // Grid of a persistent launch: every walker plus as many tile CTAs as can be
 // resident at once (never more than there are tiles).
-inline uint32_t persist_grid(const Geom& g, const Carry& cr, int occ_per_sm) {
+inline int sm_count() {
     static int sms[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -226,6 +231,10 @@ inline uint32_t persist_grid(const Geom& g, const Carry& cr, int occ_per_sm) {
         cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
         if (n_sm <= 0) n_sm = 1;
     }
+    return n_sm;
+}
+inline uint32_t persist_grid(const Geom& g, const Carry& cr, int occ_per_sm) {
+    const int n_sm = sm_count();
     const uint64_t want = (uint64_t)cr.n_walk + g.n_tiles;
     uint64_t cap = (uint64_t)occ_per_sm * (uint64_t)n_sm;
     if (cap < (uint64_t)cr.n_walk + 1) cap = (uint64_t)cr.n_walk + 1;

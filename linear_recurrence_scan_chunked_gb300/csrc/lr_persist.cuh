@@ -8,6 +8,8 @@
 //             folds those of the chunks before it -- one round trip, not one
 //             per chunk level; TMA-staged),
 //   k_tchain (chain protocol, TMA-staged, for what is none of these),
+//   k_wstream (walker protocol, warp-specialised: TMA-staged reduce and
+//             consume rings, the forward scan's long, narrow problems),
 //   k_stream (walker protocol through registers),
 //   k_chain  (chain protocol through registers: scalar / unaligned paths),
 // and launch_persist, which picks one for a call.
@@ -69,11 +71,14 @@ struct TileCoord {
     bool acc_flush;
 };
 
-// Coordinates of the tile of chunk q (scan order) and channel tile j.
+// Coordinates of the tile of chunk q (scan order) and channel tile j, for the
+// rows of warp `warp` of the tile (by default the calling warp).
 template <class Op>
-__device__ __forceinline__ TileCoord tile_coord_qj(const Geom& g, uint32_t q, uint32_t j) {
+__device__ __forceinline__ TileCoord tile_coord_qj(const Geom& g, uint32_t q, uint32_t j,
+                                                   int warp = -1) {
     constexpr int L = Op::NW * Op::R, CW = 32 * Op::VEC;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31;
+    if (warp < 0) warp = threadIdx.x >> 5;
     TileCoord tc;
     tc.q = q;
     tc.c = (int64_t)j * CW + lane * Op::VEC;
@@ -193,6 +198,472 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
         tk = s_ticket;
     }
     if (tile_role) Op::at_exit(p, xs, acc);
+}
+
+// Warp-specialised streaming kernel of the walker protocol (TMA staging).
+// One CTA per SM; its warps take fixed roles and never wait for each other
+// except through the rings between them:
+//   * the reduce producer (one thread) draws the tickets.  Ticket X >= n_walk
+//     stages tile X - n_walk into the reduce ring and queues tile
+//     X - n_walk - d_con for consumption;
+//   * NRW reducer warps fold a staged tile into its aggregate and publish it
+//     for the walkers -- they wait for nothing but their data, so a tile's
+//     aggregate follows its ticket by one HBM round trip, whatever the
+//     consumers are waiting for;
+//   * the consume producer (one thread) stages the queued tiles into the
+//     consume ring (a re-read, normally from L2);
+//   * NW consumer warps copy a staged tile into registers, hand the stage
+//     back, take the state entering the tile from the walkers and write the
+//     outputs;
+//   * the walker warp is one of the protocol's walkers when the CTA's first
+//     ticket is below n_walk (walker warp number = that ticket).
+// A tile is staged as HS stages of L/HS rows (one box per array each), so
+// that both rings hold several stages in the shared memory of one SM: STR
+// reduce stages (the HBM reads in flight) and STC consume stages (the L2
+// re-reads in flight; the consumers' side bounds the kernel, so it gets the
+// larger share).  Warp 0 of the consumers loads the walkers' state packets
+// of the next tile as soon as the consume producer has named it, a tile
+// ahead of their use.
+// Tickets below n_walk are only ever a CTA's first draw: a producer that
+// started as a walker's CTA draws again only once n_walk tickets are out, so
+// every walker is running before any tile is handed out, as in k_stream.  No
+// wait is circular: reducers wait for data only, a consume waits for the
+// aggregates of smaller tickets, and a producer blocked on a full queue holds
+// no ticket whose tile it has not staged.  Every wait is bounded; a group
+// that gives up decides to stop together, after its barrier.
+#ifndef LR_WS_HS
+#define LR_WS_HS 2
+#endif
+#ifndef LR_WS_STR
+#define LR_WS_STR 2
+#endif
+#ifndef LR_WS_STC
+#define LR_WS_STC 4
+#endif
+#ifndef LR_WS_QD
+#define LR_WS_QD 4
+#endif
+#ifndef LR_WS_LAG
+#define LR_WS_LAG 2
+#endif
+constexpr uint32_t kWsNone = 0xffffffffu;  // end of a ring or queue
+
+template <class Op>
+struct WsLayout {
+    static constexpr int NW = Op::NW, HS = LR_WS_HS, NRW = NW / HS;
+    static constexpr int W_PR = NW + NRW, W_PC = W_PR + 1, W_WALK = W_PC + 1, NWARPS = W_WALK + 1;
+    static constexpr int STR = LR_WS_STR, STC = LR_WS_STC, QD = LR_WS_QD;  // stages, queue slots
+    static constexpr int SR = NW * Op::R / HS;  // rows per stage
+    static_assert(NW % HS == 0, "a stage holds whole warps' rows");
+    // bytes of array k in a stage, its offset, and the stage size
+    __host__ __device__ static constexpr uint32_t arr_bytes(int k) {
+        return (uint32_t)(SR + Op::tma_extra(k)) * 32u * Op::VEC * (uint32_t)sizeof(typename Op::S);
+    }
+    __host__ __device__ static constexpr uint32_t off(int k) {
+        uint32_t o = 0;
+        for (int j = 0; j < k; ++j) o += (arr_bytes(j) + 127u) & ~127u;
+        return o;
+    }
+    static constexpr uint32_t SB = off(Op::TMA_N);
+};
+
+// Rows of a stage of k_wstream (row0: time of its first row).
+template <class Op>
+struct WsSrc {
+    const unsigned char* stage;
+    int64_t row0;
+    int lane_e;
+    template <class P, typename S>
+    __device__ __forceinline__ void ld(P& pk, int k, const S*, int64_t t) const {
+        constexpr int CW = 32 * Op::VEC;
+        const int row = (int)(t - row0) - Op::tma_shift(k);
+        pk.load_shared(reinterpret_cast<const S*>(stage + WsLayout<Op>::off(k)) + row * CW + lane_e);
+    }
+};
+
+// One thread: issue the boxes of stage h of `tile` (one per array).
+template <class Op>
+__device__ __forceinline__ void ws_stage(const Geom& g, const TmaDesc& td, unsigned char* dst,
+                                         uint64_t* full, uint32_t tile, int h, uint64_t pol) {
+    using Ly = WsLayout<Op>;
+    constexpr int L = Op::NW * Op::R, CW = 32 * Op::VEC;
+    const int64_t q = tile / g.n_ct, j = tile % g.n_ct;
+    const int64_t tchunk = Op::REV ? g.n_chunks - 1 - q : q;
+    const int32_t x = (int32_t)(j * CW), y0 = (int32_t)(tchunk * L + h * Ly::SR);
+    mbar_arrive_tx(full, td.tx_bytes);
+#pragma unroll
+    for (int a = 0; a < Op::TMA_N; ++a)
+        if (td.present & (1u << a))
+            tma_load_2d_hint(dst + Ly::off(a), &td.map[a], x, y0 + Op::tma_shift(a), full, pol);
+}
+
+// Ring bookkeeping of one producer thread: a stage whose last arming issued
+// copies that nobody is known to have waited for keeps that use's parity
+// (+1); before the thread exits it waits for those copies.
+template <int ST>
+struct WsRing {
+    uint32_t k = 0;         // uses taken so far
+    uint8_t pend[ST] = {};  // 0, or 1 + parity of the stage's last copy use
+    // take the next use: its stage, once free (false: the wait ran out and
+    // nothing was taken)
+    __device__ __forceinline__ bool take(uint64_t* empty, const uint32_t* err, uint32_t& st,
+                                         uint32_t& use) {
+        st = k % ST;
+        if (k >= ST && !mbar_wait(&empty[st], ((k / ST) - 1u) & 1u, err)) return false;
+        pend[st] = 0;  // its previous copies were consumed
+        use = k++;
+        return true;
+    }
+    // a taken use was armed, with copies or without (an end marker)
+    __device__ __forceinline__ void armed(uint32_t use, bool copies) {
+        pend[use % ST] = copies ? (uint8_t)(1u + ((use / ST) & 1u)) : 0;
+    }
+    __device__ __forceinline__ void drain(uint64_t* full, const uint32_t* err) const {
+        for (int i = 0; i < ST; ++i)
+            if (pend[i]) mbar_wait(&full[i], pend[i] - 1u, err);
+    }
+};
+
+template <class Op>
+__global__ void __launch_bounds__(WsLayout<Op>::NWARPS * 32, 1)
+    k_wstream(typename Op::Params p, Geom g, const Carry cr0, uint32_t d_con,
+              const __grid_constant__ TmaDesc td) {
+    if (Op::skip(p)) {  // whole launch: before any ticket or barrier
+        if (blockIdx.x == 0 && threadIdx.x == 0) retire_epoch(cr0);
+        return;
+    }
+    using Ly = WsLayout<Op>;
+    constexpr int NW = Op::NW, VEC = Op::VEC, NRW = Ly::NRW, HS = Ly::HS, STR = Ly::STR,
+                  STC = Ly::STC, QD = Ly::QD, SR = Ly::SR, L = Op::NW * Op::R, WPS = NW / HS;
+    constexpr uint32_t SB = Ly::SB;
+    extern __shared__ unsigned char dyn_smem[];
+    unsigned char* ring_r = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~(uintptr_t)127);
+    unsigned char* ring_c = ring_r + STR * SB;
+    __shared__ float s_ra[2][NW][32][VEC], s_rb[2][NW][32][VEC];  // reduce: per-warp aggregates
+    __shared__ float s_ca[2][NW][32][VEC], s_cb[2][NW][32][VEC];  // consume: per-warp aggregates
+    __shared__ float s_cin[2][32][VEC];                           // state entering the consumed tile
+    __shared__ typename Op::Smem xs;
+    __shared__ __align__(8) uint64_t full_r[STR], empty_r[STR], full_c[STC], empty_c[STC];
+    __shared__ __align__(8) uint64_t named_c[STC];  // s_ctile of the stage is written
+    __shared__ __align__(8) uint64_t q_full[QD], q_empty[QD];
+    __shared__ uint32_t s_rtile[STR], s_ctile[STC], s_q[QD];
+    __shared__ uint32_t s_first, s_epoch, s_rabort, s_cabort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Carry cr = cr0;
+    const uint32_t limit = cr.n_walk + g.n_tiles + d_con;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STR; ++i) {
+            mbar_init(&full_r[i], 1);
+            mbar_init(&empty_r[i], NRW);  // every reducer warp reads every stage
+        }
+        for (int i = 0; i < STC; ++i) {
+            mbar_init(&full_c[i], 1);
+            mbar_init(&empty_c[i], WPS);  // the consumer warps whose rows it holds
+            mbar_init(&named_c[i], 1);
+        }
+        for (int i = 0; i < QD; ++i) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 1);
+        }
+        s_rabort = 0;
+        s_cabort = 0;
+        mbar_init_fence();
+        const uint32_t t = draw_ticket(cr);
+        ticket_drawn(cr, g, t);
+        s_first = t + g.ticket_base;
+        s_epoch = cr.epoch;
+    }
+    __syncthreads();
+    cr.epoch = s_epoch;
+    const uint32_t first = s_first;
+
+    if (warp == Ly::W_WALK) {
+        if (first < cr.n_walk) walker_warp<typename Op::S>(cr, g, first, Op::init_ptr(p));
+        return;
+    }
+
+    if (warp == Ly::W_PR) {  // reduce producer
+        if (lane != 0) return;
+        const uint64_t pol = l2_evict_last();
+        uint32_t t = first;
+        bool ok = true;
+        if (t < cr.n_walk) {
+            // every walker role is taken before this CTA draws a tile ticket
+            uint32_t spins = 0, sleep_ns = 0;
+            while (true) {
+                const uint32_t drawn = (uint32_t)ld_pkt(cr.tk) + g.ticket_base;
+                if (drawn >= cr.n_walk) break;
+                if (wait_step(cr, spins, sleep_ns, 256)) {
+                    give_up(cr);
+                    ok = false;
+                    break;
+                }
+            }
+            if (ok) {
+                t = draw_ticket(cr);
+                ticket_drawn(cr, g, t);
+                t += g.ticket_base;
+            }
+        }
+        WsRing<STR> rr;
+        uint32_t kq = 0;
+        while (ok && t < limit) {
+            const uint32_t x = t - cr.n_walk;
+            if (x < g.n_tiles) {
+                for (int h = 0; h < HS && ok; ++h) {
+                    uint32_t st, use;
+                    if (!rr.take(empty_r, cr.err, st, use)) {
+                        ok = false;
+                        break;
+                    }
+                    s_rtile[st] = x;
+                    ws_stage<Op>(g, td, ring_r + st * SB, &full_r[st], x, h, pol);
+                    rr.armed(use, true);
+                }
+                if (!ok) {
+                    give_up(cr);
+                    break;
+                }
+            }
+            if (x >= d_con && x - d_con < g.n_tiles) {
+                const uint32_t sq = kq % QD;
+                if (kq >= QD && !mbar_wait(&q_empty[sq], ((kq / QD) - 1u) & 1u, cr.err)) {
+                    give_up(cr);
+                    ok = false;
+                    break;
+                }
+                s_q[sq] = x - d_con;
+                mbar_arrive(&q_full[sq]);
+                ++kq;
+            }
+            t = draw_ticket(cr);
+            ticket_drawn(cr, g, t);
+            t += g.ticket_base;
+        }
+        // the ends of the reduce ring (first stage of a tile) and of the queue;
+        // after a timeout the other groups stop on the error word
+        if (ok) {
+            uint32_t st, use;
+            if (rr.take(empty_r, cr.err, st, use)) {
+                s_rtile[st] = kWsNone;
+                mbar_arrive(&full_r[st]);
+                rr.armed(use, false);
+            }
+            const uint32_t sq = kq % QD;
+            if (kq < QD || mbar_wait(&q_empty[sq], ((kq / QD) - 1u) & 1u, cr.err)) {
+                s_q[sq] = kWsNone;
+                mbar_arrive(&q_full[sq]);
+            }
+        }
+        rr.drain(full_r, cr.err);
+        return;
+    }
+
+    if (warp == Ly::W_PC) {  // consume producer
+        if (lane != 0) return;
+        const uint64_t pol = l2_evict_first();
+        WsRing<STC> rc;
+        uint32_t kq = 0;
+        bool ok = true;
+        while (ok) {
+            const uint32_t sq = kq % QD;
+            if (!mbar_wait(&q_full[sq], (kq / QD) & 1u, cr.err)) break;
+            const uint32_t y = s_q[sq];
+            mbar_arrive(&q_empty[sq]);
+            ++kq;
+            for (int h = 0; h < HS; ++h) {  // the end goes to every stage of a tile
+                uint32_t st, use;
+                if (!rc.take(empty_c, cr.err, st, use)) {
+                    ok = false;
+                    break;
+                }
+                s_ctile[st] = y;
+                mbar_arrive(&named_c[st]);
+                if (y == kWsNone) {
+                    mbar_arrive(&full_c[st]);
+                    rc.armed(use, false);
+                } else {
+                    ws_stage<Op>(g, td, ring_c + st * SB, &full_c[st], y, h, pol);
+                    rc.armed(use, true);
+                }
+            }
+            if (y == kWsNone) break;
+        }
+        rc.drain(full_c, cr.err);
+        return;
+    }
+
+    if (warp >= NW) {  // reducer warps: reducer rw takes the rows of warp rw + h*NRW in stage h
+        const int rw = warp - NW;
+        uint32_t par = 0;
+        for (uint32_t k = 0;; ++k) {
+            uint32_t x = kWsNone;
+            bool bad = false;
+#pragma unroll
+            for (int h = 0; h < HS; ++h) {
+                const uint32_t u = k * HS + h, st = u % STR;
+                const bool got = __all_sync(0xffffffffu, mbar_wait(&full_r[st], (u / STR) & 1u, cr.err));
+                if (!got) {
+                    bad = true;
+                    break;
+                }
+                if (h == 0) x = s_rtile[st];
+                if (x == kWsNone) break;  // the end: a tile-less first stage
+                const int vw = rw + h * NRW;
+                const TileCoord tc = tile_coord_qj<Op>(g, x / (uint32_t)g.n_ct, x % (uint32_t)g.n_ct, vw);
+                typename Op::Regs rg;
+                Op::load(WsSrc<Op>{ring_r + st * SB, tc.tchunk * L + h * SR, lane * VEC}, p, g, tc, rg);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_r[st]);
+                typename Op::Work w;
+                float A[VEC], B[VEC];
+                Op::aggregate(p, g, tc, rg, w, A, B, false);
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    s_ra[par][vw][lane][v] = A[v];
+                    s_rb[par][vw][lane][v] = B[v];
+                }
+            }
+            if (bad && lane == 0) {
+                s_rabort = 1;
+                atomicOr(cr.err, ERRBIT_TIMEOUT);
+            }
+            asm volatile("bar.sync 2, %0;" ::"r"(NRW * 32) : "memory");
+            if (s_rabort != 0 || x == kWsNone) break;
+            if (rw == 0) {
+                const TileCoord tc = tile_coord_qj<Op>(g, x / (uint32_t)g.n_ct, x % (uint32_t)g.n_ct, 0);
+                if (tc.cok && tc.q < g.n_chunks - 1) {
+                    float TA[VEC], TB[VEC];
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) { TA[v] = 1.f; TB[v] = 0.f; }
+#pragma unroll
+                    for (int w = 0; w < NW; ++w)
+#pragma unroll
+                        for (int v = 0; v < VEC; ++v) {
+                            const float a = s_ra[par][w][lane][v], b = s_rb[par][w][lane][v];
+                            TB[v] = __fmaf_rn(a, TB[v], b);
+                            TA[v] *= a;
+                        }
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v)
+                        st_pkt2(cr.agg + 2 * ((tc.c + v) * g.n_chunks + tc.q), pkt(TA[v], cr.epoch),
+                                pkt(TB[v], cr.epoch));
+                }
+            }
+            par ^= 1u;
+        }
+        return;
+    }
+
+    // consumer warps: warp w's rows are in stage w / WPS of a tile
+    typename Op::Acc acc;
+    Op::acc_init(acc);
+    const typename Op::S* ip = Op::init_ptr(p);
+    const int h = warp / WPS;
+    bool any = false;
+    uint32_t par = 0;
+    // Warp 0 loads the walkers' states for a tile one tile ahead: the tile's
+    // number is in s_ctile as soon as the consume producer has named the
+    // stage, long before its data lands, so the packets' round trip overlaps
+    // the previous tile.
+    u64 pre_next[VEC];
+    auto peek = [&](uint32_t u) {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) pre_next[v] = 0ull;
+        const uint32_t st = u % STC;
+        if (!mbar_wait(&named_c[st], (u / STC) & 1u, cr.err)) return;
+        const uint32_t y = s_ctile[st];
+        if (y == kWsNone) return;
+        const TileCoord tn = tile_coord<Op>(g, y);
+        if (tn.q > 0 && tn.cok) {
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) pre_next[v] = ld_pkt_cg(cr.inc + (tn.c + v) * g.n_chunks + tn.q - 1);
+        }
+    };
+    if (warp == 0) peek(0);
+    for (uint32_t k = 0;; ++k) {
+        const uint32_t u = k * HS + h, st = u % STC;
+        const bool got = __all_sync(0xffffffffu, mbar_wait(&full_c[st], (u / STC) & 1u, cr.err));
+        const uint32_t y = got ? s_ctile[st] : kWsNone;
+        if (!got && lane == 0) {
+            s_cabort = 1;
+            atomicOr(cr.err, ERRBIT_TIMEOUT);
+        }
+        TileCoord tc{};
+        typename Op::Regs rg;
+        if (y != kWsNone) {
+            tc = tile_coord<Op>(g, y);
+            Op::load(WsSrc<Op>{ring_c + st * SB, tc.tchunk * L + h * SR, lane * VEC}, p, g, tc, rg);
+        }
+        __syncwarp();
+        if (lane == 0 && got) mbar_arrive(&empty_c[st]);  // copied into registers
+        typename Op::Work w;
+        if (y != kWsNone) {
+            u64 pre[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) pre[v] = pre_next[v];
+            if (warp == 0) peek((k + 1) * HS);
+            float A[VEC], B[VEC];
+            Op::aggregate(p, g, tc, rg, w, A, B, true);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                s_ca[par][warp][lane][v] = A[v];
+                s_cb[par][warp][lane][v] = B[v];
+            }
+            if (warp == 0) {  // the walkers' state for this tile
+                float cin[VEC];
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) cin[v] = 0.f;
+                if (tc.q == 0) {
+                    if (ip != nullptr && tc.cok) load_vec<typename Op::S, VEC>(ip + tc.c, cin);
+                } else {
+                    bool ok = true;
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) {
+                        ok = ok && (!tc.cok || pkt_ok(pre[v], cr.epoch));
+                        cin[v] = pkt_val(pre[v]);
+                    }
+                    uint32_t spins = 0, sleep_ns = 0;
+                    while (!__all_sync(0xffffffffu, ok)) {
+                        if (__any_sync(0xffffffffu, wait_step(cr, spins, sleep_ns, kTileMaxSleepNs))) {
+                            if (lane == 0) give_up(cr);
+#pragma unroll
+                            for (int v = 0; v < VEC; ++v) cin[v] = __int_as_float(0x7fc00000);
+                            break;
+                        }
+                        ok = !tc.cok || get_states_strided<VEC>(cr.inc + tc.c * g.n_chunks + tc.q - 1,
+                                                                g.n_chunks, cin, cr.epoch);
+                    }
+                }
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) s_cin[par][lane][v] = cin[v];
+            }
+        }
+        csync<NW>();
+        if (s_cabort != 0 || y == kWsNone) break;
+        any = true;
+        float PA[VEC], PB[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { PA[v] = 1.f; PB[v] = 0.f; }
+#pragma unroll
+        for (int w2 = 0; w2 < NW - 1; ++w2) {
+            if (w2 < warp) {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    const float a = s_ca[par][w2][lane][v], b = s_cb[par][w2][lane][v];
+                    PB[v] = __fmaf_rn(a, PB[v], b);
+                    PA[v] *= a;
+                }
+            }
+        }
+        float s0[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) s0[v] = __fmaf_rn(PA[v], s_cin[par][lane][v], PB[v]);
+        Op::finish(p, g, tc, rg, w, s0, xs, acc);
+        par ^= 1u;
+    }
+    if (any) Op::at_exit(p, xs, acc);
 }
 
 // Whole consumer CTA: one tile whose data is in registers -- local scan,
@@ -1481,7 +1952,13 @@ cudaError_t launch_chain(const typename Op::Params& p, Geom g, const Carry& cr, 
 // measured best on GB300), capped so that the tiles in flight (about 32 MB of
 // inputs) stay well within the L2.
 template <class Op>
+cudaError_t launch_wstream(const typename Op::Params& p, Geom g, Carry cr, cudaStream_t s);
+template <class Op>
 cudaError_t launch_stream(const typename Op::Params& p, Geom g, const Carry& cr, cudaStream_t s) {
+    if constexpr (stream_ws<Op>::value) {
+        const cudaError_t e = launch_wstream<Op>(p, g, cr, s);
+        if (e != cudaErrorNotSupported) return e;
+    }
     const uint32_t grid = persist_grid(g, cr, stream_occupancy<Op>());
     const uint64_t tile_ctas = grid > cr.n_walk ? grid - cr.n_walk : 1;
     const uint64_t tile_bytes =
@@ -1491,6 +1968,65 @@ cudaError_t launch_stream(const typename Op::Params& p, Geom g, const Carry& cr,
     if (d_con > cap) d_con = cap > 1 ? cap : 1;
     g.n_draws = g.n_tiles + (uint32_t)d_con + grid - g.ticket_base;
     k_stream<Op><<<grid, 32 * Op::NW, 0, s>>>(p, g, cr, (uint32_t)d_con);
+    return cudaGetLastError();
+}
+
+// Host: launch k_wstream<Op> (walker protocol, warp-specialised, TMA).
+// cudaErrorNotSupported when it does not apply (the walker warps would
+// outnumber the CTAs, or the arrays cannot be tensor-mapped).
+template <class Op>
+cudaError_t launch_wstream(const typename Op::Params& p, Geom g, Carry cr, cudaStream_t s) {
+    using Ly = WsLayout<Op>;
+    constexpr int CW = 32 * Op::VEC;
+    constexpr uint32_t SB = Ly::SB;
+    constexpr size_t dyn = (size_t)(Ly::STR + Ly::STC) * SB + 128;
+    static_assert(Op::TMA_N <= TMA_MAX_ARR, "too many staged arrays");
+    static_assert(Ly::SR + 1 <= 256 && CW <= 256, "a TMA box holds at most 256 rows and columns");
+    if (Op::VEC != 4 || cr.wv <= 0) return cudaErrorNotSupported;
+    TmaDesc td;
+    memset(&td, 0, sizeof td);
+    const void* ptr[TMA_MAX_ARR] = {};
+    Op::tma_arrays(p, ptr);
+    for (int a = 0; a < Op::TMA_N; ++a) {
+        if (!ptr[a]) continue;
+        if (((uintptr_t)ptr[a] & 15) != 0 || (g.C * sizeof(typename Op::S)) % 16 != 0 ||
+            !tma_encode(&td.map[a], ptr[a], sizeof(typename Op::S) == 2 ? 1 : 0, g.T, g.C, CW,
+                        Ly::SR + Op::tma_extra(a)))
+            return cudaErrorNotSupported;
+        td.present |= 1u << a;
+        td.tx_bytes += Ly::arr_bytes(a);
+    }
+    static int occ[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int& o = occ[dev & 63];
+    if (o <= 0) {
+        cudaError_t e = cudaFuncSetAttribute(k_wstream<Op>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k_wstream<Op>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_wstream<Op>, 32 * Ly::NWARPS, dyn) !=
+                cudaSuccess ||
+            n <= 0)
+            n = 1;
+        o = n;
+    }
+    // one walker warp per walker (none when the caller asked for none), and
+    // every walker's CTA resident at once: tiles are handed out only once all
+    // walker roles are taken
+    const uint64_t n_walk = cr.n_walk ? (uint64_t)((g.C + cr.wv - 1) / cr.wv) : 0;
+    if (n_walk > (uint64_t)o * (uint64_t)sm_count()) return cudaErrorNotSupported;
+    cr.n_walk = (uint32_t)n_walk;
+    const uint32_t grid = persist_grid(g, cr, o);
+    const uint64_t tile_bytes = (uint64_t)SB * Ly::HS;
+    uint64_t d_con = (uint64_t)LR_WS_LAG * grid;
+    const uint64_t cap = ((uint64_t)LR_STREAM_L2MB << 20) / (tile_bytes ? tile_bytes : 1);
+    if (d_con > cap) d_con = cap > 1 ? cap : 1;
+    g.n_draws = cr.n_walk + g.n_tiles + (uint32_t)d_con + grid - g.ticket_base;
+    k_wstream<Op><<<grid, 32 * Ly::NWARPS, dyn, s>>>(p, g, cr, (uint32_t)d_con, td);
     return cudaGetLastError();
 }
 

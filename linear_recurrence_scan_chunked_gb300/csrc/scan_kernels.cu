@@ -36,6 +36,7 @@ struct ScanFwdOp {
     static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
     static constexpr bool REV = false;
     static constexpr int IN_ARRAYS = 2;  // a, b
+    static constexpr bool STREAM_WS = LR_STREAM_WS != 0;
     static constexpr bool SCRATCH_IN_CARRY = false;
     using Params = ScanFwdParams<S>;
     struct Regs {

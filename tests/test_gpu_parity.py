@@ -16,7 +16,9 @@ pytestmark = pytest.mark.gpu
 # (T, B, D): tiles are 64 (fp32 fwd) / 32 rows and 128 / 256 channels wide
 SHAPES = [(1, 1, 4), (5, 2, 8), (64, 1, 128), (65, 1, 128), (200, 3, 96), (1000, 2, 64),
           (333, 4, 40), (77, 3, 5), (513, 1, 129), (2048, 2, 256), (3, 1, 1)]
-LONG = [(100003, 1, 4), (20000, 1, 128)]
+# long, narrow problems run the walker protocol; 200 channels need more walker
+# warps than there are SMs, so the forward takes the register kernel there
+LONG = [(100003, 1, 4), (20000, 1, 128), (20000, 1, 200)]
 # wide problems (at least 128 channel tiles) run the strip kernel: one strip
 # per CTA with a ragged last strip, and two strips per CTA (more strips than
 # resident CTAs)
