@@ -116,7 +116,7 @@ struct DeerOp {
         float wv[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) wv[v] = 0.f;
-        if (tc.cok) load_param<VEC>(p.w + tc.c % g.D, wv);
+        if (tc.cok) load_param<VEC>(p.w + tc.cd, wv);
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { A[v] = 1.f; B[v] = 0.f; }
 #pragma unroll
@@ -143,14 +143,14 @@ struct DeerOp {
         uint32_t seq = 0;
         bool live = true;
         if (per_seq && tc.cok) {
-            seq = (uint32_t)(tc.c / g.D);
+            seq = (uint32_t)chan_seq(g, tc.c);
             live = p.seq_done[seq] == 0;
         }
         uint32_t mx = 0;  // this tile's residual bits (per-sequence stopping)
         float wv[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { wv[v] = 0.f; w.NA[v] = 1.f; w.NB[v] = 0.f; }
-        if (nxt && tc.cok) load_param<VEC>(p.w + tc.c % g.D, wv);
+        if (nxt && tc.cok) load_param<VEC>(p.w + tc.cd, wv);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int64_t t = tc.t0 + r;
@@ -300,7 +300,7 @@ struct DeerBwdOp {
         float wv[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) wv[v] = 0.f;
-        if (tc.cok) load_param<VEC>(p.w + tc.c % g.D, wv);
+        if (tc.cok) load_param<VEC>(p.w + tc.cd, wv);
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { A[v] = 1.f; B[v] = 0.f; }
 #pragma unroll

@@ -133,7 +133,7 @@ struct DeerOdeOp {
         float wv[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) wv[v] = 0.f;
-        if (tc.cok) load_param<VEC>(p.w + tc.c % g.D, wv);
+        if (tc.cok) load_param<VEC>(p.w + tc.cd, wv);
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { A[v] = 1.f; B[v] = 0.f; }
         uint32_t ncl = 0;
@@ -163,7 +163,7 @@ struct DeerOdeOp {
         float wv[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { wv[v] = 0.f; w.NA[v] = 1.f; w.NB[v] = 0.f; }
-        if (nxt && tc.cok) load_param<VEC>(p.w + tc.c % g.D, wv);
+        if (nxt && tc.cok) load_param<VEC>(p.w + tc.cd, wv);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int64_t t = tc.t0 + r;

@@ -242,6 +242,7 @@ int plan(DevWS& ws, Op op, int dtype, bool vec, int64_t T, int64_t C, int64_t D,
     g->T = T;
     g->C = C;
     g->D = D;
+    set_channel_div(*g);
     g->n_chunks = cp.n_chunks;
     if ((C + ts.CW - 1) / ts.CW > INT32_MAX) return LR_ERR_TOO_LARGE;
     g->n_ct = (int)((C + ts.CW - 1) / ts.CW);

@@ -141,7 +141,39 @@ struct Geom {
     uint32_t n_draws;     // tickets drawn by the whole launch (the last drawer resets)
     uint32_t ticket_base; // added to every ticket (the timeout test starts past tile 0)
     uint32_t max_grid;    // 0, or an upper bound on the CTAs launched (timeout test)
+    // c / D without a 64-bit division (per-feature parameters, per-sequence
+    // state): while C < 2^31, c / D = (umulhi(c, d_mul) + c) >> d_shift, the
+    // round-up multiplier of Granlund and Montgomery ("Division by invariant
+    // integers using multiplication", 1994); d_mul = 0: plain division.
+    uint32_t d_mul;
+    uint32_t d_shift;
 };
+
+// Host: the multiplier and shift of c / D (0 when C or D is out of range).
+inline void set_channel_div(Geom& g) {
+    g.d_mul = 0;
+    g.d_shift = 0;
+    if (g.D < 1 || g.D >= ((int64_t)1 << 31) || g.C >= ((int64_t)1 << 31)) return;
+    uint32_t s = 0;
+    while (((uint64_t)1 << s) < (uint64_t)g.D) ++s;
+    // floor(2^32 (2^s - D) / D) + 1 < 2^32, since 2^s - D < D
+    g.d_mul = (uint32_t)((((uint64_t)1 << 32) * (((uint64_t)1 << s) - (uint64_t)g.D)) / (uint64_t)g.D + 1);
+    g.d_shift = s;
+}
+
+// Channel c's feature index c mod D and sequence index c / D.
+__host__ __device__ __forceinline__ int64_t chan_seq(const Geom& g, int64_t c) {
+    if (g.d_mul == 0) return c / g.D;
+#ifdef __CUDA_ARCH__
+    const uint32_t hi = __umulhi((uint32_t)c, g.d_mul);
+#else
+    const uint32_t hi = (uint32_t)(((uint64_t)(uint32_t)c * g.d_mul) >> 32);
+#endif
+    return (int64_t)(((uint64_t)hi + (uint32_t)c) >> g.d_shift);
+}
+__host__ __device__ __forceinline__ int64_t chan_feat(const Geom& g, int64_t c) {
+    return c - chan_seq(g, c) * g.D;
+}
 
 // Barrier of the NW consumer warps of a CTA (named barrier 1).  The scan
 // kernels that stage tiles with TMA add a producer warp that never takes part

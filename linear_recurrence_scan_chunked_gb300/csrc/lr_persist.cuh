@@ -60,6 +60,7 @@ struct TileCoord {
     int64_t q;       // chunk index in scan order
     int64_t tchunk;  // chunk index in time
     int64_t c;       // first channel of this lane
+    int64_t cd;      // its feature index, c mod D (VEC divides D on the vector path)
     bool cok;        // the lane's channels are inside the problem
     int64_t t0;      // time of this thread's first row (scan order)
     // A run of tiles of the same channels in scan order goes through this CTA
@@ -82,6 +83,7 @@ __device__ __forceinline__ TileCoord tile_coord_qj(const Geom& g, uint32_t q, ui
     TileCoord tc;
     tc.q = q;
     tc.c = (int64_t)j * CW + lane * Op::VEC;
+    tc.cd = chan_feat(g, tc.c);
     tc.cok = tc.c < g.C;
     tc.tchunk = Op::REV ? g.n_chunks - 1 - tc.q : tc.q;
     tc.t0 = Op::REV ? tc.tchunk * L + (L - 1) - warp * Op::R : tc.tchunk * L + warp * Op::R;

@@ -98,9 +98,9 @@ struct LstmFwdOp {
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { bfv[v] = 0.f; biv[v] = 0.f; bcv[v] = 0.f; }
         if (tc.cok) {
-            load_param<VEC>(p.bf + tc.c % g.D, bfv);
-            load_param<VEC>(p.bi + tc.c % g.D, biv);
-            load_param<VEC>(p.bc + tc.c % g.D, bcv);
+            load_param<VEC>(p.bf + tc.cd, bfv);
+            load_param<VEC>(p.bi + tc.cd, biv);
+            load_param<VEC>(p.bc + tc.cd, bcv);
         }
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { A[v] = 1.f; B[v] = 0.f; }
@@ -124,7 +124,7 @@ struct LstmFwdOp {
         float bov[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) bov[v] = 0.f;
-        if (tc.cok) load_param<VEC>(p.bo + tc.c % g.D, bov);
+        if (tc.cok) load_param<VEC>(p.bo + tc.cd, bov);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int64_t t = tc.t0 + r;
@@ -243,8 +243,8 @@ struct LstmBwdOp {
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { bfv[v] = 0.f; bov[v] = 0.f; w.sum_o[v] = 0.f; }
         if (tc.cok) {
-            load_param<VEC>(p.bf + tc.c % g.D, bfv);
-            load_param<VEC>(p.bo + tc.c % g.D, bov);
+            load_param<VEC>(p.bf + tc.cd, bfv);
+            load_param<VEC>(p.bo + tc.cd, bov);
         }
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { A[v] = 1.f; B[v] = 0.f; }
@@ -299,8 +299,8 @@ struct LstmBwdOp {
             sum_c[v] = 0.f;
         }
         if (tc.cok) {
-            load_param<VEC>(p.bi + tc.c % g.D, biv);
-            load_param<VEC>(p.bc + tc.c % g.D, bcv);
+            load_param<VEC>(p.bi + tc.cd, biv);
+            load_param<VEC>(p.bc + tc.cd, bcv);
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) {

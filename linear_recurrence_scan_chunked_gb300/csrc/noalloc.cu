@@ -115,6 +115,7 @@ extern "C" int lr_scan_fwd_noalloc(const void* a, const void* b, const void* h0,
     g.T = T;
     g.C = C;
     g.D = D;
+    set_channel_div(g);
     g.n_chunks = n_chunks;
     g.n_ct = (int)n_ct;
     g.n_tiles = (uint32_t)tiles;

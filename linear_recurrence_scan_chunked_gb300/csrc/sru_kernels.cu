@@ -92,7 +92,7 @@ struct SruFwdOp {
         float bfv[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) bfv[v] = 0.f;
-        if (tc.cok) load_param<VEC>(p.bf + tc.c % g.D, bfv);
+        if (tc.cok) load_param<VEC>(p.bf + tc.cd, bfv);
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { A[v] = 1.f; B[v] = 0.f; }
 #pragma unroll
@@ -113,7 +113,7 @@ struct SruFwdOp {
         float brv[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) brv[v] = 0.f;
-        if (tc.cok) load_param<VEC>(p.br + tc.c % g.D, brv);
+        if (tc.cok) load_param<VEC>(p.br + tc.cd, brv);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int64_t t = tc.t0 + r;
@@ -230,8 +230,8 @@ struct SruBwdOp {
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { bfv[v] = 0.f; brv[v] = 0.f; w.sum_r[v] = 0.f; }
         if (tc.cok) {
-            load_param<VEC>(p.bf + tc.c % g.D, bfv);
-            load_param<VEC>(p.br + tc.c % g.D, brv);
+            load_param<VEC>(p.bf + tc.cd, bfv);
+            load_param<VEC>(p.br + tc.cd, brv);
         }
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { A[v] = 1.f; B[v] = 0.f; }
