@@ -81,6 +81,11 @@ struct DeerOp {
         return stop;
     }
     __device__ static const S* init_ptr(const Params& p) { return p.h0; }
+    // This thread's rows and the row before them are all inside the problem
+    // and the previous iterate is staged: no per-row bounds checks.
+    __device__ static bool interior(const Params& p, const Geom& g, const TileCoord& tc) {
+        return tc.cok && tc.t0 >= 1 && tc.t0 + R <= g.T && p.yold != nullptr;
+    }
 
     static constexpr int TMA_N = 2;  // staged: u, previous iterate (rows t0-1 .. t0+L-1)
     __host__ __device__ static constexpr int tma_shift(int k) { return k == 1 ? -1 : 0; }
@@ -93,6 +98,13 @@ struct DeerOp {
     template <class Src>
     __device__ static void load(const Src& src, const Params& p, const Geom& g,
                                 const TileCoord& tc, Regs& rg) {
+        if (interior(p, g, tc)) {
+#pragma unroll
+            for (int i = 0; i <= R; ++i) src.ld(rg.yo[i], 1, p.yold, tc.t0 - 1 + i);
+#pragma unroll
+            for (int r = 0; r < R; ++r) src.ld(rg.u[r], 0, p.u, tc.t0 + r);
+            return;
+        }
 #pragma unroll
         for (int i = 0; i <= R; ++i) {
             const int64_t t = tc.t0 - 1 + i;
@@ -119,6 +131,21 @@ struct DeerOp {
         if (tc.cok) load_param<VEC>(p.w + tc.cd, wv);
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { A[v] = 1.f; B[v] = 0.f; }
+        if (interior(p, g, tc)) {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    const float yt = rg.yo[r].get(v);
+                    const float th = act_tanh(wv[v] * yt + rg.u[r].get(v));
+                    const float jac = wv[v] * (1.f - th * th);
+                    w.J[r][v] = jac;
+                    w.Rh[r][v] = th - jac * yt;
+                    B[v] = jac * B[v] + w.Rh[r][v];
+                    A[v] *= jac;
+                }
+            return;
+        }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const bool ok = tc.cok && tc.t0 + r < g.T;
@@ -151,6 +178,32 @@ struct DeerOp {
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { wv[v] = 0.f; w.NA[v] = 1.f; w.NB[v] = 0.f; }
         if (nxt && tc.cok) load_param<VEC>(p.w + tc.cd, wv);
+        if (nxt && !per_seq && interior(p, g, tc)) {  // the iterations' common case
+            S* out = p.ynew + tc.t0 * g.C + tc.c;
+#pragma unroll
+            for (int r = 0; r < R; ++r, out += g.C) {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    float yp = s[v];
+                    if constexpr (sizeof(S) == 2) yp = bf_lo(bf_bits(yp));
+                    const float th = act_tanh(wv[v] * yp + rg.u[r].get(v));
+                    const float jac = wv[v] * (1.f - th * th);
+                    w.NB[v] = jac * w.NB[v] + (th - jac * yp);
+                    w.NA[v] *= jac;
+                    s[v] = w.J[r][v] * s[v] + w.Rh[r][v];
+                }
+                store_vec<S, VEC>(out, s);
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    float yv = s[v];
+                    if constexpr (sizeof(S) == 2) yv = bf_lo(bf_bits(yv));
+                    const uint32_t bits = __float_as_uint(fabsf(yv - rg.yo[r + 1].get(v)));
+                    mx = bits > mx ? bits : mx;
+                }
+            }
+            acc.mx = mx > acc.mx ? mx : acc.mx;
+            return;
+        }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int64_t t = tc.t0 + r;

@@ -6,30 +6,48 @@
 // "监控与调优").
 //
 // Both are written from their exponential forms,
-//     sigmoid(z) = 1 / (1 + e^{-z}),
-//     tanh(x)    = sign(x) (1 - 2 / (e^{2|x|} + 1)),
-// with the exponential and the quotient taken from the hardware-approximate
-// intrinsics __expf and __fdividef.  That is about a third of the instruction
-// count of expf / tanhf with an IEEE division, which matters here: these
-// kernels stream 24-40 bytes per element, and three activations per element
-// with the accurate routines made the SRU kernels issue-bound.  Both forms
-// saturate correctly (an infinite exponential gives a quotient of 0), keep NaN,
-// and have an absolute error of a few 1e-7 on the whole line (no cancellation
-// issue for the absolute error near 0), well inside the 1e-5 tolerance the
-// results are checked against; lr_test_activations exposes them to the test
-// that bounds their error against fp64.
+//     sigmoid(z) = 1 / (1 + 2^{-z log2 e}),
+//     tanh(x)    = sign(x) (1 - 2 / (2^{2 |x| log2 e} + 1)),
+// with the power of two and the reciprocal taken from the hardware's
+// approximate instructions (ex2.approx, rcp.approx) in their flush-to-zero
+// forms: one instruction each, with no extra steps for subnormal results,
+// which none of these forms needs (a subnormal power of two or reciprocal only
+// occurs where the result has saturated to 0 or 1 anyway).  That is a few
+// instructions per activation, which matters here: these kernels stream 24-40
+// bytes per element, and with two to five activations per element the DEER,
+// SRU and LSTM kernels are bound by instruction issue.  Both forms saturate
+// correctly (an infinite power gives a reciprocal of 0), keep NaN, and have an
+// absolute error of a few 1e-7 on the whole line (no cancellation issue for
+// the absolute error near 0), well inside the 1e-5 tolerance the results are
+// checked against; lr_test_activations exposes them to the test that bounds
+// their error against fp64.
 #pragma once
 
 #include <cuda_runtime.h>
 
 namespace lrs {
 
+// 2^x and 1/x, hardware approximations (relative error about 2^-22), with
+// subnormal results flushed to zero.
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_ftz(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;       // log2(e)
+constexpr float kTwoLog2e = 2.8853900817779268f;    // 2 log2(e)
+
 __device__ __forceinline__ float act_sigmoid(float z) {
-    return __fdividef(1.f, 1.f + __expf(-z));
+    return rcp_ftz(1.f + ex2_ftz(-kLog2e * z));
 }
 
 __device__ __forceinline__ float act_tanh(float x) {
-    const float t = 1.f - __fdividef(2.f, __expf(2.f * fabsf(x)) + 1.f);
+    const float t = fmaf(-2.f, rcp_ftz(ex2_ftz(kTwoLog2e * fabsf(x)) + 1.f), 1.f);
     return copysignf(t, x);
 }
 
@@ -50,7 +68,7 @@ __device__ __forceinline__ float act_expm1(float x) {
         p = fmaf(x * 0.5f, p, 1.f);
         return x * p;
     }
-    return __expf(x) - 1.f;
+    return ex2_ftz(kLog2e * x) - 1.f;
 }
 
 }  // namespace lrs
