@@ -43,6 +43,8 @@
 
 #include <string.h>
 
+#include <algorithm>
+
 #include <type_traits>
 
 #include "lr_launch.h"
@@ -235,6 +237,9 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
 // that gives up decides to stop together, after its barrier.
 #ifndef LR_WS_HS
 #define LR_WS_HS 2
+#endif
+#ifndef LR_SEGRED
+#define LR_SEGRED 1
 #endif
 #ifndef LR_WS_STR
 #define LR_WS_STR 2
@@ -1354,6 +1359,105 @@ struct SegGeom {
     uint32_t n_units;  // n_seg * n_ct
 };
 
+// The next launch's segment aggregates, and nothing else (the pass before a
+// DEER solve's first iteration, whose aggregates depend on the inputs only):
+// a plain streaming reduction.  CTA b takes segments (units) b, b + G, ...; in
+// a segment warp w folds the rows of its contiguous share [w S/NW, (w+1) S/NW)
+// (S rows per segment) from global memory, R rows per step and two steps in
+// flight, and warp 0 folds the NW shares in row order and publishes the
+// segment's packets with the next launch's epoch.  Nothing waits: every CTA
+// draws one ticket only to learn the launch's epoch and to retire it.  The
+// association is fixed by position (rows of a step in order, steps in order,
+// then the warps' shares in order).
+template <class Op>
+__global__ void __launch_bounds__(Op::NW * 32, 2)
+    k_segred(typename Op::Params p, Geom g, const Carry cr0, SegGeom sg) {
+    static_assert(has_next_agg<Op>::value, "a reduce-only launch publishes the next aggregates");
+    if (Op::skip(p)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) retire_epoch(cr0);
+        return;
+    }
+    constexpr int NW = Op::NW, VEC = Op::VEC, R = Op::R, L = NW * R, CW = 32 * VEC;
+    __shared__ float sa[NW][32][VEC], sb[NW][32][VEC];
+    __shared__ uint32_t s_epoch;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Carry cr = cr0;
+    NextAgg nx = Op::next_agg(p);
+    if (threadIdx.x == 0) {
+        const uint32_t t = draw_ticket(cr);
+        ticket_drawn(cr, g, t);
+        s_epoch = cr.epoch;
+    }
+    __syncthreads();
+    nx.epoch = epoch_after(s_epoch);  // the next launch's
+    const uint64_t pol = l2_evict_first();  // every row is read once
+    const int64_t seg_rows = (int64_t)sg.seg * L, share = seg_rows / NW;
+    for (uint32_t unit = blockIdx.x; unit < sg.n_units; unit += gridDim.x) {
+        const uint32_t seg = unit / (uint32_t)g.n_ct, j = unit - seg * (uint32_t)g.n_ct;
+        TileCoord tc;
+        tc.c = (int64_t)j * CW + lane * VEC;
+        tc.cd = chan_feat(g, tc.c);
+        tc.cok = tc.c < g.C;
+        tc.acc_run = false;
+        tc.acc_flush = false;
+        const int64_t r0 = (int64_t)seg * seg_rows + warp * share;
+        float WA[VEC], WB[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { WA[v] = 1.f; WB[v] = 0.f; }
+        const GlobalSrcHint src{g.C, tc.c, pol};
+        for (int64_t k = 0; k < share; k += 2 * R) {
+            typename Op::Regs rg[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                tc.t0 = r0 + k + h * R;
+                tc.q = tc.t0 / L;
+                tc.tchunk = tc.q;
+                if (k + h * R < share && tc.t0 < g.T) Op::load(src, p, g, tc, rg[h]);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                tc.t0 = r0 + k + h * R;
+                tc.q = tc.t0 / L;
+                tc.tchunk = tc.q;
+                if (k + h * R < share && tc.t0 < g.T) {
+                    typename Op::Work w;
+                    float A[VEC], B[VEC];
+                    Op::aggregate(p, g, tc, rg[h], w, A, B, false);
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) {
+                        WB[v] = __fmaf_rn(A[v], WB[v], B[v]);
+                        WA[v] *= A[v];
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            sa[warp][lane][v] = WA[v];
+            sb[warp][lane][v] = WB[v];
+        }
+        __syncthreads();
+        if (warp == 0 && tc.cok && seg + 1 < sg.n_seg) {
+            float SA[VEC], SBv[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) { SA[v] = 1.f; SBv[v] = 0.f; }
+#pragma unroll
+            for (int w2 = 0; w2 < NW; ++w2)
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    const float a = sa[w2][lane][v];
+                    SBv[v] = __fmaf_rn(a, SBv[v], sb[w2][lane][v]);
+                    SA[v] *= a;
+                }
+#pragma unroll
+            for (int v = 0; v < VEC; ++v)
+                st_pkt2(nx.agg + 2 * ((tc.c + v) * sg.n_seg + seg), pkt(SA[v], nx.epoch),
+                        pkt(SBv[v], nx.epoch));
+        }
+        __syncthreads();  // sa / sb are rewritten by the next segment
+    }
+}
+
 template <class Op, int ST>
 __device__ __forceinline__ void seg_issue(const Geom& g, const TmaDesc& td, unsigned char* ring,
                                           uint64_t* full, uint32_t st, uint32_t q, uint32_t j,
@@ -2258,9 +2362,28 @@ cudaError_t launch_seg(const typename Op::Params& p, Geom g, const Carry& cr, cu
     sg.n_seg = (uint32_t)((g.n_chunks + seg - 1) / seg);
     sg.n_units = sg.n_seg * (uint32_t)g.n_ct;
     // The consume-only kernel takes the segments this geometry gives (the
-    // previous launch published its aggregates for them), its own grid.
-    if constexpr (has_next_agg<Op>::value)
+    // previous launch published its aggregates for them), its own grid; the
+    // reduce-only pass the streaming reduction, which needs no stages.
+    if constexpr (has_next_agg<Op>::value) {
         if (Op::next_agg(p).pre) return launch_seg1<Op>(p, g, cr, sg, td, s);
+        if (Op::next_agg(p).reduce_only && LR_SEGRED) {
+            static int occ_r[64] = {0};
+            int& orr = occ_r[dev & 63];
+            if (orr <= 0) {
+                int n = 0;
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_segred<Op>, 32 * Op::NW, 0) !=
+                        cudaSuccess ||
+                    n <= 0)
+                    n = 1;
+                orr = n;
+            }
+            const uint32_t gr = (uint32_t)std::min<uint64_t>(
+                (uint64_t)orr * (uint64_t)sm_count(), (uint64_t)std::max<uint32_t>(sg.n_units, 1u));
+            g.n_draws = gr;  // one draw per CTA
+            k_segred<Op><<<gr, 32 * Op::NW, 0, s>>>(p, g, cr, sg);
+            return cudaGetLastError();
+        }
+    }
     // walkers draw once; a segment CTA draws until one past the end
     g.n_draws = sg.n_units + grid - g.ticket_base;
     k_seg<Op, ST><<<grid, 32 * Op::NW, dyn, s>>>(p, g, cr, sg, td);
