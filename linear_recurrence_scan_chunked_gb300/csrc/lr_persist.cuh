@@ -1001,7 +1001,7 @@ __device__ __forceinline__ void look_issue(Carry& cr, const Geom& g, const TmaDe
 // tile's boxes, ST stages ahead, so that two CTAs of NW warps fit an SM and a
 // problem of up to two tiles per SM runs in one wave.
 template <class Op, int ST>
-__global__ void __launch_bounds__(Op::NW * 32, 2)
+__global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
     k_look(typename Op::Params p, Geom g, const Carry cr0, const __grid_constant__ TmaDesc td) {
     if (Op::skip(p)) {  // whole launch: before any ticket or barrier
         if (blockIdx.x == 0 && threadIdx.x == 0) retire_epoch(cr0);
@@ -1211,7 +1211,7 @@ __device__ __forceinline__ void strip_issue(const Geom& g, const TmaDesc& td, un
 // tiles in flight during the fold and the epilogue.  Otherwise a barrier at
 // the top of each tile frees the previous stage.
 template <class Op, int ST, bool ONEB>
-__global__ void __launch_bounds__(Op::NW * 32, 2)
+__global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
     k_strip(typename Op::Params p, Geom g, uint32_t* err, uint32_t G,
             const __grid_constant__ TmaDesc td) {
     if (Op::skip(p)) return;  // whole launch: before any ticket or barrier
@@ -1370,7 +1370,7 @@ struct SegGeom {
 // association is fixed by position (rows of a step in order, steps in order,
 // then the warps' shares in order).
 template <class Op>
-__global__ void __launch_bounds__(Op::NW * 32, 2)
+__global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
     k_segred(typename Op::Params p, Geom g, const Carry cr0, SegGeom sg) {
     static_assert(has_next_agg<Op>::value, "a reduce-only launch publishes the next aggregates");
     if (Op::skip(p)) {
@@ -1485,7 +1485,7 @@ struct NextPart {
 };
 
 template <class Op, int ST>
-__global__ void __launch_bounds__(Op::NW * 32, 2)
+__global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
     k_seg(typename Op::Params p, Geom g, const Carry cr0, SegGeom sg,
           const __grid_constant__ TmaDesc td) {
     if (Op::skip(p)) {  // whole launch: before any ticket or barrier
@@ -1797,7 +1797,7 @@ __global__ void __launch_bounds__(Op::NW * 32, 2)
 // out by then -- so two stages keep two tiles in flight during the fold and
 // the epilogue.
 template <class Op, int ST>
-__global__ void __launch_bounds__(Op::NW * 32, 2)
+__global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
     k_seg1(typename Op::Params p, Geom g, const Carry cr0, SegGeom sg,
            const __grid_constant__ TmaDesc td) {
     static_assert(has_next_agg<Op>::value, "a consume-only launch publishes the next aggregates");
