@@ -81,10 +81,11 @@ struct DeerOp {
         return stop;
     }
     __device__ static const S* init_ptr(const Params& p) { return p.h0; }
-    // This thread's rows and the row before them are all inside the problem
-    // and the previous iterate is staged: no per-row bounds checks.
-    __device__ static bool interior(const Params& p, const Geom& g, const TileCoord& tc) {
-        return tc.cok && tc.t0 >= 1 && tc.t0 + R <= g.T && p.yold != nullptr;
+    // This thread's rows and the row before them are all inside the problem:
+    // no per-row bounds checks (the previous iterate is staged, or it is the
+    // all-zero first guess).
+    __device__ static bool interior(const Params&, const Geom& g, const TileCoord& tc) {
+        return tc.cok && tc.t0 >= 1 && tc.t0 + R <= g.T;
     }
 
     static constexpr int TMA_N = 2;  // staged: u, previous iterate (rows t0-1 .. t0+L-1)
@@ -99,8 +100,13 @@ struct DeerOp {
     __device__ static void load(const Src& src, const Params& p, const Geom& g,
                                 const TileCoord& tc, Regs& rg) {
         if (interior(p, g, tc)) {
+            if (p.yold != nullptr) {
 #pragma unroll
-            for (int i = 0; i <= R; ++i) src.ld(rg.yo[i], 1, p.yold, tc.t0 - 1 + i);
+                for (int i = 0; i <= R; ++i) src.ld(rg.yo[i], 1, p.yold, tc.t0 - 1 + i);
+            } else {
+#pragma unroll
+                for (int i = 0; i <= R; ++i) rg.yo[i].ident(0.f);
+            }
 #pragma unroll
             for (int r = 0; r < R; ++r) src.ld(rg.u[r], 0, p.u, tc.t0 + r);
             return;
