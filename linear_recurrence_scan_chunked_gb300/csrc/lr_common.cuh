@@ -183,6 +183,17 @@ __device__ __forceinline__ void csync() {
     asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
 }
 
+// Programmatic dependent launch (sm_90+): wait until the grids this one
+// depends on have completed and their memory operations are visible; let the
+// grids that depend on this one be scheduled.  Both are no-ops for a grid
+// launched without the programmatic attribute.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------- memory ops
 
 __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {

@@ -905,6 +905,9 @@ __global__ void __maxnreg__(LR_TMA_MAXNREG)
 #ifndef LR_LOOK_PB
 #define LR_LOOK_PB 4
 #endif
+#ifndef LR_LOOK_PDL
+#define LR_LOOK_PDL 1
+#endif
 constexpr int LOOK_PB = LR_LOOK_PB;  // preceding chunks per warp per batch of loads
 
 // Warp-level: the fold of the aggregates of chunks [lo, hi) for this lane's
@@ -1003,6 +1006,12 @@ __device__ __forceinline__ void look_issue(Carry& cr, const Geom& g, const TmaDe
 template <class Op, int ST>
 __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
     k_look(typename Op::Params p, Geom g, const Carry cr0, const __grid_constant__ TmaDesc td) {
+    // Launched as a programmatic dependent of the kernel before it: its CTAs
+    // may be scheduled while that kernel still runs, and wait here until it
+    // has completed and its writes are visible (a no-op without a
+    // predecessor).  The next kernel may be scheduled as soon as this one runs.
+    griddep_wait();
+    griddep_launch_dependents();
     if (Op::skip(p)) {  // whole launch: before any ticket or barrier
         if (blockIdx.x == 0 && threadIdx.x == 0) retire_epoch(cr0);
         return;
@@ -2223,8 +2232,20 @@ cudaError_t launch_look(const typename Op::Params& p, Geom g, const Carry& cr, c
     }
     const uint32_t grid = persist_grid(g, cr, o);
     g.n_draws = g.n_tiles + grid - g.ticket_base;
-    k_look<Op, ST><<<grid, 32 * Op::NW, dyn, s>>>(p, g, cr, td);
-    return cudaGetLastError();
+    // a programmatic dependent launch: the grid is set up while the stream's
+    // previous kernel finishes (k_look waits for it before its first access)
+    cudaLaunchConfig_t lc;
+    memset(&lc, 0, sizeof lc);
+    lc.gridDim = dim3(grid);
+    lc.blockDim = dim3(32 * Op::NW);
+    lc.dynamicSmemBytes = dyn;
+    lc.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = LR_LOOK_PDL;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, k_look<Op, ST>, p, g, cr, td);
 }
 
 // Host: launch k_strip<Op, ST> when the problem has enough channel strips to
