@@ -56,7 +56,7 @@ EPS, KMAX = 1e-5, 20
 # and written by a K = 6 solve -- the reduce-only pass, iteration 1 and five
 # later iterations, captured at full size (profiles/dram_traffic.md) -- over
 # its K iteration launches.
-NCU_TRAFFIC = {"deer.solve": {"bytes": 775602645, "src": "2ef30997c35d9d2c",
+NCU_TRAFFIC = {"deer.solve": {"bytes": 775426261, "src": "a8a95e12c5db9032",
                               "file": "deer_kernels.cu"}}
 
 

@@ -250,8 +250,12 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
 #ifndef LR_WS_QD
 #define LR_WS_QD 4
 #endif
-#ifndef LR_WS_LAG
-#define LR_WS_LAG 2
+// Consume lag, in quarter rounds of the grid's tickets.  The second read of a
+// tile hits L2 more often the sooner it follows the first (at full size DRAM
+// reads were 1.31x the inputs at two rounds, 1.15x at half a round); the
+// walkers keep up at half a round.
+#ifndef LR_WS_LAG4
+#define LR_WS_LAG4 2
 #endif
 constexpr uint32_t kWsNone = 0xffffffffu;  // end of a ring or queue
 
@@ -2137,7 +2141,7 @@ cudaError_t launch_wstream(const typename Op::Params& p, Geom g, Carry cr, cudaS
     cr.n_walk = (uint32_t)n_walk;
     const uint32_t grid = persist_grid(g, cr, o);
     const uint64_t tile_bytes = (uint64_t)SB * Ly::HS;
-    uint64_t d_con = (uint64_t)LR_WS_LAG * grid;
+    uint64_t d_con = ((uint64_t)LR_WS_LAG4 * grid + 3) / 4;
     const uint64_t cap = ((uint64_t)LR_STREAM_L2MB << 20) / (tile_bytes ? tile_bytes : 1);
     if (d_con > cap) d_con = cap > 1 ? cap : 1;
     g.n_draws = cr.n_walk + g.n_tiles + (uint32_t)d_con + grid - g.ticket_base;
