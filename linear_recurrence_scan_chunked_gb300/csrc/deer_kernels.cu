@@ -143,8 +143,9 @@ struct DeerOp {
 #pragma unroll
                 for (int v = 0; v < VEC; ++v) {
                     const float yt = rg.yo[r].get(v);
-                    const float th = act_tanh(wv[v] * yt + rg.u[r].get(v));
-                    const float jac = wv[v] * (1.f - th * th);
+                    float d1;
+                    const float th = act_tanh_d(wv[v] * yt + rg.u[r].get(v), d1);
+                    const float jac = wv[v] * d1;
                     w.J[r][v] = jac;
                     w.Rh[r][v] = th - jac * yt;
                     B[v] = jac * B[v] + w.Rh[r][v];
@@ -158,8 +159,9 @@ struct DeerOp {
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
                 const float yt = rg.yo[r].get(v);
-                const float th = act_tanh(wv[v] * yt + rg.u[r].get(v));
-                const float jac = wv[v] * (1.f - th * th);
+                float d1;
+                const float th = act_tanh_d(wv[v] * yt + rg.u[r].get(v), d1);
+                const float jac = wv[v] * d1;
                 w.J[r][v] = ok ? jac : 1.f;
                 w.Rh[r][v] = ok ? th - jac * yt : 0.f;
                 B[v] = w.J[r][v] * B[v] + w.Rh[r][v];
@@ -192,8 +194,9 @@ struct DeerOp {
                 for (int v = 0; v < VEC; ++v) {
                     float yp = s[v];
                     if constexpr (sizeof(S) == 2) yp = bf_lo(bf_bits(yp));
-                    const float th = act_tanh(wv[v] * yp + rg.u[r].get(v));
-                    const float jac = wv[v] * (1.f - th * th);
+                    float d1;
+                    const float th = act_tanh_d(wv[v] * yp + rg.u[r].get(v), d1);
+                    const float jac = wv[v] * d1;
                     w.NB[v] = jac * w.NB[v] + (th - jac * yp);
                     w.NA[v] *= jac;
                     s[v] = w.J[r][v] * s[v] + w.Rh[r][v];
@@ -219,8 +222,9 @@ struct DeerOp {
                 for (int v = 0; v < VEC; ++v) {
                     float yp = s[v];
                     if constexpr (sizeof(S) == 2) yp = bf_lo(bf_bits(yp));
-                    const float th = act_tanh(wv[v] * yp + rg.u[r].get(v));
-                    const float jac = wv[v] * (1.f - th * th);
+                    float d1;
+                    const float th = act_tanh_d(wv[v] * yp + rg.u[r].get(v), d1);
+                    const float jac = wv[v] * d1;
                     w.NB[v] = jac * w.NB[v] + (th - jac * yp);
                     w.NA[v] *= jac;
                 }

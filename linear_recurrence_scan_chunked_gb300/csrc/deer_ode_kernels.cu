@@ -84,8 +84,9 @@ struct DeerOdeOp {
     // entering the step), the input and the step length: clamps G, counts it.
     __device__ static void coeffs(float wv, float yt, float uv, float dtt, float& a, float& b,
                                   uint32_t& ncl) {
-        const float th = act_tanh(wv * yt + uv);
-        float gv = 1.f - wv * (1.f - th * th);
+        float d1;
+        const float th = act_tanh_d(wv * yt + uv, d1);
+        float gv = 1.f - wv * d1;
         if (gv > kOdeGClamp) {  // (a NaN fails both tests and stays NaN)
             gv = kOdeGClamp;
             ++ncl;

@@ -7,7 +7,9 @@
 //
 // Both are written from their exponential forms,
 //     sigmoid(z) = 1 / (1 + 2^{-z log2 e}),
-//     tanh(x)    = sign(x) (1 - 2 / (2^{2 |x| log2 e} + 1)),
+//     tanh(x)    = 1 - 2 r,  r = 1 / (2^{2 x log2 e} + 1),
+// and the derivative of tanh from the same r, 1 - tanh^2 = 4 r (1 - r), free of
+// the cancellation of 1 - tanh^2 where tanh saturates;
 // with the power of two and the reciprocal taken from the hardware's
 // approximate instructions (ex2.approx, rcp.approx) in their flush-to-zero
 // forms: one instruction each, with no extra steps for subnormal results,
@@ -46,9 +48,16 @@ __device__ __forceinline__ float act_sigmoid(float z) {
     return rcp_ftz(1.f + ex2_ftz(-kLog2e * z));
 }
 
+// tanh(x) keeps its sign for x < 0 (r > 1/2 there) and saturates to -1 (the
+// power flushes to 0) and +1 (an infinite power gives r = 0).
 __device__ __forceinline__ float act_tanh(float x) {
-    const float t = fmaf(-2.f, rcp_ftz(ex2_ftz(kTwoLog2e * fabsf(x)) + 1.f), 1.f);
-    return copysignf(t, x);
+    return fmaf(-2.f, rcp_ftz(ex2_ftz(kTwoLog2e * x) + 1.f), 1.f);
+}
+// tanh(x), and in d its derivative 1 - tanh(x)^2.
+__device__ __forceinline__ float act_tanh_d(float x, float& d) {
+    const float r = rcp_ftz(ex2_ftz(kTwoLog2e * x) + 1.f);
+    d = 4.f * fmaf(-r, r, r);
+    return fmaf(-2.f, r, 1.f);
 }
 
 // e^x - 1 without the cancellation of e^x - 1 near 0 (DEER's ODE form,

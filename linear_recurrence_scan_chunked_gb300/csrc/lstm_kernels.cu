@@ -257,12 +257,13 @@ struct LstmBwdOp {
             for (int v = 0; v < VEC; ++v) {
                 const float f = act_sigmoid(rg.zf[r].get(v) + bfv[v]);
                 const float o = act_sigmoid(rg.zo[r].get(v) + bov[v]);
-                const float th = act_tanh(rg.c[r].get(v));
+                float d1;
+                const float th = act_tanh_d(rg.c[r].get(v), d1);
                 const float gv = rg.dh[r].get(v);
                 dzov[v] = gv * th * o * (1.f - o);
                 if (ok) w.sum_o[v] += dzov[v];
                 w.F[r][v] = ok ? f : 1.f;
-                w.E[r][v] = ok ? gv * o * (1.f - th * th) : 0.f;
+                w.E[r][v] = ok ? gv * o * d1 : 0.f;
                 B[v] = w.F[r][v] * (w.E[r][v] + B[v]);
                 A[v] *= w.F[r][v];
             }

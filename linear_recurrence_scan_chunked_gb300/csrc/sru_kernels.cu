@@ -244,13 +244,14 @@ struct SruBwdOp {
             for (int v = 0; v < VEC; ++v) {
                 const float f = act_sigmoid(rg.uf[r].get(v) + bfv[v]);
                 const float rg_ = act_sigmoid(rg.ur[r].get(v) + brv[v]);
-                const float th = act_tanh(rg.c[r].get(v));
+                float d1;
+                const float th = act_tanh_d(rg.c[r].get(v), d1);
                 const float gv = rg.dh[r].get(v);
                 durv[v] = gv * (th - rg.x[r].get(v)) * rg_ * (1.f - rg_);
                 dxv[v] = gv * (1.f - rg_);
                 if (ok) w.sum_r[v] += durv[v];
                 w.F[r][v] = ok ? f : 1.f;
-                w.E[r][v] = ok ? gv * rg_ * (1.f - th * th) : 0.f;
+                w.E[r][v] = ok ? gv * rg_ * d1 : 0.f;
                 w.XT[r][v] = rg.xt[r].get(v);
                 w.CP[r][v] = rg.cp[r].get(v);
                 B[v] = w.F[r][v] * (w.E[r][v] + B[v]);
