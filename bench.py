@@ -56,7 +56,7 @@ EPS, KMAX = 1e-5, 20
 # and written by a K = 6 solve -- the reduce-only pass, iteration 1 and five
 # later iterations, captured at full size (profiles/dram_traffic.md) -- over
 # its K iteration launches.
-NCU_TRAFFIC = {"deer.solve": {"bytes": 775426261, "src": "a8a95e12c5db9032",
+NCU_TRAFFIC = {"deer.solve": {"bytes": 775166827, "src": "55aa5dee9db45693",
                               "file": "deer_kernels.cu"}}
 
 
