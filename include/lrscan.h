@@ -111,8 +111,9 @@ typedef enum {
  * h_{-1} = h0.  [P1] parallel-scan paragraph; [P2] LSTM paragraph.
  * Chunks of time rows are scanned in parallel; the state entering each chunk
  * comes from the chunk aggregates published before it (a look-back over all
- * of them for short problems, walker CTAs for long ones, a CTA walking its
- * channel strip through time for wide ones).
+ * of them for short problems, walkers -- whole CTAs, or one warp in each CTA
+ * of the warp-specialised kernel -- for long ones, a CTA walking its channel
+ * strip through time for wide ones).
  *   a, b : [T,B,D] in   coefficients and inputs
  *   h0   : [B,D]   in   initial state; NULL means zeros
  *   h    : [T,B,D] out  states (h0 is not repeated in h)
@@ -359,13 +360,15 @@ int64_t lr_workspace_bytes(void);
 
 /*
  * Test hook for the bounded carry waits: launches both chain-protocol
- * forward scan kernels (register and TMA-staged) on a private 2-chunk problem
- * whose first chunk is never published, one CTA each, and the walker-protocol
- * kernels (register, fp32; segmented, bf16; consume-only segmented, a fp32
- * DEER iteration whose aggregates count as published) on a private long
- * problem with no walker CTAs, so no entering state is ever published.  Every wait is limited
- * to `spin_limit` polls and runs out.  It leaves LR_ERR_TIMEOUT in the device
- * error word.  Nothing faults or hangs.
+ * forward scan kernels (register and TMA-staged) and the look-back kernel on
+ * private 2-chunk problems whose first chunk is never published, one CTA
+ * each, and the walker-protocol kernels (the register one on the fp32 scalar
+ * path, the warp-specialised one on the fp32 vector path, the segmented one
+ * for a bf16 backward scan, and its consume-only form for a fp32 DEER
+ * iteration whose aggregates count as published) on a private long problem
+ * with no walkers, so no entering state is ever published.  Every wait is
+ * limited to `spin_limit` polls and runs out.  It leaves LR_ERR_TIMEOUT in
+ * the device error word.  Nothing faults or hangs.
  */
 int lr_test_lookback_timeout(uint32_t spin_limit, void* stream);
 

@@ -942,10 +942,10 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
     // of two time chunks and one channel tile, each with one CTA that is handed
     // tile 1: it waits for the state after tile 0, which nobody publishes.
     // Look-back protocol: the same, tile 1 waits for tile 0's aggregate.
-    // Walker protocol: the register walker kernel (vector and scalar paths),
-    // the segmented walker kernel and its consume-only form, on a long
-    // one-strip problem launched without walker CTAs: no entering state is
-    // ever published, so every consume's wait runs out.
+    // Walker protocol: the register walker kernel (scalar path), the
+    // warp-specialised one (vector path), the segmented walker kernel and its
+    // consume-only form, on a long one-strip problem launched without walkers:
+    // no entering state is ever published, so every consume's wait runs out.
     const int64_t C = tile_shape(OP_SCAN_FWD, LR_F32, true, CARRY_CHAIN).CW;
     const int64_t Tw = 8192;  // >= 128 chunks of both walker tile shapes
     if (!ws->test_buf) {
@@ -982,7 +982,7 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
         CK(launch_scan_fwd(LR_F32, true, a, a + Tw * C, nullptr, (float*)buf + 2 * Tw * C, g, cr,
                            s));
     }
-    for (int vec = 0; vec < 2; ++vec) {  // fp32 forward: register walker, scalar and vector paths
+    for (int vec = 0; vec < 2; ++vec) {  // fp32 forward: register walker (scalar), warp-specialised (vector)
         Geom g;
         Carry cr;
         TRY(plan(*ws, OP_SCAN_FWD, LR_F32, vec == 1, Tw, C, C, &g, &cr, s, 0));
