@@ -26,6 +26,10 @@
 #ifndef LR_SEG_L2MB
 #define LR_SEG_L2MB 160
 #endif
+// The same sizing for the DEER iterations' segments (no second read).
+#ifndef LR_SEG1_L2MB
+#define LR_SEG1_L2MB 320
+#endif
 
 // The fused forward cells (SRU, LSTM) run the strip kernel with one barrier
 // per tile (their backward kernels would not keep two CTAs per SM with the

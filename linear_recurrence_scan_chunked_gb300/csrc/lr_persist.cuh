@@ -2378,7 +2378,14 @@ cudaError_t launch_seg(const typename Op::Params& p, Geom g, const Carry& cr, cu
     const uint32_t grid = persist_grid(g, cr, o);
     const uint64_t tile_ctas = grid > cr.n_walk ? grid - cr.n_walk : 1;
     // SEG_LAG + 1 segments per CTA are in L2 at a time
-    uint64_t seg = ((uint64_t)LR_SEG_L2MB << 20) / ((SEG_LAG + 1) * tile_ctas * SB);
+    // (launches that publish the next launch's aggregates -- the DEER
+    // iterations, consume-only and read once -- size their segments for the
+    // walkers' and the tickets' overheads, not for L2 residency, and in rows:
+    // bf16 stages count as fp32 ones)
+    constexpr bool NXT = has_next_agg<Op>::value;
+    const uint64_t budget = NXT ? LR_SEG1_L2MB : LR_SEG_L2MB;
+    const uint64_t sb = NXT ? (uint64_t)SB * 4 / sizeof(typename Op::S) : (uint64_t)SB;
+    uint64_t seg = (budget << 20) / ((SEG_LAG + 1) * tile_ctas * sb);
     if (seg < (uint64_t)ST) seg = ST;  // the ring's look-ahead stays within one iteration
     if (seg < 2) seg = 2;
     if (seg > 64) seg = 64;
