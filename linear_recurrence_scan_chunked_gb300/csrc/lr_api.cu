@@ -234,10 +234,10 @@ int count_launch(DevWS& ws, cudaStream_t s, uint64_t n = 1) {
 // choice, and chain = true the chain protocol (the timeout test covers every
 // kernel).
 int plan(DevWS& ws, Op op, int dtype, bool vec, int64_t T, int64_t C, int64_t D, Geom* g,
-         Carry* cr, cudaStream_t s, int tma = -1, bool chain = false) {
+         Carry* cr, cudaStream_t s, int tma = -1, bool chain = false, bool cluster = true) {
     const bool want_tma = tma < 0 ? use_tma(dtype, vec, T, C) : (tma == 1);
     const CarryPlan cp = chain ? chain_plan(op, dtype, vec, want_tma, T, C)
-                               : carry_plan(op, dtype, vec, want_tma, T, C);
+                               : carry_plan(op, dtype, vec, want_tma, T, C, cluster);
     const TileShape ts = cp.ts;
     g->T = T;
     g->C = C;
@@ -973,7 +973,7 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
         const int64_t T = 2 * tile_shape(OP_SCAN_FWD, LR_F32, true, TILE_TMA).L;
         Geom g;
         Carry cr;
-        TRY(plan(*ws, OP_SCAN_FWD, LR_F32, true, T, C, C, &g, &cr, s, 1));
+        TRY(plan(*ws, OP_SCAN_FWD, LR_F32, true, T, C, C, &g, &cr, s, 1, false, false));
         if (cr.mode != CARRY_LOOK) return LR_ERR_INVALID_ARG;
         g.max_grid = 1;
         g.ticket_base = 1;

@@ -61,6 +61,7 @@ constexpr uint32_t ERRBIT_TIMEOUT = 1u;
 constexpr int CARRY_CHAIN = 0;
 constexpr int CARRY_WALK = 1;
 constexpr int CARRY_LOOK = 2;
+constexpr int CARRY_CLUSTER = 3;  // one thread-block cluster per channel tile (short problems)
 constexpr int WALK_MAX_WV = 4;  // channels per walker warp (upper bound)
 constexpr int WALK_P = 4;       // consecutive chunks per walker lane
 
@@ -89,7 +90,7 @@ struct Carry {
     uint32_t epoch;       // this launch's epoch (1 .. 2^32-1): set on the device
                           // from the ticket word by each CTA's first draw
     uint32_t spin_limit;  // polls before a wait gives up
-    int mode;             // CARRY_CHAIN, CARRY_WALK or CARRY_LOOK
+    int mode;             // CARRY_CHAIN, CARRY_WALK, CARRY_LOOK or CARRY_CLUSTER
     uint32_t n_walk;      // walker CTAs (first tickets); 0 in CHAIN / LOOK mode
     int wv;               // channels per walker warp (WALK)
     int tma;              // CHAIN: tiles are staged by TMA (k_strip / k_tchain)

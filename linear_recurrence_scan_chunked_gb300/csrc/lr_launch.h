@@ -80,7 +80,8 @@ enum Op {
 // CTAs per SM.  The TMA kernel keeps one tile in registers and ST in shared
 // memory (about 96 KB of stages per CTA, two CTAs per SM).  One table, used
 // both to instantiate the kernels and to size the workspace.
-constexpr int TILE_TMA = 2;  // kcfg row of the TMA-staged chain kernel
+constexpr int TILE_TMA = 2;      // kcfg row of the TMA-staged chain kernel
+constexpr int TILE_CLUSTER = 3;  // kcfg row of the cluster kernel
 struct KCfg {
     int NW;
     int R;
@@ -94,7 +95,8 @@ constexpr KCfg kcfg(Op op, int dtype, int mode) {
     // as the SRU cell and takes its rows; DEER's ODE form takes the tanh
     // form's rows at eight warps per CTA (its heavier producer measured slower
     // with four).
-    return op == OP_DEER_ODE   ? KCfg{8, mode == CARRY_CHAIN ? 2 : 4, mode == TILE_TMA ? 3 : 0}
+    return mode == TILE_CLUSTER ? KCfg{8, 16, 0}  // one channel per lane, 128 rows per CTA
+           : op == OP_DEER_ODE   ? KCfg{8, mode == CARRY_CHAIN ? 2 : 4, mode == TILE_TMA ? 3 : 0}
            : op == OP_DEER && dtype == 1 ? kcfg(OP_DEER, 0, mode)
            : op == OP_LSTM_FWD ? kcfg(OP_SRU_FWD, dtype, mode)
            : op == OP_LSTM_BWD ? kcfg(OP_SRU_BWD, dtype, mode)
@@ -122,11 +124,19 @@ constexpr KCfg kcfg(Op op, int dtype, int mode) {
 // 4 channels per lane: 16-byte fp32 / 8-byte bf16 accesses, 128 channels per tile
 constexpr int kvec(int dtype, bool vec) { return vec ? 4 : 1; }
 
-// mode: CARRY_CHAIN, CARRY_WALK or TILE_TMA (chain protocol, TMA staging)
+// mode: CARRY_CHAIN, CARRY_WALK, TILE_TMA (chain protocol, TMA staging) or
+// TILE_CLUSTER (one channel per lane on both paths: a warp's row is 32
+// consecutive channels, one coalesced access, and no alignment is needed)
 inline TileShape tile_shape(Op op, int dtype, bool vec, int mode) {
     const KCfg k = kcfg(op, dtype, mode);
-    return TileShape{k.NW * k.R, 32 * kvec(dtype, vec), 32 * k.NW};
+    return TileShape{k.NW * k.R, 32 * (mode == TILE_CLUSTER ? 1 : kvec(dtype, vec)), 32 * k.NW};
 }
+
+// The cluster kernel: at most this many time chunks (CTAs per cluster, the
+// portable limit), so problems of up to kClusterMax * 128 steps.  The scans
+// have a cluster form; the cells and DEER keep their protocols.
+constexpr int kClusterMax = 8;
+constexpr bool cluster_op(Op op) { return op == OP_SCAN_FWD || op == OP_SCAN_BWD; }
 
 // The chain protocol stages its tiles with TMA when the vector path applies
 // and the rows of the [T, C] sequence are 16-byte multiples (tensor-map
@@ -148,7 +158,9 @@ inline bool use_tma(int dtype, bool vec, int64_t T, int64_t C) {
 }
 
 // Which carry protocol a launch uses, its tile shape, and the packet storage
-// it needs.  WALK pays off once the chunk chain is long (a round trip per
+// it needs.  CLUSTER when every time chunk of a channel tile fits one
+// thread-block cluster (the scans of up to kClusterMax * 128 steps: no packets
+// at all).  WALK pays off once the chunk chain is long (a round trip per
 // chunk level would dominate) and the channels are few enough for a handful
 // of walker CTAs; LOOK when the problem is short enough for every tile to
 // fold all the chunk aggregates before it (TMA path); otherwise CHAIN (the
@@ -156,7 +168,7 @@ inline bool use_tma(int dtype, bool vec, int64_t T, int64_t C) {
 // given problem always gets the same association of its floating-point
 // operations.
 struct CarryPlan {
-    int mode;          // CARRY_CHAIN / CARRY_WALK / CARRY_LOOK
+    int mode;          // CARRY_CHAIN / CARRY_WALK / CARRY_LOOK / CARRY_CLUSTER
     bool tma;          // CHAIN: a TMA-staged kernel runs it (strip / TMA chain)
     TileShape ts;      // tile shape of that protocol
     int64_t n_chunks;  // ceil(T / ts.L)
@@ -192,8 +204,24 @@ inline CarryPlan chain_plan(Op op, int dtype, bool vec, bool tma, int64_t T, int
     return p;
 }
 
-inline CarryPlan carry_plan(Op op, int dtype, bool vec, bool tma, int64_t T, int64_t C) {
+inline CarryPlan carry_plan(Op op, int dtype, bool vec, bool tma, int64_t T, int64_t C,
+                            bool cluster = true) {
     CarryPlan p{};
+    if (cluster && cluster_op(op)) {  // short problems: one cluster per channel tile
+        const TileShape tk = tile_shape(op, dtype, vec, TILE_CLUSTER);
+        const int64_t nk = (T + tk.L - 1) / tk.L;
+        if (nk >= 1 && nk <= kClusterMax) {
+            p.mode = CARRY_CLUSTER;
+            p.tma = false;
+            p.ts = tk;
+            p.n_chunks = nk;
+            p.n_walk = 0;
+            p.wv = 0;
+            p.inc_elems = 0;
+            p.agg_elems = 0;
+            return p;
+        }
+    }
     tma = tma && vec;
     // the TMA kernels (segmented walker, strip, TMA chain) use the TMA tile shape
     const int wmode = tma && seg_walk(op, dtype) ? TILE_TMA : CARRY_WALK;

@@ -981,18 +981,11 @@ __device__ __forceinline__ void look_fold(const Carry& cr, const Geom& g, uint32
     }
 }
 
-// Thread 0 of a look-back CTA: draw the next ticket (tile, or past the end)
-// into s_tile[st] and, for a tile, issue its boxes into stage st.
+// Thread 0 of a look-back CTA: issue the boxes of `tile` into stage st.
 template <class Op>
-__device__ __forceinline__ void look_issue(Carry& cr, const Geom& g, const TmaDesc& td,
-                                           unsigned char* ring, uint64_t* full, uint32_t* s_tile,
-                                           uint32_t st) {
+__device__ __forceinline__ void look_load(const Geom& g, const TmaDesc& td, unsigned char* ring,
+                                          uint64_t* full, uint32_t tile, uint32_t st) {
     constexpr int L = Op::NW * Op::R, CW = 32 * Op::VEC;
-    const uint32_t t = draw_ticket(cr);
-    ticket_drawn(cr, g, t);
-    const uint32_t tile = t + g.ticket_base;
-    s_tile[st] = tile;
-    if (tile >= g.n_tiles) return;
     const int64_t q = tile / g.n_ct, j = tile % g.n_ct;
     const int64_t tchunk = Op::REV ? g.n_chunks - 1 - q : q;
     const int32_t x = (int32_t)(j * CW), y0 = (int32_t)(tchunk * L);
@@ -1004,22 +997,35 @@ __device__ __forceinline__ void look_issue(Carry& cr, const Geom& g, const TmaDe
             tma_load_2d(dst + tma_off<Op>(a), &td.map[a], x, y0 + Op::tma_shift(a), &full[st]);
 }
 
+// Thread 0 of a look-back CTA: draw the next ticket (tile, or past the end)
+// into s_tile[st] and, for a tile, issue its boxes into stage st.
+template <class Op>
+__device__ __forceinline__ void look_issue(Carry& cr, const Geom& g, const TmaDesc& td,
+                                           unsigned char* ring, uint64_t* full, uint32_t* s_tile,
+                                           uint32_t st) {
+    const uint32_t t = draw_ticket(cr);
+    ticket_drawn(cr, g, t);
+    const uint32_t tile = t + g.ticket_base;
+    s_tile[st] = tile;
+    if (tile < g.n_tiles) look_load<Op>(g, td, ring, full, tile, st);
+}
+
 // No producer warp: thread 0 draws the tickets (in order) and issues each
 // tile's boxes, ST stages ahead, so that two CTAs of NW warps fit an SM and a
 // problem of up to two tiles per SM runs in one wave.
+//
+// When the host sized the grid to one tile per CTA (g.n_draws == gridDim.x),
+// the tile is the block index and its boxes are issued as soon as the kernel
+// before has completed: no ticket stands between the dependency wait and the
+// load, and the CTAs do not queue on one atomic before they start.  The epoch
+// comes from a plain load of the ticket word, issued beside the boxes; each CTA
+// then draws one arrival ticket on the same word (after that load, in the
+// word's coherence order), and the last arrival retires the epoch when its CTA
+// ends.  A tile waits only for tiles of smaller block index, which the
+// hardware dispatches first; every one of them is resident in the same wave.
 template <class Op, int ST>
 __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
     k_look(typename Op::Params p, Geom g, const Carry cr0, const __grid_constant__ TmaDesc td) {
-    // Launched as a programmatic dependent of the kernel before it: its CTAs
-    // may be scheduled while that kernel still runs, and wait here until it
-    // has completed and its writes are visible (a no-op without a
-    // predecessor).  The next kernel may be scheduled as soon as this one runs.
-    griddep_wait();
-    griddep_launch_dependents();
-    if (Op::skip(p)) {  // whole launch: before any ticket or barrier
-        if (blockIdx.x == 0 && threadIdx.x == 0) retire_epoch(cr0);
-        return;
-    }
     constexpr int NW = Op::NW, VEC = Op::VEC, L = Op::NW * Op::R;
     constexpr uint32_t SB = tma_stage_bytes<Op>();
     extern __shared__ unsigned char dyn_smem[];
@@ -1032,17 +1038,46 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
     __shared__ __align__(8) uint64_t full[ST];
     __shared__ uint32_t s_tile[ST];
     __shared__ uint32_t s_abort, s_epoch;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    Carry cr = cr0;
-    bool drawing = true;  // thread 0: no ticket past the end drawn yet
-    uint32_t issued = 0;  // thread 0: stage uses whose ticket was drawn
+    // Before the dependency wait, only what the kernel before cannot have
+    // written: the stage barriers and the tensor maps (kernel parameters).
     if (threadIdx.x == 0) {
         for (int i = 0; i < ST; ++i) mbar_init(&full[i], 1);
         s_abort = 0;
         mbar_init_fence();
-        for (; issued < (uint32_t)ST && drawing; ++issued) {
-            look_issue<Op>(cr, g, td, ring, full, s_tile, issued);
-            if (s_tile[issued] >= g.n_tiles) drawing = false;
+#pragma unroll
+        for (int a = 0; a < Op::TMA_N; ++a)
+            if (td.present & (1u << a)) tma_prefetch_desc(&td.map[a]);
+    }
+    // Launched as a programmatic dependent of the kernel before it: its CTAs
+    // may be scheduled while that kernel still runs, and wait here until it
+    // has completed and its writes are visible (a no-op without a
+    // predecessor).  The next kernel may be scheduled as soon as this one runs.
+    griddep_wait();
+    griddep_launch_dependents();
+    if (Op::skip(p)) {  // whole launch: before any ticket or barrier
+        if (blockIdx.x == 0 && threadIdx.x == 0) retire_epoch(cr0);
+        return;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool one = g.n_draws == gridDim.x;  // one tile per CTA, in block order
+    Carry cr = cr0;
+    bool drawing = true;     // thread 0: no ticket past the end drawn yet
+    uint32_t issued = 0;     // thread 0: stage uses whose ticket was drawn
+    unsigned long long arrival = 0;  // thread 0, one tile per CTA: the arrival draw
+    if (threadIdx.x == 0) {
+        if (one) {
+            const uint32_t tile = blockIdx.x + g.ticket_base;
+            s_tile[0] = tile;
+            if (tile < g.n_tiles) look_load<Op>(g, td, ring, full, tile, 0);
+            issued = 1;
+            drawing = false;
+            cr.epoch = epoch_after((uint32_t)(ld_pkt(cr.tk) >> 32));
+            arrival = atomicAdd(reinterpret_cast<unsigned long long*>(cr.tk), 1ull);
+        } else {
+            for (; issued < (uint32_t)ST && drawing; ++issued) {
+                look_issue<Op>(cr, g, td, ring, full, s_tile, issued);
+                if (s_tile[issued] >= g.n_tiles) drawing = false;
+            }
         }
         for (uint32_t i = issued; i < (uint32_t)ST; ++i) s_tile[i] = 0xffffffffu;
         s_epoch = cr.epoch;
@@ -1104,6 +1139,13 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
                     PB[v] = __fmaf_rn(a, PB[v], sm.b[w2][lane][v]);
                     PA[v] *= a;
                 }
+        // the state before the first chunk, loaded now so that its round trip
+        // runs beside the look-back
+        float s[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) s[v] = 0.f;
+        const typename Op::S* ip = Op::init_ptr(p);
+        if (ip != nullptr && tc.cok) load_vec<typename Op::S, VEC>(ip + tc.c, s);
         csync<NW>();  // sm is free for the look-back
         // 2. this warp's share of the preceding chunks
         const uint32_t q = (uint32_t)tc.q;
@@ -1119,11 +1161,6 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
             }
         }
         csync<NW>();
-        float s[VEC];
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) s[v] = 0.f;
-        const typename Op::S* ip = Op::init_ptr(p);
-        if (ip != nullptr && tc.cok) load_vec<typename Op::S, VEC>(ip + tc.c, s);
 #pragma unroll
         for (int w2 = 0; w2 < NW; ++w2)
             if ((uint64_t)q * (w2 + 1) / NW > (uint64_t)q * w2 / NW)  // a non-empty share
@@ -1157,9 +1194,107 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
         csync<NW>();
     }
     Op::at_exit(p, xs, acc);
-    if (threadIdx.x == 0)  // after an early stop: copies still in flight land first
+    if (threadIdx.x == 0) {
+        // after an early stop: copies still in flight land first
         for (uint32_t i = k; i < issued; ++i)
             if (s_tile[i % ST] < g.n_tiles) mbar_wait(&full[i % ST], (i / ST) & 1u, cr.err);
+        if (one) ticket_drawn(cr, g, (uint32_t)arrival);  // the last arrival retires the epoch
+    }
+}
+
+// Cluster kernel (short problems): the CTAs of one thread-block cluster take
+// the time chunks of one channel tile, chunk q on the CTA of rank q.  Each CTA
+// loads its rows into registers, forms its chunk's aggregate (the composition
+// of the affine maps of its rows), and writes it into the shared memory of every
+// CTA after it in the cluster; after one cluster barrier each CTA folds the
+// aggregates of the chunks before its own, in chunk order, into the state that
+// enters its chunk, and writes its outputs.  Nothing goes through global memory
+// but the inputs and outputs: no packets, tickets or epochs, and no CTA waits
+// for another cluster, so clusters may run in any order and any number of waves.
+// The association of every operation is fixed by the chunk and warp indices:
+// the result is bitwise reproducible.
+template <class Op, int CL>
+__global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
+    k_cluster(typename Op::Params p, Geom g) {
+    constexpr int NW = Op::NW, VEC = Op::VEC;
+    // skip depends on the arguments only: the whole launch returns here,
+    // before any barrier
+    if (Op::skip(p)) return;
+    __shared__ StripSmem<VEC, NW> sm;  // the warps' aggregates of this chunk
+    __shared__ float ca[CL][32 * VEC], cb[CL][32 * VEC];  // aggregates of the chunks before it
+    __shared__ typename Op::Smem xs;
+    // the first cluster barrier phase: every CTA of the cluster runs before
+    // any CTA writes into another's shared memory
+    cluster_arrive_relaxed();
+    // a programmatic dependent launch, as k_look
+    griddep_wait();
+    griddep_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t q = cluster_rank(), n = cluster_ctas();
+    const TileCoord tc = tile_coord_qj<Op>(g, q, blockIdx.x / n);
+    float s[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) s[v] = 0.f;
+    const typename Op::S* ip = Op::init_ptr(p);
+    if (ip != nullptr && tc.cok) load_vec<typename Op::S, VEC>(ip + tc.c, s);
+    typename Op::Regs regs;
+    typename Op::Work w;
+    typename Op::Acc acc;
+    Op::acc_init(acc);
+    Op::load(GlobalSrc{g.C, tc.c}, p, g, tc, regs);
+    {
+        float A[VEC], B[VEC];
+        Op::aggregate(p, g, tc, regs, w, A, B, false);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            sm.a[warp][lane][v] = A[v];
+            sm.b[warp][lane][v] = B[v];
+        }
+    }
+    csync<NW>();
+    cluster_wait();  // the first phase
+    if (warp == 0 && q + 1 < n) {  // the chunk's aggregate, to the CTAs after this one
+        float TA[VEC], TB[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { TA[v] = 1.f; TB[v] = 0.f; }
+#pragma unroll
+        for (int w2 = 0; w2 < NW; ++w2)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                const float a = sm.a[w2][lane][v];
+                TB[v] = __fmaf_rn(a, TB[v], sm.b[w2][lane][v]);
+                TA[v] *= a;
+            }
+        for (uint32_t d = q + 1; d < n; ++d)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                st_cluster_f32(&ca[q][lane * VEC + v], d, TA[v]);
+                st_cluster_f32(&cb[q][lane * VEC + v], d, TB[v]);
+            }
+    }
+    cluster_arrive_release();
+    // the warps before this one within the chunk, while the barrier completes
+    float PA[VEC], PB[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) { PA[v] = 1.f; PB[v] = 0.f; }
+#pragma unroll
+    for (int w2 = 0; w2 < NW - 1; ++w2)
+        if (w2 < warp)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                const float a = sm.a[w2][lane][v];
+                PB[v] = __fmaf_rn(a, PB[v], sm.b[w2][lane][v]);
+                PA[v] *= a;
+            }
+    cluster_wait();  // the second phase: every earlier chunk's aggregate is here
+#pragma unroll 1
+    for (uint32_t d = 0; d < q; ++d)
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) s[v] = __fmaf_rn(ca[d][lane * VEC + v], s[v], cb[d][lane * VEC + v]);
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) s[v] = __fmaf_rn(PA[v], s[v], PB[v]);
+    Op::finish(p, g, tc, regs, w, s, xs, acc);
+    Op::at_exit(p, xs, acc);
 }
 
 // The op's scratch in the TMA strip and segmented kernels: its own space, or
@@ -2234,8 +2369,16 @@ cudaError_t launch_look(const typename Op::Params& p, Geom g, const Carry& cr, c
             n = 1;
         o = n;
     }
-    const uint32_t grid = persist_grid(g, cr, o);
-    g.n_draws = g.n_tiles + grid - g.ticket_base;
+    uint32_t grid = persist_grid(g, cr, o);
+    // every tile fits one wave: one tile per CTA, in block order, and one
+    // arrival draw each; otherwise tickets (every CTA also draws one past the end)
+    const uint32_t need = g.n_tiles - g.ticket_base;
+    if (need > 0 && grid >= need) {
+        grid = need;
+        g.n_draws = grid;
+    } else {
+        g.n_draws = g.n_tiles + grid - g.ticket_base;
+    }
     // a programmatic dependent launch: the grid is set up while the stream's
     // previous kernel finishes (k_look waits for it before its first access)
     cudaLaunchConfig_t lc;
@@ -2250,6 +2393,32 @@ cudaError_t launch_look(const typename Op::Params& p, Geom g, const Carry& cr, c
     lc.attrs = at;
     lc.numAttrs = 1;
     return cudaLaunchKernelEx(&lc, k_look<Op, ST>, p, g, cr, td);
+}
+
+// Host: launch k_cluster<Op, CL> (one cluster of n_chunks <= CL CTAs per
+// channel tile), as a programmatic dependent of the stream's previous kernel.
+template <class Op>
+cudaError_t launch_cluster(const typename Op::Params& p, const Geom& g, cudaStream_t s) {
+    constexpr int CL = kClusterMax;
+    if (g.n_chunks < 1 || g.n_chunks > CL || g.n_ct < 1) return cudaErrorInvalidValue;
+    const uint64_t grid = (uint64_t)g.n_ct * (uint64_t)g.n_chunks;
+    if (grid > 0x7fffffffu) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t lc;
+    memset(&lc, 0, sizeof lc);
+    lc.gridDim = dim3((unsigned)grid);
+    lc.blockDim = dim3(32 * Op::NW);
+    lc.dynamicSmemBytes = 0;
+    lc.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)g.n_chunks;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = LR_LOOK_PDL;
+    lc.attrs = at;
+    lc.numAttrs = 2;
+    return cudaLaunchKernelEx(&lc, k_cluster<Op, CL>, p, g);
 }
 
 // Host: launch k_strip<Op, ST> when the problem has enough channel strips to
@@ -2422,15 +2591,20 @@ cudaError_t launch_seg(const typename Op::Params& p, Geom g, const Carry& cr, cu
     return cudaGetLastError();
 }
 
-// Host: launch the kernel of the launch's carry protocol; OpC / OpW / OpT are
-// the operation instantiated with the tile shapes of the register chain, the
-// walker and the TMA-staged kernels (strip, TMA chain).
-template <class OpC, class OpW, class OpT, int ST>
+// Host: launch the kernel of the launch's carry protocol; OpC / OpW / OpT / OpK
+// are the operation instantiated with the tile shapes of the register chain,
+// the walker, the TMA-staged kernels (strip, TMA chain) and the cluster kernel
+// (void: the operation has no cluster form, and its plans never pick one).
+template <class OpC, class OpW, class OpT, int ST, class OpK = void>
 cudaError_t launch_persist(const typename OpC::Params& p, const Geom& g, const Carry& cr,
                            cudaStream_t s) {
     static_assert(std::is_same<typename OpC::Params, typename OpW::Params>::value &&
                       std::is_same<typename OpC::Params, typename OpT::Params>::value,
                   "all instantiations take the same arguments");
+    if (cr.mode == CARRY_CLUSTER) {
+        if constexpr (std::is_void<OpK>::value) return cudaErrorNotSupported;
+        else return launch_cluster<OpK>(p, g, s);
+    }
     if (cr.mode == CARRY_LOOK) return launch_look<OpT>(p, g, cr, s);
     if (cr.mode == CARRY_CHAIN) {
         if (cr.tma) {

@@ -126,6 +126,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int
         : "memory");
 }
 
+// Bring a tensor map (a __grid_constant__ kernel parameter) into the
+// descriptor cache ahead of its first copy.
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
 // As tma_load_2d, with an L2 eviction-priority policy (createpolicy) for the
 // lines it reads.
 __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m, int32_t x,
@@ -135,6 +141,39 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
         ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(b)), "l"(pol)
         : "memory");
+}
+
+// ---------------------------------------------------------- clusters
+// This CTA's rank in its thread-block cluster and the cluster's CTA count.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_ctas() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+// The cluster barrier, split: every thread of every CTA arrives, then waits.
+// The relaxed arrive orders nothing (it only marks that the CTA runs); the
+// release arrive and the acquire wait make the shared-memory writes made
+// before the arrive visible to every CTA after its wait.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Store a float into the shared memory of CTA `rank` of the cluster, at the
+// address that `p` has in this CTA.
+__device__ __forceinline__ void st_cluster_f32(const void* p, uint32_t rank, float v) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
 }
 
 // ---------------------------------------------------------- tile sources

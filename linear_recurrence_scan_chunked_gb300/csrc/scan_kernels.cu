@@ -204,11 +204,20 @@ template <typename S, bool VP, int M>
 using BwdOpT = ScanBwdOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_SCAN_BWD, sizeof(S) == 2, M).NW,
                          kcfg(OP_SCAN_BWD, sizeof(S) == 2, M).R>;
 
+// The cluster kernel's instantiations: one channel per lane on both paths.
+template <typename S>
+using FwdOpK = ScanFwdOp<S, 1, kcfg(OP_SCAN_FWD, sizeof(S) == 2, TILE_CLUSTER).NW,
+                         kcfg(OP_SCAN_FWD, sizeof(S) == 2, TILE_CLUSTER).R>;
+template <typename S>
+using BwdOpK = ScanBwdOp<S, 1, kcfg(OP_SCAN_BWD, sizeof(S) == 2, TILE_CLUSTER).NW,
+                         kcfg(OP_SCAN_BWD, sizeof(S) == 2, TILE_CLUSTER).R>;
+
 template <typename S, bool VP>
 static cudaError_t scan_fwd_t(const void* a, const void* b, const void* h0, void* h, const Geom& g,
                               const Carry& cr, cudaStream_t s) {
     return launch_persist<FwdOpT<S, VP, CARRY_CHAIN>, FwdOpT<S, VP, CARRY_WALK>,
-                          FwdOpT<S, VP, TILE_TMA>, kcfg(OP_SCAN_FWD, sizeof(S) == 2, TILE_TMA).ST>(
+                          FwdOpT<S, VP, TILE_TMA>, kcfg(OP_SCAN_FWD, sizeof(S) == 2, TILE_TMA).ST,
+                          FwdOpK<S>>(
         {(const S*)a, (const S*)b, (const S*)h0, (S*)h}, g, cr, s);
 }
 
@@ -217,7 +226,8 @@ static cudaError_t scan_bwd_t(const void* a, const void* h, const void* h0, cons
                               void* da, void* db, void* dh0, const Geom& g, const Carry& cr,
                               cudaStream_t s) {
     return launch_persist<BwdOpT<S, VP, CARRY_CHAIN>, BwdOpT<S, VP, CARRY_WALK>,
-                          BwdOpT<S, VP, TILE_TMA>, kcfg(OP_SCAN_BWD, sizeof(S) == 2, TILE_TMA).ST>(
+                          BwdOpT<S, VP, TILE_TMA>, kcfg(OP_SCAN_BWD, sizeof(S) == 2, TILE_TMA).ST,
+                          BwdOpK<S>>(
         {(const S*)a, (const S*)h, (const S*)h0, (const S*)dh, (S*)da, (S*)db, (S*)dh0}, g, cr, s);
 }
 

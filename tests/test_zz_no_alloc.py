@@ -38,10 +38,11 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
-@pytest.mark.parametrize("dtype,shape", [("f32", (1024, 4, 256)), ("f32", (3001, 2, 100)),
-                                         ("bf16", (777, 3, 512)),
+@pytest.mark.parametrize("dtype,shape", [# cluster kernel; look-back kernel
+                                         ("f32", (1024, 4, 256)), ("bf16", (777, 3, 512)),
+                                         ("f32", (2048, 4, 256)), ("f32", (3001, 2, 100)),
                                          # strip kernel; walker kernels (register, segmented)
-                                         ("f32", (40, 40, 1000)), ("f32", (20000, 1, 128)),
+                                         ("bf16", (1030, 16, 1024)), ("f32", (20000, 1, 128)),
                                          ("bf16", (20000, 1, 128))])
 @pytest.mark.parametrize("with_err", [True, False])
 def test_noalloc_matches_allocating_scan_twice(cuda, dtype, shape, with_err):
