@@ -335,20 +335,24 @@ __device__ __forceinline__ uint32_t bf_pack(float lo, float hi) {
 // --------------------------------------------------------- storage packs
 // Pack<S, VEC>: VEC consecutive elements of storage type S held in registers
 // (bf16 kept packed, two per 32-bit register).  VEC * sizeof(S) is 16 bytes on
-// the vector path and one element on the scalar path.
+// the vector path and one element on the scalar path (the cluster kernel also
+// takes two-element packs on the vector path).
 
 template <typename S, int VEC>
 struct Pack;
 
 template <int VEC>
 struct Pack<float, VEC> {
-    static_assert(VEC == 4 || VEC == 1, "fp32 packs hold 4 or 1 elements");
+    static_assert(VEC == 4 || VEC == 2 || VEC == 1, "fp32 packs hold 4, 2 or 1 elements");
     float v[VEC];
     __device__ __forceinline__ void load(const float* p) {
         if constexpr (VEC == 4) {
             uint4 r = ld_stream_u4(p);
             v[0] = __uint_as_float(r.x); v[1] = __uint_as_float(r.y);
             v[2] = __uint_as_float(r.z); v[3] = __uint_as_float(r.w);
+        } else if constexpr (VEC == 2) {
+            const uint2 r = ld_stream_u2(p);
+            v[0] = __uint_as_float(r.x); v[1] = __uint_as_float(r.y);
         } else {
             v[0] = __ldg(p);
         }
@@ -358,6 +362,9 @@ struct Pack<float, VEC> {
             uint4 r = ld_hint_u4(p, pol);
             v[0] = __uint_as_float(r.x); v[1] = __uint_as_float(r.y);
             v[2] = __uint_as_float(r.z); v[3] = __uint_as_float(r.w);
+        } else if constexpr (VEC == 2) {
+            const uint2 r = ld_hint_u2(p, pol);
+            v[0] = __uint_as_float(r.x); v[1] = __uint_as_float(r.y);
         } else {
             v[0] = __uint_as_float(ld_hint_b32(p, pol));
         }
@@ -366,6 +373,9 @@ struct Pack<float, VEC> {
         if constexpr (VEC == 4) {
             const float4 f = *reinterpret_cast<const float4*>(p);
             v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+        } else if constexpr (VEC == 2) {
+            const float2 f = *reinterpret_cast<const float2*>(p);
+            v[0] = f.x; v[1] = f.y;
         } else {
             v[0] = *p;
         }
@@ -379,7 +389,7 @@ struct Pack<float, VEC> {
 
 template <int VEC>
 struct Pack<__nv_bfloat16, VEC> {
-    static_assert(VEC == 8 || VEC == 4 || VEC == 1, "bf16 packs hold 8, 4 or 1 elements");
+    static_assert(VEC == 8 || VEC == 4 || VEC == 2 || VEC == 1, "bf16 packs hold 8, 4, 2 or 1 elements");
     static constexpr int NW_ = VEC == 1 ? 1 : VEC / 2;
     uint32_t w[NW_];
     __device__ __forceinline__ void load(const __nv_bfloat16* p) {
@@ -389,6 +399,8 @@ struct Pack<__nv_bfloat16, VEC> {
         } else if constexpr (VEC == 4) {
             const uint2 r = ld_stream_u2(p);
             w[0] = r.x; w[1] = r.y;
+        } else if constexpr (VEC == 2) {
+            w[0] = __ldg(reinterpret_cast<const unsigned int*>(p));
         } else {
             w[0] = (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p));
         }
@@ -400,6 +412,8 @@ struct Pack<__nv_bfloat16, VEC> {
         } else if constexpr (VEC == 4) {
             const uint2 r = ld_hint_u2(p, pol);
             w[0] = r.x; w[1] = r.y;
+        } else if constexpr (VEC == 2) {
+            w[0] = ld_hint_b32(p, pol);
         } else {
             w[0] = ld_hint_u16(p, pol);
         }
@@ -411,6 +425,8 @@ struct Pack<__nv_bfloat16, VEC> {
         } else if constexpr (VEC == 4) {
             const uint2 r = *reinterpret_cast<const uint2*>(p);
             w[0] = r.x; w[1] = r.y;
+        } else if constexpr (VEC == 2) {
+            w[0] = *reinterpret_cast<const uint32_t*>(p);
         } else {
             w[0] = (uint32_t)*reinterpret_cast<const unsigned short*>(p);
         }
@@ -433,6 +449,8 @@ __device__ __forceinline__ void store_vec(S* p, const float (&x)[VEC]) {
         if constexpr (VEC == 4)
             st_u4(p, make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]),
                                 __float_as_uint(x[2]), __float_as_uint(x[3])));
+        else if constexpr (VEC == 2)
+            st_u2(p, make_uint2(__float_as_uint(x[0]), __float_as_uint(x[1])));
         else
             *reinterpret_cast<float*>(p) = x[0];
     } else {
@@ -441,6 +459,8 @@ __device__ __forceinline__ void store_vec(S* p, const float (&x)[VEC]) {
                                 bf_pack(x[6], x[7])));
         else if constexpr (VEC == 4)
             st_u2(p, make_uint2(bf_pack(x[0], x[1]), bf_pack(x[2], x[3])));
+        else if constexpr (VEC == 2)
+            *reinterpret_cast<uint32_t*>(p) = bf_pack(x[0], x[1]);
         else
             *reinterpret_cast<unsigned short*>(p) = (unsigned short)bf_bits(x[0]);
     }

@@ -95,7 +95,7 @@ constexpr KCfg kcfg(Op op, int dtype, int mode) {
     // as the SRU cell and takes its rows; DEER's ODE form takes the tanh
     // form's rows at eight warps per CTA (its heavier producer measured slower
     // with four).
-    return mode == TILE_CLUSTER ? KCfg{8, 16, 0}  // one channel per lane, 128 rows per CTA
+    return mode == TILE_CLUSTER ? KCfg{8, 16, 0}  // 16 rows of 32 channels per warp, 128 per CTA
            : op == OP_DEER_ODE   ? KCfg{8, mode == CARRY_CHAIN ? 2 : 4, mode == TILE_TMA ? 3 : 0}
            : op == OP_DEER && dtype == 1 ? kcfg(OP_DEER, 0, mode)
            : op == OP_LSTM_FWD ? kcfg(OP_SRU_FWD, dtype, mode)
@@ -125,8 +125,8 @@ constexpr KCfg kcfg(Op op, int dtype, int mode) {
 constexpr int kvec(int dtype, bool vec) { return vec ? 4 : 1; }
 
 // mode: CARRY_CHAIN, CARRY_WALK, TILE_TMA (chain protocol, TMA staging) or
-// TILE_CLUSTER (one channel per lane on both paths: a warp's row is 32
-// consecutive channels, one coalesced access, and no alignment is needed)
+// TILE_CLUSTER (tiles 32 channels wide on both paths: R rows of 32 channels
+// per warp, held as VEC row groups)
 inline TileShape tile_shape(Op op, int dtype, bool vec, int mode) {
     const KCfg k = kcfg(op, dtype, mode);
     return TileShape{k.NW * k.R, 32 * (mode == TILE_CLUSTER ? 1 : kvec(dtype, vec)), 32 * k.NW};

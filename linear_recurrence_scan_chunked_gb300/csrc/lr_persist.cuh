@@ -1203,35 +1203,65 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
 }
 
 // Cluster kernel (short problems): the CTAs of one thread-block cluster take
-// the time chunks of one channel tile, chunk q on the CTA of rank q.  Each CTA
-// loads its rows into registers, forms its chunk's aggregate (the composition
-// of the affine maps of its rows), and writes it into the shared memory of every
-// CTA after it in the cluster; after one cluster barrier each CTA folds the
-// aggregates of the chunks before its own, in chunk order, into the state that
-// enters its chunk, and writes its outputs.  Nothing goes through global memory
-// but the inputs and outputs: no packets, tickets or epochs, and no CTA waits
-// for another cluster, so clusters may run in any order and any number of waves.
-// The association of every operation is fixed by the chunk and warp indices:
-// the result is bitwise reproducible.
+// the time chunks of one 32-channel tile, chunk q on the CTA of rank q.  Each
+// CTA loads its rows into registers and forms its chunk's aggregate (the
+// composition of the affine maps of its rows); one warp sends it, with
+// asynchronous stores, into the shared memory of every CTA after it in the
+// cluster, where the stores count their bytes on that CTA's barrier.  A CTA of
+// rank q waits until the q aggregates before its own have landed, folds them in
+// chunk order into the state that enters its chunk, and writes its outputs.
+// Nothing goes through global memory but the inputs and outputs: no packets,
+// tickets or epochs, and no CTA waits for another cluster, so clusters may run
+// in any order and any number of waves.
+//
+// Thread layout: a row of the tile is 32 channels, held by 32 / VEC lanes
+// (VEC channels each), so a warp holds VEC row groups of R consecutive rows:
+// lane l takes channels (l mod 32/VEC) * VEC and row group l / (32/VEC).  The
+// groups of a warp are composed by a shuffle scan, the warps through shared
+// memory.  The association of every operation is fixed by the chunk, warp and
+// lane indices: the result is bitwise reproducible.
 template <class Op, int CL>
 __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
-    k_cluster(typename Op::Params p, Geom g) {
-    constexpr int NW = Op::NW, VEC = Op::VEC;
+    k_cluster(typename Op::Params p, Geom g, const uint32_t* err) {
+    constexpr int NW = Op::NW, VEC = Op::VEC, R = Op::R;
+    constexpr int LPR = 32 / VEC;        // lanes per row
+    constexpr int RG = VEC;              // row groups per warp
+    constexpr int L = NW * RG * R;       // rows per CTA
+    constexpr uint32_t kAggBytes = 32 * 8;  // one chunk's aggregate: (A, B) per channel
+    static_assert(LPR * VEC == 32, "a row is 32 channels");
     // skip depends on the arguments only: the whole launch returns here,
     // before any barrier
     if (Op::skip(p)) return;
-    __shared__ StripSmem<VEC, NW> sm;  // the warps' aggregates of this chunk
-    __shared__ float ca[CL][32 * VEC], cb[CL][32 * VEC];  // aggregates of the chunks before it
+    __shared__ StripSmem<VEC, NW> sm;           // the warps' aggregates of this chunk
+    __shared__ __align__(16) float2 cab[CL][32];  // (A, B) of the chunks before it
+    __shared__ __align__(8) uint64_t cbar;      // counts their bytes
     __shared__ typename Op::Smem xs;
-    // the first cluster barrier phase: every CTA of the cluster runs before
-    // any CTA writes into another's shared memory
+    if (threadIdx.x == 0) {
+        mbar_init(&cbar, 1);
+        mbar_init_fence();
+    }
+    // the first cluster barrier phase: no CTA stores into another before that
+    // one runs and has initialised its barrier
     cluster_arrive_relaxed();
     // a programmatic dependent launch, as k_look
     griddep_wait();
     griddep_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cq = lane % LPR, rg = lane / LPR;
     const uint32_t q = cluster_rank(), n = cluster_ctas();
-    const TileCoord tc = tile_coord_qj<Op>(g, q, blockIdx.x / n);
+    if (threadIdx.x == 0) mbar_arrive_tx(&cbar, q * kAggBytes);
+    TileCoord tc;
+    tc.q = q;
+    tc.tchunk = Op::REV ? g.n_chunks - 1 - (int64_t)q : (int64_t)q;
+    {
+        const int vb = warp * RG + rg;  // row block of R rows, in scan order
+        tc.t0 = Op::REV ? tc.tchunk * L + (L - 1) - vb * R : tc.tchunk * L + vb * R;
+    }
+    tc.c = (int64_t)(blockIdx.x / n) * 32 + cq * VEC;
+    tc.cd = chan_feat(g, tc.c);
+    tc.cok = tc.c < g.C;
+    tc.acc_run = false;
+    tc.acc_flush = false;
     float s[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) s[v] = 0.f;
@@ -1242,18 +1272,39 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
     typename Op::Acc acc;
     Op::acc_init(acc);
     Op::load(GlobalSrc{g.C, tc.c}, p, g, tc, regs);
+    // the row groups before this one within the warp (exclusive), and the
+    // warp's aggregate (inclusive, on the last group)
+    float EA[VEC], EB[VEC];
     {
-        float A[VEC], B[VEC];
-        Op::aggregate(p, g, tc, regs, w, A, B, false);
+        float IA[VEC], IB[VEC];
+        Op::aggregate(p, g, tc, regs, w, IA, IB, false);
+#pragma unroll
+        for (int off = LPR; off < 32; off *= 2)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                const float ua = __shfl_up_sync(0xffffffffu, IA[v], off);
+                const float ub = __shfl_up_sync(0xffffffffu, IB[v], off);
+                if (lane >= off) {  // this group after the ones before it
+                    IB[v] = __fmaf_rn(IA[v], ub, IB[v]);
+                    IA[v] *= ua;
+                }
+            }
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
-            sm.a[warp][lane][v] = A[v];
-            sm.b[warp][lane][v] = B[v];
+            EA[v] = RG > 1 ? __shfl_up_sync(0xffffffffu, IA[v], LPR) : 1.f;
+            EB[v] = RG > 1 ? __shfl_up_sync(0xffffffffu, IB[v], LPR) : 0.f;
+            if (rg == 0) { EA[v] = 1.f; EB[v] = 0.f; }
         }
+        if (rg == RG - 1)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                sm.a[warp][cq][v] = IA[v];
+                sm.b[warp][cq][v] = IB[v];
+            }
     }
     csync<NW>();
     cluster_wait();  // the first phase
-    if (warp == 0 && q + 1 < n) {  // the chunk's aggregate, to the CTAs after this one
+    if (warp == 0 && rg == 0 && q + 1 < n) {  // the chunk's aggregate, to the CTAs after this one
         float TA[VEC], TB[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { TA[v] = 1.f; TB[v] = 0.f; }
@@ -1261,19 +1312,27 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
         for (int w2 = 0; w2 < NW; ++w2)
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
-                const float a = sm.a[w2][lane][v];
-                TB[v] = __fmaf_rn(a, TB[v], sm.b[w2][lane][v]);
+                const float a = sm.a[w2][cq][v];
+                TB[v] = __fmaf_rn(a, TB[v], sm.b[w2][cq][v]);
                 TA[v] *= a;
             }
-        for (uint32_t d = q + 1; d < n; ++d)
+        for (uint32_t d = q + 1; d < n; ++d) {
+            const uint32_t bar = cluster_map(&cbar, d);
+            const uint32_t dst = cluster_map(&cab[q][cq * VEC], d);  // VEC consecutive (A, B) pairs
+            if constexpr (VEC == 1) {
+                st_async_f2(dst, TA[0], TB[0], bar);
+            } else {
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) {
-                st_cluster_f32(&ca[q][lane * VEC + v], d, TA[v]);
-                st_cluster_f32(&cb[q][lane * VEC + v], d, TB[v]);
+                for (int v = 0; v < VEC; v += 2)
+                    st_async_f4(dst + v * 8, TA[v], TB[v], TA[v + 1], TB[v + 1], bar);
             }
+        }
     }
-    cluster_arrive_release();
-    // the warps before this one within the chunk, while the barrier completes
+    // the second phase: no CTA leaves while another may still store into it
+    // (every store is issued before its CTA arrives; the normal path has also
+    // seen every byte land on its barrier before it ends)
+    cluster_arrive_relaxed();
+    // the warps before this one within the chunk, while the aggregates travel
     float PA[VEC], PB[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) { PA[v] = 1.f; PB[v] = 0.f; }
@@ -1282,19 +1341,31 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
         if (w2 < warp)
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
-                const float a = sm.a[w2][lane][v];
-                PB[v] = __fmaf_rn(a, PB[v], sm.b[w2][lane][v]);
+                const float a = sm.a[w2][cq][v];
+                PB[v] = __fmaf_rn(a, PB[v], sm.b[w2][cq][v]);
                 PA[v] *= a;
             }
-    cluster_wait();  // the second phase: every earlier chunk's aggregate is here
-#pragma unroll 1
-    for (uint32_t d = 0; d < q; ++d)
+    if (!mbar_wait<true>(&cbar, 0, err)) {  // every earlier chunk's aggregate is here
+        if (lane == 0) atomicOr(const_cast<uint32_t*>(err), ERRBIT_TIMEOUT);
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) s[v] = __fmaf_rn(ca[d][lane * VEC + v], s[v], cb[d][lane * VEC + v]);
+        for (int v = 0; v < VEC; ++v) s[v] = __int_as_float(0x7fc00000);
+    }
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) s[v] = __fmaf_rn(PA[v], s[v], PB[v]);
+    for (int d = 0; d < CL - 1; ++d)  // the chunks before this one, in chunk order
+        if ((uint32_t)d < q)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                const float2 e = cab[d][cq * VEC + v];
+                s[v] = __fmaf_rn(e.x, s[v], e.y);
+            }
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+        s[v] = __fmaf_rn(PA[v], s[v], PB[v]);
+        s[v] = __fmaf_rn(EA[v], s[v], EB[v]);
+    }
     Op::finish(p, g, tc, regs, w, s, xs, acc);
     Op::at_exit(p, xs, acc);
+    cluster_wait();
 }
 
 // The op's scratch in the TMA strip and segmented kernels: its own space, or
@@ -2398,7 +2469,8 @@ cudaError_t launch_look(const typename Op::Params& p, Geom g, const Carry& cr, c
 // Host: launch k_cluster<Op, CL> (one cluster of n_chunks <= CL CTAs per
 // channel tile), as a programmatic dependent of the stream's previous kernel.
 template <class Op>
-cudaError_t launch_cluster(const typename Op::Params& p, const Geom& g, cudaStream_t s) {
+cudaError_t launch_cluster(const typename Op::Params& p, const Geom& g, const Carry& cr,
+                           cudaStream_t s) {
     constexpr int CL = kClusterMax;
     if (g.n_chunks < 1 || g.n_chunks > CL || g.n_ct < 1) return cudaErrorInvalidValue;
     const uint64_t grid = (uint64_t)g.n_ct * (uint64_t)g.n_chunks;
@@ -2418,7 +2490,7 @@ cudaError_t launch_cluster(const typename Op::Params& p, const Geom& g, cudaStre
     at[1].val.programmaticStreamSerializationAllowed = LR_LOOK_PDL;
     lc.attrs = at;
     lc.numAttrs = 2;
-    return cudaLaunchKernelEx(&lc, k_cluster<Op, CL>, p, g);
+    return cudaLaunchKernelEx(&lc, k_cluster<Op, CL>, p, g, (const uint32_t*)cr.err);
 }
 
 // Host: launch k_strip<Op, ST> when the problem has enough channel strips to
@@ -2603,7 +2675,7 @@ cudaError_t launch_persist(const typename OpC::Params& p, const Geom& g, const C
                   "all instantiations take the same arguments");
     if (cr.mode == CARRY_CLUSTER) {
         if constexpr (std::is_void<OpK>::value) return cudaErrorNotSupported;
-        else return launch_cluster<OpK>(p, g, s);
+        else return launch_cluster<OpK>(p, g, cr, s);
     }
     if (cr.mode == CARRY_LOOK) return launch_look<OpT>(p, g, cr, s);
     if (cr.mode == CARRY_CHAIN) {

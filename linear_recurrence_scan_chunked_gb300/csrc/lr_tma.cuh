@@ -94,6 +94,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// As mbar_try_wait, acquiring at cluster scope: the phase completes on data
+// that other CTAs of the cluster stored into this CTA's shared memory.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -103,11 +116,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Returns false when it gave up (about kMbarLimitNs, or the launch's sticky
 // error word says another CTA already gave up).
 constexpr uint64_t kMbarLimitNs = 2000000000ull;
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, const uint32_t* err) {
-    if (mbar_try_wait(b, parity)) return true;
+    auto done = [&]() { return CLUSTER ? mbar_try_wait_cluster(b, parity) : mbar_try_wait(b, parity); };
+    if (done()) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(b, parity)) return true;
+        if (done()) return true;
         if ((n & 255u) == 0) {
             if (globaltimer_ns() - t0 > kMbarLimitNs) return false;
             if (ld_relaxed_u32(err) & ERRBIT_TIMEOUT) return false;
@@ -156,24 +171,37 @@ __device__ __forceinline__ uint32_t cluster_ctas() {
     return r;
 }
 // The cluster barrier, split: every thread of every CTA arrives, then waits.
-// The relaxed arrive orders nothing (it only marks that the CTA runs); the
-// release arrive and the acquire wait make the shared-memory writes made
-// before the arrive visible to every CTA after its wait.
+// The relaxed arrive orders no memory access of its own (a barrier's
+// initialisation is published by fence.mbarrier_init before it); the wait
+// acquires.
 __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_arrive_release() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Store a float into the shared memory of CTA `rank` of the cluster, at the
-// address that `p` has in this CTA.
-__device__ __forceinline__ void st_cluster_f32(const void* p, uint32_t rank, float v) {
+// The address that `p` (in this CTA's shared memory) has in CTA `rank` of
+// the cluster.
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
     uint32_t a;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+    return a;
+}
+// An asynchronous store of two floats into another CTA's shared memory
+// (cluster addresses from cluster_map) that counts its 8 bytes on that CTA's
+// barrier `bar`: the storing thread does not wait for it.
+__device__ __forceinline__ void st_async_f2(uint32_t dst, float x, float y, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(dst),
+                 "f"(x), "f"(y), "r"(bar)
+                 : "memory");
+}
+// As st_async_f2, four floats (16 bytes, 16-byte aligned).
+__device__ __forceinline__ void st_async_f4(uint32_t dst, float x, float y, float z, float w,
+                                            uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
+        "f"(x), "f"(y), "f"(z), "f"(w), "r"(bar)
+        : "memory");
 }
 
 // ---------------------------------------------------------- tile sources

@@ -190,8 +190,9 @@ struct ScanBwdOp {
                 store_vec<S, VEC>(p.da + t * g.C + tc.c, av);
             }
         }
-        // row 0 is the last row of the last warp of time chunk 0: s = u_0 = dh0
-        if (tc.tchunk == 0 && (threadIdx.x >> 5) == NW - 1 && p.dh0 != nullptr && tc.cok)
+        // row 0 is this thread's last (t0 = R - 1: the last rows of time
+        // chunk 0): s = u_0 = dh0
+        if (tc.t0 == R - 1 && p.dh0 != nullptr && tc.cok)
             store_vec<S, VEC>(p.dh0 + tc.c, s);
     }
     __device__ static void at_exit(const Params&, Smem&, Acc&) {}
@@ -204,20 +205,25 @@ template <typename S, bool VP, int M>
 using BwdOpT = ScanBwdOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_SCAN_BWD, sizeof(S) == 2, M).NW,
                          kcfg(OP_SCAN_BWD, sizeof(S) == 2, M).R>;
 
-// The cluster kernel's instantiations: one channel per lane on both paths.
-template <typename S>
-using FwdOpK = ScanFwdOp<S, 1, kcfg(OP_SCAN_FWD, sizeof(S) == 2, TILE_CLUSTER).NW,
-                         kcfg(OP_SCAN_FWD, sizeof(S) == 2, TILE_CLUSTER).R>;
-template <typename S>
-using BwdOpK = ScanBwdOp<S, 1, kcfg(OP_SCAN_BWD, sizeof(S) == 2, TILE_CLUSTER).NW,
-                         kcfg(OP_SCAN_BWD, sizeof(S) == 2, TILE_CLUSTER).R>;
+// The cluster kernel's instantiations: a warp covers kcfg's R rows of 32
+// channels, as V row groups of R / V rows (V channels per lane).
+#ifndef LR_CLUSTER_VEC
+#define LR_CLUSTER_VEC 2
+#endif
+constexpr int kClusterVec(bool vp) { return vp ? LR_CLUSTER_VEC : 1; }
+template <typename S, bool VP>
+using FwdOpK = ScanFwdOp<S, kClusterVec(VP), kcfg(OP_SCAN_FWD, sizeof(S) == 2, TILE_CLUSTER).NW,
+                         kcfg(OP_SCAN_FWD, sizeof(S) == 2, TILE_CLUSTER).R / kClusterVec(VP)>;
+template <typename S, bool VP>
+using BwdOpK = ScanBwdOp<S, kClusterVec(VP), kcfg(OP_SCAN_BWD, sizeof(S) == 2, TILE_CLUSTER).NW,
+                         kcfg(OP_SCAN_BWD, sizeof(S) == 2, TILE_CLUSTER).R / kClusterVec(VP)>;
 
 template <typename S, bool VP>
 static cudaError_t scan_fwd_t(const void* a, const void* b, const void* h0, void* h, const Geom& g,
                               const Carry& cr, cudaStream_t s) {
     return launch_persist<FwdOpT<S, VP, CARRY_CHAIN>, FwdOpT<S, VP, CARRY_WALK>,
                           FwdOpT<S, VP, TILE_TMA>, kcfg(OP_SCAN_FWD, sizeof(S) == 2, TILE_TMA).ST,
-                          FwdOpK<S>>(
+                          FwdOpK<S, VP>>(
         {(const S*)a, (const S*)b, (const S*)h0, (S*)h}, g, cr, s);
 }
 
@@ -227,7 +233,7 @@ static cudaError_t scan_bwd_t(const void* a, const void* h, const void* h0, cons
                               cudaStream_t s) {
     return launch_persist<BwdOpT<S, VP, CARRY_CHAIN>, BwdOpT<S, VP, CARRY_WALK>,
                           BwdOpT<S, VP, TILE_TMA>, kcfg(OP_SCAN_BWD, sizeof(S) == 2, TILE_TMA).ST,
-                          BwdOpK<S>>(
+                          BwdOpK<S, VP>>(
         {(const S*)a, (const S*)h, (const S*)h0, (const S*)dh, (S*)da, (S*)db, (S*)dh0}, g, cr, s);
 }
 
