@@ -56,7 +56,7 @@ EPS, KMAX = 1e-5, 20
 # and written by a K = 6 solve -- the reduce-only pass, iteration 1 and five
 # later iterations, captured at full size (profiles/dram_traffic.md) -- over
 # its K iteration launches.
-NCU_TRAFFIC = {"deer.solve": {"bytes": 767139008, "src": "d1a4f531f04cc3cd",
+NCU_TRAFFIC = {"deer.solve": {"bytes": 766965248, "src": "00486a091960d1b9",
                               "file": "deer_kernels.cu"}}
 
 

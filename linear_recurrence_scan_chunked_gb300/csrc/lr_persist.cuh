@@ -1229,6 +1229,7 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
     constexpr int L = NW * RG * R;       // rows per CTA
     constexpr uint32_t kAggBytes = 32 * 8;  // one chunk's aggregate: (A, B) per channel
     static_assert(LPR * VEC == 32, "a row is 32 channels");
+    static_assert(Op::RG == RG, "the op is instantiated for this kernel's row groups");
     // skip depends on the arguments only: the whole launch returns here,
     // before any barrier
     if (Op::skip(p)) return;

@@ -30,10 +30,10 @@ struct ScanFwdParams {
     S* h;
 };
 
-template <typename S_, int VEC_, int NW_, int R_>
+template <typename S_, int VEC_, int NW_, int R_, int RG_ = 1>
 struct ScanFwdOp {
     using S = S_;
-    static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
+    static constexpr int VEC = VEC_, NW = NW_, R = R_, RG = RG_, MINB = 2;
     static constexpr bool REV = false;
     static constexpr int IN_ARRAYS = 2;  // a, b
     static constexpr bool STREAM_WS = LR_STREAM_WS != 0;
@@ -111,10 +111,12 @@ struct ScanBwdParams {
     S* dh0;
 };
 
-template <typename S_, int VEC_, int NW_, int R_>
+// RG_: row groups per warp (the lanes of a warp split into RG_ groups of R_
+// consecutive rows; 1 everywhere but the cluster kernel's vector path).
+template <typename S_, int VEC_, int NW_, int R_, int RG_ = 1>
 struct ScanBwdOp {
     using S = S_;
-    static constexpr int VEC = VEC_, NW = NW_, R = R_, MINB = 2;
+    static constexpr int VEC = VEC_, NW = NW_, R = R_, RG = RG_, MINB = 2;
     static constexpr bool REV = true;
     static constexpr int IN_ARRAYS = 3;  // a, dh, h
     static constexpr bool SCRATCH_IN_CARRY = false;
@@ -190,9 +192,10 @@ struct ScanBwdOp {
                 store_vec<S, VEC>(p.da + t * g.C + tc.c, av);
             }
         }
-        // row 0 is this thread's last (t0 = R - 1: the last rows of time
-        // chunk 0): s = u_0 = dh0
-        if (tc.t0 == R - 1 && p.dh0 != nullptr && tc.cok)
+        // row 0 is the last row of the last row group of the last warp of time
+        // chunk 0: s = u_0 = dh0
+        if (tc.tchunk == 0 && (threadIdx.x >> 5) == NW - 1 && (RG == 1 || (threadIdx.x & 31) >= 32 - 32 / RG) &&
+            p.dh0 != nullptr && tc.cok)
             store_vec<S, VEC>(p.dh0 + tc.c, s);
     }
     __device__ static void at_exit(const Params&, Smem&, Acc&) {}
@@ -213,10 +216,10 @@ using BwdOpT = ScanBwdOp<S, kvec(sizeof(S) == 2, VP), kcfg(OP_SCAN_BWD, sizeof(S
 constexpr int kClusterVec(bool vp) { return vp ? LR_CLUSTER_VEC : 1; }
 template <typename S, bool VP>
 using FwdOpK = ScanFwdOp<S, kClusterVec(VP), kcfg(OP_SCAN_FWD, sizeof(S) == 2, TILE_CLUSTER).NW,
-                         kcfg(OP_SCAN_FWD, sizeof(S) == 2, TILE_CLUSTER).R / kClusterVec(VP)>;
+                         kcfg(OP_SCAN_FWD, sizeof(S) == 2, TILE_CLUSTER).R / kClusterVec(VP), kClusterVec(VP)>;
 template <typename S, bool VP>
 using BwdOpK = ScanBwdOp<S, kClusterVec(VP), kcfg(OP_SCAN_BWD, sizeof(S) == 2, TILE_CLUSTER).NW,
-                         kcfg(OP_SCAN_BWD, sizeof(S) == 2, TILE_CLUSTER).R / kClusterVec(VP)>;
+                         kcfg(OP_SCAN_BWD, sizeof(S) == 2, TILE_CLUSTER).R / kClusterVec(VP), kClusterVec(VP)>;
 
 template <typename S, bool VP>
 static cudaError_t scan_fwd_t(const void* a, const void* b, const void* h0, void* h, const Geom& g,
