@@ -276,7 +276,7 @@ class Bench:
                 self.graphs[(name, p)] = g
         t.cuda.synchronize()
 
-    def back_to_back_us(self, name, reps=64, rounds=5):
+    def back_to_back_us(self, name, reps=64, rounds=15):
         """Device time per launch of each pass of a launch-bound row, from a
         graph of `reps` launches in a row (each starts when the previous one
         ends): the kernel's own time, no host in between.  Median of

@@ -1205,9 +1205,10 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
 // Cluster kernel (short problems): the CTAs of one thread-block cluster take
 // the time chunks of one 32-channel tile, chunk q on the CTA of rank q.  Each
 // CTA loads its rows into registers and forms its chunk's aggregate (the
-// composition of the affine maps of its rows); one warp sends it, with
+// composition of the affine maps of its rows); its warps send it, with
 // asynchronous stores, into the shared memory of every CTA after it in the
-// cluster, where the stores count their bytes on that CTA's barrier.  A CTA of
+// cluster (one warp per receiver), where the stores count their bytes on that
+// CTA's barrier.  A CTA of
 // rank q waits until the q aggregates before its own have landed, folds them in
 // chunk order into the state that enters its chunk, and writes its outputs.
 // Nothing goes through global memory but the inputs and outputs: no packets,
@@ -1230,6 +1231,7 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
     constexpr uint32_t kAggBytes = 32 * 8;  // one chunk's aggregate: (A, B) per channel
     static_assert(LPR * VEC == 32, "a row is 32 channels");
     static_assert(Op::RG == RG, "the op is instantiated for this kernel's row groups");
+    static_assert(NW >= CL - 1, "one warp per later CTA of the cluster");
     // skip depends on the arguments only: the whole launch returns here,
     // before any barrier
     if (Op::skip(p)) return;
@@ -1305,7 +1307,9 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
     }
     csync<NW>();
     cluster_wait();  // the first phase
-    if (warp == 0 && rg == 0 && q + 1 < n) {  // the chunk's aggregate, to the CTAs after this one
+    // the chunk's aggregate, to the CTAs after this one: warp k sends it to
+    // rank q + 1 + k, so that every later CTA gets it after one store
+    if (rg == 0 && (uint32_t)warp + q + 1 < n) {
         float TA[VEC], TB[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { TA[v] = 1.f; TB[v] = 0.f; }
@@ -1317,16 +1321,15 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
                 TB[v] = __fmaf_rn(a, TB[v], sm.b[w2][cq][v]);
                 TA[v] *= a;
             }
-        for (uint32_t d = q + 1; d < n; ++d) {
-            const uint32_t bar = cluster_map(&cbar, d);
-            const uint32_t dst = cluster_map(&cab[q][cq * VEC], d);  // VEC consecutive (A, B) pairs
-            if constexpr (VEC == 1) {
-                st_async_f2(dst, TA[0], TB[0], bar);
-            } else {
+        const uint32_t d = q + 1 + (uint32_t)warp;
+        const uint32_t bar = cluster_map(&cbar, d);
+        const uint32_t dst = cluster_map(&cab[q][cq * VEC], d);  // VEC consecutive (A, B) pairs
+        if constexpr (VEC == 1) {
+            st_async_f2(dst, TA[0], TB[0], bar);
+        } else {
 #pragma unroll
-                for (int v = 0; v < VEC; v += 2)
-                    st_async_f4(dst + v * 8, TA[v], TB[v], TA[v + 1], TB[v + 1], bar);
-            }
+            for (int v = 0; v < VEC; v += 2)
+                st_async_f4(dst + v * 8, TA[v], TB[v], TA[v + 1], TB[v + 1], bar);
         }
     }
     // the second phase: no CTA leaves while another may still store into it
