@@ -365,7 +365,9 @@ int64_t lr_workspace_bytes(void);
  * Test hook for the bounded carry waits: launches both chain-protocol
  * forward scan kernels (register and TMA-staged) and the look-back kernel on
  * private 2-chunk problems whose first chunk is never published, one CTA
- * each, and the walker-protocol kernels (the register one on the fp32 scalar
+ * each, the cluster kernel on a private 2-chunk problem whose CTAs each
+ * expect one chunk aggregate more than they receive, and the walker-protocol
+ * kernels (the register one on the fp32 scalar
  * path, the warp-specialised one on the fp32 vector path, the segmented one
  * for a bf16 backward scan, and its consume-only form for a fp32 DEER
  * iteration whose aggregates count as published) on a private long problem

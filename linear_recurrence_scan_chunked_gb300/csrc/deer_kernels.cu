@@ -131,21 +131,21 @@ struct DeerOp {
     __device__ static void aggregate(const Params& p, const Geom& g, const TileCoord& tc,
                                      const Regs& rg, Work& w, float (&A)[VEC], float (&B)[VEC],
                                      bool) {
-        float wv[VEC];
+        float wv[VEC], w4[VEC];  // w, and 4 w for the Jacobian w (1 - tanh^2) = 4 w q
 #pragma unroll
         for (int v = 0; v < VEC; ++v) wv[v] = 0.f;
         if (tc.cok) load_param<VEC>(p.w + tc.cd, wv);
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) { A[v] = 1.f; B[v] = 0.f; }
+        for (int v = 0; v < VEC; ++v) { A[v] = 1.f; B[v] = 0.f; w4[v] = 4.f * wv[v]; }
         if (interior(p, g, tc)) {
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
                 for (int v = 0; v < VEC; ++v) {
                     const float yt = rg.yo[r].get(v);
-                    float d1;
-                    const float th = act_tanh_d(wv[v] * yt + rg.u[r].get(v), d1);
-                    const float jac = wv[v] * d1;
+                    float q1;
+                    const float th = act_tanh_q(wv[v] * yt + rg.u[r].get(v), q1);
+                    const float jac = w4[v] * q1;
                     w.J[r][v] = jac;
                     w.Rh[r][v] = th - jac * yt;
                     B[v] = jac * B[v] + w.Rh[r][v];
@@ -159,9 +159,9 @@ struct DeerOp {
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
                 const float yt = rg.yo[r].get(v);
-                float d1;
-                const float th = act_tanh_d(wv[v] * yt + rg.u[r].get(v), d1);
-                const float jac = wv[v] * d1;
+                float q1;
+                const float th = act_tanh_q(wv[v] * yt + rg.u[r].get(v), q1);
+                const float jac = w4[v] * q1;
                 w.J[r][v] = ok ? jac : 1.f;
                 w.Rh[r][v] = ok ? th - jac * yt : 0.f;
                 B[v] = w.J[r][v] * B[v] + w.Rh[r][v];
@@ -182,10 +182,12 @@ struct DeerOp {
             live = p.seq_done[seq] == 0;
         }
         uint32_t mx = 0;  // this tile's residual bits (per-sequence stopping)
-        float wv[VEC];
+        float wv[VEC], w4[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) { wv[v] = 0.f; w.NA[v] = 1.f; w.NB[v] = 0.f; }
         if (nxt && tc.cok) load_param<VEC>(p.w + tc.cd, wv);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) w4[v] = 4.f * wv[v];
         if (nxt && !per_seq && interior(p, g, tc)) {  // the iterations' common case
             S* out = p.ynew + tc.t0 * g.C + tc.c;
 #pragma unroll
@@ -194,9 +196,9 @@ struct DeerOp {
                 for (int v = 0; v < VEC; ++v) {
                     float yp = s[v];
                     if constexpr (sizeof(S) == 2) yp = bf_lo(bf_bits(yp));
-                    float d1;
-                    const float th = act_tanh_d(wv[v] * yp + rg.u[r].get(v), d1);
-                    const float jac = wv[v] * d1;
+                    float q1;
+                    const float th = act_tanh_q(wv[v] * yp + rg.u[r].get(v), q1);
+                    const float jac = w4[v] * q1;
                     w.NB[v] = jac * w.NB[v] + (th - jac * yp);
                     w.NA[v] *= jac;
                     s[v] = w.J[r][v] * s[v] + w.Rh[r][v];
@@ -222,9 +224,9 @@ struct DeerOp {
                 for (int v = 0; v < VEC; ++v) {
                     float yp = s[v];
                     if constexpr (sizeof(S) == 2) yp = bf_lo(bf_bits(yp));
-                    float d1;
-                    const float th = act_tanh_d(wv[v] * yp + rg.u[r].get(v), d1);
-                    const float jac = wv[v] * d1;
+                    float q1;
+                    const float th = act_tanh_q(wv[v] * yp + rg.u[r].get(v), q1);
+                    const float jac = w4[v] * q1;
                     w.NB[v] = jac * w.NB[v] + (th - jac * yp);
                     w.NA[v] *= jac;
                 }

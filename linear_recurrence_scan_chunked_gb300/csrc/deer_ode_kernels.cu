@@ -82,11 +82,12 @@ struct DeerOdeOp {
 
     // The step's coefficients from the linearisation point yt (the state
     // entering the step), the input and the step length: clamps G, counts it.
-    __device__ static void coeffs(float wv, float yt, float uv, float dtt, float& a, float& b,
-                                  uint32_t& ncl) {
-        float d1;
-        const float th = act_tanh_d(wv * yt + uv, d1);
-        float gv = 1.f - wv * d1;
+    // w4 = 4 w: G = 1 - w (1 - tanh^2) = 1 - 4 w q (the same bits as with w).
+    __device__ static void coeffs(float wv, float w4, float yt, float uv, float dtt, float& a,
+                                  float& b, uint32_t& ncl) {
+        float q1;
+        const float th = act_tanh_q(wv * yt + uv, q1);
+        float gv = fmaf(-w4, q1, 1.f);
         if (gv > kOdeGClamp) {  // (a NaN fails both tests and stays NaN)
             gv = kOdeGClamp;
             ++ncl;
@@ -148,7 +149,7 @@ struct DeerOdeOp {
             for (int v = 0; v < VEC; ++v) {
                 float a, b;
                 uint32_t n = 0;
-                coeffs(wv[v], rg.yo[r].get(v), rg.u[r].get(v), dtt, a, b, n);
+                coeffs(wv[v], 4.f * wv[v], rg.yo[r].get(v), rg.u[r].get(v), dtt, a, b, n);
                 ncl += ok ? n : 0u;
                 w.J[r][v] = ok ? a : 1.f;
                 w.Rh[r][v] = ok ? b : 0.f;
@@ -176,7 +177,7 @@ struct DeerOdeOp {
                     if constexpr (sizeof(S) == 2) yp = bf_lo(bf_bits(yp));
                     float a, b;
                     uint32_t n = 0;  // counted by the next iteration itself
-                    coeffs(wv[v], yp, rg.u[r].get(v), w.DT[r], a, b, n);
+                    coeffs(wv[v], 4.f * wv[v], yp, rg.u[r].get(v), w.DT[r], a, b, n);
                     w.NB[v] = a * w.NB[v] + b;
                     w.NA[v] *= a;
                 }

@@ -59,6 +59,15 @@ __device__ __forceinline__ float act_tanh_d(float x, float& d) {
     d = 4.f * fmaf(-r, r, r);
     return fmaf(-2.f, r, 1.f);
 }
+// tanh(x), and in q a quarter of its derivative, r (1 - r) with
+// r = 1 / (e^{2x} + 1): a caller that scales the factor it multiplies the
+// derivative by with 4 once (exact in fp32) saves a multiply per element and
+// gets the same bits as 4 q times that factor.
+__device__ __forceinline__ float act_tanh_q(float x, float& q) {
+    const float r = rcp_ftz(ex2_ftz(kTwoLog2e * x) + 1.f);
+    q = fmaf(-r, r, r);
+    return fmaf(-2.f, r, 1.f);
+}
 
 // e^x - 1 without the cancellation of e^x - 1 near 0 (DEER's ODE form,
 // exp(-G dt) and (1 - exp(-G dt)) / G): below |x| = 1/4 the Taylor series

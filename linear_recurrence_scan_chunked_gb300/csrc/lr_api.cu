@@ -942,6 +942,8 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
     // of two time chunks and one channel tile, each with one CTA that is handed
     // tile 1: it waits for the state after tile 0, which nobody publishes.
     // Look-back protocol: the same, tile 1 waits for tile 0's aggregate.
+    // Cluster kernel: a two-chunk problem whose CTAs each expect one chunk
+    // aggregate more than arrives.
     // Walker protocol: the register walker kernel (scalar path), the
     // warp-specialised one (vector path), the segmented walker kernel and its
     // consume-only form, on a long one-strip problem launched without walkers:
@@ -981,6 +983,17 @@ int lr_test_lookback_timeout(uint32_t spin_limit, void* stream) {
         const float* a = (const float*)buf;
         CK(launch_scan_fwd(LR_F32, true, a, a + Tw * C, nullptr, (float*)buf + 2 * Tw * C, g, cr,
                            s));
+    }
+    {  // cluster kernel: every CTA expects one chunk aggregate more than the CTAs before it send
+        const int64_t T = 2 * tile_shape(OP_SCAN_FWD, LR_F32, true, TILE_CLUSTER).L;
+        Geom g;
+        Carry cr;
+        TRY(plan(*ws, OP_SCAN_FWD, LR_F32, true, T, C, C, &g, &cr, s, 1));
+        if (cr.mode != CARRY_CLUSTER) return LR_ERR_INVALID_ARG;
+        g.ticket_base = 1;
+        cr.spin_limit = spin_limit;
+        const float* a = (const float*)buf;
+        CK(launch_scan_fwd(LR_F32, true, a, a + Tw * C, nullptr, (float*)buf + 2 * Tw * C, g, cr, s));
     }
     for (int vec = 0; vec < 2; ++vec) {  // fp32 forward: register walker (scalar), warp-specialised (vector)
         Geom g;

@@ -1223,7 +1223,7 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
 // lane indices: the result is bitwise reproducible.
 template <class Op, int CL>
 __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
-    k_cluster(typename Op::Params p, Geom g, const uint32_t* err) {
+    k_cluster(typename Op::Params p, Geom g, const Carry cr) {
     constexpr int NW = Op::NW, VEC = Op::VEC, R = Op::R;
     constexpr int LPR = 32 / VEC;        // lanes per row
     constexpr int RG = VEC;              // row groups per warp
@@ -1252,7 +1252,9 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cq = lane % LPR, rg = lane / LPR;
     const uint32_t q = cluster_rank(), n = cluster_ctas();
-    if (threadIdx.x == 0) mbar_arrive_tx(&cbar, q * kAggBytes);
+    // the bytes of the q chunk aggregates before this one (g.ticket_base adds
+    // chunks that never come: the timeout test)
+    if (threadIdx.x == 0) mbar_arrive_tx(&cbar, (q + g.ticket_base) * kAggBytes);
     TileCoord tc;
     tc.q = q;
     tc.tchunk = Op::REV ? g.n_chunks - 1 - (int64_t)q : (int64_t)q;
@@ -1349,10 +1351,20 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
                 PB[v] = __fmaf_rn(a, PB[v], sm.b[w2][cq][v]);
                 PA[v] *= a;
             }
-    if (!mbar_wait<true>(&cbar, 0, err)) {  // every earlier chunk's aggregate is here
-        if (lane == 0) atomicOr(const_cast<uint32_t*>(err), ERRBIT_TIMEOUT);
+    {  // every earlier chunk's aggregate is here: a wait of at most cr.spin_limit polls
+        bool got = false;
+        for (uint32_t k = 0; k <= cr.spin_limit; ++k) {
+            if (mbar_try_wait_cluster(&cbar, 0)) {
+                got = true;
+                break;
+            }
+            if ((k & 63u) == 63u && (ld_relaxed_u32(cr.err) & ERRBIT_TIMEOUT)) break;
+        }
+        if (!got) {
+            if (lane == 0) atomicOr(cr.err, ERRBIT_TIMEOUT);
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) s[v] = __int_as_float(0x7fc00000);
+            for (int v = 0; v < VEC; ++v) s[v] = __int_as_float(0x7fc00000);
+        }
     }
 #pragma unroll
     for (int d = 0; d < CL - 1; ++d)  // the chunks before this one, in chunk order
@@ -2494,7 +2506,7 @@ cudaError_t launch_cluster(const typename Op::Params& p, const Geom& g, const Ca
     at[1].val.programmaticStreamSerializationAllowed = LR_LOOK_PDL;
     lc.attrs = at;
     lc.numAttrs = 2;
-    return cudaLaunchKernelEx(&lc, k_cluster<Op, CL>, p, g, (const uint32_t*)cr.err);
+    return cudaLaunchKernelEx(&lc, k_cluster<Op, CL>, p, g, cr);
 }
 
 // Host: launch k_strip<Op, ST> when the problem has enough channel strips to

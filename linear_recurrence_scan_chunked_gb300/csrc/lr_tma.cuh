@@ -116,13 +116,11 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Returns false when it gave up (about kMbarLimitNs, or the launch's sticky
 // error word says another CTA already gave up).
 constexpr uint64_t kMbarLimitNs = 2000000000ull;
-template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, const uint32_t* err) {
-    auto done = [&]() { return CLUSTER ? mbar_try_wait_cluster(b, parity) : mbar_try_wait(b, parity); };
-    if (done()) return true;
+    if (mbar_try_wait(b, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t n = 1;; ++n) {
-        if (done()) return true;
+        if (mbar_try_wait(b, parity)) return true;
         if ((n & 255u) == 0) {
             if (globaltimer_ns() - t0 > kMbarLimitNs) return false;
             if (ld_relaxed_u32(err) & ERRBIT_TIMEOUT) return false;
