@@ -15,8 +15,8 @@ DEER solve counts N*K) and the algorithmic HBM bytes per second.  Inputs are
 resident in HBM before the timed region; every input except scan_tiny's
 (12.6 MB) is larger than the 129 MB L2, and each step streams ~18 GB, so no
 step starts with its inputs cached.  The scan_tiny passes are launch-bound
-(a few microseconds of device work each): the step replays them as CUDA
-graphs captured once after the warm-up, instead of calling through Python.
+(a few microseconds of device work each): the step calls them after
+scan_large, so that the host enqueues them while the GPU is still busy.
 
 `value` and `ms_per_step` come from exactly --steps timed steps.  The
 per-operation figures (`ops`) are medians over those steps and further steps
@@ -129,7 +129,7 @@ def esize(wl):
 
 # (name, workload, passes); bytes per element per pass (algorithmic).  The
 # launch-bound scan_tiny row runs after scan_large, while the GPU is still busy
-# with it, so that its graph launches are enqueued ahead as in a training loop
+# with it, so that its launches are enqueued ahead as in a training loop
 # (the DEER solve at the end of a step waits for its residuals on the host:
 # whatever comes first in the next step starts on an idle GPU).
 ROWS = [("sru", W.SRU, ("fwd", "bwd")),
@@ -169,9 +169,10 @@ def pass_elems(wl, p, k=1):
     return wl.N * (k if p == "solve" else 1)
 
 
-# Rows run as CUDA graphs inside the step (launch-bound: microseconds of
-# device work per pass, less than the host's cost of a call through Python).
-GRAPH_ROWS = ("scan_tiny",)
+# Rows replayed as CUDA graphs inside the step (none: the tiny scan's passes,
+# called directly behind scan_large, measured 8.7-9.7 / 8.9 us per pass against
+# 10.0 / 11.0 us as one-kernel graph replays).
+GRAPH_ROWS = ()
 
 
 class Bench:
@@ -971,8 +972,8 @@ def main():
                            "graph_rows": list(GRAPH_ROWS)}}
     if "scan_tiny" in b.d:
         # the tiny scan's kernels back to back (graph of 64 launches): their
-        # own device time, which the step's per-pass figure adds a graph
-        # launch to
+        # own device time, to which the step's per-pass figure adds a launch
+        # and the events around it
         bb = b.back_to_back_us("scan_tiny")
         for p_, r in bb.items():
             r["frac"] = round(r["GBps"] / peak, 3)
