@@ -361,6 +361,44 @@ const char* lr_cuda_error_string(void);
 /* Bytes of device workspace currently held on the current device. */
 int64_t lr_workspace_bytes(void);
 
+/* Operations and carry protocols, as lr_plan_info names them. */
+typedef enum {
+    LR_OP_SCAN_FWD = 0,
+    LR_OP_SCAN_BWD = 1,
+    LR_OP_SRU_FWD = 2,
+    LR_OP_SRU_BWD = 3,
+    LR_OP_DEER = 4,
+    LR_OP_DEER_BWD = 5,
+    LR_OP_LSTM_FWD = 6,
+    LR_OP_LSTM_BWD = 7,
+    LR_OP_DEER_ODE = 8
+} lr_op;
+typedef enum {
+    LR_PROTO_CHAIN = 0,   /* a tile waits for the state after the chunk before it,
+                             or a CTA walks its channel strip through time */
+    LR_PROTO_WALK = 1,    /* walker warps fold the published chunk aggregates */
+    LR_PROTO_LOOK = 2,    /* every tile folds all earlier chunks' published aggregates */
+    LR_PROTO_CLUSTER = 3  /* one thread-block cluster per channel tile, aggregates
+                             passed through distributed shared memory */
+} lr_protocol;
+
+/*
+ * The carry protocol a call of operation `op` plans for a problem of T steps
+ * and C = B*D channels, from the shape alone: no device is needed and nothing
+ * is launched.  `vec` is 1 when the call takes the 16-byte path (D a multiple
+ * of 4 and every array 16-byte aligned).  Outputs (each may be NULL):
+ *   protocol  : one of lr_protocol
+ *   tma       : 1 when the chain or walker protocol stages tiles by TMA
+ *   tile_rows : time rows of a chunk
+ *   n_chunks  : ceil(T / tile_rows)
+ * Within a protocol the launcher still picks the kernel at launch (strip or
+ * TMA chain; warp-specialised, register or segmented walker).  Returns LR_OK,
+ * or LR_ERR_INVALID_ARG for an unknown op or dtype or T, C < 1 (an empty
+ * problem launches nothing).
+ */
+int lr_plan_info(int op, int dtype, int vec, int64_t T, int64_t C, int* protocol, int* tma,
+                 int64_t* tile_rows, int64_t* n_chunks);
+
 /*
  * Test hook for the bounded carry waits: launches both chain-protocol
  * forward scan kernels (register and TMA-staged) and the look-back kernel on

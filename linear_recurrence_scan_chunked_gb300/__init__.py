@@ -35,7 +35,10 @@ class LrError(RuntimeError):
 
 
 def build(force: bool = False) -> str:
-    from .build import build as _build
+    # the compiler driver lives in a module of another name: importing a
+    # submodule binds it as an attribute of the package, which would replace
+    # this function after its first call
+    from ._nvcc_build import build as _build
     return _build(force=force)
 
 
@@ -70,6 +73,8 @@ def load():
     lib.lr_test_activations.argtypes = [P, P, P, P, I64, P]
     lib.lr_test_fail_after_enqueue.argtypes = [P, I64, ctypes.c_float, ctypes.c_uint64, P]
     lib.lr_test_fail_after_enqueue.restype = I
+    lib.lr_plan_info.argtypes = [I, I, I, I64, I64, P, P, P, P]
+    lib.lr_plan_info.restype = I
     for f in ("lr_scan_fwd", "lr_scan_bwd", "sru_fwd", "sru_bwd", "deer_diag_solve", "deer_diag_bwd",
               "lr_last_error", "lr_test_lookback_timeout", "lr_test_activations"):
         getattr(lib, f).restype = I
@@ -360,6 +365,30 @@ def last_error() -> int:
 
 def workspace_bytes() -> int:
     return int(load().lr_workspace_bytes())
+
+
+# lr_op and lr_protocol of the header
+OPS = ("scan_fwd", "scan_bwd", "sru_fwd", "sru_bwd", "deer", "deer_bwd", "lstm_fwd", "lstm_bwd",
+       "deer_ode")
+PROTOCOLS = ("chain", "walk", "look", "cluster")
+
+
+def plan_info(op: str, dtype: str, vec: bool, T: int, C: int) -> dict:
+    """The carry protocol a call of `op` plans for T steps and C = B*D
+    channels (lr_plan_info; host only, no device): {"protocol", "tma",
+    "tile_rows", "n_chunks"}.  Raises ValueError on an argument error."""
+    lib = load()
+    proto, tma = ctypes.c_int(-1), ctypes.c_int(-1)
+    rows, nch = ctypes.c_int64(-1), ctypes.c_int64(-1)
+    if dtype not in ("f32", "bf16"):
+        raise ValueError(f"dtype must be 'f32' or 'bf16', got {dtype!r}")
+    st = lib.lr_plan_info(OPS.index(op), LR_F32 if dtype == "f32" else LR_BF16, 1 if vec else 0, int(T), int(C),
+                          ctypes.byref(proto), ctypes.byref(tma), ctypes.byref(rows),
+                          ctypes.byref(nch))
+    if st != LR_OK:
+        raise ValueError(f"lr_plan_info: {status_str(st)}")
+    return {"protocol": PROTOCOLS[proto.value], "tma": bool(tma.value), "tile_rows": rows.value,
+            "n_chunks": nch.value}
 
 
 def test_activations(x, stream=None, with_expm1=False):

@@ -907,6 +907,30 @@ int64_t lr_workspace_bytes(void) {
     return g_ws[dev]->bytes;
 }
 
+static_assert((int)LR_OP_SCAN_FWD == (int)OP_SCAN_FWD && (int)LR_OP_SCAN_BWD == (int)OP_SCAN_BWD &&
+                  (int)LR_OP_SRU_FWD == (int)OP_SRU_FWD && (int)LR_OP_SRU_BWD == (int)OP_SRU_BWD &&
+                  (int)LR_OP_DEER == (int)OP_DEER && (int)LR_OP_DEER_BWD == (int)OP_DEER_BWD &&
+                  (int)LR_OP_LSTM_FWD == (int)OP_LSTM_FWD && (int)LR_OP_LSTM_BWD == (int)OP_LSTM_BWD &&
+                  (int)LR_OP_DEER_ODE == (int)OP_DEER_ODE && (int)OP_DEER_ODE + 1 == (int)OP_COUNT,
+              "lr_op follows the library's operation order");
+static_assert(LR_PROTO_CHAIN == CARRY_CHAIN && LR_PROTO_WALK == CARRY_WALK &&
+                  LR_PROTO_LOOK == CARRY_LOOK && LR_PROTO_CLUSTER == CARRY_CLUSTER,
+              "lr_protocol follows the carry modes");
+
+int lr_plan_info(int op, int dtype, int vec, int64_t T, int64_t C, int* protocol, int* tma,
+                 int64_t* tile_rows, int64_t* n_chunks) {
+    if (op < 0 || op >= (int)OP_COUNT || (dtype != LR_F32 && dtype != LR_BF16) || T < 1 || C < 1)
+        return LR_ERR_INVALID_ARG;
+    const bool v = vec != 0;
+    // the same plan the entry points make (plan(), onepass_begin)
+    const CarryPlan cp = carry_plan((Op)op, dtype, v, use_tma(dtype, v, T, C), T, C);
+    if (protocol) *protocol = cp.mode;
+    if (tma) *tma = cp.tma ? 1 : 0;
+    if (tile_rows) *tile_rows = cp.ts.L;
+    if (n_chunks) *n_chunks = cp.n_chunks;
+    return LR_OK;
+}
+
 int lr_test_fail_after_enqueue(float* x, int64_t n, float value, uint64_t sleep_ns, void* stream) {
     if (n < 0 || (n > 0 && !x)) return LR_ERR_INVALID_ARG;
     GUARD;
