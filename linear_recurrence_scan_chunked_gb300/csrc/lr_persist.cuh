@@ -1208,9 +1208,9 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
 // composition of the affine maps of its rows); its warps send it, with
 // asynchronous stores, into the shared memory of every CTA after it in the
 // cluster (one warp per receiver), where the stores count their bytes on that
-// CTA's barrier.  A CTA of
-// rank q waits until the q aggregates before its own have landed, folds them in
-// chunk order into the state that enters its chunk, and writes its outputs.
+// CTA's barrier.  A CTA of rank q waits until the q aggregates before its own
+// have landed, folds them in chunk order into the state that enters its chunk,
+// and writes its outputs.
 // Nothing goes through global memory but the inputs and outputs: no packets,
 // tickets or epochs, and no CTA waits for another cluster, so clusters may run
 // in any order and any number of waves.
