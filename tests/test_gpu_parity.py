@@ -29,6 +29,9 @@ WIDE = [(70, 33, 520), (45, 40, 1000)]
 # (fp32 TMA tiles of 32 rows, 8 channel tiles), strip (135 channel tiles of
 # 128), register chain (scalar path: D = 7)
 SCAN_MID = [(2048, 4, 256), (1030, 33, 520), (1500, 3, 7)]
+# the cluster kernel's vector path with a ragged last channel tile (C = 20, 36:
+# lanes past the channels idle, 2 channels a lane)
+SCAN_RAGGED = [(300, 1, 20), (1000, 3, 12)]
 
 
 def _scan_case(cuda, T, B, D, dtype, seed=0):
@@ -46,7 +49,7 @@ def _scan_case(cuda, T, B, D, dtype, seed=0):
     assert_close("dh0", to_f64(dh0), rdh0, dtype)
 
 
-@pytest.mark.parametrize("shape", SHAPES + LONG + WIDE + SCAN_MID)
+@pytest.mark.parametrize("shape", SHAPES + LONG + WIDE + SCAN_MID + SCAN_RAGGED)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_scan_fwd_bwd(cuda, shape, dtype):
     _scan_case(cuda, *shape, dtype)
@@ -444,12 +447,12 @@ def _dyadic(rng, T, C):
     return a, b, g, h0
 
 
-# every carry protocol: cluster (three shapes: full clusters, one-chunk
+# every carry protocol: cluster (four shapes: full clusters, one-chunk
 # clusters of many channel tiles, ragged steps and channels on the scalar
-# path), look-back (two shapes), TMA chain (past the look-back budget),
+# path and on the vector path), look-back (two shapes), TMA chain (past the look-back budget),
 # register walker, segmented walker (bf16 forward, both backwards), strip
 # (wide), register chain (scalar path)
-DYADIC_SHAPES = [(1024, 4, 256), (64, 40, 1000), (999, 3, 7), (2048, 4, 256), (3001, 2, 100),
+DYADIC_SHAPES = [(1024, 4, 256), (64, 40, 1000), (999, 3, 7), (1000, 3, 12), (2048, 4, 256), (3001, 2, 100),
                  (4097, 2, 128), (20000, 1, 128), (50000, 1, 8), (1030, 33, 520), (1500, 3, 7)]
 
 

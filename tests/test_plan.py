@@ -27,6 +27,9 @@ def test_scans_up_to_1024_steps_take_the_cluster_kernel(op, dtype):
     # the tiny-scan configuration, and many channel tiles of one chunk
     assert plan(op, dtype, True, 1024, 4, 256)["protocol"] == "cluster"
     assert plan(op, dtype, True, 64, 40, 1000)["protocol"] == "cluster"
+    # ragged channel tiles on the vector path
+    assert plan(op, dtype, True, 300, 1, 20)["protocol"] == "cluster"
+    assert plan(op, dtype, True, 1000, 3, 12)["protocol"] == "cluster"
     # one step more: the scans' other protocols
     assert plan(op, dtype, True, 1025, 4, 256)["protocol"] != "cluster"
 
