@@ -1019,9 +1019,10 @@ __device__ __forceinline__ void look_issue(Carry& cr, const Geom& g, const TmaDe
 // before has completed: no ticket stands between the dependency wait and the
 // load, and the CTAs do not queue on one atomic before they start.  The epoch
 // comes from a plain load of the ticket word, issued beside the boxes; each CTA
-// then draws one arrival ticket on the same word (after that load, in the
-// word's coherence order), and the last arrival retires the epoch when its CTA
-// ends.  A tile waits only for tiles of smaller block index, which the
+// draws one arrival ticket on the same word once it has published its
+// aggregate (after that load, in the word's coherence order, and off the path
+// of the other CTAs' epoch loads), and the last arrival retires the epoch when
+// its CTA ends.  A tile waits only for tiles of smaller block index, which the
 // hardware dispatches first; every one of them is resident in the same wave.
 template <class Op, int ST>
 __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
@@ -1064,6 +1065,7 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
     bool drawing = true;     // thread 0: no ticket past the end drawn yet
     uint32_t issued = 0;     // thread 0: stage uses whose ticket was drawn
     unsigned long long arrival = 0;  // thread 0, one tile per CTA: the arrival draw
+    bool arrived = false;
     if (threadIdx.x == 0) {
         if (one) {
             const uint32_t tile = blockIdx.x + g.ticket_base;
@@ -1072,7 +1074,6 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
             issued = 1;
             drawing = false;
             cr.epoch = epoch_after((uint32_t)(ld_pkt(cr.tk) >> 32));
-            arrival = atomicAdd(reinterpret_cast<unsigned long long*>(cr.tk), 1ull);
         } else {
             for (; issued < (uint32_t)ST && drawing; ++issued) {
                 look_issue<Op>(cr, g, td, ring, full, s_tile, issued);
@@ -1125,6 +1126,10 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
 #pragma unroll
             for (int v = 0; v < VEC; ++v)
                 st_pkt2(cr.agg + 2 * (tc.q * g.C + tc.c + v), pkt(TA[v], cr.epoch), pkt(TB[v], cr.epoch));
+        }
+        if (one && threadIdx.x == 0 && !arrived) {  // after the publish: off the loads' path
+            arrival = atomicAdd(reinterpret_cast<unsigned long long*>(cr.tk), 1ull);
+            arrived = true;
         }
         // the warps before this one within the tile, as one affine map
         float PA[VEC], PB[VEC];
@@ -1198,7 +1203,10 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB * 8 / Op::NW)
         // after an early stop: copies still in flight land first
         for (uint32_t i = k; i < issued; ++i)
             if (s_tile[i % ST] < g.n_tiles) mbar_wait(&full[i % ST], (i / ST) & 1u, cr.err);
-        if (one) ticket_drawn(cr, g, (uint32_t)arrival);  // the last arrival retires the epoch
+        if (one) {  // the last arrival retires the epoch
+            if (!arrived) arrival = atomicAdd(reinterpret_cast<unsigned long long*>(cr.tk), 1ull);
+            ticket_drawn(cr, g, (uint32_t)arrival);
+        }
     }
 }
 
