@@ -110,7 +110,7 @@ typedef enum {
  * Forward scan (row a1): h_t = a_t * h_{t-1} + b_t for t = 0..T-1 with
  * h_{-1} = h0.  [P1] parallel-scan paragraph; [P2] LSTM paragraph.
  * Chunks of time rows are scanned in parallel; the state entering each chunk
- * comes from the aggregates of the chunks before it (for T <= 1024, the CTAs
+ * comes from the aggregates of the chunks before it (for T <= 2048, the CTAs
  * of one thread-block cluster pass them through distributed shared memory;
  * otherwise they are published to global memory: a look-back over all of them
  * for short problems, walkers -- whole CTAs, or one warp in each CTA of the
@@ -318,14 +318,14 @@ int lstm_cell_bwd(const void* zf, const void* zi, const void* zc, const void* zo
  * fail at run time or fragment its pool) and latency-critical loops (the
  * cudaFree that grows lr_scan_fwd's cached workspace synchronises the device).
  * Its scratch (chunk-state or chunk-aggregate packets, tile ticket) is one
- * fixed 4 MiB __device__ array that every GPU loading this library holds
+ * fixed 8 MiB __device__ array that every GPU loading this library holds
  * until the process exits.
  *   - Problems needing more scratch than that return LR_ERR_TOO_LARGE: the
- *     array holds ~524 K 8-byte packets, one per channel per chunk of 32 fp32
+ *     array holds ~1 M 8-byte packets, one per channel per chunk of 32 fp32
  *     or 64 bf16 time steps, two for short problems (look-back protocol),
  *     three per chunk of 64 steps for long ones (walker protocol), none for
- *     T <= 1024 (cluster kernel); e.g. B*D = 1024 channels up to T = 8 K fp32
- *     steps.
+ *     T <= 2048 (cluster kernel); e.g. B*D = 1024 channels up to T = 16 K
+ *     fp32 steps.
  *   - All calls share the array: calls whose kernels overlap on the GPU race
  *     and give wrong results; order them on one stream or with events.
  *   - Every call clears the array's internal error word and tile counter

@@ -132,10 +132,12 @@ inline TileShape tile_shape(Op op, int dtype, bool vec, int mode) {
     return TileShape{k.NW * k.R, 32 * (mode == TILE_CLUSTER ? 1 : kvec(dtype, vec)), 32 * k.NW};
 }
 
-// The cluster kernel: at most this many time chunks (CTAs per cluster, the
-// portable limit), so problems of up to kClusterMax * 128 steps.  The scans
-// have a cluster form; the cells and DEER keep their protocols.
-constexpr int kClusterMax = 8;
+// The cluster kernel: at most this many time chunks (CTAs per cluster; above
+// the portable 8, the launch opts in to Blackwell's 16), so problems of up to
+// kClusterMax * 128 steps.  The scans have a cluster form; the cells and DEER
+// keep their protocols.
+constexpr int kClusterMax = 16;
+constexpr int kClusterPortable = 8;
 constexpr bool cluster_op(Op op) { return op == OP_SCAN_FWD || op == OP_SCAN_BWD; }
 
 // The chain protocol stages its tiles with TMA when the vector path applies

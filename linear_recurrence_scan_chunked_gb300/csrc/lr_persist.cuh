@@ -1239,7 +1239,6 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
     constexpr uint32_t kAggBytes = 32 * 8;  // one chunk's aggregate: (A, B) per channel
     static_assert(LPR * VEC == 32, "a row is 32 channels");
     static_assert(Op::RG == RG, "the op is instantiated for this kernel's row groups");
-    static_assert(NW >= CL - 1, "one warp per later CTA of the cluster");
     // skip depends on the arguments only: the whole launch returns here,
     // before any barrier
     if (Op::skip(p)) return;
@@ -1318,7 +1317,8 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
     csync<NW>();
     cluster_wait();  // the first phase
     // the chunk's aggregate, to the CTAs after this one: warp k sends it to
-    // rank q + 1 + k, so that every later CTA gets it after one store
+    // ranks q + 1 + k, q + 1 + k + NW, ..., so that the later CTAs get it after
+    // one or two stores
     if (rg == 0 && (uint32_t)warp + q + 1 < n) {
         float TA[VEC], TB[VEC];
 #pragma unroll
@@ -1331,15 +1331,19 @@ __global__ void __launch_bounds__(Op::NW * 32, Op::MINB)
                 TB[v] = __fmaf_rn(a, TB[v], sm.b[w2][cq][v]);
                 TA[v] *= a;
             }
-        const uint32_t d = q + 1 + (uint32_t)warp;
-        const uint32_t bar = cluster_map(&cbar, d);
-        const uint32_t dst = cluster_map(&cab[q][cq * VEC], d);  // VEC consecutive (A, B) pairs
-        if constexpr (VEC == 1) {
-            st_async_f2(dst, TA[0], TB[0], bar);
-        } else {
 #pragma unroll
-            for (int v = 0; v < VEC; v += 2)
-                st_async_f4(dst + v * 8, TA[v], TB[v], TA[v + 1], TB[v + 1], bar);
+        for (int i = 0; i < (CL - 1 + NW - 1) / NW; ++i) {  // one pass for clusters of 8, two for 16
+            const uint32_t d = q + 1 + (uint32_t)(warp + i * NW);
+            if (d >= n) break;
+            const uint32_t bar = cluster_map(&cbar, d);
+            const uint32_t dst = cluster_map(&cab[q][cq * VEC], d);  // VEC consecutive (A, B) pairs
+            if constexpr (VEC == 1) {
+                st_async_f2(dst, TA[0], TB[0], bar);
+            } else {
+#pragma unroll
+                for (int v = 0; v < VEC; v += 2)
+                    st_async_f4(dst + v * 8, TA[v], TB[v], TA[v + 1], TB[v + 1], bar);
+            }
         }
     }
     // the second phase: no CTA leaves while another may still store into it
@@ -2492,11 +2496,22 @@ cudaError_t launch_look(const typename Op::Params& p, Geom g, const Carry& cr, c
 
 // Host: launch k_cluster<Op, CL> (one cluster of n_chunks <= CL CTAs per
 // channel tile), as a programmatic dependent of the stream's previous kernel.
-template <class Op>
-cudaError_t launch_cluster(const typename Op::Params& p, const Geom& g, const Carry& cr,
-                           cudaStream_t s) {
-    constexpr int CL = kClusterMax;
-    if (g.n_chunks < 1 || g.n_chunks > CL || g.n_ct < 1) return cudaErrorInvalidValue;
+// Up to 8 chunks the kernel is compiled for clusters of 8 (its folds and
+// pushes unrolled for 8); above, for 16, which needs the non-portable opt-in.
+template <class Op, int CL>
+cudaError_t launch_cluster_cl(const typename Op::Params& p, const Geom& g, const Carry& cr,
+                              cudaStream_t s) {
+    if (CL > kClusterPortable) {
+        static bool opted[64] = {false};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (!opted[dev & 63]) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(k_cluster<Op, CL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+            opted[dev & 63] = true;
+        }
+    }
     const uint64_t grid = (uint64_t)g.n_ct * (uint64_t)g.n_chunks;
     if (grid > 0x7fffffffu) return cudaErrorInvalidValue;
     cudaLaunchConfig_t lc;
@@ -2515,6 +2530,13 @@ cudaError_t launch_cluster(const typename Op::Params& p, const Geom& g, const Ca
     lc.attrs = at;
     lc.numAttrs = 2;
     return cudaLaunchKernelEx(&lc, k_cluster<Op, CL>, p, g, cr);
+}
+template <class Op>
+cudaError_t launch_cluster(const typename Op::Params& p, const Geom& g, const Carry& cr,
+                           cudaStream_t s) {
+    if (g.n_chunks < 1 || g.n_chunks > kClusterMax || g.n_ct < 1) return cudaErrorInvalidValue;
+    if (g.n_chunks <= kClusterPortable) return launch_cluster_cl<Op, kClusterPortable>(p, g, cr, s);
+    return launch_cluster_cl<Op, kClusterMax>(p, g, cr, s);
 }
 
 // Host: launch k_strip<Op, ST> when the problem has enough channel strips to

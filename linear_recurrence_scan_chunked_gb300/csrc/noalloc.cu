@@ -12,12 +12,13 @@
 // no cudaMalloc, cudaFree or allocating library routine.
 //
 // Costs and rules of the fixed array:
-//   * every GPU that loads the library holds kScratchBytes (4 MiB) of device
+//   * every GPU that loads the library holds kScratchBytes (8 MiB) of device
 //     memory until the process exits;
 //   * problems needing more carry packets than fit are rejected with
-//     LR_ERR_TOO_LARGE: ~524 K 8-byte packets, one per channel per chunk of
+//     LR_ERR_TOO_LARGE: ~1 M 8-byte packets, one per channel per chunk of
 //     time steps (the chain protocol), two (look-back protocol, short
-//     problems) or three (walker protocol, long ones);
+//     problems) or three (walker protocol, long ones); the cluster kernel's
+//     problems (at most 2048 steps) need none;
 //   * every call shares the one array: two calls whose kernels overlap on the
 //     GPU (different streams, no ordering between them) race on it and give
 //     wrong results.  Order such calls on one stream or with events.
@@ -41,7 +42,7 @@ namespace {
 
 using namespace lrs;
 
-constexpr size_t kScratchBytes = size_t(4) << 20;
+constexpr size_t kScratchBytes = size_t(8) << 20;
 // Header: bytes 4..7 the internal error word, 8..15 the 64-bit ticket word
 // (bytes 8..11 the tile counter, 12..15 the last retired epoch); packets from
 // byte 256 on.  Bytes 4..11 are cleared before every launch.

@@ -13,8 +13,8 @@ from lrtest import assert_close, dev_inputs, f64_inputs, to_dev, to_f64, TOL
 
 pytestmark = pytest.mark.gpu
 
-# (T, B, D).  The scans of up to 1024 steps run the cluster kernel (128 rows,
-# 32 channels per CTA; up to 8 CTAs per cluster); the cells take their tiles of
+# (T, B, D).  The scans of up to 2048 steps run the cluster kernel (128 rows,
+# 32 channels per CTA; up to 16 CTAs per cluster); the cells take their tiles of
 # 32-64 rows and 128 channels.
 SHAPES = [(1, 1, 4), (5, 2, 8), (64, 1, 128), (65, 1, 128), (200, 3, 96), (1000, 2, 64),
           (333, 4, 40), (77, 3, 5), (513, 1, 129), (2048, 2, 256), (3, 1, 1)]
@@ -25,10 +25,10 @@ LONG = [(100003, 1, 4), (20000, 1, 128), (20000, 1, 200)]
 # per CTA with a ragged last strip, and two strips per CTA (more strips than
 # resident CTAs)
 WIDE = [(70, 33, 520), (45, 40, 1000)]
-# the scans' own protocols past the cluster kernel's 1024 steps: look-back
-# (fp32 TMA tiles of 32 rows, 8 channel tiles), strip (135 channel tiles of
+# the scans' own protocols past the cluster kernel's 2048 steps: look-back
+# (fp32 TMA tiles of 32 rows, 4 channel tiles), strip (135 channel tiles of
 # 128), register chain (scalar path: D = 7)
-SCAN_MID = [(2048, 4, 256), (1030, 33, 520), (1500, 3, 7)]
+SCAN_MID = [(2100, 2, 256), (2100, 33, 520), (2100, 3, 7)]
 # the cluster kernel's vector path with a ragged last channel tile (C = 20, 36:
 # lanes past the channels idle, 2 channels a lane)
 SCAN_RAGGED = [(300, 1, 20), (1000, 3, 12)]
@@ -408,7 +408,7 @@ def test_scan_integer_valued_is_bit_exact(cuda):
     """a in {0, +1, -1}, b small integers: every association order is exact,
     so the chunked scan must equal the sequential oracle bit for bit."""
     r = np.random.default_rng(11)
-    for (T, B, D) in [(4097, 2, 128), (50000, 1, 8), (999, 3, 7), (1500, 3, 7)]:
+    for (T, B, D) in [(4097, 2, 128), (50000, 1, 8), (999, 3, 7), (2100, 3, 7)]:
         a = r.choice([0.0, 1.0, 1.0, 1.0, -1.0], size=(T, B, D)).astype(np.float32)
         b = r.integers(-3, 4, size=(T, B, D)).astype(np.float32)
         h0 = r.integers(-5, 6, size=(B, D)).astype(np.float32)
@@ -447,13 +447,13 @@ def _dyadic(rng, T, C):
     return a, b, g, h0
 
 
-# every carry protocol: cluster (four shapes: full clusters, one-chunk
-# clusters of many channel tiles, ragged steps and channels on the scalar
-# path and on the vector path), look-back (two shapes), TMA chain (past the look-back budget),
-# register walker, segmented walker (bf16 forward, both backwards), strip
-# (wide), register chain (scalar path)
-DYADIC_SHAPES = [(1024, 4, 256), (64, 40, 1000), (999, 3, 7), (1000, 3, 12), (2048, 4, 256), (3001, 2, 100),
-                 (4097, 2, 128), (20000, 1, 128), (50000, 1, 8), (1030, 33, 520), (1500, 3, 7)]
+# every carry protocol: cluster (five shapes: clusters of 8 and of 16 CTAs,
+# one-chunk clusters of many channel tiles, ragged steps and channels on the
+# scalar path and on the vector path), look-back (two shapes), TMA chain (past
+# the look-back budget), register walker, segmented walker (bf16 forward, both
+# backwards), strip (wide), register chain (scalar path)
+DYADIC_SHAPES = [(1024, 4, 256), (2048, 4, 256), (64, 40, 1000), (999, 3, 7), (1000, 3, 12), (2100, 2, 256),
+                 (3001, 2, 100), (4097, 2, 128), (20000, 1, 128), (50000, 1, 8), (2100, 33, 520), (2100, 3, 7)]
 
 
 @pytest.mark.parametrize("shape", DYADIC_SHAPES)
@@ -488,8 +488,8 @@ def test_scan_dyadic_is_bit_exact(cuda, shape, dtype):
         assert np.array_equal(xs, W.store(r, dtype)), name
 
 
-@pytest.mark.parametrize("shape", [(1024, 4, 256), (2048, 4, 256), (4097, 2, 128), (20000, 1, 128),
-                                   (64, 40, 1000), (1030, 33, 520)])
+@pytest.mark.parametrize("shape", [(1024, 4, 256), (2048, 4, 256), (2100, 2, 256), (4097, 2, 128),
+                                   (20000, 1, 128), (64, 40, 1000), (2100, 33, 520)])
 def test_scan_back_to_back_fresh_inputs(cuda, shape):
     """Calls of one shape back to back with different inputs, on one stream:
     every launch takes a fresh epoch on the device, so no tile may accept a
@@ -499,8 +499,8 @@ def test_scan_back_to_back_fresh_inputs(cuda, shape):
         _scan_case(cuda, T, B, D, "f32", seed=seed)
 
 
-@pytest.mark.parametrize("shape", [(1024, 4, 256), (2048, 4, 256), (4097, 2, 128), (20000, 1, 128),
-                                   (70, 33, 520), (1030, 33, 520)])
+@pytest.mark.parametrize("shape", [(1024, 4, 256), (2048, 4, 256), (2100, 2, 256), (4097, 2, 128),
+                                   (20000, 1, 128), (70, 33, 520), (2100, 33, 520)])
 def test_scan_graph_replay_takes_fresh_inputs(cuda, shape):
     """The forward and backward scans captured into a CUDA graph: each replay,
     with new values copied into the captured buffers, matches the oracle (the

@@ -19,9 +19,9 @@ def plan(op, dtype, vec, T, B, D):
 
 @pytest.mark.parametrize("op", ["scan_fwd", "scan_bwd"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_scans_up_to_1024_steps_take_the_cluster_kernel(op, dtype):
+def test_scans_up_to_2048_steps_take_the_cluster_kernel(op, dtype):
     for vec in (True, False):
-        for T, ch in ((1, 1), (128, 1), (129, 2), (1024, 8)):
+        for T, ch in ((1, 1), (128, 1), (129, 2), (1024, 8), (1025, 9), (2048, 16)):
             p = plan(op, dtype, vec, T, 4, 256)
             assert p == {"protocol": "cluster", "tma": False, "tile_rows": 128, "n_chunks": ch}, (T, p)
     # the tiny-scan configuration, and many channel tiles of one chunk
@@ -31,19 +31,22 @@ def test_scans_up_to_1024_steps_take_the_cluster_kernel(op, dtype):
     assert plan(op, dtype, True, 300, 1, 20)["protocol"] == "cluster"
     assert plan(op, dtype, True, 1000, 3, 12)["protocol"] == "cluster"
     # one step more: the scans' other protocols
-    assert plan(op, dtype, True, 1025, 4, 256)["protocol"] != "cluster"
+    assert plan(op, dtype, True, 2049, 4, 256)["protocol"] != "cluster"
 
 
 def test_the_scans_other_protocols_on_the_parity_shapes():
     # look-back past the cluster kernel (TMA tiles of 32 fp32 rows)
-    assert plan("scan_fwd", "f32", True, 2048, 4, 256) == {"protocol": "look", "tma": True,
-                                                            "tile_rows": 32, "n_chunks": 64}
+    assert plan("scan_fwd", "f32", True, 2100, 2, 256) == {"protocol": "look", "tma": True,
+                                                            "tile_rows": 32, "n_chunks": 66}
+    assert plan("scan_bwd", "f32", True, 2100, 2, 256)["protocol"] == "look"
     assert plan("scan_fwd", "f32", True, 3001, 2, 100)["protocol"] == "look"
-    # strip (chain protocol on TMA tiles, 135 channel tiles of 128)
-    p = plan("scan_fwd", "f32", True, 1030, 33, 520)
-    assert (p["protocol"], p["tma"]) == ("chain", True)
+    # strip (chain protocol on TMA tiles, 135 channel tiles of 128), and the
+    # strip case of the allocation-free entry's test and of smoke
+    for T, B, D, dt in ((2100, 33, 520, "f32"), (2100, 16, 1024, "bf16"), (2100, 16, 1024, "f32")):
+        p = plan("scan_fwd", dt, True, T, B, D)
+        assert (p["protocol"], p["tma"]) == ("chain", True), (T, B, D, dt)
     # register chain: the scalar path
-    p = plan("scan_fwd", "f32", False, 1500, 3, 7)
+    p = plan("scan_fwd", "f32", False, 2100, 3, 7)
     assert (p["protocol"], p["tma"]) == ("chain", False)
     # past the look-back budget (n_chunks^2 * channel tiles): the TMA chain
     p = plan("scan_fwd", "f32", True, 4097, 2, 128)

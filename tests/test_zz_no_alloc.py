@@ -38,11 +38,12 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
-@pytest.mark.parametrize("dtype,shape", [# cluster kernel; look-back kernel
+@pytest.mark.parametrize("dtype,shape", [# cluster kernel (8 and 16 CTAs); look-back kernel
                                          ("f32", (1024, 4, 256)), ("bf16", (777, 3, 512)),
-                                         ("f32", (2048, 4, 256)), ("f32", (3001, 2, 100)),
+                                         ("f32", (2048, 4, 256)),
+                                         ("f32", (2100, 2, 256)), ("f32", (3001, 2, 100)),
                                          # strip kernel; walker kernels (register, segmented)
-                                         ("bf16", (1030, 16, 1024)), ("f32", (20000, 1, 128)),
+                                         ("bf16", (2100, 16, 1024)), ("f32", (20000, 1, 128)),
                                          ("bf16", (20000, 1, 128))])
 @pytest.mark.parametrize("with_err", [True, False])
 def test_noalloc_matches_allocating_scan_twice(cuda, dtype, shape, with_err):
