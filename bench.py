@@ -56,7 +56,7 @@ EPS, KMAX = 1e-5, 20
 # and written by a K = 6 solve -- the reduce-only pass, iteration 1 and five
 # later iterations, captured at full size (profiles/dram_traffic.md) -- over
 # its K iteration launches.
-NCU_TRAFFIC = {"deer.solve": {"bytes": 767126122, "src": "13386c1a2808a4d4",
+NCU_TRAFFIC = {"deer.solve": {"bytes": 767176085, "src": "26d378f98ef291e6",
                               "file": "deer_kernels.cu"}}
 
 
